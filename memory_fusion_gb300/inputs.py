@@ -1,0 +1,171 @@
+"""Seeded synthetic inputs, shared by the CUDA path's tests/bench and the oracle.
+
+This module holds none of the method's arithmetic: it only draws random
+numbers and rounds them to the storage type the workload names (bf16 by
+round-to-nearest-even).  Both sides receive the very same values.
+
+Recipe (one ``numpy.random.Generator(PCG64(seed))`` per workload, values drawn
+as float64 normals / uniforms, scaled, cast to float32, then -- where the
+workload stores bf16 -- rounded to bf16 with round-to-nearest-even; draws are
+made in argument order):
+
+* GEMM + row-norm workloads: X[M,K], W[K,N] (bf16, N(0, x_std), N(0, w_std));
+  bias[N] ~ N(0, bias_std), gamma[N] ~ N(1, gamma_std), beta[N] ~ N(0,
+  beta_std) (fp32).
+* GEMM + softmax workloads: X, W as above; no bias unless asked.
+* Stitched workload: A[rows, cols] ~ N(0, 2) fp32, then b[rows] ~ U(-1, 1)
+  fp32; the generator is re-seeded for every shape.
+
+"N(0, s)" means standard deviation s throughout.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+__all__ = [
+    "round_to_bf16",
+    "bf16_bits",
+    "GemmWorkload",
+    "StitchWorkload",
+    "WORKLOADS",
+    "gemm_inputs",
+    "stitch_inputs",
+    "workload_inputs",
+]
+
+
+def round_to_bf16(a) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); return float32.
+
+    NaN/Inf are not produced by the generator; finite values only.
+    """
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    bits = a.view(np.uint32).astype(np.uint64)
+    lsb = (bits >> np.uint64(16)) & np.uint64(1)
+    bits = (bits + np.uint64(0x7FFF) + lsb) & np.uint64(0xFFFF0000)
+    return bits.astype(np.uint32).view(np.float32).reshape(a.shape)
+
+
+def bf16_bits(a_bf16_valued) -> np.ndarray:
+    """uint16 bit patterns of float32 values that are exactly bf16."""
+    a = np.ascontiguousarray(np.asarray(a_bf16_valued, dtype=np.float32))
+    return (a.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+@dataclass(frozen=True)
+class GemmWorkload:
+    name: str
+    kind: str              # "rownorm" | "softmax"
+    M: int
+    N: int
+    K: int
+    seed: int
+    x_std: float
+    w_std: float
+    bias_std: float = 0.0
+    gamma_std: float = 0.0
+    beta_std: float = 0.0
+    act: str = "none"      # "none" | "gelu_tanh"
+    eps: float = 1e-5
+    alpha: float = 1.0
+    scale: float = 1.0
+    description: str = ""
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    @property
+    def unavoidable_bytes(self) -> int:
+        """Inputs + final output, each once; no intermediate."""
+        b = 2 * self.M * self.K + 2 * self.K * self.N + 2 * self.M * self.N
+        if self.kind == "rownorm":
+            b += 3 * 4 * self.N
+        return b
+
+
+@dataclass(frozen=True)
+class StitchWorkload:
+    name: str
+    rows: int
+    cols: int
+    seed: int
+    description: str = ""
+
+    @property
+    def unavoidable_bytes(self) -> int:
+        return 4 * self.rows * self.cols * 2 + 4 * self.rows
+
+
+def _c(n):
+    return 1.0 / math.sqrt(n)
+
+
+WORKLOADS = {
+    "ln_tiny_128x512x256": GemmWorkload(
+        "ln_tiny_128x512x256", "rownorm", 128, 512, 256, 0, _c(256), _c(256),
+        0.1, 0.1, 0.1, "none", 1e-5,
+        description="GEMM+bias+LayerNorm, tiny: X[128,256] W[256,512]"),
+    "softmax_4096x2048x128": GemmWorkload(
+        "softmax_4096x2048x128", "softmax", 4096, 2048, 128, 1, 1.0, _c(128),
+        scale=_c(128),
+        description="GEMM+row softmax: X[4096,128] W[128,2048], scale 1/sqrt(128)"),
+    "gelu_ln_16384x4096x4096": GemmWorkload(
+        "gelu_ln_16384x4096x4096", "rownorm", 16384, 4096, 4096, 2, _c(4096), _c(4096),
+        0.02, 0.02, 0.02, "gelu_tanh", 1e-5,
+        description="GEMM+bias+GELU(tanh)+LayerNorm, FFN-sized"),
+    "wide_ln_8192x16384x2048": GemmWorkload(
+        "wide_ln_8192x16384x2048", "rownorm", 8192, 16384, 2048, 4, _c(2048), _c(2048),
+        0.1, 0.1, 0.1, "none", 1e-5,
+        description="wide-row GEMM+bias+LayerNorm, row wider than one cluster"),
+    "stitch_750000x32": StitchWorkload(
+        "stitch_750000x32", 750000, 32, 3,
+        description="stitched y=A^3+b[row] -> row softmax, very many tiny rows"),
+    "stitch_64x30000": StitchWorkload(
+        "stitch_64x30000", 64, 30000, 3,
+        description="stitched y=A^3+b[row] -> row softmax, very few huge rows"),
+}
+
+
+def _normal(rng, shape, std, mean=0.0):
+    return (rng.standard_normal(size=shape) * std + mean).astype(np.float32)
+
+
+def gemm_inputs(M: int, N: int, K: int, seed: int, *, x_std: float = 1.0,
+                w_std: float = 1.0, bias_std: float | None = 0.1,
+                gamma_std: float | None = 0.1, beta_std: float | None = 0.1) -> dict:
+    """X, W (bf16-valued float32) and the row-vector parameters (float32).
+
+    A ``None`` std skips that draw (the key is then None).
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = {}
+    out["X"] = round_to_bf16(_normal(rng, (M, K), x_std))
+    out["W"] = round_to_bf16(_normal(rng, (K, N), w_std))
+    out["bias"] = None if bias_std is None else _normal(rng, (N,), bias_std)
+    out["gamma"] = None if gamma_std is None else _normal(rng, (N,), gamma_std, 1.0)
+    out["beta"] = None if beta_std is None else _normal(rng, (N,), beta_std)
+    return out
+
+
+def stitch_inputs(rows: int, cols: int, seed: int = 3) -> dict:
+    """A[rows, cols] ~ N(0, 2) fp32 and row_bias[rows] ~ U(-1, 1) fp32."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    A = _normal(rng, (rows, cols), 2.0)
+    b = (rng.random(size=rows) * 2.0 - 1.0).astype(np.float32)
+    return {"A": A, "row_bias": b}
+
+
+def workload_inputs(name: str) -> dict:
+    w = WORKLOADS[name]
+    if isinstance(w, StitchWorkload):
+        return stitch_inputs(w.rows, w.cols, w.seed)
+    if w.kind == "rownorm":
+        return gemm_inputs(w.M, w.N, w.K, w.seed, x_std=w.x_std, w_std=w.w_std,
+                           bias_std=w.bias_std, gamma_std=w.gamma_std,
+                           beta_std=w.beta_std)
+    return gemm_inputs(w.M, w.N, w.K, w.seed, x_std=w.x_std, w_std=w.w_std,
+                       bias_std=None, gamma_std=None, beta_std=None)

@@ -1,0 +1,211 @@
+"""Plain, slow, fp64 CPU oracle for the fused GEMM + row-reduce/broadcast path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute this module: only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` use it.  It shares
+no code with the CUDA path; the only thing both sides share is the seeded
+input generator, which holds none of the method's arithmetic.
+
+What is computed, and where it is defined
+-----------------------------------------
+The pages describe *exact* fusion: the fused kernel must reach the result of
+the unfused operator chain ("semantics fully preserved", ComFuse, Fusion Spec
+IR, Eq. (10); ownership legality, sass2mlir "Kernel fusion", section
+"Epilogue fusion - the core technique").  So the oracle is the unfused chain
+written out in float64 on the same (bf16 / fp32) input values:
+
+* MatMul      P = X . W                       (ComFuse, Eq. (6) notation)
+* Stage 1     x = alpha * P + bias            (ComFuse, Stage-Stream Execution
+                                               Model, Fig. 3: x = alpha*Acc+Bias)
+* activation  g = GELU_tanh(x) or g = x       (a unary compute node, ComFuse,
+                                               Fusion Spec IR mapping Phi)
+* reduction   LayerNorm / Softmax as "reduce over the inputs, normalise the
+              original values" (ComFuse, nested Fusion Spec IR at reductions)
+* stitched    y = A^3 + b[row]; rowwise softmax (AStitch, "Adaptive thread
+              mapping": row reductions on 750000x32 and 64x30000)
+
+Pages cited (full titles):
+  ComFuse  -- "ComFuse: Fusing Complex Memory-Intensive Subgraphs with
+              Compute-Intensive Kernels For Modern GPU Architectures"
+  AStitch  -- "AStitch: enabling a new multi-dimensional optimization space for
+              memory-intensive ML training and inference on modern SIMT
+              architectures"
+  sass2mlir -- the sass2mlir "kernel fusion" page ("Two answers to the same
+              idle GPU": CUDA graphs, then "How we fuse kernels")
+
+Readings taken where the pages are silent:
+  * LayerNorm variance is the biased one (divide by N), eps inside the square
+    root, gamma/beta applied after normalising; with GELU the norm is taken
+    over the post-GELU values.
+  * Softmax scale multiplies the accumulator before max/exp; an optional bias
+    is added after scaling.  Exponent base e.
+  * GELU is the tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+  * pow(A, 3) is the real cube with its sign (A*A*A).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
+forms, invariants, brute force on tiny inputs and library routines.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "gemm",
+    "gemm_naive",
+    "gelu_tanh",
+    "layernorm_rows",
+    "softmax_rows",
+    "gemm_bias_rownorm",
+    "gemm_rowsoftmax",
+    "stitch_rowreduce_broadcast",
+    "ROW_CHUNK",
+]
+
+# Row chunk used to bound the oracle's memory on the large configurations.
+# Chunking over rows changes nothing: every row is computed independently.
+ROW_CHUNK = 1024
+
+_SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
+_GELU_CUBIC = 0.044715
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def gemm(X, W) -> np.ndarray:
+    """P = X . W in float64 (ComFuse, Eq. (6): X in R^{MxK}, W in R^{KxN}).
+
+    bf16 inputs widen exactly to float64 and every bf16 x bf16 product is
+    exact in float64, so the only rounding is the float64 summation.
+    """
+    X = _f64(X)
+    W = _f64(W)
+    if X.ndim != 2 or W.ndim != 2 or X.shape[1] != W.shape[0]:
+        raise ValueError(f"gemm: incompatible shapes {X.shape} x {W.shape}")
+    return X @ W
+
+
+def gemm_naive(X, W) -> np.ndarray:
+    """Triple-loop MatMul, pure Python.  For tiny inputs only (pins gemm)."""
+    X = _f64(X)
+    W = _f64(W)
+    M, K = X.shape
+    K2, N = W.shape
+    if K != K2:
+        raise ValueError("gemm_naive: inner dimensions differ")
+    P = np.zeros((M, N), dtype=np.float64)
+    for i in range(M):
+        for j in range(N):
+            s = 0.0
+            for k in range(K):
+                s += float(X[i, k]) * float(W[k, j])
+            P[i, j] = s
+    return P
+
+
+def gelu_tanh(x) -> np.ndarray:
+    """GELU, tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))."""
+    x = _f64(x)
+    return 0.5 * x * (1.0 + np.tanh(_SQRT_2_OVER_PI * (x + _GELU_CUBIC * x * x * x)))
+
+
+def layernorm_rows(g, gamma, beta, eps: float) -> np.ndarray:
+    """LayerNorm over the last axis, two-pass.
+
+    mean = (1/N) sum g;  var = (1/N) sum (g - mean)^2  (biased);
+    y = (g - mean) / sqrt(var + eps) * gamma + beta.
+    This is the "reduce over inputs but normalise using original values"
+    pattern the ComFuse Fusion Spec IR nests at a Reduction node: the first
+    reduction (mean) feeds the second (variance), whose statistic is then
+    broadcast back over the row together with the bypassed values.
+    """
+    g = _f64(g)
+    mean = g.mean(axis=-1, keepdims=True)
+    d = g - mean
+    var = (d * d).mean(axis=-1, keepdims=True)
+    return d / np.sqrt(var + float(eps)) * _f64(gamma) + _f64(beta)
+
+
+def softmax_rows(z) -> np.ndarray:
+    """Row softmax: m = max z; e = exp(z - m); y = e / sum(e)."""
+    z = _f64(z)
+    m = z.max(axis=-1, keepdims=True)
+    e = np.exp(z - m)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def _row_chunks(M: int, rows):
+    if rows is None:
+        for r0 in range(0, M, ROW_CHUNK):
+            yield np.arange(r0, min(M, r0 + ROW_CHUNK))
+    else:
+        rows = np.asarray(rows, dtype=np.int64)
+        for r0 in range(0, rows.size, ROW_CHUNK):
+            yield rows[r0:r0 + ROW_CHUNK]
+
+
+def gemm_bias_rownorm(X, W, bias, gamma, beta, *, alpha: float = 1.0,
+                      eps: float = 1e-5, act: str = "none", rows=None) -> np.ndarray:
+    """y = LayerNorm(act(alpha * X.W + bias)) * gamma + beta, row by row.
+
+    ComFuse, Stage-Stream Execution Model, Fig. 3 (stage 1: x = alpha*Acc+Bias,
+    mean; stage 2: x - mean, ...) with an optional GELU node between the
+    bias add and the reductions.  ``rows`` selects a subset of output rows
+    (every row is independent, so a sampled row is exact).
+    ``bias`` may be None (no bias node).
+    """
+    if act not in ("none", "gelu_tanh"):
+        raise ValueError(f"unknown activation {act!r}")
+    X = np.asarray(X)
+    M = X.shape[0]
+    N = np.asarray(W).shape[1]
+    out_rows = M if rows is None else len(rows)
+    out = np.empty((out_rows, N), dtype=np.float64)
+    b = np.zeros(N) if bias is None else _f64(bias)
+    o = 0
+    for idx in _row_chunks(M, rows):
+        x = float(alpha) * gemm(X[idx], W) + b
+        g = gelu_tanh(x) if act == "gelu_tanh" else x
+        out[o:o + idx.size] = layernorm_rows(g, gamma, beta, eps)
+        o += idx.size
+    return out
+
+
+def gemm_rowsoftmax(X, W, *, scale: float, bias=None, rows=None) -> np.ndarray:
+    """y = softmax(scale * X.W (+ bias)) over each row."""
+    X = np.asarray(X)
+    M = X.shape[0]
+    N = np.asarray(W).shape[1]
+    out_rows = M if rows is None else len(rows)
+    out = np.empty((out_rows, N), dtype=np.float64)
+    o = 0
+    for idx in _row_chunks(M, rows):
+        z = float(scale) * gemm(X[idx], W)
+        if bias is not None:
+            z = z + _f64(bias)
+        out[o:o + idx.size] = softmax_rows(z)
+        o += idx.size
+    return out
+
+
+def stitch_rowreduce_broadcast(A, row_bias, rows=None) -> np.ndarray:
+    """Stitched memory-intensive subgraph (AStitch, "Adaptive thread mapping"):
+
+    y = A*A*A + b[row]  (elementwise power, then a broadcast row bias);
+    m = rowmax(y); s = rowsum(exp(y - m)); out = exp(y - m) / s.
+    """
+    A = np.asarray(A)
+    b = np.asarray(row_bias)
+    M, N = A.shape
+    out_rows = M if rows is None else len(rows)
+    out = np.empty((out_rows, N), dtype=np.float64)
+    o = 0
+    for idx in _row_chunks(M, rows):
+        a = _f64(A[idx])
+        y = a * a * a + _f64(b[idx])[:, None]
+        out[o:o + idx.size] = softmax_rows(y)
+        o += idx.size
+    return out

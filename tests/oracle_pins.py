@@ -1,0 +1,275 @@
+"""Pin checks for the fp64 oracle, written against what the mathematics fixes.
+
+Each ``check_*`` takes the function under test as an argument and returns a
+list of failure strings (empty = pinned).  ``test_oracle_pins.py`` runs them
+on the oracle; ``test_oracle_mutations.py`` runs them on deliberately broken
+copies (a dropped term, a wrong sign, a transposed operand ...) to show each
+plausible mistake fails at least one pin.  Nothing here calls the oracle's
+own helpers to compute an expected value: expected values are closed forms,
+brute force, hand-derived fixtures or independent library routines.
+"""
+from __future__ import annotations
+
+import math
+import os
+import statistics
+from fractions import Fraction
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _load_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            rows.append([float(v) for v in line.split()])
+    return np.array(rows, dtype=np.float64)
+
+
+def _fail(fails, ok, msg):
+    if not ok:
+        fails.append(msg)
+
+
+# ----------------------------------------------------------------------------
+# MatMul
+# ----------------------------------------------------------------------------
+def check_gemm(gemm) -> list:
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(11))
+    # brute force with exact rational arithmetic on small integer matrices
+    for (M, K, N) in [(3, 5, 7), (4, 2, 9), (1, 6, 1), (5, 1, 3)]:
+        X = rng.integers(-8, 9, size=(M, K))
+        W = rng.integers(-8, 9, size=(K, N))
+        exact = np.array([[sum(Fraction(int(X[i, k])) * int(W[k, j]) for k in range(K))
+                           for j in range(N)] for i in range(M)], dtype=np.float64)
+        P = np.asarray(gemm(X.astype(np.float64), W.astype(np.float64)))
+        _fail(fails, P.shape == (M, N), f"gemm shape {P.shape} != {(M, N)}")
+        _fail(fails, P.shape == (M, N) and np.array_equal(P, exact),
+              f"gemm {M}x{K}x{N} integer product not exact")
+    # bf16-valued reals: products exact in fp64; compare with a Python loop
+    X = np.round(rng.standard_normal((6, 10)) * 64) / 64
+    W = np.round(rng.standard_normal((10, 4)) * 64) / 64
+    ref = np.array([[math.fsum(X[i, k] * W[k, j] for k in range(10)) for j in range(4)]
+                    for i in range(6)])
+    P = np.asarray(gemm(X, W))
+    _fail(fails, P.shape == ref.shape and np.allclose(P, ref, rtol=1e-13, atol=1e-13),
+          "gemm real-valued mismatch vs fsum brute force")
+    return fails
+
+
+# ----------------------------------------------------------------------------
+# GELU (tanh form)
+# ----------------------------------------------------------------------------
+def check_gelu(gelu) -> list:
+    fails = []
+    _fail(fails, float(np.asarray(gelu(np.array([0.0])))[0]) == 0.0, "GELU(0) != 0")
+    x = np.linspace(-6, 6, 241)
+    g = np.asarray(gelu(x))
+    gm = np.asarray(gelu(-x))
+    # tanh is odd: GELU(x) - GELU(-x) = x exactly up to rounding
+    _fail(fails, np.allclose(g - gm, x, rtol=1e-14, atol=1e-14), "GELU(x)-GELU(-x) != x")
+    # asymptotes
+    _fail(fails, abs(float(np.asarray(gelu(np.array([12.0])))[0]) - 12.0) < 1e-12, "GELU(12) != 12")
+    _fail(fails, abs(float(np.asarray(gelu(np.array([-12.0])))[0])) < 1e-12, "GELU(-12) != 0")
+    # second-order coefficient: (GELU(h)+GELU(-h))/(2h^2) -> sqrt(2/pi)/2
+    h = 1e-4
+    even = (float(np.asarray(gelu(np.array([h])))[0]) + float(np.asarray(gelu(np.array([-h])))[0])) / (2 * h * h)
+    _fail(fails, abs(even - math.sqrt(2 / math.pi) / 2) < 1e-6, f"GELU curvature {even}")
+    # independent library routine (fp64)
+    import torch
+    ref = torch.nn.functional.gelu(torch.from_numpy(x), approximate="tanh").numpy()
+    _fail(fails, np.allclose(g, ref, rtol=1e-13, atol=1e-15), "GELU vs torch gelu(tanh) fp64")
+    return fails
+
+
+# ----------------------------------------------------------------------------
+# LayerNorm
+# ----------------------------------------------------------------------------
+def check_layernorm(ln) -> list:
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(12))
+    # eps = 0, gamma = 1, beta = 0: row mean 0 and (biased) variance 1 to 1e-9
+    for N in (2, 3, 7, 512, 4096):
+        g = rng.standard_normal((5, N)) * 0.013 + 0.37
+        y = np.asarray(ln(g, np.ones(N), np.zeros(N), 0.0))
+        mean = y.mean(axis=1)
+        var = ((y - y.mean(axis=1, keepdims=True)) ** 2).mean(axis=1)
+        _fail(fails, np.all(np.abs(mean) < 1e-9), f"LN eps=0 mean N={N}: {mean}")
+        _fail(fails, np.all(np.abs(var - 1) < 1e-9), f"LN eps=0 var N={N}: {var}")
+    # eps > 0: output variance = s2/(s2+eps), s2 from Python's statistics module
+    for N in (4, 33):
+        row = rng.standard_normal(N) * 0.01
+        s2 = statistics.pvariance([float(v) for v in row])
+        eps = 1e-5
+        y = np.asarray(ln(row[None, :], np.ones(N), np.zeros(N), eps))[0]
+        v = float(((y - y.mean()) ** 2).mean())
+        _fail(fails, abs(v - s2 / (s2 + eps)) < 1e-9, f"LN eps>0 var {v} vs {s2 / (s2 + eps)}")
+    # constant row -> beta exactly
+    N = 16
+    beta = rng.standard_normal(N)
+    y = np.asarray(ln(np.full((1, N), 3.25), rng.standard_normal(N), beta, 1e-5))[0]
+    _fail(fails, np.array_equal(y, beta), "LN constant row != beta")
+    # two elements [a, b]: y = [-d, d]/sqrt(d^2+eps) with d = (b-a)/2
+    a, b, eps = 0.3, -1.1, 1e-3
+    d = (b - a) / 2
+    y = np.asarray(ln(np.array([[a, b]]), np.ones(2), np.zeros(2), eps))[0]
+    want = np.array([-d, d]) / math.sqrt(d * d + eps)
+    _fail(fails, np.allclose(y, want, rtol=1e-13, atol=1e-15), "LN two-element closed form")
+    # positive row scaling leaves the result unchanged at eps = 0
+    g = rng.standard_normal((3, 64))
+    y1 = np.asarray(ln(g, np.ones(64), np.zeros(64), 0.0))
+    y2 = np.asarray(ln(g * 37.5, np.ones(64), np.zeros(64), 0.0))
+    _fail(fails, np.allclose(y1, y2, rtol=1e-12, atol=1e-12), "LN scale invariance")
+    # hand-derived worked fixture (gamma/beta affine after normalising)
+    t = _load_golden("layernorm_worked.txt")
+    for blk in (t[:4], t[4:]):
+        g, gam, bet, eps, want = blk[:, 0], blk[:, 1], blk[:, 2], blk[0, 3], blk[:, 4]
+        y = np.asarray(ln(g[None, :], gam, bet, eps))[0]
+        _fail(fails, np.allclose(y, want, rtol=1e-12, atol=1e-12), f"LN golden {y} vs {want}")
+    # independent library routine (fp64)
+    import torch
+    g = rng.standard_normal((4, 96)) * 0.02
+    gam = 1 + 0.1 * rng.standard_normal(96)
+    bet = 0.1 * rng.standard_normal(96)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(g), (96,), torch.from_numpy(gam),
+                                         torch.from_numpy(bet), 1e-5).numpy()
+    y = np.asarray(ln(g, gam, bet, 1e-5))
+    _fail(fails, np.allclose(y, ref, rtol=1e-11, atol=1e-12), "LN vs torch layer_norm fp64")
+    return fails
+
+
+# ----------------------------------------------------------------------------
+# Softmax
+# ----------------------------------------------------------------------------
+def check_softmax(sm) -> list:
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(13))
+    z = rng.standard_normal((6, 2048)) * 3
+    y = np.asarray(sm(z))
+    _fail(fails, np.all(np.abs(y.sum(axis=1) - 1) < 1e-12), "softmax rows do not sum to 1")
+    _fail(fails, np.all(y > 0), "softmax not positive")
+    # invariance to a per-row constant shift
+    shift = rng.standard_normal((6, 1)) * 50
+    y2 = np.asarray(sm(z + shift))
+    _fail(fails, np.allclose(y, y2, rtol=1e-11, atol=1e-16), "softmax shift invariance")
+    # large magnitudes must not overflow (the max subtraction is part of it)
+    big = np.array([[1000.0, 999.0, 998.0]])
+    yb = np.asarray(sm(big))
+    _fail(fails, bool(np.all(np.isfinite(yb))) and abs(float(yb.sum()) - 1) < 1e-12,
+          "softmax overflow at large logits")
+    # constant row -> 1/N; N = 1 -> 1
+    _fail(fails, np.allclose(np.asarray(sm(np.full((1, 37), -4.5))), 1 / 37, rtol=1e-14), "softmax const row")
+    _fail(fails, float(np.asarray(sm(np.array([[7.0]])))[0, 0]) == 1.0, "softmax N=1")
+    # two elements: sigmoid closed form, base e
+    a, b = 0.25, 1.75
+    y = np.asarray(sm(np.array([[a, b]])))[0]
+    _fail(fails, abs(y[0] - 1 / (1 + math.exp(b - a))) < 1e-15, "softmax two-element closed form")
+    # argmax preserved
+    _fail(fails, np.array_equal(np.argmax(np.asarray(sm(z)), 1), np.argmax(z, 1)), "softmax argmax")
+    # hand-derived fixture
+    t = _load_golden("softmax_worked.txt")
+    for off in (0.0, 100.0):
+        y = np.asarray(sm(t[None, :, 0] + off))[0]
+        _fail(fails, np.allclose(y, t[:, 1], rtol=1e-13), f"softmax golden (offset {off})")
+    import torch
+    ref = torch.softmax(torch.from_numpy(z), dim=1).numpy()
+    _fail(fails, np.allclose(np.asarray(sm(z)), ref, rtol=1e-12, atol=1e-18), "softmax vs torch fp64")
+    return fails
+
+
+# ----------------------------------------------------------------------------
+# Compositions (library cross-check of the wiring: alpha, bias, act, norm)
+# ----------------------------------------------------------------------------
+def check_rownorm_composition(fused) -> list:
+    import torch
+    F = torch.nn.functional
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(14))
+    M, K, N = 9, 24, 40
+    X = rng.standard_normal((M, K)) / 5
+    W = rng.standard_normal((K, N)) / 5
+    bias = rng.standard_normal(N) * 0.1
+    gam = 1 + rng.standard_normal(N) * 0.1
+    bet = rng.standard_normal(N) * 0.1
+    t = {k: torch.from_numpy(v) for k, v in dict(X=X, W=W, b=bias, g=gam, be=bet).items()}
+    for act in ("none", "gelu_tanh"):
+        for alpha in (1.0, 0.5):
+            x = alpha * (t["X"] @ t["W"]) + t["b"]
+            if act == "gelu_tanh":
+                x = F.gelu(x, approximate="tanh")
+            ref = F.layer_norm(x, (N,), t["g"], t["be"], 1e-5).numpy()
+            y = np.asarray(fused(X, W, bias, gam, bet, alpha=alpha, eps=1e-5, act=act))
+            _fail(fails, y.shape == ref.shape and np.allclose(y, ref, rtol=1e-10, atol=1e-11),
+                  f"rownorm composition act={act} alpha={alpha}")
+    # bias=None is the same as a zero bias
+    y0 = np.asarray(fused(X, W, None, gam, bet, alpha=1.0, eps=1e-5, act="none"))
+    y1 = np.asarray(fused(X, W, np.zeros(N), gam, bet, alpha=1.0, eps=1e-5, act="none"))
+    _fail(fails, np.allclose(y0, y1, rtol=0, atol=1e-15), "rownorm bias=None")
+    # sampled rows == the same rows of the full result
+    rows = [8, 0, 3]
+    ys = np.asarray(fused(X, W, bias, gam, bet, alpha=1.0, eps=1e-5, act="gelu_tanh", rows=rows))
+    yf = np.asarray(fused(X, W, bias, gam, bet, alpha=1.0, eps=1e-5, act="gelu_tanh"))
+    _fail(fails, ys.shape == yf[rows].shape and np.allclose(ys, yf[rows], rtol=1e-13, atol=1e-14), "rownorm rows= subset")
+    return fails
+
+
+def check_softmax_composition(fused) -> list:
+    import torch
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(15))
+    M, K, N = 7, 16, 33
+    X = rng.standard_normal((M, K))
+    W = rng.standard_normal((K, N)) / 4
+    bias = rng.standard_normal(N)
+    for b in (None, bias):
+        z = 0.3 * (torch.from_numpy(X) @ torch.from_numpy(W))
+        if b is not None:
+            z = z + torch.from_numpy(b)
+        ref = torch.softmax(z, dim=1).numpy()
+        y = np.asarray(fused(X, W, scale=0.3, bias=b))
+        _fail(fails, y.shape == ref.shape and np.allclose(y, ref, rtol=1e-12, atol=1e-16),
+              f"softmax composition bias={'yes' if b is not None else 'no'}")
+    rows = [6, 2]
+    ys = np.asarray(fused(X, W, scale=0.3, rows=rows))
+    yf = np.asarray(fused(X, W, scale=0.3))[rows]
+    _fail(fails, ys.shape == yf.shape and np.allclose(ys, yf, rtol=1e-13, atol=1e-18), "softmax rows= subset")
+    return fails
+
+
+def check_stitch(st) -> list:
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(16))
+    # row [0, c]: y = [b, c^3 + b] -> [1/(1+e^{c^3}), e^{c^3}/(1+e^{c^3})]
+    for c, b in ((0.7, 0.4), (-1.3, -0.9)):
+        y = np.asarray(st(np.array([[0.0, c]]), np.array([b])))[0]
+        p1 = 1 / (1 + math.exp(-(c ** 3)))
+        _fail(fails, abs(y[1] - p1) < 1e-15 and abs(y[0] - (1 - p1)) < 1e-15,
+              f"stitch two-element closed form c={c}")
+    # the cube keeps its sign: A = [-1, 1] -> y = [-1+b, 1+b]
+    y = np.asarray(st(np.array([[-1.0, 1.0]]), np.array([0.5])))[0]
+    _fail(fails, abs(y[0] - 1 / (1 + math.e ** 2)) < 1e-15, "stitch cube sign")
+    # the row bias is a per-row shift: the result equals the zero-bias one
+    A = rng.standard_normal((5, 32)) * 2
+    b = rng.random(5) * 2 - 1
+    y1 = np.asarray(st(A, b))
+    y0 = np.asarray(st(A, np.zeros(5)))
+    _fail(fails, np.allclose(y1, y0, rtol=1e-12, atol=1e-300), "stitch row-bias shift invariance")
+    _fail(fails, np.all(np.abs(y1.sum(axis=1) - 1) < 1e-12), "stitch row sums")
+    # brute force on a tiny case with Python floats
+    A = rng.standard_normal((3, 5))
+    b = rng.random(3)
+    ref = np.zeros_like(A)
+    for i in range(3):
+        yv = [float(A[i, j]) ** 3 + float(b[i]) for j in range(5)]
+        m = max(yv)
+        e = [math.exp(v - m) for v in yv]
+        s = math.fsum(e)
+        ref[i] = [v / s for v in e]
+    _fail(fails, np.allclose(np.asarray(st(A, b)), ref, rtol=1e-13, atol=1e-16), "stitch brute force")
+    return fails

@@ -1,0 +1,170 @@
+"""Plant plausible mistakes in copies of the oracle and check a pin catches each.
+
+The mistakes live here, on the CPU, in throw-away lambdas; the oracle itself
+is untouched.  Each mutant must fail at least one pin in ``oracle_pins``.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import oracle_pins as pins
+
+S = math.sqrt(2 / math.pi)
+
+
+def _ln(g, gamma, beta, eps, *, ddof=0, eps_out=False, use_beta=True, center_out=True,
+        gamma_first=False, var_about_zero=False):
+    g = np.asarray(g, dtype=np.float64)
+    gamma = np.asarray(gamma, dtype=np.float64)
+    if gamma_first:
+        g = g * gamma
+    mean = g.mean(-1, keepdims=True)
+    d = g - mean
+    if var_about_zero:
+        var = (g * g).mean(-1, keepdims=True)
+    else:
+        var = (d * d).sum(-1, keepdims=True) / (g.shape[-1] - ddof)
+    den = (np.sqrt(var) + eps) if eps_out else np.sqrt(var + eps)
+    y = (d if center_out else g) / den
+    if not gamma_first:
+        y = y * gamma
+    return y + (beta if use_beta else 0.0)
+
+
+LN_MUTANTS = {
+    "unbiased variance": lambda g, ga, be, e: _ln(g, ga, be, e, ddof=1),
+    "eps outside sqrt": lambda g, ga, be, e: _ln(g, ga, be, e, eps_out=True),
+    "beta dropped": lambda g, ga, be, e: _ln(g, ga, be, e, use_beta=False),
+    "mean not subtracted": lambda g, ga, be, e: _ln(g, ga, be, e, center_out=False),
+    "gamma before normalising": lambda g, ga, be, e: _ln(g, ga, be, e, gamma_first=True),
+    "variance about zero": lambda g, ga, be, e: _ln(g, ga, be, e, var_about_zero=True),
+}
+
+
+def _sm(z, *, sub_max=True, base=math.e, by_max=False):
+    z = np.asarray(z, dtype=np.float64)
+    m = z.max(-1, keepdims=True) if sub_max else 0.0
+    e = np.power(base, z - m)
+    return e / (e.max(-1, keepdims=True) if by_max else e.sum(-1, keepdims=True))
+
+
+SM_MUTANTS = {
+    "no max subtraction": lambda z: _sm(z, sub_max=False),
+    "base 2": lambda z: _sm(z, base=2.0),
+    "divide by max": lambda z: _sm(z, by_max=True),
+    "softmax over columns": lambda z: (lambda zz: np.exp(zz - zz.max(0)) / np.exp(zz - zz.max(0)).sum(0))(np.asarray(z, dtype=np.float64)),
+}
+
+GELU_MUTANTS = {
+    "cubic coefficient": lambda x: 0.5 * x * (1 + np.tanh(S * (x + 0.0447 * x ** 3))),
+    "sqrt(2/pi) dropped": lambda x: 0.5 * x * (1 + np.tanh(x + 0.044715 * x ** 3)),
+    "sigmoid form": lambda x: x / (1 + np.exp(-1.702 * x)),
+    "missing half": lambda x: x * (1 + np.tanh(S * (x + 0.044715 * x ** 3))),
+    "erf form": lambda x: 0.5 * x * (1 + np.vectorize(math.erf)(np.asarray(x) / math.sqrt(2))),
+}
+
+GEMM_MUTANTS = {
+    "transposed W": lambda X, W: np.asarray(X) @ np.asarray(W).T if np.asarray(W).shape[0] == np.asarray(W).shape[1] else (np.asarray(X) @ np.asarray(W)).T,
+    "dropped last k term": lambda X, W: np.asarray(X, float)[:, :-1] @ np.asarray(W, float)[:-1],
+    "fp32 accumulation": lambda X, W: (np.asarray(X, np.float32) @ np.asarray(W, np.float32)).astype(np.float64) + 1e-9,
+}
+
+
+def _rownorm(X, W, bias, gamma, beta, *, alpha=1.0, eps=1e-5, act="none", rows=None,
+             order="ok"):
+    X = np.asarray(X, float)
+    if rows is not None:
+        X = X[rows]
+    P = X @ np.asarray(W, float)
+    b = 0.0 if bias is None else np.asarray(bias, float)
+    x = alpha * (P + b) if order == "bias before alpha" else alpha * P + b
+    if order == "gelu after norm":
+        y = oracle.layernorm_rows(x, gamma, beta, eps)
+        return oracle.gelu_tanh(y) if act == "gelu_tanh" else y
+    g = oracle.gelu_tanh(x) if act == "gelu_tanh" else x
+    if order == "bias after gelu":
+        g = (oracle.gelu_tanh(alpha * P) if act == "gelu_tanh" else alpha * P) + b
+    return oracle.layernorm_rows(g, gamma, beta, eps)
+
+
+ROWNORM_MUTANTS = {
+    k: (lambda kk: (lambda *a, **kw: _rownorm(*a, order=kk, **kw)))(k)
+    for k in ("bias before alpha", "gelu after norm", "bias after gelu")
+}
+
+
+def _softmax_fused(X, W, *, scale, bias=None, rows=None, mistake):
+    X = np.asarray(X, float)
+    if rows is not None:
+        X = X[rows]
+    z = X @ np.asarray(W, float)
+    if mistake == "scale after bias" and bias is not None:
+        z = scale * (z + np.asarray(bias))
+    elif mistake == "bias ignored":
+        z = scale * z
+    elif mistake == "scale dropped":
+        z = z + (0 if bias is None else np.asarray(bias))
+    else:
+        z = scale * z + (0 if bias is None else np.asarray(bias))
+    return oracle.softmax_rows(z)
+
+
+SOFTMAX_FUSED_MUTANTS = {k: (lambda kk: (lambda *a, **kw: _softmax_fused(*a, mistake=kk, **kw)))(k)
+                         for k in ("scale after bias", "bias ignored", "scale dropped")}
+
+
+def _stitch(A, b, rows=None, *, mistake):
+    A = np.asarray(A, float)
+    b = np.asarray(b, float)
+    if mistake == "square":
+        y = A * A + b[:, None]
+    elif mistake == "abs cube":
+        y = np.abs(A) ** 3 + b[:, None]
+    elif mistake == "bias multiplies":
+        y = A ** 3 * b[:, None]
+    else:
+        y = A ** 3 + b[None, :A.shape[1]] if A.shape[1] == b.shape[0] else A ** 3 - b[:, None] * A
+    return oracle.softmax_rows(y)
+
+
+STITCH_MUTANTS = {k: (lambda kk: (lambda A, b, rows=None: _stitch(A, b, rows, mistake=kk)))(k)
+                  for k in ("square", "abs cube", "bias multiplies", "bias per column")}
+
+
+@pytest.mark.parametrize("name", sorted(LN_MUTANTS))
+def test_layernorm_mutant_caught(name):
+    assert pins.check_layernorm(LN_MUTANTS[name]), name
+
+
+@pytest.mark.parametrize("name", sorted(SM_MUTANTS))
+def test_softmax_mutant_caught(name):
+    with np.errstate(over="ignore", invalid="ignore"):
+        assert pins.check_softmax(SM_MUTANTS[name]), name
+
+
+@pytest.mark.parametrize("name", sorted(GELU_MUTANTS))
+def test_gelu_mutant_caught(name):
+    assert pins.check_gelu(GELU_MUTANTS[name]), name
+
+
+@pytest.mark.parametrize("name", sorted(GEMM_MUTANTS))
+def test_gemm_mutant_caught(name):
+    assert pins.check_gemm(GEMM_MUTANTS[name]), name
+
+
+@pytest.mark.parametrize("name", sorted(ROWNORM_MUTANTS))
+def test_rownorm_mutant_caught(name):
+    assert pins.check_rownorm_composition(ROWNORM_MUTANTS[name]), name
+
+
+@pytest.mark.parametrize("name", sorted(SOFTMAX_FUSED_MUTANTS))
+def test_softmax_composition_mutant_caught(name):
+    assert pins.check_softmax_composition(SOFTMAX_FUSED_MUTANTS[name]), name
+
+
+@pytest.mark.parametrize("name", sorted(STITCH_MUTANTS))
+def test_stitch_mutant_caught(name):
+    with np.errstate(over="ignore", invalid="ignore"):
+        assert pins.check_stitch(STITCH_MUTANTS[name]), name
