@@ -1,0 +1,256 @@
+/*
+ * cf.h -- C ABI of libcf: a dense bf16 GEMM fused, in one kernel, with a
+ * dependency-rich memory-intensive epilogue (elementwise ops -> row reduction
+ * -> broadcast back over the row), plus the GEMM-free stitched
+ * reduce -> broadcast subgraph on irregular shapes.  sm_103a (GB300) only.
+ *
+ * Pages the operations come from (cited by title and section):
+ *   [ComFuse]   "ComFuse: Fusing Complex Memory-Intensive Subgraphs with
+ *               Compute-Intensive Kernels For Modern GPU Architectures"
+ *   [AStitch]   "AStitch: enabling a new multi-dimensional optimization space
+ *               for memory-intensive ML training and inference on modern SIMT
+ *               architectures"
+ *   [sass2mlir] the sass2mlir kernel-fusion page ("Two answers to the same
+ *               idle GPU"; section "How we fuse kernels")
+ *
+ * Conventions for every call
+ *   - Pointers marked (device) are CUDA device pointers owned by the caller;
+ *     the library never allocates, frees or keeps them.  (host) pointers are
+ *     read during the call only.
+ *   - Matrices are dense row-major with no padding: X[M,K], W[K,N], Y[M,N].
+ *     bf16 is IEEE bfloat16 stored as 16-bit words; fp32 is IEEE binary32.
+ *   - Every call is asynchronous and stream-ordered on `stream` (NULL = the
+ *     legacy default stream).  The return value reports argument, shape,
+ *     alignment, residency and launch errors synchronously; nothing is
+ *     launched when it is not CF_OK.
+ *   - Errors found on the device (a bounded wait that ran out, an index check)
+ *     are recorded in the workspace's error word and reported by
+ *     cf_get_device_status().  Kernels never trap: on such an error they
+ *     skip the remaining waits, finish, and leave garbage in the output.
+ *   - A workspace is caller-owned device memory of at least the size the
+ *     matching *_workspace_size() call returns, zeroed once (cf_workspace_init
+ *     or cudaMemset) before first use.  Its counters clean themselves at the
+ *     end of every launch, so it is reusable by later calls on the same
+ *     stream without re-zeroing; it must not be used by two launches that can
+ *     run at the same time.  After CF_ERR_DEVICE_TIMEOUT re-zero it.
+ *   - Y must not alias X or W (each output element is owned by exactly one
+ *     tile: [sass2mlir] "Epilogue fusion - the core technique", ownership
+ *     legality).
+ */
+#ifndef CF_H
+#define CF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CF_API __attribute__((visibility("default")))
+#else
+#define CF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *cf_stream_t;
+
+typedef enum {
+    CF_OK = 0,
+    CF_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad enum      */
+    CF_ERR_UNSUPPORTED = 2,        /* shape outside the supported set (below)    */
+    CF_ERR_MISALIGNED = 3,         /* pointer not 16-byte aligned                */
+    CF_ERR_WORKSPACE_TOO_SMALL = 4,
+    CF_ERR_NOT_RESIDENT = 5,       /* the launch cannot keep every CTA that must
+                                      meet at an in-kernel barrier resident     */
+    CF_ERR_CUDA = 6,               /* a CUDA runtime call failed (see
+                                      cf_last_cuda_error)                        */
+    CF_ERR_DEVICE_TIMEOUT = 7,     /* device: a bounded wait ran out             */
+    CF_ERR_DEVICE_BOUNDS = 8,      /* device: an index check failed              */
+    CF_ERR_NO_DEVICE = 9           /* no sm_103 device is current                */
+} cf_status;
+
+typedef enum {
+    CF_ACT_NONE = 0,
+    CF_ACT_GELU_TANH = 1           /* 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))) */
+} cf_activation;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+CF_API const char *cf_status_string(cf_status status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+CF_API int cf_version(void);
+
+/* The cudaError_t of the most recent failing CUDA call made by this thread
+ * inside the library (0 if none). */
+CF_API int cf_last_cuda_error(void);
+
+/* ------------------------------------------------------------------------ */
+/* Tuning knobs.  Every field's zero value means "choose automatically".    */
+/* ------------------------------------------------------------------------ */
+typedef struct cf_tuning {
+    int32_t n_slice;        /* GEMM: columns of one CTA tile (64, 128, 256)        */
+    int32_t cluster_size;   /* GEMM: CTAs per cluster along the row (1..16)
+                               stitched: CTAs per row for the split mapping      */
+    int32_t peer_max;       /* inter-CTA aggregation: peer all-to-all when the
+                               participating CTA count C_N <= peer_max, else
+                               leader-follower ([ComFuse] dual-mode strategy).
+                               0 = 8; negative = always leader-follower          */
+    int32_t max_clusters;   /* cap on resident clusters of the persistent grid     */
+    int32_t stages;         /* GEMM: depth of the shared-memory operand ring       */
+    int32_t stitch_mapping; /* 0 auto, 1 packed rows, 2 split rows over a cluster  */
+    uint32_t timeout_us;    /* bound of every device spin (0 = 200000 us)          */
+    int32_t extra_arrivals; /* TEST HOOK: added to the arrival count the global
+                               barrier waits for; > 0 makes that wait run out
+                               (CF_ERR_DEVICE_TIMEOUT) without faulting.  0 in
+                               normal use.                                        */
+} cf_tuning;
+
+/* Fill *t with the defaults (all zero). */
+CF_API void cf_tuning_default(cf_tuning *t);
+
+/* ------------------------------------------------------------------------ */
+/* Launch plan (host logic, no GPU needed).                                 */
+/* ------------------------------------------------------------------------ */
+typedef struct cf_plan {
+    int32_t n_slice;        /* tile columns per CTA                                */
+    int32_t ctas_per_row;   /* C_total = N / n_slice                               */
+    int32_t cluster_size;   /* C_N: CTAs of one cluster along the row              */
+    int32_t groups;         /* G = C_total / C_N clusters per row block; G > 1 uses
+                               the global partial buffer + in-kernel barrier      */
+    int32_t leader_mode;    /* 0 peer all-to-all, 1 leader-follower                */
+    int32_t row_blocks;     /* ceil(M / 128)                                       */
+    int32_t clusters;       /* clusters of the persistent grid                     */
+    int32_t stages;         /* operand ring depth                                  */
+    int32_t smem_bytes;     /* dynamic shared memory per CTA                       */
+} cf_plan;
+
+/* Plan a fused GEMM+row-reduce launch for a device with `sm_count` SMs, where
+ * max_active_clusters[c] (c = 1..16) is how many clusters of c CTAs can be
+ * resident at once (0 = that size cannot launch).  Pure host arithmetic: the
+ * same choice the launch calls make after querying the device.
+ * Returns CF_UNSUPPORTED for shapes outside the supported set and
+ * CF_ERR_NOT_RESIDENT if no residency-valid plan exists. */
+CF_API cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
+                             const int32_t max_active_clusters[17],
+                             const cf_tuning *tuning, cf_plan *plan);
+
+/* The plan the fused GEMM calls would use on the current device for the
+ * epilogue `kind` (0 LayerNorm, 1 GELU+LayerNorm, 2 softmax).  Queries the
+ * device's residency for every cluster size that could be chosen;
+ * max_active_clusters (may be NULL) receives those counts (index = cluster
+ * size).  Synchronous, launches nothing. */
+CF_API cf_status cf_query_gemm_fused_plan(int64_t M, int64_t N, int64_t K, int32_t kind,
+                                          const cf_tuning *tuning, cf_plan *plan,
+                                          int32_t max_active_clusters[17]);
+
+/* ------------------------------------------------------------------------ */
+/* Workspace                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of workspace a fused GEMM call on (M, N, K) may need under any
+ * tuning: error word + per-row-block arrival/departure counters + the global
+ * partial buffer (one 8-byte statistic per row and cluster group). */
+CF_API size_t cf_gemm_fused_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* Bytes of workspace a stitched call on (rows, cols) needs (error word). */
+CF_API size_t cf_stitch_workspace_size(int64_t rows, int64_t cols);
+
+/* Zero `bytes` of the workspace (device) on `stream`. */
+CF_API cf_status cf_workspace_init(void *workspace, size_t bytes, cf_stream_t stream);
+
+/* Wait for `stream`, then read and clear the workspace's error word.
+ * Returns CF_OK or the first device-side error recorded since the last read;
+ * *info (may be NULL) receives where it happened (the row block of a global
+ * barrier wait that ran out, or the pipeline wait's role id). */
+CF_API cf_status cf_get_device_status(void *workspace, cf_stream_t stream, int32_t *info);
+
+/* ------------------------------------------------------------------------ */
+/* Fused GEMM + bias (+GELU) + LayerNorm                                     */
+/* ------------------------------------------------------------------------ */
+/* Y = LayerNorm_row(act(alpha * X.W + bias)) * gamma + beta
+ *
+ * [ComFuse] Stage-Stream Execution Model, Fig. 3: stage 1 computes
+ * x = alpha*Acc + Bias and the mean reduction; stage 2 reuses x through the
+ * bypass path for x - mean; the LayerNorm is the nested "reduce over inputs,
+ * normalise using original values" pattern of the Fusion Spec IR (Eq. (10)).
+ * Mean and biased variance are taken over the N values of each row (after
+ * the activation), eps inside the square root, gamma/beta after normalising.
+ *
+ *   X     (device) bf16 [M,K] row-major (K contiguous)
+ *   W     (device) bf16 [K,N] row-major (N contiguous)
+ *   bias  (device) fp32 [N], or NULL for no bias
+ *   gamma (device) fp32 [N];  beta (device) fp32 [N]
+ *   Y     (device) bf16 [M,N] row-major, written (round to nearest even)
+ *   alpha, eps    scalars; act: CF_ACT_NONE or CF_ACT_GELU_TANH
+ *   workspace     (device) >= cf_gemm_fused_workspace_size(M,N,K) bytes
+ * Accumulation is fp32 in tensor memory; the epilogue is fp32.
+ * Supported: M >= 0 (M = 0 is a no-op), K a positive multiple of 64,
+ * N a positive multiple of 64 with N / n_slice <= 16 * 64 CTAs per row;
+ * X, W, Y, bias, gamma, beta 16-byte aligned.
+ * Rows wider than one cluster use the global partial buffer and an in-kernel
+ * barrier ([AStitch] "Global" stitching scheme; [sass2mlir] "Grid-barrier
+ * synthesis"); this needs every cluster of the persistent grid resident and
+ * returns CF_ERR_NOT_RESIDENT otherwise. */
+CF_API cf_status cf_gemm_fused_rownorm(const void *X, const void *W, const float *bias,
+                                const float *gamma, const float *beta, void *Y,
+                                int64_t M, int64_t N, int64_t K, float alpha,
+                                float eps, cf_activation act, void *workspace,
+                                size_t workspace_bytes, cf_stream_t stream);
+
+CF_API cf_status cf_gemm_fused_rownorm_ex(const void *X, const void *W, const float *bias,
+                                   const float *gamma, const float *beta, void *Y,
+                                   int64_t M, int64_t N, int64_t K, float alpha,
+                                   float eps, cf_activation act, void *workspace,
+                                   size_t workspace_bytes, cf_stream_t stream,
+                                   const cf_tuning *tuning);
+
+/* ------------------------------------------------------------------------ */
+/* Fused GEMM + scaled row softmax                                           */
+/* ------------------------------------------------------------------------ */
+/* Y = softmax_row(scale * X.W + bias)
+ *
+ * [ComFuse] Fusion Spec IR: Softmax as a nested reduction (row max, then the
+ * sum of exp(z - max)), whose statistics are broadcast back over the row.
+ * X, W, Y, workspace as for cf_gemm_fused_rownorm; bias (device) fp32 [N] or
+ * NULL.  Same supported shapes. */
+CF_API cf_status cf_gemm_fused_rowsoftmax(const void *X, const void *W, const float *bias,
+                                   void *Y, int64_t M, int64_t N, int64_t K, float scale,
+                                   void *workspace, size_t workspace_bytes,
+                                   cf_stream_t stream);
+
+CF_API cf_status cf_gemm_fused_rowsoftmax_ex(const void *X, const void *W, const float *bias,
+                                      void *Y, int64_t M, int64_t N, int64_t K,
+                                      float scale, void *workspace, size_t workspace_bytes,
+                                      cf_stream_t stream, const cf_tuning *tuning);
+
+/* ------------------------------------------------------------------------ */
+/* Stitched reduce -> broadcast subgraph (no GEMM)                           */
+/* ------------------------------------------------------------------------ */
+/* out = softmax_row(A*A*A + row_bias[row])
+ *
+ * [AStitch] "Adaptive thread mapping": very many tiny rows are packed several
+ * to a warp (horizontal packing); very few huge rows are split over the CTAs
+ * of a cluster (task splitting), the mapping chosen from the actual shape.
+ *   A        (device) fp32 [rows, cols] row-major
+ *   row_bias (device) fp32 [rows]
+ *   out      (device) fp32 [rows, cols] row-major; must not alias A
+ *   workspace (device) >= cf_stitch_workspace_size(rows, cols) bytes
+ * Supported: rows >= 0, cols >= 0 (either 0 is a no-op), cols <= 262144.
+ * 16-byte aligned A/out with cols % 4 == 0 take the 128-bit path; anything
+ * else takes the scalar path of the same kernels. */
+CF_API cf_status cf_stitch_rowreduce_broadcast(const float *A, const float *row_bias, float *out,
+                                        int64_t rows, int64_t cols, void *workspace,
+                                        size_t workspace_bytes, cf_stream_t stream);
+
+CF_API cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *row_bias,
+                                           float *out, int64_t rows, int64_t cols,
+                                           void *workspace, size_t workspace_bytes,
+                                           cf_stream_t stream, const cf_tuning *tuning);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CF_H */

@@ -1,0 +1,447 @@
+// cf_api.cu -- the C ABI of libcf (declared in include/cf.h): argument and
+// alignment checks, the launch planner (row-to-CTA/cluster mapping, residency
+// check for the in-kernel barrier), TMA descriptor construction, launches,
+// and the device error word.  No allocation happens on any call path.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/cf.h"
+#include "cf_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+cf_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = int(e);
+    return CF_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int next_pow2(int v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+constexpr int kMaxSmem = 232448;  // 227 KB dynamic shared memory per CTA (sm_100 family)
+constexpr uint32_t kDefaultTimeoutUs = 200000;
+
+std::mutex g_mu;
+
+// -------------------------------------------------------------------------
+// driver entry point for tensor-map encoding (no link-time libcuda dependency)
+// -------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box (box_cols x box_rows),
+// 128-byte swizzle; out-of-range elements read as zero.
+bool make_tmap_bf16(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                    uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// -------------------------------------------------------------------------
+// occupancy cache: max co-resident clusters for (device, kind, cluster, smem)
+// -------------------------------------------------------------------------
+int max_active_cached(int device, int kind, int cluster, int smem) {
+    static std::map<std::tuple<int, int, int, int>, int> cache;
+    auto key = std::make_tuple(device, kind, cluster, smem);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int n = cf::gemm_fused_max_active_clusters(kind, cluster, smem);
+    std::lock_guard<std::mutex> lk(g_mu);
+    cache[key] = n;
+    return n;
+}
+
+int gemm_stages_for(int n_slice, int cluster, int requested) {
+    int s = requested > 0 ? requested : 6;
+    while (s > 2 && cf::gemm_fused_smem_bytes(s, cluster, n_slice) > kMaxSmem) --s;
+    return s;
+}
+
+}  // namespace
+
+namespace cf {
+
+bool current_device_info(DeviceInfo *out) {
+    static std::map<int, DeviceInfo> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = cache.find(dev);
+        if (it != cache.end()) {
+            *out = it->second;
+            return true;
+        }
+    }
+    DeviceInfo d;
+    d.device = dev;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    cache[dev] = d;
+    *out = d;
+    return true;
+}
+
+}  // namespace cf
+
+// =========================================================================
+// C ABI
+// =========================================================================
+extern "C" {
+
+const char *cf_status_string(cf_status s) {
+    switch (s) {
+        case CF_OK: return "CF_OK";
+        case CF_ERR_INVALID_ARG: return "CF_ERR_INVALID_ARG";
+        case CF_ERR_UNSUPPORTED: return "CF_ERR_UNSUPPORTED";
+        case CF_ERR_MISALIGNED: return "CF_ERR_MISALIGNED";
+        case CF_ERR_WORKSPACE_TOO_SMALL: return "CF_ERR_WORKSPACE_TOO_SMALL";
+        case CF_ERR_NOT_RESIDENT: return "CF_ERR_NOT_RESIDENT";
+        case CF_ERR_CUDA: return "CF_ERR_CUDA";
+        case CF_ERR_DEVICE_TIMEOUT: return "CF_ERR_DEVICE_TIMEOUT";
+        case CF_ERR_DEVICE_BOUNDS: return "CF_ERR_DEVICE_BOUNDS";
+        case CF_ERR_NO_DEVICE: return "CF_ERR_NO_DEVICE";
+        default: return "CF_ERR_UNKNOWN";
+    }
+}
+
+int cf_version(void) { return 100; }
+
+int cf_last_cuda_error(void) { return g_last_cuda_error; }
+
+void cf_tuning_default(cf_tuning *t) {
+    if (t) std::memset(t, 0, sizeof(*t));
+}
+
+cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
+                             const int32_t max_active_clusters[17], const cf_tuning *tuning, cf_plan *plan) {
+    if (!plan || !max_active_clusters || M < 0 || N <= 0 || K <= 0 || sm_count <= 0) return CF_ERR_INVALID_ARG;
+    cf_tuning tz;
+    cf_tuning_default(&tz);
+    const cf_tuning &t = tuning ? *tuning : tz;
+    if (K % 64 != 0 || N % 64 != 0) return CF_ERR_UNSUPPORTED;
+    if (M > (int64_t(1) << 31) - 128 || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return CF_ERR_UNSUPPORTED;
+    int ns = t.n_slice;
+    if (ns == 0) ns = (N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64;
+    if ((ns != 64 && ns != 128 && ns != 256) || N % ns != 0) return CF_ERR_UNSUPPORTED;
+    const int64_t cpr64 = N / ns;
+    if (cpr64 > 16 * 64) return CF_ERR_UNSUPPORTED;
+    const int cpr = int(cpr64);
+    int C = 0;
+    if (t.cluster_size > 0) {
+        if (t.cluster_size > 16 || cpr % t.cluster_size != 0) return CF_ERR_UNSUPPORTED;
+        if (max_active_clusters[t.cluster_size] <= 0) return CF_ERR_NOT_RESIDENT;
+        C = t.cluster_size;
+    } else if (cpr <= 16 && max_active_clusters[cpr] > 0) {
+        C = cpr;  // one cluster holds the whole row: pure DSMEM path
+    } else {
+        for (int c = std::min(16, cpr); c >= 1; --c)
+            if (cpr % c == 0 && max_active_clusters[c] > 0) {
+                C = c;
+                break;
+            }
+        if (C == 0) return CF_ERR_NOT_RESIDENT;
+    }
+    const int G = cpr / C;
+    const int rb = int((M + cf::kBlockM - 1) / cf::kBlockM);
+    const int64_t tickets = int64_t(rb) * G;
+    int ncl = max_active_clusters[C];
+    if (t.max_clusters > 0) ncl = std::min(ncl, int(t.max_clusters));
+    if (G > 1) {
+        // every cluster that meets at a row block's barrier must be resident:
+        // the persistent grid never exceeds the resident cluster count, and
+        // holds a multiple of G clusters so each keeps one column group
+        ncl = (ncl / G) * G;
+        if (ncl < G) return CF_ERR_NOT_RESIDENT;
+    }
+    if (tickets < ncl) ncl = int(std::max<int64_t>(tickets, G > 1 ? G : 1));
+    const int peer_max = t.peer_max == 0 ? 8 : t.peer_max;
+    plan->n_slice = ns;
+    plan->ctas_per_row = cpr;
+    plan->cluster_size = C;
+    plan->groups = G;
+    plan->leader_mode = (peer_max < 0 || C > peer_max) ? 1 : 0;
+    plan->row_blocks = rb;
+    plan->clusters = std::max(ncl, 1);
+    plan->stages = gemm_stages_for(ns, C, t.stages);
+    plan->smem_bytes = cf::gemm_fused_smem_bytes(plan->stages, C, ns);
+    if (plan->smem_bytes > kMaxSmem) return CF_ERR_UNSUPPORTED;
+    return CF_OK;
+}
+
+size_t cf_gemm_fused_workspace_size(int64_t M, int64_t N, int64_t K) {
+    (void)K;
+    if (M < 0 || N <= 0) return cf::kErrBytes;
+    const size_t rb = size_t((M + cf::kBlockM - 1) / cf::kBlockM);
+    const size_t gmax = size_t((N + 63) / 64);
+    return cf::kErrBytes + cf::align_up(8 * rb, 256) + rb * gmax * 128 * sizeof(float2);
+}
+
+size_t cf_stitch_workspace_size(int64_t rows, int64_t cols) {
+    (void)rows;
+    (void)cols;
+    return cf::kErrBytes;
+}
+
+cf_status cf_workspace_init(void *ws, size_t bytes, cf_stream_t stream) {
+    if (!ws) return CF_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(ws, 0, bytes, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CF_OK : cuda_fail(e);
+}
+
+cf_status cf_get_device_status(void *ws, cf_stream_t stream, int32_t *info) {
+    if (!ws) return CF_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t w[2] = {0, 0};
+    e = cudaMemcpy(w, ws, sizeof(w), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (info) *info = int32_t(w[1]);
+    if (w[0] != 0) {
+        e = cudaMemset(ws, 0, sizeof(w));
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return cf_status(w[0]);
+}
+
+// -------------------------------------------------------------------------
+// stitched subgraph
+// -------------------------------------------------------------------------
+cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *row_bias, float *out, int64_t rows,
+                                           int64_t cols, void *ws, size_t ws_bytes, cf_stream_t stream,
+                                           const cf_tuning *tuning) {
+    if (rows < 0 || cols < 0) return CF_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return CF_OK;
+    if (!A || !row_bias || !out || !ws) return CF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(row_bias)) & 3u)
+        return CF_ERR_MISALIGNED;
+    if (cols > 262144) return CF_ERR_UNSUPPORTED;
+    if (ws_bytes < cf_stitch_workspace_size(rows, cols)) return CF_ERR_WORKSPACE_TOO_SMALL;
+    cf_tuning tz;
+    cf_tuning_default(&tz);
+    const cf_tuning &t = tuning ? *tuning : tz;
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+
+    cf::StitchPlan p;
+    p.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out);
+    const int ng = int((cols + 3) / 4);
+    int mapping = t.stitch_mapping;
+    if (mapping == 0) mapping = (ng <= 32) ? 1 : 2;
+    if (mapping == 1 && ng > 32) return CF_ERR_UNSUPPORTED;
+    p.mapping = mapping;
+    if (mapping == 1) {
+        p.lpr = next_pow2(ng);
+        const int rows_per_cta_iter = 8 * (32 / p.lpr) * 4;
+        const int64_t want = (rows + rows_per_cta_iter - 1) / rows_per_cta_iter;
+        int bps = cf::stitch_packed_blocks_per_sm(p.lpr, p.vec);
+        if (bps <= 0) bps = 1;
+        p.grid = int(std::min<int64_t>(want, int64_t(dev.sm_count) * bps));
+    } else if (mapping == 2) {
+        int C = t.cluster_size;
+        if (C <= 0) {
+            const int c_min = (ng + 256 * 16 - 1) / (256 * 16);
+            int c_par = 1;
+            if (rows < 2 * dev.sm_count) c_par = next_pow2(int((2 * dev.sm_count + rows - 1) / rows));
+            C = std::max(c_min, c_par);
+            C = std::min(C, 16);
+            while (C > 1 && C > ng) C >>= 1;
+        }
+        if (C < 1 || C > 16) return CF_ERR_UNSUPPORTED;
+        const int gpc = (ng + C - 1) / C;
+        const int v = next_pow2((gpc + 255) / 256);
+        if (v > 16) return CF_ERR_UNSUPPORTED;
+        p.cluster = C;
+        p.per_thread = v;
+        const int peer_max = t.peer_max == 0 ? 8 : t.peer_max;
+        p.leader = (peer_max < 0 || C > peer_max) ? 1 : 0;
+        const int64_t clusters = std::min<int64_t>(rows, 8192);
+        p.grid = int(clusters * C);
+    } else {
+        return CF_ERR_INVALID_ARG;
+    }
+    cudaError_t e = cf::launch_stitch(p, A, row_bias, out, rows, cols, static_cast<uint32_t *>(ws),
+                                      reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CF_OK;
+}
+
+cf_status cf_stitch_rowreduce_broadcast(const float *A, const float *row_bias, float *out, int64_t rows,
+                                        int64_t cols, void *ws, size_t ws_bytes, cf_stream_t stream) {
+    return cf_stitch_rowreduce_broadcast_ex(A, row_bias, out, rows, cols, ws, ws_bytes, stream, nullptr);
+}
+
+// -------------------------------------------------------------------------
+// fused GEMM
+// -------------------------------------------------------------------------
+// residency of every candidate cluster size at the shared memory it would use
+static cf_status device_plan(int kind, int64_t M, int64_t N, int64_t K, const cf_tuning *tuning,
+                             const cf::DeviceInfo &dev, cf_plan *plan, int32_t active[17]) {
+    cf_tuning tz;
+    cf_tuning_default(&tz);
+    const cf_tuning &t = tuning ? *tuning : tz;
+    if (N <= 0 || K <= 0 || N % 64 != 0 || K % 64 != 0) return CF_ERR_UNSUPPORTED;
+    int ns = t.n_slice ? t.n_slice : ((N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64);
+    if ((ns != 64 && ns != 128 && ns != 256) || N % ns != 0) return CF_ERR_UNSUPPORTED;
+    const int64_t cpr = N / ns;
+    for (int c = 0; c <= 16; ++c) active[c] = 0;
+    for (int c = 1; c <= 16; ++c) {
+        if (cpr % c != 0) continue;
+        if (t.cluster_size > 0 && c != t.cluster_size) continue;
+        const int st = gemm_stages_for(ns, c, t.stages);
+        const int smem = cf::gemm_fused_smem_bytes(st, c, ns);
+        if (smem > std::min(kMaxSmem, dev.max_smem_optin)) continue;
+        active[c] = max_active_cached(dev.device, kind, c, smem);
+    }
+    return cf_plan_gemm_fused(M, N, K, dev.sm_count, active, tuning, plan);
+}
+
+cf_status cf_query_gemm_fused_plan(int64_t M, int64_t N, int64_t K, int32_t kind, const cf_tuning *tuning,
+                                   cf_plan *plan, int32_t max_active_clusters[17]) {
+    if (!plan || kind < 0 || kind > 2 || M < 0) return CF_ERR_INVALID_ARG;
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+    int32_t active[17];
+    cf_status st = device_plan(kind, M, N, K, tuning, dev, plan, active);
+    if (max_active_clusters)
+        for (int c = 0; c <= 16; ++c) max_active_clusters[c] = active[c];
+    return st;
+}
+
+static cf_status gemm_fused_common(int kind, const void *X, const void *W, const float *bias, const float *gamma,
+                                   const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha,
+                                   float eps, void *ws, size_t ws_bytes, cf_stream_t stream,
+                                   const cf_tuning *tuning) {
+    if (M < 0 || N <= 0 || K <= 0) return CF_ERR_INVALID_ARG;
+    if (!X || !W || !Y || !ws) return CF_ERR_INVALID_ARG;
+    if (kind != cf::EPI_SOFTMAX && (!gamma || !beta)) return CF_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || (bias && !aligned16(bias)) ||
+        (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)))
+        return CF_ERR_MISALIGNED;
+    if (K % 64 != 0 || N % 64 != 0) return CF_ERR_UNSUPPORTED;
+    if (ws_bytes < cf_gemm_fused_workspace_size(M, N, K)) return CF_ERR_WORKSPACE_TOO_SMALL;
+    if (M == 0) return CF_OK;
+    cf_tuning tz;
+    cf_tuning_default(&tz);
+    const cf_tuning &t = tuning ? *tuning : tz;
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+
+    cf_plan plan;
+    int32_t active[17];
+    cf_status st = device_plan(kind, M, N, K, tuning, dev, &plan, active);
+    if (st != CF_OK) return st;
+
+    cf::GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, 128)) return CF_ERR_CUDA;
+    if (!make_tmap_bf16(&a.tmap_w, W, uint64_t(K), uint64_t(N), 64, 64)) return CF_ERR_CUDA;
+    a.bias = bias;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.y = static_cast<uint16_t *>(Y);
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    a.err = reinterpret_cast<uint32_t *>(wsb);
+    a.counters = reinterpret_cast<uint32_t *>(wsb + cf::kErrBytes);
+    a.partials = reinterpret_cast<float2 *>(wsb + cf::kErrBytes + cf::align_up(8 * size_t(plan.row_blocks), 256));
+    a.M = int(M);
+    a.N = int(N);
+    a.K = int(K);
+    a.alpha = alpha;
+    a.eps = eps;
+    a.n_slice = plan.n_slice;
+    a.cluster = plan.cluster_size;
+    a.groups = plan.groups;
+    a.leader = plan.leader_mode;
+    a.row_blocks = plan.row_blocks;
+    a.extra_arrivals = t.extra_arrivals;
+    a.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
+    cudaError_t e = cf::launch_gemm_fused(kind, a, plan.clusters, plan.stages, plan.smem_bytes,
+                                          reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CF_OK;
+}
+
+cf_status cf_gemm_fused_rownorm_ex(const void *X, const void *W, const float *bias, const float *gamma,
+                                   const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha,
+                                   float eps, cf_activation act, void *ws, size_t ws_bytes, cf_stream_t stream,
+                                   const cf_tuning *tuning) {
+    int kind;
+    if (act == CF_ACT_NONE) kind = cf::EPI_LN;
+    else if (act == CF_ACT_GELU_TANH) kind = cf::EPI_GELU_LN;
+    else return CF_ERR_INVALID_ARG;
+    return gemm_fused_common(kind, X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, ws, ws_bytes, stream, tuning);
+}
+
+cf_status cf_gemm_fused_rownorm(const void *X, const void *W, const float *bias, const float *gamma,
+                                const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha,
+                                float eps, cf_activation act, void *ws, size_t ws_bytes, cf_stream_t stream) {
+    return cf_gemm_fused_rownorm_ex(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, ws, ws_bytes, stream,
+                                    nullptr);
+}
+
+cf_status cf_gemm_fused_rowsoftmax_ex(const void *X, const void *W, const float *bias, void *Y, int64_t M,
+                                      int64_t N, int64_t K, float scale, void *ws, size_t ws_bytes,
+                                      cf_stream_t stream, const cf_tuning *tuning) {
+    return gemm_fused_common(cf::EPI_SOFTMAX, X, W, bias, nullptr, nullptr, Y, M, N, K, scale, 0.f, ws, ws_bytes,
+                             stream, tuning);
+}
+
+cf_status cf_gemm_fused_rowsoftmax(const void *X, const void *W, const float *bias, void *Y, int64_t M, int64_t N,
+                                   int64_t K, float scale, void *ws, size_t ws_bytes, cf_stream_t stream) {
+    return cf_gemm_fused_rowsoftmax_ex(X, W, bias, Y, M, N, K, scale, ws, ws_bytes, stream, nullptr);
+}
+
+}  // extern "C"

@@ -1,0 +1,90 @@
+// cf_internal.h -- launchers shared between the C-ABI layer (cf_api.cu) and
+// the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace cf {
+
+// Workspace layout (device, caller-owned, zeroed once):
+//   [0, 256)                 error word: u32 status, u32 info, rest reserved
+//   [256, 256 + 8*RB pad)    per-row-block counters: arrive[RB], depart[RB]
+//   [...]                    global partials: [RB][G][128] float2
+constexpr size_t kErrBytes = 256;
+constexpr int kBlockM = 128;  // rows of one GEMM tile (tcgen05 M = 128, one row per TMEM lane)
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int max_smem_optin = 0;
+};
+
+// Returns the current device's info (cached per device).  false if none.
+bool current_device_info(DeviceInfo *out);
+
+// --------------------------------------------------------------------------
+// stitched kernels (stitch.cu)
+// --------------------------------------------------------------------------
+struct StitchPlan {
+    int mapping = 0;      // 1 packed, 2 split
+    int lpr = 0;          // packed: lanes per row (1..32, power of two)
+    int cluster = 0;      // split: CTAs per row
+    int per_thread = 0;   // split: float4 groups per thread (1..16, power of two)
+    int leader = 0;       // split: leader-follower aggregation
+    bool vec = false;     // 128-bit path
+    int grid = 0;         // CTAs
+};
+
+cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias, float *out, int64_t rows,
+                          int64_t cols, uint32_t *err, cudaStream_t stream);
+
+int stitch_packed_blocks_per_sm(int lpr, bool vec);
+
+// --------------------------------------------------------------------------
+// fused GEMM kernels (gemm_fused.cu)
+// --------------------------------------------------------------------------
+enum EpiKind : int {
+    EPI_LN = 0,        // alpha*acc + bias -> LayerNorm -> bf16
+    EPI_GELU_LN = 1,   // alpha*acc + bias -> GELU(tanh) -> LayerNorm -> bf16
+    EPI_SOFTMAX = 2,   // scale*acc + bias -> softmax -> bf16
+};
+
+struct GemmArgs {
+    CUtensorMap tmap_x;   // X [M,K] bf16, box 64(K) x 128(M), 128B swizzle
+    CUtensorMap tmap_w;   // W [K,N] bf16, box 64(N) x 64(K), 128B swizzle
+    const float *bias;    // [N] or null
+    const float *gamma;   // [N] (LN)
+    const float *beta;    // [N] (LN)
+    uint16_t *y;          // [M,N] bf16
+    uint32_t *err;        // workspace error word
+    uint32_t *counters;   // [2*RB]: arrive, depart
+    float2 *partials;     // [RB][G][128]
+    int M, N, K;
+    float alpha;          // LN: multiplies acc; softmax: scale
+    float eps;
+    int n_slice;          // columns of one tile
+    int cluster;          // C_N
+    int groups;           // G
+    int leader;           // leader-follower aggregation in the cluster
+    int row_blocks;       // RB
+    int extra_arrivals;   // test hook
+    unsigned long long timeout_ns;
+};
+
+// dynamic shared memory of one CTA for a ring of `stages` and a cluster of `cluster`
+int gemm_fused_smem_bytes(int stages, int cluster, int n_slice);
+
+// Query max co-resident clusters of `cluster` CTAs for the fused kernel of
+// `kind` with `smem` dynamic shared memory (0 if it cannot launch).
+int gemm_fused_max_active_clusters(int kind, int cluster, int smem);
+
+cudaError_t launch_gemm_fused(int kind, const GemmArgs &a, int clusters, int stages, int smem,
+                              cudaStream_t stream);
+
+}  // namespace cf

@@ -1,0 +1,638 @@
+// gemm_fused.cu -- one persistent sm_103a kernel computing a bf16 GEMM and,
+// in the same kernel, a dependency-rich epilogue whose row reductions span
+// many tiles and CTAs:
+//     LN:       y = LayerNorm(alpha*acc + bias) * gamma + beta
+//     GELU_LN:  y = LayerNorm(GELU_tanh(alpha*acc + bias)) * gamma + beta
+//     SOFTMAX:  y = softmax(scale*acc + bias)
+//
+// Design (GB300-first; the page mechanisms it realises are cited inline):
+//  * Tiles are 128 rows x n_slice columns (n_slice <= 256).  A row block's
+//    N / n_slice tiles go to the CTAs of one thread-block cluster (CTA rank
+//    r -> column slice r), so all CTAs of one reduction are co-scheduled
+//    ([ComFuse] Stage-Stream Execution Model, cluster mapping).  Rows wider
+//    than one cluster are split over G clusters that meet through a
+//    global-memory partial buffer and an in-kernel counter barrier
+//    ([AStitch] "Global" stitching scheme; [sass2mlir] "Grid-barrier
+//    synthesis").
+//  * Warp roles: warp 0 issues TMA loads of X and W tiles into an S-stage
+//    shared-memory ring; warp 1 allocates tensor memory and issues
+//    tcgen05.mma (bf16 x bf16 -> fp32) into one of two TMEM accumulators;
+//    warps 2..9 run the epilogue of tile i while the MMA of tile i+1 fills the
+//    other accumulator ([ComFuse] PingPong MainLoop/Epilogue overlap).
+//  * Epilogue = chained stage DAGs ([ComFuse] Stage-Stream Execution Model):
+//    pass 1 streams 32-column fragments out of TMEM through the elementwise
+//    nodes and aggregates thread-locally at the reduction node; the stage-1
+//    value is written back into TMEM (the bypass path of Fig. 3, so GELU and
+//    the bias are not recomputed); the reduce phase runs three levels
+//    (thread-local over the fragment -> the other half-row's warps through
+//    one shared-memory buffer -> the cluster over DSMEM with TMA bulk copies,
+//    peer all-to-all for few CTAs or leader-follower for many) and, for wide
+//    rows, the global partial buffer; pass 2 (the PostOp) re-reads TMEM,
+//    normalises with the broadcast statistics and stores bf16.
+//  * Every wait is bounded by %globaltimer; on expiry the error word in the
+//    workspace records CF_ERR_DEVICE_TIMEOUT and all roles drain.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "cf_internal.h"
+#include "ptx.cuh"
+#include "rowstats.cuh"
+
+namespace cf {
+namespace {
+
+constexpr int kThreads = 320;      // 10 warps
+constexpr int kEpiWarps = 8;       // warps 2..9
+constexpr int kEpiThreads = 256;
+constexpr int kBK = 64;            // K per stage (128 bytes of bf16: one swizzle atom)
+constexpr int kABytes = kBlockM * kBK * 2;  // 16 KB
+
+// named barriers (0 is __syncthreads)
+constexpr uint32_t kBarEpi = 1;    // all 256 epilogue threads
+constexpr uint32_t kBarHalf0 = 2;  // epilogue half 0 (columns [0, n_slice/2))
+
+// error info codes for the bounded pipeline waits
+constexpr uint32_t kInfoProducer = 0x10000000u;
+constexpr uint32_t kInfoMma = 0x20000000u;
+constexpr uint32_t kInfoEpi = 0x30000000u;
+constexpr uint32_t kInfoXchg = 0x40000000u;
+constexpr uint32_t kInfoGlobal = 0x50000000u;
+
+struct SmemLayout {
+    uint32_t stage_bytes;  // A + B of one stage
+    uint32_t ring;         // offset of the operand ring (1024-aligned)
+    uint32_t send;         // float2 [2][128]
+    uint32_t slot;         // float2 [2][C][128]
+    uint32_t res;          // float2 [2][128]
+    uint32_t red;          // float2 [128]
+    uint32_t bars;         // mbarriers
+    uint32_t total;        // bytes from the aligned base
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n_slice) {
+    SmemLayout L;
+    L.stage_bytes = kABytes + uint32_t(n_slice) * kBK * 2;
+    L.ring = 0;
+    uint32_t off = L.ring + uint32_t(stages) * L.stage_bytes;
+    L.send = off;
+    off += 2 * 128 * 8;
+    L.slot = off;
+    off += 2 * uint32_t(cluster) * 128 * 8;
+    L.res = off;
+    off += 2 * 128 * 8;
+    L.red = off;
+    off += 128 * 8;
+    L.bars = off;
+    off += 256;
+    L.total = off;
+    return L;
+}
+
+// barrier slots inside L.bars (8 bytes each)
+struct Bars {
+    uint32_t full0, empty0;  // [stages] each
+    uint32_t tmem_full0, tmem_empty0;  // [2]
+    uint32_t xfull0, xres0;            // [2]
+    uint32_t mma_done;
+    uint32_t misc;  // u32: tmem base, u32: abort flag
+};
+
+__device__ __forceinline__ Bars bars_at(uint32_t base, int stages) {
+    Bars b;
+    b.full0 = base;
+    b.empty0 = base + 8 * stages;
+    b.tmem_full0 = base + 16 * stages;
+    b.tmem_empty0 = b.tmem_full0 + 16;
+    b.xfull0 = b.tmem_empty0 + 16;
+    b.xres0 = b.xfull0 + 16;
+    b.mma_done = b.xres0 + 16;
+    b.misc = b.mma_done + 8;
+    return b;
+}
+
+// tcgen05 shared-memory matrix descriptor, 128-byte swizzle
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+    d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+    d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+    d |= uint64_t(1) << 46;  // descriptor version for tcgen05
+    d |= uint64_t(2) << 61;  // SWIZZLE_128B
+    return d;
+}
+
+// instruction descriptor: kind::f16, A = B = bf16, D = fp32, A K-major,
+// B MN-major (W is [K,N] with N contiguous), M = 128, N = n
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) | (uint32_t(n >> 3) << 17) |
+           (uint32_t(kBlockM >> 4) << 24);
+}
+
+__device__ __forceinline__ float gelu_tanh_dev(float x) {
+    // 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+    const float k0 = 0.7978845608028654f;
+    const float k1 = 0.044715f;
+    const float u = k0 * fmaf(k1 * x, x * x, x);
+    return 0.5f * x * (1.0f + ptx::tanh_approx(u));
+}
+
+__device__ __forceinline__ float4 ldg4(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
+
+// load 32 consecutive parameters (or zeros when p is null)
+__device__ __forceinline__ void load_param32(const float *p, float (&v)[32]) {
+    if (p == nullptr) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float4 t = ldg4(p + 4 * j);
+        v[4 * j + 0] = t.x;
+        v[4 * j + 1] = t.y;
+        v[4 * j + 2] = t.z;
+        v[4 * j + 3] = t.w;
+    }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_constant__ GemmArgs a, int stages) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+
+    const int C = a.cluster;
+    const int G = a.groups;
+    const int ns = a.n_slice;
+    const int half = ns / 2;
+    const int nk = a.K / kBK;
+    const int T = a.row_blocks * G;  // tickets: (row block, cluster group), row-block major
+    const SmemLayout L = smem_layout(stages, C, ns);
+    const Bars B = bars_at(base + L.bars, stages);
+    volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + (B.misc - base));
+    volatile uint32_t *abort = misc + 1;
+    const uint64_t tmo = a.timeout_ns;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const uint32_t cid = ptx::cluster_id_x();
+    const uint32_t ncl = ptx::nclusters_x();
+    const uint32_t tmem_cols = (ns * 2 <= 32) ? 32u : uint32_t(ns * 2);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            ptx::mbar_init(B.full0 + 8 * s, 1);
+            ptx::mbar_init(B.empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(B.tmem_full0 + 8 * b, 1);
+            ptx::mbar_init(B.tmem_empty0 + 8 * b, kEpiWarps);
+            ptx::mbar_init(B.xfull0 + 8 * b, 1);
+            ptx::mbar_init(B.xres0 + 8 * b, 1);
+        }
+        ptx::mbar_init(B.mma_done, 1);
+        misc[1] = 0u;
+        ptx::fence_mbarrier_init_cluster();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(B.misc, tmem_cols);
+        ptx::tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&a.tmap_x);
+        ptx::prefetch_tensormap(&a.tmap_w);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    // barrier initialisation is visible cluster-wide before any peer signals it
+    ptx::cluster_sync();
+    const uint32_t tmem_base = misc[0];
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint32_t tx = uint32_t(kABytes) + uint32_t(ns) * kBK * 2;
+            uint32_t it = 0;
+            for (int t = cid; t < T; t += ncl) {
+                const int rb = t / G, g = t % G;
+                const int m0 = rb * kBlockM;
+                const int n0 = (g * C + int(rank)) * ns;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const uint32_t s = it % uint32_t(stages);
+                    const uint32_t ph = (it / uint32_t(stages)) & 1u;
+                    ptx::mbar_wait_bounded(B.empty0 + 8 * s, ph ^ 1u, tmo, abort, a.err, kInfoProducer | s);
+                    if (*abort) break;
+                    const uint32_t sa = base + L.ring + s * L.stage_bytes;
+                    const uint32_t sb = sa + kABytes;
+                    ptx::mbar_arrive_expect_tx(B.full0 + 8 * s, tx);
+                    ptx::tma_load_2d(sa, &a.tmap_x, B.full0 + 8 * s, kb * kBK, m0);
+                    for (int j = 0; j < ns / 64; ++j)
+                        ptx::tma_load_2d(sb + j * 8192, &a.tmap_w, B.full0 + 8 * s, n0 + j * 64, kb * kBK);
+                }
+                if (*abort) break;
+            }
+            // drain: every load issued has landed before the CTA may exit
+            const uint32_t issued = it;
+            const uint32_t first = issued > uint32_t(stages) ? issued - uint32_t(stages) : 0u;
+            for (uint32_t i = first; i < issued; ++i) {
+                const uint32_t s = i % uint32_t(stages);
+                const uint32_t ph = (i / uint32_t(stages)) & 1u;
+                uint32_t dummy = 0;
+                volatile uint32_t local_abort = 0;
+                ptx::mbar_wait_bounded(B.full0 + 8 * s, ph, tmo, &local_abort, nullptr, 0);
+                (void)dummy;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(ns);
+            uint32_t it = 0;
+            int tile = 0;
+            for (int t = cid; t < T; t += ncl, ++tile) {
+                const uint32_t buf = tile & 1;
+                const uint32_t tph = (uint32_t(tile) >> 1) & 1u;
+                ptx::mbar_wait_bounded(B.tmem_empty0 + 8 * buf, tph ^ 1u, tmo, abort, a.err, kInfoMma | buf);
+                if (*abort) break;
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + buf * uint32_t(ns);
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const uint32_t s = it % uint32_t(stages);
+                    const uint32_t ph = (it / uint32_t(stages)) & 1u;
+                    ptx::mbar_wait_bounded(B.full0 + 8 * s, ph, tmo, abort, a.err, kInfoMma | 0x100u | s);
+                    if (*abort) break;
+                    ptx::tc_fence_after();
+                    const uint32_t sa = base + L.ring + s * L.stage_bytes;
+                    const uint32_t sb = sa + kABytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        // A: K-major, advance 16 elements (32 B) inside the swizzle atom
+                        const uint64_t ad = sw128_desc(sa + k * 32, 16, 1024);
+                        // B: MN-major, 64-column blocks 8 KB apart, 8-row K groups 1 KB apart;
+                        // advance 16 K rows = 2 KB
+                        const uint64_t bd = sw128_desc(sb + k * 2048, 8192, 1024);
+                        ptx::mma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(B.empty0 + 8 * s);  // stage free once these MMAs completed
+                }
+                if (*abort) break;
+                ptx::mma_commit(B.tmem_full0 + 8 * buf);  // accumulator ready
+            }
+            // every MMA issued has completed before TMEM may be released
+            ptx::mma_commit(B.mma_done);
+            volatile uint32_t local_abort = 0;
+            ptx::mbar_wait_bounded(B.mma_done, 0, tmo, &local_abort, nullptr, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int e = warp - 2;              // 0..7
+        const int q = warp & 3;              // TMEM lane quadrant this warp may access
+        const int h = e >> 2;                // column half of the tile
+        const int row = q * 32 + lane;       // row of the tile == TMEM lane
+        const int et = threadIdx.x - 64;     // 0..255
+        const bool et0 = (et == 0);
+        float2 *const send = reinterpret_cast<float2 *>(gbase + L.send);
+        float2 *const slot = reinterpret_cast<float2 *>(gbase + L.slot);
+        float2 *const res = reinterpret_cast<float2 *>(gbase + L.res);
+        float2 *const red = reinterpret_cast<float2 *>(gbase + L.red);
+        const float fN = float(a.N);
+
+        int tile = 0;
+        for (int t = cid; t < T; t += ncl, ++tile) {
+            const int rb = t / G, g = t % G;
+            const int m0 = rb * kBlockM;
+            const int nc0 = (g * C + int(rank)) * ns + h * half;  // first global column of this thread
+            const uint32_t buf = tile & 1;
+            const uint32_t tph = (uint32_t(tile) >> 1) & 1u;
+            const uint32_t xp = buf;  // exchange buffer set
+            const uint32_t xph = tph;
+
+            ptx::mbar_wait_bounded(B.tmem_full0 + 8 * buf, tph, tmo, abort, a.err, kInfoEpi | buf);
+            ptx::tc_fence_after();
+            const uint32_t tacc = tmem_base + (uint32_t(q * 32) << 16) + buf * uint32_t(ns) + uint32_t(h * half);
+            const int nchunks = half / 32;
+
+            // ---------------- stage 1: compute phase + thread-local aggregation
+            float2 part;  // LN: (mean, M2) over `half` columns; softmax: (max, sum exp)
+            if constexpr (EPI == EPI_SOFTMAX) {
+                float mt = neg_inf();
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t v[32];
+                    float bb[32];
+                    ptx::tmem_ld32(tacc + c * 32, v);
+                    load_param32(a.bias ? a.bias + nc0 + c * 32 : nullptr, bb);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) mt = fmaxf(mt, fmaf(a.alpha, __uint_as_float(v[j]), bb[j]));
+                }
+                float st = 0.f;
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t v[32];
+                    float bb[32];
+                    ptx::tmem_ld32(tacc + c * 32, v);
+                    load_param32(a.bias ? a.bias + nc0 + c * 32 : nullptr, bb);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float z = fmaf(a.alpha, __uint_as_float(v[j]), bb[j]);
+                        const float ex = ptx::ex2_approx((z - mt) * kLog2e);
+                        st += ex;
+                        v[j] = __float_as_uint(ex);
+                    }
+                    ptx::tmem_st32(tacc + c * 32, v);  // bypass: exp(z - mt) for the PostOp
+                }
+                ptx::tmem_st_wait();
+                part = make_float2(mt, st);
+            } else {
+                MeanM2 acc{0.f, 0.f};
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t v[32];
+                    float x[32];
+                    ptx::tmem_ld32(tacc + c * 32, v);
+                    load_param32(a.bias ? a.bias + nc0 + c * 32 : nullptr, x);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        float xv = fmaf(a.alpha, __uint_as_float(v[j]), x[j]);
+                        if constexpr (EPI == EPI_GELU_LN) xv = gelu_tanh_dev(xv);
+                        x[j] = xv;
+                        v[j] = __float_as_uint(xv);
+                    }
+                    ptx::tmem_st32(tacc + c * 32, v);  // bypass: stage-1 value for the PostOp
+                    const MeanM2 cs = chunk_mean_m2(x);
+                    acc = (c == 0) ? cs : combine_counts(acc, float(32 * c), cs, 32.f);
+                }
+                ptx::tmem_st_wait();
+                part = make_float2(acc.mean, acc.m2);
+            }
+
+            // ---------------- level 2: the two column halves through shared memory
+            if (h == 1) red[row] = part;
+            ptx::named_bar_sync(kBarEpi, kEpiThreads);
+            if (h == 0) {
+                const float2 o = red[row];
+                float2 cta;
+                if constexpr (EPI == EPI_SOFTMAX) {
+                    const MaxSum r = combine_maxsum(MaxSum{part.x, part.y}, MaxSum{o.x, o.y});
+                    cta = make_float2(r.m, r.s);
+                } else {
+                    const MeanM2 r = combine_equal(MeanM2{part.x, part.y}, MeanM2{o.x, o.y}, float(half));
+                    cta = make_float2(r.mean, r.m2);
+                }
+                send[xp * 128 + row] = cta;
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar_sync(kBarHalf0, 128);
+                // ---------------- level 3: inter-CTA over DSMEM (TMA bulk copies)
+                if (et0 && !*abort) {
+                    const uint32_t src = base + L.send + xp * 1024;
+                    const uint32_t my_slot = base + L.slot + (xp * C + rank) * 1024;
+                    const uint32_t xfull = B.xfull0 + 8 * xp;
+                    if (!a.leader) {
+                        ptx::mbar_arrive_expect_tx(xfull, uint32_t(C) * 1024u);
+                        for (int r = 0; r < C; ++r)
+                            ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, r), src, 1024, ptx::mapa(xfull, r));
+                    } else {
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(xfull, uint32_t(C) * 1024u);
+                        else ptx::mbar_arrive_expect_tx(B.xres0 + 8 * xp, 1024u);
+                        ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, 0), src, 1024, ptx::mapa(xfull, 0));
+                    }
+                }
+            }
+            float2 stat;  // cluster-combined statistic of this row
+            if (!a.leader) {
+                ptx::mbar_wait_bounded<true>(B.xfull0 + 8 * xp, xph, tmo, abort, a.err, kInfoXchg | xp);
+                const float2 *sl = slot + xp * C * 128 + row;
+                stat = sl[0];
+                for (int r = 1; r < C; ++r) {
+                    const float2 o = sl[r * 128];
+                    if constexpr (EPI == EPI_SOFTMAX) {
+                        const MaxSum m = combine_maxsum(MaxSum{stat.x, stat.y}, MaxSum{o.x, o.y});
+                        stat = make_float2(m.m, m.s);
+                    } else {
+                        const MeanM2 m = combine_counts(MeanM2{stat.x, stat.y}, float(r * ns), MeanM2{o.x, o.y}, float(ns));
+                        stat = make_float2(m.mean, m.m2);
+                    }
+                }
+            } else {
+                if (rank == 0) {
+                    if (h == 0) {
+                        ptx::mbar_wait_bounded<true>(B.xfull0 + 8 * xp, xph, tmo, abort, a.err, kInfoXchg | xp);
+                        const float2 *sl = slot + xp * C * 128 + row;
+                        float2 s2 = sl[0];
+                        for (int r = 1; r < C; ++r) {
+                            const float2 o = sl[r * 128];
+                            if constexpr (EPI == EPI_SOFTMAX) {
+                                const MaxSum m = combine_maxsum(MaxSum{s2.x, s2.y}, MaxSum{o.x, o.y});
+                                s2 = make_float2(m.m, m.s);
+                            } else {
+                                const MeanM2 m =
+                                    combine_counts(MeanM2{s2.x, s2.y}, float(r * ns), MeanM2{o.x, o.y}, float(ns));
+                                s2 = make_float2(m.mean, m.m2);
+                            }
+                        }
+                        res[xp * 128 + row] = s2;
+                        ptx::fence_proxy_async_smem();
+                        ptx::named_bar_sync(kBarHalf0, 128);
+                        if (et0 && !*abort) {
+                            const uint32_t src = base + L.res + xp * 1024;
+                            for (int r = 1; r < C; ++r)
+                                ptx::bulk_copy_s2cluster(ptx::mapa(src, r), src, 1024, ptx::mapa(B.xres0 + 8 * xp, r));
+                        }
+                    }
+                    ptx::named_bar_sync(kBarEpi, kEpiThreads);
+                } else {
+                    ptx::mbar_wait_bounded<true>(B.xres0 + 8 * xp, xph, tmo, abort, a.err, kInfoXchg | 0x10u | xp);
+                }
+                stat = res[xp * 128 + row];
+            }
+
+            // ---------------- level 4: rows wider than a cluster (global partials)
+            if (G > 1) {
+                uint32_t *cnt = a.counters + rb;
+                uint32_t *dep = a.counters + a.row_blocks + rb;
+                float2 *pbase = a.partials + (size_t(rb) * G) * 128;
+                if (rank == 0 && h == 0) {
+                    pbase[g * 128 + row] = stat;
+                    __threadfence();
+                    ptx::named_bar_sync(kBarHalf0, 128);
+                    if (et0) ptx::atom_add_release_gpu(cnt, 1u);
+                }
+                if (et0) {
+                    const uint32_t target = uint32_t(G + a.extra_arrivals);
+                    const uint64_t t0 = ptx::globaltimer();
+                    while (!*abort) {
+                        if (ptx::ld_acquire_gpu(cnt) >= target) break;
+                        if (ptx::ld_relaxed_gpu(a.err) != 0u) {
+                            *abort = 1u;
+                            break;
+                        }
+                        if (ptx::globaltimer() - t0 > tmo) {
+                            *abort = 1u;
+                            ptx::record_error(a.err, 7u, kInfoGlobal | uint32_t(rb));
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    // last CTA of this row block to leave resets its counters
+                    if (ptx::atom_add_acq_rel_gpu(dep, 1u) == uint32_t(G * C) - 1u) {
+                        ptx::st_relaxed_gpu(cnt, 0u);
+                        ptx::st_relaxed_gpu(dep, 0u);
+                    }
+                }
+                ptx::named_bar_sync(kBarEpi, kEpiThreads);
+                float2 s2 = ptx::ld_relaxed_gpu_f2(pbase + row);
+                for (int gg = 1; gg < G; ++gg) {
+                    const float2 o = ptx::ld_relaxed_gpu_f2(pbase + gg * 128 + row);
+                    if constexpr (EPI == EPI_SOFTMAX) {
+                        const MaxSum m = combine_maxsum(MaxSum{s2.x, s2.y}, MaxSum{o.x, o.y});
+                        s2 = make_float2(m.m, m.s);
+                    } else {
+                        const float nc = float(ns * C);
+                        const MeanM2 m = combine_counts(MeanM2{s2.x, s2.y}, float(gg) * nc, MeanM2{o.x, o.y}, nc);
+                        s2 = make_float2(m.mean, m.m2);
+                    }
+                }
+                stat = s2;
+            }
+
+            // ---------------- stage 2 (PostOp): broadcast the statistic back over the row
+            const int grow = m0 + row;
+            uint16_t *yrow = a.y + size_t(grow) * a.N + nc0;
+            if constexpr (EPI == EPI_SOFTMAX) {
+                // exp(z - mt) * exp(mt - m) / s
+                const float f = ptx::ex2_approx((part.x - stat.x) * kLog2e) / stat.y;
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tacc + c * 32, v);
+                    ptx::tmem_ld_wait();
+                    if (grow < a.M) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 w;
+                            w.x = ptx::pack_bf16x2(__uint_as_float(v[8 * j + 0]) * f, __uint_as_float(v[8 * j + 1]) * f);
+                            w.y = ptx::pack_bf16x2(__uint_as_float(v[8 * j + 2]) * f, __uint_as_float(v[8 * j + 3]) * f);
+                            w.z = ptx::pack_bf16x2(__uint_as_float(v[8 * j + 4]) * f, __uint_as_float(v[8 * j + 5]) * f);
+                            w.w = ptx::pack_bf16x2(__uint_as_float(v[8 * j + 6]) * f, __uint_as_float(v[8 * j + 7]) * f);
+                            dst[j] = w;
+                        }
+                    }
+                }
+            } else {
+                const float mean = stat.x;
+                const float rstd = rsqrtf(stat.y / fN + a.eps);
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t v[32];
+                    float gm[32], bt[32];
+                    ptx::tmem_ld32(tacc + c * 32, v);
+                    load_param32(a.gamma + nc0 + c * 32, gm);
+                    load_param32(a.beta + nc0 + c * 32, bt);
+                    ptx::tmem_ld_wait();
+                    if (grow < a.M) {
+                        float y[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) y[j] = fmaf((__uint_as_float(v[j]) - mean) * rstd, gm[j], bt[j]);
+                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 w;
+                            w.x = ptx::pack_bf16x2(y[8 * j + 0], y[8 * j + 1]);
+                            w.y = ptx::pack_bf16x2(y[8 * j + 2], y[8 * j + 3]);
+                            w.z = ptx::pack_bf16x2(y[8 * j + 4], y[8 * j + 5]);
+                            w.w = ptx::pack_bf16x2(y[8 * j + 6], y[8 * j + 7]);
+                            dst[j] = w;
+                        }
+                    }
+                }
+            }
+            // accumulator buffer free for the MMA of tile + 2
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(B.tmem_empty0 + 8 * buf);
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    // no CTA leaves while a peer may still access its shared memory
+    ptx::cluster_sync();
+    if (warp == 1) ptx::tmem_dealloc(tmem_base, tmem_cols);
+}
+
+void *kernel_for(int kind) {
+    switch (kind) {
+        case EPI_LN: return reinterpret_cast<void *>(&gemm_fused_kernel<EPI_LN>);
+        case EPI_GELU_LN: return reinterpret_cast<void *>(&gemm_fused_kernel<EPI_GELU_LN>);
+        case EPI_SOFTMAX: return reinterpret_cast<void *>(&gemm_fused_kernel<EPI_SOFTMAX>);
+        default: return nullptr;
+    }
+}
+
+}  // namespace
+
+int gemm_fused_smem_bytes(int stages, int cluster, int n_slice) {
+    return int(smem_layout(stages, cluster, n_slice).total) + 1024;  // + alignment slack
+}
+
+int gemm_fused_max_active_clusters(int kind, int cluster, int smem) {
+    void *fn = kernel_for(kind);
+    if (!fn) return 0;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+    if (cluster > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster * 64);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+cudaError_t launch_gemm_fused(int kind, const GemmArgs &a, int clusters, int stages, int smem,
+                              cudaStream_t stream) {
+    void *fn = kernel_for(kind);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (a.cluster > 8) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(clusters * a.cluster);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = a.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int st = stages;
+    void *args[] = {(void *)&a, (void *)&st};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace cf

@@ -1,0 +1,123 @@
+// rowstats.cuh -- statistics carried by the row reductions and their combine
+// operators, used at every level of the three-level reduction ([ComFuse]
+// three-level reduction scheme, Fig. 4): thread-local aggregation over a
+// fragment, warp butterfly shuffles, warp-group combine through shared
+// memory, and inter-CTA aggregation over distributed shared memory (and, for
+// rows wider than a cluster, a global-memory partial buffer).
+//
+// Two statistics are needed by the epilogues here:
+//  * LayerNorm: (mean, M2) of n values, M2 = sum (x - mean)^2, combined with
+//    Chan et al.'s pairwise update; n is implicit (every partial of one level
+//    covers the same number of columns).
+//  * Softmax: (m, s) with m = max z, s = sum exp(z - m), combined by
+//    rescaling the smaller-max side ("online softmax").
+// Combines happen in a fixed order everywhere, so every CTA that combines the
+// same partials obtains bitwise-identical statistics, and repeated launches
+// are bitwise reproducible (no floating-point atomics).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace cf {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// --------------------------------------------------------------------------
+// LayerNorm statistics
+// --------------------------------------------------------------------------
+struct MeanM2 {
+    float mean;
+    float m2;
+};
+
+// Combine two partials over the same count n each; result covers 2n.
+__device__ __forceinline__ MeanM2 combine_equal(MeanM2 a, MeanM2 b, float n) {
+    const float d = b.mean - a.mean;
+    MeanM2 r;
+    r.mean = a.mean + 0.5f * d;
+    r.m2 = a.m2 + b.m2 + d * d * (0.5f * n);
+    return r;
+}
+
+// Fold partial b (count nb) into running a (count na).
+__device__ __forceinline__ MeanM2 combine_counts(MeanM2 a, float na, MeanM2 b, float nb) {
+    const float n = na + nb;
+    const float d = b.mean - a.mean;
+    const float f = nb / n;
+    MeanM2 r;
+    r.mean = a.mean + d * f;
+    r.m2 = a.m2 + b.m2 + d * d * (na * f);
+    return r;
+}
+
+// (mean, M2) of 32 values held by one thread: two passes over registers.
+__device__ __forceinline__ MeanM2 chunk_mean_m2(const float (&x)[32]) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) s += x[j];
+    const float mean = s * (1.0f / 32.0f);
+    float m2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float d = x[j] - mean;
+        m2 = fmaf(d, d, m2);
+    }
+    return MeanM2{mean, m2};
+}
+
+// --------------------------------------------------------------------------
+// Softmax statistics
+// --------------------------------------------------------------------------
+struct MaxSum {
+    float m;
+    float s;
+};
+
+__device__ __forceinline__ MaxSum combine_maxsum(MaxSum a, MaxSum b) {
+    const float m = fmaxf(a.m, b.m);
+    MaxSum r;
+    r.m = m;
+    if (m == neg_inf()) {
+        r.s = 0.f;
+    } else {
+        r.s = a.s * ptx::ex2_approx((a.m - m) * kLog2e) + b.s * ptx::ex2_approx((b.m - m) * kLog2e);
+    }
+    return r;
+}
+
+// --------------------------------------------------------------------------
+// level 1: warp butterfly over groups of `width` lanes (power of two)
+// --------------------------------------------------------------------------
+template <int kWidth>
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = kWidth / 2; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+template <int kWidth>
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = kWidth / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+template <int kWidth>
+__device__ __forceinline__ MaxSum warp_maxsum(MaxSum v) {
+#pragma unroll
+    for (int off = kWidth / 2; off > 0; off >>= 1) {
+        MaxSum o;
+        o.m = __shfl_xor_sync(0xffffffffu, v.m, off);
+        o.s = __shfl_xor_sync(0xffffffffu, v.s, off);
+        // lower lane first: every lane folds the same pair in the same order
+        v = (threadIdx.x & off) ? combine_maxsum(o, v) : combine_maxsum(v, o);
+    }
+    return v;
+}
+
+}  // namespace cf

@@ -1,0 +1,313 @@
+// stitch.cu -- GEMM-free stitched reduce -> broadcast subgraph
+//     y = A*A*A + b[row];  m = rowmax y;  s = rowsum exp(y - m);  out = exp(y - m)/s
+// on irregular shapes ([AStitch] "Adaptive thread mapping": 750000x32 rows are
+// packed many to a block, 64x30000 rows are split over several blocks; the
+// mapping is chosen from the actual shape).
+//
+// Every element is read from HBM once with a 128-bit streaming load (the
+// value is single-use: [sass2mlir] "Load widening and cache policy"), kept in
+// registers through the whole subgraph (the exp is computed once and reused
+// for the output), and written once.  The reduction is the three-level
+// scheme of [ComFuse] (three-level reduction, Fig. 4): warp butterfly, then
+// shared memory across warps, then -- when a row is split over the CTAs of a
+// thread-block cluster -- distributed shared memory, peer all-to-all for few
+// CTAs or leader-follower for many.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "cf_internal.h"
+#include "ptx.cuh"
+#include "rowstats.cuh"
+
+namespace cf {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;  // row slots per thread in flight (memory-level parallelism)
+
+__device__ __forceinline__ float cube_plus(float a, float b) { return a * a * a + b; }
+
+// --------------------------------------------------------------------------
+// Packed mapping: LPR lanes per row (horizontal packing), each lane one
+// 4-column group, 32/LPR rows per warp and kUnroll row slots per thread.
+// --------------------------------------------------------------------------
+template <int LPR, bool VEC>
+__global__ void __launch_bounds__(kThreads) stitch_packed_kernel(const float *__restrict__ A,
+                                                                 const float *__restrict__ bias,
+                                                                 float *__restrict__ out, int64_t rows,
+                                                                 int cols) {
+    constexpr int RPW = 32 / LPR;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & (LPR - 1);
+    const int rsub = lane / LPR;
+    const int c0 = sub * 4;
+    const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+    constexpr int64_t kRowsPerIter = int64_t(RPW) * kUnroll;
+
+    for (int64_t base = warp * kRowsPerIter; base < rows; base += nwarps * kRowsPerIter) {
+        float v[kUnroll][4];
+        float bb[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t r = base + u * RPW + rsub;
+            const bool rv = r < rows;
+            if constexpr (VEC) {
+                float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (rv && c0 < cols) t = __ldcs(reinterpret_cast<const float4 *>(A + r * cols + c0));
+                v[u][0] = t.x;
+                v[u][1] = t.y;
+                v[u][2] = t.z;
+                v[u][3] = t.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[u][j] = (rv && c0 + j < cols) ? __ldcs(A + r * cols + c0 + j) : 0.f;
+            }
+            bb[u] = rv ? __ldg(bias + r) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t r = base + u * RPW + rsub;
+            float m = neg_inf();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[u][j] = cube_plus(v[u][j], bb[u]);
+                if (c0 + j < cols) m = fmaxf(m, v[u][j]);
+            }
+            m = warp_max<LPR>(m);
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float e = (c0 + j < cols) ? ptx::ex2_approx((v[u][j] - m) * kLog2e) : 0.f;
+                v[u][j] = e;
+                s += e;
+            }
+            s = warp_sum<LPR>(s);
+            const float inv = 1.0f / s;
+            if (r < rows) {
+                if constexpr (VEC) {
+                    if (c0 < cols)
+                        __stcs(reinterpret_cast<float4 *>(out + r * cols + c0),
+                               make_float4(v[u][0] * inv, v[u][1] * inv, v[u][2] * inv, v[u][3] * inv));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (c0 + j < cols) __stcs(out + r * cols + c0 + j, v[u][j] * inv);
+                }
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// Split mapping: one row per cluster of C CTAs (task splitting).  CTA `rank`
+// owns 4-column groups [rank*gpc, rank*gpc + gpc); each thread holds up to V
+// groups in registers.
+// --------------------------------------------------------------------------
+template <int V, bool VEC>
+__global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__restrict__ A,
+                                                                const float *__restrict__ bias,
+                                                                float *__restrict__ out, int64_t rows, int cols,
+                                                                int gpc, int leader) {
+    __shared__ MaxSum red[kThreads / 32];
+    __shared__ __align__(16) MaxSum slot[2][16];  // level-3 partials, by row parity
+    __shared__ __align__(16) MaxSum res[2];       // leader's result, by row parity
+
+    const uint32_t C = ptx::cluster_nctarank();
+    const uint32_t rank = ptx::cluster_ctarank();
+    const uint32_t cid = ptx::cluster_id_x();
+    const uint32_t ncl = ptx::nclusters_x();
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int ng = (cols + 3) >> 2;
+    const int g0 = int(rank) * gpc;
+    const int g1 = min(ng, g0 + gpc);
+
+    // every peer CTA is running before anyone touches its shared memory
+    ptx::cluster_sync();
+
+    int it = 0;
+    for (int64_t row = cid; row < rows; row += ncl, ++it) {
+        const int par = it & 1;
+        const float *a = A + row * cols;
+        float *o = out + row * cols;
+        const float bb = __ldg(bias + row);
+
+        float e[V][4];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int g = g0 + threadIdx.x + v * kThreads;
+            if constexpr (VEC) {
+                float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (g < g1) t = __ldcs(reinterpret_cast<const float4 *>(a) + g);
+                e[v][0] = t.x;
+                e[v][1] = t.y;
+                e[v][2] = t.z;
+                e[v][3] = t.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) e[v][j] = (g < g1 && 4 * g + j < cols) ? __ldcs(a + 4 * g + j) : 0.f;
+            }
+        }
+        // thread-local aggregation: max, then sum of exp (exp kept for the output)
+        float mt = neg_inf();
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int g = g0 + threadIdx.x + v * kThreads;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                e[v][j] = cube_plus(e[v][j], bb);
+                if (g < g1 && 4 * g + j < cols) mt = fmaxf(mt, e[v][j]);
+            }
+        }
+        float st = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int g = g0 + threadIdx.x + v * kThreads;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool ok = g < g1 && 4 * g + j < cols;
+                const float x = ok ? ptx::ex2_approx((e[v][j] - mt) * kLog2e) : 0.f;
+                e[v][j] = x;
+                st += x;
+            }
+        }
+        // level 1: warp butterfly
+        MaxSum p = warp_maxsum<32>(MaxSum{mt, st});
+        // level 2: across the CTA's warps through shared memory
+        if (lane == 0) red[warp] = p;
+        __syncthreads();
+        if (warp == 0) {
+            MaxSum q = (lane < kThreads / 32) ? red[lane] : MaxSum{neg_inf(), 0.f};
+            q = warp_maxsum<kThreads / 32>(q);
+            if (lane == 0) {
+                // level 3: distributed shared memory across the cluster
+                const uint32_t my_slot = ptx::smem_u32(&slot[par][rank]);
+                if (!leader) {
+                    for (uint32_t r = 0; r < C; ++r) ptx::st_cluster_v2f32(ptx::mapa(my_slot, r), q.m, q.s);
+                } else {
+                    ptx::st_cluster_v2f32(ptx::mapa(my_slot, 0), q.m, q.s);
+                }
+            }
+        }
+        ptx::cluster_sync();
+        MaxSum tot;
+        if (!leader) {
+            tot = slot[par][0];
+            for (uint32_t r = 1; r < C; ++r) tot = combine_maxsum(tot, slot[par][r]);
+        } else {
+            if (rank == 0 && threadIdx.x == 0) {
+                MaxSum t = slot[par][0];
+                for (uint32_t r = 1; r < C; ++r) t = combine_maxsum(t, slot[par][r]);
+                const uint32_t res_addr = ptx::smem_u32(&res[par]);
+                for (uint32_t r = 0; r < C; ++r) ptx::st_cluster_v2f32(ptx::mapa(res_addr, r), t.m, t.s);
+            }
+            ptx::cluster_sync();
+            tot = res[par];
+        }
+        // broadcast back over the row: out = exp(y - mt) * exp(mt - m) / s
+        const float f = (mt == neg_inf()) ? 0.f : ptx::ex2_approx((mt - tot.m) * kLog2e) / tot.s;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int g = g0 + threadIdx.x + v * kThreads;
+            if constexpr (VEC) {
+                if (g < g1)
+                    __stcs(reinterpret_cast<float4 *>(o) + g,
+                           make_float4(e[v][0] * f, e[v][1] * f, e[v][2] * f, e[v][3] * f));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (g < g1 && 4 * g + j < cols) __stcs(o + 4 * g + j, e[v][j] * f);
+            }
+        }
+        // slot[par] / res[par] are written again two rows later, after every CTA
+        // of the cluster has passed the next row's cluster barrier
+    }
+    // no CTA leaves while a peer may still access its shared memory
+    ptx::cluster_sync();
+}
+
+template <int LPR, bool VEC>
+void *packed_fn() {
+    return reinterpret_cast<void *>(&stitch_packed_kernel<LPR, VEC>);
+}
+
+void *packed_kernel(int lpr, bool vec) {
+    switch (lpr) {
+        case 1: return vec ? packed_fn<1, true>() : packed_fn<1, false>();
+        case 2: return vec ? packed_fn<2, true>() : packed_fn<2, false>();
+        case 4: return vec ? packed_fn<4, true>() : packed_fn<4, false>();
+        case 8: return vec ? packed_fn<8, true>() : packed_fn<8, false>();
+        case 16: return vec ? packed_fn<16, true>() : packed_fn<16, false>();
+        case 32: return vec ? packed_fn<32, true>() : packed_fn<32, false>();
+        default: return nullptr;
+    }
+}
+
+template <int V, bool VEC>
+void *split_fn() {
+    return reinterpret_cast<void *>(&stitch_split_kernel<V, VEC>);
+}
+
+void *split_kernel(int v, bool vec) {
+    switch (v) {
+        case 1: return vec ? split_fn<1, true>() : split_fn<1, false>();
+        case 2: return vec ? split_fn<2, true>() : split_fn<2, false>();
+        case 4: return vec ? split_fn<4, true>() : split_fn<4, false>();
+        case 8: return vec ? split_fn<8, true>() : split_fn<8, false>();
+        case 16: return vec ? split_fn<16, true>() : split_fn<16, false>();
+        default: return nullptr;
+    }
+}
+
+}  // namespace
+
+int stitch_packed_blocks_per_sm(int lpr, bool vec) {
+    void *fn = packed_kernel(lpr, vec);
+    if (!fn) return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess) return 0;
+    return n;
+}
+
+cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias, float *out, int64_t rows,
+                          int64_t cols, uint32_t * /*err*/, cudaStream_t stream) {
+    if (p.mapping == 1) {
+        void *fn = packed_kernel(p.lpr, p.vec);
+        if (!fn) return cudaErrorInvalidValue;
+        int icols = int(cols);
+        void *args[] = {(void *)&A, (void *)&bias, (void *)&out, (void *)&rows, (void *)&icols};
+        return cudaLaunchKernel(fn, dim3(p.grid), dim3(kThreads), args, 0, stream);
+    }
+    if (p.mapping == 2) {
+        void *fn = split_kernel(p.per_thread, p.vec);
+        if (!fn) return cudaErrorInvalidValue;
+        if (p.cluster > 8) {
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+        const int ng = int((cols + 3) / 4);
+        int gpc = (ng + p.cluster - 1) / p.cluster;
+        int icols = int(cols);
+        int leader = p.leader;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(p.grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = p.cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        void *args[] = {(void *)&A, (void *)&bias, (void *)&out, (void *)&rows, (void *)&icols, (void *)&gpc,
+                        (void *)&leader};
+        return cudaLaunchKernelExC(&cfg, fn, args);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace cf

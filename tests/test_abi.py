@@ -1,0 +1,150 @@
+"""The C-ABI library loads, exports every symbol include/cf.h declares, and its
+host-only logic (status strings, planner, workspace sizing, argument checks
+that return before any CUDA call) behaves.  No compute calls: CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from memory_fusion_gb300 import cf
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from memory_fusion_gb300 import build
+    build.build()
+
+
+def header_symbols():
+    txt = open(os.path.join(ROOT, "include", "cf.h")).read()
+    return sorted(set(re.findall(r"^CF_API[^(]*?\b(cf_\w+)\(", txt, flags=re.M)))
+
+
+def test_header_declares_the_hot_path_calls():
+    syms = header_symbols()
+    for s in ("cf_gemm_fused_rownorm", "cf_gemm_fused_rowsoftmax", "cf_stitch_rowreduce_broadcast",
+              "cf_get_device_status", "cf_status_string", "cf_gemm_fused_workspace_size"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(cf.LIB_PATH)
+    missing = [s for s in header_symbols() if not hasattr(L, s)]
+    assert missing == []
+
+
+def test_binding_covers_every_declared_symbol():
+    assert sorted(cf.declared_symbols()) == header_symbols()
+
+
+def test_status_strings():
+    assert cf.status_string(cf.CF_OK) == "CF_OK"
+    assert cf.status_string(cf.CF_ERR_DEVICE_TIMEOUT) == "CF_ERR_DEVICE_TIMEOUT"
+    assert cf.status_string(1234) == "CF_ERR_UNKNOWN"
+    assert cf.cf_version() >= 100
+
+
+def test_tuning_default_is_zero():
+    t = cf.cf_tuning_default()
+    assert all(getattr(t, f) == 0 for f, _ in t._fields_)
+
+
+def _active(d):
+    a = [0] * 17
+    for k, v in d.items():
+        a[k] = v
+    return a
+
+
+GB300_LIKE = _active({1: 148, 2: 74, 4: 37, 8: 18, 16: 9})
+
+
+def test_plan_single_cluster_rows():
+    # N = 2048 -> 8 slices of 256 -> one cluster of 8, peer mode
+    st, p = cf.cf_plan_gemm_fused(4096, 2048, 128, 148, GB300_LIKE)
+    assert st == cf.CF_OK
+    assert (p.n_slice, p.ctas_per_row, p.cluster_size, p.groups, p.leader_mode) == (256, 8, 8, 1, 0)
+    assert p.row_blocks == 32 and p.clusters == 18
+    assert p.smem_bytes <= 232448 and p.stages >= 2
+
+
+def test_plan_leader_mode_above_threshold():
+    st, p = cf.cf_plan_gemm_fused(16384, 4096, 4096, 148, GB300_LIKE)
+    assert st == cf.CF_OK
+    assert (p.cluster_size, p.groups, p.leader_mode) == (16, 1, 1)
+    assert p.clusters == 9
+    st, p = cf.cf_plan_gemm_fused(16384, 4096, 4096, 148, GB300_LIKE, cf.tuning(peer_max=16))
+    assert p.leader_mode == 0
+
+
+def test_plan_wide_rows_use_global_path():
+    # N = 16384 -> 64 slices -> 4 clusters of 16 per row block
+    st, p = cf.cf_plan_gemm_fused(8192, 16384, 2048, 148, GB300_LIKE)
+    assert st == cf.CF_OK
+    assert (p.cluster_size, p.groups) == (16, 4)
+    assert p.clusters % p.groups == 0 and p.clusters <= 9
+    # cluster 8 forced: G = 8 and the grid holds a multiple of 8 resident clusters
+    st, p = cf.cf_plan_gemm_fused(8192, 16384, 2048, 148, GB300_LIKE, cf.tuning(cluster_size=8))
+    assert (p.cluster_size, p.groups, p.clusters) == (8, 8, 16)
+
+
+def test_plan_residency_refused():
+    # only 2 clusters of 16 resident but 4 must meet at the barrier
+    st, _ = cf.cf_plan_gemm_fused(8192, 16384, 2048, 148, _active({16: 2}), cf.tuning(cluster_size=16))
+    assert st == cf.CF_ERR_NOT_RESIDENT
+    st, _ = cf.cf_plan_gemm_fused(8192, 16384, 2048, 148, _active({}))
+    assert st == cf.CF_ERR_NOT_RESIDENT
+
+
+def test_plan_shapes():
+    assert cf.cf_plan_gemm_fused(128, 100, 256, 148, GB300_LIKE)[0] == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_plan_gemm_fused(128, 512, 100, 148, GB300_LIKE)[0] == cf.CF_ERR_UNSUPPORTED
+    st, p = cf.cf_plan_gemm_fused(128, 192, 64, 148, GB300_LIKE)  # 192 = 3 x 64
+    assert st == cf.CF_OK
+    assert (p.n_slice, p.ctas_per_row) == (64, 3)
+    st, p = cf.cf_plan_gemm_fused(1, 384, 64, 148, _active({3: 40}))
+    assert (p.n_slice, p.cluster_size, p.row_blocks, p.clusters) == (128, 3, 1, 1)
+    # tiny: one row block, one cluster of 2
+    st, p = cf.cf_plan_gemm_fused(128, 512, 256, 148, GB300_LIKE)
+    assert (p.cluster_size, p.clusters, p.row_blocks) == (2, 1, 1)
+
+
+def test_workspace_sizes():
+    # error word + counters + one float2 per row and 64-column group
+    assert cf.cf_gemm_fused_workspace_size(8192, 16384, 2048) == 256 + 512 + 64 * 256 * 128 * 8
+    assert cf.cf_gemm_fused_workspace_size(0, 512, 256) == 256 + 0
+    assert cf.cf_stitch_workspace_size(750000, 32) == 256
+
+
+def test_argument_errors_need_no_gpu():
+    L = cf.lib()
+    # null operands
+    assert cf.cf_gemm_fused_rownorm(None, None, None, None, None, None, 128, 512, 256, 1.0, 1e-5, 0,
+                                    None, 0, 0) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_gemm_fused_rowsoftmax(16, 16, None, 16, -1, 512, 256, 1.0, 16, 4096, 0) == cf.CF_ERR_INVALID_ARG
+    # misaligned pointer (checked before any device access)
+    assert cf.cf_gemm_fused_rowsoftmax(16 + 2, 16, None, 16, 128, 512, 256, 1.0, 16, 1 << 20, 0) == \
+        cf.CF_ERR_MISALIGNED
+    # K not a multiple of 64
+    assert cf.cf_gemm_fused_rowsoftmax(16, 16, None, 16, 128, 512, 100, 1.0, 16, 1 << 20, 0) == \
+        cf.CF_ERR_UNSUPPORTED
+    # workspace too small
+    assert cf.cf_gemm_fused_rowsoftmax(16, 16, None, 16, 128, 512, 256, 1.0, 16, 8, 0) == \
+        cf.CF_ERR_WORKSPACE_TOO_SMALL
+    # LayerNorm needs gamma and beta
+    assert cf.cf_gemm_fused_rownorm(16, 16, None, None, 16, 16, 128, 512, 256, 1.0, 1e-5, 0,
+                                    16, 1 << 20, 0) == cf.CF_ERR_INVALID_ARG
+    # bad activation enum
+    assert cf.cf_gemm_fused_rownorm(16, 16, None, 16, 16, 16, 128, 512, 256, 1.0, 1e-5, 7,
+                                    16, 1 << 20, 0) == cf.CF_ERR_INVALID_ARG
+    # M = 0 and empty stitched inputs are no-ops
+    assert cf.cf_gemm_fused_rowsoftmax(16, 16, None, 16, 0, 512, 256, 1.0, 16, 1 << 20, 0) == cf.CF_OK
+    assert cf.cf_stitch_rowreduce_broadcast(None, None, None, 0, 32, None, 0, 0) == cf.CF_OK
+    assert cf.cf_stitch_rowreduce_broadcast(None, None, None, 5, 0, None, 0, 0) == cf.CF_OK
+    assert cf.cf_stitch_rowreduce_broadcast(None, None, None, -1, 4, None, 0, 0) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_stitch_rowreduce_broadcast(16, 16, 16, 4, 300000, 16, 4096, 0) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_stitch_rowreduce_broadcast(18, 16, 16, 4, 32, 16, 4096, 0) == cf.CF_ERR_MISALIGNED
+    assert L is not None

@@ -1,0 +1,191 @@
+"""GPU parity of the fused GEMM + row-reduce/broadcast kernels (through the C
+ABI) against the fp64 oracle: LayerNorm, GELU+LayerNorm and softmax
+epilogues; ragged row tails; tile widths 64/128/256; cluster sizes 1..16;
+peer and leader-follower aggregation; the global partial-buffer path; the
+full workloads on sampled rows; determinism, invariants and the device
+timeout path (a bounded wait that runs out, reported without a fault)."""
+import numpy as np
+import pytest
+
+import oracle
+from memory_fusion_gb300 import cf, inputs
+from tests.gpu_util import check_ln, check_softmax, dev_bf16, dev_f32, host, sample_rows, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def _ln_inputs(M, N, K, seed, bias_std=0.1):
+    return inputs.gemm_inputs(M, N, K, seed, x_std=K ** -0.5, w_std=K ** -0.5,
+                              bias_std=bias_std, gamma_std=0.1, beta_std=0.1)
+
+
+def _rownorm(d, act="none", alpha=1.0, eps=1e-5, tuning=None, bias=True, ws=None):
+    torch = torch_cuda()
+    X, W = dev_bf16(d["X"]), dev_bf16(d["W"])
+    M, K = d["X"].shape
+    N = d["W"].shape[1]
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    if ws is None:
+        ws = cf.new_workspace(cf.cf_gemm_fused_workspace_size(M, N, K))
+    a = {"none": cf.CF_ACT_NONE, "gelu_tanh": cf.CF_ACT_GELU_TANH}[act]
+    st = cf.cf_gemm_fused_rownorm(X, W, dev_f32(d["bias"]) if bias else None, dev_f32(d["gamma"]),
+                                  dev_f32(d["beta"]), Y, M, N, K, alpha, eps, a, ws, ws.numel(), None, tuning)
+    assert st == cf.CF_OK, cf.status_string(st)
+    torch.cuda.synchronize()
+    dst, info = cf.cf_get_device_status(ws)
+    assert dst == cf.CF_OK, (cf.status_string(dst), hex(info))
+    return host(Y)
+
+
+def _softmax(d, scale, bias=None, tuning=None):
+    torch = torch_cuda()
+    X, W = dev_bf16(d["X"]), dev_bf16(d["W"])
+    M, K = d["X"].shape
+    N = d["W"].shape[1]
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = cf.new_workspace(cf.cf_gemm_fused_workspace_size(M, N, K))
+    st = cf.cf_gemm_fused_rowsoftmax(X, W, dev_f32(bias), Y, M, N, K, scale, ws, ws.numel(), None, tuning)
+    assert st == cf.CF_OK, cf.status_string(st)
+    torch.cuda.synchronize()
+    dst, info = cf.cf_get_device_status(ws)
+    assert dst == cf.CF_OK, (cf.status_string(dst), hex(info))
+    return host(Y)
+
+
+def _ref_ln(d, act="none", alpha=1.0, eps=1e-5, bias=True, rows=None):
+    return oracle.gemm_bias_rownorm(d["X"], d["W"], d["bias"] if bias else None, d["gamma"], d["beta"],
+                                    alpha=alpha, eps=eps, act=act, rows=rows)
+
+
+# ---------------------------------------------------------------------------
+# the tiny workload, whole
+# ---------------------------------------------------------------------------
+def test_ln_tiny_workload():
+    w = inputs.WORKLOADS["ln_tiny_128x512x256"]
+    d = inputs.workload_inputs(w.name)
+    check_ln(_rownorm(d, eps=w.eps), _ref_ln(d, eps=w.eps), w.name, strict=True)
+
+
+# ---------------------------------------------------------------------------
+# small shapes spanning several tiles, clusters and a ragged row tail
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("M,N,K,act", [
+    (300, 512, 256, "none"), (300, 512, 256, "gelu_tanh"), (129, 1024, 128, "none"),
+    (1, 256, 64, "none"), (257, 2048, 192, "gelu_tanh"), (640, 4096, 128, "gelu_tanh"),
+])
+def test_rownorm_small(M, N, K, act):
+    d = _ln_inputs(M, N, K, seed=M + N + K)
+    check_ln(_rownorm(d, act=act), _ref_ln(d, act=act), f"{M}x{N}x{K} {act}")
+
+
+@pytest.mark.parametrize("n_slice", [64, 128, 256])
+def test_rownorm_tile_widths(n_slice):
+    d = _ln_inputs(200, 1024, 128, seed=7)
+    check_ln(_rownorm(d, tuning=cf.tuning(n_slice=n_slice)), _ref_ln(d), f"n_slice={n_slice}")
+
+
+@pytest.mark.parametrize("C,leader", [(1, 0), (2, 0), (4, 0), (4, 1), (8, 0), (8, 1), (16, 0), (16, 1)])
+def test_rownorm_cluster_modes(C, leader):
+    """All CTAs of a row in one cluster of C; peer all-to-all or leader-follower."""
+    N = 256 * C
+    d = _ln_inputs(260, N, 128, seed=11 + C)
+    t = cf.tuning(cluster_size=C, peer_max=-1 if leader else 16)
+    check_ln(_rownorm(d, act="gelu_tanh", tuning=t), _ref_ln(d, act="gelu_tanh"), f"C={C} leader={leader}")
+
+
+@pytest.mark.parametrize("C,N,leader", [(2, 2048, 0), (4, 4096, 1), (1, 1024, 0), (8, 8192, 0)])
+def test_rownorm_global_path(C, N, leader):
+    """Rows wider than one cluster: G = N/(256 C) clusters meet at the in-kernel barrier."""
+    d = _ln_inputs(390, N, 128, seed=21 + C)
+    t = cf.tuning(cluster_size=C, peer_max=-1 if leader else 16)
+    check_ln(_rownorm(d, tuning=t), _ref_ln(d), f"global C={C} N={N}")
+
+
+def test_rownorm_alpha_and_no_bias():
+    d = _ln_inputs(200, 512, 128, seed=5)
+    check_ln(_rownorm(d, alpha=0.37, bias=False), _ref_ln(d, alpha=0.37, bias=False), "alpha, no bias")
+
+
+def test_layernorm_invariant_on_gpu():
+    """gamma=1, beta=0, eps=0: each output row has mean 0 and variance 1 (to bf16 rounding)."""
+    d = _ln_inputs(256, 1024, 256, seed=9)
+    d["gamma"] = np.ones(1024, np.float32)
+    d["beta"] = np.zeros(1024, np.float32)
+    y = _rownorm(d, act="gelu_tanh", eps=0.0)
+    assert np.abs(y.mean(1)).max() < 5e-3
+    assert np.abs(y.var(1) - 1).max() < 1e-2
+
+
+def test_rownorm_deterministic_and_workspace_reusable():
+    torch = torch_cuda()
+    d = _ln_inputs(300, 2048, 128, seed=3)
+    ws = cf.new_workspace(cf.cf_gemm_fused_workspace_size(300, 2048, 128))
+    t = cf.tuning(cluster_size=2)  # global path, counters reused by every call
+    ys = [_rownorm(d, tuning=t, ws=ws) for _ in range(3)]
+    assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[1], ys[2])
+    assert int(ws[256:256 + 8 * 3].sum().item()) == 0  # counters cleaned themselves
+    del torch
+
+
+# ---------------------------------------------------------------------------
+# softmax
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("M,N,K", [(300, 2048, 128), (128, 512, 64), (77, 1024, 256)])
+def test_softmax_small(M, N, K):
+    d = inputs.gemm_inputs(M, N, K, seed=M + N, x_std=1.0, w_std=K ** -0.5,
+                           bias_std=None, gamma_std=None, beta_std=None)
+    s = K ** -0.5
+    check_softmax(_softmax(d, s), oracle.gemm_rowsoftmax(d["X"], d["W"], scale=s), f"softmax {M}x{N}x{K}")
+
+
+def test_softmax_with_bias_and_modes():
+    d = inputs.gemm_inputs(200, 2048, 128, seed=4, x_std=1.0, w_std=128 ** -0.5,
+                           bias_std=0.5, gamma_std=None, beta_std=None)
+    ref = oracle.gemm_rowsoftmax(d["X"], d["W"], scale=0.1, bias=d["bias"])
+    for t in (None, cf.tuning(peer_max=-1), cf.tuning(cluster_size=2), cf.tuning(n_slice=128)):
+        check_softmax(_softmax(d, 0.1, bias=d["bias"], tuning=t), ref, f"softmax bias tuning={t}")
+
+
+# ---------------------------------------------------------------------------
+# the full workloads, sampled rows (every row is independent)
+# ---------------------------------------------------------------------------
+def test_softmax_full_workload():
+    w = inputs.WORKLOADS["softmax_4096x2048x128"]
+    d = inputs.workload_inputs(w.name)
+    y = _softmax(d, w.scale)
+    rows = sample_rows(w.M, 512)
+    check_softmax(y[rows], oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows), w.name)
+    assert np.abs(y.sum(1) - 1).max() <= 1e-2  # every row
+
+
+@pytest.mark.parametrize("name", ["gelu_ln_16384x4096x4096", "wide_ln_8192x16384x2048"])
+def test_rownorm_full_workload(name):
+    w = inputs.WORKLOADS[name]
+    d = inputs.workload_inputs(name)
+    y = _rownorm(d, act=w.act, eps=w.eps)
+    rows = sample_rows(w.M, 512)
+    check_ln(y[rows], _ref_ln(d, act=w.act, eps=w.eps, rows=rows), name, strict=True)
+
+
+# ---------------------------------------------------------------------------
+# device-side failure reporting without a fault
+# ---------------------------------------------------------------------------
+def test_global_barrier_timeout_is_reported():
+    """One more arrival than can happen: the bounded wait runs out, the kernel
+    records CF_ERR_DEVICE_TIMEOUT with the row block, and finishes."""
+    torch = torch_cuda()
+    d = _ln_inputs(256, 1024, 64, seed=2)
+    M, K, N = 256, 64, 1024
+    ws = cf.new_workspace(cf.cf_gemm_fused_workspace_size(M, N, K))
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    t = cf.tuning(cluster_size=2, extra_arrivals=1, timeout_us=20000)
+    st = cf.cf_gemm_fused_rownorm(dev_bf16(d["X"]), dev_bf16(d["W"]), dev_f32(d["bias"]), dev_f32(d["gamma"]),
+                                  dev_f32(d["beta"]), Y, M, N, K, 1.0, 1e-5, 0, ws, ws.numel(), None, t)
+    assert st == cf.CF_OK
+    dst, info = cf.cf_get_device_status(ws)
+    assert dst == cf.CF_ERR_DEVICE_TIMEOUT
+    assert (info >> 28) == 5 and (info & 0xFFFF) in (0, 1)  # global wait of row block 0 or 1
+    # the context is still usable and the error word was cleared by the read
+    assert cf.cf_get_device_status(ws)[0] == cf.CF_OK
+    cf.check(cf.cf_workspace_init(ws, ws.numel()))
+    check_ln(_rownorm(d, tuning=cf.tuning(cluster_size=2), ws=ws), _ref_ln(d), "after timeout")
