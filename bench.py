@@ -1,0 +1,524 @@
+"""Benchmark of the fused GEMM + row-reduce/broadcast path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--quick]
+
+One step = one call of the fused kernel over one batch of the workload
+(default: GEMM + row softmax, X[4096,128] . W[128,2048], the workload the
+headline metric is quoted on).  Inputs are resident in HBM when the timed
+region starts; between steps the input/output buffer set rotates so the
+footprint of consecutive steps exceeds L2 three times over.  The K timed
+steps are replayed from CUDA graphs and timed with CUDA events on the
+launching stream, bracketed by a barrier and synchronize on both sides; the
+max over ranks is reported.  Under torchrun every rank runs its own batch on
+its own GPU (weak scaling; no collective on the data path).
+
+The JSON line also carries: roofline (dominant kernel vs the measured HBM
+or tensor peak), e2e (the same metric through the public C-ABI call with
+host buffers, H2D/D2H copies inside the timed region), the CPU oracle timed
+on a bounded sample (cpu_baseline), SM clocks sampled during the timed
+region, and each page workload's fused-kernel numbers (per_workload).
+
+``--impl reference`` times the fp64 CPU oracle instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from memory_fusion_gb300 import inputs  # noqa: E402
+
+HEADLINE = "softmax_4096x2048x128"
+METRIC = "fused GEMM+row-reduce TFLOP/s and HBM GB/s at 1 GB300; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def kind_of(w):
+    if w.kind == "softmax":
+        return 2
+    return 1 if w.act == "gelu_tanh" else 0
+
+
+def roofline_time_s(w, peaks):
+    t_flop = w.flops / (peaks["bf16_tflops"] * 1e12)
+    t_byte = w.unavoidable_bytes / (peaks["hbm_gbs"] * 1e9)
+    return max(t_flop, t_byte), ("tensor" if t_flop >= t_byte else "hbm")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(os.path.join(ROOT, "memory_fusion_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "memory_fusion_gb300", "csrc", f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, kernel):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload, {}).get(kernel)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            n += 1
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+class FusedRunner:
+    """Device buffers of one workload, rotating over `nsets` sets, and one
+    launcher per set that calls the C ABI on the current stream."""
+
+    def __init__(self, torch, cf, w, nsets, seed_offset=0, device="cuda"):
+        self.torch, self.cf, self.w = torch, cf, w
+        d = (inputs.workload_inputs(w.name) if seed_offset == 0 else
+             _seeded_inputs(w, seed_offset))
+        self.host = d
+        bf = torch.bfloat16
+        X = torch.from_numpy(d["X"]).to(device, bf)
+        W = torch.from_numpy(d["W"]).to(device, bf)
+        self.sets = []
+        for i in range(nsets):
+            s = {"X": X if i == 0 else X.clone(), "W": W if i == 0 else W.clone(),
+                 "Y": torch.empty((w.M, w.N), dtype=bf, device=device)}
+            if w.kind == "rownorm":
+                for k in ("bias", "gamma", "beta"):
+                    s[k] = torch.from_numpy(d[k]).to(device)
+            self.sets.append(s)
+        self.ws_bytes = cf.cf_gemm_fused_workspace_size(w.M, w.N, w.K)
+        self.ws = cf.new_workspace(self.ws_bytes, device)
+
+    def launch(self, i, stream=None):
+        cf, w = self.cf, self.w
+        s = self.sets[i % len(self.sets)]
+        if w.kind == "softmax":
+            st = cf.cf_gemm_fused_rowsoftmax(s["X"], s["W"], None, s["Y"], w.M, w.N, w.K, w.scale,
+                                             self.ws, self.ws_bytes, stream)
+        else:
+            act = cf.CF_ACT_GELU_TANH if w.act == "gelu_tanh" else cf.CF_ACT_NONE
+            st = cf.cf_gemm_fused_rownorm(s["X"], s["W"], s["bias"], s["gamma"], s["beta"], s["Y"],
+                                          w.M, w.N, w.K, w.alpha, w.eps, act, self.ws, self.ws_bytes, stream)
+        cf.check(st, "fused launch")
+
+
+def _seeded_inputs(w, off):
+    if w.kind == "rownorm":
+        return inputs.gemm_inputs(w.M, w.N, w.K, w.seed + 1000 * off, x_std=w.x_std, w_std=w.w_std,
+                                  bias_std=w.bias_std, gamma_std=w.gamma_std, beta_std=w.beta_std)
+    return inputs.gemm_inputs(w.M, w.N, w.K, w.seed + 1000 * off, x_std=w.x_std, w_std=w.w_std,
+                              bias_std=None, gamma_std=None, beta_std=None)
+
+
+def bytes_per_set(w):
+    return 2 * w.M * w.K + 2 * w.K * w.N + 2 * w.M * w.N
+
+
+def capture_graph(torch, runner, start, count):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(count):
+                runner.launch(start + i)
+    torch.cuda.current_stream().wait_stream(s)
+    return g
+
+
+def time_steps(torch, runner, steps, warmup, barrier, sampler=None, graph_len=500):
+    """Warm up, then time exactly `steps` launches replayed from CUDA graphs.
+    Returns (seconds, launches)."""
+    for i in range(warmup):
+        runner.launch(i)
+    torch.cuda.synchronize()
+    R = max(1, min(steps, graph_len))
+    reps, rem = divmod(steps, R)
+    g = capture_graph(torch, runner, 0, R)
+    g_rem = capture_graph(torch, runner, R, rem) if rem else None
+    g.replay()  # upload + one untimed pass
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    return e0.elapsed_time(e1) / 1e3, reps * R + rem, clocks
+
+
+def time_e2e(torch, cf, w, steps, device):
+    """The public call with host buffers: per step, H2D of X and W from pinned
+    memory, the fused call, D2H of Y into pinned memory; CUDA events around."""
+    d = inputs.workload_inputs(w.name)
+    bf = torch.bfloat16
+    hX = torch.from_numpy(d["X"]).to(bf).pin_memory()
+    hW = torch.from_numpy(d["W"]).to(bf).pin_memory()
+    hY = torch.empty((w.M, w.N), dtype=bf).pin_memory()
+    X = torch.empty_like(hX, device=device)
+    W = torch.empty_like(hW, device=device)
+    Y = torch.empty((w.M, w.N), dtype=bf, device=device)
+    extra = {}
+    if w.kind == "rownorm":
+        for k in ("bias", "gamma", "beta"):
+            extra[k] = torch.from_numpy(d[k]).pin_memory()
+            extra["d_" + k] = torch.empty_like(extra[k], device=device)
+    wsb = cf.cf_gemm_fused_workspace_size(w.M, w.N, w.K)
+    ws = cf.new_workspace(wsb, device)
+
+    def step():
+        X.copy_(hX, non_blocking=True)
+        W.copy_(hW, non_blocking=True)
+        if w.kind == "softmax":
+            cf.check(cf.cf_gemm_fused_rowsoftmax(X, W, None, Y, w.M, w.N, w.K, w.scale, ws, wsb))
+        else:
+            for k in ("bias", "gamma", "beta"):
+                extra["d_" + k].copy_(extra[k], non_blocking=True)
+            act = cf.CF_ACT_GELU_TANH if w.act == "gelu_tanh" else cf.CF_ACT_NONE
+            cf.check(cf.cf_gemm_fused_rownorm(X, W, extra["d_bias"], extra["d_gamma"], extra["d_beta"], Y,
+                                              w.M, w.N, w.K, w.alpha, w.eps, act, ws, wsb))
+        hY.copy_(Y, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    h2d = hX.numel() * 2 + hW.numel() * 2 + (3 * 4 * w.N if w.kind == "rownorm" else 0)
+    d2h = hY.numel() * 2
+    return t, h2d, d2h
+
+
+def per_workload(torch, cf, peaks, device, names):
+    """Each page workload's fused kernel, timed alone (graph of launches,
+    rotating buffers where one set is smaller than 3x L2)."""
+    out = {}
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    for name in names:
+        w = inputs.WORKLOADS[name]
+        if isinstance(w, inputs.StitchWorkload):
+            out[name] = stitch_numbers(torch, cf, w, peaks, device, l2)
+            continue
+        nsets = max(1, min(32, math.ceil(3 * l2 / bytes_per_set(w))))
+        r = FusedRunner(torch, cf, w, nsets, device=device)
+        reps = max(nsets, 20 if w.flops > 1e11 else 400)
+        t, n, _ = time_steps(torch, r, reps, 3, lambda: None, graph_len=reps)
+        t1 = t / n
+        troof, bound = roofline_time_s(w, peaks)
+        _, plan, _ = cf.cf_query_gemm_fused_plan(w.M, w.N, w.K, kind_of(w))
+        out[name] = {"us": round(t1 * 1e6, 2), "tflops": round(w.flops / t1 / 1e12, 1),
+                     "gbs": round(w.unavoidable_bytes / t1 / 1e9, 1), "bound": bound,
+                     "roofline_frac": round(troof / t1, 3), "buffer_sets": nsets,
+                     "plan": plan.as_dict()}
+        del r
+        torch.cuda.empty_cache()
+    return out
+
+
+def stitch_numbers(torch, cf, w, peaks, device, l2):
+    d = inputs.workload_inputs(w.name)
+    nsets = max(1, min(32, math.ceil(3 * l2 / w.unavoidable_bytes)))
+    A = [torch.from_numpy(d["A"]).to(device) for _ in range(nsets)]
+    b = torch.from_numpy(d["row_bias"]).to(device)
+    O = [torch.empty_like(A[0]) for _ in range(nsets)]
+    wsb = cf.cf_stitch_workspace_size(w.rows, w.cols)
+    ws = cf.new_workspace(wsb, device)
+
+    class R:
+        def launch(self, i, stream=None):
+            cf.check(cf.cf_stitch_rowreduce_broadcast(A[i % nsets], b, O[i % nsets], w.rows, w.cols,
+                                                      ws, wsb, stream))
+
+    reps = max(nsets, 200)
+    t, n, _ = time_steps(torch, R(), reps, 3, lambda: None, graph_len=reps)
+    t1 = t / n
+    gbs = w.unavoidable_bytes / t1 / 1e9
+    return {"us": round(t1 * 1e6, 2), "gbs": round(gbs, 1), "bound": "hbm",
+            "roofline_frac": round(gbs / peaks["hbm_gbs"], 3), "buffer_sets": nsets}
+
+
+def cpu_oracle_sample(w, budget_s=10.0, max_rows=None):
+    """The fp64 oracle as it stands, on whole-row samples of the workload,
+    repeated until ~budget_s of CPU time; returns (flops/s, seconds, rows)."""
+    import oracle
+    d = inputs.workload_inputs(w.name)
+    rows_per = min(w.M, max_rows or w.M)
+    rng = np.random.Generator(np.random.PCG64(0))
+    done_rows, t_total = 0, 0.0
+    while t_total < budget_s:
+        rows = np.sort(rng.choice(w.M, size=rows_per, replace=False))
+        t0 = time.perf_counter()
+        if w.kind == "softmax":
+            oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows)
+        else:
+            oracle.gemm_bias_rownorm(d["X"], d["W"], d["bias"], d["gamma"], d["beta"], alpha=w.alpha,
+                                     eps=w.eps, act=w.act, rows=rows)
+        t_total += time.perf_counter() - t0
+        done_rows += rows_per
+    flops = 2.0 * done_rows * w.N * w.K
+    return flops / t_total, t_total, done_rows
+
+
+def blas_threads():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return len(os.sched_getaffinity(0))
+
+
+def run_ours(args):
+    import torch
+    from memory_fusion_gb300 import cf
+
+    ws_, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        barrier = lambda: dist.barrier()  # noqa: E731
+    else:
+        barrier = lambda: None  # noqa: E731
+    peaks, peak_src = load_peaks()
+    w = inputs.WORKLOADS[args.workload]
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    nsets = max(1, min(64, math.ceil(3 * l2 / bytes_per_set(w))))
+    runner = FusedRunner(torch, cf, w, nsets, seed_offset=rank, device=device)
+    props = torch.cuda.get_device_properties(device)
+    gpu_id = str(getattr(props, "uuid", local))
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id if gpu_id.startswith("GPU-") else str(local))
+    t, n, clocks = time_steps(torch, runner, args.steps, args.warmup, barrier, sampler)
+    if ws_ > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t], device=device, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    t1 = t / n
+    total_flops = w.flops * n * ws_
+    value = total_flops / t / 1e12
+    troof, bound = roofline_time_s(w, peaks)
+    kernel = {2: "gemm_fused_kernel<SOFTMAX>", 1: "gemm_fused_kernel<GELU_LN>", 0: "gemm_fused_kernel<LN>"}[kind_of(w)]
+    if bound == "hbm":
+        achieved = w.unavoidable_bytes / t1 / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = w.flops / t1 / 1e12
+        pk = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk, "unit": "TFLOP/s",
+                "frac": round(achieved / pk, 4)}
+    traffic = profiled_traffic(w.name, kernel)
+    roof["traffic"] = traffic
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roof["kernel"] = kernel
+    roof["algorithmic_bytes_per_launch"] = w.unavoidable_bytes
+    roof["flops_per_launch"] = w.flops
+
+    _, plan, active = cf.cf_query_gemm_fused_plan(w.M, w.N, w.K, kind_of(w))
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t1 * 1e3, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "dtype_detail": "bf16 operands, fp32 accumulate (TMEM) and fp32 epilogue, bf16 output",
+        "data": "synthetic (seeded, shaped like the page workload)",
+        "config": {"workload": w.name, "description": w.description, "M": w.M, "N": w.N, "K": w.K,
+                   "batch_per_gpu": 1, "parallelism": f"replicas x{ws_} (rows independent)",
+                   "l2": f"{nsets} rotating input/output sets (>= 3x L2 of {l2 >> 20} MiB)",
+                   "plan": plan.as_dict()},
+        "hbm_gbs": round(w.unavoidable_bytes * n * ws_ / t / 1e9, 1),
+        "roofline_frac": round(troof / t1, 4),
+        "roofline": roof,
+        "gpu_launches": n,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        te, h2d, d2h = time_e2e(torch, cf, w, max(10, min(args.steps, 200)), device)
+        line["e2e"] = {"value": round(w.flops * ws_ / te / 1e12, 3), "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(te * 1e3, 4)}
+        if not args.quick:
+            names = [k for k in inputs.WORKLOADS]
+            line["per_workload"] = per_workload(torch, cf, peaks, device, names)
+        if not args.no_cpu:
+            v, secs, rows = cpu_oracle_sample(w, budget_s=args.cpu_budget)
+            line["cpu_baseline"] = {"value": round(v / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(),
+                                    "kind": "oracle",
+                                    "sample": f"{rows} whole rows of {w.name} (fp64 numpy oracle, "
+                                              f"{secs:.1f} s; BLAS threads = cores, elementwise single-thread)"}
+        print(json.dumps(line), flush=True)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[args.workload]
+    import oracle
+    d = inputs.workload_inputs(w.name)
+    rows_per_step = 128
+    rng = np.random.Generator(np.random.PCG64(1))
+
+    def step():
+        rows = np.sort(rng.choice(w.M, size=rows_per_step, replace=False))
+        if w.kind == "softmax":
+            oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows)
+        else:
+            oracle.gemm_bias_rownorm(d["X"], d["W"], d["bias"], d["gamma"], d["beta"], alpha=w.alpha,
+                                     eps=w.eps, act=w.act, rows=rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * w.N * w.K * args.steps
+    v = flops / t / 1e12
+    sample = f"{rows_per_step} random whole rows of {w.name} per step (fp64 numpy oracle)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": ws_,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(k for k, v in inputs.WORKLOADS.items()
+                                                                   if isinstance(v, inputs.GemmWorkload)))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
