@@ -583,12 +583,15 @@ int gemm_fused_smem_bytes(int stages, int cluster, int n_slice) {
     return int(smem_layout(stages, cluster, n_slice).total) + 1024;  // + alignment slack
 }
 
+static cudaError_t ensure_attributes(int kind, void *fn, int smem);
+
 int gemm_fused_max_active_clusters(int kind, int cluster, int smem) {
     void *fn = kernel_for(kind);
     if (!fn) return 0;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
-    if (cluster > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    if (ensure_attributes(kind, fn, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
         return 0;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cluster * 64);
     cfg.blockDim = dim3(kThreads);
@@ -608,16 +611,35 @@ int gemm_fused_max_active_clusters(int kind, int cluster, int smem) {
     return n;
 }
 
+// Function attributes are set once per (device, kernel) to the largest
+// shared-memory size seen, so launches made under stream capture issue no
+// attribute calls.
+static cudaError_t ensure_attributes(int kind, void *fn, int smem) {
+    static int set_smem[64][3] = {};
+    static bool nonportable[64][3] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (smem > set_smem[dev][kind]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        set_smem[dev][kind] = smem;
+    }
+    if (!nonportable[dev][kind]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        nonportable[dev][kind] = true;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_gemm_fused(int kind, const GemmArgs &a, int clusters, int stages, int smem,
                               cudaStream_t stream) {
     void *fn = kernel_for(kind);
     if (!fn) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = ensure_attributes(kind, fn, smem);
     if (e != cudaSuccess) return e;
-    if (a.cluster > 8) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(clusters * a.cluster);
     cfg.blockDim = dim3(kThreads);

@@ -264,11 +264,24 @@ void *split_kernel(int v, bool vec) {
 }  // namespace
 
 int stitch_packed_blocks_per_sm(int lpr, bool vec) {
+    // cached per (device, variant): no occupancy query under stream capture
+    static int cache[64][6][2] = {};
     void *fn = packed_kernel(lpr, vec);
     if (!fn) return 0;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess) return 0;
-    return n;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int li = 0;
+    while ((1 << li) < lpr) ++li;
+    int &c = cache[dev][li][vec ? 1 : 0];
+    if (c == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        c = n;
+    }
+    return c;
 }
 
 cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias, float *out, int64_t rows,
@@ -284,8 +297,18 @@ cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias
         void *fn = split_kernel(p.per_thread, p.vec);
         if (!fn) return cudaErrorInvalidValue;
         if (p.cluster > 8) {
-            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            static bool done[64][5][2] = {};
+            int dev = 0;
+            cudaError_t e = cudaGetDevice(&dev);
             if (e != cudaSuccess) return e;
+            int vi = 0;
+            while ((1 << vi) < p.per_thread) ++vi;
+            if (dev < 0 || dev >= 64 || vi > 4) return cudaErrorInvalidValue;
+            if (!done[dev][vi][p.vec ? 1 : 0]) {
+                e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return e;
+                done[dev][vi][p.vec ? 1 : 0] = true;
+            }
         }
         const int ng = int((cols + 3) / 4);
         int gpc = (ng + p.cluster - 1) / p.cluster;
