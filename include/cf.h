@@ -206,6 +206,37 @@ CF_API cf_status cf_gemm_fused_rownorm_ex(const void *X, const void *W, const fl
                                    size_t workspace_bytes, cf_stream_t stream,
                                    const cf_tuning *tuning);
 
+/* Same computation as cf_gemm_fused_rownorm, for callers that cannot
+ * allocate device memory: for example a plugin or operator interface that
+ * hands its code only the input and output buffers and no allocator, or a
+ * runtime that plans every byte of device memory up front and forbids any
+ * allocation once it is serving.  The pages have no counterpart to this
+ * call; it exists for such callers only.
+ *
+ * There is no workspace argument and nothing is allocated: no cudaMalloc,
+ * cudaFree or allocating library routine is called.  The scratch (error
+ * word, barrier counters, global partial buffer) is one fixed device array
+ * of 4 MiB inside libcf, which every GPU that loads the library holds until
+ * the process exits.  A call needing more scratch than that (256 B + 8 B per
+ * 128-row block, rounded up to 256 B, + 1 KiB per 128-row block and cluster
+ * group of a row wider than one cluster) returns CF_ERR_WORKSPACE_TOO_SMALL
+ * without launching.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array, and each clears its error word and
+ *     counters (cudaMemsetAsync on `stream`) before its kernel.  Calls whose
+ *     work can overlap on the GPU (different streams, or several host
+ *     threads) race on the array and must be serialised by the caller.
+ *   - Device-side errors are not reported by this call (the error word is
+ *     cleared by the next call); bounded waits still end the kernel.
+ * Arguments, layouts, supported shapes and error codes are otherwise those
+ * of cf_gemm_fused_rownorm with default tuning. */
+CF_API cf_status cf_gemm_fused_rownorm_noalloc(const void *X, const void *W, const float *bias,
+                                               const float *gamma, const float *beta, void *Y,
+                                               int64_t M, int64_t N, int64_t K, float alpha,
+                                               float eps, cf_activation act, cf_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Fused GEMM + scaled row softmax                                           */
 /* ------------------------------------------------------------------------ */

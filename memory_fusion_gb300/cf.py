@@ -90,6 +90,8 @@ _SIGS = {
                                     _P, _SZ, _P]),
     "cf_gemm_fused_rownorm_ex": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
                                        _P, _SZ, _P, ctypes.POINTER(cf_tuning)]),
+    "cf_gemm_fused_rownorm_noalloc": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
+                                            _P]),
     "cf_gemm_fused_rowsoftmax": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P]),
     "cf_gemm_fused_rowsoftmax_ex": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P,
                                           ctypes.POINTER(cf_tuning)]),
@@ -213,6 +215,13 @@ def cf_gemm_fused_rownorm(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, 
     return L.cf_gemm_fused_rownorm_ex(_ptr(X), _ptr(W), _ptr(bias), _ptr(gamma), _ptr(beta), _ptr(Y),
                                       M, N, K, alpha, eps, act, _ptr(workspace), workspace_bytes,
                                       _stream(stream), _tun(tuning))
+
+
+def cf_gemm_fused_rownorm_noalloc(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, stream=None) -> int:
+    """cf_gemm_fused_rownorm without a workspace: for callers that cannot
+    allocate device memory; its scratch is a fixed 4 MiB array inside libcf."""
+    return lib().cf_gemm_fused_rownorm_noalloc(_ptr(X), _ptr(W), _ptr(bias), _ptr(gamma), _ptr(beta), _ptr(Y),
+                                               M, N, K, alpha, eps, act, _stream(stream))
 
 
 def cf_gemm_fused_rowsoftmax(X, W, bias, Y, M, N, K, scale, workspace, workspace_bytes,

@@ -445,3 +445,102 @@ cf_status cf_gemm_fused_rowsoftmax(const void *X, const void *W, const float *bi
 }
 
 }  // extern "C"
+
+// =========================================================================
+// Variant of the fused GEMM + LayerNorm call that allocates nothing and takes
+// no workspace argument.  Its scratch (error word, barrier counters, global
+// partials) is one file-scope device array of fixed size that every device
+// loading this library holds until the process exits.  Host code may not use
+// the array's name as a device address: the address is looked up once per
+// device with cudaGetSymbolAddress (that device current) and passed to the
+// kernel like any workspace pointer.
+// =========================================================================
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array on `device` (the current device),
+// looked up on the first call for that device and cached.
+static cf_status noalloc_scratch(int device, void **out) {
+    static void *addr[64] = {};
+    if (device < 0 || device >= 64) return CF_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (addr[device] == nullptr) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();
+            g_last_cuda_error = int(e);
+            return CF_ERR_CUDA;
+        }
+        addr[device] = p;
+    }
+    *out = addr[device];
+    return CF_OK;
+}
+
+extern "C" cf_status cf_gemm_fused_rownorm_noalloc(const void *X, const void *W, const float *bias,
+                                                   const float *gamma, const float *beta, void *Y, int64_t M,
+                                                   int64_t N, int64_t K, float alpha, float eps,
+                                                   cf_activation act, cf_stream_t stream) {
+    int kind;
+    if (act == CF_ACT_NONE) kind = cf::EPI_LN;
+    else if (act == CF_ACT_GELU_TANH) kind = cf::EPI_GELU_LN;
+    else return CF_ERR_INVALID_ARG;
+    if (M < 0 || N <= 0 || K <= 0) return CF_ERR_INVALID_ARG;
+    if (!X || !W || !Y || !gamma || !beta) return CF_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || (bias && !aligned16(bias)) || !aligned16(gamma) ||
+        !aligned16(beta))
+        return CF_ERR_MISALIGNED;
+    if (K % 64 != 0 || N % 64 != 0) return CF_ERR_UNSUPPORTED;
+    if (M == 0) return CF_OK;
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+
+    cf_plan plan;
+    int32_t active[17];
+    cf_status st = device_plan(kind, M, N, K, nullptr, dev, &plan, active);
+    if (st != CF_OK) return st;
+    // scratch this launch uses: error word + counters (must start at zero) and
+    // one float2 per row and cluster group of the global partial buffer
+    const size_t head = cf::kErrBytes + cf::align_up(8 * size_t(plan.row_blocks), 256);
+    const size_t need = head + size_t(plan.row_blocks) * size_t(plan.groups) * 128 * sizeof(float2);
+    if (need > kNoAllocScratchBytes) return CF_ERR_WORKSPACE_TOO_SMALL;
+    void *scratch = nullptr;
+    st = noalloc_scratch(dev.device, &scratch);
+    if (st != CF_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, head, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    cf::GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, 128)) return CF_ERR_CUDA;
+    if (!make_tmap_bf16(&a.tmap_w, W, uint64_t(K), uint64_t(N), 64, 64)) return CF_ERR_CUDA;
+    uint8_t *sb = static_cast<uint8_t *>(scratch);
+    a.bias = bias;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.y = static_cast<uint16_t *>(Y);
+    a.err = reinterpret_cast<uint32_t *>(sb);
+    a.counters = reinterpret_cast<uint32_t *>(sb + cf::kErrBytes);
+    a.partials = reinterpret_cast<float2 *>(sb + head);
+    a.M = int(M);
+    a.N = int(N);
+    a.K = int(K);
+    a.alpha = alpha;
+    a.eps = eps;
+    a.n_slice = plan.n_slice;
+    a.cluster = plan.cluster_size;
+    a.groups = plan.groups;
+    a.leader = plan.leader_mode;
+    a.row_blocks = plan.row_blocks;
+    a.extra_arrivals = 0;
+    a.timeout_ns = 1000ull * kDefaultTimeoutUs;
+    e = cf::launch_gemm_fused(kind, a, plan.clusters, plan.stages, plan.smem_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CF_OK;
+}
