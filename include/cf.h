@@ -105,7 +105,34 @@ typedef struct cf_tuning {
                                barrier waits for; > 0 makes that wait run out
                                (CF_ERR_DEVICE_TIMEOUT) without faulting.  0 in
                                normal use.                                        */
+    uint64_t *trace;        /* TRACING (fused GEMM): device buffer of
+                               grid_ctas * CF_TRACE_SLOTS u64 %globaltimer stamps
+                               (ns), or NULL for none.  Per CTA: slots 0..3 =
+                               kernel start, set-up done, role loops done, exit;
+                               then CF_TRACE_EVENTS slots for each of the CTA's
+                               first CF_TRACE_TILES tiles (see cf_trace_event).
+                               Slots not reached stay as the caller left them.   */
 } cf_tuning;
+
+#define CF_TRACE_TILES 16
+#define CF_TRACE_EVENTS 12
+#define CF_TRACE_SLOTS (4 + CF_TRACE_TILES * CF_TRACE_EVENTS)
+
+/* Per-tile trace events (slot 4 + tile * CF_TRACE_EVENTS + event). */
+typedef enum {
+    CF_TR_TMA_FIRST = 0,     /* producer issued the tile's first TMA load      */
+    CF_TR_TMA_LAST = 1,      /* producer issued the tile's last TMA load       */
+    CF_TR_MMA_ACC_FREE = 2,  /* MMA warp: accumulator buffer free             */
+    CF_TR_MMA_FIRST = 3,     /* MMA warp: first operand stage ready            */
+    CF_TR_MMA_DONE = 4,      /* MMA warp: last MMA of the tile issued          */
+    CF_TR_MMA_WAIT_NS = 5,   /* duration: MMA warp's time waiting for operands */
+    CF_TR_EPI_START = 6,     /* epilogue: accumulator ready                    */
+    CF_TR_EPI_STATS = 7,     /* epilogue: thread-local statistics done         */
+    CF_TR_EPI_CTA = 8,       /* epilogue: CTA statistic done (level 2)         */
+    CF_TR_EPI_CLUSTER = 9,   /* epilogue: cluster statistic done (level 3)     */
+    CF_TR_EPI_GLOBAL = 10,   /* epilogue: row statistic done (global path)     */
+    CF_TR_EPI_STORED = 11    /* epilogue: output stores issued                 */
+} cf_trace_event;
 
 /* Fill *t with the defaults (all zero). */
 CF_API void cf_tuning_default(cf_tuning *t);

@@ -39,7 +39,15 @@ class cf_tuning(ctypes.Structure):
         ("stitch_mapping", ctypes.c_int32),
         ("timeout_us", ctypes.c_uint32),
         ("extra_arrivals", ctypes.c_int32),
+        ("trace", ctypes.c_void_p),
     ]
+
+
+CF_TRACE_TILES = 16
+CF_TRACE_EVENTS = 12
+CF_TRACE_SLOTS = 4 + CF_TRACE_TILES * CF_TRACE_EVENTS
+TRACE_EVENT_NAMES = ["tma_first", "tma_last", "mma_acc_free", "mma_first", "mma_done", "mma_wait_ns",
+                     "epi_start", "epi_stats", "epi_cta", "epi_cluster", "epi_global", "epi_stored"]
 
 
 class cf_plan(ctypes.Structure):
@@ -256,7 +264,7 @@ def check(status: int, what: str = "libcf"):
 def tuning(**kw) -> cf_tuning:
     t = cf_tuning_default()
     for k, v in kw.items():
-        setattr(t, k, v)
+        setattr(t, k, v.data_ptr() if k == "trace" and hasattr(v, "data_ptr") else v)
     return t
 
 

@@ -57,10 +57,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box (box_cols x box_rows),
-// 128-byte swizzle; out-of-range elements read as zero.
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box (box_cols x box_rows);
+// out-of-range elements read as zero and are not written.
 bool make_tmap_bf16(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
-                    uint32_t box_rows) {
+                    uint32_t box_rows, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {cols, rows};
@@ -68,7 +68,7 @@ bool make_tmap_bf16(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t col
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -175,34 +175,49 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
     const int64_t cpr64 = N / ns;
     if (cpr64 > 16 * 64) return CF_ERR_UNSUPPORTED;
     const int cpr = int(cpr64);
-    int C = 0;
+    const int rb = int((M + cf::kBlockM - 1) / cf::kBlockM);
+    // Choose the cluster size C (a divisor of the CTAs per row) that keeps the
+    // most SM-time on useful tiles.  The persistent grid holds ncl clusters
+    // (never more than can be resident); each takes ceil(T / ncl) tickets of
+    // T = row_blocks * G, so the useful fraction of SM-time is
+    //     row_blocks * cpr / (ceil(T / ncl) * sm_count).
+    // Rows wider than one cluster (G > 1) meet at the in-kernel barrier: every
+    // one of a row block's G clusters must be resident (ncl >= G), and the
+    // barrier costs a little (more when a short K loop cannot hide it).
+    auto score = [&](int c, int *ncl_out) -> double {
+        if (c < 1 || c > 16 || cpr % c != 0 || max_active_clusters[c] <= 0) return -1.0;
+        const int g = cpr / c;
+        int n = max_active_clusters[c];
+        if (t.max_clusters > 0) n = std::min(n, int(t.max_clusters));
+        if (g > 1 && n < g) return -1.0;
+        const int64_t T = int64_t(rb) * g;
+        if (T < n) n = int(T);
+        const int64_t per = (T + n - 1) / n;
+        double eff = double(rb) * cpr / (double(per) * sm_count);
+        if (g > 1) eff *= (K / 64 >= 8) ? 0.97 : 0.85;
+        *ncl_out = n;
+        return eff;
+    };
+    int C = 0, ncl = 0;
     if (t.cluster_size > 0) {
         if (t.cluster_size > 16 || cpr % t.cluster_size != 0) return CF_ERR_UNSUPPORTED;
         if (max_active_clusters[t.cluster_size] <= 0) return CF_ERR_NOT_RESIDENT;
+        if (score(t.cluster_size, &ncl) < 0) return CF_ERR_NOT_RESIDENT;
         C = t.cluster_size;
-    } else if (cpr <= 16 && max_active_clusters[cpr] > 0) {
-        C = cpr;  // one cluster holds the whole row: pure DSMEM path
     } else {
-        for (int c = std::min(16, cpr); c >= 1; --c)
-            if (cpr % c == 0 && max_active_clusters[c] > 0) {
+        double best = -1.0;
+        for (int c = std::min(16, cpr); c >= 1; --c) {  // larger clusters win ties
+            int n = 0;
+            const double e = score(c, &n);
+            if (e > best + 1e-9) {
+                best = e;
                 C = c;
-                break;
+                ncl = n;
             }
+        }
         if (C == 0) return CF_ERR_NOT_RESIDENT;
     }
     const int G = cpr / C;
-    const int rb = int((M + cf::kBlockM - 1) / cf::kBlockM);
-    const int64_t tickets = int64_t(rb) * G;
-    int ncl = max_active_clusters[C];
-    if (t.max_clusters > 0) ncl = std::min(ncl, int(t.max_clusters));
-    if (G > 1) {
-        // every cluster that meets at a row block's barrier must be resident:
-        // the persistent grid never exceeds the resident cluster count, and
-        // holds a multiple of G clusters so each keeps one column group
-        ncl = (ncl / G) * G;
-        if (ncl < G) return CF_ERR_NOT_RESIDENT;
-    }
-    if (tickets < ncl) ncl = int(std::max<int64_t>(tickets, G > 1 ? G : 1));
     const int peer_max = t.peer_max == 0 ? 8 : t.peer_max;
     plan->n_slice = ns;
     plan->ctas_per_row = cpr;
@@ -388,6 +403,7 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
     std::memset(&a, 0, sizeof(a));
     if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, 128)) return CF_ERR_CUDA;
     if (!make_tmap_bf16(&a.tmap_w, W, uint64_t(K), uint64_t(N), 64, 64)) return CF_ERR_CUDA;
+    if (!make_tmap_bf16(&a.tmap_y, Y, uint64_t(M), uint64_t(N), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return CF_ERR_CUDA;
     a.bias = bias;
     a.gamma = gamma;
     a.beta = beta;
@@ -408,6 +424,7 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
     a.row_blocks = plan.row_blocks;
     a.extra_arrivals = t.extra_arrivals;
     a.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
+    a.trace = reinterpret_cast<unsigned long long *>(t.trace);
     cudaError_t e = cf::launch_gemm_fused(kind, a, plan.clusters, plan.stages, plan.smem_bytes,
                                           reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
@@ -520,6 +537,7 @@ extern "C" cf_status cf_gemm_fused_rownorm_noalloc(const void *X, const void *W,
     std::memset(&a, 0, sizeof(a));
     if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, 128)) return CF_ERR_CUDA;
     if (!make_tmap_bf16(&a.tmap_w, W, uint64_t(K), uint64_t(N), 64, 64)) return CF_ERR_CUDA;
+    if (!make_tmap_bf16(&a.tmap_y, Y, uint64_t(M), uint64_t(N), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return CF_ERR_CUDA;
     uint8_t *sb = static_cast<uint8_t *>(scratch);
     a.bias = bias;
     a.gamma = gamma;

@@ -58,6 +58,7 @@ enum EpiKind : int {
 struct GemmArgs {
     CUtensorMap tmap_x;   // X [M,K] bf16, box 64(K) x 128(M), 128B swizzle
     CUtensorMap tmap_w;   // W [K,N] bf16, box 64(N) x 64(K), 128B swizzle
+    CUtensorMap tmap_y;   // Y [M,N] bf16, box 32(N) x 32(M), 64B swizzle (stores)
     const float *bias;    // [N] or null
     const float *gamma;   // [N] (LN)
     const float *beta;    // [N] (LN)
@@ -75,6 +76,7 @@ struct GemmArgs {
     int row_blocks;       // RB
     int extra_arrivals;   // test hook
     unsigned long long timeout_ns;
+    unsigned long long *trace;  // optional %globaltimer stamps, CF_TRACE_SLOTS per CTA
 };
 
 // dynamic shared memory of one CTA for a ring of `stages` and a cluster of `cluster`

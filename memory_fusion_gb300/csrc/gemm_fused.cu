@@ -36,12 +36,25 @@
 
 #include <cstdint>
 
+#include "../../include/cf.h"
 #include "cf_internal.h"
 #include "ptx.cuh"
 #include "rowstats.cuh"
 
 namespace cf {
 namespace {
+
+// optional timeline stamps (tracing): one slot per (CTA, tile, event)
+__device__ __forceinline__ void trace_stamp(unsigned long long *tr, int slot) {
+    if (tr != nullptr) tr[blockIdx.x * CF_TRACE_SLOTS + slot] = ptx::globaltimer();
+}
+__device__ __forceinline__ void trace_tile(unsigned long long *tr, int tile, int ev) {
+    if (tr != nullptr && tile < CF_TRACE_TILES)
+        tr[blockIdx.x * CF_TRACE_SLOTS + 4 + tile * CF_TRACE_EVENTS + ev] = ptx::globaltimer();
+}
+__device__ __forceinline__ void trace_tile_value(unsigned long long *tr, int tile, int ev, unsigned long long v) {
+    if (tr != nullptr && tile < CF_TRACE_TILES) tr[blockIdx.x * CF_TRACE_SLOTS + 4 + tile * CF_TRACE_EVENTS + ev] = v;
+}
 
 constexpr int kThreads = 320;      // 10 warps
 constexpr int kEpiWarps = 8;       // warps 2..9
@@ -63,10 +76,12 @@ constexpr uint32_t kInfoGlobal = 0x50000000u;
 struct SmemLayout {
     uint32_t stage_bytes;  // A + B of one stage
     uint32_t ring;         // offset of the operand ring (1024-aligned)
+    uint32_t stg;          // bf16 output staging, 2 KiB per epilogue warp (64B swizzle)
     uint32_t send;         // float2 [2][128]
     uint32_t slot;         // float2 [2][C][128]
     uint32_t res;          // float2 [2][128]
     uint32_t red;          // float2 [128]
+    uint32_t prm;          // float [2][3][256]: bias, gamma, beta of the tile's columns
     uint32_t bars;         // mbarriers
     uint32_t total;        // bytes from the aligned base
 };
@@ -76,6 +91,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n
     L.stage_bytes = kABytes + uint32_t(n_slice) * kBK * 2;
     L.ring = 0;
     uint32_t off = L.ring + uint32_t(stages) * L.stage_bytes;
+    L.stg = off;
+    off += kEpiWarps * 2048;
     L.send = off;
     off += 2 * 128 * 8;
     L.slot = off;
@@ -84,6 +101,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n
     off += 2 * 128 * 8;
     L.red = off;
     off += 128 * 8;
+    L.prm = off;
+    off += 2 * 3 * 256 * 4;
     L.bars = off;
     off += 256;
     L.total = off;
@@ -138,23 +157,72 @@ __device__ __forceinline__ float gelu_tanh_dev(float x) {
     return 0.5f * x * (1.0f + ptx::tanh_approx(u));
 }
 
-__device__ __forceinline__ float4 ldg4(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
+// Softmax stage-1 nodes on one 32-column fragment: z = alpha*acc + bias;
+// online (max, sum exp) update; the fragment is replaced by exp(z - m) where m
+// is the running max after this fragment.
+__device__ __forceinline__ void softmax_fragment(uint32_t (&v)[32], const float *p, float alpha, float &m,
+                                                 float &ssum) {
+    float z[32];
+    float cm = neg_inf();
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 b = *reinterpret_cast<const float4 *>(p + 4 * j4);
+        z[4 * j4 + 0] = fmaf(alpha, __uint_as_float(v[4 * j4 + 0]), b.x);
+        z[4 * j4 + 1] = fmaf(alpha, __uint_as_float(v[4 * j4 + 1]), b.y);
+        z[4 * j4 + 2] = fmaf(alpha, __uint_as_float(v[4 * j4 + 2]), b.z);
+        z[4 * j4 + 3] = fmaf(alpha, __uint_as_float(v[4 * j4 + 3]), b.w);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cm = fmaxf(cm, z[j]);
+    const float mn = fmaxf(m, cm);
+    float s = ssum * ptx::ex2_approx((m - mn) * kLog2e);  // m = -inf on the first fragment: s stays 0
+    const float off = mn * kLog2e;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float ex = ptx::ex2_approx(fmaf(z[j], kLog2e, -off));
+        s += ex;
+        v[j] = __float_as_uint(ex);
+    }
+    ssum = s;
+    m = mn;
+}
 
-// load 32 consecutive parameters (or zeros when p is null)
-__device__ __forceinline__ void load_param32(const float *p, float (&v)[32]) {
-    if (p == nullptr) {
+// LayerNorm stage-1 nodes on one fragment: x = alpha*acc + bias (-> GELU);
+// the fragment is replaced by the stage-1 value; returns its (mean, M2).
+template <bool kGelu>
+__device__ __forceinline__ MeanM2 ln_fragment(uint32_t (&v)[32], const float *p, float alpha) {
+    float x[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0.f;
-        return;
+    for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 b = *reinterpret_cast<const float4 *>(p + 4 * j4);
+        x[4 * j4 + 0] = fmaf(alpha, __uint_as_float(v[4 * j4 + 0]), b.x);
+        x[4 * j4 + 1] = fmaf(alpha, __uint_as_float(v[4 * j4 + 1]), b.y);
+        x[4 * j4 + 2] = fmaf(alpha, __uint_as_float(v[4 * j4 + 2]), b.z);
+        x[4 * j4 + 3] = fmaf(alpha, __uint_as_float(v[4 * j4 + 3]), b.w);
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float4 t = ldg4(p + 4 * j);
-        v[4 * j + 0] = t.x;
-        v[4 * j + 1] = t.y;
-        v[4 * j + 2] = t.z;
-        v[4 * j + 3] = t.w;
+    for (int j = 0; j < 32; ++j) {
+        if constexpr (kGelu) x[j] = gelu_tanh_dev(x[j]);
+        v[j] = __float_as_uint(x[j]);
     }
+    return chunk_mean_m2(x);
+}
+
+// Combine the C per-CTA partials of one row (slot r at s[r*128]) in rank order.
+template <bool kSoftmax>
+__device__ __forceinline__ float2 combine_slots(const float2 *s, int C, float n_slice) {
+    float2 st = s[0];
+    for (int r = 1; r < C; ++r) {
+        const float2 o = s[r * 128];
+        if constexpr (kSoftmax) {
+            const MaxSum m = combine_maxsum(MaxSum{st.x, st.y}, MaxSum{o.x, o.y});
+            st = make_float2(m.m, m.s);
+        } else {
+            const MeanM2 m = combine_counts(MeanM2{st.x, st.y}, float(r) * n_slice, MeanM2{o.x, o.y}, n_slice);
+            st = make_float2(m.mean, m.m2);
+        }
+    }
+    return st;
 }
 
 template <int EPI>
@@ -182,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     const uint32_t cid = ptx::cluster_id_x();
     const uint32_t ncl = ptx::nclusters_x();
     const uint32_t tmem_cols = (ns * 2 <= 32) ? 32u : uint32_t(ns * 2);
+    if (threadIdx.x == 0) trace_stamp(a.trace, 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -212,13 +281,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     // barrier initialisation is visible cluster-wide before any peer signals it
     ptx::cluster_sync();
     const uint32_t tmem_base = misc[0];
+    if (threadIdx.x == 0) trace_stamp(a.trace, 1);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint32_t tx = uint32_t(kABytes) + uint32_t(ns) * kBK * 2;
             uint32_t it = 0;
-            for (int t = cid; t < T; t += ncl) {
+            int ptile = 0;
+            for (int t = cid; t < T; t += ncl, ++ptile) {
                 const int rb = t / G, g = t % G;
                 const int m0 = rb * kBlockM;
                 const int n0 = (g * C + int(rank)) * ns;
@@ -233,6 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                     ptx::tma_load_2d(sa, &a.tmap_x, B.full0 + 8 * s, kb * kBK, m0);
                     for (int j = 0; j < ns / 64; ++j)
                         ptx::tma_load_2d(sb + j * 8192, &a.tmap_w, B.full0 + 8 * s, n0 + j * 64, kb * kBK);
+                    if (kb == 0) trace_tile(a.trace, ptile, CF_TR_TMA_FIRST);
+                    if (kb == nk - 1) trace_tile(a.trace, ptile, CF_TR_TMA_LAST);
                 }
                 if (*abort) break;
             }
@@ -260,13 +333,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 const uint32_t tph = (uint32_t(tile) >> 1) & 1u;
                 ptx::mbar_wait_bounded(B.tmem_empty0 + 8 * buf, tph ^ 1u, tmo, abort, a.err, kInfoMma | buf);
                 if (*abort) break;
+                trace_tile(a.trace, tile, CF_TR_MMA_ACC_FREE);
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + buf * uint32_t(ns);
+                unsigned long long waited = 0;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const uint32_t s = it % uint32_t(stages);
                     const uint32_t ph = (it / uint32_t(stages)) & 1u;
+                    const unsigned long long w0 = a.trace ? ptx::globaltimer() : 0ull;
                     ptx::mbar_wait_bounded(B.full0 + 8 * s, ph, tmo, abort, a.err, kInfoMma | 0x100u | s);
                     if (*abort) break;
+                    if (a.trace) {
+                        waited += ptx::globaltimer() - w0;
+                        if (kb == 0) trace_tile(a.trace, tile, CF_TR_MMA_FIRST);
+                    }
                     ptx::tc_fence_after();
                     const uint32_t sa = base + L.ring + s * L.stage_bytes;
                     const uint32_t sb = sa + kABytes;
@@ -283,6 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 }
                 if (*abort) break;
                 ptx::mma_commit(B.tmem_full0 + 8 * buf);  // accumulator ready
+                trace_tile(a.trace, tile, CF_TR_MMA_DONE);
+                trace_tile_value(a.trace, tile, CF_TR_MMA_WAIT_NS, waited);
             }
             // every MMA issued has completed before TMEM may be released
             ptx::mma_commit(B.mma_done);
@@ -302,78 +384,95 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
         float2 *const slot = reinterpret_cast<float2 *>(gbase + L.slot);
         float2 *const res = reinterpret_cast<float2 *>(gbase + L.res);
         float2 *const red = reinterpret_cast<float2 *>(gbase + L.red);
+        float *const prm = reinterpret_cast<float *>(gbase + L.prm);
+        const uint32_t stg = base + L.stg + uint32_t(e) * 2048u;  // this warp's staging buffer
         const float fN = float(a.N);
+        const int nchunks = half / 32;  // 1, 2 or 4 fragments of 32 columns per thread
 
         int tile = 0;
         for (int t = cid; t < T; t += ncl, ++tile) {
             const int rb = t / G, g = t % G;
             const int m0 = rb * kBlockM;
-            const int nc0 = (g * C + int(rank)) * ns + h * half;  // first global column of this thread
+            const int ncta = (g * C + int(rank)) * ns;  // first global column of this CTA's tile
+            const int hc0 = h * half;                   // first tile column of this thread's half
             const uint32_t buf = tile & 1;
             const uint32_t tph = (uint32_t(tile) >> 1) & 1u;
             const uint32_t xp = buf;  // exchange buffer set
             const uint32_t xph = tph;
 
+            // Row-vector parameters of the tile's columns into shared memory, fetched
+            // before the accumulator is ready (double-buffered by tile parity: set `buf`
+            // is rewritten two tiles later, after every thread passed the next tile's
+            // parameter barrier).
+            float *const pb = prm + buf * 768;
+            float *const pg = pb + 256;
+            float *const pe = pb + 512;
+            if (et < ns) {
+                pb[et] = a.bias ? __ldg(a.bias + ncta + et) : 0.f;
+                if constexpr (EPI != EPI_SOFTMAX) {
+                    pg[et] = __ldg(a.gamma + ncta + et);
+                    pe[et] = __ldg(a.beta + ncta + et);
+                }
+            }
             ptx::mbar_wait_bounded(B.tmem_full0 + 8 * buf, tph, tmo, abort, a.err, kInfoEpi | buf);
             ptx::tc_fence_after();
-            const uint32_t tacc = tmem_base + (uint32_t(q * 32) << 16) + buf * uint32_t(ns) + uint32_t(h * half);
-            const int nchunks = half / 32;
+            ptx::named_bar_sync(kBarEpi, kEpiThreads);  // parameters visible to every epilogue thread
+            if (et0) trace_tile(a.trace, tile, CF_TR_EPI_START);
+            const uint32_t tacc = tmem_base + (uint32_t(q * 32) << 16) + buf * uint32_t(ns) + uint32_t(hc0);
 
-            // ---------------- stage 1: compute phase + thread-local aggregation
-            float2 part;  // LN: (mean, M2) over `half` columns; softmax: (max, sum exp)
+            // ---------------- stage 1: compute phase + thread-local aggregation.
+            // Fragments of 32 columns stream out of TMEM two at a time; the stage-1
+            // value is written back in place for the PostOp (bypass path).
+            float2 part;     // LN: (mean, M2) over `half` columns; softmax: (max, sum exp)
+            float mrun[4];   // softmax: running max when each fragment's exps were taken
             if constexpr (EPI == EPI_SOFTMAX) {
-                float mt = neg_inf();
-                for (int c = 0; c < nchunks; ++c) {
-                    uint32_t v[32];
-                    float bb[32];
-                    ptx::tmem_ld32(tacc + c * 32, v);
-                    load_param32(a.bias ? a.bias + nc0 + c * 32 : nullptr, bb);
-                    ptx::tmem_ld_wait();
+                float m = neg_inf(), ssum = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) mt = fmaxf(mt, fmaf(a.alpha, __uint_as_float(v[j]), bb[j]));
-                }
-                float st = 0.f;
-                for (int c = 0; c < nchunks; ++c) {
-                    uint32_t v[32];
-                    float bb[32];
-                    ptx::tmem_ld32(tacc + c * 32, v);
-                    load_param32(a.bias ? a.bias + nc0 + c * 32 : nullptr, bb);
-                    ptx::tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float z = fmaf(a.alpha, __uint_as_float(v[j]), bb[j]);
-                        const float ex = ptx::ex2_approx((z - mt) * kLog2e);
-                        st += ex;
-                        v[j] = __float_as_uint(ex);
+                for (int c = 0; c < 4; c += 2) {
+                    if (c < nchunks) {
+                        uint32_t v0[32], v1[32];
+                        const bool two = (c + 1 < nchunks);
+                        ptx::tmem_ld32(tacc + c * 32, v0);
+                        if (two) ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
+                        ptx::tmem_ld_wait();
+                        softmax_fragment(v0, pb + hc0 + c * 32, a.alpha, m, ssum);
+                        mrun[c] = m;
+                        ptx::tmem_st32(tacc + c * 32, v0);
+                        if (two) {
+                            softmax_fragment(v1, pb + hc0 + (c + 1) * 32, a.alpha, m, ssum);
+                            mrun[c + 1] = m;
+                            ptx::tmem_st32(tacc + (c + 1) * 32, v1);
+                        }
                     }
-                    ptx::tmem_st32(tacc + c * 32, v);  // bypass: exp(z - mt) for the PostOp
                 }
                 ptx::tmem_st_wait();
-                part = make_float2(mt, st);
+                part = make_float2(m, ssum);
             } else {
                 MeanM2 acc{0.f, 0.f};
-                for (int c = 0; c < nchunks; ++c) {
-                    uint32_t v[32];
-                    float x[32];
-                    ptx::tmem_ld32(tacc + c * 32, v);
-                    load_param32(a.bias ? a.bias + nc0 + c * 32 : nullptr, x);
-                    ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        float xv = fmaf(a.alpha, __uint_as_float(v[j]), x[j]);
-                        if constexpr (EPI == EPI_GELU_LN) xv = gelu_tanh_dev(xv);
-                        x[j] = xv;
-                        v[j] = __float_as_uint(xv);
+                for (int c = 0; c < 4; c += 2) {
+                    if (c < nchunks) {
+                        uint32_t v0[32], v1[32];
+                        const bool two = (c + 1 < nchunks);
+                        ptx::tmem_ld32(tacc + c * 32, v0);
+                        if (two) ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
+                        ptx::tmem_ld_wait();
+                        const MeanM2 c0 = ln_fragment<EPI == EPI_GELU_LN>(v0, pb + hc0 + c * 32, a.alpha);
+                        ptx::tmem_st32(tacc + c * 32, v0);
+                        acc = (c == 0) ? c0 : combine_counts(acc, float(32 * c), c0, 32.f);
+                        if (two) {
+                            const MeanM2 c1 = ln_fragment<EPI == EPI_GELU_LN>(v1, pb + hc0 + (c + 1) * 32, a.alpha);
+                            ptx::tmem_st32(tacc + (c + 1) * 32, v1);
+                            acc = combine_counts(acc, float(32 * (c + 1)), c1, 32.f);
+                        }
                     }
-                    ptx::tmem_st32(tacc + c * 32, v);  // bypass: stage-1 value for the PostOp
-                    const MeanM2 cs = chunk_mean_m2(x);
-                    acc = (c == 0) ? cs : combine_counts(acc, float(32 * c), cs, 32.f);
                 }
                 ptx::tmem_st_wait();
                 part = make_float2(acc.mean, acc.m2);
             }
+            if (et0) trace_tile(a.trace, tile, CF_TR_EPI_STATS);
 
-            // ---------------- level 2: the two column halves through shared memory
+            // ---------------- level 2: the two column halves through one shared buffer
             if (h == 1) red[row] = part;
             ptx::named_bar_sync(kBarEpi, kEpiThreads);
             if (h == 0) {
@@ -389,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 send[xp * 128 + row] = cta;
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar_sync(kBarHalf0, 128);
+                if (et0) trace_tile(a.trace, tile, CF_TR_EPI_CTA);
                 // ---------------- level 3: inter-CTA over DSMEM (TMA bulk copies)
                 if (et0 && !*abort) {
                     const uint32_t src = base + L.send + xp * 1024;
@@ -408,36 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             float2 stat;  // cluster-combined statistic of this row
             if (!a.leader) {
                 ptx::mbar_wait_bounded<true>(B.xfull0 + 8 * xp, xph, tmo, abort, a.err, kInfoXchg | xp);
-                const float2 *sl = slot + xp * C * 128 + row;
-                stat = sl[0];
-                for (int r = 1; r < C; ++r) {
-                    const float2 o = sl[r * 128];
-                    if constexpr (EPI == EPI_SOFTMAX) {
-                        const MaxSum m = combine_maxsum(MaxSum{stat.x, stat.y}, MaxSum{o.x, o.y});
-                        stat = make_float2(m.m, m.s);
-                    } else {
-                        const MeanM2 m = combine_counts(MeanM2{stat.x, stat.y}, float(r * ns), MeanM2{o.x, o.y}, float(ns));
-                        stat = make_float2(m.mean, m.m2);
-                    }
-                }
+                stat = combine_slots<EPI == EPI_SOFTMAX>(slot + xp * C * 128 + row, C, float(ns));
             } else {
                 if (rank == 0) {
                     if (h == 0) {
                         ptx::mbar_wait_bounded<true>(B.xfull0 + 8 * xp, xph, tmo, abort, a.err, kInfoXchg | xp);
-                        const float2 *sl = slot + xp * C * 128 + row;
-                        float2 s2 = sl[0];
-                        for (int r = 1; r < C; ++r) {
-                            const float2 o = sl[r * 128];
-                            if constexpr (EPI == EPI_SOFTMAX) {
-                                const MaxSum m = combine_maxsum(MaxSum{s2.x, s2.y}, MaxSum{o.x, o.y});
-                                s2 = make_float2(m.m, m.s);
-                            } else {
-                                const MeanM2 m =
-                                    combine_counts(MeanM2{s2.x, s2.y}, float(r * ns), MeanM2{o.x, o.y}, float(ns));
-                                s2 = make_float2(m.mean, m.m2);
-                            }
-                        }
-                        res[xp * 128 + row] = s2;
+                        res[xp * 128 + row] = combine_slots<EPI == EPI_SOFTMAX>(slot + xp * C * 128 + row, C, float(ns));
                         ptx::fence_proxy_async_smem();
                         ptx::named_bar_sync(kBarHalf0, 128);
                         if (et0 && !*abort) {
@@ -452,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 }
                 stat = res[xp * 128 + row];
             }
+            if (et0) trace_tile(a.trace, tile, CF_TR_EPI_CLUSTER);
 
             // ---------------- level 4: rows wider than a cluster (global partials)
             if (G > 1) {
@@ -460,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 float2 *pbase = a.partials + (size_t(rb) * G) * 128;
                 if (rank == 0 && h == 0) {
                     pbase[g * 128 + row] = stat;
-                    __threadfence();
+                    // the 128 writes happen before the barrier; the release arrive
+                    // below publishes all of them
                     ptx::named_bar_sync(kBarHalf0, 128);
                     if (et0) ptx::atom_add_release_gpu(cnt, 1u);
                 }
@@ -478,7 +556,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                             ptx::record_error(a.err, 7u, kInfoGlobal | uint32_t(rb));
                             break;
                         }
-                        __nanosleep(64);
                     }
                     // last CTA of this row block to leave resets its counters
                     if (ptx::atom_add_acq_rel_gpu(dep, 1u) == uint32_t(G * C) - 1u) {
@@ -501,53 +578,68 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 }
                 stat = s2;
             }
+            if (et0) trace_tile(a.trace, tile, CF_TR_EPI_GLOBAL);
 
-            // ---------------- stage 2 (PostOp): broadcast the statistic back over the row
-            const int grow = m0 + row;
-            uint16_t *yrow = a.y + size_t(grow) * a.N + nc0;
-            if constexpr (EPI == EPI_SOFTMAX) {
-                // exp(z - mt) * exp(mt - m) / s
-                const float f = ptx::ex2_approx((part.x - stat.x) * kLog2e) / stat.y;
-                for (int c = 0; c < nchunks; ++c) {
-                    uint32_t v[32];
-                    ptx::tmem_ld32(tacc + c * 32, v);
-                    ptx::tmem_ld_wait();
-                    if (grow < a.M) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + c * 32);
+            // ---------------- stage 2 (PostOp): broadcast the statistic back over the row,
+            // bf16 into this warp's staging buffer, TMA bulk store of each 32x32 block
+            const bool rows_live = (m0 + q * 32) < a.M;  // warp-uniform: this warp's 32 rows exist
+            const int ystore = m0 + q * 32;
+            float mean = 0.f, rstd = 0.f;
+            if constexpr (EPI != EPI_SOFTMAX) {
+                mean = stat.x;
+                rstd = rsqrtf(stat.y / fN + a.eps);
+            }
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint4 w;
-                            w.x = ptx::pack_bf16x2(__uint_as_float(v[8 * j + 0]) * f, __uint_as_float(v[8 * j + 1]) * f);
-                            w.y = ptx::pack_bf16x2(__uint_as_float(v[8 * j + 2]) * f, __uint_as_float(v[8 * j + 3]) * f);
-                            w.z = ptx::pack_bf16x2(__uint_as_float(v[8 * j + 4]) * f, __uint_as_float(v[8 * j + 5]) * f);
-                            w.w = ptx::pack_bf16x2(__uint_as_float(v[8 * j + 6]) * f, __uint_as_float(v[8 * j + 7]) * f);
-                            dst[j] = w;
+            for (int c = 0; c < 4; c += 2) {
+                if (c < nchunks) {
+                    uint32_t v0[32], v1[32];
+                    const bool two = (c + 1 < nchunks);
+                    ptx::tmem_ld32(tacc + c * 32, v0);
+                    if (two) ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        if (k == 1 && !two) break;
+                        uint32_t(&v)[32] = k == 0 ? v0 : v1;
+                        const int cc = c + k;
+                        uint32_t w[16];
+                        if constexpr (EPI == EPI_SOFTMAX) {
+                            const float f = ptx::ex2_approx((mrun[cc] - stat.x) * kLog2e) / stat.y;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                w[j] = ptx::pack_bf16x2(__uint_as_float(v[2 * j]) * f, __uint_as_float(v[2 * j + 1]) * f);
+                        } else {
+                            const float *gp = pg + hc0 + cc * 32;
+                            const float *bp = pe + hc0 + cc * 32;
+#pragma unroll
+                            for (int j4 = 0; j4 < 8; ++j4) {
+                                const float4 gm = *reinterpret_cast<const float4 *>(gp + 4 * j4);
+                                const float4 bt = *reinterpret_cast<const float4 *>(bp + 4 * j4);
+                                const float y0 = fmaf((__uint_as_float(v[4 * j4 + 0]) - mean) * rstd, gm.x, bt.x);
+                                const float y1 = fmaf((__uint_as_float(v[4 * j4 + 1]) - mean) * rstd, gm.y, bt.y);
+                                const float y2 = fmaf((__uint_as_float(v[4 * j4 + 2]) - mean) * rstd, gm.z, bt.z);
+                                const float y3 = fmaf((__uint_as_float(v[4 * j4 + 3]) - mean) * rstd, gm.w, bt.w);
+                                w[2 * j4] = ptx::pack_bf16x2(y0, y1);
+                                w[2 * j4 + 1] = ptx::pack_bf16x2(y2, y3);
+                            }
                         }
-                    }
-                }
-            } else {
-                const float mean = stat.x;
-                const float rstd = rsqrtf(stat.y / fN + a.eps);
-                for (int c = 0; c < nchunks; ++c) {
-                    uint32_t v[32];
-                    float gm[32], bt[32];
-                    ptx::tmem_ld32(tacc + c * 32, v);
-                    load_param32(a.gamma + nc0 + c * 32, gm);
-                    load_param32(a.beta + nc0 + c * 32, bt);
-                    ptx::tmem_ld_wait();
-                    if (grow < a.M) {
-                        float y[32];
+                        if (rows_live) {
+                            // the previous store from this buffer has finished reading it
+                            if (lane == 0) ptx::bulk_wait_group_read0();
+                            __syncwarp();
+                            // row `lane` of the 32x32 block: four 16-byte pieces, 64B swizzle
+                            const uint32_t ra = stg + uint32_t(lane) * 64u;
+                            const uint32_t sw = (uint32_t(lane) >> 1) & 3u;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) y[j] = fmaf((__uint_as_float(v[j]) - mean) * rstd, gm[j], bt[j]);
-                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + c * 32);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint4 w;
-                            w.x = ptx::pack_bf16x2(y[8 * j + 0], y[8 * j + 1]);
-                            w.y = ptx::pack_bf16x2(y[8 * j + 2], y[8 * j + 3]);
-                            w.z = ptx::pack_bf16x2(y[8 * j + 4], y[8 * j + 5]);
-                            w.w = ptx::pack_bf16x2(y[8 * j + 6], y[8 * j + 7]);
-                            dst[j] = w;
+                            for (int k4 = 0; k4 < 4; ++k4)
+                                ptx::st_shared_v4(ra + ((uint32_t(k4) ^ sw) << 4), w[4 * k4], w[4 * k4 + 1],
+                                                  w[4 * k4 + 2], w[4 * k4 + 3]);
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                ptx::tma_store_2d(&a.tmap_y, stg, ncta + hc0 + cc * 32, ystore);
+                                ptx::bulk_commit_group();
+                            }
                         }
                     }
                 }
@@ -556,8 +648,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(B.tmem_empty0 + 8 * buf);
+            if (et0) trace_tile(a.trace, tile, CF_TR_EPI_STORED);
         }
+        // every bulk store of this warp has completed before the CTA may leave
+        if (lane == 0) ptx::bulk_wait_group0();
+        __syncwarp();
     }
+    if (threadIdx.x == 64) trace_stamp(a.trace, 2);
 
     // ------------------------------------------------------------ teardown
     ptx::tc_fence_before();
@@ -566,6 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     // no CTA leaves while a peer may still access its shared memory
     ptx::cluster_sync();
     if (warp == 1) ptx::tmem_dealloc(tmem_base, tmem_cols);
+    if (threadIdx.x == 64) trace_stamp(a.trace, 3);
 }
 
 void *kernel_for(int kind) {

@@ -49,7 +49,7 @@ def test_status_strings():
 
 def test_tuning_default_is_zero():
     t = cf.cf_tuning_default()
-    assert all(getattr(t, f) == 0 for f, _ in t._fields_)
+    assert all(getattr(t, f) in (0, None) for f, _ in t._fields_)
 
 
 def _active(d):
@@ -59,36 +59,57 @@ def _active(d):
     return a
 
 
-GB300_LIKE = _active({1: 148, 2: 74, 4: 37, 8: 18, 16: 9})
+# cluster residency measured on a GB300 (152 SMs) for this kernel's shared-memory sizes
+GB300 = _active({1: 152, 2: 76, 4: 36, 8: 15, 16: 7})
+GB300_LIKE = GB300
 
 
-def test_plan_single_cluster_rows():
-    # N = 2048 -> 8 slices of 256 -> one cluster of 8, peer mode
-    st, p = cf.cf_plan_gemm_fused(4096, 2048, 128, 148, GB300_LIKE)
+def test_plan_forced_single_cluster_rows():
+    # N = 2048 -> 8 slices of 256; forcing a cluster of 8 keeps the row in one cluster (peer mode)
+    st, p = cf.cf_plan_gemm_fused(4096, 2048, 128, 152, GB300, cf.tuning(cluster_size=8))
     assert st == cf.CF_OK
     assert (p.n_slice, p.ctas_per_row, p.cluster_size, p.groups, p.leader_mode) == (256, 8, 8, 1, 0)
-    assert p.row_blocks == 32 and p.clusters == 18
+    assert p.row_blocks == 32 and p.clusters == 15
     assert p.smem_bytes <= 232448 and p.stages >= 2
 
 
+def test_plan_chooses_most_useful_sm_time():
+    """The automatic choice maximises row_blocks*cpr/(ceil(T/ncl)*SMs) (x0.97, or x0.85
+    for K < 512, when the row needs the global barrier); larger clusters win ties."""
+    cases = {
+        (4096, 2048, 128): (4, 2, 36),      # cluster 8 would leave 32 SMs idle and run 3 tiles deep
+        (16384, 4096, 4096): (2, 8, 76),
+        (8192, 16384, 2048): (2, 32, 76),
+        (128, 512, 256): (2, 1, 1),
+    }
+    for (M, N, K), (C, G, ncl) in cases.items():
+        st, p = cf.cf_plan_gemm_fused(M, N, K, 152, GB300)
+        assert st == cf.CF_OK
+        assert (p.cluster_size, p.groups, p.clusters) == (C, G, ncl), (M, N, K, p.as_dict())
+
+
 def test_plan_leader_mode_above_threshold():
-    st, p = cf.cf_plan_gemm_fused(16384, 4096, 4096, 148, GB300_LIKE)
+    t = cf.tuning(cluster_size=16)
+    st, p = cf.cf_plan_gemm_fused(16384, 4096, 4096, 152, GB300, t)
     assert st == cf.CF_OK
-    assert (p.cluster_size, p.groups, p.leader_mode) == (16, 1, 1)
-    assert p.clusters == 9
-    st, p = cf.cf_plan_gemm_fused(16384, 4096, 4096, 148, GB300_LIKE, cf.tuning(peer_max=16))
+    assert (p.cluster_size, p.groups, p.leader_mode, p.clusters) == (16, 1, 1, 7)
+    st, p = cf.cf_plan_gemm_fused(16384, 4096, 4096, 152, GB300, cf.tuning(cluster_size=16, peer_max=16))
     assert p.leader_mode == 0
+    st, p = cf.cf_plan_gemm_fused(16384, 4096, 4096, 152, GB300, cf.tuning(cluster_size=2, peer_max=-1))
+    assert p.leader_mode == 1
 
 
 def test_plan_wide_rows_use_global_path():
-    # N = 16384 -> 64 slices -> 4 clusters of 16 per row block
-    st, p = cf.cf_plan_gemm_fused(8192, 16384, 2048, 148, GB300_LIKE)
+    # N = 16384 -> 64 slices; a cluster of 16 needs G = 4 resident clusters per row block
+    st, p = cf.cf_plan_gemm_fused(8192, 16384, 2048, 152, GB300, cf.tuning(cluster_size=16))
     assert st == cf.CF_OK
-    assert (p.cluster_size, p.groups) == (16, 4)
-    assert p.clusters % p.groups == 0 and p.clusters <= 9
-    # cluster 8 forced: G = 8 and the grid holds a multiple of 8 resident clusters
-    st, p = cf.cf_plan_gemm_fused(8192, 16384, 2048, 148, GB300_LIKE, cf.tuning(cluster_size=8))
-    assert (p.cluster_size, p.groups, p.clusters) == (8, 8, 16)
+    assert (p.cluster_size, p.groups, p.clusters) == (16, 4, 7)
+    # cluster 8 forced: G = 8 and all 15 resident clusters are used
+    st, p = cf.cf_plan_gemm_fused(8192, 16384, 2048, 152, GB300, cf.tuning(cluster_size=8))
+    assert (p.cluster_size, p.groups, p.clusters) == (8, 8, 15)
+    # never more clusters than tickets
+    st, p = cf.cf_plan_gemm_fused(128, 16384, 2048, 152, GB300, cf.tuning(cluster_size=2))
+    assert (p.groups, p.clusters) == (32, 32)
 
 
 def test_plan_residency_refused():
@@ -105,10 +126,10 @@ def test_plan_shapes():
     st, p = cf.cf_plan_gemm_fused(128, 192, 64, 148, GB300_LIKE)  # 192 = 3 x 64
     assert st == cf.CF_OK
     assert (p.n_slice, p.ctas_per_row) == (64, 3)
-    st, p = cf.cf_plan_gemm_fused(1, 384, 64, 148, _active({3: 40}))
+    st, p = cf.cf_plan_gemm_fused(1, 384, 64, 152, _active({3: 40}))
     assert (p.n_slice, p.cluster_size, p.row_blocks, p.clusters) == (128, 3, 1, 1)
     # tiny: one row block, one cluster of 2
-    st, p = cf.cf_plan_gemm_fused(128, 512, 256, 148, GB300_LIKE)
+    st, p = cf.cf_plan_gemm_fused(128, 512, 256, 152, GB300)
     assert (p.cluster_size, p.clusters, p.row_blocks) == (2, 1, 1)
 
 
