@@ -105,6 +105,12 @@ typedef struct cf_tuning {
                                barrier waits for; > 0 makes that wait run out
                                (CF_ERR_DEVICE_TIMEOUT) without faulting.  0 in
                                normal use.                                        */
+    int32_t cluster_m;      /* GEMM: row blocks per cluster (1 or 2); 2 pairs the
+                               two row blocks' CTAs into one tcgen05 MMA stream
+                               (cta_group::2, M = 256; each CTA stages half of
+                               the W tile).  0 = auto                           */
+    int32_t multicast_x;    /* GEMM, C_M = 1: multicast each X tile along the row
+                               group instead of loading it in every CTA        */
     uint64_t *trace;        /* TRACING (fused GEMM): device buffer of
                                grid_ctas * CF_TRACE_SLOTS u64 %globaltimer stamps
                                (ns), or NULL for none.  Per CTA: slots 0..3 =
@@ -151,11 +157,14 @@ typedef struct cf_plan {
     int32_t clusters;       /* clusters of the persistent grid                     */
     int32_t stages;         /* operand ring depth                                  */
     int32_t smem_bytes;     /* dynamic shared memory per CTA                       */
+    int32_t cluster_m;      /* C_M: row blocks per cluster; a cluster holds
+                               C_M * C_N CTAs; C_M = 2 runs CTA pairs (ranks
+                               2i, 2i+1) as one cta_group::2 MMA stream           */
 } cf_plan;
 
 /* Plan a fused GEMM+row-reduce launch for a device with `sm_count` SMs, where
- * max_active_clusters[c] (c = 1..16) is how many clusters of c CTAs can be
- * resident at once (0 = that size cannot launch).  Pure host arithmetic: the
+ * max_active_clusters[c] (c = 1..16) is how many clusters of c CTAs (one CTA
+ * per SM) can be resident at once (0 = that size cannot launch).  Pure host arithmetic: the
  * same choice the launch calls make after querying the device.
  * Returns CF_UNSUPPORTED for shapes outside the supported set and
  * CF_ERR_NOT_RESIDENT if no residency-valid plan exists. */
@@ -246,8 +255,8 @@ CF_API cf_status cf_gemm_fused_rownorm_ex(const void *X, const void *W, const fl
  * of 4 MiB inside libcf, which every GPU that loads the library holds until
  * the process exits.  A call needing more scratch than that (256 B + 8 B per
  * 128-row block, rounded up to 256 B, + 1 KiB per 128-row block and cluster
- * group of a row wider than one cluster) returns CF_ERR_WORKSPACE_TOO_SMALL
- * without launching.
+ * group -- rounded up to an even count -- of a row wider than one cluster)
+ * returns CF_ERR_WORKSPACE_TOO_SMALL without launching.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.

@@ -39,6 +39,8 @@ class cf_tuning(ctypes.Structure):
         ("stitch_mapping", ctypes.c_int32),
         ("timeout_us", ctypes.c_uint32),
         ("extra_arrivals", ctypes.c_int32),
+        ("cluster_m", ctypes.c_int32),
+        ("multicast_x", ctypes.c_int32),
         ("trace", ctypes.c_void_p),
     ]
 
@@ -61,6 +63,7 @@ class cf_plan(ctypes.Structure):
         ("clusters", ctypes.c_int32),
         ("stages", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32),
+        ("cluster_m", ctypes.c_int32),
     ]
 
     def as_dict(self):

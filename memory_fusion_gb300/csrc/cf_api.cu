@@ -76,23 +76,23 @@ bool make_tmap_bf16(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t col
 // -------------------------------------------------------------------------
 // occupancy cache: max co-resident clusters for (device, kind, cluster, smem)
 // -------------------------------------------------------------------------
-int max_active_cached(int device, int kind, int cluster, int smem) {
-    static std::map<std::tuple<int, int, int, int>, int> cache;
-    auto key = std::make_tuple(device, kind, cluster, smem);
+int max_active_cached(int device, int kind, bool pair, int cluster, int smem) {
+    static std::map<std::tuple<int, int, int, int, int>, int> cache;
+    auto key = std::make_tuple(device, kind, pair ? 1 : 0, cluster, smem);
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    int n = cf::gemm_fused_max_active_clusters(kind, cluster, smem);
+    int n = cf::gemm_fused_max_active_clusters(kind, pair, cluster, smem);
     std::lock_guard<std::mutex> lk(g_mu);
     cache[key] = n;
     return n;
 }
 
-int gemm_stages_for(int n_slice, int cluster, int requested) {
+int gemm_stages_for(int n_slice, int cluster, int requested, bool pair) {
     int s = requested > 0 ? requested : 6;
-    while (s > 2 && cf::gemm_fused_smem_bytes(s, cluster, n_slice) > kMaxSmem) --s;
+    while (s > 2 && cf::gemm_fused_smem_bytes(s, cluster, n_slice, pair) > kMaxSmem) --s;
     return s;
 }
 
@@ -176,46 +176,60 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
     if (cpr64 > 16 * 64) return CF_ERR_UNSUPPORTED;
     const int cpr = int(cpr64);
     const int rb = int((M + cf::kBlockM - 1) / cf::kBlockM);
-    // Choose the cluster size C (a divisor of the CTAs per row) that keeps the
-    // most SM-time on useful tiles.  The persistent grid holds ncl clusters
-    // (never more than can be resident); each takes ceil(T / ncl) tickets of
-    // T = row_blocks * G, so the useful fraction of SM-time is
-    //     row_blocks * cpr / (ceil(T / ncl) * sm_count).
-    // Rows wider than one cluster (G > 1) meet at the in-kernel barrier: every
-    // one of a row block's G clusters must be resident (ncl >= G), and the
-    // barrier costs a little (more when a short K loop cannot hide it).
-    auto score = [&](int c, int *ncl_out) -> double {
-        if (c < 1 || c > 16 || cpr % c != 0 || max_active_clusters[c] <= 0) return -1.0;
-        const int g = cpr / c;
+    const int nk = int(K / 64);
+    // Choose C_N (CTAs along a row, a divisor of the CTAs per row) and C_M (row
+    // blocks per cluster: 2 = CTA pairs sharing one cta_group::2 MMA stream) by
+    // predicted time.  The persistent grid holds ncl clusters (never more than
+    // can be resident); each takes ceil(T / ncl) of T = ceil(row_blocks / C_M) * G
+    // tickets, one tile per CTA each.  A tile costs max(mainloop, epilogue):
+    // the TMEM double buffer overlaps one tile's epilogue with the next tile's
+    // mainloop.  The constants were measured on GB300 with the device trace
+    // (tensor-bound workloads, 128x256 tiles per CTA):
+    //   mainloop  ~ 0.48 us per 64-deep k-block for a CTA pair, 0.55 us single
+    //   epilogue  ~ 4.5 us, plus 4 + 0.2 G us when the row spans G > 1 clusters
+    //               (the global barrier waits for the slowest of G clusters),
+    //               plus 0.5 us for a CTA pair when K < 512
+    // Rows wider than one row group need all G clusters of a row block
+    // resident (ncl >= G).
+    auto predict = [&](int cn, int cm, int *ncl_out) -> double {
+        const int c = cn * cm;
+        if (cn < 1 || c > 16 || cpr % cn != 0 || max_active_clusters[c] <= 0) return -1.0;
+        if (cm == 2 && (ns < 128 || rb < 2)) return -1.0;
+        const int g = cpr / cn;
         int n = max_active_clusters[c];
         if (t.max_clusters > 0) n = std::min(n, int(t.max_clusters));
         if (g > 1 && n < g) return -1.0;
-        const int64_t T = int64_t(rb) * g;
+        const int64_t T = int64_t((rb + cm - 1) / cm) * g;
         if (T < n) n = int(T);
         const int64_t per = (T + n - 1) / n;
-        double eff = double(rb) * cpr / (double(per) * sm_count);
-        if (g > 1) eff *= (K / 64 >= 8) ? 0.97 : 0.85;
+        const double t_main = nk * (cm == 2 ? 0.48 : 0.55) * (ns / 256.0);
+        // a pair's coupled pipelines cost latency that only long K loops repay
+        const double t_epi = 4.5 + (g > 1 ? 4.0 + 0.2 * g : 0.6) + (cm == 2 && nk < 8 ? 0.5 : 0.0);
         *ncl_out = n;
-        return eff;
+        return double(per) * std::max(t_main, t_epi) + t_epi;
     };
-    int C = 0, ncl = 0;
-    if (t.cluster_size > 0) {
-        if (t.cluster_size > 16 || cpr % t.cluster_size != 0) return CF_ERR_UNSUPPORTED;
-        if (max_active_clusters[t.cluster_size] <= 0) return CF_ERR_NOT_RESIDENT;
-        if (score(t.cluster_size, &ncl) < 0) return CF_ERR_NOT_RESIDENT;
-        C = t.cluster_size;
-    } else {
-        double best = -1.0;
-        for (int c = std::min(16, cpr); c >= 1; --c) {  // larger clusters win ties
-            int n = 0;
-            const double e = score(c, &n);
-            if (e > best + 1e-9) {
-                best = e;
-                C = c;
-                ncl = n;
+    int C = 0, CMs = 0, ncl = 0;
+    {
+        double best = 0.0;
+        for (int cm = 2; cm >= 1; --cm) {
+            if (t.cluster_m > 0 && cm != t.cluster_m) continue;
+            for (int cn = std::min(16, cpr); cn >= 1; --cn) {  // larger clusters win ties
+                if (t.cluster_size > 0 && cn != t.cluster_size) continue;
+                int n = 0;
+                const double e = predict(cn, cm, &n);
+                if (e > 0.0 && (C == 0 || e < best * (1.0 - 1e-9))) {
+                    best = e;
+                    C = cn;
+                    CMs = cm;
+                    ncl = n;
+                }
             }
         }
-        if (C == 0) return CF_ERR_NOT_RESIDENT;
+        if (C == 0) {
+            if (t.cluster_size > 16 || (t.cluster_size > 0 && cpr % t.cluster_size != 0)) return CF_ERR_UNSUPPORTED;
+            if (t.cluster_m > 2 || t.cluster_m < 0) return CF_ERR_UNSUPPORTED;
+            return CF_ERR_NOT_RESIDENT;
+        }
     }
     const int G = cpr / C;
     const int peer_max = t.peer_max == 0 ? 8 : t.peer_max;
@@ -226,8 +240,9 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
     plan->leader_mode = (peer_max < 0 || C > peer_max) ? 1 : 0;
     plan->row_blocks = rb;
     plan->clusters = std::max(ncl, 1);
-    plan->stages = gemm_stages_for(ns, C, t.stages);
-    plan->smem_bytes = cf::gemm_fused_smem_bytes(plan->stages, C, ns);
+    plan->stages = gemm_stages_for(ns, C, t.stages, CMs == 2);
+    plan->smem_bytes = cf::gemm_fused_smem_bytes(plan->stages, C, ns, CMs == 2);
+    plan->cluster_m = CMs;
     if (plan->smem_bytes > kMaxSmem) return CF_ERR_UNSUPPORTED;
     return CF_OK;
 }
@@ -235,8 +250,9 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
 size_t cf_gemm_fused_workspace_size(int64_t M, int64_t N, int64_t K) {
     (void)K;
     if (M < 0 || N <= 0) return cf::kErrBytes;
-    const size_t rb = size_t((M + cf::kBlockM - 1) / cf::kBlockM);
-    const size_t gmax = size_t((N + 63) / 64);
+    size_t rb = size_t((M + cf::kBlockM - 1) / cf::kBlockM);
+    rb += rb & 1;  // row blocks are padded to whole clusters of two
+    const size_t gmax = size_t((N + 63) / 64) + 1;  // cluster groups, rounded up to even
     return cf::kErrBytes + cf::align_up(8 * rb, 256) + rb * gmax * 128 * sizeof(float2);
 }
 
@@ -350,13 +366,17 @@ static cf_status device_plan(int kind, int64_t M, int64_t N, int64_t K, const cf
     if ((ns != 64 && ns != 128 && ns != 256) || N % ns != 0) return CF_ERR_UNSUPPORTED;
     const int64_t cpr = N / ns;
     for (int c = 0; c <= 16; ++c) active[c] = 0;
+    // residency is per SM (one CTA per SM at any of these shared-memory
+    // sizes), so one query per total cluster size serves every (C_N, C_M)
     for (int c = 1; c <= 16; ++c) {
-        if (cpr % c != 0) continue;
-        if (t.cluster_size > 0 && c != t.cluster_size) continue;
-        const int st = gemm_stages_for(ns, c, t.stages);
-        const int smem = cf::gemm_fused_smem_bytes(st, c, ns);
+        const bool as_cn = (cpr % c == 0);
+        const bool as_pair = (c % 2 == 0) && (cpr % (c / 2) == 0) && ns >= 128;
+        if (!as_cn && !as_pair) continue;
+        const int cn = as_cn ? c : c / 2;
+        const int st = gemm_stages_for(ns, cn, t.stages, !as_cn);
+        const int smem = cf::gemm_fused_smem_bytes(st, cn, ns, !as_cn);
         if (smem > std::min(kMaxSmem, dev.max_smem_optin)) continue;
-        active[c] = max_active_cached(dev.device, kind, c, smem);
+        active[c] = max_active_cached(dev.device, kind, !as_cn, c, smem);
     }
     return cf_plan_gemm_fused(M, N, K, dev.sm_count, active, tuning, plan);
 }
@@ -401,7 +421,11 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
 
     cf::GemmArgs a;
     std::memset(&a, 0, sizeof(a));
-    if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, 128)) return CF_ERR_CUDA;
+    {
+        const bool mcx = t.multicast_x && plan.cluster_m == 1 && plan.cluster_size > 1;
+        if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, mcx ? 128 / plan.cluster_size : 128))
+            return CF_ERR_CUDA;
+    }
     if (!make_tmap_bf16(&a.tmap_w, W, uint64_t(K), uint64_t(N), 64, 64)) return CF_ERR_CUDA;
     if (!make_tmap_bf16(&a.tmap_y, Y, uint64_t(M), uint64_t(N), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return CF_ERR_CUDA;
     a.bias = bias;
@@ -411,7 +435,10 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     a.err = reinterpret_cast<uint32_t *>(wsb);
     a.counters = reinterpret_cast<uint32_t *>(wsb + cf::kErrBytes);
-    a.partials = reinterpret_cast<float2 *>(wsb + cf::kErrBytes + cf::align_up(8 * size_t(plan.row_blocks), 256));
+    {
+        const size_t rba = size_t((plan.row_blocks + plan.cluster_m - 1) / plan.cluster_m) * plan.cluster_m;
+        a.partials = reinterpret_cast<float2 *>(wsb + cf::kErrBytes + cf::align_up(8 * rba, 256));
+    }
     a.M = int(M);
     a.N = int(N);
     a.K = int(K);
@@ -419,12 +446,16 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
     a.eps = eps;
     a.n_slice = plan.n_slice;
     a.cluster = plan.cluster_size;
+    a.cluster_m = plan.cluster_m;
     a.groups = plan.groups;
     a.leader = plan.leader_mode;
     a.row_blocks = plan.row_blocks;
+    a.super_blocks = (plan.row_blocks + plan.cluster_m - 1) / plan.cluster_m;
+    a.row_blocks_alloc = a.super_blocks * plan.cluster_m;
     a.extra_arrivals = t.extra_arrivals;
     a.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
     a.trace = reinterpret_cast<unsigned long long *>(t.trace);
+    a.multicast_x = (t.multicast_x && plan.cluster_m == 1 && plan.cluster_size > 1) ? 1 : 0;
     cudaError_t e = cf::launch_gemm_fused(kind, a, plan.clusters, plan.stages, plan.smem_bytes,
                                           reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
@@ -523,8 +554,10 @@ extern "C" cf_status cf_gemm_fused_rownorm_noalloc(const void *X, const void *W,
     if (st != CF_OK) return st;
     // scratch this launch uses: error word + counters (must start at zero) and
     // one float2 per row and cluster group of the global partial buffer
-    const size_t head = cf::kErrBytes + cf::align_up(8 * size_t(plan.row_blocks), 256);
-    const size_t need = head + size_t(plan.row_blocks) * size_t(plan.groups) * 128 * sizeof(float2);
+    const size_t rba = size_t((plan.row_blocks + plan.cluster_m - 1) / plan.cluster_m) * plan.cluster_m;
+    const size_t head = cf::kErrBytes + cf::align_up(8 * rba, 256);
+    const size_t gp = size_t(plan.groups) + size_t(plan.groups & 1);
+    const size_t need = head + rba * gp * 128 * sizeof(float2);
     if (need > kNoAllocScratchBytes) return CF_ERR_WORKSPACE_TOO_SMALL;
     void *scratch = nullptr;
     st = noalloc_scratch(dev.device, &scratch);
@@ -553,9 +586,12 @@ extern "C" cf_status cf_gemm_fused_rownorm_noalloc(const void *X, const void *W,
     a.eps = eps;
     a.n_slice = plan.n_slice;
     a.cluster = plan.cluster_size;
+    a.cluster_m = plan.cluster_m;
     a.groups = plan.groups;
     a.leader = plan.leader_mode;
     a.row_blocks = plan.row_blocks;
+    a.super_blocks = (plan.row_blocks + plan.cluster_m - 1) / plan.cluster_m;
+    a.row_blocks_alloc = a.super_blocks * plan.cluster_m;
     a.extra_arrivals = 0;
     a.timeout_ns = 1000ull * kDefaultTimeoutUs;
     e = cf::launch_gemm_fused(kind, a, plan.clusters, plan.stages, plan.smem_bytes, s);

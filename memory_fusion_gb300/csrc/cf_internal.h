@@ -12,7 +12,7 @@ namespace cf {
 // Workspace layout (device, caller-owned, zeroed once):
 //   [0, 256)                 error word: u32 status, u32 info, rest reserved
 //   [256, 256 + 8*RB pad)    per-row-block counters: arrive[RB], depart[RB]
-//   [...]                    global partials: [RB][G][128] float2
+//   [...]                    global partials: [RB][128][G rounded up to even] float2
 constexpr size_t kErrBytes = 256;
 constexpr int kBlockM = 128;  // rows of one GEMM tile (tcgen05 M = 128, one row per TMEM lane)
 
@@ -56,7 +56,7 @@ enum EpiKind : int {
 };
 
 struct GemmArgs {
-    CUtensorMap tmap_x;   // X [M,K] bf16, box 64(K) x 128(M), 128B swizzle
+    CUtensorMap tmap_x;   // X [M,K] bf16, box 64(K) x (128/C_N)(M), 128B swizzle
     CUtensorMap tmap_w;   // W [K,N] bf16, box 64(N) x 64(K), 128B swizzle
     CUtensorMap tmap_y;   // Y [M,N] bf16, box 32(N) x 32(M), 64B swizzle (stores)
     const float *bias;    // [N] or null
@@ -65,26 +65,33 @@ struct GemmArgs {
     uint16_t *y;          // [M,N] bf16
     uint32_t *err;        // workspace error word
     uint32_t *counters;   // [2*RB]: arrive, depart
-    float2 *partials;     // [RB][G][128]
+    float2 *partials;     // [RB][128][Gp]
     int M, N, K;
     float alpha;          // LN: multiplies acc; softmax: scale
     float eps;
     int n_slice;          // columns of one tile
-    int cluster;          // C_N
+    int cluster;          // C_N: CTAs of one row group (along N)
+    int cluster_m;        // C_M: row blocks per cluster; 2 = CTA pairs sharing one
+                          // cta_group::2 MMA stream (M = 256, W split between the pair)
+    int multicast_x;      // single-CTA MMA: multicast each X tile along the row group
     int groups;           // G
-    int leader;           // leader-follower aggregation in the cluster
-    int row_blocks;       // RB
+    int leader;           // leader-follower aggregation in the row group
+    int row_blocks;       // RB = ceil(M / 128)
+    int row_blocks_alloc; // RB rounded up to a multiple of C_M (counter / partial rows)
+    int super_blocks;     // RB_alloc / C_M
     int extra_arrivals;   // test hook
     unsigned long long timeout_ns;
     unsigned long long *trace;  // optional %globaltimer stamps, CF_TRACE_SLOTS per CTA
 };
 
-// dynamic shared memory of one CTA for a ring of `stages` and a cluster of `cluster`
-int gemm_fused_smem_bytes(int stages, int cluster, int n_slice);
+// dynamic shared memory of one CTA for a ring of `stages`, a row group of
+// `cluster` CTAs, and the CTA-pair MMA mode or not
+int gemm_fused_smem_bytes(int stages, int cluster, int n_slice, bool pair);
 
-// Query max co-resident clusters of `cluster` CTAs for the fused kernel of
-// `kind` with `smem` dynamic shared memory (0 if it cannot launch).
-int gemm_fused_max_active_clusters(int kind, int cluster, int smem);
+// Query max co-resident clusters of `cluster` CTAs (total) for the fused
+// kernel of `kind` and mode with `smem` dynamic shared memory (0 if it cannot
+// launch).
+int gemm_fused_max_active_clusters(int kind, bool pair, int cluster, int smem);
 
 cudaError_t launch_gemm_fused(int kind, const GemmArgs &a, int clusters, int stages, int smem,
                               cudaStream_t stream);

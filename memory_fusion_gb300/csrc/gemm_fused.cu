@@ -86,9 +86,10 @@ struct SmemLayout {
     uint32_t total;        // bytes from the aligned base
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n_slice) {
+__host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n_slice, bool pair) {
     SmemLayout L;
-    L.stage_bytes = kABytes + uint32_t(n_slice) * kBK * 2;
+    // a CTA of a pair stages its own 128 rows of X and half of the tile's W columns
+    L.stage_bytes = kABytes + uint32_t(pair ? n_slice / 2 : n_slice) * kBK * 2;
     L.ring = 0;
     uint32_t off = L.ring + uint32_t(stages) * L.stage_bytes;
     L.stg = off;
@@ -143,10 +144,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 }
 
 // instruction descriptor: kind::f16, A = B = bf16, D = fp32, A K-major,
-// B MN-major (W is [K,N] with N contiguous), M = 128, N = n
-__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+// B MN-major (W is [K,N] with N contiguous), M = m (128, or 256 for a CTA pair), N = n
+__device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) | (uint32_t(n >> 3) << 17) |
-           (uint32_t(kBlockM >> 4) << 24);
+           (uint32_t(m >> 4) << 24);
 }
 
 __device__ __forceinline__ float gelu_tanh_dev(float x) {
@@ -225,20 +226,23 @@ __device__ __forceinline__ float2 combine_slots(const float2 *s, int C, float n_
     return st;
 }
 
-template <int EPI>
+template <int EPI, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_constant__ GemmArgs a, int stages) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *const gbase = smem_raw + (base - raw);
 
-    const int C = a.cluster;
+    const int C = a.cluster;                // C_N: CTAs of one row group
+    const int CM = kPair ? 2 : 1;           // row blocks per cluster
     const int G = a.groups;
     const int ns = a.n_slice;
     const int half = ns / 2;
     const int nk = a.K / kBK;
-    const int T = a.row_blocks * G;  // tickets: (row block, cluster group), row-block major
-    const SmemLayout L = smem_layout(stages, C, ns);
+    const int T = a.super_blocks * G;       // tickets: (super row block, cluster group), row-block major
+    const int nbox = ns / 64;               // 64-column W boxes of a tile
+    const int my_boxes = kPair ? nbox / 2 : nbox;  // W boxes staged in this CTA
+    const SmemLayout L = smem_layout(stages, C, ns, kPair);
     const Bars B = bars_at(base + L.bars, stages);
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + (B.misc - base));
     volatile uint32_t *abort = misc + 1;
@@ -246,20 +250,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = ptx::cluster_ctarank();
+    const uint32_t crank = ptx::cluster_ctarank();
     const uint32_t cid = ptx::cluster_id_x();
     const uint32_t ncl = ptx::nclusters_x();
+    // Cluster rank = rank * C_M + m_sub: m_sub is this CTA's row block within the
+    // cluster; a CTA pair (cta_group::2) is two consecutive ranks; `rank` is the
+    // column slice within the row group {j * C_M + m_sub}.
+    const int m_sub = int(crank) % CM;
+    const uint32_t rank = crank / uint32_t(CM);
+    const uint32_t pair_leader = crank & ~1u;         // even CTA of the pair (issues the MMAs)
+    const bool is_leader = !kPair || (crank & 1u) == 0u;
+    // optional X multicast along the row group (single-CTA MMA only)
+    const bool mcx = !kPair && a.multicast_x && C > 1;
+    uint16_t a_mask = uint16_t(1u << crank);
+    if (mcx) a_mask = uint16_t((1u << C) - 1u);
+    const int a_rows = mcx ? kBlockM / C : kBlockM;  // rows of the X tile this CTA loads
     const uint32_t tmem_cols = (ns * 2 <= 32) ? 32u : uint32_t(ns * 2);
     if (threadIdx.x == 0) trace_stamp(a.trace, 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             ptx::mbar_init(B.full0 + 8 * s, 1);
-            ptx::mbar_init(B.empty0 + 8 * s, 1);
+            ptx::mbar_init(B.empty0 + 8 * s, uint32_t(__popc(a_mask)));
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(B.tmem_full0 + 8 * b, 1);
-            ptx::mbar_init(B.tmem_empty0 + 8 * b, kEpiWarps);
+            // the pair leader waits for both CTAs' epilogue warps
+            ptx::mbar_init(B.tmem_empty0 + 8 * b, kPair ? 2 * kEpiWarps : kEpiWarps);
             ptx::mbar_init(B.xfull0 + 8 * b, 1);
             ptx::mbar_init(B.xres0 + 8 * b, 1);
         }
@@ -268,8 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
         ptx::fence_mbarrier_init_cluster();
     }
     if (warp == 1) {
-        ptx::tmem_alloc(B.misc, tmem_cols);
-        ptx::tmem_relinquish();
+        if constexpr (kPair) {
+            ptx::tmem_alloc_pair(B.misc, tmem_cols);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(B.misc, tmem_cols);
+            ptx::tmem_relinquish();
+        }
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&a.tmap_x);
@@ -286,46 +308,65 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const uint32_t tx = uint32_t(kABytes) + uint32_t(ns) * kBK * 2;
+            // bytes landing on the full barrier of this CTA (pair: the leader's
+            // barrier receives both CTAs' tiles)
+            const uint32_t tx_cta = uint32_t(kABytes) + uint32_t(my_boxes) * 8192u;
+            const uint32_t tx = kPair ? 2u * tx_cta : tx_cta;
             uint32_t it = 0;
             int ptile = 0;
             for (int t = cid; t < T; t += ncl, ++ptile) {
-                const int rb = t / G, g = t % G;
+                const int rb = (t / G) * CM + m_sub, g = t % G;
                 const int m0 = rb * kBlockM;
                 const int n0 = (g * C + int(rank)) * ns;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const uint32_t s = it % uint32_t(stages);
                     const uint32_t ph = (it / uint32_t(stages)) & 1u;
+                    // every CTA that reads this stage has released it
                     ptx::mbar_wait_bounded(B.empty0 + 8 * s, ph ^ 1u, tmo, abort, a.err, kInfoProducer | s);
                     if (*abort) break;
                     const uint32_t sa = base + L.ring + s * L.stage_bytes;
                     const uint32_t sb = sa + kABytes;
-                    ptx::mbar_arrive_expect_tx(B.full0 + 8 * s, tx);
-                    ptx::tma_load_2d(sa, &a.tmap_x, B.full0 + 8 * s, kb * kBK, m0);
-                    for (int j = 0; j < ns / 64; ++j)
-                        ptx::tma_load_2d(sb + j * 8192, &a.tmap_w, B.full0 + 8 * s, n0 + j * 64, kb * kBK);
+                    const uint32_t fb = B.full0 + 8 * s;
+                    if constexpr (kPair) {
+                        // both CTAs' loads complete on the leader's full barrier
+                        const uint32_t fbl = ptx::mapa(fb, pair_leader);
+                        if (is_leader) ptx::mbar_arrive_expect_tx(fb, tx);
+                        ptx::tma_load_2d_pair(sa, &a.tmap_x, fbl, kb * kBK, m0);
+                        // this CTA stages W columns [m_sub * ns/2, +ns/2) of the 256-row MMA's N
+                        for (int j = 0; j < my_boxes; ++j)
+                            ptx::tma_load_2d_pair(sb + j * 8192, &a.tmap_w, fbl, n0 + (m_sub * my_boxes + j) * 64,
+                                                  kb * kBK);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(fb, tx);  // the whole stage, whoever loads it
+                        const uint32_t adst = sa + uint32_t(mcx ? rank : 0u) * uint32_t(a_rows) * 128u;
+                        if (mcx) ptx::tma_load_2d_mc(adst, &a.tmap_x, fb, kb * kBK, m0 + int(rank) * a_rows, a_mask);
+                        else ptx::tma_load_2d(adst, &a.tmap_x, fb, kb * kBK, m0);
+                        for (int j = 0; j < nbox; ++j)
+                            ptx::tma_load_2d(sb + j * 8192, &a.tmap_w, fb, n0 + j * 64, kb * kBK);
+                    }
                     if (kb == 0) trace_tile(a.trace, ptile, CF_TR_TMA_FIRST);
                     if (kb == nk - 1) trace_tile(a.trace, ptile, CF_TR_TMA_LAST);
                 }
                 if (*abort) break;
             }
-            // drain: every load issued has landed before the CTA may exit
+            // drain: every stage this producer filled has been released by all of
+            // its readers (so every load landed and every release signal aimed at
+            // this CTA arrived) before the CTA may exit
             const uint32_t issued = it;
             const uint32_t first = issued > uint32_t(stages) ? issued - uint32_t(stages) : 0u;
             for (uint32_t i = first; i < issued; ++i) {
                 const uint32_t s = i % uint32_t(stages);
                 const uint32_t ph = (i / uint32_t(stages)) & 1u;
-                uint32_t dummy = 0;
                 volatile uint32_t local_abort = 0;
-                ptx::mbar_wait_bounded(B.full0 + 8 * s, ph, tmo, &local_abort, nullptr, 0);
-                (void)dummy;
+                ptx::mbar_wait_bounded(B.empty0 + 8 * s, ph, tmo, &local_abort, nullptr, 0);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(ns);
+        if (lane == 0 && is_leader) {
+            const uint32_t idesc = idesc_bf16(kPair ? 2 * kBlockM : kBlockM, ns);
+            const uint16_t pair_mask = uint16_t(3u << pair_leader);
             uint32_t it = 0;
             int tile = 0;
             for (int t = cid; t < T; t += ncl, ++tile) {
@@ -357,17 +398,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         // B: MN-major, 64-column blocks 8 KB apart, 8-row K groups 1 KB apart;
                         // advance 16 K rows = 2 KB
                         const uint64_t bd = sw128_desc(sb + k * 2048, 8192, 1024);
-                        ptx::mma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        if constexpr (kPair) ptx::mma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        else ptx::mma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
-                    ptx::mma_commit(B.empty0 + 8 * s);  // stage free once these MMAs completed
+                    // the stage is free once these MMAs completed: tell every CTA whose
+                    // producer filled it
+                    if constexpr (kPair) ptx::mma_commit_pair_mc(B.empty0 + 8 * s, pair_mask);
+                    else if (a_mask != (1u << crank)) ptx::mma_commit_mc(B.empty0 + 8 * s, a_mask);
+                    else ptx::mma_commit(B.empty0 + 8 * s);
                 }
                 if (*abort) break;
-                ptx::mma_commit(B.tmem_full0 + 8 * buf);  // accumulator ready
+                // accumulator ready (pair: in both CTAs' tensor memory)
+                if constexpr (kPair) ptx::mma_commit_pair_mc(B.tmem_full0 + 8 * buf, pair_mask);
+                else ptx::mma_commit(B.tmem_full0 + 8 * buf);
                 trace_tile(a.trace, tile, CF_TR_MMA_DONE);
                 trace_tile_value(a.trace, tile, CF_TR_MMA_WAIT_NS, waited);
             }
             // every MMA issued has completed before TMEM may be released
-            ptx::mma_commit(B.mma_done);
+            if constexpr (kPair) ptx::mma_commit_pair_mc(B.mma_done, uint16_t(1u << crank));
+            else ptx::mma_commit(B.mma_done);
             volatile uint32_t local_abort = 0;
             ptx::mbar_wait_bounded(B.mma_done, 0, tmo, &local_abort, nullptr, 0);
         }
@@ -391,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
 
         int tile = 0;
         for (int t = cid; t < T; t += ncl, ++tile) {
-            const int rb = t / G, g = t % G;
+            const int rb = (t / G) * CM + m_sub, g = t % G;
             const int m0 = rb * kBlockM;
             const int ncta = (g * C + int(rank)) * ns;  // first global column of this CTA's tile
             const int hc0 = h * half;                   // first tile column of this thread's half
@@ -497,11 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                     if (!a.leader) {
                         ptx::mbar_arrive_expect_tx(xfull, uint32_t(C) * 1024u);
                         for (int r = 0; r < C; ++r)
-                            ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, r), src, 1024, ptx::mapa(xfull, r));
+                            ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, r * CM + m_sub), src, 1024,
+                                                     ptx::mapa(xfull, r * CM + m_sub));
                     } else {
                         if (rank == 0) ptx::mbar_arrive_expect_tx(xfull, uint32_t(C) * 1024u);
                         else ptx::mbar_arrive_expect_tx(B.xres0 + 8 * xp, 1024u);
-                        ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, 0), src, 1024, ptx::mapa(xfull, 0));
+                        ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, m_sub), src, 1024, ptx::mapa(xfull, m_sub));
                     }
                 }
             }
@@ -519,7 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         if (et0 && !*abort) {
                             const uint32_t src = base + L.res + xp * 1024;
                             for (int r = 1; r < C; ++r)
-                                ptx::bulk_copy_s2cluster(ptx::mapa(src, r), src, 1024, ptx::mapa(B.xres0 + 8 * xp, r));
+                                ptx::bulk_copy_s2cluster(ptx::mapa(src, r * CM + m_sub), src, 1024,
+                                                         ptx::mapa(B.xres0 + 8 * xp, r * CM + m_sub));
                         }
                     }
                     ptx::named_bar_sync(kBarEpi, kEpiThreads);
@@ -530,13 +581,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             }
             if (et0) trace_tile(a.trace, tile, CF_TR_EPI_CLUSTER);
 
-            // ---------------- level 4: rows wider than a cluster (global partials)
+            // ---------------- level 4: rows wider than a cluster (global partials).
+            // Layout [row block][row][Gp] float2 (Gp = G rounded up to even): the G
+            // partials of one row are contiguous, so a row's reader fetches them
+            // with independent 16-byte loads, 8 partials in flight at a time.
             if (G > 1) {
                 uint32_t *cnt = a.counters + rb;
-                uint32_t *dep = a.counters + a.row_blocks + rb;
-                float2 *pbase = a.partials + (size_t(rb) * G) * 128;
+                uint32_t *dep = a.counters + a.row_blocks_alloc + rb;
+                const int Gp = G + (G & 1);
+                float2 *prow = a.partials + (size_t(rb) * 128 + row) * Gp;
                 if (rank == 0 && h == 0) {
-                    pbase[g * 128 + row] = stat;
+                    prow[g] = stat;
                     // the 128 writes happen before the barrier; the release arrive
                     // below publishes all of them
                     ptx::named_bar_sync(kBarHalf0, 128);
@@ -564,16 +619,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                     }
                 }
                 ptx::named_bar_sync(kBarEpi, kEpiThreads);
-                float2 s2 = ptx::ld_relaxed_gpu_f2(pbase + row);
-                for (int gg = 1; gg < G; ++gg) {
-                    const float2 o = ptx::ld_relaxed_gpu_f2(pbase + gg * 128 + row);
-                    if constexpr (EPI == EPI_SOFTMAX) {
-                        const MaxSum m = combine_maxsum(MaxSum{s2.x, s2.y}, MaxSum{o.x, o.y});
-                        s2 = make_float2(m.m, m.s);
-                    } else {
-                        const float nc = float(ns * C);
-                        const MeanM2 m = combine_counts(MeanM2{s2.x, s2.y}, float(gg) * nc, MeanM2{o.x, o.y}, nc);
-                        s2 = make_float2(m.mean, m.m2);
+                const float nc = float(ns * C);  // columns behind each partial
+                float2 s2 = make_float2(0.f, 0.f);
+                for (int g0 = 0; g0 < G; g0 += 8) {
+                    float4 v[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (g0 + 2 * i < G) v[i] = ptx::ld_relaxed_gpu_f4(prow + g0 + 2 * i);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int gg = g0 + i;
+                        if (gg >= G) break;
+                        const float2 o = (i & 1) ? make_float2(v[i >> 1].z, v[i >> 1].w)
+                                                 : make_float2(v[i >> 1].x, v[i >> 1].y);
+                        if (gg == 0) {
+                            s2 = o;
+                        } else if constexpr (EPI == EPI_SOFTMAX) {
+                            const MaxSum m = combine_maxsum(MaxSum{s2.x, s2.y}, MaxSum{o.x, o.y});
+                            s2 = make_float2(m.m, m.s);
+                        } else {
+                            const MeanM2 m = combine_counts(MeanM2{s2.x, s2.y}, float(gg) * nc, MeanM2{o.x, o.y}, nc);
+                            s2 = make_float2(m.mean, m.m2);
+                        }
                     }
                 }
                 stat = s2;
@@ -644,10 +711,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                     }
                 }
             }
-            // accumulator buffer free for the MMA of tile + 2
+            // accumulator buffer free for the MMA of tile + 2 (pair: tell the leader)
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(B.tmem_empty0 + 8 * buf);
+            if (lane == 0) {
+                if (kPair) ptx::mbar_arrive_cluster(ptx::mapa(B.tmem_empty0 + 8 * buf, pair_leader));
+                else ptx::mbar_arrive(B.tmem_empty0 + 8 * buf);
+            }
             if (et0) trace_tile(a.trace, tile, CF_TR_EPI_STORED);
         }
         // every bulk store of this warp has completed before the CTA may leave
@@ -662,31 +732,61 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     ptx::tc_fence_after();
     // no CTA leaves while a peer may still access its shared memory
     ptx::cluster_sync();
-    if (warp == 1) ptx::tmem_dealloc(tmem_base, tmem_cols);
+    if (warp == 1) {
+        if constexpr (kPair) ptx::tmem_dealloc_pair(tmem_base, tmem_cols);
+        else ptx::tmem_dealloc(tmem_base, tmem_cols);
+    }
     if (threadIdx.x == 64) trace_stamp(a.trace, 3);
 }
 
-void *kernel_for(int kind) {
+void *kernel_for(int kind, bool pair) {
     switch (kind) {
-        case EPI_LN: return reinterpret_cast<void *>(&gemm_fused_kernel<EPI_LN>);
-        case EPI_GELU_LN: return reinterpret_cast<void *>(&gemm_fused_kernel<EPI_GELU_LN>);
-        case EPI_SOFTMAX: return reinterpret_cast<void *>(&gemm_fused_kernel<EPI_SOFTMAX>);
+        case EPI_LN:
+            return pair ? reinterpret_cast<void *>(&gemm_fused_kernel<EPI_LN, true>)
+                        : reinterpret_cast<void *>(&gemm_fused_kernel<EPI_LN, false>);
+        case EPI_GELU_LN:
+            return pair ? reinterpret_cast<void *>(&gemm_fused_kernel<EPI_GELU_LN, true>)
+                        : reinterpret_cast<void *>(&gemm_fused_kernel<EPI_GELU_LN, false>);
+        case EPI_SOFTMAX:
+            return pair ? reinterpret_cast<void *>(&gemm_fused_kernel<EPI_SOFTMAX, true>)
+                        : reinterpret_cast<void *>(&gemm_fused_kernel<EPI_SOFTMAX, false>);
         default: return nullptr;
     }
 }
 
-}  // namespace
-
-int gemm_fused_smem_bytes(int stages, int cluster, int n_slice) {
-    return int(smem_layout(stages, cluster, n_slice).total) + 1024;  // + alignment slack
+// Function attributes are set once per (device, kernel) to the largest
+// shared-memory size seen, so launches made under stream capture issue no
+// attribute calls.
+cudaError_t ensure_attributes(int variant, void *fn, int smem) {
+    static int set_smem[64][6] = {};
+    static bool nonportable[64][6] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || variant < 0 || variant >= 6) return cudaErrorInvalidValue;
+    if (smem > set_smem[dev][variant]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        set_smem[dev][variant] = smem;
+    }
+    if (!nonportable[dev][variant]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        nonportable[dev][variant] = true;
+    }
+    return cudaSuccess;
 }
 
-static cudaError_t ensure_attributes(int kind, void *fn, int smem);
+}  // namespace
 
-int gemm_fused_max_active_clusters(int kind, int cluster, int smem) {
-    void *fn = kernel_for(kind);
+int gemm_fused_smem_bytes(int stages, int cluster, int n_slice, bool pair) {
+    return int(smem_layout(stages, cluster, n_slice, pair).total) + 1024;  // + alignment slack
+}
+
+int gemm_fused_max_active_clusters(int kind, bool pair, int cluster, int smem) {
+    void *fn = kernel_for(kind, pair);
     if (!fn) return 0;
-    if (ensure_attributes(kind, fn, smem) != cudaSuccess) {
+    if (ensure_attributes(kind * 2 + (pair ? 1 : 0), fn, smem) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
@@ -709,43 +809,21 @@ int gemm_fused_max_active_clusters(int kind, int cluster, int smem) {
     return n;
 }
 
-// Function attributes are set once per (device, kernel) to the largest
-// shared-memory size seen, so launches made under stream capture issue no
-// attribute calls.
-static cudaError_t ensure_attributes(int kind, void *fn, int smem) {
-    static int set_smem[64][3] = {};
-    static bool nonportable[64][3] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (smem > set_smem[dev][kind]) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        set_smem[dev][kind] = smem;
-    }
-    if (!nonportable[dev][kind]) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        nonportable[dev][kind] = true;
-    }
-    return cudaSuccess;
-}
-
 cudaError_t launch_gemm_fused(int kind, const GemmArgs &a, int clusters, int stages, int smem,
                               cudaStream_t stream) {
-    void *fn = kernel_for(kind);
+    const bool pair = a.cluster_m == 2;
+    void *fn = kernel_for(kind, pair);
     if (!fn) return cudaErrorInvalidValue;
-    cudaError_t e = ensure_attributes(kind, fn, smem);
+    cudaError_t e = ensure_attributes(kind * 2 + (pair ? 1 : 0), fn, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(clusters * a.cluster);
+    cfg.gridDim = dim3(clusters * a.cluster * a.cluster_m);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = a.cluster;
+    attr[0].val.clusterDim.x = a.cluster * a.cluster_m;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;

@@ -73,19 +73,30 @@ def test_plan_forced_single_cluster_rows():
     assert p.smem_bytes <= 232448 and p.stages >= 2
 
 
-def test_plan_chooses_most_useful_sm_time():
-    """The automatic choice maximises row_blocks*cpr/(ceil(T/ncl)*SMs) (x0.97, or x0.85
-    for K < 512, when the row needs the global barrier); larger clusters win ties."""
+def test_plan_chooses_fastest_predicted():
+    """The automatic choice minimises the planner's time model: ceil(T/ncl) tiles per
+    CTA, each max(mainloop, epilogue), plus one exposed epilogue."""
     cases = {
-        (4096, 2048, 128): (4, 2, 36),      # cluster 8 would leave 32 SMs idle and run 3 tiles deep
-        (16384, 4096, 4096): (2, 8, 76),
-        (8192, 16384, 2048): (2, 32, 76),
-        (128, 512, 256): (2, 1, 1),
+        (4096, 2048, 128): (8, 1, 1, 15),     # whole row in one cluster of 8; K too short for pairs
+        (16384, 4096, 4096): (1, 2, 16, 76),  # CTA pairs (cta_group::2), rows over 16 clusters
+        (8192, 16384, 2048): (2, 2, 32, 36),  # CTA pairs, rows over 32 clusters
+        (128, 512, 256): (2, 1, 1, 1),        # one row block: no pair
     }
-    for (M, N, K), (C, G, ncl) in cases.items():
+    for (M, N, K), (C, CM, G, ncl) in cases.items():
         st, p = cf.cf_plan_gemm_fused(M, N, K, 152, GB300)
         assert st == cf.CF_OK
-        assert (p.cluster_size, p.groups, p.clusters) == (C, G, ncl), (M, N, K, p.as_dict())
+        assert (p.cluster_size, p.cluster_m, p.groups, p.clusters) == (C, CM, G, ncl), (M, N, K, p.as_dict())
+        assert p.smem_bytes <= 232448
+
+
+def test_plan_pair_mode_limits():
+    # pairs need two row blocks and tiles of at least 128 columns
+    st, p = cf.cf_plan_gemm_fused(128, 4096, 4096, 152, GB300, cf.tuning(cluster_m=2))
+    assert st == cf.CF_ERR_NOT_RESIDENT
+    st, p = cf.cf_plan_gemm_fused(4096, 4096, 4096, 152, GB300, cf.tuning(cluster_m=2, n_slice=64))
+    assert st == cf.CF_ERR_NOT_RESIDENT
+    st, p = cf.cf_plan_gemm_fused(4096, 4096, 4096, 152, GB300, cf.tuning(cluster_m=2, n_slice=128))
+    assert st == cf.CF_OK and p.cluster_m == 2 and p.stages == 6
 
 
 def test_plan_leader_mode_above_threshold():
@@ -134,9 +145,11 @@ def test_plan_shapes():
 
 
 def test_workspace_sizes():
-    # error word + counters + one float2 per row and 64-column group
-    assert cf.cf_gemm_fused_workspace_size(8192, 16384, 2048) == 256 + 512 + 64 * 256 * 128 * 8
+    # error word + counters + one float2 per row and 64-column group (rounded up to even)
+    assert cf.cf_gemm_fused_workspace_size(8192, 16384, 2048) == 256 + 512 + 64 * 257 * 128 * 8
     assert cf.cf_gemm_fused_workspace_size(0, 512, 256) == 256 + 0
+    # an odd row-block count is padded to whole CTA pairs
+    assert cf.cf_gemm_fused_workspace_size(129, 512, 256) == 256 + 256 + 2 * 9 * 128 * 8
     assert cf.cf_stitch_workspace_size(750000, 32) == 256
 
 
