@@ -90,9 +90,9 @@ int max_active_cached(int device, int kind, bool pair, int cluster, int smem) {
     return n;
 }
 
-int gemm_stages_for(int n_slice, int cluster, int requested, bool pair) {
+int gemm_stages_for(int n_slice, int cluster, int requested, bool pair, bool leader) {
     int s = requested > 0 ? requested : 6;
-    while (s > 2 && cf::gemm_fused_smem_bytes(s, cluster, n_slice, pair) > kMaxSmem) --s;
+    while (s > 2 && cf::gemm_fused_smem_bytes(s, cluster, n_slice, pair, leader) > kMaxSmem) --s;
     return s;
 }
 
@@ -180,15 +180,16 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
     // Choose C_N (CTAs along a row, a divisor of the CTAs per row) and C_M (row
     // blocks per cluster: 2 = CTA pairs sharing one cta_group::2 MMA stream) by
     // predicted time.  The persistent grid holds ncl clusters (never more than
-    // can be resident); each takes ceil(T / ncl) of T = ceil(row_blocks / C_M) * G
-    // tickets, one tile per CTA each.  A tile costs max(mainloop, epilogue):
-    // the TMEM double buffer overlaps one tile's epilogue with the next tile's
-    // mainloop.  The constants were measured on GB300 with the device trace
-    // (tensor-bound workloads, 128x256 tiles per CTA):
+    // can be resident); each takes per = ceil(T / ncl) of T = ceil(row_blocks /
+    // C_M) * G tickets, one tile per CTA each.  With two TMEM accumulators and
+    // two epilogue groups, tiles go in rounds of two: a round costs
+    // max(2 mainloops, one epilogue).  Constants measured on GB300 with the
+    // device trace (128x256 tiles per CTA):
     //   mainloop  ~ 0.48 us per 64-deep k-block for a CTA pair, 0.55 us single
-    //   epilogue  ~ 4.5 us, plus 4 + 0.2 G us when the row spans G > 1 clusters
-    //               (the global barrier waits for the slowest of G clusters),
-    //               plus 0.5 us for a CTA pair when K < 512
+    //   epilogue  ~ 4.5 us; + 1.5 + 0.2 G us when the row spans G > 1 clusters
+    //               (the global barrier waits for the slowest of G clusters);
+    //               + 0.5 us for a CTA pair when K < 512
+    //   skew      ~ 0.05 G us per tile when G > 1
     // Rows wider than one row group need all G clusters of a row block
     // resident (ncl >= G).
     auto predict = [&](int cn, int cm, int *ncl_out) -> double {
@@ -203,10 +204,9 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
         if (T < n) n = int(T);
         const int64_t per = (T + n - 1) / n;
         const double t_main = nk * (cm == 2 ? 0.48 : 0.55) * (ns / 256.0);
-        // a pair's coupled pipelines cost latency that only long K loops repay
-        const double t_epi = 4.5 + (g > 1 ? 4.0 + 0.2 * g : 0.6) + (cm == 2 && nk < 8 ? 0.5 : 0.0);
+        const double t_epi = 4.5 + (g > 1 ? 1.5 + 0.2 * g : 0.0) + (cm == 2 && nk < 8 ? 0.5 : 0.0);
         *ncl_out = n;
-        return double(per) * std::max(t_main, t_epi) + t_epi;
+        return double((per + 1) / 2) * std::max(2.0 * t_main, t_epi) + t_main + (g > 1 ? per * 0.05 * g : 0.0);
     };
     int C = 0, CMs = 0, ncl = 0;
     {
@@ -240,8 +240,8 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
     plan->leader_mode = (peer_max < 0 || C > peer_max) ? 1 : 0;
     plan->row_blocks = rb;
     plan->clusters = std::max(ncl, 1);
-    plan->stages = gemm_stages_for(ns, C, t.stages, CMs == 2);
-    plan->smem_bytes = cf::gemm_fused_smem_bytes(plan->stages, C, ns, CMs == 2);
+    plan->stages = gemm_stages_for(ns, C, t.stages, CMs == 2, plan->leader_mode != 0);
+    plan->smem_bytes = cf::gemm_fused_smem_bytes(plan->stages, C, ns, CMs == 2, plan->leader_mode != 0);
     plan->cluster_m = CMs;
     if (plan->smem_bytes > kMaxSmem) return CF_ERR_UNSUPPORTED;
     return CF_OK;
@@ -373,8 +373,8 @@ static cf_status device_plan(int kind, int64_t M, int64_t N, int64_t K, const cf
         const bool as_pair = (c % 2 == 0) && (cpr % (c / 2) == 0) && ns >= 128;
         if (!as_cn && !as_pair) continue;
         const int cn = as_cn ? c : c / 2;
-        const int st = gemm_stages_for(ns, cn, t.stages, !as_cn);
-        const int smem = cf::gemm_fused_smem_bytes(st, cn, ns, !as_cn);
+        const int st = gemm_stages_for(ns, cn, t.stages, !as_cn, true);
+        const int smem = cf::gemm_fused_smem_bytes(st, cn, ns, !as_cn, true);
         if (smem > std::min(kMaxSmem, dev.max_smem_optin)) continue;
         active[c] = max_active_cached(dev.device, kind, !as_cn, c, smem);
     }

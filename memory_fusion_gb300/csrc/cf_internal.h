@@ -85,8 +85,8 @@ struct GemmArgs {
 };
 
 // dynamic shared memory of one CTA for a ring of `stages`, a row group of
-// `cluster` CTAs, and the CTA-pair MMA mode or not
-int gemm_fused_smem_bytes(int stages, int cluster, int n_slice, bool pair);
+// `cluster` CTAs, the CTA-pair MMA mode or not, leader-follower or peer exchange
+int gemm_fused_smem_bytes(int stages, int cluster, int n_slice, bool pair, bool leader);
 
 // Query max co-resident clusters of `cluster` CTAs (total) for the fused
 // kernel of `kind` and mode with `smem` dynamic shared memory (0 if it cannot

@@ -57,14 +57,13 @@ __device__ __forceinline__ void trace_tile_value(unsigned long long *tr, int til
 }
 
 constexpr int kThreads = 320;      // 10 warps
-constexpr int kEpiWarps = 8;       // warps 2..9
-constexpr int kEpiThreads = 256;
+constexpr int kEpiWarps = 8;       // warps 2..9: two groups of 4
+constexpr int kGroupWarps = 4;     // one group: all 128 TMEM lanes (rows) of a tile
+constexpr int kGroupThreads = 128;
 constexpr int kBK = 64;            // K per stage (128 bytes of bf16: one swizzle atom)
 constexpr int kABytes = kBlockM * kBK * 2;  // 16 KB
 
-// named barriers (0 is __syncthreads)
-constexpr uint32_t kBarEpi = 1;    // all 256 epilogue threads
-constexpr uint32_t kBarHalf0 = 2;  // epilogue half 0 (columns [0, n_slice/2))
+// named barriers (0 is __syncthreads): 1 + g for epilogue group g
 
 // error info codes for the bounded pipeline waits
 constexpr uint32_t kInfoProducer = 0x10000000u;
@@ -77,16 +76,17 @@ struct SmemLayout {
     uint32_t stage_bytes;  // A + B of one stage
     uint32_t ring;         // offset of the operand ring (1024-aligned)
     uint32_t stg;          // bf16 output staging, 2 KiB per epilogue warp (64B swizzle)
-    uint32_t send;         // float2 [2][128]
-    uint32_t slot;         // float2 [2][C][128]
-    uint32_t res;          // float2 [2][128]
-    uint32_t red;          // float2 [128]
-    uint32_t prm;          // float [2][3][256]: bias, gamma, beta of the tile's columns
+    uint32_t send;         // float2 [4][128]: this CTA's partial, by exchange set
+    uint32_t slot;         // float2 [4][C][128]: the row group's partials, by exchange set
+    uint32_t res;          // float2 [4][128]: leader-follower result, by exchange set
+    uint32_t prm;          // float [2][3][256]: bias, gamma, beta of the tile's columns, per group
     uint32_t bars;         // mbarriers
     uint32_t total;        // bytes from the aligned base
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n_slice, bool pair) {
+constexpr int kXSets = 4;  // exchange buffer sets (tile mod 4)
+
+__host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n_slice, bool pair, bool leader) {
     SmemLayout L;
     // a CTA of a pair stages its own 128 rows of X and half of the tile's W columns
     L.stage_bytes = kABytes + uint32_t(pair ? n_slice / 2 : n_slice) * kBK * 2;
@@ -94,14 +94,14 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n
     uint32_t off = L.ring + uint32_t(stages) * L.stage_bytes;
     L.stg = off;
     off += kEpiWarps * 2048;
+    // exchange buffers exist only when a row group has more than one CTA
+    const uint32_t xc = cluster > 1 ? 1u : 0u;
     L.send = off;
-    off += 2 * 128 * 8;
+    off += xc * kXSets * 128 * 8;
     L.slot = off;
-    off += 2 * uint32_t(cluster) * 128 * 8;
-    L.res = off;
-    off += 2 * 128 * 8;
-    L.red = off;
-    off += 128 * 8;
+    off += xc * kXSets * uint32_t(cluster) * 128 * 8;
+    L.res = off;  // the leader-follower result (not used by peer all-to-all)
+    off += (leader ? xc : 0u) * kXSets * 128 * 8;
     L.prm = off;
     off += 2 * 3 * 256 * 4;
     L.bars = off;
@@ -112,9 +112,9 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n
 
 // barrier slots inside L.bars (8 bytes each)
 struct Bars {
-    uint32_t full0, empty0;  // [stages] each
+    uint32_t full0, empty0;            // [stages] each
     uint32_t tmem_full0, tmem_empty0;  // [2]
-    uint32_t xfull0, xres0;            // [2]
+    uint32_t xfull0, xres0;            // [kXSets]
     uint32_t mma_done;
     uint32_t misc;  // u32: tmem base, u32: abort flag
 };
@@ -126,8 +126,8 @@ __device__ __forceinline__ Bars bars_at(uint32_t base, int stages) {
     b.tmem_full0 = base + 16 * stages;
     b.tmem_empty0 = b.tmem_full0 + 16;
     b.xfull0 = b.tmem_empty0 + 16;
-    b.xres0 = b.xfull0 + 16;
-    b.mma_done = b.xres0 + 16;
+    b.xres0 = b.xfull0 + 8 * kXSets;
+    b.mma_done = b.xres0 + 8 * kXSets;
     b.misc = b.mma_done + 8;
     return b;
 }
@@ -228,10 +228,16 @@ __device__ __forceinline__ float2 combine_slots(const float2 *s, int C, float n_
 
 template <int EPI, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_constant__ GemmArgs a, int stages) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = ptx::smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *const gbase = smem_raw + (base - raw);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = ptx::smem_u32(smem_raw);
+    uint8_t *const gbase = smem_raw;
+    // The 128B-swizzled operand tiles need a 1024-byte aligned ring.  The
+    // dynamic shared window starts aligned; if it ever did not, report it and
+    // do nothing (every CTA sees the same base, so none enters a cluster barrier).
+    if ((base & 1023u) != 0u) {
+        if (threadIdx.x == 0) ptx::record_error(a.err, 8u /*CF_ERR_DEVICE_BOUNDS*/, 0x60000000u | (base & 1023u));
+        return;
+    }
 
     const int C = a.cluster;                // C_N: CTAs of one row group
     const int CM = kPair ? 2 : 1;           // row blocks per cluster
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     const int T = a.super_blocks * G;       // tickets: (super row block, cluster group), row-block major
     const int nbox = ns / 64;               // 64-column W boxes of a tile
     const int my_boxes = kPair ? nbox / 2 : nbox;  // W boxes staged in this CTA
-    const SmemLayout L = smem_layout(stages, C, ns, kPair);
+    const SmemLayout L = smem_layout(stages, C, ns, kPair, a.leader != 0);
     const Bars B = bars_at(base + L.bars, stages);
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + (B.misc - base));
     volatile uint32_t *abort = misc + 1;
@@ -275,10 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(B.tmem_full0 + 8 * b, 1);
-            // the pair leader waits for both CTAs' epilogue warps
-            ptx::mbar_init(B.tmem_empty0 + 8 * b, kPair ? 2 * kEpiWarps : kEpiWarps);
-            ptx::mbar_init(B.xfull0 + 8 * b, 1);
-            ptx::mbar_init(B.xres0 + 8 * b, 1);
+            // one epilogue group (4 warps) drains each accumulator; the pair
+            // leader waits for both CTAs' groups
+            ptx::mbar_init(B.tmem_empty0 + 8 * b, kPair ? 2 * kGroupWarps : kGroupWarps);
+        }
+        for (int x = 0; x < kXSets; ++x) {
+            ptx::mbar_init(B.xfull0 + 8 * x, 1);
+            ptx::mbar_init(B.xres0 + 8 * x, 1);
         }
         ptx::mbar_init(B.mma_done, 1);
         misc[1] = 0u;
@@ -423,75 +432,75 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        const int e = warp - 2;              // 0..7
-        const int q = warp & 3;              // TMEM lane quadrant this warp may access
-        const int h = e >> 2;                // column half of the tile
-        const int row = q * 32 + lane;       // row of the tile == TMEM lane
-        const int et = threadIdx.x - 64;     // 0..255
-        const bool et0 = (et == 0);
+        // Two groups of 4 warps take alternate tiles (PingPong over the two TMEM
+        // accumulators): while one group waits on an exchange or the global
+        // barrier, the other streams its tile.  Warp w of a group reads TMEM
+        // lane quadrant w % 4, so thread = one row, all n_slice columns.
+        const int e = warp - 2;               // 0..7
+        const int grp = e >> 2;               // epilogue group = accumulator buffer
+        const int q = warp & 3;               // TMEM lane quadrant this warp may access
+        const int row = q * 32 + lane;        // row of the tile == TMEM lane
+        const int gt = (e & 3) * 32 + lane;   // thread index within the group
+        const bool gt0 = (gt == 0);
+        const uint32_t bar_grp = 1u + uint32_t(grp);
         float2 *const send = reinterpret_cast<float2 *>(gbase + L.send);
         float2 *const slot = reinterpret_cast<float2 *>(gbase + L.slot);
         float2 *const res = reinterpret_cast<float2 *>(gbase + L.res);
-        float2 *const red = reinterpret_cast<float2 *>(gbase + L.red);
-        float *const prm = reinterpret_cast<float *>(gbase + L.prm);
+        float *const prm = reinterpret_cast<float *>(gbase + L.prm) + grp * 768;
         const uint32_t stg = base + L.stg + uint32_t(e) * 2048u;  // this warp's staging buffer
         const float fN = float(a.N);
-        const int nchunks = half / 32;  // 1, 2 or 4 fragments of 32 columns per thread
+        const int nchunks = ns / 32;  // 2, 4 or 8 fragments of 32 columns per thread
+        float *const pb = prm;        // bias, gamma, beta of this group's current tile
+        float *const pg = prm + 256;
+        float *const pe = prm + 512;
 
-        int tile = 0;
-        for (int t = cid; t < T; t += ncl, ++tile) {
+        int tile = grp;
+        for (int t = cid + grp * ncl; t < T; t += 2 * ncl, tile += 2) {
             const int rb = (t / G) * CM + m_sub, g = t % G;
             const int m0 = rb * kBlockM;
             const int ncta = (g * C + int(rank)) * ns;  // first global column of this CTA's tile
-            const int hc0 = h * half;                   // first tile column of this thread's half
-            const uint32_t buf = tile & 1;
+            const uint32_t buf = uint32_t(grp);
             const uint32_t tph = (uint32_t(tile) >> 1) & 1u;
-            const uint32_t xp = buf;  // exchange buffer set
-            const uint32_t xph = tph;
+            const uint32_t xs = uint32_t(tile) & 3u;    // exchange buffer set
+            const uint32_t xph = (uint32_t(tile) >> 2) & 1u;
 
-            // Row-vector parameters of the tile's columns into shared memory, fetched
-            // before the accumulator is ready (double-buffered by tile parity: set `buf`
-            // is rewritten two tiles later, after every thread passed the next tile's
-            // parameter barrier).
-            float *const pb = prm + buf * 768;
-            float *const pg = pb + 256;
-            float *const pe = pb + 512;
-            if (et < ns) {
-                pb[et] = a.bias ? __ldg(a.bias + ncta + et) : 0.f;
+            // Row-vector parameters of the tile's columns into this group's shared
+            // buffer, fetched before the accumulator is ready; the group's previous
+            // tile finished reading them before the group barrier that ended it.
+            for (int c = gt; c < ns; c += kGroupThreads) {
+                pb[c] = a.bias ? __ldg(a.bias + ncta + c) : 0.f;
                 if constexpr (EPI != EPI_SOFTMAX) {
-                    pg[et] = __ldg(a.gamma + ncta + et);
-                    pe[et] = __ldg(a.beta + ncta + et);
+                    pg[c] = __ldg(a.gamma + ncta + c);
+                    pe[c] = __ldg(a.beta + ncta + c);
                 }
             }
             ptx::mbar_wait_bounded(B.tmem_full0 + 8 * buf, tph, tmo, abort, a.err, kInfoEpi | buf);
             ptx::tc_fence_after();
-            ptx::named_bar_sync(kBarEpi, kEpiThreads);  // parameters visible to every epilogue thread
-            if (et0) trace_tile(a.trace, tile, CF_TR_EPI_START);
-            const uint32_t tacc = tmem_base + (uint32_t(q * 32) << 16) + buf * uint32_t(ns) + uint32_t(hc0);
+            ptx::named_bar_sync(bar_grp, kGroupThreads);  // parameters visible to the group
+            if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_START);
+            const uint32_t tacc = tmem_base + (uint32_t(q * 32) << 16) + buf * uint32_t(ns);
 
             // ---------------- stage 1: compute phase + thread-local aggregation.
             // Fragments of 32 columns stream out of TMEM two at a time; the stage-1
-            // value is written back in place for the PostOp (bypass path).
-            float2 part;     // LN: (mean, M2) over `half` columns; softmax: (max, sum exp)
-            float mrun[4];   // softmax: running max when each fragment's exps were taken
+            // value is written back in place for the PostOp (bypass path).  The
+            // thread's statistic covers the CTA's whole row slice.
+            float2 part;     // LN: (mean, M2) over n_slice columns; softmax: (max, sum exp)
+            float mrun[8];   // softmax: running max when each fragment's exps were taken
             if constexpr (EPI == EPI_SOFTMAX) {
                 float m = neg_inf(), ssum = 0.f;
 #pragma unroll
-                for (int c = 0; c < 4; c += 2) {
+                for (int c = 0; c < 8; c += 2) {
                     if (c < nchunks) {
                         uint32_t v0[32], v1[32];
-                        const bool two = (c + 1 < nchunks);
                         ptx::tmem_ld32(tacc + c * 32, v0);
-                        if (two) ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
+                        ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
                         ptx::tmem_ld_wait();
-                        softmax_fragment(v0, pb + hc0 + c * 32, a.alpha, m, ssum);
+                        softmax_fragment(v0, pb + c * 32, a.alpha, m, ssum);
                         mrun[c] = m;
                         ptx::tmem_st32(tacc + c * 32, v0);
-                        if (two) {
-                            softmax_fragment(v1, pb + hc0 + (c + 1) * 32, a.alpha, m, ssum);
-                            mrun[c + 1] = m;
-                            ptx::tmem_st32(tacc + (c + 1) * 32, v1);
-                        }
+                        softmax_fragment(v1, pb + (c + 1) * 32, a.alpha, m, ssum);
+                        mrun[c + 1] = m;
+                        ptx::tmem_st32(tacc + (c + 1) * 32, v1);
                     }
                 }
                 ptx::tmem_st_wait();
@@ -499,87 +508,73 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             } else {
                 MeanM2 acc{0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < 4; c += 2) {
+                for (int c = 0; c < 8; c += 2) {
                     if (c < nchunks) {
                         uint32_t v0[32], v1[32];
-                        const bool two = (c + 1 < nchunks);
                         ptx::tmem_ld32(tacc + c * 32, v0);
-                        if (two) ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
+                        ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
                         ptx::tmem_ld_wait();
-                        const MeanM2 c0 = ln_fragment<EPI == EPI_GELU_LN>(v0, pb + hc0 + c * 32, a.alpha);
+                        const MeanM2 c0 = ln_fragment<EPI == EPI_GELU_LN>(v0, pb + c * 32, a.alpha);
                         ptx::tmem_st32(tacc + c * 32, v0);
                         acc = (c == 0) ? c0 : combine_counts(acc, float(32 * c), c0, 32.f);
-                        if (two) {
-                            const MeanM2 c1 = ln_fragment<EPI == EPI_GELU_LN>(v1, pb + hc0 + (c + 1) * 32, a.alpha);
-                            ptx::tmem_st32(tacc + (c + 1) * 32, v1);
-                            acc = combine_counts(acc, float(32 * (c + 1)), c1, 32.f);
-                        }
+                        const MeanM2 c1 = ln_fragment<EPI == EPI_GELU_LN>(v1, pb + (c + 1) * 32, a.alpha);
+                        ptx::tmem_st32(tacc + (c + 1) * 32, v1);
+                        acc = combine_counts(acc, float(32 * (c + 1)), c1, 32.f);
                     }
                 }
                 ptx::tmem_st_wait();
                 part = make_float2(acc.mean, acc.m2);
             }
-            if (et0) trace_tile(a.trace, tile, CF_TR_EPI_STATS);
+            if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_STATS);
 
-            // ---------------- level 2: the two column halves through one shared buffer
-            if (h == 1) red[row] = part;
-            ptx::named_bar_sync(kBarEpi, kEpiThreads);
-            if (h == 0) {
-                const float2 o = red[row];
-                float2 cta;
-                if constexpr (EPI == EPI_SOFTMAX) {
-                    const MaxSum r = combine_maxsum(MaxSum{part.x, part.y}, MaxSum{o.x, o.y});
-                    cta = make_float2(r.m, r.s);
-                } else {
-                    const MeanM2 r = combine_equal(MeanM2{part.x, part.y}, MeanM2{o.x, o.y}, float(half));
-                    cta = make_float2(r.mean, r.m2);
-                }
-                send[xp * 128 + row] = cta;
+            // ---------------- level 2: the CTA statistic of a row is one thread's; it
+            // goes into the unified reduce buffer of this exchange set
+            if (C > 1) {
+                send[xs * 128 + row] = part;
                 ptx::fence_proxy_async_smem();
-                ptx::named_bar_sync(kBarHalf0, 128);
-                if (et0) trace_tile(a.trace, tile, CF_TR_EPI_CTA);
-                // ---------------- level 3: inter-CTA over DSMEM (TMA bulk copies)
-                if (et0 && !*abort) {
-                    const uint32_t src = base + L.send + xp * 1024;
-                    const uint32_t my_slot = base + L.slot + (xp * C + rank) * 1024;
-                    const uint32_t xfull = B.xfull0 + 8 * xp;
-                    if (!a.leader) {
-                        ptx::mbar_arrive_expect_tx(xfull, uint32_t(C) * 1024u);
-                        for (int r = 0; r < C; ++r)
-                            ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, r * CM + m_sub), src, 1024,
-                                                     ptx::mapa(xfull, r * CM + m_sub));
-                    } else {
-                        if (rank == 0) ptx::mbar_arrive_expect_tx(xfull, uint32_t(C) * 1024u);
-                        else ptx::mbar_arrive_expect_tx(B.xres0 + 8 * xp, 1024u);
-                        ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, m_sub), src, 1024, ptx::mapa(xfull, m_sub));
-                    }
+                ptx::named_bar_sync(bar_grp, kGroupThreads);
+            }
+            if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_CTA);
+            // ---------------- level 3: inter-CTA over DSMEM (TMA bulk copies)
+            if (C > 1 && gt0 && !*abort) {
+                const uint32_t src = base + L.send + xs * 1024;
+                const uint32_t my_slot = base + L.slot + (xs * C + rank) * 1024;
+                const uint32_t xfull = B.xfull0 + 8 * xs;
+                if (!a.leader) {
+                    ptx::mbar_arrive_expect_tx(xfull, uint32_t(C) * 1024u);
+                    for (int r = 0; r < C; ++r)
+                        ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, r * CM + m_sub), src, 1024,
+                                                 ptx::mapa(xfull, r * CM + m_sub));
+                } else {
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(xfull, uint32_t(C) * 1024u);
+                    else ptx::mbar_arrive_expect_tx(B.xres0 + 8 * xs, 1024u);
+                    ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, m_sub), src, 1024, ptx::mapa(xfull, m_sub));
                 }
             }
             float2 stat;  // cluster-combined statistic of this row
-            if (!a.leader) {
-                ptx::mbar_wait_bounded<true>(B.xfull0 + 8 * xp, xph, tmo, abort, a.err, kInfoXchg | xp);
-                stat = combine_slots<EPI == EPI_SOFTMAX>(slot + xp * C * 128 + row, C, float(ns));
+            if (C == 1) {
+                stat = part;  // the row group is this CTA alone
+            } else if (!a.leader) {
+                ptx::mbar_wait_bounded<true>(B.xfull0 + 8 * xs, xph, tmo, abort, a.err, kInfoXchg | xs);
+                stat = combine_slots<EPI == EPI_SOFTMAX>(slot + xs * C * 128 + row, C, float(ns));
             } else {
                 if (rank == 0) {
-                    if (h == 0) {
-                        ptx::mbar_wait_bounded<true>(B.xfull0 + 8 * xp, xph, tmo, abort, a.err, kInfoXchg | xp);
-                        res[xp * 128 + row] = combine_slots<EPI == EPI_SOFTMAX>(slot + xp * C * 128 + row, C, float(ns));
-                        ptx::fence_proxy_async_smem();
-                        ptx::named_bar_sync(kBarHalf0, 128);
-                        if (et0 && !*abort) {
-                            const uint32_t src = base + L.res + xp * 1024;
-                            for (int r = 1; r < C; ++r)
-                                ptx::bulk_copy_s2cluster(ptx::mapa(src, r * CM + m_sub), src, 1024,
-                                                         ptx::mapa(B.xres0 + 8 * xp, r * CM + m_sub));
-                        }
+                    ptx::mbar_wait_bounded<true>(B.xfull0 + 8 * xs, xph, tmo, abort, a.err, kInfoXchg | xs);
+                    res[xs * 128 + row] = combine_slots<EPI == EPI_SOFTMAX>(slot + xs * C * 128 + row, C, float(ns));
+                    ptx::fence_proxy_async_smem();
+                    ptx::named_bar_sync(bar_grp, kGroupThreads);
+                    if (gt0 && !*abort) {
+                        const uint32_t src = base + L.res + xs * 1024;
+                        for (int r = 1; r < C; ++r)
+                            ptx::bulk_copy_s2cluster(ptx::mapa(src, r * CM + m_sub), src, 1024,
+                                                     ptx::mapa(B.xres0 + 8 * xs, r * CM + m_sub));
                     }
-                    ptx::named_bar_sync(kBarEpi, kEpiThreads);
                 } else {
-                    ptx::mbar_wait_bounded<true>(B.xres0 + 8 * xp, xph, tmo, abort, a.err, kInfoXchg | 0x10u | xp);
+                    ptx::mbar_wait_bounded<true>(B.xres0 + 8 * xs, xph, tmo, abort, a.err, kInfoXchg | 0x10u | xs);
                 }
-                stat = res[xp * 128 + row];
+                stat = res[xs * 128 + row];
             }
-            if (et0) trace_tile(a.trace, tile, CF_TR_EPI_CLUSTER);
+            if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_CLUSTER);
 
             // ---------------- level 4: rows wider than a cluster (global partials).
             // Layout [row block][row][Gp] float2 (Gp = G rounded up to even): the G
@@ -590,14 +585,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 uint32_t *dep = a.counters + a.row_blocks_alloc + rb;
                 const int Gp = G + (G & 1);
                 float2 *prow = a.partials + (size_t(rb) * 128 + row) * Gp;
-                if (rank == 0 && h == 0) {
+                if (rank == 0) {
                     prow[g] = stat;
                     // the 128 writes happen before the barrier; the release arrive
                     // below publishes all of them
-                    ptx::named_bar_sync(kBarHalf0, 128);
-                    if (et0) ptx::atom_add_release_gpu(cnt, 1u);
+                    ptx::named_bar_sync(bar_grp, kGroupThreads);
+                    if (gt0) ptx::atom_add_release_gpu(cnt, 1u);
                 }
-                if (et0) {
+                if (gt0) {
                     const uint32_t target = uint32_t(G + a.extra_arrivals);
                     const uint64_t t0 = ptx::globaltimer();
                     while (!*abort) {
@@ -618,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         ptx::st_relaxed_gpu(dep, 0u);
                     }
                 }
-                ptx::named_bar_sync(kBarEpi, kEpiThreads);
+                ptx::named_bar_sync(bar_grp, kGroupThreads);
                 const float nc = float(ns * C);  // columns behind each partial
                 float2 s2 = make_float2(0.f, 0.f);
                 for (int g0 = 0; g0 < G; g0 += 8) {
@@ -645,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 }
                 stat = s2;
             }
-            if (et0) trace_tile(a.trace, tile, CF_TR_EPI_GLOBAL);
+            if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_GLOBAL);
 
             // ---------------- stage 2 (PostOp): broadcast the statistic back over the row,
             // bf16 into this warp's staging buffer, TMA bulk store of each 32x32 block
@@ -657,16 +652,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 rstd = rsqrtf(stat.y / fN + a.eps);
             }
 #pragma unroll
-            for (int c = 0; c < 4; c += 2) {
+            for (int c = 0; c < 8; c += 2) {
                 if (c < nchunks) {
                     uint32_t v0[32], v1[32];
-                    const bool two = (c + 1 < nchunks);
                     ptx::tmem_ld32(tacc + c * 32, v0);
-                    if (two) ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
+                    ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
                     ptx::tmem_ld_wait();
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
-                        if (k == 1 && !two) break;
                         uint32_t(&v)[32] = k == 0 ? v0 : v1;
                         const int cc = c + k;
                         uint32_t w[16];
@@ -676,8 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                             for (int j = 0; j < 16; ++j)
                                 w[j] = ptx::pack_bf16x2(__uint_as_float(v[2 * j]) * f, __uint_as_float(v[2 * j + 1]) * f);
                         } else {
-                            const float *gp = pg + hc0 + cc * 32;
-                            const float *bp = pe + hc0 + cc * 32;
+                            const float *gp = pg + cc * 32;
+                            const float *bp = pe + cc * 32;
 #pragma unroll
                             for (int j4 = 0; j4 < 8; ++j4) {
                                 const float4 gm = *reinterpret_cast<const float4 *>(gp + 4 * j4);
@@ -704,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                             ptx::fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                ptx::tma_store_2d(&a.tmap_y, stg, ncta + hc0 + cc * 32, ystore);
+                                ptx::tma_store_2d(&a.tmap_y, stg, ncta + cc * 32, ystore);
                                 ptx::bulk_commit_group();
                             }
                         }
@@ -718,7 +711,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 if (kPair) ptx::mbar_arrive_cluster(ptx::mapa(B.tmem_empty0 + 8 * buf, pair_leader));
                 else ptx::mbar_arrive(B.tmem_empty0 + 8 * buf);
             }
-            if (et0) trace_tile(a.trace, tile, CF_TR_EPI_STORED);
+            // the group's shared parameters may be rewritten for its next tile only
+            // after every thread of the group is done with them
+            ptx::named_bar_sync(bar_grp, kGroupThreads);
+            if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_STORED);
         }
         // every bulk store of this warp has completed before the CTA may leave
         if (lane == 0) ptx::bulk_wait_group0();
@@ -779,8 +775,8 @@ cudaError_t ensure_attributes(int variant, void *fn, int smem) {
 
 }  // namespace
 
-int gemm_fused_smem_bytes(int stages, int cluster, int n_slice, bool pair) {
-    return int(smem_layout(stages, cluster, n_slice, pair).total) + 1024;  // + alignment slack
+int gemm_fused_smem_bytes(int stages, int cluster, int n_slice, bool pair, bool leader) {
+    return int(smem_layout(stages, cluster, n_slice, pair, leader).total);
 }
 
 int gemm_fused_max_active_clusters(int kind, bool pair, int cluster, int smem) {

@@ -75,9 +75,10 @@ def test_plan_forced_single_cluster_rows():
 
 def test_plan_chooses_fastest_predicted():
     """The automatic choice minimises the planner's time model: ceil(T/ncl) tiles per
-    CTA, each max(mainloop, epilogue), plus one exposed epilogue."""
+    CTA in rounds of two (two accumulators, two epilogue groups), each round
+    max(2 mainloops, epilogue), plus the global barrier's skew."""
     cases = {
-        (4096, 2048, 128): (8, 1, 1, 15),     # whole row in one cluster of 8; K too short for pairs
+        (4096, 2048, 128): (4, 1, 2, 36),     # 2 tiles per CTA (one round) beats 3 in a cluster of 8
         (16384, 4096, 4096): (1, 2, 16, 76),  # CTA pairs (cta_group::2), rows over 16 clusters
         (8192, 16384, 2048): (2, 2, 32, 36),  # CTA pairs, rows over 32 clusters
         (128, 512, 256): (2, 1, 1, 1),        # one row block: no pair
