@@ -111,6 +111,10 @@ typedef struct cf_tuning {
                                the W tile).  0 = auto                           */
     int32_t multicast_x;    /* GEMM, C_M = 1: multicast each X tile along the row
                                group instead of loading it in every CTA        */
+    int32_t disable_pdl;    /* GEMM: 1 = launch without programmatic dependent
+                               launch (by default the kernel's set-up overlaps
+                               the previous kernel's tail on the same stream and
+                               waits for it before touching memory)            */
     uint64_t *trace;        /* TRACING (fused GEMM): device buffer of
                                grid_ctas * CF_TRACE_SLOTS u64 %globaltimer stamps
                                (ns), or NULL for none.  Per CTA: slots 0..3 =
@@ -160,6 +164,7 @@ typedef struct cf_plan {
     int32_t cluster_m;      /* C_M: row blocks per cluster; a cluster holds
                                C_M * C_N CTAs; C_M = 2 runs CTA pairs (ranks
                                2i, 2i+1) as one cta_group::2 MMA stream           */
+    int32_t staging_buffers;/* bf16 output staging buffers per epilogue warp      */
 } cf_plan;
 
 /* Plan a fused GEMM+row-reduce launch for a device with `sm_count` SMs, where

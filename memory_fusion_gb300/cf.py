@@ -41,6 +41,7 @@ class cf_tuning(ctypes.Structure):
         ("extra_arrivals", ctypes.c_int32),
         ("cluster_m", ctypes.c_int32),
         ("multicast_x", ctypes.c_int32),
+        ("disable_pdl", ctypes.c_int32),
         ("trace", ctypes.c_void_p),
     ]
 
@@ -64,6 +65,7 @@ class cf_plan(ctypes.Structure):
         ("stages", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32),
         ("cluster_m", ctypes.c_int32),
+        ("staging_buffers", ctypes.c_int32),
     ]
 
     def as_dict(self):

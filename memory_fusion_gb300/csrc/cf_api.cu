@@ -90,9 +90,9 @@ int max_active_cached(int device, int kind, bool pair, int cluster, int smem) {
     return n;
 }
 
-int gemm_stages_for(int n_slice, int cluster, int requested, bool pair, bool leader) {
+int gemm_stages_for(int n_slice, int cluster, int requested, bool pair, bool leader, int stg_bufs = 1) {
     int s = requested > 0 ? requested : 6;
-    while (s > 2 && cf::gemm_fused_smem_bytes(s, cluster, n_slice, pair, leader) > kMaxSmem) --s;
+    while (s > 2 && cf::gemm_fused_smem_bytes(s, cluster, n_slice, pair, leader, stg_bufs) > kMaxSmem) --s;
     return s;
 }
 
@@ -240,8 +240,19 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
     plan->leader_mode = (peer_max < 0 || C > peer_max) ? 1 : 0;
     plan->row_blocks = rb;
     plan->clusters = std::max(ncl, 1);
-    plan->stages = gemm_stages_for(ns, C, t.stages, CMs == 2, plan->leader_mode != 0);
-    plan->smem_bytes = cf::gemm_fused_smem_bytes(plan->stages, C, ns, CMs == 2, plan->leader_mode != 0);
+    {
+        // operand ring first; a second output staging buffer per warp only where
+        // it costs no ring stage the K loop can use (at most nk + 1 are useful)
+        const bool pair = CMs == 2, lead = plan->leader_mode != 0;
+        int st = gemm_stages_for(ns, C, t.stages, pair, lead, 1);
+        int sb = 1;
+        const int useful = std::max(2, nk + 1);
+        if (t.stages <= 0 && st > useful) st = useful;
+        if (cf::gemm_fused_smem_bytes(st, C, ns, pair, lead, 2) <= kMaxSmem) sb = 2;
+        plan->stages = st;
+        plan->staging_buffers = sb;
+        plan->smem_bytes = cf::gemm_fused_smem_bytes(st, C, ns, pair, lead, sb);
+    }
     plan->cluster_m = CMs;
     if (plan->smem_bytes > kMaxSmem) return CF_ERR_UNSUPPORTED;
     return CF_OK;
@@ -374,7 +385,7 @@ static cf_status device_plan(int kind, int64_t M, int64_t N, int64_t K, const cf
         if (!as_cn && !as_pair) continue;
         const int cn = as_cn ? c : c / 2;
         const int st = gemm_stages_for(ns, cn, t.stages, !as_cn, true);
-        const int smem = cf::gemm_fused_smem_bytes(st, cn, ns, !as_cn, true);
+        const int smem = cf::gemm_fused_smem_bytes(st, cn, ns, !as_cn, true, 1);
         if (smem > std::min(kMaxSmem, dev.max_smem_optin)) continue;
         active[c] = max_active_cached(dev.device, kind, !as_cn, c, smem);
     }
@@ -456,7 +467,8 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
     a.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
     a.trace = reinterpret_cast<unsigned long long *>(t.trace);
     a.multicast_x = (t.multicast_x && plan.cluster_m == 1 && plan.cluster_size > 1) ? 1 : 0;
-    cudaError_t e = cf::launch_gemm_fused(kind, a, plan.clusters, plan.stages, plan.smem_bytes,
+    a.stg_bufs = plan.staging_buffers;
+    cudaError_t e = cf::launch_gemm_fused(kind, a, plan.clusters, plan.stages, plan.smem_bytes, t.disable_pdl == 0,
                                           reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return CF_OK;
@@ -594,7 +606,8 @@ extern "C" cf_status cf_gemm_fused_rownorm_noalloc(const void *X, const void *W,
     a.row_blocks_alloc = a.super_blocks * plan.cluster_m;
     a.extra_arrivals = 0;
     a.timeout_ns = 1000ull * kDefaultTimeoutUs;
-    e = cf::launch_gemm_fused(kind, a, plan.clusters, plan.stages, plan.smem_bytes, s);
+    a.stg_bufs = plan.staging_buffers;
+    e = cf::launch_gemm_fused(kind, a, plan.clusters, plan.stages, plan.smem_bytes, true, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return CF_OK;
 }

@@ -74,6 +74,7 @@ struct GemmArgs {
     int cluster_m;        // C_M: row blocks per cluster; 2 = CTA pairs sharing one
                           // cta_group::2 MMA stream (M = 256, W split between the pair)
     int multicast_x;      // single-CTA MMA: multicast each X tile along the row group
+    int stg_bufs;         // output staging buffers per epilogue warp (1 or 2)
     int groups;           // G
     int leader;           // leader-follower aggregation in the row group
     int row_blocks;       // RB = ceil(M / 128)
@@ -86,14 +87,16 @@ struct GemmArgs {
 
 // dynamic shared memory of one CTA for a ring of `stages`, a row group of
 // `cluster` CTAs, the CTA-pair MMA mode or not, leader-follower or peer exchange
-int gemm_fused_smem_bytes(int stages, int cluster, int n_slice, bool pair, bool leader);
+int gemm_fused_smem_bytes(int stages, int cluster, int n_slice, bool pair, bool leader, int stg_bufs);
 
 // Query max co-resident clusters of `cluster` CTAs (total) for the fused
 // kernel of `kind` and mode with `smem` dynamic shared memory (0 if it cannot
 // launch).
 int gemm_fused_max_active_clusters(int kind, bool pair, int cluster, int smem);
 
-cudaError_t launch_gemm_fused(int kind, const GemmArgs &a, int clusters, int stages, int smem,
+// pdl: allow programmatic dependent launch (the kernel waits on griddepcontrol
+// before touching global memory)
+cudaError_t launch_gemm_fused(int kind, const GemmArgs &a, int clusters, int stages, int smem, bool pdl,
                               cudaStream_t stream);
 
 }  // namespace cf

@@ -75,7 +75,7 @@ constexpr uint32_t kInfoGlobal = 0x50000000u;
 struct SmemLayout {
     uint32_t stage_bytes;  // A + B of one stage
     uint32_t ring;         // offset of the operand ring (1024-aligned)
-    uint32_t stg;          // bf16 output staging, 2 KiB per epilogue warp (64B swizzle)
+    uint32_t stg;          // bf16 output staging, 1 or 2 x 2 KiB per epilogue warp (64B swizzle)
     uint32_t send;         // float2 [4][128]: this CTA's partial, by exchange set
     uint32_t slot;         // float2 [4][C][128]: the row group's partials, by exchange set
     uint32_t res;          // float2 [4][128]: leader-follower result, by exchange set
@@ -86,14 +86,15 @@ struct SmemLayout {
 
 constexpr int kXSets = 4;  // exchange buffer sets (tile mod 4)
 
-__host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n_slice, bool pair, bool leader) {
+__host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n_slice, bool pair, bool leader,
+                                                  int stg_bufs) {
     SmemLayout L;
     // a CTA of a pair stages its own 128 rows of X and half of the tile's W columns
     L.stage_bytes = kABytes + uint32_t(pair ? n_slice / 2 : n_slice) * kBK * 2;
     L.ring = 0;
     uint32_t off = L.ring + uint32_t(stages) * L.stage_bytes;
     L.stg = off;
-    off += kEpiWarps * 2048;
+    off += kEpiWarps * 2048 * uint32_t(stg_bufs);
     // exchange buffers exist only when a row group has more than one CTA
     const uint32_t xc = cluster > 1 ? 1u : 0u;
     L.send = off;
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     // dynamic shared window starts aligned; if it ever did not, report it and
     // do nothing (every CTA sees the same base, so none enters a cluster barrier).
     if ((base & 1023u) != 0u) {
+        ptx::griddep_wait();
         if (threadIdx.x == 0) ptx::record_error(a.err, 8u /*CF_ERR_DEVICE_BOUNDS*/, 0x60000000u | (base & 1023u));
         return;
     }
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     const int T = a.super_blocks * G;       // tickets: (super row block, cluster group), row-block major
     const int nbox = ns / 64;               // 64-column W boxes of a tile
     const int my_boxes = kPair ? nbox / 2 : nbox;  // W boxes staged in this CTA
-    const SmemLayout L = smem_layout(stages, C, ns, kPair, a.leader != 0);
+    const SmemLayout L = smem_layout(stages, C, ns, kPair, a.leader != 0, a.stg_bufs);
     const Bars B = bars_at(base + L.bars, stages);
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + (B.misc - base));
     volatile uint32_t *abort = misc + 1;
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     if (mcx) a_mask = uint16_t((1u << C) - 1u);
     const int a_rows = mcx ? kBlockM / C : kBlockM;  // rows of the X tile this CTA loads
     const uint32_t tmem_cols = (ns * 2 <= 32) ? 32u : uint32_t(ns * 2);
-    if (threadIdx.x == 0) trace_stamp(a.trace, 0);
+    const unsigned long long t_start = ptx::globaltimer();  // traced after the dependency wait
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -312,7 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     // barrier initialisation is visible cluster-wide before any peer signals it
     ptx::cluster_sync();
     const uint32_t tmem_base = misc[0];
-    if (threadIdx.x == 0) trace_stamp(a.trace, 1);
+    // Programmatic dependent launch: the set-up above overlapped the previous
+    // grid's tail; nothing in global memory is touched before it completed.
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+    if (threadIdx.x == 0 && a.trace != nullptr) {
+        a.trace[blockIdx.x * CF_TRACE_SLOTS + 0] = t_start;
+        trace_stamp(a.trace, 1);
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -447,7 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
         float2 *const slot = reinterpret_cast<float2 *>(gbase + L.slot);
         float2 *const res = reinterpret_cast<float2 *>(gbase + L.res);
         float *const prm = reinterpret_cast<float *>(gbase + L.prm) + grp * 768;
-        const uint32_t stg = base + L.stg + uint32_t(e) * 2048u;  // this warp's staging buffer
+        const uint32_t stg0 = base + L.stg + uint32_t(e) * 2048u * uint32_t(a.stg_bufs);  // this warp's staging
+        uint32_t nstore = 0;  // stores issued by this warp (selects the staging buffer)
         const float fN = float(a.N);
         const int nchunks = ns / 32;  // 2, 4 or 8 fragments of 32 columns per thread
         float *const pb = prm;        // bias, gamma, beta of this group's current tile
@@ -685,7 +695,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         }
                         if (rows_live) {
                             // the previous store from this buffer has finished reading it
-                            if (lane == 0) ptx::bulk_wait_group_read0();
+                            // (with two buffers: at most one store may still be reading)
+                            const uint32_t stg = stg0 + (a.stg_bufs > 1 ? (nstore & 1u) * 2048u : 0u);
+                            if (lane == 0) {
+                                if (a.stg_bufs > 1) ptx::bulk_wait_group_read1();
+                                else ptx::bulk_wait_group_read0();
+                            }
                             __syncwarp();
                             // row `lane` of the 32x32 block: four 16-byte pieces, 64B swizzle
                             const uint32_t ra = stg + uint32_t(lane) * 64u;
@@ -700,6 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                                 ptx::tma_store_2d(&a.tmap_y, stg, ncta + cc * 32, ystore);
                                 ptx::bulk_commit_group();
                             }
+                            ++nstore;
                         }
                     }
                 }
@@ -775,8 +791,8 @@ cudaError_t ensure_attributes(int variant, void *fn, int smem) {
 
 }  // namespace
 
-int gemm_fused_smem_bytes(int stages, int cluster, int n_slice, bool pair, bool leader) {
-    return int(smem_layout(stages, cluster, n_slice, pair, leader).total);
+int gemm_fused_smem_bytes(int stages, int cluster, int n_slice, bool pair, bool leader, int stg_bufs) {
+    return int(smem_layout(stages, cluster, n_slice, pair, leader, stg_bufs).total);
 }
 
 int gemm_fused_max_active_clusters(int kind, bool pair, int cluster, int smem) {
@@ -805,7 +821,7 @@ int gemm_fused_max_active_clusters(int kind, bool pair, int cluster, int smem) {
     return n;
 }
 
-cudaError_t launch_gemm_fused(int kind, const GemmArgs &a, int clusters, int stages, int smem,
+cudaError_t launch_gemm_fused(int kind, const GemmArgs &a, int clusters, int stages, int smem, bool pdl,
                               cudaStream_t stream) {
     const bool pair = a.cluster_m == 2;
     void *fn = kernel_for(kind, pair);
@@ -817,13 +833,15 @@ cudaError_t launch_gemm_fused(int kind, const GemmArgs &a, int clusters, int sta
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = a.cluster * a.cluster_m;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     int st = stages;
     void *args[] = {(void *)&a, (void *)&st};
     return cudaLaunchKernelExC(&cfg, fn, args);

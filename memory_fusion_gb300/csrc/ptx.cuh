@@ -57,6 +57,17 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// wait until every grid this one depends on has completed and its memory is visible
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// allow the next dependent grid to be scheduled (it still waits for our completion
+// in its own griddep_wait before touching memory)
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // cluster barrier (hardware; every thread of every CTA of the cluster)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void cluster_arrive_release() {
@@ -249,6 +260,10 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 // this thread's committed bulk stores have finished reading shared memory
 __device__ __forceinline__ void bulk_wait_group_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// at most one of this thread's committed bulk stores is still reading shared memory
+__device__ __forceinline__ void bulk_wait_group_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // this thread's committed bulk stores are complete
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
