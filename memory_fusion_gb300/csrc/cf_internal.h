@@ -38,6 +38,7 @@ struct StitchPlan {
     int per_thread = 0;   // split: float4 groups per thread (1..16, power of two)
     int leader = 0;       // split: leader-follower aggregation
     bool vec = false;     // 128-bit path
+    bool pdl = true;      // programmatic dependent launch
     int grid = 0;         // CTAs
 };
 

@@ -45,6 +45,9 @@ __global__ void __launch_bounds__(kThreads) stitch_packed_kernel(const float *__
     const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
     constexpr int64_t kRowsPerIter = int64_t(RPW) * kUnroll;
+    // programmatic dependent launch: nothing in global memory before the
+    // previous grid on the stream has completed
+    ptx::griddep_wait();
 
     for (int64_t base = warp * kRowsPerIter; base < rows; base += nwarps * kRowsPerIter) {
         float v[kUnroll][4];
@@ -98,6 +101,8 @@ __global__ void __launch_bounds__(kThreads) stitch_packed_kernel(const float *__
             }
         }
     }
+    // the next grid may be scheduled once this CTA's rows are written
+    ptx::griddep_launch_dependents();
 }
 
 // --------------------------------------------------------------------------
@@ -124,8 +129,9 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
     const int g0 = int(rank) * gpc;
     const int g1 = min(ng, g0 + gpc);
 
-    // every peer CTA is running before anyone touches its shared memory
-    ptx::cluster_sync();
+    // programmatic dependent launch: nothing in global memory before the
+    // previous grid on the stream has completed
+    ptx::griddep_wait();
 
     int it = 0;
     for (int64_t row = cid; row < rows; row += ncl, ++it) {
@@ -150,6 +156,9 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
                 for (int j = 0; j < 4; ++j) e[v][j] = (g < g1 && 4 * g + j < cols) ? __ldcs(a + 4 * g + j) : 0.f;
             }
         }
+        // every peer CTA is running before anyone touches its shared memory; the
+        // first row's loads are already in flight behind this barrier
+        if (it == 0) ptx::cluster_sync();
         // thread-local aggregation: max, then sum of exp (exp kept for the output)
         float mt = neg_inf();
 #pragma unroll
@@ -224,6 +233,8 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
         // slot[par] / res[par] are written again two rows later, after every CTA
         // of the cluster has passed the next row's cluster barrier
     }
+    // the next grid may be scheduled once this CTA's rows are written
+    ptx::griddep_launch_dependents();
     // no CTA leaves while a peer may still access its shared memory
     ptx::cluster_sync();
 }
@@ -291,7 +302,17 @@ cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias
         if (!fn) return cudaErrorInvalidValue;
         int icols = int(cols);
         void *args[] = {(void *)&A, (void *)&bias, (void *)&out, (void *)&rows, (void *)&icols};
-        return cudaLaunchKernel(fn, dim3(p.grid), dim3(kThreads), args, 0, stream);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(p.grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = p.pdl ? 1 : 0;
+        return cudaLaunchKernelExC(&cfg, fn, args);
     }
     if (p.mapping == 2) {
         void *fn = split_kernel(p.per_thread, p.vec);
@@ -319,13 +340,15 @@ cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = p.cluster;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = p.pdl ? 2 : 1;
         void *args[] = {(void *)&A, (void *)&bias, (void *)&out, (void *)&rows, (void *)&icols, (void *)&gpc,
                         (void *)&leader};
         return cudaLaunchKernelExC(&cfg, fn, args);
