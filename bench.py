@@ -311,13 +311,39 @@ def per_workload(torch, cf, peaks, device, names):
         t1 = t / n
         troof, bound = roofline_time_s(w, peaks)
         _, plan, _ = cf.cf_query_gemm_fused_plan(w.M, w.N, w.K, kind_of(w))
+        tu = unfused_time(torch, cf, r, reps)
         out[name] = {"us": round(t1 * 1e6, 2), "tflops": round(w.flops / t1 / 1e12, 1),
                      "gbs": round(w.unavoidable_bytes / t1 / 1e9, 1), "bound": bound,
                      "roofline_frac": round(troof / t1, 3), "buffer_sets": nsets,
+                     "unfused_us": round(tu * 1e6, 2), "fused_speedup": round(tu / t1, 2),
                      "plan": plan.as_dict()}
         del r
         torch.cuda.empty_cache()
     return out
+
+
+def unfused_time(torch, cf, runner, reps):
+    """The same workload through the unfused two-kernel composition (GEMM to an
+    fp32 intermediate, then the row kernel), same buffer rotation."""
+    w = runner.w
+    wsb = cf.cf_unfused_workspace_size(w.M, w.N, w.K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=runner.sets[0]["X"].device)
+
+    class U:
+        def launch(self, i, stream=None):
+            s = runner.sets[i % len(runner.sets)]
+            if w.kind == "softmax":
+                st = cf.cf_unfused_gemm_rowsoftmax(s["X"], s["W"], None, s["Y"], w.M, w.N, w.K, w.scale, ws, wsb,
+                                                   stream)
+            else:
+                act = cf.CF_ACT_GELU_TANH if w.act == "gelu_tanh" else cf.CF_ACT_NONE
+                st = cf.cf_unfused_gemm_rownorm(s["X"], s["W"], s["bias"], s["gamma"], s["beta"], s["Y"], w.M, w.N,
+                                                w.K, w.alpha, w.eps, act, ws, wsb, stream)
+            cf.check(st, "unfused launch")
+
+    t, n, _ = time_steps(torch, U(), reps, 3, lambda: None, graph_len=reps)
+    del ws
+    return t / n
 
 
 def stitch_numbers(torch, cf, w, peaks, device, l2):

@@ -321,6 +321,30 @@ CF_API cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *r
                                            void *workspace, size_t workspace_bytes,
                                            cf_stream_t stream, const cf_tuning *tuning);
 
+/* ------------------------------------------------------------------------ */
+/* The unfused two-kernel composition (measured baseline)                    */
+/* ------------------------------------------------------------------------ */
+/* The same computations as cf_gemm_fused_rownorm / cf_gemm_fused_rowsoftmax,
+ * scheduled the way fusion avoids: kernel 1 writes P = X.W as fp32 [M,N] into
+ * the workspace (the intermediate that [ComFuse] Stage-Stream Execution Model
+ * keeps out of GMEM), kernel 2 reads it back and applies bias (GELU) and the
+ * row reduction + broadcast.  For measuring what fusion saves; not a
+ * fallback.  Arguments as for the fused calls; the workspace (device,
+ * >= cf_unfused_workspace_size bytes, 16-byte aligned) holds P and an error
+ * word.  Supported: N a multiple of 64 up to 16384, K a multiple of 64. */
+CF_API size_t cf_unfused_workspace_size(int64_t M, int64_t N, int64_t K);
+
+CF_API cf_status cf_unfused_gemm_rownorm(const void *X, const void *W, const float *bias,
+                                         const float *gamma, const float *beta, void *Y,
+                                         int64_t M, int64_t N, int64_t K, float alpha, float eps,
+                                         cf_activation act, void *workspace,
+                                         size_t workspace_bytes, cf_stream_t stream);
+
+CF_API cf_status cf_unfused_gemm_rowsoftmax(const void *X, const void *W, const float *bias,
+                                            void *Y, int64_t M, int64_t N, int64_t K, float scale,
+                                            void *workspace, size_t workspace_bytes,
+                                            cf_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

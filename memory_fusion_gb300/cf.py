@@ -108,6 +108,10 @@ _SIGS = {
     "cf_gemm_fused_rowsoftmax": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P]),
     "cf_gemm_fused_rowsoftmax_ex": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P,
                                           ctypes.POINTER(cf_tuning)]),
+    "cf_unfused_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "cf_unfused_gemm_rownorm": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
+                                      _P, _SZ, _P]),
+    "cf_unfused_gemm_rowsoftmax": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P]),
     "cf_stitch_rowreduce_broadcast": (_ST, [_P, _P, _P, _I64, _I64, _P, _SZ, _P]),
     "cf_stitch_rowreduce_broadcast_ex": (_ST, [_P, _P, _P, _I64, _I64, _P, _SZ, _P,
                                                ctypes.POINTER(cf_tuning)]),
@@ -256,6 +260,23 @@ def cf_stitch_rowreduce_broadcast(A, row_bias, out, rows, cols, workspace, works
     return L.cf_stitch_rowreduce_broadcast_ex(_ptr(A), _ptr(row_bias), _ptr(out), rows, cols,
                                               _ptr(workspace), workspace_bytes, _stream(stream),
                                               _tun(tuning))
+
+
+def cf_unfused_workspace_size(M, N, K) -> int:
+    return lib().cf_unfused_workspace_size(M, N, K)
+
+
+def cf_unfused_gemm_rownorm(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, workspace, workspace_bytes,
+                            stream=None) -> int:
+    """The unfused two-kernel composition (GEMM -> fp32 P -> row kernel), for comparison."""
+    return lib().cf_unfused_gemm_rownorm(_ptr(X), _ptr(W), _ptr(bias), _ptr(gamma), _ptr(beta), _ptr(Y),
+                                         M, N, K, alpha, eps, act, _ptr(workspace), workspace_bytes,
+                                         _stream(stream))
+
+
+def cf_unfused_gemm_rowsoftmax(X, W, bias, Y, M, N, K, scale, workspace, workspace_bytes, stream=None) -> int:
+    return lib().cf_unfused_gemm_rowsoftmax(_ptr(X), _ptr(W), _ptr(bias), _ptr(Y), M, N, K, scale,
+                                            _ptr(workspace), workspace_bytes, _stream(stream))
 
 
 def check(status: int, what: str = "libcf"):

@@ -73,6 +73,21 @@ bool make_tmap_bf16(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t col
     return r == CUDA_SUCCESS;
 }
 
+// 2-D fp32 tensor map over a row-major [rows, cols] matrix for TMA stores of
+// 16-column x 32-row blocks (64-byte rows, 64B swizzle)
+bool make_tmap_f32_store(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {16, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // -------------------------------------------------------------------------
 // occupancy cache: max co-resident clusters for (device, kind, cluster, smem)
 // -------------------------------------------------------------------------
@@ -611,4 +626,108 @@ extern "C" cf_status cf_gemm_fused_rownorm_noalloc(const void *X, const void *W,
     e = cf::launch_gemm_fused(kind, a, plan.clusters, plan.stages, plan.smem_bytes, true, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return CF_OK;
+}
+
+// =========================================================================
+// The unfused two-kernel composition (a measured baseline, not a fallback):
+// GEMM -> fp32 P in global memory -> row kernel.  Same results within the
+// fused calls' tolerances; it pays the intermediate's write and read.
+// =========================================================================
+namespace {
+
+size_t unfused_p_bytes(int64_t M, int64_t N) { return cf::align_up(size_t(M) * size_t(N) * 4, 256); }
+
+// P = X . W (fp32), with the fused kernel's store-only epilogue: every tile
+// is independent (no row reduction), so any resident cluster count works.
+cf_status gemm_store_f32(const void *X, const void *W, float *P, uint32_t *err, int64_t M, int64_t N, int64_t K,
+                         cudaStream_t stream) {
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+    const int ns = (N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64;
+    const int cpr = int(N / ns);
+    const int rb = int((M + cf::kBlockM - 1) / cf::kBlockM);
+    const int nk = int(K / 64);
+    const int cm = (nk >= 8 && rb >= 2 && ns >= 128) ? 2 : 1;
+    const bool pair = cm == 2;
+    const int stages = gemm_stages_for(ns, 1, 0, pair, false, 1);
+    int sb = 1;
+    if (cf::gemm_fused_smem_bytes(stages, 1, ns, pair, false, 2) <= kMaxSmem) sb = 2;
+    const int smem = cf::gemm_fused_smem_bytes(stages, 1, ns, pair, false, sb);
+    const int active = max_active_cached(dev.device, cf::EPI_STORE_F32, pair, cm, smem);
+    if (active <= 0) return CF_ERR_NOT_RESIDENT;
+    const int sblocks = (rb + cm - 1) / cm;
+    const int64_t tickets = int64_t(sblocks) * cpr;
+    const int clusters = int(std::min<int64_t>(active, tickets));
+
+    cf::GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, 128)) return CF_ERR_CUDA;
+    if (!make_tmap_bf16(&a.tmap_w, W, uint64_t(K), uint64_t(N), 64, 64)) return CF_ERR_CUDA;
+    if (!make_tmap_f32_store(&a.tmap_y, P, uint64_t(M), uint64_t(N))) return CF_ERR_CUDA;
+    a.err = err;
+    a.M = int(M);
+    a.N = int(N);
+    a.K = int(K);
+    a.alpha = 1.f;
+    a.n_slice = ns;
+    a.cluster = 1;
+    a.cluster_m = cm;
+    a.groups = cpr;  // tickets enumerate every tile of a row block
+    a.row_blocks = rb;
+    a.super_blocks = sblocks;
+    a.row_blocks_alloc = sblocks * cm;
+    a.timeout_ns = 1000ull * kDefaultTimeoutUs;
+    a.stg_bufs = sb;
+    cudaError_t e = cf::launch_gemm_fused(cf::EPI_STORE_F32, a, clusters, stages, smem, true, stream);
+    return e == cudaSuccess ? CF_OK : cuda_fail(e);
+}
+
+cf_status unfused_common(int op, const void *X, const void *W, const float *bias, const float *gamma,
+                         const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha, float eps,
+                         void *ws, size_t ws_bytes, cf_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0) return CF_ERR_INVALID_ARG;
+    if (!X || !W || !Y || !ws) return CF_ERR_INVALID_ARG;
+    if (op != 2 && (!gamma || !beta)) return CF_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(ws) || (bias && !aligned16(bias)) ||
+        (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)))
+        return CF_ERR_MISALIGNED;
+    if (K % 64 != 0 || N % 64 != 0 || N > 256 * 64) return CF_ERR_UNSUPPORTED;
+    if (ws_bytes < cf_unfused_workspace_size(M, N, K)) return CF_ERR_WORKSPACE_TOO_SMALL;
+    if (M == 0) return CF_OK;
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    float *P = reinterpret_cast<float *>(w8);
+    uint32_t *err = reinterpret_cast<uint32_t *>(w8 + unfused_p_bytes(M, N));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cf_status st = gemm_store_f32(X, W, P, err, M, N, K, s);
+    if (st != CF_OK) return st;
+    cudaError_t e = cf::launch_row_epilogue(op, P, bias, gamma, beta, static_cast<uint16_t *>(Y), M, int(N), alpha,
+                                            eps, s);
+    return e == cudaSuccess ? CF_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" size_t cf_unfused_workspace_size(int64_t M, int64_t N, int64_t K) {
+    (void)K;
+    if (M < 0 || N <= 0) return cf::kErrBytes;
+    return unfused_p_bytes(M, N) + cf::kErrBytes;
+}
+
+extern "C" cf_status cf_unfused_gemm_rownorm(const void *X, const void *W, const float *bias, const float *gamma,
+                                             const float *beta, void *Y, int64_t M, int64_t N, int64_t K,
+                                             float alpha, float eps, cf_activation act, void *workspace,
+                                             size_t workspace_bytes, cf_stream_t stream) {
+    int op;
+    if (act == CF_ACT_NONE) op = 0;
+    else if (act == CF_ACT_GELU_TANH) op = 1;
+    else return CF_ERR_INVALID_ARG;
+    return unfused_common(op, X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, workspace, workspace_bytes, stream);
+}
+
+extern "C" cf_status cf_unfused_gemm_rowsoftmax(const void *X, const void *W, const float *bias, void *Y, int64_t M,
+                                                int64_t N, int64_t K, float scale, void *workspace,
+                                                size_t workspace_bytes, cf_stream_t stream) {
+    return unfused_common(2, X, W, bias, nullptr, nullptr, Y, M, N, K, scale, 0.f, workspace, workspace_bytes,
+                          stream);
 }

@@ -48,18 +48,27 @@ cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias
 int stitch_packed_blocks_per_sm(int lpr, bool vec);
 
 // --------------------------------------------------------------------------
+// row epilogue kernel of the unfused baseline (rowkernel.cu):
+//   op 0 LN, 1 GELU+LN, 2 softmax over fp32 rows of P -> bf16 Y
+// --------------------------------------------------------------------------
+cudaError_t launch_row_epilogue(int op, const float *P, const float *bias, const float *gamma, const float *beta,
+                                uint16_t *Y, int64_t M, int N, float alpha, float eps, cudaStream_t stream);
+
+// --------------------------------------------------------------------------
 // fused GEMM kernels (gemm_fused.cu)
 // --------------------------------------------------------------------------
 enum EpiKind : int {
     EPI_LN = 0,        // alpha*acc + bias -> LayerNorm -> bf16
     EPI_GELU_LN = 1,   // alpha*acc + bias -> GELU(tanh) -> LayerNorm -> bf16
     EPI_SOFTMAX = 2,   // scale*acc + bias -> softmax -> bf16
+    EPI_STORE_F32 = 3, // raw fp32 accumulator to P [M,N] (the unfused baseline's GEMM)
 };
 
 struct GemmArgs {
     CUtensorMap tmap_x;   // X [M,K] bf16, box 64(K) x (128/C_N)(M), 128B swizzle
     CUtensorMap tmap_w;   // W [K,N] bf16, box 64(N) x 64(K), 128B swizzle
-    CUtensorMap tmap_y;   // Y [M,N] bf16, box 32(N) x 32(M), 64B swizzle (stores)
+    CUtensorMap tmap_y;   // Y [M,N] bf16, box 32(N) x 32(M), 64B swizzle (stores);
+                          // EPI_STORE_F32: P [M,N] fp32, box 16(N) x 32(M)
     const float *bias;    // [N] or null
     const float *gamma;   // [N] (LN)
     const float *beta;    // [N] (LN)

@@ -477,11 +477,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             // Row-vector parameters of the tile's columns into this group's shared
             // buffer, fetched before the accumulator is ready; the group's previous
             // tile finished reading them before the group barrier that ended it.
-            for (int c = gt; c < ns; c += kGroupThreads) {
-                pb[c] = a.bias ? __ldg(a.bias + ncta + c) : 0.f;
-                if constexpr (EPI != EPI_SOFTMAX) {
-                    pg[c] = __ldg(a.gamma + ncta + c);
-                    pe[c] = __ldg(a.beta + ncta + c);
+            if constexpr (EPI != EPI_STORE_F32) {
+                for (int c = gt; c < ns; c += kGroupThreads) {
+                    pb[c] = a.bias ? __ldg(a.bias + ncta + c) : 0.f;
+                    if constexpr (EPI != EPI_SOFTMAX) {
+                        pg[c] = __ldg(a.gamma + ncta + c);
+                        pe[c] = __ldg(a.beta + ncta + c);
+                    }
                 }
             }
             ptx::mbar_wait_bounded(B.tmem_full0 + 8 * buf, tph, tmo, abort, a.err, kInfoEpi | buf);
@@ -489,6 +491,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             ptx::named_bar_sync(bar_grp, kGroupThreads);  // parameters visible to the group
             if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_START);
             const uint32_t tacc = tmem_base + (uint32_t(q * 32) << 16) + buf * uint32_t(ns);
+
+            if constexpr (EPI == EPI_STORE_F32) {
+                // Unfused-baseline mode: the raw fp32 accumulator tile is written to
+                // P [M, N]; no epilogue nodes, no row reduction.  Each 32-column
+                // fragment leaves as two 16-column x 32-row blocks (64B swizzle).
+                const bool rows_live = (m0 + q * 32) < a.M;
+                const int ystore = m0 + q * 32;
+#pragma unroll
+                for (int c = 0; c < 8; c += 2) {
+                    if (c < nchunks) {
+                        uint32_t v0[32], v1[32];
+                        ptx::tmem_ld32(tacc + c * 32, v0);
+                        ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uint32_t(&v)[32] = (k >> 1) == 0 ? v0 : v1;
+                            const int hh = k & 1;
+                            if (rows_live) {
+                                const uint32_t stg = stg0 + (a.stg_bufs > 1 ? (nstore & 1u) * 2048u : 0u);
+                                if (lane == 0) {
+                                    if (a.stg_bufs > 1) ptx::bulk_wait_group_read1();
+                                    else ptx::bulk_wait_group_read0();
+                                }
+                                __syncwarp();
+                                const uint32_t ra = stg + uint32_t(lane) * 64u;
+                                const uint32_t sw = (uint32_t(lane) >> 1) & 3u;
+#pragma unroll
+                                for (int k4 = 0; k4 < 4; ++k4)
+                                    ptx::st_shared_v4(ra + ((uint32_t(k4) ^ sw) << 4), v[16 * hh + 4 * k4],
+                                                      v[16 * hh + 4 * k4 + 1], v[16 * hh + 4 * k4 + 2],
+                                                      v[16 * hh + 4 * k4 + 3]);
+                                ptx::fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    ptx::tma_store_2d(&a.tmap_y, stg, ncta + (c + (k >> 1)) * 32 + hh * 16, ystore);
+                                    ptx::bulk_commit_group();
+                                }
+                                ++nstore;
+                            }
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (kPair) ptx::mbar_arrive_cluster(ptx::mapa(B.tmem_empty0 + 8 * buf, pair_leader));
+                    else ptx::mbar_arrive(B.tmem_empty0 + 8 * buf);
+                }
+                ptx::named_bar_sync(bar_grp, kGroupThreads);
+                continue;
+            }
 
             // ---------------- stage 1: compute phase + thread-local aggregation.
             // Fragments of 32 columns stream out of TMEM two at a time; the stage-1
@@ -753,6 +807,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
 
 void *kernel_for(int kind, bool pair) {
     switch (kind) {
+        case EPI_STORE_F32:
+            return pair ? reinterpret_cast<void *>(&gemm_fused_kernel<EPI_STORE_F32, true>)
+                        : reinterpret_cast<void *>(&gemm_fused_kernel<EPI_STORE_F32, false>);
         case EPI_LN:
             return pair ? reinterpret_cast<void *>(&gemm_fused_kernel<EPI_LN, true>)
                         : reinterpret_cast<void *>(&gemm_fused_kernel<EPI_LN, false>);
@@ -770,12 +827,12 @@ void *kernel_for(int kind, bool pair) {
 // shared-memory size seen, so launches made under stream capture issue no
 // attribute calls.
 cudaError_t ensure_attributes(int variant, void *fn, int smem) {
-    static int set_smem[64][6] = {};
-    static bool nonportable[64][6] = {};
+    static int set_smem[64][8] = {};
+    static bool nonportable[64][8] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || variant < 0 || variant >= 6) return cudaErrorInvalidValue;
+    if (dev < 0 || dev >= 64 || variant < 0 || variant >= 8) return cudaErrorInvalidValue;
     if (smem > set_smem[dev][variant]) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
