@@ -39,6 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+from memory_fusion_gb300 import dist as mdist  # noqa: E402
 from memory_fusion_gb300 import inputs  # noqa: E402
 
 HEADLINE = "softmax_4096x2048x128"
@@ -60,10 +61,7 @@ def load_peaks():
 
 
 def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return mdist.env()
 
 
 def kind_of(w):
@@ -190,11 +188,12 @@ class FusedRunner:
         cf.check(st, "fused launch")
 
 
-def _seeded_inputs(w, off):
+def _seeded_inputs(w, rank):
+    seed = mdist.seed_for(w.seed, rank)
     if w.kind == "rownorm":
-        return inputs.gemm_inputs(w.M, w.N, w.K, w.seed + 1000 * off, x_std=w.x_std, w_std=w.w_std,
+        return inputs.gemm_inputs(w.M, w.N, w.K, seed, x_std=w.x_std, w_std=w.w_std,
                                   bias_std=w.bias_std, gamma_std=w.gamma_std, beta_std=w.beta_std)
-    return inputs.gemm_inputs(w.M, w.N, w.K, w.seed + 1000 * off, x_std=w.x_std, w_std=w.w_std,
+    return inputs.gemm_inputs(w.M, w.N, w.K, seed, x_std=w.x_std, w_std=w.w_std,
                               bias_std=None, gamma_std=None, beta_std=None)
 
 
@@ -404,12 +403,8 @@ def run_ours(args):
     ws_, rank, local = dist_env()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    if ws_ > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=device)
-        barrier = lambda: dist.barrier()  # noqa: E731
-    else:
-        barrier = lambda: None  # noqa: E731
+    ranks = mdist.Ranks("nccl", device)
+    barrier = ranks.barrier
     peaks, peak_src = load_peaks()
     w = inputs.WORKLOADS[args.workload]
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -421,14 +416,9 @@ def run_ours(args):
         gpu_id = "GPU-" + gpu_id
     sampler = ClockSampler(gpu_id if gpu_id.startswith("GPU-") else str(local))
     t, n, clocks = time_steps(torch, runner, args.steps, args.warmup, barrier, sampler)
-    if ws_ > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t], device=device, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+    t = ranks.max(t)  # the slowest rank sets the job time
     t1 = t / n
-    total_flops = w.flops * n * ws_
-    value = total_flops / t / 1e12
+    value = mdist.job_throughput(w.flops * n, ws_, t) / 1e12
     troof, bound = roofline_time_s(w, peaks)
     kernel = {2: "gemm_fused_kernel<SOFTMAX>", 1: "gemm_fused_kernel<GELU_LN>", 0: "gemm_fused_kernel<LN>"}[kind_of(w)]
     if bound == "hbm":
@@ -458,7 +448,7 @@ def run_ours(args):
                    "batch_per_gpu": 1, "parallelism": f"replicas x{ws_} (rows independent)",
                    "l2": f"{nsets} rotating input/output sets (>= 3x L2 of {l2 >> 20} MiB)",
                    "plan": plan.as_dict()},
-        "hbm_gbs": round(w.unavoidable_bytes * n * ws_ / t / 1e9, 1),
+        "hbm_gbs": round(mdist.job_throughput(w.unavoidable_bytes * n, ws_, t) / 1e9, 1),
         "roofline_frac": round(troof / t1, 4),
         "roofline": roof,
         "gpu_launches": n,
@@ -479,10 +469,7 @@ def run_ours(args):
                                     "sample": f"{rows} whole rows of {w.name} (fp64 numpy oracle, "
                                               f"{secs:.1f} s; BLAS threads = cores, elementwise single-thread)"}
         print(json.dumps(line), flush=True)
-    if ws_ > 1:
-        import torch.distributed as dist
-        dist.barrier()
-        dist.destroy_process_group()
+    ranks.close()
 
 
 # ---------------------------------------------------------------------------
