@@ -472,6 +472,46 @@ def run_ours(args):
     ranks.close()
 
 
+def run_stitch(args):
+    """A stitched workload as the timed workload (GB/s; used to profile the
+    stitched kernels from a plain command line)."""
+    import torch
+    from memory_fusion_gb300 import cf
+
+    ws_, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    ranks = mdist.Ranks("nccl", device)
+    peaks, peak_src = load_peaks()
+    w = inputs.WORKLOADS[args.workload]
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    d = inputs.stitch_inputs(w.rows, w.cols, mdist.seed_for(w.seed, rank))
+    nsets = max(1, min(32, math.ceil(3 * l2 / w.unavoidable_bytes)))
+    A = [torch.from_numpy(d["A"]).to(device) for _ in range(nsets)]
+    b = torch.from_numpy(d["row_bias"]).to(device)
+    O = [torch.empty_like(A[0]) for _ in range(nsets)]
+    wsb = cf.cf_stitch_workspace_size(w.rows, w.cols)
+    ws = cf.new_workspace(wsb, device)
+
+    class R:
+        def launch(self, i, stream=None):
+            cf.check(cf.cf_stitch_rowreduce_broadcast(A[i % nsets], b, O[i % nsets], w.rows, w.cols, ws, wsb,
+                                                      stream))
+
+    t, n, _ = time_steps(torch, R(), args.steps, args.warmup, ranks.barrier)
+    t = ranks.max(t)
+    gbs = mdist.job_throughput(w.unavoidable_bytes * n, ws_, t) / 1e9
+    if rank == 0:
+        print(json.dumps({"metric": "stitched reduce->broadcast HBM GB/s", "value": round(gbs, 1), "unit": "GB/s",
+                          "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": round(t / n * 1e3, 6), "higher_is_better": True, "scaling": "weak",
+                          "config": {"workload": w.name, "rows": w.rows, "cols": w.cols},
+                          "roofline": {"bound": "hbm", "achieved": round(gbs / ws_, 1), "peak": peaks["hbm_gbs"],
+                                       "unit": "GB/s", "frac": round(gbs / ws_ / peaks["hbm_gbs"], 4)},
+                          "gpu_launches": n}), flush=True)
+    ranks.close()
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the fp64 CPU oracle
 # ---------------------------------------------------------------------------
@@ -518,8 +558,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100000)
     ap.add_argument("--warmup", type=int, default=200)
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(k for k, v in inputs.WORKLOADS.items()
-                                                                   if isinstance(v, inputs.GemmWorkload)))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip the per-workload table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -527,8 +566,14 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    stitched = isinstance(inputs.WORKLOADS[args.workload], inputs.StitchWorkload)
     if args.impl == "reference":
+        if stitched:
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times GEMM workloads"}))
+            return
         run_reference(args)
+    elif stitched:
+        run_stitch(args)
     else:
         run_ours(args)
 

@@ -349,8 +349,10 @@ cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *row_bias
         int C = t.cluster_size;
         if (C <= 0) {
             const int c_min = (ng + 256 * 16 - 1) / (256 * 16);
+            // about one CTA per SM for few rows (measured on the 64x30000 shape:
+            // 4 CTAs per row beat 8 and 16; the cluster barriers grow with C)
             int c_par = 1;
-            if (rows < 2 * dev.sm_count) c_par = next_pow2(int((2 * dev.sm_count + rows - 1) / rows));
+            if (rows < dev.sm_count) c_par = next_pow2(int((dev.sm_count + rows - 1) / rows));
             C = std::max(c_min, c_par);
             C = std::min(C, 16);
             while (C > 1 && C > ng) C >>= 1;

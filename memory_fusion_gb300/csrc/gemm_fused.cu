@@ -330,6 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             // barrier receives both CTAs' tiles)
             const uint32_t tx_cta = uint32_t(kABytes) + uint32_t(my_boxes) * 8192u;
             const uint32_t tx = kPair ? 2u * tx_cta : tx_cta;
+            // W tiles are reused by every row block: keep them in L2 ahead of the
+            // streaming output
+            const uint64_t pol_w = ptx::policy_evict_last();
             uint32_t it = 0;
             int ptile = 0;
             for (int t = cid; t < T; t += ncl, ++ptile) {
@@ -352,15 +355,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         ptx::tma_load_2d_pair(sa, &a.tmap_x, fbl, kb * kBK, m0);
                         // this CTA stages W columns [m_sub * ns/2, +ns/2) of the 256-row MMA's N
                         for (int j = 0; j < my_boxes; ++j)
-                            ptx::tma_load_2d_pair(sb + j * 8192, &a.tmap_w, fbl, n0 + (m_sub * my_boxes + j) * 64,
-                                                  kb * kBK);
+                            ptx::tma_load_2d_pair_hint(sb + j * 8192, &a.tmap_w, fbl,
+                                                       n0 + (m_sub * my_boxes + j) * 64, kb * kBK, pol_w);
                     } else {
                         ptx::mbar_arrive_expect_tx(fb, tx);  // the whole stage, whoever loads it
                         const uint32_t adst = sa + uint32_t(mcx ? rank : 0u) * uint32_t(a_rows) * 128u;
                         if (mcx) ptx::tma_load_2d_mc(adst, &a.tmap_x, fb, kb * kBK, m0 + int(rank) * a_rows, a_mask);
                         else ptx::tma_load_2d(adst, &a.tmap_x, fb, kb * kBK, m0);
                         for (int j = 0; j < nbox; ++j)
-                            ptx::tma_load_2d(sb + j * 8192, &a.tmap_w, fb, n0 + j * 64, kb * kBK);
+                            ptx::tma_load_2d_hint(sb + j * 8192, &a.tmap_w, fb, n0 + j * 64, kb * kBK, pol_w);
                     }
                     if (kb == 0) trace_tile(a.trace, ptile, CF_TR_TMA_FIRST);
                     if (kb == nk - 1) trace_tile(a.trace, ptile, CF_TR_TMA_LAST);
@@ -458,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
         float *const prm = reinterpret_cast<float *>(gbase + L.prm) + grp * 768;
         const uint32_t stg0 = base + L.stg + uint32_t(e) * 2048u * uint32_t(a.stg_bufs);  // this warp's staging
         uint32_t nstore = 0;  // stores issued by this warp (selects the staging buffer)
+        const uint64_t pol_y = ptx::policy_evict_first();  // output is written once
         const float fN = float(a.N);
         const int nchunks = ns / 32;  // 2, 4 or 8 fragments of 32 columns per thread
         float *const pb = prm;        // bias, gamma, beta of this group's current tile
@@ -526,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                                 ptx::fence_proxy_async_smem();
                                 __syncwarp();
                                 if (lane == 0) {
-                                    ptx::tma_store_2d(&a.tmap_y, stg, ncta + (c + (k >> 1)) * 32 + hh * 16, ystore);
+                                    ptx::tma_store_2d_hint(&a.tmap_y, stg, ncta + (c + (k >> 1)) * 32 + hh * 16, ystore, pol_y);
                                     ptx::bulk_commit_group();
                                 }
                                 ++nstore;
@@ -766,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                             ptx::fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                ptx::tma_store_2d(&a.tmap_y, stg, ncta + cc * 32, ystore);
+                                ptx::tma_store_2d_hint(&a.tmap_y, stg, ncta + cc * 32, ystore, pol_y);
                                 ptx::bulk_commit_group();
                             }
                             ++nstore;

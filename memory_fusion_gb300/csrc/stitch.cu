@@ -235,8 +235,11 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
     }
     // the next grid may be scheduled once this CTA's rows are written
     ptx::griddep_launch_dependents();
-    // no CTA leaves while a peer may still access its shared memory
-    ptx::cluster_sync();
+    // No CTA leaves while a peer may still access its shared memory.  Every
+    // remote write was ordered by the last exchange barrier (release/acquire),
+    // so this one needs no release: it must not wait for the row's global stores.
+    ptx::cluster_arrive_relaxed();
+    ptx::cluster_wait_acquire();
 }
 
 template <int LPR, bool VEC>
