@@ -184,34 +184,41 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
     const cf_tuning &t = tuning ? *tuning : tz;
     if (K % 64 != 0 || N % 64 != 0) return CF_ERR_UNSUPPORTED;
     if (M > (int64_t(1) << 31) - 128 || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return CF_ERR_UNSUPPORTED;
-    int ns = t.n_slice;
-    if (ns == 0) ns = (N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64;
-    if ((ns != 64 && ns != 128 && ns != 256) || N % ns != 0) return CF_ERR_UNSUPPORTED;
-    const int64_t cpr64 = N / ns;
-    if (cpr64 > 16 * 64) return CF_ERR_UNSUPPORTED;
-    const int cpr = int(cpr64);
+    // n_slice candidates: the requested one, else the widest of 256/128/64 that
+    // divides N and, when 512 divides N, the wide tile (512 columns: all of
+    // tensor memory, both epilogue groups on one tile)
+    const int ns_narrow = (N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64;
+    if (t.n_slice != 0 && ((t.n_slice != 64 && t.n_slice != 128 && t.n_slice != 256 && t.n_slice != 512) ||
+                           N % t.n_slice != 0))
+        return CF_ERR_UNSUPPORTED;
+    if (N / ns_narrow > 16 * 64) return CF_ERR_UNSUPPORTED;
     const int rb = int((M + cf::kBlockM - 1) / cf::kBlockM);
     const int nk = int(K / 64);
-    // Choose C_N (CTAs along a row, a divisor of the CTAs per row) and C_M (row
-    // blocks per cluster: 2 = CTA pairs sharing one cta_group::2 MMA stream) by
-    // predicted time.  The persistent grid holds ncl clusters (never more than
-    // can be resident); each takes per = ceil(T / ncl) of T = ceil(row_blocks /
-    // C_M) * G tickets, one tile per CTA each.  With two TMEM accumulators and
-    // two epilogue groups, tiles go in rounds of two: a round costs
-    // max(2 mainloops, one epilogue).  Constants measured on GB300 with the
-    // device trace (128x256 tiles per CTA):
+    // Choose n_slice, C_N (CTAs along a row, a divisor of the CTAs per row) and
+    // C_M (row blocks per cluster: 2 = CTA pairs sharing one cta_group::2 MMA
+    // stream) by predicted time.  The persistent grid holds ncl clusters (never
+    // more than can be resident); each takes per = ceil(T / ncl) of T =
+    // ceil(row_blocks / C_M) * G tickets, one tile per CTA each.  With two TMEM
+    // accumulators and two epilogue groups, tiles go in rounds of two: a round
+    // costs max(2 mainloops, one epilogue).  A wide tile has one accumulator, so
+    // its tiles run one after another: mainloop + epilogue each.  Constants
+    // measured on GB300 with the device trace (128x256 tiles per CTA):
     //   mainloop  ~ 0.48 us per 64-deep k-block for a CTA pair, 0.55 us single
+    //               (per 256 columns of W staged)
     //   epilogue  ~ 4.5 us; + 1.5 + 0.2 G us when the row spans G > 1 clusters
     //               (the global barrier waits for the slowest of G clusters);
     //               + 0.5 us for a CTA pair when K < 512
     //   skew      ~ 0.05 G us per tile when G > 1
     // Rows wider than one row group need all G clusters of a row block
-    // resident (ncl >= G).
-    auto predict = [&](int cn, int cm, int *ncl_out) -> double {
+    // resident (ncl >= G); a wide tile's row never leaves its cluster (G = 1).
+    auto predict = [&](int ns, int cn, int cm, int *ncl_out) -> double {
+        const int cpr = int(N / ns);
         const int c = cn * cm;
+        const bool wide = ns > 256;
         if (cn < 1 || c > 16 || cpr % cn != 0 || max_active_clusters[c] <= 0) return -1.0;
-        if (cm == 2 && (ns < 128 || rb < 2)) return -1.0;
+        if (cm == 2 && (ns < 128 || rb < 2 || wide)) return -1.0;
         const int g = cpr / cn;
+        if (wide && g > 1) return -1.0;
         int n = max_active_clusters[c];
         if (t.max_clusters > 0) n = std::min(n, int(t.max_clusters));
         if (g > 1 && n < g) return -1.0;
@@ -221,31 +228,45 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
         const double t_main = nk * (cm == 2 ? 0.48 : 0.55) * (ns / 256.0);
         const double t_epi = 4.5 + (g > 1 ? 1.5 + 0.2 * g : 0.0) + (cm == 2 && nk < 8 ? 0.5 : 0.0);
         *ncl_out = n;
+        if (wide) return double(per) * (t_main + t_epi);
         return double((per + 1) / 2) * std::max(2.0 * t_main, t_epi) + t_main + (g > 1 ? per * 0.05 * g : 0.0);
     };
-    int C = 0, CMs = 0, ncl = 0;
+    int ns = 0, C = 0, CMs = 0, ncl = 0;
     {
         double best = 0.0;
-        for (int cm = 2; cm >= 1; --cm) {
-            if (t.cluster_m > 0 && cm != t.cluster_m) continue;
-            for (int cn = std::min(16, cpr); cn >= 1; --cn) {  // larger clusters win ties
-                if (t.cluster_size > 0 && cn != t.cluster_size) continue;
-                int n = 0;
-                const double e = predict(cn, cm, &n);
-                if (e > 0.0 && (C == 0 || e < best * (1.0 - 1e-9))) {
-                    best = e;
-                    C = cn;
-                    CMs = cm;
-                    ncl = n;
+        const int cand[2] = {t.n_slice != 0 ? int(t.n_slice) : ns_narrow,
+                             (t.n_slice == 0 && N % 512 == 0) ? 512 : 0};
+        for (int ci = 0; ci < 2; ++ci) {
+            const int nsc = cand[ci];
+            if (nsc == 0) continue;
+            const int cpr = int(N / nsc);
+            for (int cm = 2; cm >= 1; --cm) {
+                if (t.cluster_m > 0 && cm != t.cluster_m) continue;
+                for (int cn = std::min(16, cpr); cn >= 1; --cn) {  // larger clusters win ties
+                    if (t.cluster_size > 0 && cn != t.cluster_size) continue;
+                    int n = 0;
+                    const double e = predict(nsc, cn, cm, &n);
+                    if (e > 0.0 && (C == 0 || e < best * (1.0 - 1e-9))) {
+                        best = e;
+                        ns = nsc;
+                        C = cn;
+                        CMs = cm;
+                        ncl = n;
+                    }
                 }
             }
         }
         if (C == 0) {
+            const int cpr = int(N / cand[0]);
             if (t.cluster_size > 16 || (t.cluster_size > 0 && cpr % t.cluster_size != 0)) return CF_ERR_UNSUPPORTED;
             if (t.cluster_m > 2 || t.cluster_m < 0) return CF_ERR_UNSUPPORTED;
+            // a wide tile's row must fit one cluster of at most 16, without pairs
+            if (cand[0] > 256 && (cpr > 16 || t.cluster_m == 2 || (t.cluster_size > 0 && t.cluster_size != cpr)))
+                return CF_ERR_UNSUPPORTED;
             return CF_ERR_NOT_RESIDENT;
         }
     }
+    const int cpr = int(N / ns);
     const int G = cpr / C;
     const int peer_max = t.peer_max == 0 ? 8 : t.peer_max;
     plan->n_slice = ns;
@@ -391,8 +412,11 @@ static cf_status device_plan(int kind, int64_t M, int64_t N, int64_t K, const cf
     cf_tuning_default(&tz);
     const cf_tuning &t = tuning ? *tuning : tz;
     if (N <= 0 || K <= 0 || N % 64 != 0 || K % 64 != 0) return CF_ERR_UNSUPPORTED;
+    // residency is queried at the narrow tile's shared memory; a wide tile's is
+    // also above half of the SM's, so it is one CTA per SM all the same
     int ns = t.n_slice ? t.n_slice : ((N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64);
-    if ((ns != 64 && ns != 128 && ns != 256) || N % ns != 0) return CF_ERR_UNSUPPORTED;
+    if ((ns != 64 && ns != 128 && ns != 256 && ns != 512) || N % ns != 0) return CF_ERR_UNSUPPORTED;
+    if (ns == 512) ns = 256;
     const int64_t cpr = N / ns;
     for (int c = 0; c <= 16; ++c) active[c] = 0;
     // residency is per SM (one CTA per SM at any of these shared-memory

@@ -6,7 +6,9 @@
 //     SOFTMAX:  y = softmax(scale*acc + bias)
 //
 // Design (GB300-first; the page mechanisms it realises are cited inline):
-//  * Tiles are 128 rows x n_slice columns (n_slice <= 256).  A row block's
+//  * Tiles are 128 rows x n_slice columns (n_slice <= 256; or 512, a wide
+//    tile filling all of tensor memory, which both epilogue groups share, one
+//    half of its columns each).  A row block's
 //    N / n_slice tiles go to the CTAs of one thread-block cluster (CTA rank
 //    r -> column slice r), so all CTAs of one reduction are co-scheduled
 //    ([ComFuse] Stage-Stream Execution Model, cluster mapping).  Rows wider
@@ -80,6 +82,7 @@ struct SmemLayout {
     uint32_t slot;         // float2 [4][C][128]: the row group's partials, by exchange set
     uint32_t res;          // float2 [4][128]: leader-follower result, by exchange set
     uint32_t prm;          // float [2][3][256]: bias, gamma, beta of the tile's columns, per group
+    uint32_t comb;         // float2 [2][128]: the two groups' half-row partials of a wide tile
     uint32_t bars;         // mbarriers
     uint32_t total;        // bytes from the aligned base
 };
@@ -105,6 +108,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n
     off += (leader ? xc : 0u) * kXSets * 128 * 8;
     L.prm = off;
     off += 2 * 3 * 256 * 4;
+    L.comb = off;  // only a wide tile (n_slice 512) has two groups on one row
+    off += (n_slice > 256 ? 2u * 128u * 8u : 0u);
     L.bars = off;
     off += 256;
     L.total = off;
@@ -235,7 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     // The 128B-swizzled operand tiles need a 1024-byte aligned ring.  The
     // dynamic shared window starts aligned; if it ever did not, report it and
     // do nothing (every CTA sees the same base, so none enters a cluster barrier).
-    if ((base & 1023u) != 0u) {
+    // A wide tile's two groups cannot share the global path: the host never plans
+    // that; refuse it the same way.
+    if ((base & 1023u) != 0u || (a.n_slice > 256 && a.groups > 1)) {
         ptx::griddep_wait();
         if (threadIdx.x == 0) ptx::record_error(a.err, 8u /*CF_ERR_DEVICE_BOUNDS*/, 0x60000000u | (base & 1023u));
         return;
@@ -245,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     const int CM = kPair ? 2 : 1;           // row blocks per cluster
     const int G = a.groups;
     const int ns = a.n_slice;
-    const int half = ns / 2;
+    // a wide tile (512 columns) takes both accumulators and both epilogue groups
+    const bool wide = !kPair && EPI != EPI_STORE_F32 && ns > 256;
     const int nk = a.K / kBK;
     const int T = a.super_blocks * G;       // tickets: (super row block, cluster group), row-block major
     const int nbox = ns / 64;               // 64-column W boxes of a tile
@@ -273,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     uint16_t a_mask = uint16_t(1u << crank);
     if (mcx) a_mask = uint16_t((1u << C) - 1u);
     const int a_rows = mcx ? kBlockM / C : kBlockM;  // rows of the X tile this CTA loads
-    const uint32_t tmem_cols = (ns * 2 <= 32) ? 32u : uint32_t(ns * 2);
+    const uint32_t tmem_cols = wide ? 512u : (ns * 2 <= 32) ? 32u : uint32_t(ns * 2);
     const unsigned long long t_start = ptx::globaltimer();  // traced after the dependency wait
 
     if (threadIdx.x == 0) {
@@ -284,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(B.tmem_full0 + 8 * b, 1);
             // one epilogue group (4 warps) drains each accumulator; the pair
-            // leader waits for both CTAs' groups
-            ptx::mbar_init(B.tmem_empty0 + 8 * b, kPair ? 2 * kGroupWarps : kGroupWarps);
+            // leader waits for both CTAs' groups; a wide tile, for both groups
+            ptx::mbar_init(B.tmem_empty0 + 8 * b, kPair ? 2 * kGroupWarps : wide ? kEpiWarps : kGroupWarps);
         }
         for (int x = 0; x < kXSets; ++x) {
             ptx::mbar_init(B.xfull0 + 8 * x, 1);
@@ -386,13 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && is_leader) {
-            const uint32_t idesc = idesc_bf16(kPair ? 2 * kBlockM : kBlockM, ns);
+            // a wide tile is two N = 256 MMAs per K step into adjacent TMEM columns
+            const uint32_t idesc = idesc_bf16(kPair ? 2 * kBlockM : kBlockM, wide ? 256 : ns);
             const uint16_t pair_mask = uint16_t(3u << pair_leader);
             uint32_t it = 0;
             int tile = 0;
             for (int t = cid; t < T; t += ncl, ++tile) {
-                const uint32_t buf = tile & 1;
-                const uint32_t tph = (uint32_t(tile) >> 1) & 1u;
+                const uint32_t buf = wide ? 0u : uint32_t(tile & 1);
+                const uint32_t tph = wide ? (uint32_t(tile) & 1u) : ((uint32_t(tile) >> 1) & 1u);
                 ptx::mbar_wait_bounded(B.tmem_empty0 + 8 * buf, tph ^ 1u, tmo, abort, a.err, kInfoMma | buf);
                 if (*abort) break;
                 trace_tile(a.trace, tile, CF_TR_MMA_ACC_FREE);
@@ -419,8 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         // B: MN-major, 64-column blocks 8 KB apart, 8-row K groups 1 KB apart;
                         // advance 16 K rows = 2 KB
                         const uint64_t bd = sw128_desc(sb + k * 2048, 8192, 1024);
-                        if constexpr (kPair) ptx::mma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-                        else ptx::mma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        if constexpr (kPair) {
+                            ptx::mma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        } else {
+                            ptx::mma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                            // wide: columns 256..511 from W boxes 4..7
+                            if (wide)
+                                ptx::mma_bf16(d + 256u, ad, sw128_desc(sb + 4 * 8192 + k * 2048, 8192, 1024), idesc,
+                                              (kb | k) != 0 ? 1u : 0u);
+                        }
                     }
                     // the stage is free once these MMAs completed: tell every CTA whose
                     // producer filled it
@@ -463,18 +479,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
         uint32_t nstore = 0;  // stores issued by this warp (selects the staging buffer)
         const uint64_t pol_y = ptx::policy_evict_first();  // output is written once
         const float fN = float(a.N);
-        const int nchunks = ns / 32;  // 2, 4 or 8 fragments of 32 columns per thread
+        const int ecols = wide ? 256 : ns;       // columns of a tile this group handles
+        const int coff = wide ? grp * 256 : 0;   // and their offset within the tile
+        const int nchunks = ecols / 32;          // 2, 4 or 8 fragments of 32 columns per thread
+        float2 *const comb = reinterpret_cast<float2 *>(gbase + L.comb);
         float *const pb = prm;        // bias, gamma, beta of this group's current tile
         float *const pg = prm + 256;
         float *const pe = prm + 512;
 
-        int tile = grp;
-        for (int t = cid + grp * ncl; t < T; t += 2 * ncl, tile += 2) {
+        const int tstep = wide ? 1 : 2;  // PingPong: alternate tiles; wide: every tile
+        int tile = wide ? 0 : grp;
+        for (int t = cid + (wide ? 0 : grp) * ncl; t < T; t += tstep * ncl, tile += tstep) {
             const int rb = (t / G) * CM + m_sub, g = t % G;
             const int m0 = rb * kBlockM;
-            const int ncta = (g * C + int(rank)) * ns;  // first global column of this CTA's tile
-            const uint32_t buf = uint32_t(grp);
-            const uint32_t tph = (uint32_t(tile) >> 1) & 1u;
+            const int ncta = (g * C + int(rank)) * ns + coff;  // first global column this group handles
+            const uint32_t buf = wide ? 0u : uint32_t(grp);
+            const uint32_t tph = wide ? (uint32_t(tile) & 1u) : ((uint32_t(tile) >> 1) & 1u);
             const uint32_t xs = uint32_t(tile) & 3u;    // exchange buffer set
             const uint32_t xph = (uint32_t(tile) >> 2) & 1u;
 
@@ -482,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             // buffer, fetched before the accumulator is ready; the group's previous
             // tile finished reading them before the group barrier that ended it.
             if constexpr (EPI != EPI_STORE_F32) {
-                for (int c = gt; c < ns; c += kGroupThreads) {
+                for (int c = gt; c < ecols; c += kGroupThreads) {
                     pb[c] = a.bias ? __ldg(a.bias + ncta + c) : 0.f;
                     if constexpr (EPI != EPI_SOFTMAX) {
                         pg[c] = __ldg(a.gamma + ncta + c);
@@ -494,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             ptx::tc_fence_after();
             ptx::named_bar_sync(bar_grp, kGroupThreads);  // parameters visible to the group
             if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_START);
-            const uint32_t tacc = tmem_base + (uint32_t(q * 32) << 16) + buf * uint32_t(ns);
+            const uint32_t tacc = tmem_base + (uint32_t(q * 32) << 16) + buf * uint32_t(ns) + uint32_t(coff);
 
             if constexpr (EPI == EPI_STORE_F32) {
                 // Unfused-baseline mode: the raw fp32 accumulator tile is written to
@@ -595,16 +615,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             }
             if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_STATS);
 
-            // ---------------- level 2: the CTA statistic of a row is one thread's; it
-            // goes into the unified reduce buffer of this exchange set
-            if (C > 1) {
+            // ---------------- level 2: the CTA statistic of a row is one thread's (a wide
+            // tile: two threads', one per group, combined through shared memory in a
+            // fixed order so both groups hold the same value); group 0's goes into the
+            // unified reduce buffer of this exchange set
+            if (wide) {
+                comb[grp * 128 + row] = part;
+                ptx::named_bar_sync(3u, 2 * kGroupThreads);
+                const float2 p0 = comb[row], p1 = comb[128 + row];
+                if constexpr (EPI == EPI_SOFTMAX) {
+                    const MaxSum m = combine_maxsum(MaxSum{p0.x, p0.y}, MaxSum{p1.x, p1.y});
+                    part = make_float2(m.m, m.s);
+                } else {
+                    const MeanM2 m = combine_equal(MeanM2{p0.x, p0.y}, MeanM2{p1.x, p1.y}, float(ecols));
+                    part = make_float2(m.mean, m.m2);
+                }
+            }
+            const bool sender = !wide || grp == 0;  // the group that sends this CTA's partial
+            if (C > 1 && sender) {
                 send[xs * 128 + row] = part;
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar_sync(bar_grp, kGroupThreads);
             }
             if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_CTA);
             // ---------------- level 3: inter-CTA over DSMEM (TMA bulk copies)
-            if (C > 1 && gt0 && !*abort) {
+            if (C > 1 && sender && gt0 && !*abort) {
                 const uint32_t src = base + L.send + xs * 1024;
                 const uint32_t my_slot = base + L.slot + (xs * C + rank) * 1024;
                 const uint32_t xfull = B.xfull0 + 8 * xs;
@@ -628,19 +663,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             } else {
                 if (rank == 0) {
                     ptx::mbar_wait_bounded<true>(B.xfull0 + 8 * xs, xph, tmo, abort, a.err, kInfoXchg | xs);
-                    res[xs * 128 + row] = combine_slots<EPI == EPI_SOFTMAX>(slot + xs * C * 128 + row, C, float(ns));
-                    ptx::fence_proxy_async_smem();
-                    ptx::named_bar_sync(bar_grp, kGroupThreads);
-                    if (gt0 && !*abort) {
-                        const uint32_t src = base + L.res + xs * 1024;
-                        for (int r = 1; r < C; ++r)
-                            ptx::bulk_copy_s2cluster(ptx::mapa(src, r * CM + m_sub), src, 1024,
-                                                     ptx::mapa(B.xres0 + 8 * xs, r * CM + m_sub));
+                    stat = combine_slots<EPI == EPI_SOFTMAX>(slot + xs * C * 128 + row, C, float(ns));
+                    if (sender) {
+                        res[xs * 128 + row] = stat;
+                        ptx::fence_proxy_async_smem();
+                        ptx::named_bar_sync(bar_grp, kGroupThreads);
+                        if (gt0 && !*abort) {
+                            const uint32_t src = base + L.res + xs * 1024;
+                            for (int r = 1; r < C; ++r)
+                                ptx::bulk_copy_s2cluster(ptx::mapa(src, r * CM + m_sub), src, 1024,
+                                                         ptx::mapa(B.xres0 + 8 * xs, r * CM + m_sub));
+                        }
                     }
                 } else {
                     ptx::mbar_wait_bounded<true>(B.xres0 + 8 * xs, xph, tmo, abort, a.err, kInfoXchg | 0x10u | xs);
+                    stat = res[xs * 128 + row];
                 }
-                stat = res[xs * 128 + row];
             }
             if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_CLUSTER);
 

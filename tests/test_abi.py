@@ -78,7 +78,7 @@ def test_plan_chooses_fastest_predicted():
     CTA in rounds of two (two accumulators, two epilogue groups), each round
     max(2 mainloops, epilogue), plus the global barrier's skew."""
     cases = {
-        (4096, 2048, 128): (4, 1, 2, 36),     # 2 tiles per CTA (one round) beats 3 in a cluster of 8
+        (4096, 2048, 128): (4, 1, 1, 32),     # wide tiles: one per CTA, each row in one cluster of 4
         (16384, 4096, 4096): (1, 2, 16, 76),  # CTA pairs (cta_group::2), rows over 16 clusters
         (8192, 16384, 2048): (2, 2, 32, 36),  # CTA pairs, rows over 32 clusters
         (128, 512, 256): (2, 1, 1, 1),        # one row block: no pair
@@ -88,6 +88,21 @@ def test_plan_chooses_fastest_predicted():
         assert st == cf.CF_OK
         assert (p.cluster_size, p.cluster_m, p.groups, p.clusters) == (C, CM, G, ncl), (M, N, K, p.as_dict())
         assert p.smem_bytes <= 232448
+
+
+def test_plan_wide_tile():
+    """n_slice 512: one tile fills tensor memory and both epilogue groups share it; the
+    row must stay in one cluster (G = 1) of at most 16, with single-CTA MMAs."""
+    st, p = cf.cf_plan_gemm_fused(4096, 2048, 128, 152, GB300, cf.tuning(n_slice=512))
+    assert st == cf.CF_OK
+    assert (p.n_slice, p.ctas_per_row, p.cluster_size, p.groups, p.cluster_m, p.clusters) == (512, 4, 4, 1, 1, 32)
+    assert p.stages == 2 and p.smem_bytes <= 232448
+    for M, N, kw in [(256, 4096, dict(cluster_size=4)), (256, 16384, {}), (512, 1024, dict(cluster_m=2))]:
+        st, _ = cf.cf_plan_gemm_fused(M, N, 128, 152, GB300, cf.tuning(n_slice=512, **kw))
+        assert st == cf.CF_ERR_UNSUPPORTED, (M, N, kw)
+    # N not a multiple of 512: no wide candidate, and a request for one is refused
+    st, _ = cf.cf_plan_gemm_fused(256, 768, 128, 152, GB300, cf.tuning(n_slice=512))
+    assert st == cf.CF_ERR_UNSUPPORTED
 
 
 def test_plan_pair_mode_limits():

@@ -78,7 +78,7 @@ def test_rownorm_small(M, N, K, act):
     check_ln(_rownorm(d, act=act), _ref_ln(d, act=act), f"{M}x{N}x{K} {act}")
 
 
-@pytest.mark.parametrize("n_slice", [64, 128, 256])
+@pytest.mark.parametrize("n_slice", [64, 128, 256, 512])
 def test_rownorm_tile_widths(n_slice):
     d = _ln_inputs(200, 1024, 128, seed=7)
     check_ln(_rownorm(d, tuning=cf.tuning(n_slice=n_slice)), _ref_ln(d), f"n_slice={n_slice}")
@@ -112,6 +112,37 @@ def test_rownorm_multicast_clusters(C, CM, N, M, leader):
     st, plan, _ = cf.cf_query_gemm_fused_plan(M, N, 192, 1, t)
     assert st == cf.CF_OK and plan.cluster_m == CM and plan.cluster_size == C
     check_ln(_rownorm(d, act="gelu_tanh", tuning=t), _ref_ln(d, act="gelu_tanh"), f"C={C} CM={CM} N={N}")
+
+
+@pytest.mark.parametrize("C,leader,epi,M,K,max_clusters", [
+    (1, 0, "none", 300, 256, 0), (2, 0, "gelu_tanh", 260, 128, 0), (4, 0, "softmax", 300, 128, 0),
+    (4, 1, "gelu_tanh", 200, 192, 0), (8, 0, "none", 129, 64, 0), (8, 1, "softmax", 257, 128, 0),
+    (2, 0, "softmax", 1000, 128, 2), (2, 1, "gelu_tanh", 1100, 64, 1),
+])
+def test_wide_tile_modes(C, leader, epi, M, K, max_clusters):
+    """Wide tiles (n_slice 512: all of tensor memory, both epilogue groups on one tile,
+    their half-row statistics combined in shared memory) in clusters of C, peer or
+    leader-follower; with few clusters every CTA runs several wide tiles in a row
+    (one accumulator: phases and exchange sets advance every tile)."""
+    N = 512 * C
+    t = cf.tuning(n_slice=512, cluster_size=C, peer_max=-1 if leader else 16, max_clusters=max_clusters)
+    kind = 2 if epi == "softmax" else (1 if epi == "gelu_tanh" else 0)
+    st, plan, _ = cf.cf_query_gemm_fused_plan(M, N, K, kind, t)
+    assert st == cf.CF_OK and plan.n_slice == 512 and plan.groups == 1 and plan.cluster_size == C
+    if epi == "softmax":
+        d = inputs.gemm_inputs(M, N, K, seed=90 + C, x_std=1.0, w_std=K ** -0.5,
+                               bias_std=0.5, gamma_std=None, beta_std=None)
+        ref = oracle.gemm_rowsoftmax(d["X"], d["W"], scale=K ** -0.5, bias=d["bias"])
+        check_softmax(_softmax(d, K ** -0.5, bias=d["bias"], tuning=t), ref, f"wide softmax C={C}")
+    else:
+        d = _ln_inputs(M, N, K, seed=95 + C)
+        check_ln(_rownorm(d, act=epi, tuning=t), _ref_ln(d, act=epi), f"wide {epi} C={C} leader={leader}")
+
+
+def test_wide_tile_x_multicast():
+    d = _ln_inputs(300, 2048, 128, seed=78)
+    t = cf.tuning(n_slice=512, cluster_size=4, multicast_x=1)
+    check_ln(_rownorm(d, act="gelu_tanh", tuning=t), _ref_ln(d, act="gelu_tanh"), "wide multicast_x")
 
 
 def test_rownorm_x_multicast_row_group():
@@ -207,7 +238,8 @@ def test_global_barrier_timeout_is_reported():
     M, K, N = 256, 64, 1024
     ws = cf.new_workspace(cf.cf_gemm_fused_workspace_size(M, N, K))
     Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    t = cf.tuning(cluster_size=2, extra_arrivals=1, timeout_us=20000)
+    # 256-column tiles: four per row, two clusters of two meet at the global barrier
+    t = cf.tuning(n_slice=256, cluster_size=2, extra_arrivals=1, timeout_us=20000)
     st = cf.cf_gemm_fused_rownorm(dev_bf16(d["X"]), dev_bf16(d["W"]), dev_f32(d["bias"]), dev_f32(d["gamma"]),
                                   dev_f32(d["beta"]), Y, M, N, K, 1.0, 1e-5, 0, ws, ws.numel(), None, t)
     assert st == cf.CF_OK
@@ -217,4 +249,4 @@ def test_global_barrier_timeout_is_reported():
     # the context is still usable and the error word was cleared by the read
     assert cf.cf_get_device_status(ws)[0] == cf.CF_OK
     cf.check(cf.cf_workspace_init(ws, ws.numel()))
-    check_ln(_rownorm(d, tuning=cf.tuning(cluster_size=2), ws=ws), _ref_ln(d), "after timeout")
+    check_ln(_rownorm(d, tuning=cf.tuning(n_slice=256, cluster_size=2), ws=ws), _ref_ln(d), "after timeout")
