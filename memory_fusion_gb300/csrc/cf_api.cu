@@ -73,6 +73,25 @@ bool make_tmap_bf16(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t col
     return r == CUDA_SUCCESS;
 }
 
+// W [K, N] bf16 row-major as a 3-D tensor {64 columns, K rows, N/64 column
+// blocks} with strides N*2 and 128 bytes; a box of `blocks` 64x64 blocks lands
+// as consecutive 8 KB, 128B-swizzled blocks (the MN-major B operand layout)
+bool make_tmap_w(CUtensorMap *m, const void *ptr, uint64_t K, uint64_t N, uint32_t blocks) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, K, N / 64};
+    cuuint64_t strides[2] = {N * 2, 128};
+    cuuint32_t box[3] = {64, 64, blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// W column blocks one CTA stages per k-block (a CTA of a pair: half the tile's)
+uint32_t w_blocks(int n_slice, int cluster_m) { return uint32_t(n_slice / 64 / (cluster_m == 2 ? 2 : 1)); }
+
 // 2-D fp32 tensor map over a row-major [rows, cols] matrix for TMA stores of
 // 16-column x 32-row blocks (64-byte rows, 64B swizzle)
 bool make_tmap_f32_store(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols) {
@@ -479,7 +498,8 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
         if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, mcx ? 128 / plan.cluster_size : 128))
             return CF_ERR_CUDA;
     }
-    if (!make_tmap_bf16(&a.tmap_w, W, uint64_t(K), uint64_t(N), 64, 64)) return CF_ERR_CUDA;
+    if (!make_tmap_w(&a.tmap_w, W, uint64_t(K), uint64_t(N), w_blocks(plan.n_slice, plan.cluster_m)))
+        return CF_ERR_CUDA;
     if (!make_tmap_bf16(&a.tmap_y, Y, uint64_t(M), uint64_t(N), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return CF_ERR_CUDA;
     a.bias = bias;
     a.gamma = gamma;
@@ -623,7 +643,8 @@ extern "C" cf_status cf_gemm_fused_rownorm_noalloc(const void *X, const void *W,
     cf::GemmArgs a;
     std::memset(&a, 0, sizeof(a));
     if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, 128)) return CF_ERR_CUDA;
-    if (!make_tmap_bf16(&a.tmap_w, W, uint64_t(K), uint64_t(N), 64, 64)) return CF_ERR_CUDA;
+    if (!make_tmap_w(&a.tmap_w, W, uint64_t(K), uint64_t(N), w_blocks(plan.n_slice, plan.cluster_m)))
+        return CF_ERR_CUDA;
     if (!make_tmap_bf16(&a.tmap_y, Y, uint64_t(M), uint64_t(N), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return CF_ERR_CUDA;
     uint8_t *sb = static_cast<uint8_t *>(scratch);
     a.bias = bias;
@@ -689,7 +710,7 @@ cf_status gemm_store_f32(const void *X, const void *W, float *P, uint32_t *err, 
     cf::GemmArgs a;
     std::memset(&a, 0, sizeof(a));
     if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, 128)) return CF_ERR_CUDA;
-    if (!make_tmap_bf16(&a.tmap_w, W, uint64_t(K), uint64_t(N), 64, 64)) return CF_ERR_CUDA;
+    if (!make_tmap_w(&a.tmap_w, W, uint64_t(K), uint64_t(N), w_blocks(ns, cm))) return CF_ERR_CUDA;
     if (!make_tmap_f32_store(&a.tmap_y, P, uint64_t(M), uint64_t(N))) return CF_ERR_CUDA;
     a.err = err;
     a.M = int(M);

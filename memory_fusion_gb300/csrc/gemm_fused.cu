@@ -341,18 +341,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             // W tiles are reused by every row block: keep them in L2 ahead of the
             // streaming output
             const uint64_t pol_w = ptx::policy_evict_last();
-            uint32_t it = 0;
+            uint32_t it = 0;         // k-blocks issued
+            uint32_t s = 0, ph = 0;  // their ring position
+            bool ok = true;
             int ptile = 0;
-            for (int t = cid; t < T; t += ncl, ++ptile) {
+            for (int t = cid; t < T && ok; t += ncl, ++ptile) {
                 const int rb = (t / G) * CM + m_sub, g = t % G;
                 const int m0 = rb * kBlockM;
                 const int n0 = (g * C + int(rank)) * ns;
-                for (int kb = 0; kb < nk; ++kb, ++it) {
-                    const uint32_t s = it % uint32_t(stages);
-                    const uint32_t ph = (it / uint32_t(stages)) & 1u;
+                for (int kb = 0; kb < nk; ++kb) {
                     // every CTA that reads this stage has released it
-                    ptx::mbar_wait_bounded(B.empty0 + 8 * s, ph ^ 1u, tmo, abort, a.err, kInfoProducer | s);
-                    if (*abort) break;
+                    ok = ptx::mbar_wait_bounded(B.empty0 + 8 * s, ph ^ 1u, tmo, abort, a.err, kInfoProducer | s);
+                    if (!ok) break;
                     const uint32_t sa = base + L.ring + s * L.stage_bytes;
                     const uint32_t sb = sa + kABytes;
                     const uint32_t fb = B.full0 + 8 * s;
@@ -361,22 +361,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         const uint32_t fbl = ptx::mapa(fb, pair_leader);
                         if (is_leader) ptx::mbar_arrive_expect_tx(fb, tx);
                         ptx::tma_load_2d_pair(sa, &a.tmap_x, fbl, kb * kBK, m0);
-                        // this CTA stages W columns [m_sub * ns/2, +ns/2) of the 256-row MMA's N
-                        for (int j = 0; j < my_boxes; ++j)
-                            ptx::tma_load_2d_pair_hint(sb + j * 8192, &a.tmap_w, fbl,
-                                                       n0 + (m_sub * my_boxes + j) * 64, kb * kBK, pol_w);
+                        // this CTA stages W columns [m_sub * ns/2, +ns/2) of the 256-row MMA's N:
+                        // my_boxes 64-column blocks in one 3-D copy
+                        ptx::tma_load_3d_pair_hint(sb, &a.tmap_w, fbl, 0, kb * kBK, n0 / 64 + m_sub * my_boxes, pol_w);
                     } else {
                         ptx::mbar_arrive_expect_tx(fb, tx);  // the whole stage, whoever loads it
                         const uint32_t adst = sa + uint32_t(mcx ? rank : 0u) * uint32_t(a_rows) * 128u;
                         if (mcx) ptx::tma_load_2d_mc(adst, &a.tmap_x, fb, kb * kBK, m0 + int(rank) * a_rows, a_mask);
                         else ptx::tma_load_2d(adst, &a.tmap_x, fb, kb * kBK, m0);
-                        for (int j = 0; j < nbox; ++j)
-                            ptx::tma_load_2d_hint(sb + j * 8192, &a.tmap_w, fb, n0 + j * 64, kb * kBK, pol_w);
+                        ptx::tma_load_3d_hint(sb, &a.tmap_w, fb, 0, kb * kBK, n0 / 64, pol_w);  // nbox blocks
                     }
                     if (kb == 0) trace_tile(a.trace, ptile, CF_TR_TMA_FIRST);
                     if (kb == nk - 1) trace_tile(a.trace, ptile, CF_TR_TMA_LAST);
+                    ++it;
+                    if (++s == uint32_t(stages)) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
-                if (*abort) break;
             }
             // drain: every stage this producer filled has been released by all of
             // its readers (so every load landed and every release signal aimed at
@@ -397,54 +399,63 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             // a wide tile is two N = 256 MMAs per K step into adjacent TMEM columns
             const uint32_t idesc = idesc_bf16(kPair ? 2 * kBlockM : kBlockM, wide ? 256 : ns);
             const uint16_t pair_mask = uint16_t(3u << pair_leader);
-            uint32_t it = 0;
+            const bool commit_mc = !kPair && a_mask != uint16_t(1u << crank);
+            // Operand descriptors of ring stage 0.  A stage's own are these plus its
+            // byte offset >> 4 in the address field (the ring ends below 256 KB, so
+            // the 14-bit field never carries); within a stage, A advances 16 K
+            // elements = 32 B inside the swizzle atom and B (MN-major: 64-column
+            // blocks 8 KB apart, 8-row K groups 1 KB apart) 16 K rows = 2 KB.  The
+            // loop below keeps the single issuing thread's work between MMA groups
+            // short, so the tensor pipe's queue never runs dry.
+            const uint64_t ad0 = sw128_desc(base + L.ring, 16, 1024);
+            const uint64_t bd0 = sw128_desc(base + L.ring + kABytes, 8192, 1024);
+            uint32_t s = 0, ph = 0;  // ring position of the next k-block
             int tile = 0;
             for (int t = cid; t < T; t += ncl, ++tile) {
                 const uint32_t buf = wide ? 0u : uint32_t(tile & 1);
                 const uint32_t tph = wide ? (uint32_t(tile) & 1u) : ((uint32_t(tile) >> 1) & 1u);
-                ptx::mbar_wait_bounded(B.tmem_empty0 + 8 * buf, tph ^ 1u, tmo, abort, a.err, kInfoMma | buf);
-                if (*abort) break;
+                if (!ptx::mbar_wait_bounded(B.tmem_empty0 + 8 * buf, tph ^ 1u, tmo, abort, a.err, kInfoMma | buf))
+                    break;
                 trace_tile(a.trace, tile, CF_TR_MMA_ACC_FREE);
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + buf * uint32_t(ns);
                 unsigned long long waited = 0;
-                for (int kb = 0; kb < nk; ++kb, ++it) {
-                    const uint32_t s = it % uint32_t(stages);
-                    const uint32_t ph = (it / uint32_t(stages)) & 1u;
-                    const unsigned long long w0 = a.trace ? ptx::globaltimer() : 0ull;
-                    ptx::mbar_wait_bounded(B.full0 + 8 * s, ph, tmo, abort, a.err, kInfoMma | 0x100u | s);
-                    if (*abort) break;
-                    if (a.trace) {
-                        waited += ptx::globaltimer() - w0;
-                        if (kb == 0) trace_tile(a.trace, tile, CF_TR_MMA_FIRST);
+                bool ok = true;
+                for (int kb = 0; kb < nk; ++kb) {
+                    const uint32_t fb = B.full0 + 8 * s;
+                    if (!ptx::mbar_try_wait(fb, ph)) {  // not landed yet: the bounded slow path
+                        const unsigned long long w0 = a.trace ? ptx::globaltimer() : 0ull;
+                        ok = ptx::mbar_wait_bounded(fb, ph, tmo, abort, a.err, kInfoMma | 0x100u | s);
+                        if (!ok) break;
+                        if (a.trace) waited += ptx::globaltimer() - w0;
                     }
+                    if (kb == 0) trace_tile(a.trace, tile, CF_TR_MMA_FIRST);
                     ptx::tc_fence_after();
-                    const uint32_t sa = base + L.ring + s * L.stage_bytes;
-                    const uint32_t sb = sa + kABytes;
+                    const uint64_t soff = uint64_t((s * L.stage_bytes) >> 4);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
-                        // A: K-major, advance 16 elements (32 B) inside the swizzle atom
-                        const uint64_t ad = sw128_desc(sa + k * 32, 16, 1024);
-                        // B: MN-major, 64-column blocks 8 KB apart, 8-row K groups 1 KB apart;
-                        // advance 16 K rows = 2 KB
-                        const uint64_t bd = sw128_desc(sb + k * 2048, 8192, 1024);
+                        const uint64_t ad = ad0 + soff + uint64_t(2 * k);
+                        const uint64_t bd = bd0 + soff + uint64_t(128 * k);
+                        const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
                         if constexpr (kPair) {
-                            ptx::mma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                            ptx::mma_bf16_pair(d, ad, bd, idesc, accum);
                         } else {
-                            ptx::mma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-                            // wide: columns 256..511 from W boxes 4..7
-                            if (wide)
-                                ptx::mma_bf16(d + 256u, ad, sw128_desc(sb + 4 * 8192 + k * 2048, 8192, 1024), idesc,
-                                              (kb | k) != 0 ? 1u : 0u);
+                            ptx::mma_bf16(d, ad, bd, idesc, accum);
+                            // wide: columns 256..511 from W blocks 4..7 (32 KB further)
+                            if (wide) ptx::mma_bf16(d + 256u, ad, bd + uint64_t(32768 >> 4), idesc, accum);
                         }
                     }
                     // the stage is free once these MMAs completed: tell every CTA whose
                     // producer filled it
                     if constexpr (kPair) ptx::mma_commit_pair_mc(B.empty0 + 8 * s, pair_mask);
-                    else if (a_mask != (1u << crank)) ptx::mma_commit_mc(B.empty0 + 8 * s, a_mask);
+                    else if (commit_mc) ptx::mma_commit_mc(B.empty0 + 8 * s, a_mask);
                     else ptx::mma_commit(B.empty0 + 8 * s);
+                    if (++s == uint32_t(stages)) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
-                if (*abort) break;
+                if (!ok) break;
                 // accumulator ready (pair: in both CTAs' tensor memory)
                 if constexpr (kPair) ptx::mma_commit_pair_mc(B.tmem_full0 + 8 * buf, pair_mask);
                 else ptx::mma_commit(B.tmem_full0 + 8 * buf);

@@ -252,6 +252,21 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// 3-D tiled TMA load with an L2 cache policy.  W [K, N] is described as a
+// 3-D tensor {64 columns, K rows, N/64 column blocks} (strides N*2 and 128
+// bytes), so one copy stages several 64-column blocks of a k-block, each as a
+// contiguous 128B-swizzled [64 x 64] block: the layout the MN-major B operand
+// descriptor walks with its 8 KB leading-byte offset.  Fewer, larger copies
+// cost the TMA unit less than one copy per block.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y,
+                                                 int32_t z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
 // 2-D tiled TMA load multicast to every CTA of `mask` in the cluster: the box
 // lands at the same shared-memory offset in each, and complete_tx is signalled
 // on the mbarrier at the same offset in each
@@ -372,6 +387,15 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void *
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+// the 3-D W copy of a CTA of a pair (completion on the pair leader's barrier)
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void *tmap, uint32_t bar_cluster, int32_t x,
+                                                      int32_t y, int32_t z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "l"(policy)
         : "memory");
 }
 // arrive on an mbarrier of another CTA of the cluster (shared::cluster address)

@@ -18,8 +18,9 @@ pytestmark = pytest.mark.gpu
 
 def test_noalloc_matches_workspace_entry_point_twice():
     torch = torch_cuda()
-    # N = 8192 is wider than one cluster, so the global partial buffer (scratch) is used
-    M, N, K = 390, 8192, 128
+    # N = 16384 is wider than any cluster (256 columns x 16 CTAs, or 512 x 16), so the
+    # global partial buffer (scratch) is used
+    M, N, K = 390, 16384, 128
     d = inputs.gemm_inputs(M, N, K, 31, x_std=K ** -0.5, w_std=K ** -0.5, bias_std=0.1, gamma_std=0.1,
                            beta_std=0.1)
     X, W = dev_bf16(d["X"]), dev_bf16(d["W"])
