@@ -694,27 +694,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_CLUSTER);
 
             // ---------------- level 4: rows wider than a cluster (global partials).
-            // Layout [row block][row][Gp] float2 (Gp = G rounded up to even): the G
-            // partials of one row are contiguous, so a row's reader fetches them
-            // with independent 16-byte loads, 8 partials in flight at a time.
+            // Layout [row block][g][128 rows] float2: one cluster group's 128 partials
+            // are contiguous, so both the writes and each warp's reads are coalesced
+            // 256-byte accesses.  After the last cluster's arrival
+            // the critical path is three L2 round trips: its release arrive, the
+            // pollers' acquire load that sees the full count, and one batch of
+            // independent loads of all partials (up to 32 per batch).  The
+            // error word is polled every 64 spins only, and this CTA's departure
+            // (which lets the last one reset the counters) is taken off the path.
+            uint32_t dep_old = 0;
+            uint32_t *dep = nullptr;
             if (G > 1) {
                 uint32_t *cnt = a.counters + rb;
-                uint32_t *dep = a.counters + a.row_blocks_alloc + rb;
+                dep = a.counters + a.row_blocks_alloc + rb;
                 const int Gp = G + (G & 1);
-                float2 *prow = a.partials + (size_t(rb) * 128 + row) * Gp;
+                float2 *pblk = a.partials + size_t(rb) * size_t(Gp) * 128u;
                 if (rank == 0) {
-                    prow[g] = stat;
+                    pblk[g * 128 + row] = stat;
                     // the 128 writes happen before the barrier; the release arrive
                     // below publishes all of them
                     ptx::named_bar_sync(bar_grp, kGroupThreads);
-                    if (gt0) ptx::atom_add_release_gpu(cnt, 1u);
+                    if (gt0) ptx::red_add_release_gpu(cnt, 1u);
                 }
                 if (gt0) {
                     const uint32_t target = uint32_t(G + a.extra_arrivals);
                     const uint64_t t0 = ptx::globaltimer();
-                    while (!*abort) {
+                    for (uint32_t spin = 0; !*abort; ++spin) {
                         if (ptx::ld_acquire_gpu(cnt) >= target) break;
-                        if (ptx::ld_relaxed_gpu(a.err) != 0u) {
+                        if ((spin & 63u) == 63u && ptx::ld_relaxed_gpu(a.err) != 0u) {
                             *abort = 1u;
                             break;
                         }
@@ -724,36 +731,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                             break;
                         }
                     }
-                    // last CTA of this row block to leave resets its counters
-                    if (ptx::atom_add_acq_rel_gpu(dep, 1u) == uint32_t(G * C) - 1u) {
-                        ptx::st_relaxed_gpu(cnt, 0u);
-                        ptx::st_relaxed_gpu(dep, 0u);
-                    }
+                    // departure: the last of the row block's G * C CTAs resets its
+                    // counters.  Relaxed: it is ordered after the acquire poll above
+                    // (so every poll of the row block precedes the last departure),
+                    // and nothing here waits for its result, looked at after pass 2.
+                    dep_old = ptx::atom_add_relaxed_gpu(dep, 1u);
                 }
                 ptx::named_bar_sync(bar_grp, kGroupThreads);
+                // combine in a fixed pairwise tree over index order (batches of 32, then
+                // batch results left to right): every CTA of the row folds the same
+                // partials identically, so all of them hold bitwise-equal statistics
                 const float nc = float(ns * C);  // columns behind each partial
                 float2 s2 = make_float2(0.f, 0.f);
-                for (int g0 = 0; g0 < G; g0 += 8) {
-                    float4 v[4];
+                float sn = 0.f;
+                for (int g0 = 0; g0 < G; g0 += 32) {
+                    const int rem = G - g0;  // partials in this batch (>= 1; <= 32 used)
+                    float2 p[32];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (g0 + 2 * i < G) v[i] = ptx::ld_relaxed_gpu_f4(prow + g0 + 2 * i);
+                    for (int i = 0; i < 32; ++i)
+                        p[i] = (i < rem) ? ptx::ld_relaxed_gpu_f2(pblk + (g0 + i) * 128 + row) : make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int gg = g0 + i;
-                        if (gg >= G) break;
-                        const float2 o = (i & 1) ? make_float2(v[i >> 1].z, v[i >> 1].w)
-                                                 : make_float2(v[i >> 1].x, v[i >> 1].y);
-                        if (gg == 0) {
-                            s2 = o;
-                        } else if constexpr (EPI == EPI_SOFTMAX) {
-                            const MaxSum m = combine_maxsum(MaxSum{s2.x, s2.y}, MaxSum{o.x, o.y});
-                            s2 = make_float2(m.m, m.s);
-                        } else {
-                            const MeanM2 m = combine_counts(MeanM2{s2.x, s2.y}, float(gg) * nc, MeanM2{o.x, o.y}, nc);
-                            s2 = make_float2(m.mean, m.m2);
+                    for (int w = 1; w < 32; w *= 2) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2 * w) {
+                            // p[i] covers entries [i, i+w), p[i+w] covers [i+w, i+2w), clipped to rem
+                            const int nb_i = min(max(rem - i - w, 0), w);
+                            if (nb_i > 0) {
+                                if constexpr (EPI == EPI_SOFTMAX) {
+                                    const MaxSum m = combine_maxsum(MaxSum{p[i].x, p[i].y}, MaxSum{p[i + w].x, p[i + w].y});
+                                    p[i] = make_float2(m.m, m.s);
+                                } else {
+                                    // p[i] is full (i + w < rem here); equal halves need no division
+                                    const MeanM2 m = (nb_i == w)
+                                                         ? combine_equal(MeanM2{p[i].x, p[i].y}, MeanM2{p[i + w].x, p[i + w].y},
+                                                                         float(w) * nc)
+                                                         : combine_counts(MeanM2{p[i].x, p[i].y}, float(w) * nc,
+                                                                          MeanM2{p[i + w].x, p[i + w].y}, float(nb_i) * nc);
+                                    p[i] = make_float2(m.mean, m.m2);
+                                }
+                            }
                         }
                     }
+                    const float bn = float(min(rem, 32)) * nc;
+                    if (g0 == 0) {
+                        s2 = p[0];
+                    } else if constexpr (EPI == EPI_SOFTMAX) {
+                        const MaxSum m = combine_maxsum(MaxSum{s2.x, s2.y}, MaxSum{p[0].x, p[0].y});
+                        s2 = make_float2(m.m, m.s);
+                    } else {
+                        const MeanM2 m = combine_counts(MeanM2{s2.x, s2.y}, sn, MeanM2{p[0].x, p[0].y}, bn);
+                        s2 = make_float2(m.mean, m.m2);
+                    }
+                    sn += bn;
                 }
                 stat = s2;
             }
@@ -838,6 +867,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             // after every thread of the group is done with them
             ptx::named_bar_sync(bar_grp, kGroupThreads);
             if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_STORED);
+            // the last CTA of the row block to depart resets its counters (for the
+            // next launch on this workspace); every poller of this launch is done
+            if (gt0 && dep != nullptr && dep_old == uint32_t(G * C) - 1u) {
+                ptx::st_relaxed_gpu(a.counters + rb, 0u);
+                ptx::st_relaxed_gpu(dep, 0u);
+            }
         }
         // every bulk store of this warp has completed before the CTA may leave
         if (lane == 0) ptx::bulk_wait_group0();
