@@ -24,6 +24,7 @@ region, and each page workload's fused-kernel numbers (per_workload).
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -102,7 +103,7 @@ def profiled_traffic(workload, kernel):
 class ClockSampler:
     """nvidia-smi clock / throttle sampling in the background."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -120,7 +121,11 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, window=None):
+        """Median SM clock and the throttle reasons seen; with `window` = (t0, t1)
+        (time.time() around the timed region) only the samples inside it count,
+        unless none fell inside (a region shorter than the 50 ms sampling
+        period), which the result says."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
@@ -129,24 +134,27 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons, n = [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                samples.append((ts, float(parts[1]), float(parts[2]),
+                                {nm for nm, v in zip(names, parts[5:9]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            n += 1
-            for nm, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": n}
+        inside = [x for x in samples if window and window[0] - 0.02 <= x[0] <= window[1] + 0.02]
+        use = inside if inside else samples
+        reasons = set().union(*[x[3] for x in use]) if use else set()
+        res = {"sm_mhz": statistics.median([x[1] for x in use]) if use else None,
+               "sm_max_mhz": max(x[2] for x in use) if use else None,
+               "reasons": sorted(reasons), "samples": len(use)}
+        if window and not inside:
+            res["note"] = "no sample inside the timed region (shorter than the sampling period); all samples"
+        return res
 
 
 # ---------------------------------------------------------------------------
@@ -233,6 +241,7 @@ def time_steps(torch, runner, steps, warmup, barrier, sampler=None, graph_len=50
     if sampler:
         sampler.start()
         time.sleep(0.3)
+    w0 = time.time()
     e0.record(stream)
     for _ in range(reps):
         g.replay()
@@ -240,8 +249,9 @@ def time_steps(torch, runner, steps, warmup, barrier, sampler=None, graph_len=50
         g_rem.replay()
     e1.record(stream)
     torch.cuda.synchronize()
+    w1 = time.time()
     barrier()
-    clocks = sampler.stop() if sampler else None
+    clocks = sampler.stop((w0, w1)) if sampler else None
     return e0.elapsed_time(e1) / 1e3, reps * R + rem, clocks
 
 
@@ -498,17 +508,30 @@ def run_stitch(args):
             cf.check(cf.cf_stitch_rowreduce_broadcast(A[i % nsets], b, O[i % nsets], w.rows, w.cols, ws, wsb,
                                                       stream))
 
-    t, n, _ = time_steps(torch, R(), args.steps, args.warmup, ranks.barrier)
+    props = torch.cuda.get_device_properties(device)
+    gpu_id = str(getattr(props, "uuid", local))
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id if gpu_id.startswith("GPU-") else str(local))
+    t, n, clocks = time_steps(torch, R(), args.steps, args.warmup, ranks.barrier, sampler)
     t = ranks.max(t)
     gbs = mdist.job_throughput(w.unavoidable_bytes * n, ws_, t) / 1e9
+    # the planner's rule: rows of at most 32 float4 groups go packed, wider ones split
+    kernel = "stitch_packed_kernel" if (w.cols + 3) // 4 <= 32 else "stitch_split_kernel"
     if rank == 0:
         print(json.dumps({"metric": "stitched reduce->broadcast HBM GB/s", "value": round(gbs, 1), "unit": "GB/s",
                           "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
                           "ms_per_step": round(t / n * 1e3, 6), "higher_is_better": True, "scaling": "weak",
-                          "config": {"workload": w.name, "rows": w.rows, "cols": w.cols},
+                          "dtype": "f32", "data": "synthetic (seeded, shaped like the page workload)",
+                          "config": {"workload": w.name, "rows": w.rows, "cols": w.cols,
+                                     "l2": f"{nsets} rotating input/output sets (>= 3x L2 of {l2 >> 20} MiB)"},
                           "roofline": {"bound": "hbm", "achieved": round(gbs / ws_, 1), "peak": peaks["hbm_gbs"],
-                                       "unit": "GB/s", "frac": round(gbs / ws_ / peaks["hbm_gbs"], 4)},
-                          "gpu_launches": n}), flush=True)
+                                       "unit": "GB/s", "frac": round(gbs / ws_ / peaks["hbm_gbs"], 4),
+                                       "traffic": profiled_traffic(w.name, kernel), "kernel": kernel,
+                                       "algorithmic_bytes_per_launch": w.unavoidable_bytes,
+                                       "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
+                                       else "fallback"},
+                          "gpu_launches": n, "clocks": clocks}), flush=True)
     ranks.close()
 
 
