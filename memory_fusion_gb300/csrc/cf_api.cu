@@ -237,7 +237,7 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
         if (cn < 1 || c > 16 || cpr % cn != 0 || max_active_clusters[c] <= 0) return -1.0;
         if (cm == 2 && (ns < 128 || rb < 2 || wide)) return -1.0;
         const int g = cpr / cn;
-        if (wide && g > 1) return -1.0;
+        if (wide && (g > 1 || cn > 8)) return -1.0;  // a wide row: one cluster of <= 8 (<= 16 partials)
         int n = max_active_clusters[c];
         if (t.max_clusters > 0) n = std::min(n, int(t.max_clusters));
         if (g > 1 && n < g) return -1.0;
@@ -279,8 +279,8 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
             const int cpr = int(N / cand[0]);
             if (t.cluster_size > 16 || (t.cluster_size > 0 && cpr % t.cluster_size != 0)) return CF_ERR_UNSUPPORTED;
             if (t.cluster_m > 2 || t.cluster_m < 0) return CF_ERR_UNSUPPORTED;
-            // a wide tile's row must fit one cluster of at most 16, without pairs
-            if (cand[0] > 256 && (cpr > 16 || t.cluster_m == 2 || (t.cluster_size > 0 && t.cluster_size != cpr)))
+            // a wide tile's row must fit one cluster of at most 8, without pairs
+            if (cand[0] > 256 && (cpr > 8 || t.cluster_m == 2 || (t.cluster_size > 0 && t.cluster_size != cpr)))
                 return CF_ERR_UNSUPPORTED;
             return CF_ERR_NOT_RESIDENT;
         }

@@ -78,11 +78,9 @@ struct SmemLayout {
     uint32_t stage_bytes;  // A + B of one stage
     uint32_t ring;         // offset of the operand ring (1024-aligned)
     uint32_t stg;          // bf16 output staging, 1 or 2 x 2 KiB per epilogue warp (64B swizzle)
-    uint32_t send;         // float2 [4][128]: this CTA's partial, by exchange set
-    uint32_t slot;         // float2 [4][C][128]: the row group's partials, by exchange set
+    uint32_t slot;         // float2 [sets][partials][128]: the row group's partials (4 x C, or 2 x 2C for a wide tile)
     uint32_t res;          // float2 [4][128]: leader-follower result, by exchange set
     uint32_t prm;          // float [2][3][256]: bias, gamma, beta of the tile's columns, per group
-    uint32_t comb;         // float2 [2][128]: the two groups' half-row partials of a wide tile
     uint32_t bars;         // mbarriers
     uint32_t total;        // bytes from the aligned base
 };
@@ -98,18 +96,17 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int cluster, int n
     uint32_t off = L.ring + uint32_t(stages) * L.stage_bytes;
     L.stg = off;
     off += kEpiWarps * 2048 * uint32_t(stg_bufs);
-    // exchange buffers exist only when a row group has more than one CTA
-    const uint32_t xc = cluster > 1 ? 1u : 0u;
-    L.send = off;
-    off += xc * kXSets * 128 * 8;
+    // exchange buffers exist only when a row group has more than one partial:
+    // 4 sets x C (PingPong), or 2 sets x 2C for a wide tile (two groups per CTA,
+    // one accumulator, so the CTAs of a cluster are never two tiles apart)
+    const bool wide = n_slice > 256;
+    const uint32_t xc = (cluster > 1 || wide) ? 1u : 0u;
     L.slot = off;
     off += xc * kXSets * uint32_t(cluster) * 128 * 8;
     L.res = off;  // the leader-follower result (not used by peer all-to-all)
     off += (leader ? xc : 0u) * kXSets * 128 * 8;
     L.prm = off;
     off += 2 * 3 * 256 * 4;
-    L.comb = off;  // only a wide tile (n_slice 512) has two groups on one row
-    off += (n_slice > 256 ? 2u * 128u * 8u : 0u);
     L.bars = off;
     off += 256;
     L.total = off;
@@ -215,21 +212,41 @@ __device__ __forceinline__ MeanM2 ln_fragment(uint32_t (&v)[32], const float *p,
     return chunk_mean_m2(x);
 }
 
-// Combine the C per-CTA partials of one row (slot r at s[r*128]) in rank order.
-template <bool kSoftmax>
-__device__ __forceinline__ float2 combine_slots(const float2 *s, int C, float n_slice) {
-    float2 st = s[0];
-    for (int r = 1; r < C; ++r) {
-        const float2 o = s[r * 128];
-        if constexpr (kSoftmax) {
-            const MaxSum m = combine_maxsum(MaxSum{st.x, st.y}, MaxSum{o.x, o.y});
-            st = make_float2(m.m, m.s);
-        } else {
-            const MeanM2 m = combine_counts(MeanM2{st.x, st.y}, float(r) * n_slice, MeanM2{o.x, o.y}, n_slice);
-            st = make_float2(m.mean, m.m2);
+// Fold n (<= kN) partials p[0..n) of equal column count `cnt` in a fixed
+// pairwise tree over index order (level W merges p[i] and p[i+W]); every CTA
+// folding the same partials obtains bitwise-equal statistics.  The levels are
+// compile-time so that p stays in registers.
+template <bool kSoftmax, int kN, int W>
+__device__ __forceinline__ void tree_level(float2 (&p)[kN], int n, float cnt) {
+#pragma unroll
+    for (int i = 0; i < kN; i += 2 * W) {
+        const int nb = min(max(n - i - W, 0), W);  // p[i+W] covers nb partials; p[i] covers W
+        if (nb > 0) {
+            if constexpr (kSoftmax) {
+                const MaxSum m = combine_maxsum(MaxSum{p[i].x, p[i].y}, MaxSum{p[i + W].x, p[i + W].y});
+                p[i] = make_float2(m.m, m.s);
+            } else {
+                const MeanM2 m = combine_counts(MeanM2{p[i].x, p[i].y}, float(W) * cnt, MeanM2{p[i + W].x, p[i + W].y},
+                                                float(nb) * cnt);
+                p[i] = make_float2(m.mean, m.m2);
+            }
         }
     }
-    return st;
+    if constexpr (2 * W < kN) tree_level<kSoftmax, kN, 2 * W>(p, n, cnt);
+}
+template <bool kSoftmax, int kN>
+__device__ __forceinline__ float2 tree_fold(float2 (&p)[kN], int n, float cnt) {
+    tree_level<kSoftmax, kN, 1>(p, n, cnt);
+    return p[0];
+}
+
+// The n (<= 16) partials of one row in the exchange slots (partial j at s[j*128]).
+template <bool kSoftmax>
+__device__ __forceinline__ float2 combine_slots(const float2 *s, int n, float cnt) {
+    float2 p[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) p[j] = (j < n) ? s[j * 128] : make_float2(0.f, 0.f);
+    return tree_fold<kSoftmax, 16>(p, n, cnt);
 }
 
 template <int EPI, bool kPair>
@@ -482,7 +499,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
         const int gt = (e & 3) * 32 + lane;   // thread index within the group
         const bool gt0 = (gt == 0);
         const uint32_t bar_grp = 1u + uint32_t(grp);
-        float2 *const send = reinterpret_cast<float2 *>(gbase + L.send);
         float2 *const slot = reinterpret_cast<float2 *>(gbase + L.slot);
         float2 *const res = reinterpret_cast<float2 *>(gbase + L.res);
         float *const prm = reinterpret_cast<float *>(gbase + L.prm) + grp * 768;
@@ -493,7 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
         const int ecols = wide ? 256 : ns;       // columns of a tile this group handles
         const int coff = wide ? grp * 256 : 0;   // and their offset within the tile
         const int nchunks = ecols / 32;          // 2, 4 or 8 fragments of 32 columns per thread
-        float2 *const comb = reinterpret_cast<float2 *>(gbase + L.comb);
+        const int parts = wide ? 2 : 1;  // partials per CTA: one per group on the tile
+        const int npart = C * parts;     // partials of one row group
         float *const pb = prm;        // bias, gamma, beta of this group's current tile
         float *const pg = prm + 256;
         float *const pe = prm + 512;
@@ -506,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             const int ncta = (g * C + int(rank)) * ns + coff;  // first global column this group handles
             const uint32_t buf = wide ? 0u : uint32_t(grp);
             const uint32_t tph = wide ? (uint32_t(tile) & 1u) : ((uint32_t(tile) >> 1) & 1u);
-            const uint32_t xs = uint32_t(tile) & 3u;    // exchange buffer set
-            const uint32_t xph = (uint32_t(tile) >> 2) & 1u;
+            const uint32_t xs = wide ? (uint32_t(tile) & 1u) : (uint32_t(tile) & 3u);  // exchange buffer set
+            const uint32_t xph = wide ? ((uint32_t(tile) >> 1) & 1u) : ((uint32_t(tile) >> 2) & 1u);
 
             // Row-vector parameters of the tile's columns into this group's shared
             // buffer, fetched before the accumulator is ready; the group's previous
@@ -626,70 +643,60 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             }
             if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_STATS);
 
-            // ---------------- level 2: the CTA statistic of a row is one thread's (a wide
-            // tile: two threads', one per group, combined through shared memory in a
-            // fixed order so both groups hold the same value); group 0's goes into the
-            // unified reduce buffer of this exchange set
-            if (wide) {
-                comb[grp * 128 + row] = part;
-                ptx::named_bar_sync(3u, 2 * kGroupThreads);
-                const float2 p0 = comb[row], p1 = comb[128 + row];
-                if constexpr (EPI == EPI_SOFTMAX) {
-                    const MaxSum m = combine_maxsum(MaxSum{p0.x, p0.y}, MaxSum{p1.x, p1.y});
-                    part = make_float2(m.m, m.s);
-                } else {
-                    const MeanM2 m = combine_equal(MeanM2{p0.x, p0.y}, MeanM2{p1.x, p1.y}, float(ecols));
-                    part = make_float2(m.mean, m.m2);
-                }
-            }
-            const bool sender = !wide || grp == 0;  // the group that sends this CTA's partial
-            if (C > 1 && sender) {
-                send[xs * 128 + row] = part;
-                ptx::fence_proxy_async_smem();
-                ptx::named_bar_sync(bar_grp, kGroupThreads);
-            }
+            // ---------------- levels 2 and 3: a row's statistic over this CTA's columns
+            // is one thread's (a wide tile: two threads', one per group).  Each thread
+            // sends its row's partial straight into the gathering CTAs' shared memory
+            // with an 8-byte st.async that completes on their mbarrier: every CTA of
+            // the row group (peer all-to-all) or rank 0 (leader-follower, which sends
+            // the combined statistics back with a bulk copy).  The gatherer folds
+            // the partials in index order (CTA rank, then group), the same in every
+            // CTA.  No shared-memory fence or group barrier precedes the sends.
             if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_CTA);
-            // ---------------- level 3: inter-CTA over DSMEM (TMA bulk copies)
-            if (C > 1 && sender && gt0 && !*abort) {
-                const uint32_t src = base + L.send + xs * 1024;
-                const uint32_t my_slot = base + L.slot + (xs * C + rank) * 1024;
+            const bool lead_grp = !wide || grp == 0;  // does the per-CTA steps of the tile
+            float2 stat;                              // row-group statistic of this row
+            if (npart == 1) {
+                stat = part;  // the row group is this CTA's one group
+            } else if (!*abort) {
                 const uint32_t xfull = B.xfull0 + 8 * xs;
+                const uint32_t sl = base + L.slot + xs * uint32_t(npart) * 1024u;  // [npart][128] float2
+                // this partial's index: CTA rank, then (wide tile) the group
+                const uint32_t mine = sl + uint32_t(int(rank) * parts + (wide ? grp : 0)) * 1024u + uint32_t(row) * 8u;
+                const float2 *slot_row = slot + size_t(xs) * size_t(npart) * 128u + row;
                 if (!a.leader) {
-                    ptx::mbar_arrive_expect_tx(xfull, uint32_t(C) * 1024u);
-                    for (int r = 0; r < C; ++r)
-                        ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, r * CM + m_sub), src, 1024,
-                                                 ptx::mapa(xfull, r * CM + m_sub));
-                } else {
-                    if (rank == 0) ptx::mbar_arrive_expect_tx(xfull, uint32_t(C) * 1024u);
-                    else ptx::mbar_arrive_expect_tx(B.xres0 + 8 * xs, 1024u);
-                    ptx::bulk_copy_s2cluster(ptx::mapa(my_slot, m_sub), src, 1024, ptx::mapa(xfull, m_sub));
-                }
-            }
-            float2 stat;  // cluster-combined statistic of this row
-            if (C == 1) {
-                stat = part;  // the row group is this CTA alone
-            } else if (!a.leader) {
-                ptx::mbar_wait_bounded<true>(B.xfull0 + 8 * xs, xph, tmo, abort, a.err, kInfoXchg | xs);
-                stat = combine_slots<EPI == EPI_SOFTMAX>(slot + xs * C * 128 + row, C, float(ns));
-            } else {
-                if (rank == 0) {
-                    ptx::mbar_wait_bounded<true>(B.xfull0 + 8 * xs, xph, tmo, abort, a.err, kInfoXchg | xs);
-                    stat = combine_slots<EPI == EPI_SOFTMAX>(slot + xs * C * 128 + row, C, float(ns));
-                    if (sender) {
-                        res[xs * 128 + row] = stat;
-                        ptx::fence_proxy_async_smem();
-                        ptx::named_bar_sync(bar_grp, kGroupThreads);
-                        if (gt0 && !*abort) {
-                            const uint32_t src = base + L.res + xs * 1024;
-                            for (int r = 1; r < C; ++r)
-                                ptx::bulk_copy_s2cluster(ptx::mapa(src, r * CM + m_sub), src, 1024,
-                                                         ptx::mapa(B.xres0 + 8 * xs, r * CM + m_sub));
-                        }
+                    if (gt0 && lead_grp) ptx::mbar_arrive_expect_tx(xfull, uint32_t(npart) * 1024u);
+                    for (int r = 0; r < C; ++r) {
+                        const uint32_t peer = uint32_t(r * CM + m_sub);
+                        ptx::st_async_f2(ptx::mapa(mine, peer), part.x, part.y, ptx::mapa(xfull, peer));
                     }
+                    ptx::mbar_wait_bounded<true>(xfull, xph, tmo, abort, a.err, kInfoXchg | xs);
+                    stat = combine_slots<EPI == EPI_SOFTMAX>(slot_row, npart, float(ecols));
                 } else {
-                    ptx::mbar_wait_bounded<true>(B.xres0 + 8 * xs, xph, tmo, abort, a.err, kInfoXchg | 0x10u | xs);
-                    stat = res[xs * 128 + row];
+                    if (gt0 && lead_grp) {
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(xfull, uint32_t(npart) * 1024u);
+                        else ptx::mbar_arrive_expect_tx(B.xres0 + 8 * xs, 1024u);
+                    }
+                    ptx::st_async_f2(ptx::mapa(mine, uint32_t(m_sub)), part.x, part.y, ptx::mapa(xfull, uint32_t(m_sub)));
+                    if (rank == 0) {
+                        ptx::mbar_wait_bounded<true>(xfull, xph, tmo, abort, a.err, kInfoXchg | xs);
+                        stat = combine_slots<EPI == EPI_SOFTMAX>(slot_row, npart, float(ecols));
+                        if (lead_grp) {
+                            res[xs * 128 + row] = stat;
+                            ptx::fence_proxy_async_smem();
+                            ptx::named_bar_sync(bar_grp, kGroupThreads);
+                            if (gt0 && !*abort) {
+                                const uint32_t src = base + L.res + xs * 1024;
+                                for (int r = 1; r < C; ++r)
+                                    ptx::bulk_copy_s2cluster(ptx::mapa(src, r * CM + m_sub), src, 1024,
+                                                             ptx::mapa(B.xres0 + 8 * xs, r * CM + m_sub));
+                            }
+                        }
+                    } else {
+                        ptx::mbar_wait_bounded<true>(B.xres0 + 8 * xs, xph, tmo, abort, a.err, kInfoXchg | 0x10u | xs);
+                        stat = res[xs * 128 + row];
+                    }
                 }
+            } else {
+                stat = part;  // aborting: the values no longer matter
             }
             if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_CLUSTER);
 
@@ -750,28 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         p[i] = (i < rem) ? ptx::ld_relaxed_gpu_f2(pblk + (g0 + i) * 128 + row) : make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int w = 1; w < 32; w *= 2) {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2 * w) {
-                            // p[i] covers entries [i, i+w), p[i+w] covers [i+w, i+2w), clipped to rem
-                            const int nb_i = min(max(rem - i - w, 0), w);
-                            if (nb_i > 0) {
-                                if constexpr (EPI == EPI_SOFTMAX) {
-                                    const MaxSum m = combine_maxsum(MaxSum{p[i].x, p[i].y}, MaxSum{p[i + w].x, p[i + w].y});
-                                    p[i] = make_float2(m.m, m.s);
-                                } else {
-                                    // p[i] is full (i + w < rem here); equal halves need no division
-                                    const MeanM2 m = (nb_i == w)
-                                                         ? combine_equal(MeanM2{p[i].x, p[i].y}, MeanM2{p[i + w].x, p[i + w].y},
-                                                                         float(w) * nc)
-                                                         : combine_counts(MeanM2{p[i].x, p[i].y}, float(w) * nc,
-                                                                          MeanM2{p[i + w].x, p[i + w].y}, float(nb_i) * nc);
-                                    p[i] = make_float2(m.mean, m.m2);
-                                }
-                            }
-                        }
-                    }
+                    tree_fold<EPI == EPI_SOFTMAX, 32>(p, rem, nc);
                     const float bn = float(min(rem, 32)) * nc;
                     if (g0 == 0) {
                         s2 = p[0];
@@ -874,8 +860,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 ptx::st_relaxed_gpu(dep, 0u);
             }
         }
-        // every bulk store of this warp has completed before the CTA may leave
-        if (lane == 0) ptx::bulk_wait_group0();
+        // every bulk store of this warp has finished reading its staging buffer
+        // before the CTA may leave (the writes complete with the grid)
+        if (lane == 0) ptx::bulk_wait_group_read0();
         __syncwarp();
     }
     if (threadIdx.x == 64) trace_stamp(a.trace, 2);

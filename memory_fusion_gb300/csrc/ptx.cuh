@@ -291,6 +291,15 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, u
 // bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
 // shared::cluster address; completion is signalled (complete_tx) on the
 // mbarrier at shared::cluster address `remote_bar` in the destination CTA.
+// 8-byte asynchronous store into a CTA of the cluster (shared::cluster
+// address), completing on that CTA's mbarrier with complete_tx of 8 bytes
+__device__ __forceinline__ void st_async_f2(uint32_t remote_addr, float x, float y, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                     remote_addr),
+                 "f"(x), "f"(y), "r"(remote_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
                                                     uint32_t remote_bar) {
     asm volatile(
