@@ -373,6 +373,7 @@ cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *row_bias
     cf::StitchPlan p;
     p.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out);
     p.pdl = t.disable_pdl == 0;
+    p.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
     const int ng = int((cols + 3) / 4);
     int mapping = t.stitch_mapping;
     if (mapping == 0) mapping = (ng <= 32) ? 1 : 2;

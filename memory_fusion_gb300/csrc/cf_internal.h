@@ -40,6 +40,7 @@ struct StitchPlan {
     bool vec = false;     // 128-bit path
     bool pdl = true;      // programmatic dependent launch
     int grid = 0;         // CTAs
+    unsigned long long timeout_ns = 200000000ull;  // bound of every wait (split mapping)
 };
 
 cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias, float *out, int64_t rows,

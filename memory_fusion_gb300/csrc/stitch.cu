@@ -114,10 +114,13 @@ template <int V, bool VEC>
 __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__restrict__ A,
                                                                 const float *__restrict__ bias,
                                                                 float *__restrict__ out, int64_t rows, int cols,
-                                                                int gpc, int leader) {
+                                                                int gpc, int leader, uint32_t *err,
+                                                                unsigned long long tmo) {
     __shared__ MaxSum red[kThreads / 32];
     __shared__ __align__(16) MaxSum slot[2][16];  // level-3 partials, by row parity
     __shared__ __align__(16) MaxSum res[2];       // leader's result, by row parity
+    __shared__ __align__(8) uint64_t xbar[2];     // exchange barriers, by row parity
+    __shared__ uint32_t abort_flag;
 
     const uint32_t C = ptx::cluster_nctarank();
     const uint32_t rank = ptx::cluster_ctarank();
@@ -128,7 +131,19 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
     const int ng = (cols + 3) >> 2;
     const int g0 = int(rank) * gpc;
     const int g1 = min(ng, g0 + gpc);
+    volatile uint32_t *abort = &abort_flag;
 
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&xbar[0]), 1);
+        ptx::mbar_init(ptx::smem_u32(&xbar[1]), 1);
+        abort_flag = 0u;
+        ptx::fence_mbarrier_init_cluster();
+    }
+    __syncthreads();
+    // Peers may signal these barriers once every CTA of the cluster initialised
+    // its own: arrive now, wait just before the first exchange (the first row's
+    // loads are in flight in between).
+    ptx::cluster_arrive_relaxed();
     // programmatic dependent launch: nothing in global memory before the
     // previous grid on the stream has completed
     ptx::griddep_wait();
@@ -136,6 +151,8 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
     int it = 0;
     for (int64_t row = cid; row < rows; row += ncl, ++it) {
         const int par = it & 1;
+        const uint32_t xb = ptx::smem_u32(&xbar[par]);
+        const uint32_t xph = uint32_t(it >> 1) & 1u;
         const float *a = A + row * cols;
         float *o = out + row * cols;
         const float bb = __ldg(bias + row);
@@ -156,9 +173,7 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
                 for (int j = 0; j < 4; ++j) e[v][j] = (g < g1 && 4 * g + j < cols) ? __ldcs(a + 4 * g + j) : 0.f;
             }
         }
-        // every peer CTA is running before anyone touches its shared memory; the
-        // first row's loads are already in flight behind this barrier
-        if (it == 0) ptx::cluster_sync();
+        if (it == 0) ptx::cluster_wait_acquire();
         // thread-local aggregation: max, then sum of exp (exp kept for the output)
         float mt = neg_inf();
 #pragma unroll
@@ -190,29 +205,32 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
         if (warp == 0) {
             MaxSum q = (lane < kThreads / 32) ? red[lane] : MaxSum{neg_inf(), 0.f};
             q = warp_maxsum<kThreads / 32>(q);
-            if (lane == 0) {
-                // level 3: distributed shared memory across the cluster
+            if (lane == 0 && !*abort) {
+                // level 3: an 8-byte st.async of this CTA's (max, sum) into the
+                // gathering CTAs' shared memory, completing on their barrier
                 const uint32_t my_slot = ptx::smem_u32(&slot[par][rank]);
                 if (!leader) {
-                    for (uint32_t r = 0; r < C; ++r) ptx::st_cluster_v2f32(ptx::mapa(my_slot, r), q.m, q.s);
+                    ptx::mbar_arrive_expect_tx(xb, C * 8u);
+                    for (uint32_t r = 0; r < C; ++r)
+                        ptx::st_async_f2(ptx::mapa(my_slot, r), q.m, q.s, ptx::mapa(xb, r));
                 } else {
-                    ptx::st_cluster_v2f32(ptx::mapa(my_slot, 0), q.m, q.s);
+                    ptx::mbar_arrive_expect_tx(xb, rank == 0 ? C * 8u : 8u);
+                    ptx::st_async_f2(ptx::mapa(my_slot, 0), q.m, q.s, ptx::mapa(xb, 0));
                 }
             }
         }
-        ptx::cluster_sync();
         MaxSum tot;
-        if (!leader) {
+        if (!leader || rank == 0) {
+            ptx::mbar_wait_bounded<true>(xb, xph, tmo, abort, err, 0x70000000u | uint32_t(par));
             tot = slot[par][0];
             for (uint32_t r = 1; r < C; ++r) tot = combine_maxsum(tot, slot[par][r]);
-        } else {
-            if (rank == 0 && threadIdx.x == 0) {
-                MaxSum t = slot[par][0];
-                for (uint32_t r = 1; r < C; ++r) t = combine_maxsum(t, slot[par][r]);
+            if (leader && threadIdx.x == 0 && !*abort) {
+                // the leader sends the row statistics back to each follower
                 const uint32_t res_addr = ptx::smem_u32(&res[par]);
-                for (uint32_t r = 0; r < C; ++r) ptx::st_cluster_v2f32(ptx::mapa(res_addr, r), t.m, t.s);
+                for (uint32_t r = 1; r < C; ++r) ptx::st_async_f2(ptx::mapa(res_addr, r), tot.m, tot.s, ptx::mapa(xb, r));
             }
-            ptx::cluster_sync();
+        } else {
+            ptx::mbar_wait_bounded<true>(xb, xph, tmo, abort, err, 0x70000010u | uint32_t(par));
             tot = res[par];
         }
         // broadcast back over the row: out = exp(y - mt) * exp(mt - m) / s
@@ -230,14 +248,14 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
                     if (g < g1 && 4 * g + j < cols) __stcs(o + 4 * g + j, e[v][j] * f);
             }
         }
-        // slot[par] / res[par] are written again two rows later, after every CTA
-        // of the cluster has passed the next row's cluster barrier
+        // slot[par] / res[par] are written again two rows later: a peer sends for
+        // row it+2 only after this CTA sent for row it+1, which its thread 0 does
+        // after the barrier above that every thread passes once done with row it
     }
     // the next grid may be scheduled once this CTA's rows are written
     ptx::griddep_launch_dependents();
-    // No CTA leaves while a peer may still access its shared memory.  Every
-    // remote write was ordered by the last exchange barrier (release/acquire),
-    // so this one needs no release: it must not wait for the row's global stores.
+    // No CTA leaves while a peer may still access its shared memory (every
+    // incoming st.async was waited for; this covers the outgoing ones).
     ptx::cluster_arrive_relaxed();
     ptx::cluster_wait_acquire();
 }
@@ -299,7 +317,7 @@ int stitch_packed_blocks_per_sm(int lpr, bool vec) {
 }
 
 cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias, float *out, int64_t rows,
-                          int64_t cols, uint32_t * /*err*/, cudaStream_t stream) {
+                          int64_t cols, uint32_t *err, cudaStream_t stream) {
     if (p.mapping == 1) {
         void *fn = packed_kernel(p.lpr, p.vec);
         if (!fn) return cudaErrorInvalidValue;
@@ -352,8 +370,9 @@ cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = p.pdl ? 2 : 1;
+        unsigned long long tmo = p.timeout_ns;
         void *args[] = {(void *)&A, (void *)&bias, (void *)&out, (void *)&rows, (void *)&icols, (void *)&gpc,
-                        (void *)&leader};
+                        (void *)&leader, (void *)&err, (void *)&tmo};
         return cudaLaunchKernelExC(&cfg, fn, args);
     }
     return cudaErrorInvalidValue;
