@@ -222,7 +222,7 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
     // costs max(2 mainloops, one epilogue).  A wide tile has one accumulator, so
     // its tiles run one after another: mainloop + epilogue each.  Constants
     // measured on GB300 with the device trace (128x256 tiles per CTA):
-    //   mainloop  ~ 0.48 us per 64-deep k-block for a CTA pair, 0.55 us single
+    //   mainloop  ~ 0.35 us per 64-deep k-block for a CTA pair, 0.50 us single
     //               (per 256 columns of W staged)
     //   epilogue  ~ 4.5 us; + 1.5 + 0.2 G us when the row spans G > 1 clusters
     //               (the global barrier waits for the slowest of G clusters);
@@ -244,7 +244,7 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
         const int64_t T = int64_t((rb + cm - 1) / cm) * g;
         if (T < n) n = int(T);
         const int64_t per = (T + n - 1) / n;
-        const double t_main = nk * (cm == 2 ? 0.48 : 0.55) * (ns / 256.0);
+        const double t_main = nk * (cm == 2 ? 0.35 : 0.50) * (ns / 256.0);
         const double t_epi = 4.5 + (g > 1 ? 1.5 + 0.2 * g : 0.0) + (cm == 2 && nk < 8 ? 0.5 : 0.0);
         *ncl_out = n;
         if (wide) return double(per) * (t_main + t_epi);

@@ -198,6 +198,24 @@ def test_softmax_small(M, N, K):
     check_softmax(_softmax(d, s), oracle.gemm_rowsoftmax(d["X"], d["W"], scale=s), f"softmax {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("scale,n_slice", [(128 ** -0.5, 0), (1.0, 0), (4.0, 256)])
+def test_softmax_within_one_bf16_ulp(scale, n_slice):
+    """Every output within one bf16 ulp of the exact value: the exponentials
+    (three of four on MUFU ex2, one on the FMA pipe) and the row sums are
+    fp32-accurate, so only the final rounding to bf16 remains.  Scale 4 gives
+    peaked rows whose largest entries carry the relative error."""
+    M, N, K = 300, 2048, 128
+    d = inputs.gemm_inputs(M, N, K, seed=61, x_std=1.0, w_std=K ** -0.5,
+                           bias_std=None, gamma_std=None, beta_std=None)
+    t = cf.tuning(n_slice=n_slice) if n_slice else None
+    y = _softmax(d, scale, tuning=t)
+    ref = oracle.gemm_rowsoftmax(d["X"], d["W"], scale=scale)
+    err = np.abs(y - ref)
+    bound = np.abs(ref) * 2.0 ** -8 + 1e-30
+    worst = float(np.max(err / bound))
+    assert worst <= 1.0, f"scale {scale}: worst error {worst:.3f} bf16 ulps"
+
+
 def test_softmax_with_bias_and_modes():
     d = inputs.gemm_inputs(200, 2048, 128, seed=4, x_std=1.0, w_std=128 ** -0.5,
                            bias_std=0.5, gamma_std=None, beta_std=None)
