@@ -19,8 +19,9 @@ written out in float64 on the same (bf16 / fp32) input values:
                                                Model, Fig. 3: x = alpha*Acc+Bias)
 * activation  g = GELU_tanh(x) or g = x       (a unary compute node, ComFuse,
                                                Fusion Spec IR mapping Phi)
-* reduction   LayerNorm / Softmax as "reduce over the inputs, normalise the
-              original values" (ComFuse, nested Fusion Spec IR at reductions)
+* reduction   LayerNorm / RMSNorm / Softmax as "reduce over the inputs,
+              normalise the original values" (ComFuse, nested Fusion Spec IR
+              at reductions, which names all three patterns)
 * stitched    y = A^3 + b[row]; rowwise softmax (AStitch, "Adaptive thread
               mapping": row reductions on 750000x32 and 64x30000)
 
@@ -37,6 +38,9 @@ Readings taken where the pages are silent:
   * LayerNorm variance is the biased one (divide by N), eps inside the square
     root, gamma/beta applied after normalising; with GELU the norm is taken
     over the post-GELU values.
+  * RMSNorm divides each value by sqrt(mean of the squares + eps) with no mean
+    subtraction (the usual definition, Zhang & Sennrich 2019); gamma scales
+    after normalising and beta, when given, is added last.
   * Softmax scale multiplies the accumulator before max/exp; an optional bias
     is added after scaling.  Exponent base e.
   * GELU is the tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
@@ -56,8 +60,10 @@ __all__ = [
     "gemm_naive",
     "gelu_tanh",
     "layernorm_rows",
+    "rmsnorm_rows",
     "softmax_rows",
     "gemm_bias_rownorm",
+    "gemm_bias_rmsnorm",
     "gemm_rowsoftmax",
     "stitch_rowreduce_broadcast",
     "ROW_CHUNK",
@@ -129,6 +135,19 @@ def layernorm_rows(g, gamma, beta, eps: float) -> np.ndarray:
     return d / np.sqrt(var + float(eps)) * _f64(gamma) + _f64(beta)
 
 
+def rmsnorm_rows(g, gamma, beta, eps: float) -> np.ndarray:
+    """y = g / sqrt(mean(g^2) + eps) * gamma (+ beta), each row of g.
+
+    RMSNorm as a nested stage DAG (ComFuse, Fusion Spec IR): the reduction is
+    the mean of the squares over the row; the PostOp rescales the original
+    values.  ``beta`` may be None (no shift node).
+    """
+    g = _f64(g)
+    ms = (g * g).mean(axis=-1, keepdims=True)
+    y = g / np.sqrt(ms + float(eps)) * _f64(gamma)
+    return y if beta is None else y + _f64(beta)
+
+
 def softmax_rows(z) -> np.ndarray:
     """Row softmax: m = max z; e = exp(z - m); y = e / sum(e)."""
     z = _f64(z)
@@ -170,6 +189,31 @@ def gemm_bias_rownorm(X, W, bias, gamma, beta, *, alpha: float = 1.0,
         x = float(alpha) * gemm(X[idx], W) + b
         g = gelu_tanh(x) if act == "gelu_tanh" else x
         out[o:o + idx.size] = layernorm_rows(g, gamma, beta, eps)
+        o += idx.size
+    return out
+
+
+def gemm_bias_rmsnorm(X, W, bias, gamma, beta=None, *, alpha: float = 1.0,
+                      eps: float = 1e-5, act: str = "none", rows=None) -> np.ndarray:
+    """y = RMSNorm(act(alpha * X.W + bias)) * gamma (+ beta), row by row.
+
+    The same stage-1 nodes as ``gemm_bias_rownorm`` (ComFuse, Stage-Stream
+    Execution Model, Fig. 3: x = alpha*Acc+Bias, then the optional GELU node)
+    followed by the RMSNorm reduction and PostOp.
+    """
+    if act not in ("none", "gelu_tanh"):
+        raise ValueError(f"unknown activation {act!r}")
+    X = np.asarray(X)
+    M = X.shape[0]
+    N = np.asarray(W).shape[1]
+    out_rows = M if rows is None else len(rows)
+    out = np.empty((out_rows, N), dtype=np.float64)
+    b = np.zeros(N) if bias is None else _f64(bias)
+    o = 0
+    for idx in _row_chunks(M, rows):
+        x = float(alpha) * gemm(X[idx], W) + b
+        g = gelu_tanh(x) if act == "gelu_tanh" else x
+        out[o:o + idx.size] = rmsnorm_rows(g, gamma, beta, eps)
         o += idx.size
     return out
 

@@ -145,6 +145,92 @@ def check_layernorm(ln) -> list:
 
 
 # ----------------------------------------------------------------------------
+# RMSNorm
+# ----------------------------------------------------------------------------
+def check_rmsnorm(rms) -> list:
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(16))
+    # eps = 0, gamma = 1, no beta: every row's mean square is 1 to 1e-12
+    for N in (1, 2, 7, 512, 4096):
+        g = rng.standard_normal((5, N)) * 0.013 + 0.37
+        y = np.asarray(rms(g, np.ones(N), None, 0.0))
+        ms = (y * y).mean(axis=1)
+        _fail(fails, np.all(np.abs(ms - 1) < 1e-12), f"RMS eps=0 mean square N={N}: {ms}")
+    # the mean is not subtracted: a row with a large offset keeps its sign pattern
+    g = np.array([[10.0, 10.5, 9.5]])
+    y = np.asarray(rms(g, np.ones(3), None, 0.0))[0]
+    _fail(fails, np.all(y > 0), "RMS keeps the mean (no centring)")
+    # eps > 0: output mean square = ms / (ms + eps), ms by exact summation of squares
+    for N in (4, 33):
+        row = rng.standard_normal(N) * 0.01
+        ms = math.fsum(float(v) * float(v) for v in row) / N
+        eps = 1e-5
+        y = np.asarray(rms(row[None, :], np.ones(N), None, eps))[0]
+        _fail(fails, abs(float((y * y).mean()) - ms / (ms + eps)) < 1e-12, "RMS eps>0 mean square")
+    # constant row c: y = c / sqrt(c^2 + eps) * gamma + beta
+    N, c, eps = 8, -2.5, 0.25
+    gam = rng.standard_normal(N)
+    bet = rng.standard_normal(N)
+    y = np.asarray(rms(np.full((1, N), c), gam, bet, eps))[0]
+    _fail(fails, np.allclose(y, c / math.sqrt(c * c + eps) * gam + bet, rtol=1e-14, atol=1e-15), "RMS constant row")
+    # odd under sign flip, invariant under positive scaling at eps = 0
+    g = rng.standard_normal((3, 64))
+    y1 = np.asarray(rms(g, np.ones(64), None, 0.0))
+    _fail(fails, np.allclose(np.asarray(rms(-g, np.ones(64), None, 0.0)), -y1, rtol=0, atol=1e-15), "RMS sign")
+    _fail(fails, np.allclose(np.asarray(rms(g * 37.5, np.ones(64), None, 0.0)), y1, rtol=1e-12, atol=1e-12),
+          "RMS scale invariance")
+    # beta None == beta 0
+    _fail(fails, np.array_equal(np.asarray(rms(g, np.ones(64), None, 1e-5)),
+                                np.asarray(rms(g, np.ones(64), np.zeros(64), 1e-5))), "RMS beta None")
+    # hand-derived worked fixture
+    t = _load_golden("rmsnorm_worked.txt")
+    for blk in (t[:2], t[2:]):
+        g, gam, bet, eps, want = blk[:, 0], blk[:, 1], blk[:, 2], blk[0, 3], blk[:, 4]
+        y = np.asarray(rms(g[None, :], gam, bet, eps))[0]
+        _fail(fails, np.allclose(y, want, rtol=1e-13, atol=1e-15), f"RMS golden {y} vs {want}")
+    # independent library routine (fp64)
+    import torch
+    g = rng.standard_normal((4, 96)) * 0.02
+    gam = 1 + 0.1 * rng.standard_normal(96)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(g), (96,), torch.from_numpy(gam), 1e-5).numpy()
+    _fail(fails, np.allclose(np.asarray(rms(g, gam, None, 1e-5)), ref, rtol=1e-11, atol=1e-12),
+          "RMS vs torch rms_norm fp64")
+    return fails
+
+
+def check_rmsnorm_composition(fused) -> list:
+    import torch
+    F = torch.nn.functional
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(17))
+    M, K, N = 9, 24, 40
+    X = rng.standard_normal((M, K)) / 5
+    W = rng.standard_normal((K, N)) / 5
+    bias = rng.standard_normal(N) * 0.1
+    gam = 1 + rng.standard_normal(N) * 0.1
+    bet = rng.standard_normal(N) * 0.1
+    t = {k: torch.from_numpy(v) for k, v in dict(X=X, W=W, b=bias, g=gam, be=bet).items()}
+    for act in ("none", "gelu_tanh"):
+        for alpha in (1.0, 0.5):
+            x = alpha * (t["X"] @ t["W"]) + t["b"]
+            if act == "gelu_tanh":
+                x = F.gelu(x, approximate="tanh")
+            ref = (F.rms_norm(x, (N,), t["g"], 1e-5) + t["be"]).numpy()
+            y = np.asarray(fused(X, W, bias, gam, bet, alpha=alpha, eps=1e-5, act=act))
+            _fail(fails, y.shape == ref.shape and np.allclose(y, ref, rtol=1e-10, atol=1e-11),
+                  f"rmsnorm composition act={act} alpha={alpha}")
+    y0 = np.asarray(fused(X, W, None, gam, None, alpha=1.0, eps=1e-5, act="none"))
+    y1 = np.asarray(fused(X, W, np.zeros(N), gam, np.zeros(N), alpha=1.0, eps=1e-5, act="none"))
+    _fail(fails, np.allclose(y0, y1, rtol=0, atol=1e-15), "rmsnorm bias/beta None")
+    rows = [8, 0, 3]
+    ys = np.asarray(fused(X, W, bias, gam, bet, alpha=1.0, eps=1e-5, act="gelu_tanh", rows=rows))
+    yf = np.asarray(fused(X, W, bias, gam, bet, alpha=1.0, eps=1e-5, act="gelu_tanh"))
+    _fail(fails, ys.shape == yf[rows].shape and np.allclose(ys, yf[rows], rtol=1e-13, atol=1e-14),
+          "rmsnorm rows= subset")
+    return fails
+
+
+# ----------------------------------------------------------------------------
 # Softmax
 # ----------------------------------------------------------------------------
 def check_softmax(sm) -> list:

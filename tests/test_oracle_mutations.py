@@ -43,6 +43,33 @@ LN_MUTANTS = {
 }
 
 
+def _rms(g, gamma, beta, eps, *, center=False, eps_out=False, use_sum=False, beta_inside=False,
+         gamma_first=False):
+    g = np.asarray(g, dtype=np.float64)
+    gamma = np.asarray(gamma, dtype=np.float64)
+    b = 0.0 if beta is None else np.asarray(beta, dtype=np.float64)
+    if beta_inside:
+        g = g + b
+    if gamma_first:
+        g = g * gamma
+    c = g - g.mean(-1, keepdims=True) if center else g
+    ms = (c * c).sum(-1, keepdims=True) if use_sum else (c * c).mean(-1, keepdims=True)
+    den = (np.sqrt(ms) + eps) if eps_out else np.sqrt(ms + eps)
+    y = c / den
+    if not gamma_first:
+        y = y * gamma
+    return y if beta_inside else y + b
+
+
+RMS_MUTANTS = {
+    "mean subtracted": lambda g, ga, be, e: _rms(g, ga, be, e, center=True),
+    "eps outside sqrt": lambda g, ga, be, e: _rms(g, ga, be, e, eps_out=True),
+    "sum of squares": lambda g, ga, be, e: _rms(g, ga, be, e, use_sum=True),
+    "beta before normalising": lambda g, ga, be, e: _rms(g, ga, be, e, beta_inside=True),
+    "gamma before normalising": lambda g, ga, be, e: _rms(g, ga, be, e, gamma_first=True),
+}
+
+
 def _sm(z, *, sub_max=True, base=math.e, by_max=False):
     z = np.asarray(z, dtype=np.float64)
     m = z.max(-1, keepdims=True) if sub_max else 0.0
@@ -136,6 +163,12 @@ STITCH_MUTANTS = {k: (lambda kk: (lambda A, b, rows=None: _stitch(A, b, rows, mi
 @pytest.mark.parametrize("name", sorted(LN_MUTANTS))
 def test_layernorm_mutant_caught(name):
     assert pins.check_layernorm(LN_MUTANTS[name]), name
+
+
+@pytest.mark.parametrize("name", sorted(RMS_MUTANTS))
+def test_rmsnorm_mutant_caught(name):
+    with np.errstate(invalid="ignore", divide="ignore"):  # centring a 1-column row gives 0/0
+        assert pins.check_rmsnorm(RMS_MUTANTS[name]), name
 
 
 @pytest.mark.parametrize("name", sorted(SM_MUTANTS))

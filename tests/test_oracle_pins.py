@@ -30,6 +30,14 @@ def test_layernorm_pinned():
     assert pins.check_layernorm(oracle.layernorm_rows) == []
 
 
+def test_rmsnorm_pinned():
+    assert pins.check_rmsnorm(oracle.rmsnorm_rows) == []
+
+
+def test_rmsnorm_composition_pinned():
+    assert pins.check_rmsnorm_composition(oracle.gemm_bias_rmsnorm) == []
+
+
 def test_softmax_pinned():
     assert pins.check_softmax(oracle.softmax_rows) == []
 
