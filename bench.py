@@ -66,9 +66,42 @@ def dist_env():
 
 
 def kind_of(w):
+    """Kernel kind of a GEMM workload (RMSNorm runs in the LayerNorm kernels)."""
     if w.kind == "softmax":
         return 2
     return 1 if w.act == "gelu_tanh" else 0
+
+
+def fused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None):
+    """The public fused call of workload w."""
+    if w.kind == "softmax":
+        return cf.cf_gemm_fused_rowsoftmax(X, W, None, Y, w.M, w.N, w.K, w.scale, ws, wsb, stream)
+    act = cf.CF_ACT_GELU_TANH if w.act == "gelu_tanh" else cf.CF_ACT_NONE
+    fn = cf.cf_gemm_fused_rmsnorm if w.kind == "rmsnorm" else cf.cf_gemm_fused_rownorm
+    return fn(X, W, bias, gamma, beta, Y, w.M, w.N, w.K, w.alpha, w.eps, act, ws, wsb, stream)
+
+
+def unfused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None):
+    if w.kind == "softmax":
+        return cf.cf_unfused_gemm_rowsoftmax(X, W, None, Y, w.M, w.N, w.K, w.scale, ws, wsb, stream)
+    act = cf.CF_ACT_GELU_TANH if w.act == "gelu_tanh" else cf.CF_ACT_NONE
+    fn = cf.cf_unfused_gemm_rmsnorm if w.kind == "rmsnorm" else cf.cf_unfused_gemm_rownorm
+    return fn(X, W, bias, gamma, beta, Y, w.M, w.N, w.K, w.alpha, w.eps, act, ws, wsb, stream)
+
+
+def oracle_rows(oracle, w, d, rows):
+    if w.kind == "softmax":
+        return oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows)
+    fn = oracle.gemm_bias_rmsnorm if w.kind == "rmsnorm" else oracle.gemm_bias_rownorm
+    return fn(d["X"], d["W"], d["bias"], d["gamma"], d["beta"], alpha=w.alpha, eps=w.eps, act=w.act, rows=rows)
+
+
+def row_vectors(w):
+    """The fp32 [N] inputs of a workload's epilogue that are present."""
+    if w.kind == "softmax":
+        return ()
+    return tuple(k for k, sd in (("bias", w.bias_std), ("gamma", w.gamma_std), ("beta", w.beta_std))
+                 if sd is not None)
 
 
 def roofline_time_s(w, peaks):
@@ -176,9 +209,8 @@ class FusedRunner:
         for i in range(nsets):
             s = {"X": X if i == 0 else X.clone(), "W": W if i == 0 else W.clone(),
                  "Y": torch.empty((w.M, w.N), dtype=bf, device=device)}
-            if w.kind == "rownorm":
-                for k in ("bias", "gamma", "beta"):
-                    s[k] = torch.from_numpy(d[k]).to(device)
+            for k in ("bias", "gamma", "beta"):
+                s[k] = torch.from_numpy(d[k]).to(device) if k in row_vectors(w) else None
             self.sets.append(s)
         self.ws_bytes = cf.cf_gemm_fused_workspace_size(w.M, w.N, w.K)
         self.ws = cf.new_workspace(self.ws_bytes, device)
@@ -186,19 +218,14 @@ class FusedRunner:
     def launch(self, i, stream=None):
         cf, w = self.cf, self.w
         s = self.sets[i % len(self.sets)]
-        if w.kind == "softmax":
-            st = cf.cf_gemm_fused_rowsoftmax(s["X"], s["W"], None, s["Y"], w.M, w.N, w.K, w.scale,
-                                             self.ws, self.ws_bytes, stream)
-        else:
-            act = cf.CF_ACT_GELU_TANH if w.act == "gelu_tanh" else cf.CF_ACT_NONE
-            st = cf.cf_gemm_fused_rownorm(s["X"], s["W"], s["bias"], s["gamma"], s["beta"], s["Y"],
-                                          w.M, w.N, w.K, w.alpha, w.eps, act, self.ws, self.ws_bytes, stream)
+        st = fused_call(cf, w, s["X"], s["W"], s["bias"], s["gamma"], s["beta"], s["Y"], self.ws, self.ws_bytes,
+                        stream)
         cf.check(st, "fused launch")
 
 
 def _seeded_inputs(w, rank):
     seed = mdist.seed_for(w.seed, rank)
-    if w.kind == "rownorm":
+    if w.kind in ("rownorm", "rmsnorm"):
         return inputs.gemm_inputs(w.M, w.N, w.K, seed, x_std=w.x_std, w_std=w.w_std,
                                   bias_std=w.bias_std, gamma_std=w.gamma_std, beta_std=w.beta_std)
     return inputs.gemm_inputs(w.M, w.N, w.K, seed, x_std=w.x_std, w_std=w.w_std,
@@ -266,25 +293,19 @@ def time_e2e(torch, cf, w, steps, device):
     X = torch.empty_like(hX, device=device)
     W = torch.empty_like(hW, device=device)
     Y = torch.empty((w.M, w.N), dtype=bf, device=device)
-    extra = {}
-    if w.kind == "rownorm":
-        for k in ("bias", "gamma", "beta"):
-            extra[k] = torch.from_numpy(d[k]).pin_memory()
-            extra["d_" + k] = torch.empty_like(extra[k], device=device)
+    extra = {"d_bias": None, "d_gamma": None, "d_beta": None}
+    for k in row_vectors(w):
+        extra[k] = torch.from_numpy(d[k]).pin_memory()
+        extra["d_" + k] = torch.empty_like(extra[k], device=device)
     wsb = cf.cf_gemm_fused_workspace_size(w.M, w.N, w.K)
     ws = cf.new_workspace(wsb, device)
 
     def step():
         X.copy_(hX, non_blocking=True)
         W.copy_(hW, non_blocking=True)
-        if w.kind == "softmax":
-            cf.check(cf.cf_gemm_fused_rowsoftmax(X, W, None, Y, w.M, w.N, w.K, w.scale, ws, wsb))
-        else:
-            for k in ("bias", "gamma", "beta"):
-                extra["d_" + k].copy_(extra[k], non_blocking=True)
-            act = cf.CF_ACT_GELU_TANH if w.act == "gelu_tanh" else cf.CF_ACT_NONE
-            cf.check(cf.cf_gemm_fused_rownorm(X, W, extra["d_bias"], extra["d_gamma"], extra["d_beta"], Y,
-                                              w.M, w.N, w.K, w.alpha, w.eps, act, ws, wsb))
+        for k in row_vectors(w):
+            extra["d_" + k].copy_(extra[k], non_blocking=True)
+        cf.check(fused_call(cf, w, X, W, extra["d_bias"], extra["d_gamma"], extra["d_beta"], Y, ws, wsb))
         hY.copy_(Y, non_blocking=True)
 
     for _ in range(3):
@@ -298,7 +319,7 @@ def time_e2e(torch, cf, w, steps, device):
     e1.record()
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) / 1e3 / steps
-    h2d = hX.numel() * 2 + hW.numel() * 2 + (3 * 4 * w.N if w.kind == "rownorm" else 0)
+    h2d = hX.numel() * 2 + hW.numel() * 2 + 4 * w.N * len(row_vectors(w))
     d2h = hY.numel() * 2
     return t, h2d, d2h
 
@@ -341,13 +362,7 @@ def unfused_time(torch, cf, runner, reps):
     class U:
         def launch(self, i, stream=None):
             s = runner.sets[i % len(runner.sets)]
-            if w.kind == "softmax":
-                st = cf.cf_unfused_gemm_rowsoftmax(s["X"], s["W"], None, s["Y"], w.M, w.N, w.K, w.scale, ws, wsb,
-                                                   stream)
-            else:
-                act = cf.CF_ACT_GELU_TANH if w.act == "gelu_tanh" else cf.CF_ACT_NONE
-                st = cf.cf_unfused_gemm_rownorm(s["X"], s["W"], s["bias"], s["gamma"], s["beta"], s["Y"], w.M, w.N,
-                                                w.K, w.alpha, w.eps, act, ws, wsb, stream)
+            st = unfused_call(cf, w, s["X"], s["W"], s["bias"], s["gamma"], s["beta"], s["Y"], ws, wsb, stream)
             cf.check(st, "unfused launch")
 
     t, n, _ = time_steps(torch, U(), reps, 3, lambda: None, graph_len=reps)
@@ -388,11 +403,7 @@ def cpu_oracle_sample(w, budget_s=10.0, max_rows=None):
     while t_total < budget_s:
         rows = np.sort(rng.choice(w.M, size=rows_per, replace=False))
         t0 = time.perf_counter()
-        if w.kind == "softmax":
-            oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows)
-        else:
-            oracle.gemm_bias_rownorm(d["X"], d["W"], d["bias"], d["gamma"], d["beta"], alpha=w.alpha,
-                                     eps=w.eps, act=w.act, rows=rows)
+        oracle_rows(oracle, w, d, rows)
         t_total += time.perf_counter() - t0
         done_rows += rows_per
     flops = 2.0 * done_rows * w.N * w.K
@@ -431,6 +442,8 @@ def run_ours(args):
     value = mdist.job_throughput(w.flops * n, ws_, t) / 1e12
     troof, bound = roofline_time_s(w, peaks)
     kernel = {2: "gemm_fused_kernel<SOFTMAX>", 1: "gemm_fused_kernel<GELU_LN>", 0: "gemm_fused_kernel<LN>"}[kind_of(w)]
+    if w.kind == "rmsnorm":
+        kernel += " (RMSNorm)"
     if bound == "hbm":
         achieved = w.unavoidable_bytes / t1 / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -550,11 +563,7 @@ def run_reference(args):
 
     def step():
         rows = np.sort(rng.choice(w.M, size=rows_per_step, replace=False))
-        if w.kind == "softmax":
-            oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows)
-        else:
-            oracle.gemm_bias_rownorm(d["X"], d["W"], d["bias"], d["gamma"], d["beta"], alpha=w.alpha,
-                                     eps=w.eps, act=w.act, rows=rows)
+        oracle_rows(oracle, w, d, rows)
 
     for _ in range(args.warmup):
         step()

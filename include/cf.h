@@ -279,6 +279,34 @@ CF_API cf_status cf_gemm_fused_rownorm_noalloc(const void *X, const void *W, con
                                                float eps, cf_activation act, cf_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Fused GEMM + bias (+ GELU) + RMSNorm                                      */
+/* ------------------------------------------------------------------------ */
+/* Y = RMSNorm_row(act(alpha * X.W + bias)) * gamma (+ beta), where
+ * RMSNorm_row(g) = g / sqrt(mean_row(g^2) + eps) (no mean subtraction).
+ *
+ * [ComFuse] Fusion Spec IR names RMSNorm among the patterns that become
+ * nested stage DAGs: the reduction (mean of the squares) runs over the
+ * stage-1 values and the PostOp rescales those values.  The kernel reduces the
+ * same per-row (mean, M2) statistics as LayerNorm -- mean(g^2) = M2/N + mean^2
+ * -- so every schedule of cf_gemm_fused_rownorm (clusters, the global
+ * partial buffer, CTA pairs, wide tiles) applies unchanged.
+ * Arguments, layouts, ownership, workspace, supported shapes and errors as for
+ * cf_gemm_fused_rownorm, except: beta (device, fp32 [N]) may be NULL (no
+ * shift); gamma is required. */
+CF_API cf_status cf_gemm_fused_rmsnorm(const void *X, const void *W, const float *bias,
+                                       const float *gamma, const float *beta, void *Y,
+                                       int64_t M, int64_t N, int64_t K, float alpha,
+                                       float eps, cf_activation act, void *workspace,
+                                       size_t workspace_bytes, cf_stream_t stream);
+
+CF_API cf_status cf_gemm_fused_rmsnorm_ex(const void *X, const void *W, const float *bias,
+                                          const float *gamma, const float *beta, void *Y,
+                                          int64_t M, int64_t N, int64_t K, float alpha,
+                                          float eps, cf_activation act, void *workspace,
+                                          size_t workspace_bytes, cf_stream_t stream,
+                                          const cf_tuning *tuning);
+
+/* ------------------------------------------------------------------------ */
 /* Fused GEMM + scaled row softmax                                           */
 /* ------------------------------------------------------------------------ */
 /* Y = softmax_row(scale * X.W + bias)
@@ -335,6 +363,13 @@ CF_API cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *r
 CF_API size_t cf_unfused_workspace_size(int64_t M, int64_t N, int64_t K);
 
 CF_API cf_status cf_unfused_gemm_rownorm(const void *X, const void *W, const float *bias,
+                                         const float *gamma, const float *beta, void *Y,
+                                         int64_t M, int64_t N, int64_t K, float alpha, float eps,
+                                         cf_activation act, void *workspace,
+                                         size_t workspace_bytes, cf_stream_t stream);
+
+/* The unfused composition of cf_gemm_fused_rmsnorm (beta may be NULL). */
+CF_API cf_status cf_unfused_gemm_rmsnorm(const void *X, const void *W, const float *bias,
                                          const float *gamma, const float *beta, void *Y,
                                          int64_t M, int64_t N, int64_t K, float alpha, float eps,
                                          cf_activation act, void *workspace,

@@ -105,11 +105,17 @@ _SIGS = {
                                        _P, _SZ, _P, ctypes.POINTER(cf_tuning)]),
     "cf_gemm_fused_rownorm_noalloc": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
                                             _P]),
+    "cf_gemm_fused_rmsnorm": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
+                                    _P, _SZ, _P]),
+    "cf_gemm_fused_rmsnorm_ex": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
+                                       _P, _SZ, _P, ctypes.POINTER(cf_tuning)]),
     "cf_gemm_fused_rowsoftmax": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P]),
     "cf_gemm_fused_rowsoftmax_ex": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P,
                                           ctypes.POINTER(cf_tuning)]),
     "cf_unfused_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "cf_unfused_gemm_rownorm": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
+                                      _P, _SZ, _P]),
+    "cf_unfused_gemm_rmsnorm": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
                                       _P, _SZ, _P]),
     "cf_unfused_gemm_rowsoftmax": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P]),
     "cf_stitch_rowreduce_broadcast": (_ST, [_P, _P, _P, _I64, _I64, _P, _SZ, _P]),
@@ -234,6 +240,19 @@ def cf_gemm_fused_rownorm(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, 
                                       _stream(stream), _tun(tuning))
 
 
+def cf_gemm_fused_rmsnorm(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, workspace,
+                          workspace_bytes, stream=None, tuning=None) -> int:
+    """Y = RMSNorm(act(alpha*X.W + bias)) * gamma (+ beta); beta may be None."""
+    L = lib()
+    if tuning is None:
+        return L.cf_gemm_fused_rmsnorm(_ptr(X), _ptr(W), _ptr(bias), _ptr(gamma), _ptr(beta), _ptr(Y),
+                                       M, N, K, alpha, eps, act, _ptr(workspace), workspace_bytes,
+                                       _stream(stream))
+    return L.cf_gemm_fused_rmsnorm_ex(_ptr(X), _ptr(W), _ptr(bias), _ptr(gamma), _ptr(beta), _ptr(Y),
+                                      M, N, K, alpha, eps, act, _ptr(workspace), workspace_bytes,
+                                      _stream(stream), _tun(tuning))
+
+
 def cf_gemm_fused_rownorm_noalloc(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, stream=None) -> int:
     """cf_gemm_fused_rownorm without a workspace: for callers that cannot
     allocate device memory; its scratch is a fixed 4 MiB array inside libcf."""
@@ -270,6 +289,13 @@ def cf_unfused_gemm_rownorm(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act
                             stream=None) -> int:
     """The unfused two-kernel composition (GEMM -> fp32 P -> row kernel), for comparison."""
     return lib().cf_unfused_gemm_rownorm(_ptr(X), _ptr(W), _ptr(bias), _ptr(gamma), _ptr(beta), _ptr(Y),
+                                         M, N, K, alpha, eps, act, _ptr(workspace), workspace_bytes,
+                                         _stream(stream))
+
+
+def cf_unfused_gemm_rmsnorm(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, workspace, workspace_bytes,
+                            stream=None) -> int:
+    return lib().cf_unfused_gemm_rmsnorm(_ptr(X), _ptr(W), _ptr(bias), _ptr(gamma), _ptr(beta), _ptr(Y),
                                          M, N, K, alpha, eps, act, _ptr(workspace), workspace_bytes,
                                          _stream(stream))
 
@@ -313,6 +339,21 @@ def gemm_fused_rownorm(X, W, bias, gamma, beta, *, alpha=1.0, eps=1e-5, act="non
     a = {"none": CF_ACT_NONE, "gelu_tanh": CF_ACT_GELU_TANH}[act]
     check(cf_gemm_fused_rownorm(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, a, ws, ws.numel(),
                                 stream, tuning), "cf_gemm_fused_rownorm")
+    return Y
+
+
+def gemm_fused_rmsnorm(X, W, bias, gamma, beta=None, *, alpha=1.0, eps=1e-5, act="none", out=None,
+                       workspace=None, stream=None, tuning=None):
+    """Y = RMSNorm(act(alpha*X@W + bias))*gamma (+ beta); X, W bf16 CUDA tensors."""
+    import torch
+    M, K = X.shape
+    N = W.shape[1]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    ws = workspace if workspace is not None else new_workspace(cf_gemm_fused_workspace_size(M, N, K),
+                                                               X.device, stream)
+    a = {"none": CF_ACT_NONE, "gelu_tanh": CF_ACT_GELU_TANH}[act]
+    check(cf_gemm_fused_rmsnorm(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, a, ws, ws.numel(),
+                                stream, tuning), "cf_gemm_fused_rmsnorm")
     return Y
 
 

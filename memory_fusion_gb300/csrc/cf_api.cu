@@ -470,10 +470,10 @@ cf_status cf_query_gemm_fused_plan(int64_t M, int64_t N, int64_t K, int32_t kind
 static cf_status gemm_fused_common(int kind, const void *X, const void *W, const float *bias, const float *gamma,
                                    const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha,
                                    float eps, void *ws, size_t ws_bytes, cf_stream_t stream,
-                                   const cf_tuning *tuning) {
+                                   const cf_tuning *tuning, int rms = 0) {
     if (M < 0 || N <= 0 || K <= 0) return CF_ERR_INVALID_ARG;
     if (!X || !W || !Y || !ws) return CF_ERR_INVALID_ARG;
-    if (kind != cf::EPI_SOFTMAX && (!gamma || !beta)) return CF_ERR_INVALID_ARG;
+    if (kind != cf::EPI_SOFTMAX && (!gamma || (!beta && !rms))) return CF_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || (bias && !aligned16(bias)) ||
         (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)))
         return CF_ERR_MISALIGNED;
@@ -527,6 +527,7 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
     a.super_blocks = (plan.row_blocks + plan.cluster_m - 1) / plan.cluster_m;
     a.row_blocks_alloc = a.super_blocks * plan.cluster_m;
     a.extra_arrivals = t.extra_arrivals;
+    a.rms = rms;
     a.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
     a.trace = reinterpret_cast<unsigned long long *>(t.trace);
     a.multicast_x = (t.multicast_x && plan.cluster_m == 1 && plan.cluster_size > 1) ? 1 : 0;
@@ -552,6 +553,25 @@ cf_status cf_gemm_fused_rownorm(const void *X, const void *W, const float *bias,
                                 const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha,
                                 float eps, cf_activation act, void *ws, size_t ws_bytes, cf_stream_t stream) {
     return cf_gemm_fused_rownorm_ex(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, ws, ws_bytes, stream,
+                                    nullptr);
+}
+
+cf_status cf_gemm_fused_rmsnorm_ex(const void *X, const void *W, const float *bias, const float *gamma,
+                                   const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha,
+                                   float eps, cf_activation act, void *ws, size_t ws_bytes, cf_stream_t stream,
+                                   const cf_tuning *tuning) {
+    int kind;
+    if (act == CF_ACT_NONE) kind = cf::EPI_LN;
+    else if (act == CF_ACT_GELU_TANH) kind = cf::EPI_GELU_LN;
+    else return CF_ERR_INVALID_ARG;
+    return gemm_fused_common(kind, X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, ws, ws_bytes, stream, tuning,
+                             1);
+}
+
+cf_status cf_gemm_fused_rmsnorm(const void *X, const void *W, const float *bias, const float *gamma,
+                                const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha,
+                                float eps, cf_activation act, void *ws, size_t ws_bytes, cf_stream_t stream) {
+    return cf_gemm_fused_rmsnorm_ex(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, ws, ws_bytes, stream,
                                     nullptr);
 }
 
@@ -733,10 +753,10 @@ cf_status gemm_store_f32(const void *X, const void *W, float *P, uint32_t *err, 
 
 cf_status unfused_common(int op, const void *X, const void *W, const float *bias, const float *gamma,
                          const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha, float eps,
-                         void *ws, size_t ws_bytes, cf_stream_t stream) {
+                         void *ws, size_t ws_bytes, cf_stream_t stream, int rms = 0) {
     if (M < 0 || N <= 0 || K <= 0) return CF_ERR_INVALID_ARG;
     if (!X || !W || !Y || !ws) return CF_ERR_INVALID_ARG;
-    if (op != 2 && (!gamma || !beta)) return CF_ERR_INVALID_ARG;
+    if (op != 2 && (!gamma || (!beta && !rms))) return CF_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(ws) || (bias && !aligned16(bias)) ||
         (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)))
         return CF_ERR_MISALIGNED;
@@ -750,7 +770,7 @@ cf_status unfused_common(int op, const void *X, const void *W, const float *bias
     cf_status st = gemm_store_f32(X, W, P, err, M, N, K, s);
     if (st != CF_OK) return st;
     cudaError_t e = cf::launch_row_epilogue(op, P, bias, gamma, beta, static_cast<uint16_t *>(Y), M, int(N), alpha,
-                                            eps, s);
+                                            eps, rms, s);
     return e == cudaSuccess ? CF_OK : cuda_fail(e);
 }
 
@@ -771,6 +791,18 @@ extern "C" cf_status cf_unfused_gemm_rownorm(const void *X, const void *W, const
     else if (act == CF_ACT_GELU_TANH) op = 1;
     else return CF_ERR_INVALID_ARG;
     return unfused_common(op, X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, workspace, workspace_bytes, stream);
+}
+
+extern "C" cf_status cf_unfused_gemm_rmsnorm(const void *X, const void *W, const float *bias, const float *gamma,
+                                             const float *beta, void *Y, int64_t M, int64_t N, int64_t K,
+                                             float alpha, float eps, cf_activation act, void *workspace,
+                                             size_t workspace_bytes, cf_stream_t stream) {
+    int op;
+    if (act == CF_ACT_NONE) op = 0;
+    else if (act == CF_ACT_GELU_TANH) op = 1;
+    else return CF_ERR_INVALID_ARG;
+    return unfused_common(op, X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, workspace, workspace_bytes, stream,
+                          1);
 }
 
 extern "C" cf_status cf_unfused_gemm_rowsoftmax(const void *X, const void *W, const float *bias, void *Y, int64_t M,

@@ -53,7 +53,7 @@ int stitch_packed_blocks_per_sm(int lpr, bool vec);
 //   op 0 LN, 1 GELU+LN, 2 softmax over fp32 rows of P -> bf16 Y
 // --------------------------------------------------------------------------
 cudaError_t launch_row_epilogue(int op, const float *P, const float *bias, const float *gamma, const float *beta,
-                                uint16_t *Y, int64_t M, int N, float alpha, float eps, cudaStream_t stream);
+                                uint16_t *Y, int64_t M, int N, float alpha, float eps, int rms, cudaStream_t stream);
 
 // --------------------------------------------------------------------------
 // fused GEMM kernels (gemm_fused.cu)
@@ -71,12 +71,12 @@ struct GemmArgs {
     CUtensorMap tmap_y;   // Y [M,N] bf16, box 32(N) x 32(M), 64B swizzle (stores);
                           // EPI_STORE_F32: P [M,N] fp32, box 16(N) x 32(M)
     const float *bias;    // [N] or null
-    const float *gamma;   // [N] (LN)
-    const float *beta;    // [N] (LN)
+    const float *gamma;   // [N] (LN, RMSNorm)
+    const float *beta;    // [N] (LN; RMSNorm: or null)
     uint16_t *y;          // [M,N] bf16
     uint32_t *err;        // workspace error word
     uint32_t *counters;   // [2*RB]: arrive, depart
-    float2 *partials;     // [RB][128][Gp]
+    float2 *partials;     // [RB][Gp][128]
     int M, N, K;
     float alpha;          // LN: multiplies acc; softmax: scale
     float eps;
@@ -92,6 +92,7 @@ struct GemmArgs {
     int row_blocks_alloc; // RB rounded up to a multiple of C_M (counter / partial rows)
     int super_blocks;     // RB_alloc / C_M
     int extra_arrivals;   // test hook
+    int rms;              // LN kinds: normalise by sqrt(mean(g^2) + eps), no centring (RMSNorm)
     unsigned long long timeout_ns;
     unsigned long long *trace;  // optional %globaltimer stamps, CF_TRACE_SLOTS per CTA
 };

@@ -3,6 +3,7 @@
 // many tiles and CTAs:
 //     LN:       y = LayerNorm(alpha*acc + bias) * gamma + beta
 //     GELU_LN:  y = LayerNorm(GELU_tanh(alpha*acc + bias)) * gamma + beta
+//               (with GemmArgs::rms, RMSNorm in place of LayerNorm for both)
 //     SOFTMAX:  y = softmax(scale*acc + bias)
 //
 // Design (GB300-first; the page mechanisms it realises are cited inline):
@@ -534,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                     pb[c] = a.bias ? __ldg(a.bias + ncta + c) : 0.f;
                     if constexpr (EPI != EPI_SOFTMAX) {
                         pg[c] = __ldg(a.gamma + ncta + c);
-                        pe[c] = __ldg(a.beta + ncta + c);
+                        pe[c] = a.beta ? __ldg(a.beta + ncta + c) : 0.f;
                     }
                 }
             }
@@ -780,8 +781,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             const int ystore = m0 + q * 32;
             float mean = 0.f, rstd = 0.f;
             if constexpr (EPI != EPI_SOFTMAX) {
-                mean = stat.x;
-                rstd = rsqrtf(stat.y / fN + a.eps);
+                // LayerNorm: (g - mean) / sqrt(M2/N + eps); RMSNorm: g / sqrt(mean(g^2) + eps)
+                // with mean(g^2) = M2/N + mean^2 from the same statistics
+                const float var = stat.y / fN;
+                mean = a.rms ? 0.f : stat.x;
+                rstd = rsqrtf((a.rms ? fmaf(stat.x, stat.x, var) : var) + a.eps);
             }
 #pragma unroll
             for (int c = 0; c < 8; c += 2) {

@@ -5,6 +5,7 @@
 //     op 0 (LN):       y = LayerNorm(alpha*P + bias) * gamma + beta
 //     op 1 (GELU_LN):  y = LayerNorm(GELU_tanh(alpha*P + bias)) * gamma + beta
 //     op 2 (SOFTMAX):  y = softmax(alpha*P + bias)
+// (ops 0 and 1 with `rms`: RMSNorm, y = g / sqrt(mean(g^2) + eps) * gamma + beta)
 // This is the materialised-intermediate schedule the fusion removes ([ComFuse]
 // Stage-Stream Execution Model: an edge that would otherwise be a buffer in
 // GMEM); it exists so the cost of that buffer can be measured, not as a
@@ -47,7 +48,7 @@ __global__ void __launch_bounds__(kRowThreads) row_epilogue_kernel(const float *
                                                                    const float *__restrict__ gamma,
                                                                    const float *__restrict__ beta,
                                                                    uint16_t *__restrict__ Y, int64_t M, int N,
-                                                                   float alpha, float eps) {
+                                                                   float alpha, float eps, int rms) {
     constexpr int G4 = VPT / 4;  // float4 groups per thread; group j holds columns (j*256 + t)*4 ..
     __shared__ float4 red[kRowThreads / 32];
     __shared__ float2 fin;
@@ -130,7 +131,9 @@ __global__ void __launch_bounds__(kRowThreads) row_epilogue_kernel(const float *
             if (t == 0) {
                 Stat3 a{red[0].x, red[0].y, red[0].z};
                 for (int w = 1; w < kRowThreads / 32; ++w) a = combine3(a, Stat3{red[w].x, red[w].y, red[w].z});
-                fin = make_float2(a.mean, rsqrtf(a.m2 / float(N) + eps));
+                const float var = a.m2 / float(N);
+                fin = rms ? make_float2(0.f, rsqrtf(fmaf(a.mean, a.mean, var) + eps))
+                          : make_float2(a.mean, rsqrtf(var + eps));
             }
             __syncthreads();
             stat = fin;
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kRowThreads) row_epilogue_kernel(const float *
             float y0 = x[4 * j], y1 = x[4 * j + 1], y2 = x[4 * j + 2], y3 = x[4 * j + 3];
             if constexpr (OP != 2) {
                 const float4 g = __ldg(reinterpret_cast<const float4 *>(gamma + c));
-                const float4 b = __ldg(reinterpret_cast<const float4 *>(beta + c));
+                const float4 b = beta ? __ldg(reinterpret_cast<const float4 *>(beta + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
                 y0 = fmaf((y0 - stat.x) * stat.y, g.x, b.x);
                 y1 = fmaf((y1 - stat.x) * stat.y, g.y, b.y);
                 y2 = fmaf((y2 - stat.x) * stat.y, g.z, b.z);
@@ -174,7 +177,7 @@ void *row_fn(int vpt) {
 }  // namespace
 
 cudaError_t launch_row_epilogue(int op, const float *P, const float *bias, const float *gamma, const float *beta,
-                                uint16_t *Y, int64_t M, int N, float alpha, float eps, cudaStream_t stream) {
+                                uint16_t *Y, int64_t M, int N, float alpha, float eps, int rms, cudaStream_t stream) {
     int vpt = 4;
     while (vpt * kRowThreads < N) vpt *= 2;
     if (vpt > 64) return cudaErrorInvalidValue;
@@ -182,7 +185,7 @@ cudaError_t launch_row_epilogue(int op, const float *P, const float *bias, const
     if (!fn) return cudaErrorInvalidValue;
     const int64_t grid = M < 65536 ? M : 65536;
     void *args[] = {(void *)&P, (void *)&bias, (void *)&gamma, (void *)&beta, (void *)&Y, (void *)&M, (void *)&N,
-                    (void *)&alpha, (void *)&eps};
+                    (void *)&alpha, (void *)&eps, (void *)&rms};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
     cfg.blockDim = dim3(kRowThreads);

@@ -58,16 +58,16 @@ def bf16_bits(a_bf16_valued) -> np.ndarray:
 @dataclass(frozen=True)
 class GemmWorkload:
     name: str
-    kind: str              # "rownorm" | "softmax"
+    kind: str              # "rownorm" | "rmsnorm" | "softmax"
     M: int
     N: int
     K: int
     seed: int
     x_std: float
     w_std: float
-    bias_std: float = 0.0
+    bias_std: float | None = 0.0
     gamma_std: float = 0.0
-    beta_std: float = 0.0
+    beta_std: float | None = 0.0
     act: str = "none"      # "none" | "gelu_tanh"
     eps: float = 1e-5
     alpha: float = 1.0
@@ -84,6 +84,8 @@ class GemmWorkload:
         b = 2 * self.M * self.K + 2 * self.K * self.N + 2 * self.M * self.N
         if self.kind == "rownorm":
             b += 3 * 4 * self.N
+        elif self.kind == "rmsnorm":
+            b += (1 + (self.bias_std is not None) + (self.beta_std is not None)) * 4 * self.N
         return b
 
 
@@ -121,6 +123,10 @@ WORKLOADS = {
         "wide_ln_8192x16384x2048", "rownorm", 8192, 16384, 2048, 4, _c(2048), _c(2048),
         0.1, 0.1, 0.1, "none", 1e-5,
         description="wide-row GEMM+bias+LayerNorm, row wider than one cluster"),
+    "rms_16384x4096x4096": GemmWorkload(
+        "rms_16384x4096x4096", "rmsnorm", 16384, 4096, 4096, 5, _c(4096), _c(4096),
+        0.02, 0.02, None, "none", 1e-5,
+        description="GEMM+bias+RMSNorm (gamma, no beta), FFN-sized"),
     "stitch_750000x32": StitchWorkload(
         "stitch_750000x32", 750000, 32, 3,
         description="stitched y=A^3+b[row] -> row softmax, very many tiny rows"),
@@ -163,7 +169,7 @@ def workload_inputs(name: str) -> dict:
     w = WORKLOADS[name]
     if isinstance(w, StitchWorkload):
         return stitch_inputs(w.rows, w.cols, w.seed)
-    if w.kind == "rownorm":
+    if w.kind in ("rownorm", "rmsnorm"):
         return gemm_inputs(w.M, w.N, w.K, w.seed, x_std=w.x_std, w_std=w.w_std,
                            bias_std=w.bias_std, gamma_std=w.gamma_std,
                            beta_std=w.beta_std)
