@@ -41,6 +41,8 @@ Readings taken where the pages are silent:
   * RMSNorm divides each value by sqrt(mean of the squares + eps) with no mean
     subtraction (the usual definition, Zhang & Sennrich 2019); gamma scales
     after normalising and beta, when given, is added last.
+  * Residual add + norm: the residual R is added after the activation node
+    and before the reduction (the "add & norm" of a transformer block).
   * Softmax scale multiplies the accumulator before max/exp; an optional bias
     is added after scaling.  Exponent base e.
   * GELU is the tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
@@ -64,6 +66,7 @@ __all__ = [
     "softmax_rows",
     "gemm_bias_rownorm",
     "gemm_bias_rmsnorm",
+    "gemm_bias_residual_norm",
     "gemm_rowsoftmax",
     "stitch_rowreduce_broadcast",
     "ROW_CHUNK",
@@ -214,6 +217,38 @@ def gemm_bias_rmsnorm(X, W, bias, gamma, beta=None, *, alpha: float = 1.0,
         x = float(alpha) * gemm(X[idx], W) + b
         g = gelu_tanh(x) if act == "gelu_tanh" else x
         out[o:o + idx.size] = rmsnorm_rows(g, gamma, beta, eps)
+        o += idx.size
+    return out
+
+
+def gemm_bias_residual_norm(X, W, bias, R, gamma, beta, *, alpha: float = 1.0, eps: float = 1e-5,
+                            act: str = "none", norm: str = "layer", rows=None) -> np.ndarray:
+    """y = Norm(act(alpha * X.W + bias) + R) * gamma (+ beta), row by row.
+
+    sass2mlir, "Epilogue fusion - the core technique": activation, norm and
+    residual add run on the accumulator in the producer's epilogue.  The
+    residual R [M, N] is one more elementwise node before the reduction
+    (ComFuse, Stage-Stream Execution Model: stage-1 nodes, then the row
+    reduction).  norm is "layer" (LayerNorm) or "rms" (RMSNorm; beta may be
+    None there).
+    """
+    if act not in ("none", "gelu_tanh"):
+        raise ValueError(f"unknown activation {act!r}")
+    if norm not in ("layer", "rms"):
+        raise ValueError(f"unknown norm {norm!r}")
+    X = np.asarray(X)
+    R = np.asarray(R)
+    M = X.shape[0]
+    N = np.asarray(W).shape[1]
+    out_rows = M if rows is None else len(rows)
+    out = np.empty((out_rows, N), dtype=np.float64)
+    b = np.zeros(N) if bias is None else _f64(bias)
+    o = 0
+    for idx in _row_chunks(M, rows):
+        x = float(alpha) * gemm(X[idx], W) + b
+        g = (gelu_tanh(x) if act == "gelu_tanh" else x) + _f64(R[idx])
+        out[o:o + idx.size] = (layernorm_rows(g, gamma, beta, eps) if norm == "layer"
+                               else rmsnorm_rows(g, gamma, beta, eps))
         o += idx.size
     return out
 

@@ -230,6 +230,48 @@ def check_rmsnorm_composition(fused) -> list:
     return fails
 
 
+def check_residual_norm(fused) -> list:
+    """Residual add + norm: torch compositions in fp64; R = 0 is the plain call;
+    LayerNorm is invariant to a constant added to every column of a row, so a
+    per-row constant residual changes nothing; the residual enters after GELU."""
+    import torch
+    F = torch.nn.functional
+    import oracle
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(18))
+    M, K, N = 9, 24, 40
+    X = rng.standard_normal((M, K)) / 5
+    W = rng.standard_normal((K, N)) / 5
+    R = rng.standard_normal((M, N)) * 0.3
+    bias = rng.standard_normal(N) * 0.1
+    gam = 1 + rng.standard_normal(N) * 0.1
+    bet = rng.standard_normal(N) * 0.1
+    t = {k: torch.from_numpy(v) for k, v in dict(X=X, W=W, R=R, b=bias, g=gam, be=bet).items()}
+    for act in ("none", "gelu_tanh"):
+        for norm in ("layer", "rms"):
+            x = 0.5 * (t["X"] @ t["W"]) + t["b"]
+            if act == "gelu_tanh":
+                x = F.gelu(x, approximate="tanh")
+            g = x + t["R"]
+            ref = (F.layer_norm(g, (N,), t["g"], t["be"], 1e-5) if norm == "layer"
+                   else F.rms_norm(g, (N,), t["g"], 1e-5) + t["be"]).numpy()
+            y = np.asarray(fused(X, W, bias, R, gam, bet, alpha=0.5, eps=1e-5, act=act, norm=norm))
+            _fail(fails, y.shape == ref.shape and np.allclose(y, ref, rtol=1e-10, atol=1e-11),
+                  f"residual composition act={act} norm={norm}")
+    y0 = np.asarray(fused(X, W, bias, np.zeros((M, N)), gam, bet, eps=1e-5, act="gelu_tanh", norm="layer"))
+    y1 = oracle.gemm_bias_rownorm(X, W, bias, gam, bet, eps=1e-5, act="gelu_tanh")
+    _fail(fails, np.allclose(y0, y1, rtol=1e-13, atol=1e-14), "residual R=0 is the plain LayerNorm call")
+    shift = np.repeat(rng.standard_normal((M, 1)) * 5, N, axis=1)
+    y2 = np.asarray(fused(X, W, bias, shift, gam, bet, eps=0.0, act="none", norm="layer"))
+    y3 = np.asarray(fused(X, W, bias, np.zeros((M, N)), gam, bet, eps=0.0, act="none", norm="layer"))
+    _fail(fails, np.allclose(y2, y3, rtol=1e-9, atol=1e-10), "LayerNorm ignores a per-row constant residual")
+    rows = [8, 0, 3]
+    ys = np.asarray(fused(X, W, bias, R, gam, None, act="none", norm="rms", rows=rows))
+    yf = np.asarray(fused(X, W, bias, R, gam, None, act="none", norm="rms"))
+    _fail(fails, np.allclose(ys, yf[rows], rtol=1e-13, atol=1e-14), "residual rows= subset")
+    return fails
+
+
 # ----------------------------------------------------------------------------
 # Softmax
 # ----------------------------------------------------------------------------

@@ -197,6 +197,36 @@ def test_softmax_composition_mutant_caught(name):
     assert pins.check_softmax_composition(SOFTMAX_FUSED_MUTANTS[name]), name
 
 
+def _residual(X, W, bias, R, gamma, beta, *, alpha=1.0, eps=1e-5, act="none", norm="layer", rows=None,
+              mistake):
+    X = np.asarray(X, float)
+    R = np.asarray(R, float)
+    if rows is not None:
+        X, R = X[rows], R[rows]
+    x = alpha * (X @ np.asarray(W, float)) + (0 if bias is None else np.asarray(bias))
+    if mistake == "residual before GELU":
+        g = oracle.gelu_tanh(x + R) if act == "gelu_tanh" else x + R
+    elif mistake == "residual after norm":
+        g = oracle.gelu_tanh(x) if act == "gelu_tanh" else x
+        y = oracle.layernorm_rows(g, gamma, beta, eps) if norm == "layer" else oracle.rmsnorm_rows(g, gamma, beta, eps)
+        return y + R
+    elif mistake == "residual scaled by alpha":
+        g = alpha * R + (oracle.gelu_tanh(x) if act == "gelu_tanh" else x)
+    else:
+        g = (oracle.gelu_tanh(x) if act == "gelu_tanh" else x) + R.T[:R.shape[0], :R.shape[1]] if R.shape[0] == R.shape[1] else (oracle.gelu_tanh(x) if act == "gelu_tanh" else x) - R
+    return oracle.layernorm_rows(g, gamma, beta, eps) if norm == "layer" else oracle.rmsnorm_rows(g, gamma, beta, eps)
+
+
+RESIDUAL_MUTANTS = {k: (lambda kk: (lambda *a, **kw: _residual(*a, mistake=kk, **kw)))(k)
+                    for k in ("residual before GELU", "residual after norm", "residual scaled by alpha",
+                              "residual subtracted")}
+
+
+@pytest.mark.parametrize("name", sorted(RESIDUAL_MUTANTS))
+def test_residual_mutant_caught(name):
+    assert pins.check_residual_norm(RESIDUAL_MUTANTS[name]), name
+
+
 @pytest.mark.parametrize("name", sorted(STITCH_MUTANTS))
 def test_stitch_mutant_caught(name):
     with np.errstate(over="ignore", invalid="ignore"):

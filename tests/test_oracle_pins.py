@@ -38,6 +38,10 @@ def test_rmsnorm_composition_pinned():
     assert pins.check_rmsnorm_composition(oracle.gemm_bias_rmsnorm) == []
 
 
+def test_residual_norm_pinned():
+    assert pins.check_residual_norm(oracle.gemm_bias_residual_norm) == []
+
+
 def test_softmax_pinned():
     assert pins.check_softmax(oracle.softmax_rows) == []
 
