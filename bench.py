@@ -72,19 +72,27 @@ def kind_of(w):
     return 1 if w.act == "gelu_tanh" else 0
 
 
-def fused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None):
+def fused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None, R=None):
     """The public fused call of workload w."""
     if w.kind == "softmax":
         return cf.cf_gemm_fused_rowsoftmax(X, W, None, Y, w.M, w.N, w.K, w.scale, ws, wsb, stream)
     act = cf.CF_ACT_GELU_TANH if w.act == "gelu_tanh" else cf.CF_ACT_NONE
+    if w.resid_std is not None:
+        norm = cf.CF_NORM_RMS if w.kind == "rmsnorm" else cf.CF_NORM_LAYER
+        return cf.cf_gemm_fused_residual_norm(X, W, bias, R, gamma, beta, Y, w.M, w.N, w.K, w.alpha, w.eps, act,
+                                              norm, ws, wsb, stream)
     fn = cf.cf_gemm_fused_rmsnorm if w.kind == "rmsnorm" else cf.cf_gemm_fused_rownorm
     return fn(X, W, bias, gamma, beta, Y, w.M, w.N, w.K, w.alpha, w.eps, act, ws, wsb, stream)
 
 
-def unfused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None):
+def unfused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None, R=None):
     if w.kind == "softmax":
         return cf.cf_unfused_gemm_rowsoftmax(X, W, None, Y, w.M, w.N, w.K, w.scale, ws, wsb, stream)
     act = cf.CF_ACT_GELU_TANH if w.act == "gelu_tanh" else cf.CF_ACT_NONE
+    if w.resid_std is not None:
+        norm = cf.CF_NORM_RMS if w.kind == "rmsnorm" else cf.CF_NORM_LAYER
+        return cf.cf_unfused_gemm_residual_norm(X, W, bias, R, gamma, beta, Y, w.M, w.N, w.K, w.alpha, w.eps, act,
+                                                norm, ws, wsb, stream)
     fn = cf.cf_unfused_gemm_rmsnorm if w.kind == "rmsnorm" else cf.cf_unfused_gemm_rownorm
     return fn(X, W, bias, gamma, beta, Y, w.M, w.N, w.K, w.alpha, w.eps, act, ws, wsb, stream)
 
@@ -92,6 +100,10 @@ def unfused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None):
 def oracle_rows(oracle, w, d, rows):
     if w.kind == "softmax":
         return oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows)
+    if w.resid_std is not None:
+        return oracle.gemm_bias_residual_norm(d["X"], d["W"], d["bias"], d["R"], d["gamma"], d["beta"],
+                                              alpha=w.alpha, eps=w.eps, act=w.act,
+                                              norm="rms" if w.kind == "rmsnorm" else "layer", rows=rows)
     fn = oracle.gemm_bias_rmsnorm if w.kind == "rmsnorm" else oracle.gemm_bias_rownorm
     return fn(d["X"], d["W"], d["bias"], d["gamma"], d["beta"], alpha=w.alpha, eps=w.eps, act=w.act, rows=rows)
 
@@ -211,6 +223,7 @@ class FusedRunner:
                  "Y": torch.empty((w.M, w.N), dtype=bf, device=device)}
             for k in ("bias", "gamma", "beta"):
                 s[k] = torch.from_numpy(d[k]).to(device) if k in row_vectors(w) else None
+            s["R"] = torch.from_numpy(d["R"]).to(device, bf) if d.get("R") is not None else None
             self.sets.append(s)
         self.ws_bytes = cf.cf_gemm_fused_workspace_size(w.M, w.N, w.K)
         self.ws = cf.new_workspace(self.ws_bytes, device)
@@ -219,7 +232,7 @@ class FusedRunner:
         cf, w = self.cf, self.w
         s = self.sets[i % len(self.sets)]
         st = fused_call(cf, w, s["X"], s["W"], s["bias"], s["gamma"], s["beta"], s["Y"], self.ws, self.ws_bytes,
-                        stream)
+                        stream, R=s["R"])
         cf.check(st, "fused launch")
 
 
@@ -227,7 +240,8 @@ def _seeded_inputs(w, rank):
     seed = mdist.seed_for(w.seed, rank)
     if w.kind in ("rownorm", "rmsnorm"):
         return inputs.gemm_inputs(w.M, w.N, w.K, seed, x_std=w.x_std, w_std=w.w_std,
-                                  bias_std=w.bias_std, gamma_std=w.gamma_std, beta_std=w.beta_std)
+                                  bias_std=w.bias_std, gamma_std=w.gamma_std, beta_std=w.beta_std,
+                                  resid_std=w.resid_std)
     return inputs.gemm_inputs(w.M, w.N, w.K, seed, x_std=w.x_std, w_std=w.w_std,
                               bias_std=None, gamma_std=None, beta_std=None)
 
@@ -293,19 +307,23 @@ def time_e2e(torch, cf, w, steps, device):
     X = torch.empty_like(hX, device=device)
     W = torch.empty_like(hW, device=device)
     Y = torch.empty((w.M, w.N), dtype=bf, device=device)
-    extra = {"d_bias": None, "d_gamma": None, "d_beta": None}
+    extra = {"d_bias": None, "d_gamma": None, "d_beta": None, "d_R": None}
     for k in row_vectors(w):
         extra[k] = torch.from_numpy(d[k]).pin_memory()
         extra["d_" + k] = torch.empty_like(extra[k], device=device)
+    if d.get("R") is not None:
+        extra["R"] = torch.from_numpy(d["R"]).to(bf).pin_memory()
+        extra["d_R"] = torch.empty_like(extra["R"], device=device)
     wsb = cf.cf_gemm_fused_workspace_size(w.M, w.N, w.K)
     ws = cf.new_workspace(wsb, device)
 
     def step():
         X.copy_(hX, non_blocking=True)
         W.copy_(hW, non_blocking=True)
-        for k in row_vectors(w):
+        for k in row_vectors(w) + (("R",) if extra["d_R"] is not None else ()):
             extra["d_" + k].copy_(extra[k], non_blocking=True)
-        cf.check(fused_call(cf, w, X, W, extra["d_bias"], extra["d_gamma"], extra["d_beta"], Y, ws, wsb))
+        cf.check(fused_call(cf, w, X, W, extra["d_bias"], extra["d_gamma"], extra["d_beta"], Y, ws, wsb,
+                            R=extra["d_R"]))
         hY.copy_(Y, non_blocking=True)
 
     for _ in range(3):
@@ -319,7 +337,8 @@ def time_e2e(torch, cf, w, steps, device):
     e1.record()
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) / 1e3 / steps
-    h2d = hX.numel() * 2 + hW.numel() * 2 + 4 * w.N * len(row_vectors(w))
+    h2d = hX.numel() * 2 + hW.numel() * 2 + 4 * w.N * len(row_vectors(w)) + (
+        2 * w.M * w.N if extra["d_R"] is not None else 0)
     d2h = hY.numel() * 2
     return t, h2d, d2h
 
@@ -362,7 +381,8 @@ def unfused_time(torch, cf, runner, reps):
     class U:
         def launch(self, i, stream=None):
             s = runner.sets[i % len(runner.sets)]
-            st = unfused_call(cf, w, s["X"], s["W"], s["bias"], s["gamma"], s["beta"], s["Y"], ws, wsb, stream)
+            st = unfused_call(cf, w, s["X"], s["W"], s["bias"], s["gamma"], s["beta"], s["Y"], ws, wsb, stream,
+                              R=s["R"])
             cf.check(st, "unfused launch")
 
     t, n, _ = time_steps(torch, U(), reps, 3, lambda: None, graph_len=reps)
@@ -444,6 +464,8 @@ def run_ours(args):
     kernel = {2: "gemm_fused_kernel<SOFTMAX>", 1: "gemm_fused_kernel<GELU_LN>", 0: "gemm_fused_kernel<LN>"}[kind_of(w)]
     if w.kind == "rmsnorm":
         kernel += " (RMSNorm)"
+    if w.resid_std is not None:
+        kernel += " (residual)"
     if bound == "hbm":
         achieved = w.unavoidable_bytes / t1 / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",

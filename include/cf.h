@@ -307,6 +307,38 @@ CF_API cf_status cf_gemm_fused_rmsnorm_ex(const void *X, const void *W, const fl
                                           const cf_tuning *tuning);
 
 /* ------------------------------------------------------------------------ */
+/* Fused GEMM + bias (+ GELU) + residual + LayerNorm / RMSNorm               */
+/* ------------------------------------------------------------------------ */
+typedef enum { CF_NORM_LAYER = 0, CF_NORM_RMS = 1 } cf_norm;
+
+/* Y = Norm(act(alpha * X.W + bias) + R) * gamma (+ beta), Norm = LayerNorm or
+ * RMSNorm (`norm`) -- the "add & norm" of a transformer block.
+ *
+ * [sass2mlir] "Epilogue fusion - the core technique": activation, norm and
+ * residual add run on the accumulator in the GEMM's epilogue.  The residual is
+ * one more stage-1 node before the row reduction ([ComFuse] Stage-Stream
+ * Execution Model); each CTA reads its rows of R once, in pass 1.
+ *   R (device) bf16 [M, N] row-major, 16-byte aligned; it may be the same
+ *     buffer as Y (every element of R is read by the CTA that later writes
+ *     that element of Y, before writing it), but not X or W.
+ * Everything else as for cf_gemm_fused_rownorm (CF_NORM_LAYER) or
+ * cf_gemm_fused_rmsnorm (CF_NORM_RMS: beta may be NULL). */
+CF_API cf_status cf_gemm_fused_residual_norm(const void *X, const void *W, const float *bias,
+                                             const void *R, const float *gamma, const float *beta,
+                                             void *Y, int64_t M, int64_t N, int64_t K, float alpha,
+                                             float eps, cf_activation act, cf_norm norm,
+                                             void *workspace, size_t workspace_bytes,
+                                             cf_stream_t stream);
+
+CF_API cf_status cf_gemm_fused_residual_norm_ex(const void *X, const void *W, const float *bias,
+                                                const void *R, const float *gamma, const float *beta,
+                                                void *Y, int64_t M, int64_t N, int64_t K,
+                                                float alpha, float eps, cf_activation act,
+                                                cf_norm norm, void *workspace,
+                                                size_t workspace_bytes, cf_stream_t stream,
+                                                const cf_tuning *tuning);
+
+/* ------------------------------------------------------------------------ */
 /* Fused GEMM + scaled row softmax                                           */
 /* ------------------------------------------------------------------------ */
 /* Y = softmax_row(scale * X.W + bias)
@@ -374,6 +406,14 @@ CF_API cf_status cf_unfused_gemm_rmsnorm(const void *X, const void *W, const flo
                                          int64_t M, int64_t N, int64_t K, float alpha, float eps,
                                          cf_activation act, void *workspace,
                                          size_t workspace_bytes, cf_stream_t stream);
+
+/* The unfused composition of cf_gemm_fused_residual_norm. */
+CF_API cf_status cf_unfused_gemm_residual_norm(const void *X, const void *W, const float *bias,
+                                               const void *R, const float *gamma, const float *beta,
+                                               void *Y, int64_t M, int64_t N, int64_t K, float alpha,
+                                               float eps, cf_activation act, cf_norm norm,
+                                               void *workspace, size_t workspace_bytes,
+                                               cf_stream_t stream);
 
 CF_API cf_status cf_unfused_gemm_rowsoftmax(const void *X, const void *W, const float *bias,
                                             void *Y, int64_t M, int64_t N, int64_t K, float scale,

@@ -109,6 +109,10 @@ _SIGS = {
                                     _P, _SZ, _P]),
     "cf_gemm_fused_rmsnorm_ex": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
                                        _P, _SZ, _P, ctypes.POINTER(cf_tuning)]),
+    "cf_gemm_fused_residual_norm": (_ST, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
+                                          ctypes.c_int, _P, _SZ, _P]),
+    "cf_gemm_fused_residual_norm_ex": (_ST, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
+                                             ctypes.c_int, _P, _SZ, _P, ctypes.POINTER(cf_tuning)]),
     "cf_gemm_fused_rowsoftmax": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P]),
     "cf_gemm_fused_rowsoftmax_ex": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P,
                                           ctypes.POINTER(cf_tuning)]),
@@ -117,6 +121,8 @@ _SIGS = {
                                       _P, _SZ, _P]),
     "cf_unfused_gemm_rmsnorm": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
                                       _P, _SZ, _P]),
+    "cf_unfused_gemm_residual_norm": (_ST, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
+                                            ctypes.c_int, _P, _SZ, _P]),
     "cf_unfused_gemm_rowsoftmax": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P]),
     "cf_stitch_rowreduce_broadcast": (_ST, [_P, _P, _P, _I64, _I64, _P, _SZ, _P]),
     "cf_stitch_rowreduce_broadcast_ex": (_ST, [_P, _P, _P, _I64, _I64, _P, _SZ, _P,
@@ -251,6 +257,30 @@ def cf_gemm_fused_rmsnorm(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, 
     return L.cf_gemm_fused_rmsnorm_ex(_ptr(X), _ptr(W), _ptr(bias), _ptr(gamma), _ptr(beta), _ptr(Y),
                                       M, N, K, alpha, eps, act, _ptr(workspace), workspace_bytes,
                                       _stream(stream), _tun(tuning))
+
+
+CF_NORM_LAYER = 0
+CF_NORM_RMS = 1
+
+
+def cf_gemm_fused_residual_norm(X, W, bias, R, gamma, beta, Y, M, N, K, alpha, eps, act, norm, workspace,
+                                workspace_bytes, stream=None, tuning=None) -> int:
+    """Y = Norm(act(alpha*X.W + bias) + R) * gamma (+ beta); norm CF_NORM_LAYER or CF_NORM_RMS."""
+    L = lib()
+    if tuning is None:
+        return L.cf_gemm_fused_residual_norm(_ptr(X), _ptr(W), _ptr(bias), _ptr(R), _ptr(gamma), _ptr(beta),
+                                             _ptr(Y), M, N, K, alpha, eps, act, norm, _ptr(workspace),
+                                             workspace_bytes, _stream(stream))
+    return L.cf_gemm_fused_residual_norm_ex(_ptr(X), _ptr(W), _ptr(bias), _ptr(R), _ptr(gamma), _ptr(beta),
+                                            _ptr(Y), M, N, K, alpha, eps, act, norm, _ptr(workspace),
+                                            workspace_bytes, _stream(stream), _tun(tuning))
+
+
+def cf_unfused_gemm_residual_norm(X, W, bias, R, gamma, beta, Y, M, N, K, alpha, eps, act, norm, workspace,
+                                  workspace_bytes, stream=None) -> int:
+    return lib().cf_unfused_gemm_residual_norm(_ptr(X), _ptr(W), _ptr(bias), _ptr(R), _ptr(gamma), _ptr(beta),
+                                               _ptr(Y), M, N, K, alpha, eps, act, norm, _ptr(workspace),
+                                               workspace_bytes, _stream(stream))
 
 
 def cf_gemm_fused_rownorm_noalloc(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, stream=None) -> int:

@@ -470,13 +470,14 @@ cf_status cf_query_gemm_fused_plan(int64_t M, int64_t N, int64_t K, int32_t kind
 static cf_status gemm_fused_common(int kind, const void *X, const void *W, const float *bias, const float *gamma,
                                    const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha,
                                    float eps, void *ws, size_t ws_bytes, cf_stream_t stream,
-                                   const cf_tuning *tuning, int rms = 0) {
+                                   const cf_tuning *tuning, int rms = 0, const void *R = nullptr) {
     if (M < 0 || N <= 0 || K <= 0) return CF_ERR_INVALID_ARG;
     if (!X || !W || !Y || !ws) return CF_ERR_INVALID_ARG;
     if (kind != cf::EPI_SOFTMAX && (!gamma || (!beta && !rms))) return CF_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || (bias && !aligned16(bias)) ||
-        (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)))
+        (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)) || (R && !aligned16(R)))
         return CF_ERR_MISALIGNED;
+    if (R && (R == X || R == W)) return CF_ERR_INVALID_ARG;
     if (K % 64 != 0 || N % 64 != 0) return CF_ERR_UNSUPPORTED;
     if (ws_bytes < cf_gemm_fused_workspace_size(M, N, K)) return CF_ERR_WORKSPACE_TOO_SMALL;
     if (M == 0) return CF_OK;
@@ -528,6 +529,7 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
     a.row_blocks_alloc = a.super_blocks * plan.cluster_m;
     a.extra_arrivals = t.extra_arrivals;
     a.rms = rms;
+    a.resid = static_cast<const uint16_t *>(R);
     a.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
     a.trace = reinterpret_cast<unsigned long long *>(t.trace);
     a.multicast_x = (t.multicast_x && plan.cluster_m == 1 && plan.cluster_size > 1) ? 1 : 0;
@@ -573,6 +575,28 @@ cf_status cf_gemm_fused_rmsnorm(const void *X, const void *W, const float *bias,
                                 float eps, cf_activation act, void *ws, size_t ws_bytes, cf_stream_t stream) {
     return cf_gemm_fused_rmsnorm_ex(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, ws, ws_bytes, stream,
                                     nullptr);
+}
+
+cf_status cf_gemm_fused_residual_norm_ex(const void *X, const void *W, const float *bias, const void *R,
+                                         const float *gamma, const float *beta, void *Y, int64_t M, int64_t N,
+                                         int64_t K, float alpha, float eps, cf_activation act, cf_norm norm,
+                                         void *ws, size_t ws_bytes, cf_stream_t stream, const cf_tuning *tuning) {
+    int kind;
+    if (act == CF_ACT_NONE) kind = cf::EPI_LN;
+    else if (act == CF_ACT_GELU_TANH) kind = cf::EPI_GELU_LN;
+    else return CF_ERR_INVALID_ARG;
+    if (norm != CF_NORM_LAYER && norm != CF_NORM_RMS) return CF_ERR_INVALID_ARG;
+    if (!R) return CF_ERR_INVALID_ARG;
+    return gemm_fused_common(kind, X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, ws, ws_bytes, stream, tuning,
+                             norm == CF_NORM_RMS ? 1 : 0, R);
+}
+
+cf_status cf_gemm_fused_residual_norm(const void *X, const void *W, const float *bias, const void *R,
+                                      const float *gamma, const float *beta, void *Y, int64_t M, int64_t N,
+                                      int64_t K, float alpha, float eps, cf_activation act, cf_norm norm, void *ws,
+                                      size_t ws_bytes, cf_stream_t stream) {
+    return cf_gemm_fused_residual_norm_ex(X, W, bias, R, gamma, beta, Y, M, N, K, alpha, eps, act, norm, ws,
+                                          ws_bytes, stream, nullptr);
 }
 
 cf_status cf_gemm_fused_rowsoftmax_ex(const void *X, const void *W, const float *bias, void *Y, int64_t M,
@@ -753,12 +777,12 @@ cf_status gemm_store_f32(const void *X, const void *W, float *P, uint32_t *err, 
 
 cf_status unfused_common(int op, const void *X, const void *W, const float *bias, const float *gamma,
                          const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha, float eps,
-                         void *ws, size_t ws_bytes, cf_stream_t stream, int rms = 0) {
+                         void *ws, size_t ws_bytes, cf_stream_t stream, int rms = 0, const void *R = nullptr) {
     if (M < 0 || N <= 0 || K <= 0) return CF_ERR_INVALID_ARG;
     if (!X || !W || !Y || !ws) return CF_ERR_INVALID_ARG;
     if (op != 2 && (!gamma || (!beta && !rms))) return CF_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(ws) || (bias && !aligned16(bias)) ||
-        (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)))
+        (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)) || (R && !aligned16(R)))
         return CF_ERR_MISALIGNED;
     if (K % 64 != 0 || N % 64 != 0 || N > 256 * 64) return CF_ERR_UNSUPPORTED;
     if (ws_bytes < cf_unfused_workspace_size(M, N, K)) return CF_ERR_WORKSPACE_TOO_SMALL;
@@ -770,7 +794,7 @@ cf_status unfused_common(int op, const void *X, const void *W, const float *bias
     cf_status st = gemm_store_f32(X, W, P, err, M, N, K, s);
     if (st != CF_OK) return st;
     cudaError_t e = cf::launch_row_epilogue(op, P, bias, gamma, beta, static_cast<uint16_t *>(Y), M, int(N), alpha,
-                                            eps, rms, s);
+                                            eps, rms, static_cast<const uint16_t *>(R), s);
     return e == cudaSuccess ? CF_OK : cuda_fail(e);
 }
 
@@ -803,6 +827,20 @@ extern "C" cf_status cf_unfused_gemm_rmsnorm(const void *X, const void *W, const
     else return CF_ERR_INVALID_ARG;
     return unfused_common(op, X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, workspace, workspace_bytes, stream,
                           1);
+}
+
+extern "C" cf_status cf_unfused_gemm_residual_norm(const void *X, const void *W, const float *bias, const void *R,
+                                                   const float *gamma, const float *beta, void *Y, int64_t M,
+                                                   int64_t N, int64_t K, float alpha, float eps, cf_activation act,
+                                                   cf_norm norm, void *workspace, size_t workspace_bytes,
+                                                   cf_stream_t stream) {
+    int op;
+    if (act == CF_ACT_NONE) op = 0;
+    else if (act == CF_ACT_GELU_TANH) op = 1;
+    else return CF_ERR_INVALID_ARG;
+    if ((norm != CF_NORM_LAYER && norm != CF_NORM_RMS) || !R) return CF_ERR_INVALID_ARG;
+    return unfused_common(op, X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, workspace, workspace_bytes, stream,
+                          norm == CF_NORM_RMS ? 1 : 0, R);
 }
 
 extern "C" cf_status cf_unfused_gemm_rowsoftmax(const void *X, const void *W, const float *bias, void *Y, int64_t M,

@@ -53,7 +53,8 @@ int stitch_packed_blocks_per_sm(int lpr, bool vec);
 //   op 0 LN, 1 GELU+LN, 2 softmax over fp32 rows of P -> bf16 Y
 // --------------------------------------------------------------------------
 cudaError_t launch_row_epilogue(int op, const float *P, const float *bias, const float *gamma, const float *beta,
-                                uint16_t *Y, int64_t M, int N, float alpha, float eps, int rms, cudaStream_t stream);
+                                uint16_t *Y, int64_t M, int N, float alpha, float eps, int rms, const uint16_t *R,
+                                cudaStream_t stream);
 
 // --------------------------------------------------------------------------
 // fused GEMM kernels (gemm_fused.cu)
@@ -93,6 +94,7 @@ struct GemmArgs {
     int super_blocks;     // RB_alloc / C_M
     int extra_arrivals;   // test hook
     int rms;              // LN kinds: normalise by sqrt(mean(g^2) + eps), no centring (RMSNorm)
+    const uint16_t *resid;  // LN kinds: bf16 [M,N] residual added after the activation, or null
     unsigned long long timeout_ns;
     unsigned long long *trace;  // optional %globaltimer stamps, CF_TRACE_SLOTS per CTA
 };

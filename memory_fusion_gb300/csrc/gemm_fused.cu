@@ -3,7 +3,8 @@
 // many tiles and CTAs:
 //     LN:       y = LayerNorm(alpha*acc + bias) * gamma + beta
 //     GELU_LN:  y = LayerNorm(GELU_tanh(alpha*acc + bias)) * gamma + beta
-//               (with GemmArgs::rms, RMSNorm in place of LayerNorm for both)
+//               (with GemmArgs::rms, RMSNorm in place of LayerNorm for both; with
+//               GemmArgs::resid, a bf16 residual added after the activation)
 //     SOFTMAX:  y = softmax(scale*acc + bias)
 //
 // Design (GB300-first; the page mechanisms it realises are cited inline):
@@ -194,8 +195,10 @@ __device__ __forceinline__ void softmax_fragment(uint32_t (&v)[32], const float 
 
 // LayerNorm stage-1 nodes on one fragment: x = alpha*acc + bias (-> GELU);
 // the fragment is replaced by the stage-1 value; returns its (mean, M2).
+// (With a residual: `r` holds the fragment's 32 bf16 residual values of this
+// thread's row, added after the activation.)
 template <bool kGelu>
-__device__ __forceinline__ MeanM2 ln_fragment(uint32_t (&v)[32], const float *p, float alpha) {
+__device__ __forceinline__ MeanM2 ln_fragment(uint32_t (&v)[32], const float *p, float alpha, const uint4 *r) {
     float x[32];
 #pragma unroll
     for (int j4 = 0; j4 < 8; ++j4) {
@@ -208,6 +211,11 @@ __device__ __forceinline__ MeanM2 ln_fragment(uint32_t (&v)[32], const float *p,
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         if constexpr (kGelu) x[j] = gelu_tanh_dev(x[j]);
+        if (r != nullptr) {
+            const uint4 q = r[j >> 3];
+            const uint32_t w = ((j >> 1) & 3) == 0 ? q.x : ((j >> 1) & 3) == 1 ? q.y : ((j >> 1) & 3) == 2 ? q.z : q.w;
+            x[j] += __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));  // bf16 -> fp32
+        }
         v[j] = __float_as_uint(x[j]);
     }
     return chunk_mean_m2(x);
@@ -624,17 +632,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 part = make_float2(m, ssum);
             } else {
                 MeanM2 acc{0.f, 0.f};
+                // residual R [M, N] bf16: this thread's row slice of the fragment pair,
+                // read (streaming) before the TMEM loads so the two latencies overlap
+                const bool has_r = a.resid != nullptr;
+                const uint4 *rrow = has_r && (m0 + row) < a.M
+                                        ? reinterpret_cast<const uint4 *>(a.resid + size_t(m0 + row) * size_t(a.N) + ncta)
+                                        : nullptr;
 #pragma unroll
                 for (int c = 0; c < 8; c += 2) {
                     if (c < nchunks) {
                         uint32_t v0[32], v1[32];
+                        uint4 r[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) r[k] = rrow ? __ldcs(rrow + c * 4 + k) : make_uint4(0u, 0u, 0u, 0u);
                         ptx::tmem_ld32(tacc + c * 32, v0);
                         ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
                         ptx::tmem_ld_wait();
-                        const MeanM2 c0 = ln_fragment<EPI == EPI_GELU_LN>(v0, pb + c * 32, a.alpha);
+                        const MeanM2 c0 = ln_fragment<EPI == EPI_GELU_LN>(v0, pb + c * 32, a.alpha, has_r ? r : nullptr);
                         ptx::tmem_st32(tacc + c * 32, v0);
                         acc = (c == 0) ? c0 : combine_counts(acc, float(32 * c), c0, 32.f);
-                        const MeanM2 c1 = ln_fragment<EPI == EPI_GELU_LN>(v1, pb + (c + 1) * 32, a.alpha);
+                        const MeanM2 c1 = ln_fragment<EPI == EPI_GELU_LN>(v1, pb + (c + 1) * 32, a.alpha,
+                                                                          has_r ? r + 4 : nullptr);
                         ptx::tmem_st32(tacc + (c + 1) * 32, v1);
                         acc = combine_counts(acc, float(32 * (c + 1)), c1, 32.f);
                     }

@@ -5,7 +5,8 @@
 //     op 0 (LN):       y = LayerNorm(alpha*P + bias) * gamma + beta
 //     op 1 (GELU_LN):  y = LayerNorm(GELU_tanh(alpha*P + bias)) * gamma + beta
 //     op 2 (SOFTMAX):  y = softmax(alpha*P + bias)
-// (ops 0 and 1 with `rms`: RMSNorm, y = g / sqrt(mean(g^2) + eps) * gamma + beta)
+// (ops 0 and 1 with `rms`: RMSNorm, y = g / sqrt(mean(g^2) + eps) * gamma + beta;
+//  with a residual R [M,N] bf16, g = act(alpha*P + bias) + R)
 // This is the materialised-intermediate schedule the fusion removes ([ComFuse]
 // Stage-Stream Execution Model: an edge that would otherwise be a buffer in
 // GMEM); it exists so the cost of that buffer can be measured, not as a
@@ -48,7 +49,8 @@ __global__ void __launch_bounds__(kRowThreads) row_epilogue_kernel(const float *
                                                                    const float *__restrict__ gamma,
                                                                    const float *__restrict__ beta,
                                                                    uint16_t *__restrict__ Y, int64_t M, int N,
-                                                                   float alpha, float eps, int rms) {
+                                                                   float alpha, float eps, int rms,
+                                                                   const uint16_t *__restrict__ R) {
     constexpr int G4 = VPT / 4;  // float4 groups per thread; group j holds columns (j*256 + t)*4 ..
     __shared__ float4 red[kRowThreads / 32];
     __shared__ float2 fin;
@@ -112,6 +114,10 @@ __global__ void __launch_bounds__(kRowThreads) row_epilogue_kernel(const float *
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     if constexpr (OP == 1) x[4 * j + k] = gelu_tanh_row(x[4 * j + k]);
+                    if (R) {
+                        const uint32_t w = reinterpret_cast<const uint32_t *>(R + r * N + (j * kRowThreads + t) * 4)[k >> 1];
+                        x[4 * j + k] += __uint_as_float((k & 1) ? (w & 0xFFFF0000u) : (w << 16));
+                    }
                     s += x[4 * j + k];
                 }
                 const float mu = 0.25f * s;
@@ -177,7 +183,8 @@ void *row_fn(int vpt) {
 }  // namespace
 
 cudaError_t launch_row_epilogue(int op, const float *P, const float *bias, const float *gamma, const float *beta,
-                                uint16_t *Y, int64_t M, int N, float alpha, float eps, int rms, cudaStream_t stream) {
+                                uint16_t *Y, int64_t M, int N, float alpha, float eps, int rms, const uint16_t *R,
+                                cudaStream_t stream) {
     int vpt = 4;
     while (vpt * kRowThreads < N) vpt *= 2;
     if (vpt > 64) return cudaErrorInvalidValue;
@@ -185,7 +192,7 @@ cudaError_t launch_row_epilogue(int op, const float *P, const float *bias, const
     if (!fn) return cudaErrorInvalidValue;
     const int64_t grid = M < 65536 ? M : 65536;
     void *args[] = {(void *)&P, (void *)&bias, (void *)&gamma, (void *)&beta, (void *)&Y, (void *)&M, (void *)&N,
-                    (void *)&alpha, (void *)&eps, (void *)&rms};
+                    (void *)&alpha, (void *)&eps, (void *)&rms, (void *)&R};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
     cfg.blockDim = dim3(kRowThreads);

@@ -70,6 +70,7 @@ class GemmWorkload:
     beta_std: float | None = 0.0
     act: str = "none"      # "none" | "gelu_tanh"
     eps: float = 1e-5
+    resid_std: float | None = None  # a bf16 residual R [M, N] added before the norm
     alpha: float = 1.0
     scale: float = 1.0
     description: str = ""
@@ -86,6 +87,8 @@ class GemmWorkload:
             b += 3 * 4 * self.N
         elif self.kind == "rmsnorm":
             b += (1 + (self.bias_std is not None) + (self.beta_std is not None)) * 4 * self.N
+        if self.resid_std is not None:
+            b += 2 * self.M * self.N
         return b
 
 
@@ -127,6 +130,10 @@ WORKLOADS = {
         "rms_16384x4096x4096", "rmsnorm", 16384, 4096, 4096, 5, _c(4096), _c(4096),
         0.02, 0.02, None, "none", 1e-5,
         description="GEMM+bias+RMSNorm (gamma, no beta), FFN-sized"),
+    "residual_ln_16384x4096x4096": GemmWorkload(
+        "residual_ln_16384x4096x4096", "rownorm", 16384, 4096, 4096, 6, _c(4096), _c(4096),
+        0.02, 0.02, 0.02, "none", 1e-5, resid_std=0.02,
+        description="GEMM+bias+residual+LayerNorm (add & norm), FFN-sized"),
     "stitch_750000x32": StitchWorkload(
         "stitch_750000x32", 750000, 32, 3,
         description="stitched y=A^3+b[row] -> row softmax, very many tiny rows"),
@@ -142,7 +149,8 @@ def _normal(rng, shape, std, mean=0.0):
 
 def gemm_inputs(M: int, N: int, K: int, seed: int, *, x_std: float = 1.0,
                 w_std: float = 1.0, bias_std: float | None = 0.1,
-                gamma_std: float | None = 0.1, beta_std: float | None = 0.1) -> dict:
+                gamma_std: float | None = 0.1, beta_std: float | None = 0.1,
+                resid_std: float | None = None) -> dict:
     """X, W (bf16-valued float32) and the row-vector parameters (float32).
 
     A ``None`` std skips that draw (the key is then None).
@@ -154,6 +162,8 @@ def gemm_inputs(M: int, N: int, K: int, seed: int, *, x_std: float = 1.0,
     out["bias"] = None if bias_std is None else _normal(rng, (N,), bias_std)
     out["gamma"] = None if gamma_std is None else _normal(rng, (N,), gamma_std, 1.0)
     out["beta"] = None if beta_std is None else _normal(rng, (N,), beta_std)
+    # drawn last, so the other draws of a seed do not depend on it
+    out["R"] = None if resid_std is None else round_to_bf16(_normal(rng, (M, N), resid_std))
     return out
 
 
@@ -172,6 +182,6 @@ def workload_inputs(name: str) -> dict:
     if w.kind in ("rownorm", "rmsnorm"):
         return gemm_inputs(w.M, w.N, w.K, w.seed, x_std=w.x_std, w_std=w.w_std,
                            bias_std=w.bias_std, gamma_std=w.gamma_std,
-                           beta_std=w.beta_std)
+                           beta_std=w.beta_std, resid_std=w.resid_std)
     return gemm_inputs(w.M, w.N, w.K, w.seed, x_std=w.x_std, w_std=w.w_std,
                        bias_std=None, gamma_std=None, beta_std=None)
