@@ -43,6 +43,9 @@ Readings taken where the pages are silent:
     after normalising and beta, when given, is added last.
   * Residual add + norm: the residual R is added after the activation node
     and before the reduction (the "add & norm" of a transformer block).
+  * Masked softmax: a causal mask keeps element (i, j) of the scaled scores
+    iff j <= i + offset (masked elements are -inf before the softmax); a row
+    with no kept element is all zeros.
   * Softmax scale multiplies the accumulator before max/exp; an optional bias
     is added after scaling.  Exponent base e.
   * GELU is the tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
@@ -67,6 +70,7 @@ __all__ = [
     "gemm_bias_rownorm",
     "gemm_bias_rmsnorm",
     "gemm_bias_residual_norm",
+    "gemm_rowsoftmax_causal",
     "gemm_rowsoftmax",
     "stitch_rowreduce_broadcast",
     "ROW_CHUNK",
@@ -266,6 +270,32 @@ def gemm_rowsoftmax(X, W, *, scale: float, bias=None, rows=None) -> np.ndarray:
         if bias is not None:
             z = z + _f64(bias)
         out[o:o + idx.size] = softmax_rows(z)
+        o += idx.size
+    return out
+
+
+def gemm_rowsoftmax_causal(X, W, *, scale: float, offset: int, bias=None, rows=None) -> np.ndarray:
+    """y = softmax(mask(scale * X.W (+ bias))) over each row, where the mask
+    keeps column j of row i iff j <= i + offset; a fully masked row is 0.
+
+    A masked reduction node ahead of Softmax's nested stage DAG (ComFuse,
+    Fusion Spec IR): masked elements take no part in the max or the sum and
+    are 0 in the output.
+    """
+    X = np.asarray(X)
+    M = X.shape[0]
+    N = np.asarray(W).shape[1]
+    idx_all = np.arange(M) if rows is None else np.asarray(rows)
+    out = np.zeros((idx_all.size, N), dtype=np.float64)
+    o = 0
+    for idx in _row_chunks(M, rows):
+        z = float(scale) * gemm(X[idx], W)
+        if bias is not None:
+            z = z + _f64(bias)
+        keep = np.arange(N)[None, :] <= (idx[:, None] + int(offset))
+        for r in range(idx.size):
+            if keep[r].any():
+                out[o + r, keep[r]] = softmax_rows(z[r, keep[r]][None, :])[0]
         o += idx.size
     return out
 

@@ -370,6 +370,46 @@ def check_softmax_composition(fused) -> list:
     return fails
 
 
+def check_softmax_causal(fused) -> list:
+    """Causal softmax: torch's softmax over masked_fill(-inf) in fp64; an offset at
+    least N - 1 is the unmasked call; masked entries are exactly 0 and kept rows
+    sum to 1; a fully masked row is 0; a row keeping one element puts 1 there."""
+    import torch
+    import oracle
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(19))
+    M, K, N = 12, 16, 20
+    X = rng.standard_normal((M, K))
+    W = rng.standard_normal((K, N)) / 4
+    bias = rng.standard_normal(N)
+    for off in (0, 3, -2):
+        for b in (None, bias):
+            z = 0.7 * (torch.from_numpy(X) @ torch.from_numpy(W))
+            if b is not None:
+                z = z + torch.from_numpy(b)
+            keep = torch.arange(N)[None, :] <= (torch.arange(M)[:, None] + off)
+            ref = torch.softmax(z.masked_fill(~keep, float("-inf")), dim=1)
+            ref = torch.nan_to_num(ref, nan=0.0).numpy()
+            y = np.asarray(fused(X, W, scale=0.7, offset=off, bias=b))
+            _fail(fails, y.shape == ref.shape and np.allclose(y, ref, rtol=1e-12, atol=1e-16),
+                  f"causal softmax offset={off} bias={'yes' if b is not None else 'no'}")
+            k = keep.numpy()
+            _fail(fails, np.all(y[~k] == 0.0), f"causal masked entries are 0 (offset {off})")
+            live = k.any(axis=1)
+            _fail(fails, np.allclose(y[live].sum(1), 1.0, rtol=0, atol=1e-12), f"causal kept rows sum to 1 ({off})")
+            _fail(fails, np.all(y[~live] == 0.0), f"causal fully masked rows are 0 ({off})")
+    y = np.asarray(fused(X, W, scale=0.7, offset=N - 1))
+    _fail(fails, np.allclose(y, oracle.gemm_rowsoftmax(X, W, scale=0.7), rtol=1e-13, atol=1e-16),
+          "causal offset N-1 is the unmasked softmax")
+    y = np.asarray(fused(X, W, scale=0.7, offset=-5))
+    _fail(fails, y[5, 0] == 1.0 and np.all(y[5, 1:] == 0.0) and np.all(y[:5] == 0.0), "causal one kept element")
+    rows = [11, 0, 4]
+    ys = np.asarray(fused(X, W, scale=0.7, offset=1, rows=rows))
+    yf = np.asarray(fused(X, W, scale=0.7, offset=1))[rows]
+    _fail(fails, np.allclose(ys, yf, rtol=1e-13, atol=1e-18), "causal rows= subset")
+    return fails
+
+
 def check_stitch(st) -> list:
     fails = []
     rng = np.random.Generator(np.random.PCG64(16))

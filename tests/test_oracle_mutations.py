@@ -227,6 +227,37 @@ def test_residual_mutant_caught(name):
     assert pins.check_residual_norm(RESIDUAL_MUTANTS[name]), name
 
 
+def _causal(X, W, *, scale, offset, bias=None, rows=None, mistake):
+    X = np.asarray(X, float)
+    M = X.shape[0]
+    idx = np.arange(M) if rows is None else np.asarray(rows)
+    z = scale * (X[idx] @ np.asarray(W, float)) + (0 if bias is None else np.asarray(bias))
+    N = z.shape[1]
+    if mistake == "strict inequality":
+        keep = np.arange(N)[None, :] < idx[:, None] + offset
+    elif mistake == "mask transposed":
+        keep = np.arange(N)[None, :] >= idx[:, None] - offset
+    else:
+        keep = np.arange(N)[None, :] <= idx[:, None] + offset
+    if mistake == "masked entries keep exp":
+        e = np.exp(z - np.where(keep, z, -np.inf).max(1, keepdims=True).clip(-1e300))
+        y = e / np.where(keep, e, 0).sum(1, keepdims=True)
+        return np.nan_to_num(y)
+    e = np.where(keep, np.exp(z - np.where(keep, z, -np.inf).max(1, keepdims=True).clip(-1e300)), 0.0)
+    s = e.sum(1, keepdims=True)
+    return np.divide(e, s, out=np.zeros_like(e), where=s > 0)
+
+
+CAUSAL_MUTANTS = {k: (lambda kk: (lambda *a, **kw: _causal(*a, mistake=kk, **kw)))(k)
+                  for k in ("strict inequality", "mask transposed", "masked entries keep exp")}
+
+
+@pytest.mark.parametrize("name", sorted(CAUSAL_MUTANTS))
+def test_causal_mutant_caught(name):
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        assert pins.check_softmax_causal(CAUSAL_MUTANTS[name]), name
+
+
 @pytest.mark.parametrize("name", sorted(STITCH_MUTANTS))
 def test_stitch_mutant_caught(name):
     with np.errstate(over="ignore", invalid="ignore"):

@@ -54,6 +54,10 @@ def test_softmax_composition_pinned():
     assert pins.check_softmax_composition(oracle.gemm_rowsoftmax) == []
 
 
+def test_softmax_causal_pinned():
+    assert pins.check_softmax_causal(oracle.gemm_rowsoftmax_causal) == []
+
+
 def test_stitch_pinned():
     assert pins.check_stitch(oracle.stitch_rowreduce_broadcast) == []
 
