@@ -66,23 +66,27 @@ def dist_env():
 
 
 def kind_of(w):
-    """Kernel kind of a GEMM workload (RMSNorm runs in the LayerNorm kernels)."""
-    if w.kind == "softmax":
+    """Kernel kind of a GEMM workload for the plan query (RMSNorm runs in the
+    LayerNorm kernels, the causal softmax plans like the plain one)."""
+    if w.kind in ("softmax", "softmax_causal"):
         return 2
     return 1 if w.act == "gelu_tanh" else 0
 
 
-def fused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None, R=None):
-    """The public fused call of workload w."""
+def fused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None, R=None, tuning=None):
+    """The public fused call of workload w (tuning: optional cf_tuning)."""
     if w.kind == "softmax":
-        return cf.cf_gemm_fused_rowsoftmax(X, W, None, Y, w.M, w.N, w.K, w.scale, ws, wsb, stream)
+        return cf.cf_gemm_fused_rowsoftmax(X, W, None, Y, w.M, w.N, w.K, w.scale, ws, wsb, stream, tuning)
+    if w.kind == "softmax_causal":
+        return cf.cf_gemm_fused_rowsoftmax_causal(X, W, None, Y, w.M, w.N, w.K, w.scale, w.mask_offset, ws, wsb,
+                                                  stream, tuning)
     act = cf.CF_ACT_GELU_TANH if w.act == "gelu_tanh" else cf.CF_ACT_NONE
     if w.resid_std is not None:
         norm = cf.CF_NORM_RMS if w.kind == "rmsnorm" else cf.CF_NORM_LAYER
         return cf.cf_gemm_fused_residual_norm(X, W, bias, R, gamma, beta, Y, w.M, w.N, w.K, w.alpha, w.eps, act,
-                                              norm, ws, wsb, stream)
+                                              norm, ws, wsb, stream, tuning)
     fn = cf.cf_gemm_fused_rmsnorm if w.kind == "rmsnorm" else cf.cf_gemm_fused_rownorm
-    return fn(X, W, bias, gamma, beta, Y, w.M, w.N, w.K, w.alpha, w.eps, act, ws, wsb, stream)
+    return fn(X, W, bias, gamma, beta, Y, w.M, w.N, w.K, w.alpha, w.eps, act, ws, wsb, stream, tuning)
 
 
 def unfused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None, R=None):
@@ -100,6 +104,8 @@ def unfused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None, R=None
 def oracle_rows(oracle, w, d, rows):
     if w.kind == "softmax":
         return oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows)
+    if w.kind == "softmax_causal":
+        return oracle.gemm_rowsoftmax_causal(d["X"], d["W"], scale=w.scale, offset=w.mask_offset, rows=rows)
     if w.resid_std is not None:
         return oracle.gemm_bias_residual_norm(d["X"], d["W"], d["bias"], d["R"], d["gamma"], d["beta"],
                                               alpha=w.alpha, eps=w.eps, act=w.act,
@@ -110,7 +116,7 @@ def oracle_rows(oracle, w, d, rows):
 
 def row_vectors(w):
     """The fp32 [N] inputs of a workload's epilogue that are present."""
-    if w.kind == "softmax":
+    if w.kind in ("softmax", "softmax_causal"):
         return ()
     return tuple(k for k, sd in (("bias", w.bias_std), ("gamma", w.gamma_std), ("beta", w.beta_std))
                  if sd is not None)
@@ -360,11 +366,13 @@ def per_workload(torch, cf, peaks, device, names):
         t1 = t / n
         troof, bound = roofline_time_s(w, peaks)
         _, plan, _ = cf.cf_query_gemm_fused_plan(w.M, w.N, w.K, kind_of(w))
-        tu = unfused_time(torch, cf, r, reps)
+        # the unfused composition exists for the unmasked epilogues only
+        tu = unfused_time(torch, cf, r, reps) if w.kind != "softmax_causal" else None
         out[name] = {"us": round(t1 * 1e6, 2), "tflops": round(w.flops / t1 / 1e12, 1),
                      "gbs": round(w.unavoidable_bytes / t1 / 1e9, 1), "bound": bound,
                      "roofline_frac": round(troof / t1, 3), "buffer_sets": nsets,
-                     "unfused_us": round(tu * 1e6, 2), "fused_speedup": round(tu / t1, 2),
+                     "unfused_us": round(tu * 1e6, 2) if tu else None,
+                     "fused_speedup": round(tu / t1, 2) if tu else None,
                      "plan": plan.as_dict()}
         del r
         torch.cuda.empty_cache()
@@ -462,6 +470,8 @@ def run_ours(args):
     value = mdist.job_throughput(w.flops * n, ws_, t) / 1e12
     troof, bound = roofline_time_s(w, peaks)
     kernel = {2: "gemm_fused_kernel<SOFTMAX>", 1: "gemm_fused_kernel<GELU_LN>", 0: "gemm_fused_kernel<LN>"}[kind_of(w)]
+    if w.kind == "softmax_causal":
+        kernel = "gemm_fused_kernel<SOFTMAX_MASK>"
     if w.kind == "rmsnorm":
         kernel += " (RMSNorm)"
     if w.resid_std is not None:

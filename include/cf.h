@@ -357,6 +357,24 @@ CF_API cf_status cf_gemm_fused_rowsoftmax_ex(const void *X, const void *W, const
                                       float scale, void *workspace, size_t workspace_bytes,
                                       cf_stream_t stream, const cf_tuning *tuning);
 
+/* Y = softmax_row(mask(scale * X.W + bias)): the causally masked variant.
+ * Column j of row i is kept iff j <= i + offset; masked entries take no part
+ * in the row max or sum and are 0 in Y; a row with no kept column is all 0.
+ * The pages name the softmax pattern but print no mask: this is the causal
+ * mask of attention scores (offset 0 for a square score matrix).  Arguments
+ * otherwise as for cf_gemm_fused_rowsoftmax; any offset is accepted. */
+CF_API cf_status cf_gemm_fused_rowsoftmax_causal(const void *X, const void *W, const float *bias,
+                                                 void *Y, int64_t M, int64_t N, int64_t K,
+                                                 float scale, int64_t offset, void *workspace,
+                                                 size_t workspace_bytes, cf_stream_t stream);
+
+CF_API cf_status cf_gemm_fused_rowsoftmax_causal_ex(const void *X, const void *W,
+                                                    const float *bias, void *Y, int64_t M,
+                                                    int64_t N, int64_t K, float scale,
+                                                    int64_t offset, void *workspace,
+                                                    size_t workspace_bytes, cf_stream_t stream,
+                                                    const cf_tuning *tuning);
+
 /* ------------------------------------------------------------------------ */
 /* Stitched reduce -> broadcast subgraph (no GEMM)                           */
 /* ------------------------------------------------------------------------ */

@@ -113,6 +113,9 @@ _SIGS = {
                                           ctypes.c_int, _P, _SZ, _P]),
     "cf_gemm_fused_residual_norm_ex": (_ST, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
                                              ctypes.c_int, _P, _SZ, _P, ctypes.POINTER(cf_tuning)]),
+    "cf_gemm_fused_rowsoftmax_causal": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _I64, _P, _SZ, _P]),
+    "cf_gemm_fused_rowsoftmax_causal_ex": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _I64, _P, _SZ, _P,
+                                                 ctypes.POINTER(cf_tuning)]),
     "cf_gemm_fused_rowsoftmax": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P]),
     "cf_gemm_fused_rowsoftmax_ex": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P,
                                           ctypes.POINTER(cf_tuning)]),
@@ -321,6 +324,17 @@ def cf_unfused_gemm_rownorm(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act
     return lib().cf_unfused_gemm_rownorm(_ptr(X), _ptr(W), _ptr(bias), _ptr(gamma), _ptr(beta), _ptr(Y),
                                          M, N, K, alpha, eps, act, _ptr(workspace), workspace_bytes,
                                          _stream(stream))
+
+
+def cf_gemm_fused_rowsoftmax_causal(X, W, bias, Y, M, N, K, scale, offset, workspace, workspace_bytes,
+                                    stream=None, tuning=None) -> int:
+    """Y = softmax over each row of scale*X.W + bias keeping column j of row i iff j <= i + offset."""
+    L = lib()
+    if tuning is None:
+        return L.cf_gemm_fused_rowsoftmax_causal(_ptr(X), _ptr(W), _ptr(bias), _ptr(Y), M, N, K, scale, offset,
+                                                 _ptr(workspace), workspace_bytes, _stream(stream))
+    return L.cf_gemm_fused_rowsoftmax_causal_ex(_ptr(X), _ptr(W), _ptr(bias), _ptr(Y), M, N, K, scale, offset,
+                                                _ptr(workspace), workspace_bytes, _stream(stream), _tun(tuning))
 
 
 def cf_unfused_gemm_rmsnorm(X, W, bias, gamma, beta, Y, M, N, K, alpha, eps, act, workspace, workspace_bytes,

@@ -227,6 +227,8 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
     //   epilogue  ~ 4.5 us; + 1.5 + 0.2 G us when the row spans G > 1 clusters
     //               (the global barrier waits for the slowest of G clusters);
     //               + 0.5 us for a CTA pair when K < 512
+    //               + 0.05 C_N us for the cluster exchange (peer all-to-all), or
+    //               1 us when it goes through a leader (two hops)
     //   skew      ~ 0.05 G us per tile when G > 1
     // Rows wider than one row group need all G clusters of a row block
     // resident (ncl >= G); a wide tile's row never leaves its cluster (G = 1).
@@ -245,7 +247,9 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
         if (T < n) n = int(T);
         const int64_t per = (T + n - 1) / n;
         const double t_main = nk * (cm == 2 ? 0.35 : 0.50) * (ns / 256.0);
-        const double t_epi = 4.5 + (g > 1 ? 1.5 + 0.2 * g : 0.0) + (cm == 2 && nk < 8 ? 0.5 : 0.0);
+        const int pm = t.peer_max == 0 ? 8 : t.peer_max;
+        const double t_x = (pm < 0 || cn > pm) ? 1.0 : 0.05 * cn;
+        const double t_epi = 4.5 + t_x + (g > 1 ? 1.5 + 0.2 * g : 0.0) + (cm == 2 && nk < 8 ? 0.5 : 0.0);
         *ncl_out = n;
         if (wide) return double(per) * (t_main + t_epi);
         return double((per + 1) / 2) * std::max(2.0 * t_main, t_epi) + t_main + (g > 1 ? per * 0.05 * g : 0.0);
@@ -470,10 +474,12 @@ cf_status cf_query_gemm_fused_plan(int64_t M, int64_t N, int64_t K, int32_t kind
 static cf_status gemm_fused_common(int kind, const void *X, const void *W, const float *bias, const float *gamma,
                                    const float *beta, void *Y, int64_t M, int64_t N, int64_t K, float alpha,
                                    float eps, void *ws, size_t ws_bytes, cf_stream_t stream,
-                                   const cf_tuning *tuning, int rms = 0, const void *R = nullptr) {
+                                   const cf_tuning *tuning, int rms = 0, const void *R = nullptr,
+                                   long long mask_offset = 0) {
     if (M < 0 || N <= 0 || K <= 0) return CF_ERR_INVALID_ARG;
     if (!X || !W || !Y || !ws) return CF_ERR_INVALID_ARG;
-    if (kind != cf::EPI_SOFTMAX && (!gamma || (!beta && !rms))) return CF_ERR_INVALID_ARG;
+    const bool sm = kind == cf::EPI_SOFTMAX || kind == cf::EPI_SOFTMAX_MASK;
+    if (!sm && (!gamma || (!beta && !rms))) return CF_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || (bias && !aligned16(bias)) ||
         (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)) || (R && !aligned16(R)))
         return CF_ERR_MISALIGNED;
@@ -530,6 +536,7 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
     a.extra_arrivals = t.extra_arrivals;
     a.rms = rms;
     a.resid = static_cast<const uint16_t *>(R);
+    a.mask_offset = mask_offset;
     a.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
     a.trace = reinterpret_cast<unsigned long long *>(t.trace);
     a.multicast_x = (t.multicast_x && plan.cluster_m == 1 && plan.cluster_size > 1) ? 1 : 0;
@@ -604,6 +611,20 @@ cf_status cf_gemm_fused_rowsoftmax_ex(const void *X, const void *W, const float 
                                       cf_stream_t stream, const cf_tuning *tuning) {
     return gemm_fused_common(cf::EPI_SOFTMAX, X, W, bias, nullptr, nullptr, Y, M, N, K, scale, 0.f, ws, ws_bytes,
                              stream, tuning);
+}
+
+cf_status cf_gemm_fused_rowsoftmax_causal_ex(const void *X, const void *W, const float *bias, void *Y, int64_t M,
+                                             int64_t N, int64_t K, float scale, int64_t offset, void *ws,
+                                             size_t ws_bytes, cf_stream_t stream, const cf_tuning *tuning) {
+    return gemm_fused_common(cf::EPI_SOFTMAX_MASK, X, W, bias, nullptr, nullptr, Y, M, N, K, scale, 0.f, ws,
+                             ws_bytes, stream, tuning, 0, nullptr, (long long)offset);
+}
+
+cf_status cf_gemm_fused_rowsoftmax_causal(const void *X, const void *W, const float *bias, void *Y, int64_t M,
+                                          int64_t N, int64_t K, float scale, int64_t offset, void *ws,
+                                          size_t ws_bytes, cf_stream_t stream) {
+    return cf_gemm_fused_rowsoftmax_causal_ex(X, W, bias, Y, M, N, K, scale, offset, ws, ws_bytes, stream,
+                                              nullptr);
 }
 
 cf_status cf_gemm_fused_rowsoftmax(const void *X, const void *W, const float *bias, void *Y, int64_t M, int64_t N,

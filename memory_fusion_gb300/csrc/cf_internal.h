@@ -64,6 +64,7 @@ enum EpiKind : int {
     EPI_GELU_LN = 1,   // alpha*acc + bias -> GELU(tanh) -> LayerNorm -> bf16
     EPI_SOFTMAX = 2,   // scale*acc + bias -> softmax -> bf16
     EPI_STORE_F32 = 3, // raw fp32 accumulator to P [M,N] (the unfused baseline's GEMM)
+    EPI_SOFTMAX_MASK = 4,  // EPI_SOFTMAX over the causally masked row (keep col <= row + offset)
 };
 
 struct GemmArgs {
@@ -95,6 +96,7 @@ struct GemmArgs {
     int extra_arrivals;   // test hook
     int rms;              // LN kinds: normalise by sqrt(mean(g^2) + eps), no centring (RMSNorm)
     const uint16_t *resid;  // LN kinds: bf16 [M,N] residual added after the activation, or null
+    long long mask_offset;  // EPI_SOFTMAX_MASK: column j of row i is kept iff j <= i + mask_offset
     unsigned long long timeout_ns;
     unsigned long long *trace;  // optional %globaltimer stamps, CF_TRACE_SLOTS per CTA
 };

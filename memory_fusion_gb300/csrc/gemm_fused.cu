@@ -5,7 +5,8 @@
 //     GELU_LN:  y = LayerNorm(GELU_tanh(alpha*acc + bias)) * gamma + beta
 //               (with GemmArgs::rms, RMSNorm in place of LayerNorm for both; with
 //               GemmArgs::resid, a bf16 residual added after the activation)
-//     SOFTMAX:  y = softmax(scale*acc + bias)
+//     SOFTMAX:  y = softmax(scale*acc + bias)   (SOFTMAX_MASK: over the causally
+//               masked row, keeping column j of row i iff j <= i + offset)
 //
 // Design (GB300-first; the page mechanisms it realises are cited inline):
 //  * Tiles are 128 rows x n_slice columns (n_slice <= 256; or 512, a wide
@@ -165,9 +166,12 @@ __device__ __forceinline__ float gelu_tanh_dev(float x) {
 
 // Softmax stage-1 nodes on one 32-column fragment: z = alpha*acc + bias;
 // online (max, sum exp) update; the fragment is replaced by exp(z - m) where m
-// is the running max after this fragment.
+// is the running max after this fragment.  kMask: only the first `nvalid`
+// columns take part (the rest are -inf, exp 0); a thread with no kept column
+// so far keeps (m, s) = (-inf, 0).
+template <bool kMask>
 __device__ __forceinline__ void softmax_fragment(uint32_t (&v)[32], const float *p, float alpha, float &m,
-                                                 float &ssum) {
+                                                 float &ssum, int nvalid = 32) {
     float z[32];
     float cm = neg_inf();
 #pragma unroll
@@ -178,14 +182,24 @@ __device__ __forceinline__ void softmax_fragment(uint32_t (&v)[32], const float 
         z[4 * j4 + 2] = fmaf(alpha, __uint_as_float(v[4 * j4 + 2]), b.z);
         z[4 * j4 + 3] = fmaf(alpha, __uint_as_float(v[4 * j4 + 3]), b.w);
     }
+    if constexpr (kMask) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j >= nvalid) z[j] = neg_inf();
+    }
 #pragma unroll
     for (int j = 0; j < 32; ++j) cm = fmaxf(cm, z[j]);
     const float mn = fmaxf(m, cm);
+    if (kMask && mn == neg_inf()) {  // nothing kept yet in this row slice
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0u;
+        return;
+    }
     float s = ssum * ptx::ex2_approx((m - mn) * kLog2e);  // m = -inf on the first fragment: s stays 0
     const float off = mn * kLog2e;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-        const float ex = ptx::ex2_approx(fmaf(z[j], kLog2e, -off));
+        const float ex = ptx::ex2_approx(fmaf(z[j], kLog2e, -off));  // masked: exp(-inf) = 0
         s += ex;
         v[j] = __float_as_uint(ex);
     }
@@ -274,6 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
         return;
     }
 
+    constexpr bool kMask = EPI == EPI_SOFTMAX_MASK;        // causally masked softmax
+    constexpr bool kSm = EPI == EPI_SOFTMAX || kMask;       // a softmax epilogue
     const int C = a.cluster;                // C_N: CTAs of one row group
     const int CM = kPair ? 2 : 1;           // row blocks per cluster
     const int G = a.groups;
@@ -541,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             if constexpr (EPI != EPI_STORE_F32) {
                 for (int c = gt; c < ecols; c += kGroupThreads) {
                     pb[c] = a.bias ? __ldg(a.bias + ncta + c) : 0.f;
-                    if constexpr (EPI != EPI_SOFTMAX) {
+                    if constexpr (!kSm) {
                         pg[c] = __ldg(a.gamma + ncta + c);
                         pe[c] = a.beta ? __ldg(a.beta + ncta + c) : 0.f;
                     }
@@ -611,8 +627,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             // thread's statistic covers the CTA's whole row slice.
             float2 part;     // LN: (mean, M2) over n_slice columns; softmax: (max, sum exp)
             float mrun[8];   // softmax: running max when each fragment's exps were taken
-            if constexpr (EPI == EPI_SOFTMAX) {
+            if constexpr (kSm) {
                 float m = neg_inf(), ssum = 0.f;
+                // causal mask: columns of this row slice kept, counted from its first
+                // column (clamped into each fragment below)
+                const long long keep = kMask ? (long long)(m0 + row) + a.mask_offset - (long long)ncta + 1 : 0;
 #pragma unroll
                 for (int c = 0; c < 8; c += 2) {
                     if (c < nchunks) {
@@ -620,10 +639,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         ptx::tmem_ld32(tacc + c * 32, v0);
                         ptx::tmem_ld32(tacc + (c + 1) * 32, v1);
                         ptx::tmem_ld_wait();
-                        softmax_fragment(v0, pb + c * 32, a.alpha, m, ssum);
+                        const int nv0 = kMask ? int(keep - 32 * c < 0 ? 0 : keep - 32 * c > 32 ? 32 : keep - 32 * c) : 32;
+                        const int nv1 = kMask ? int(keep - 32 * (c + 1) < 0 ? 0 : keep - 32 * (c + 1) > 32 ? 32
+                                                                                                  : keep - 32 * (c + 1))
+                                              : 32;
+                        softmax_fragment<kMask>(v0, pb + c * 32, a.alpha, m, ssum, nv0);
                         mrun[c] = m;
                         ptx::tmem_st32(tacc + c * 32, v0);
-                        softmax_fragment(v1, pb + (c + 1) * 32, a.alpha, m, ssum);
+                        softmax_fragment<kMask>(v1, pb + (c + 1) * 32, a.alpha, m, ssum, nv1);
                         mrun[c + 1] = m;
                         ptx::tmem_st32(tacc + (c + 1) * 32, v1);
                     }
@@ -688,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         ptx::st_async_f2(ptx::mapa(mine, peer), part.x, part.y, ptx::mapa(xfull, peer));
                     }
                     ptx::mbar_wait_bounded<true>(xfull, xph, tmo, abort, a.err, kInfoXchg | xs);
-                    stat = combine_slots<EPI == EPI_SOFTMAX>(slot_row, npart, float(ecols));
+                    stat = combine_slots<kSm>(slot_row, npart, float(ecols));
                 } else {
                     if (gt0 && lead_grp) {
                         if (rank == 0) ptx::mbar_arrive_expect_tx(xfull, uint32_t(npart) * 1024u);
@@ -697,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                     ptx::st_async_f2(ptx::mapa(mine, uint32_t(m_sub)), part.x, part.y, ptx::mapa(xfull, uint32_t(m_sub)));
                     if (rank == 0) {
                         ptx::mbar_wait_bounded<true>(xfull, xph, tmo, abort, a.err, kInfoXchg | xs);
-                        stat = combine_slots<EPI == EPI_SOFTMAX>(slot_row, npart, float(ecols));
+                        stat = combine_slots<kSm>(slot_row, npart, float(ecols));
                         if (lead_grp) {
                             res[xs * 128 + row] = stat;
                             ptx::fence_proxy_async_smem();
@@ -776,11 +799,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         p[i] = (i < rem) ? ptx::ld_relaxed_gpu_f2(pblk + (g0 + i) * 128 + row) : make_float2(0.f, 0.f);
-                    tree_fold<EPI == EPI_SOFTMAX, 32>(p, rem, nc);
+                    tree_fold<kSm, 32>(p, rem, nc);
                     const float bn = float(min(rem, 32)) * nc;
                     if (g0 == 0) {
                         s2 = p[0];
-                    } else if constexpr (EPI == EPI_SOFTMAX) {
+                    } else if constexpr (kSm) {
                         const MaxSum m = combine_maxsum(MaxSum{s2.x, s2.y}, MaxSum{p[0].x, p[0].y});
                         s2 = make_float2(m.m, m.s);
                     } else {
@@ -798,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             const bool rows_live = (m0 + q * 32) < a.M;  // warp-uniform: this warp's 32 rows exist
             const int ystore = m0 + q * 32;
             float mean = 0.f, rstd = 0.f;
-            if constexpr (EPI != EPI_SOFTMAX) {
+            if constexpr (!kSm) {
                 // LayerNorm: (g - mean) / sqrt(M2/N + eps); RMSNorm: g / sqrt(mean(g^2) + eps)
                 // with mean(g^2) = M2/N + mean^2 from the same statistics
                 const float var = stat.y / fN;
@@ -817,8 +840,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         uint32_t(&v)[32] = k == 0 ? v0 : v1;
                         const int cc = c + k;
                         uint32_t w[16];
-                        if constexpr (EPI == EPI_SOFTMAX) {
-                            const float f = ptx::ex2_approx((mrun[cc] - stat.x) * kLog2e) / stat.y;
+                        if constexpr (kSm) {
+                            // a fully masked row (sum 0) is all zeros
+                            const float f =
+                                (kMask && !(stat.y > 0.f)) ? 0.f : ptx::ex2_approx((mrun[cc] - stat.x) * kLog2e) / stat.y;
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
                                 w[j] = ptx::pack_bf16x2(__uint_as_float(v[2 * j]) * f, __uint_as_float(v[2 * j + 1]) * f);
@@ -916,6 +941,9 @@ void *kernel_for(int kind, bool pair) {
         case EPI_SOFTMAX:
             return pair ? reinterpret_cast<void *>(&gemm_fused_kernel<EPI_SOFTMAX, true>)
                         : reinterpret_cast<void *>(&gemm_fused_kernel<EPI_SOFTMAX, false>);
+        case EPI_SOFTMAX_MASK:
+            return pair ? reinterpret_cast<void *>(&gemm_fused_kernel<EPI_SOFTMAX_MASK, true>)
+                        : reinterpret_cast<void *>(&gemm_fused_kernel<EPI_SOFTMAX_MASK, false>);
         default: return nullptr;
     }
 }
@@ -924,12 +952,12 @@ void *kernel_for(int kind, bool pair) {
 // shared-memory size seen, so launches made under stream capture issue no
 // attribute calls.
 cudaError_t ensure_attributes(int variant, void *fn, int smem) {
-    static int set_smem[64][8] = {};
-    static bool nonportable[64][8] = {};
+    static int set_smem[64][16] = {};
+    static bool nonportable[64][16] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || variant < 0 || variant >= 8) return cudaErrorInvalidValue;
+    if (dev < 0 || dev >= 64 || variant < 0 || variant >= 16) return cudaErrorInvalidValue;
     if (smem > set_smem[dev][variant]) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;

@@ -58,7 +58,7 @@ def bf16_bits(a_bf16_valued) -> np.ndarray:
 @dataclass(frozen=True)
 class GemmWorkload:
     name: str
-    kind: str              # "rownorm" | "rmsnorm" | "softmax"
+    kind: str              # "rownorm" | "rmsnorm" | "softmax" | "softmax_causal"
     M: int
     N: int
     K: int
@@ -71,6 +71,7 @@ class GemmWorkload:
     act: str = "none"      # "none" | "gelu_tanh"
     eps: float = 1e-5
     resid_std: float | None = None  # a bf16 residual R [M, N] added before the norm
+    mask_offset: int = 0   # softmax_causal: column j of row i kept iff j <= i + mask_offset
     alpha: float = 1.0
     scale: float = 1.0
     description: str = ""
@@ -134,6 +135,10 @@ WORKLOADS = {
         "residual_ln_16384x4096x4096", "rownorm", 16384, 4096, 4096, 6, _c(4096), _c(4096),
         0.02, 0.02, 0.02, "none", 1e-5, resid_std=0.02,
         description="GEMM+bias+residual+LayerNorm (add & norm), FFN-sized"),
+    "causal_softmax_4096x4096x128": GemmWorkload(
+        "causal_softmax_4096x4096x128", "softmax_causal", 4096, 4096, 128, 7, 1.0, _c(128),
+        scale=_c(128), mask_offset=0,
+        description="GEMM+causally masked row softmax: attention scores Q[4096,128] K^T[128,4096]"),
     "stitch_750000x32": StitchWorkload(
         "stitch_750000x32", 750000, 32, 3,
         description="stitched y=A^3+b[row] -> row softmax, very many tiny rows"),

@@ -59,10 +59,24 @@ def check_ln(y, ref, what="", strict=False):
     return float(err.max()), float(err.mean())
 
 
-def check_softmax(y, ref, what=""):
+def check_softmax(y, ref, what="", bf16_out=False, strict=False):
+    """max-abs 1e-3 and every row sum within 1e-2 of 1, against the unrounded
+    fp64 oracle.
+
+    A bf16 output (``bf16_out``) carries its own rounding: half an ulp exceeds
+    1e-3 where |ref| >= 1/2, so there the bound is half an ulp plus the
+    2.3e-5 the 1e-3 budget leaves for fp32 arithmetic below 1/2
+    (1e-3 - 2^-10).  ``strict=True`` asserts that no element needs it (the
+    page workload's outputs are about 1/2048).
+    """
     err = np.abs(y - ref)
     assert np.all(np.isfinite(y)), f"{what}: non-finite output"
-    assert err.max() <= SM_MAX_ABS, f"{what}: max-abs {err.max():.3e} > {SM_MAX_ABS}"
+    if strict:
+        assert np.abs(ref).max() < 0.5, f"{what}: |ref| reaches {np.abs(ref).max():.3f}"
+    bound = np.maximum(SM_MAX_ABS, bf16_half_ulp(ref) + (SM_MAX_ABS - 2.0 ** -10)) if bf16_out else SM_MAX_ABS
+    worst = np.argmax(err - bound)
+    bw = bound.flat[worst] if bf16_out else bound
+    assert err.flat[worst] <= bw, f"{what}: error {err.flat[worst]:.3e} at |ref|={abs(ref.flat[worst]):.3f} > {bw:.3e}"
     rs = np.abs(y.sum(axis=1) - 1.0)
     assert rs.max() <= SM_ROWSUM, f"{what}: row-sum error {rs.max():.3e} > {SM_ROWSUM}"
     return float(err.max()), float(rs.max())

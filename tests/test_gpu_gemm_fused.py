@@ -133,7 +133,7 @@ def test_wide_tile_modes(C, leader, epi, M, K, max_clusters):
         d = inputs.gemm_inputs(M, N, K, seed=90 + C, x_std=1.0, w_std=K ** -0.5,
                                bias_std=0.5, gamma_std=None, beta_std=None)
         ref = oracle.gemm_rowsoftmax(d["X"], d["W"], scale=K ** -0.5, bias=d["bias"])
-        check_softmax(_softmax(d, K ** -0.5, bias=d["bias"], tuning=t), ref, f"wide softmax C={C}")
+        check_softmax(_softmax(d, K ** -0.5, bias=d["bias"], tuning=t), ref, f"wide softmax C={C}", bf16_out=True)
     else:
         d = _ln_inputs(M, N, K, seed=95 + C)
         check_ln(_rownorm(d, act=epi, tuning=t), _ref_ln(d, act=epi), f"wide {epi} C={C} leader={leader}")
@@ -158,7 +158,7 @@ def test_softmax_multicast_cluster():
                            bias_std=None, gamma_std=None, beta_std=None)
     ref = oracle.gemm_rowsoftmax(d["X"], d["W"], scale=0.05)
     for t in (cf.tuning(cluster_size=4, cluster_m=2), cf.tuning(cluster_size=8, cluster_m=2)):
-        check_softmax(_softmax(d, 0.05, tuning=t), ref, "softmax multicast")
+        check_softmax(_softmax(d, 0.05, tuning=t), ref, "softmax multicast", bf16_out=True)
 
 
 def test_rownorm_alpha_and_no_bias():
@@ -195,7 +195,7 @@ def test_softmax_small(M, N, K):
     d = inputs.gemm_inputs(M, N, K, seed=M + N, x_std=1.0, w_std=K ** -0.5,
                            bias_std=None, gamma_std=None, beta_std=None)
     s = K ** -0.5
-    check_softmax(_softmax(d, s), oracle.gemm_rowsoftmax(d["X"], d["W"], scale=s), f"softmax {M}x{N}x{K}")
+    check_softmax(_softmax(d, s), oracle.gemm_rowsoftmax(d["X"], d["W"], scale=s), f"softmax {M}x{N}x{K}", bf16_out=True)
 
 
 @pytest.mark.parametrize("scale,n_slice", [(128 ** -0.5, 0), (1.0, 0), (4.0, 256)])
@@ -221,7 +221,7 @@ def test_softmax_with_bias_and_modes():
                            bias_std=0.5, gamma_std=None, beta_std=None)
     ref = oracle.gemm_rowsoftmax(d["X"], d["W"], scale=0.1, bias=d["bias"])
     for t in (None, cf.tuning(peer_max=-1), cf.tuning(cluster_size=2), cf.tuning(n_slice=128)):
-        check_softmax(_softmax(d, 0.1, bias=d["bias"], tuning=t), ref, f"softmax bias tuning={t}")
+        check_softmax(_softmax(d, 0.1, bias=d["bias"], tuning=t), ref, f"softmax bias tuning={t}", bf16_out=True)
 
 
 # ---------------------------------------------------------------------------
@@ -232,7 +232,8 @@ def test_softmax_full_workload():
     d = inputs.workload_inputs(w.name)
     y = _softmax(d, w.scale)
     rows = sample_rows(w.M, 512)
-    check_softmax(y[rows], oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows), w.name)
+    check_softmax(y[rows], oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows), w.name, bf16_out=True,
+                  strict=True)
     assert np.abs(y.sum(1) - 1).max() <= 1e-2  # every row
 
 
