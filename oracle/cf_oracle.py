@@ -43,6 +43,10 @@ Readings taken where the pages are silent:
     after normalising and beta, when given, is added last.
   * Residual add + norm: the residual R is added after the activation node
     and before the reduction (the "add & norm" of a transformer block).
+  * B2BGEMM: O = S . W2 with S = F(alpha * X.W1 + b1) held in bf16 -- the
+    dtype of the intermediate tensor the unfused chain would materialise
+    (the tensor cores consume bf16 operands); F is GELU(tanh) or the row
+    softmax over N1.
   * Masked softmax: a causal mask keeps element (i, j) of the scaled scores
     iff j <= i + offset (masked elements are -inf before the softmax); a row
     with no kept element is all zeros.
@@ -71,6 +75,7 @@ __all__ = [
     "gemm_bias_rmsnorm",
     "gemm_bias_residual_norm",
     "gemm_rowsoftmax_causal",
+    "b2b_gemm",
     "gemm_rowsoftmax",
     "stitch_rowreduce_broadcast",
     "ROW_CHUNK",
@@ -298,6 +303,40 @@ def gemm_rowsoftmax_causal(X, W, *, scale: float, offset: int, bias=None, rows=N
                 out[o + r, keep[r]] = softmax_rows(z[r, keep[r]][None, :])[0]
         o += idx.size
     return out
+
+
+def b2b_gemm(X, W1, W2, *, op: str, alpha: float = 1.0, b1=None, rows=None) -> np.ndarray:
+    """O = bf16(F(alpha * X.W1 + b1)) . W2, F = GELU_tanh or the row softmax.
+
+    ComFuse, B2BGEMM (Eqs. 3-7): MatMul_1, the epilogue F giving S_tile
+    (Eq. 3), MatMul_2 over the intermediate dimension N1 (Eqs. 4-5).  The
+    intermediate S is rounded to bf16 (round to nearest even), the precision
+    of the tensor the unfused chain stores between the two GEMMs.
+    """
+    if op not in ("softmax", "gelu_tanh"):
+        raise ValueError(f"unknown op {op!r}")
+    X = np.asarray(X)
+    M = X.shape[0]
+    N2 = np.asarray(W2).shape[1]
+    out_rows = M if rows is None else len(rows)
+    out = np.empty((out_rows, N2), dtype=np.float64)
+    b = 0.0 if b1 is None else _f64(b1)
+    o = 0
+    for idx in _row_chunks(M, rows):
+        z = float(alpha) * gemm(X[idx], W1) + b
+        S = softmax_rows(z) if op == "softmax" else gelu_tanh(z)
+        S = _round_bf16(S)
+        out[o:o + idx.size] = gemm(S, W2)
+        o += idx.size
+    return out
+
+
+def _round_bf16(a) -> np.ndarray:
+    """Nearest bf16 value (ties to even) of each element, via float32."""
+    f = np.asarray(a, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
 def stitch_rowreduce_broadcast(A, row_bias, rows=None) -> np.ndarray:

@@ -410,6 +410,43 @@ def check_softmax_causal(fused) -> list:
     return fails
 
 
+def check_b2b(fused) -> list:
+    """B2BGEMM: torch fp64 compositions with the intermediate cast to bf16 by
+    torch; W2 = identity returns bf16(S); the softmax row sums of bf16(S) . 1
+    equal the rounded S's row sums; linearity in W2."""
+    import torch
+    F = torch.nn.functional
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(20))
+    M, K, N1, N2 = 7, 16, 24, 10
+    X = rng.standard_normal((M, K))
+    W1 = rng.standard_normal((K, N1)) / 4
+    W2 = rng.standard_normal((N1, N2))
+    b1 = rng.standard_normal(N1) * 0.1
+    t = {k: torch.from_numpy(v) for k, v in dict(X=X, W1=W1, W2=W2, b=b1).items()}
+    for op in ("softmax", "gelu_tanh"):
+        z = 0.5 * (t["X"] @ t["W1"]) + t["b"]
+        S = torch.softmax(z, dim=1) if op == "softmax" else F.gelu(z, approximate="tanh")
+        S = S.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+        ref = (S @ t["W2"]).numpy()
+        y = np.asarray(fused(X, W1, W2, op=op, alpha=0.5, b1=b1))
+        _fail(fails, y.shape == ref.shape and np.allclose(y, ref, rtol=1e-12, atol=1e-13), f"b2b {op} vs torch")
+        # identity W2 returns the rounded intermediate itself
+        I = np.eye(N1)
+        yi = np.asarray(fused(X, W1, I, op=op, alpha=0.5, b1=b1))
+        _fail(fails, np.array_equal(yi, S.numpy()), f"b2b {op} identity W2")
+    # linearity in W2
+    W2b = rng.standard_normal((N1, N2))
+    y1 = np.asarray(fused(X, W1, W2 + 2.0 * W2b, op="softmax"))
+    y2 = np.asarray(fused(X, W1, W2, op="softmax")) + 2.0 * np.asarray(fused(X, W1, W2b, op="softmax"))
+    _fail(fails, np.allclose(y1, y2, rtol=1e-12, atol=1e-12), "b2b linear in W2")
+    rows = [6, 1]
+    ys = np.asarray(fused(X, W1, W2, op="gelu_tanh", rows=rows))
+    yf = np.asarray(fused(X, W1, W2, op="gelu_tanh"))[rows]
+    _fail(fails, np.allclose(ys, yf, rtol=1e-13, atol=1e-14), "b2b rows= subset")
+    return fails
+
+
 def check_stitch(st) -> list:
     fails = []
     rng = np.random.Generator(np.random.PCG64(16))

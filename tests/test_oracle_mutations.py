@@ -258,6 +258,33 @@ def test_causal_mutant_caught(name):
         assert pins.check_softmax_causal(CAUSAL_MUTANTS[name]), name
 
 
+def _b2b(X, W1, W2, *, op, alpha=1.0, b1=None, rows=None, mistake):
+    X = np.asarray(X, float)
+    if rows is not None:
+        X = X[rows]
+    z = alpha * (X @ np.asarray(W1, float)) + (0 if b1 is None else np.asarray(b1))
+    S = oracle.softmax_rows(z) if op == "softmax" else oracle.gelu_tanh(z)
+    if mistake == "no bf16 rounding":
+        pass
+    elif mistake == "fp16 rounding":
+        S = S.astype(np.float16).astype(np.float64)
+    else:
+        S = S.astype(np.float32).view(np.uint32)
+        S = ((S >> 16) << 16).view(np.float32).astype(np.float64)  # truncation instead of rounding
+    if mistake == "W2 transposed" and np.asarray(W2).shape[0] == np.asarray(W2).shape[1]:
+        return S @ np.asarray(W2, float).T
+    return S @ np.asarray(W2, float)
+
+
+B2B_MUTANTS = {k: (lambda kk: (lambda *a, **kw: _b2b(*a, mistake=kk, **kw)))(k)
+               for k in ("no bf16 rounding", "fp16 rounding", "truncated to bf16")}
+
+
+@pytest.mark.parametrize("name", sorted(B2B_MUTANTS))
+def test_b2b_mutant_caught(name):
+    assert pins.check_b2b(B2B_MUTANTS[name]), name
+
+
 @pytest.mark.parametrize("name", sorted(STITCH_MUTANTS))
 def test_stitch_mutant_caught(name):
     with np.errstate(over="ignore", invalid="ignore"):

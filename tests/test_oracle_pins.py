@@ -58,6 +58,10 @@ def test_softmax_causal_pinned():
     assert pins.check_softmax_causal(oracle.gemm_rowsoftmax_causal) == []
 
 
+def test_b2b_pinned():
+    assert pins.check_b2b(oracle.b2b_gemm) == []
+
+
 def test_stitch_pinned():
     assert pins.check_stitch(oracle.stitch_rowreduce_broadcast) == []
 
