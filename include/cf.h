@@ -376,6 +376,57 @@ CF_API cf_status cf_gemm_fused_rowsoftmax_causal_ex(const void *X, const void *W
                                                     const cf_tuning *tuning);
 
 /* ------------------------------------------------------------------------ */
+/* Back-to-back GEMM with the intermediate kept on chip                      */
+/* ------------------------------------------------------------------------ */
+/* O = bf16( S . W2 ),  S = bf16( F(alpha * X.W1 + b1) )
+ *
+ * [ComFuse] B2BGEMM, Eqs. 3-7 and Fig. 5: MatMul_1 is partitioned along the
+ * intermediate dimension N1 over the C = N1/256 CTAs of a thread-block
+ * cluster (256 columns each); the epilogue F turns each CTA's P tile into its
+ * S tile in tensor memory (S never reaches global memory); MatMul_2 reads S
+ * from there with the CTA's 256-row slice of W2 staged through the same
+ * operand ring as X and W1; the C partial output tiles are summed across the
+ * cluster (in rank order, deterministic) and written once.
+ *   op   CF_B2B_SOFTMAX: F = row softmax over all N1 columns (the row max and
+ *        sum are reduced across the cluster); CF_B2B_GELU_TANH: F = GELU(tanh)
+ *   X  (device) bf16 [M, K] row-major      W1 (device) bf16 [K, N1] row-major
+ *   b1 (device) fp32 [N1] or NULL           W2 (device) bf16 [N1, N2] row-major
+ *   O  (device) bf16 [M, N2] row-major, written; must not alias an input
+ *   workspace (device) >= cf_b2b_workspace_size() bytes, zeroed once by
+ *        cf_workspace_init; holds the device error word
+ * S is rounded to bf16 before MatMul_2 (the operand precision of the tensor
+ * core), as the unfused chain rounds the tensor it stores between the GEMMs.
+ * Supported: M >= 0 (0 is a no-op); K > 0 with K % 8 == 0 (a ragged last
+ * 64-deep block is zero-filled); N1 in {256, 512, 1024, 2048}; N2 in {64, 128}.
+ * All pointers 16-byte aligned (CF_ERR_MISALIGNED).  Asynchronous on
+ * `stream`; device-side timeouts are reported by cf_get_device_status. */
+typedef enum {
+    CF_B2B_SOFTMAX = 0,
+    CF_B2B_GELU_TANH = 1
+} cf_b2b_op;
+
+CF_API size_t cf_b2b_workspace_size(void);
+
+/* The launch the B2B calls would make on the current device (cluster_size =
+ * C, clusters, stages, smem_bytes, row_blocks; n_slice = 256).  Tuning fields
+ * used: stages, max_clusters (others ignored).  Synchronous, launches nothing. */
+CF_API cf_status cf_query_b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, cf_b2b_op op,
+                                   const cf_tuning *tuning, cf_plan *plan);
+
+CF_API cf_status cf_b2b_gemm(const void *X, const void *W1, const float *b1, const void *W2,
+                             void *O, int64_t M, int64_t K, int64_t N1, int64_t N2, float alpha,
+                             cf_b2b_op op, void *workspace, size_t workspace_bytes,
+                             cf_stream_t stream);
+
+/* As cf_b2b_gemm; tuning fields used: stages, max_clusters, timeout_us,
+ * disable_pdl. */
+CF_API cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, const void *W2,
+                                void *O, int64_t M, int64_t K, int64_t N1, int64_t N2,
+                                float alpha, cf_b2b_op op, void *workspace,
+                                size_t workspace_bytes, cf_stream_t stream,
+                                const cf_tuning *tuning);
+
+/* ------------------------------------------------------------------------ */
 /* Stitched reduce -> broadcast subgraph (no GEMM)                           */
 /* ------------------------------------------------------------------------ */
 /* out = softmax_row(A*A*A + row_bias[row])

@@ -127,6 +127,12 @@ _SIGS = {
     "cf_unfused_gemm_residual_norm": (_ST, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
                                             ctypes.c_int, _P, _SZ, _P]),
     "cf_unfused_gemm_rowsoftmax": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _SZ, _P]),
+    "cf_b2b_workspace_size": (_SZ, []),
+    "cf_query_b2b_plan": (_ST, [_I64, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(cf_tuning),
+                                ctypes.POINTER(cf_plan)]),
+    "cf_b2b_gemm": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F, ctypes.c_int, _P, _SZ, _P]),
+    "cf_b2b_gemm_ex": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F, ctypes.c_int, _P, _SZ, _P,
+                             ctypes.POINTER(cf_tuning)]),
     "cf_stitch_rowreduce_broadcast": (_ST, [_P, _P, _P, _I64, _I64, _P, _SZ, _P]),
     "cf_stitch_rowreduce_broadcast_ex": (_ST, [_P, _P, _P, _I64, _I64, _P, _SZ, _P,
                                                ctypes.POINTER(cf_tuning)]),
@@ -349,6 +355,32 @@ def cf_unfused_gemm_rowsoftmax(X, W, bias, Y, M, N, K, scale, workspace, workspa
                                             _ptr(workspace), workspace_bytes, _stream(stream))
 
 
+CF_B2B_SOFTMAX = 0
+CF_B2B_GELU_TANH = 1
+
+
+def cf_b2b_workspace_size() -> int:
+    return lib().cf_b2b_workspace_size()
+
+
+def cf_query_b2b_plan(M, K, N1, N2, op, tuning=None):
+    """(status, plan) of the back-to-back GEMM launch on the current device."""
+    p = cf_plan()
+    st = lib().cf_query_b2b_plan(M, K, N1, N2, op, _tun(tuning), ctypes.byref(p))
+    return st, p
+
+
+def cf_b2b_gemm(X, W1, b1, W2, O, M, K, N1, N2, alpha, op, workspace, workspace_bytes, stream=None,
+                tuning=None) -> int:
+    """O = bf16(F(alpha*X.W1 + b1)) . W2 with F the row softmax (op 0) or GELU_tanh (op 1)."""
+    L = lib()
+    if tuning is None:
+        return L.cf_b2b_gemm(_ptr(X), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(O), M, K, N1, N2, alpha, op,
+                             _ptr(workspace), workspace_bytes, _stream(stream))
+    return L.cf_b2b_gemm_ex(_ptr(X), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(O), M, K, N1, N2, alpha, op,
+                            _ptr(workspace), workspace_bytes, _stream(stream), _tun(tuning))
+
+
 def check(status: int, what: str = "libcf"):
     if status != CF_OK:
         raise CfError(status, what)
@@ -413,6 +445,23 @@ def gemm_fused_rowsoftmax(X, W, bias=None, *, scale=1.0, out=None, workspace=Non
     check(cf_gemm_fused_rowsoftmax(X, W, bias, Y, M, N, K, scale, ws, ws.numel(), stream, tuning),
           "cf_gemm_fused_rowsoftmax")
     return Y
+
+
+def b2b_gemm(X, W1, W2, b1=None, *, op="softmax", alpha=1.0, out=None, workspace=None, stream=None,
+             tuning=None):
+    """O = bf16(F(alpha*X@W1 + b1)) @ W2, F = "softmax" (rows) or "gelu_tanh"; bf16 CUDA tensors."""
+    import torch
+    ops = {"softmax": CF_B2B_SOFTMAX, "gelu_tanh": CF_B2B_GELU_TANH}
+    if op not in ops:
+        raise ValueError(f"unknown op {op!r}")
+    M, K = X.shape
+    N1 = W1.shape[1]
+    N2 = W2.shape[1]
+    O = out if out is not None else torch.empty((M, N2), dtype=torch.bfloat16, device=X.device)
+    ws = workspace if workspace is not None else new_workspace(cf_b2b_workspace_size(), X.device, stream)
+    check(cf_b2b_gemm(X, W1, b1, W2, O, M, K, N1, N2, alpha, ops[op], ws, ws.numel(), stream, tuning),
+          "cf_b2b_gemm")
+    return O
 
 
 def stitch_rowreduce_broadcast(A, row_bias, *, out=None, workspace=None, stream=None, tuning=None):

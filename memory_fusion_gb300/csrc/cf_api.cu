@@ -632,6 +632,113 @@ cf_status cf_gemm_fused_rowsoftmax(const void *X, const void *W, const float *bi
     return cf_gemm_fused_rowsoftmax_ex(X, W, bias, Y, M, N, K, scale, ws, ws_bytes, stream, nullptr);
 }
 
+// -------------------------------------------------------------------------
+// back-to-back GEMM
+// -------------------------------------------------------------------------
+size_t cf_b2b_workspace_size(void) { return cf::kErrBytes; }
+
+static int b2b_active_cached(int device, int op, int cluster, int smem) {
+    static std::map<std::tuple<int, int, int, int>, int> cache;
+    auto key = std::make_tuple(device, op, cluster, smem);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int n = cf::b2b_max_active_clusters(op, cluster, smem);
+    std::lock_guard<std::mutex> lk(g_mu);
+    cache[key] = n;
+    return n;
+}
+
+static cf_status b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, int op, const cf_tuning *tuning,
+                          const cf::DeviceInfo &dev, cf_plan *plan) {
+    if (M < 0 || K <= 0 || N1 <= 0 || N2 <= 0) return CF_ERR_INVALID_ARG;
+    if (op != CF_B2B_SOFTMAX && op != CF_B2B_GELU_TANH) return CF_ERR_INVALID_ARG;
+    if (K % 8 != 0 || N1 % 256 != 0 || (N2 != 64 && N2 != 128)) return CF_ERR_UNSUPPORTED;
+    const int64_t C = N1 / 256;
+    if (C != 1 && C != 2 && C != 4 && C != 8) return CF_ERR_UNSUPPORTED;
+    if (M > (int64_t(1) << 31) - 128 || K > (int64_t(1) << 30)) return CF_ERR_UNSUPPORTED;
+    const int req = tuning ? tuning->stages : 0;
+    if (req < 0 || req > 6) return CF_ERR_UNSUPPORTED;
+    int stages = req > 0 ? req : 4;
+    while (stages > 2 && cf::b2b_smem_bytes(stages, int(C), int(N2)) > kMaxSmem) --stages;
+    const int smem = cf::b2b_smem_bytes(stages, int(C), int(N2));
+    if (smem > kMaxSmem || smem > dev.max_smem_optin) return CF_ERR_UNSUPPORTED;
+    std::memset(plan, 0, sizeof(*plan));
+    plan->n_slice = 256;
+    plan->ctas_per_row = int32_t(C);
+    plan->cluster_size = int32_t(C);
+    plan->groups = 1;
+    plan->cluster_m = 1;
+    plan->row_blocks = int32_t((M + 127) / 128);
+    plan->stages = stages;
+    plan->smem_bytes = smem;
+    const int active = b2b_active_cached(dev.device, op, int(C), smem);
+    if (active <= 0) return CF_ERR_NOT_RESIDENT;
+    int clusters = std::min<int64_t>(plan->row_blocks, active);
+    if (tuning && tuning->max_clusters > 0) clusters = std::min(clusters, int(tuning->max_clusters));
+    plan->clusters = clusters;
+    return CF_OK;
+}
+
+cf_status cf_query_b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, cf_b2b_op op, const cf_tuning *tuning,
+                            cf_plan *plan) {
+    if (!plan) return CF_ERR_INVALID_ARG;
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+    return b2b_plan(M, K, N1, N2, int(op), tuning, dev, plan);
+}
+
+cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, const void *W2, void *O, int64_t M,
+                         int64_t K, int64_t N1, int64_t N2, float alpha, cf_b2b_op op, void *ws, size_t ws_bytes,
+                         cf_stream_t stream, const cf_tuning *tuning) {
+    if (M < 0 || K <= 0 || N1 <= 0 || N2 <= 0) return CF_ERR_INVALID_ARG;
+    if (op != CF_B2B_SOFTMAX && op != CF_B2B_GELU_TANH) return CF_ERR_INVALID_ARG;
+    if (!X || !W1 || !W2 || !O || !ws) return CF_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W1) || !aligned16(W2) || !aligned16(O) || (b1 && !aligned16(b1)))
+        return CF_ERR_MISALIGNED;
+    if (O == X || O == W1 || O == W2) return CF_ERR_INVALID_ARG;
+    if (K % 8 != 0 || N1 % 256 != 0 || (N2 != 64 && N2 != 128)) return CF_ERR_UNSUPPORTED;
+    if (ws_bytes < cf_b2b_workspace_size()) return CF_ERR_WORKSPACE_TOO_SMALL;
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+    cf_plan plan;
+    cf_status st = b2b_plan(M, K, N1, N2, int(op), tuning, dev, &plan);
+    if (st != CF_OK) return st;
+    if (M == 0) return CF_OK;
+
+    cf::B2bArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, 128)) return CF_ERR_CUDA;
+    if (!make_tmap_w(&a.tmap_w1, W1, uint64_t(K), uint64_t(N1), 4)) return CF_ERR_CUDA;
+    if (!make_tmap_w(&a.tmap_w2, W2, uint64_t(N1), uint64_t(N2), uint32_t(N2 / 64))) return CF_ERR_CUDA;
+    a.b1 = b1;
+    a.out = static_cast<uint16_t *>(O);
+    a.err = static_cast<uint32_t *>(ws);
+    a.M = int(M);
+    a.K = int(K);
+    a.N1 = int(N1);
+    a.N2 = int(N2);
+    a.cluster = plan.cluster_size;
+    a.alpha = alpha;
+    const uint32_t tus = tuning && tuning->timeout_us ? tuning->timeout_us : kDefaultTimeoutUs;
+    a.timeout_ns = 1000ull * tus;
+    const bool pdl = !(tuning && tuning->disable_pdl);
+    cudaError_t e = cf::launch_b2b(int(op), a, plan.clusters, plan.stages, plan.smem_bytes, pdl,
+                                   reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CF_OK;
+}
+
+cf_status cf_b2b_gemm(const void *X, const void *W1, const float *b1, const void *W2, void *O, int64_t M, int64_t K,
+                      int64_t N1, int64_t N2, float alpha, cf_b2b_op op, void *ws, size_t ws_bytes,
+                      cf_stream_t stream) {
+    return cf_b2b_gemm_ex(X, W1, b1, W2, O, M, K, N1, N2, alpha, op, ws, ws_bytes, stream, nullptr);
+}
+
 }  // extern "C"
 
 // =========================================================================

@@ -115,4 +115,24 @@ int gemm_fused_max_active_clusters(int kind, bool pair, int cluster, int smem);
 cudaError_t launch_gemm_fused(int kind, const GemmArgs &a, int clusters, int stages, int smem, bool pdl,
                               cudaStream_t stream);
 
+// --------------------------------------------------------------------------
+// back-to-back GEMM (b2b.cu): O = F(alpha * X.W1 + b1) . W2, F = softmax / GELU
+// --------------------------------------------------------------------------
+struct B2bArgs {
+    CUtensorMap tmap_x;   // X [M,K] bf16, box 64(K) x 128(M), 128B swizzle
+    CUtensorMap tmap_w1;  // W1 [K,N1] bf16 as {64, K, N1/64}, box {64, 64, 4}
+    CUtensorMap tmap_w2;  // W2 [N1,N2] bf16 as {64, N1, N2/64}, box {64, 64, N2/64}
+    const float *b1;      // [N1] or null
+    uint16_t *out;        // O [M,N2] bf16
+    uint32_t *err;        // workspace error word
+    int M, K, N1, N2;
+    int cluster;          // C = N1 / 256 CTAs per row block
+    float alpha;
+    unsigned long long timeout_ns;
+};
+
+int b2b_smem_bytes(int stages, int cluster, int n2);
+int b2b_max_active_clusters(int op, int cluster, int smem);
+cudaError_t launch_b2b(int op, const B2bArgs &a, int clusters, int stages, int smem, bool pdl, cudaStream_t stream);
+
 }  // namespace cf

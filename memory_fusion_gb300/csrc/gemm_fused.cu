@@ -45,6 +45,7 @@
 #include "cf_internal.h"
 #include "ptx.cuh"
 #include "rowstats.cuh"
+#include "umma.cuh"
 
 namespace cf {
 namespace {
@@ -136,32 +137,6 @@ __device__ __forceinline__ Bars bars_at(uint32_t base, int stages) {
     b.mma_done = b.xres0 + 8 * kXSets;
     b.misc = b.mma_done + 8;
     return b;
-}
-
-// tcgen05 shared-memory matrix descriptor, 128-byte swizzle
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= uint64_t((saddr & 0x3FFFFu) >> 4);
-    d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
-    d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
-    d |= uint64_t(1) << 46;  // descriptor version for tcgen05
-    d |= uint64_t(2) << 61;  // SWIZZLE_128B
-    return d;
-}
-
-// instruction descriptor: kind::f16, A = B = bf16, D = fp32, A K-major,
-// B MN-major (W is [K,N] with N contiguous), M = m (128, or 256 for a CTA pair), N = n
-__device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) | (uint32_t(n >> 3) << 17) |
-           (uint32_t(m >> 4) << 24);
-}
-
-__device__ __forceinline__ float gelu_tanh_dev(float x) {
-    // 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
-    const float k0 = 0.7978845608028654f;
-    const float k1 = 0.044715f;
-    const float u = k0 * fmaf(k1 * x, x * x, x);
-    return 0.5f * x * (1.0f + ptx::tanh_approx(u));
 }
 
 // Softmax stage-1 nodes on one 32-column fragment: z = alpha*acc + bias;

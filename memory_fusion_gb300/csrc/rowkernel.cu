@@ -25,11 +25,6 @@ namespace {
 
 constexpr int kRowThreads = 256;
 
-__device__ __forceinline__ float gelu_tanh_row(float x) {
-    const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-    return 0.5f * x * (1.0f + ptx::tanh_approx(u));
-}
-
 // (count, mean, M2) of a thread's values, combined with Chan's update
 struct Stat3 {
     float n, mean, m2;
@@ -113,7 +108,7 @@ __global__ void __launch_bounds__(kRowThreads) row_epilogue_kernel(const float *
                 float s = 0.f;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    if constexpr (OP == 1) x[4 * j + k] = gelu_tanh_row(x[4 * j + k]);
+                    if constexpr (OP == 1) x[4 * j + k] = gelu_tanh_dev(x[4 * j + k]);
                     if (R) {
                         const uint32_t w = reinterpret_cast<const uint32_t *>(R + r * N + (j * kRowThreads + t) * 4)[k >> 1];
                         x[4 * j + k] += __uint_as_float((k & 1) ? (w & 0xFFFF0000u) : (w << 16));

@@ -25,6 +25,15 @@ namespace cf {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// The GELU node (tanh form): 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))),
+// tanh by the tanh.approx.f32 instruction.
+__device__ __forceinline__ float gelu_tanh_dev(float x) {
+    const float k0 = 0.7978845608028654f;
+    const float k1 = 0.044715f;
+    const float u = k0 * fmaf(k1 * x, x * x, x);
+    return 0.5f * x * (1.0f + ptx::tanh_approx(u));
+}
+
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
 // --------------------------------------------------------------------------

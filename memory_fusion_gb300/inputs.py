@@ -15,6 +15,9 @@ made in argument order):
 * GEMM + softmax workloads: X, W as above; no bias unless asked.
 * Stitched workload: A[rows, cols] ~ N(0, 2) fp32, then b[rows] ~ U(-1, 1)
   fp32; the generator is re-seeded for every shape.
+* Back-to-back GEMM workloads: X[M,K], W1[K,N1], W2[N1,N2] (bf16, N(0,
+  x_std), N(0, w1_std), N(0, w2_std)), then b1[N1] ~ N(0, b1_std) fp32 (not
+  drawn when b1_std is None).
 
 "N(0, s)" means standard deviation s throughout.
 """
@@ -30,6 +33,8 @@ __all__ = [
     "bf16_bits",
     "GemmWorkload",
     "StitchWorkload",
+    "B2bWorkload",
+    "b2b_inputs",
     "WORKLOADS",
     "gemm_inputs",
     "stitch_inputs",
@@ -106,6 +111,36 @@ class StitchWorkload:
         return 4 * self.rows * self.cols * 2 + 4 * self.rows
 
 
+@dataclass(frozen=True)
+class B2bWorkload:
+    name: str
+    op: str                # "softmax" | "gelu_tanh"
+    M: int
+    K: int
+    N1: int
+    N2: int
+    seed: int
+    x_std: float
+    w1_std: float
+    w2_std: float
+    b1_std: float | None = None
+    alpha: float = 1.0
+    description: str = ""
+    kind: str = "b2b"
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.K * self.N1 + 2.0 * self.M * self.N1 * self.N2
+
+    @property
+    def unavoidable_bytes(self) -> int:
+        """X, W1, b1, W2 read once and O written once; S never leaves the chip."""
+        b = 2 * self.M * self.K + 2 * self.K * self.N1 + 2 * self.N1 * self.N2 + 2 * self.M * self.N2
+        if self.b1_std is not None:
+            b += 4 * self.N1
+        return b
+
+
 def _c(n):
     return 1.0 / math.sqrt(n)
 
@@ -139,6 +174,16 @@ WORKLOADS = {
         "causal_softmax_4096x4096x128", "softmax_causal", 4096, 4096, 128, 7, 1.0, _c(128),
         scale=_c(128), mask_offset=0,
         description="GEMM+causally masked row softmax: attention scores Q[4096,128] K^T[128,4096]"),
+    "b2b_attn_32768x128x1024x128": B2bWorkload(
+        "b2b_attn_32768x128x1024x128", "softmax", 32768, 128, 1024, 128, 8, 1.0, _c(128), 1.0,
+        alpha=_c(128),
+        description="B2BGEMM with a row softmax between the GEMMs, attention-shaped: "
+                    "Q[32768,128] K^T[128,1024] V[1024,128], scale 1/sqrt(128)"),
+    "b2b_gelu_16384x1024x2048x128": B2bWorkload(
+        "b2b_gelu_16384x1024x2048x128", "gelu_tanh", 16384, 1024, 2048, 128, 9, 1.0, _c(1024), _c(2048),
+        b1_std=0.1,
+        description="B2BGEMM with bias+GELU(tanh) between the GEMMs, MLP-shaped: "
+                    "X[16384,1024] W1[1024,2048] W2[2048,128]"),
     "stitch_750000x32": StitchWorkload(
         "stitch_750000x32", 750000, 32, 3,
         description="stitched y=A^3+b[row] -> row softmax, very many tiny rows"),
@@ -180,10 +225,25 @@ def stitch_inputs(rows: int, cols: int, seed: int = 3) -> dict:
     return {"A": A, "row_bias": b}
 
 
+def b2b_inputs(M: int, K: int, N1: int, N2: int, seed: int, *, x_std: float = 1.0, w1_std: float = 1.0,
+               w2_std: float = 1.0, b1_std: float | None = None) -> dict:
+    """X, W1, W2 (bf16-valued float32) and b1 (float32, or None)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = {}
+    out["X"] = round_to_bf16(_normal(rng, (M, K), x_std))
+    out["W1"] = round_to_bf16(_normal(rng, (K, N1), w1_std))
+    out["W2"] = round_to_bf16(_normal(rng, (N1, N2), w2_std))
+    out["b1"] = None if b1_std is None else _normal(rng, (N1,), b1_std)
+    return out
+
+
 def workload_inputs(name: str) -> dict:
     w = WORKLOADS[name]
     if isinstance(w, StitchWorkload):
         return stitch_inputs(w.rows, w.cols, w.seed)
+    if isinstance(w, B2bWorkload):
+        return b2b_inputs(w.M, w.K, w.N1, w.N2, w.seed, x_std=w.x_std, w1_std=w.w1_std, w2_std=w.w2_std,
+                          b1_std=w.b1_std)
     if w.kind in ("rownorm", "rmsnorm"):
         return gemm_inputs(w.M, w.N, w.K, w.seed, x_std=w.x_std, w_std=w.w_std,
                            bias_std=w.bias_std, gamma_std=w.gamma_std,

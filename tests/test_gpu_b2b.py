@@ -1,0 +1,168 @@
+"""GPU parity of the back-to-back GEMM O = bf16(F(alpha X.W1 + b1)) . W2
+(through the C ABI) against the fp64 oracle: both epilogues, every cluster
+width N1/256 in {1, 2, 4, 8}, both output widths, ragged rows and a ragged
+last K block, several row blocks per cluster (the ring, tensor memory and the
+reduce-scatter buffer reused across tiles), ring depths, a selector W2 that
+reads S back column by column, unsupported shapes, and both page-sized
+workloads on sampled rows.
+
+Tolerance.  The kernel rounds its fp32 S to bf16 and the oracle rounds its
+fp64 S to bf16; the two roundings can land one bf16 ulp apart, and the
+kernel's S carries its own fp32 error e_j.  So per output element
+
+    |O - O_ref| <= sum_j (2^-7 |s_j| + e_j) |W2_jk| + N1 2^-24 sum_j |s_j W2_jk|
+                   + half a bf16 ulp of the output,
+
+with e_j <= 2^-16 |s_j| (exp2/FMA chain) and, for GELU, e_j also carries the
+tanh.approx absolute error 2^-10.98 times 0.5 |z_j|.  The bound assumes every
+S element flips, so the mean error is checked as well: at most half a bf16
+ulp of the output on average plus 2^-12 of the flip term (a flip fraction
+far above what rounding noise produces fails it).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from memory_fusion_gb300 import cf, inputs
+from tests.gpu_util import bf16_half_ulp, dev_bf16, dev_f32, host, sample_rows, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+OPS = {"softmax": cf.CF_B2B_SOFTMAX, "gelu_tanh": cf.CF_B2B_GELU_TANH}
+
+
+def _run(d, op, alpha, tuning=None, expect=cf.CF_OK):
+    torch = torch_cuda()
+    M, K = d["X"].shape
+    N1 = d["W1"].shape[1]
+    N2 = d["W2"].shape[1]
+    X, W1, W2 = dev_bf16(d["X"]), dev_bf16(d["W1"]), dev_bf16(d["W2"])
+    b1 = dev_f32(d.get("b1"))
+    O = torch.full((max(M, 1), N2), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = cf.new_workspace(cf.cf_b2b_workspace_size())
+    st = cf.cf_b2b_gemm(X, W1, b1, W2, O, M, K, N1, N2, alpha, OPS[op], ws, ws.numel(), None, tuning)
+    assert st == expect, cf.status_string(st)
+    torch.cuda.synchronize()
+    dst, info = cf.cf_get_device_status(ws)
+    assert dst == cf.CF_OK, (cf.status_string(dst), hex(info))
+    return host(O)[:M]
+
+
+def _terms(d, op, alpha, rows=None):
+    """Per element of the output: sum_j |s_j||W2_jk| and sum_j |z_j||W2_jk|."""
+    X = d["X"] if rows is None else d["X"][rows]
+    z = alpha * oracle.gemm(X, d["W1"]) + (0.0 if d.get("b1") is None else np.asarray(d["b1"], np.float64))
+    s = oracle.softmax_rows(z) if op == "softmax" else oracle.gelu_tanh(z)
+    aw = np.abs(np.asarray(d["W2"], np.float64))
+    return np.abs(s) @ aw, np.abs(z) @ aw
+
+
+def check_b2b(o, ref, d, op, alpha, what, rows=None):
+    assert np.all(np.isfinite(o)), f"{what}: non-finite output"
+    N1 = d["W1"].shape[1]
+    A, Z = _terms(d, op, alpha, rows)
+    flip = (2.0 ** -7 + 2.0 ** -16 + N1 * 2.0 ** -24) * A
+    if op == "gelu_tanh":
+        flip = flip + 0.5 * 2.0 ** -10.98 * Z
+    bound = flip + bf16_half_ulp(np.abs(ref) + flip)
+    err = np.abs(o - ref)
+    worst = np.argmax(err - bound)
+    assert err.flat[worst] <= bound.flat[worst], (
+        f"{what}: error {err.flat[worst]:.3e} > bound {bound.flat[worst]:.3e} at |ref|={abs(ref.flat[worst]):.3e}")
+    mean_bound = bf16_half_ulp(np.abs(ref)).mean() + 2.0 ** -12 * flip.mean()
+    assert err.mean() <= mean_bound, f"{what}: mean error {err.mean():.3e} > {mean_bound:.3e}"
+
+
+def _inputs(M, K, N1, N2, seed, op, b1=True):
+    return inputs.b2b_inputs(M, K, N1, N2, seed, x_std=1.0, w1_std=K ** -0.5,
+                             w2_std=1.0 if op == "softmax" else N1 ** -0.5, b1_std=0.2 if b1 else None)
+
+
+@pytest.mark.parametrize("op", ["softmax", "gelu_tanh"])
+@pytest.mark.parametrize("M,K,N1,N2", [(128, 64, 256, 64), (200, 128, 512, 128), (333, 128, 1024, 64),
+                                       (257, 192, 2048, 128), (130, 136, 1024, 128)])
+def test_b2b_shapes(op, M, K, N1, N2):
+    d = _inputs(M, K, N1, N2, seed=M + K + N1 + N2, op=op)
+    alpha = K ** -0.5 if op == "softmax" else 1.0
+    o = _run(d, op, alpha)
+    ref = oracle.b2b_gemm(d["X"], d["W1"], d["W2"], op=op, alpha=alpha, b1=d["b1"])
+    check_b2b(o, ref, d, op, alpha, f"b2b {op} {M}x{K}x{N1}x{N2}")
+
+
+@pytest.mark.parametrize("op", ["softmax", "gelu_tanh"])
+@pytest.mark.parametrize("kw", [dict(max_clusters=1), dict(max_clusters=3, stages=2), dict(stages=3),
+                                dict(max_clusters=2, disable_pdl=1)])
+def test_b2b_persistent_tiles(op, kw):
+    """Few clusters for many row blocks: each cluster walks several tiles."""
+    M, K, N1, N2 = 1000, 256, 1024, 128
+    d = _inputs(M, K, N1, N2, seed=17, op=op, b1=False)
+    alpha = 0.25 if op == "softmax" else 1.0
+    o = _run(d, op, alpha, tuning=cf.tuning(**kw))
+    ref = oracle.b2b_gemm(d["X"], d["W1"], d["W2"], op=op, alpha=alpha)
+    check_b2b(o, ref, d, op, alpha, f"b2b {op} {kw}")
+
+
+@pytest.mark.parametrize("op", ["softmax", "gelu_tanh"])
+@pytest.mark.parametrize("N1,N2", [(256, 64), (2048, 128)])
+def test_b2b_selector_reads_back_s(op, N1, N2):
+    """W2 with a single 1 per column: O[:, k] = bf16(S[:, c_k]) exactly up to
+    the one-ulp rounding difference of S, for columns c_k spread over every
+    CTA of the cluster and every position of the packed bf16 pairs."""
+    M, K = 256, 128
+    d = _inputs(M, K, N1, N2, seed=23, op=op)
+    cols = (np.arange(N2) * (N1 // N2) + (np.arange(N2) * 7) % (N1 // N2)) % N1
+    W2 = np.zeros((N1, N2), np.float32)
+    W2[cols, np.arange(N2)] = 1.0
+    d["W2"] = W2
+    alpha = K ** -0.5
+    o = _run(d, op, alpha)
+    z = alpha * oracle.gemm(d["X"], d["W1"]) + np.asarray(d["b1"], np.float64)
+    s = oracle.softmax_rows(z) if op == "softmax" else oracle.gelu_tanh(z)
+    sel = s[:, cols]
+    e = 2.0 ** -16 * np.abs(sel) + (0.5 * 2.0 ** -10.98 * np.abs(z[:, cols]) if op == "gelu_tanh" else 0.0)
+    bound = 2 * bf16_half_ulp(np.abs(sel) + e) + e
+    err = np.abs(o - sel)
+    worst = np.argmax(err - bound)
+    assert err.flat[worst] <= bound.flat[worst], (
+        f"selector {op}: error {err.flat[worst]:.3e} > {bound.flat[worst]:.3e} (col {cols[worst % N2]})")
+
+
+def test_b2b_empty_and_unsupported():
+    torch = torch_cuda()
+    ws = cf.new_workspace(cf.cf_b2b_workspace_size())
+    X = torch.zeros((128, 128), dtype=torch.bfloat16, device="cuda")
+    W1 = torch.zeros((128, 512), dtype=torch.bfloat16, device="cuda")
+    W2 = torch.zeros((512, 128), dtype=torch.bfloat16, device="cuda")
+    O = torch.zeros((128, 128), dtype=torch.bfloat16, device="cuda")
+    n = ws.numel()
+    assert cf.cf_b2b_gemm(X, W1, None, W2, O, 0, 128, 512, 128, 1.0, 0, ws, n) == cf.CF_OK
+    assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 384, 128, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 96, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 12, 512, 128, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 4096, 128, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 128, 1.0, 2, ws, n) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_b2b_gemm(X, W1, None, W2, X, 128, 128, 512, 128, 1.0, 0, ws, n) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 128, 1.0, 0, ws, 16) == cf.CF_ERR_WORKSPACE_TOO_SMALL
+    torch.cuda.synchronize()
+    assert cf.cf_get_device_status(ws)[0] == cf.CF_OK
+
+
+def test_b2b_plan():
+    torch_cuda()
+    st, p = cf.cf_query_b2b_plan(32768, 128, 1024, 128, cf.CF_B2B_SOFTMAX)
+    assert st == cf.CF_OK
+    assert p.cluster_size == 4 and p.row_blocks == 256 and 1 <= p.clusters <= 256 // 1
+    assert p.clusters * p.cluster_size <= 152 and p.smem_bytes <= 232448 and p.stages >= 2
+    st, p = cf.cf_query_b2b_plan(100, 64, 2048, 64, cf.CF_B2B_GELU_TANH, cf.tuning(max_clusters=1))
+    assert st == cf.CF_OK and p.cluster_size == 8 and p.clusters == 1
+
+
+@pytest.mark.parametrize("name", ["b2b_attn_32768x128x1024x128", "b2b_gelu_16384x1024x2048x128"])
+def test_b2b_full_workload(name):
+    w = inputs.WORKLOADS[name]
+    d = inputs.workload_inputs(name)
+    o = _run(d, w.op, w.alpha)
+    rows = sample_rows(w.M, 384, seed=11)
+    ref = oracle.b2b_gemm(d["X"], d["W1"], d["W2"], op=w.op, alpha=w.alpha, b1=d["b1"], rows=rows)
+    sub = dict(d, X=d["X"][rows])
+    check_b2b(o[rows], ref, sub, w.op, w.alpha, name)
