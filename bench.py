@@ -102,6 +102,8 @@ def unfused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None, R=None
 
 
 def oracle_rows(oracle, w, d, rows):
+    if w.kind == "b2b":
+        return oracle.b2b_gemm(d["X"], d["W1"], d["W2"], op=w.op, alpha=w.alpha, b1=d["b1"], rows=rows)
     if w.kind == "softmax":
         return oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows)
     if w.kind == "softmax_causal":
@@ -128,10 +130,18 @@ def roofline_time_s(w, peaks):
     return max(t_flop, t_byte), ("tensor" if t_flop >= t_byte else "hbm")
 
 
-def kernel_source_hash():
+KERNEL_TU = {"gemm_fused_kernel": "gemm_fused.cu", "stitch_": "stitch.cu", "b2b_kernel": "b2b.cu"}
+
+
+def kernel_source_hash(kernel):
+    """Hash of the translation unit that holds `kernel` and of every shared
+    header (a kernel's DRAM traffic can only change when one of them does)."""
+    csrc = os.path.join(ROOT, "memory_fusion_gb300", "csrc")
+    tu = next((f for k, f in KERNEL_TU.items() if kernel.startswith(k)), None)
+    files = sorted(f for f in os.listdir(csrc) if f.endswith((".cuh", ".h")) or f == tu)
     h = hashlib.sha256()
-    for f in sorted(os.listdir(os.path.join(ROOT, "memory_fusion_gb300", "csrc"))):
-        with open(os.path.join(ROOT, "memory_fusion_gb300", "csrc", f), "rb") as fh:
+    for f in files:
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
@@ -144,7 +154,7 @@ def profiled_traffic(workload, kernel):
         with open(p) as f:
             d = json.load(f)
         e = d.get(workload, {}).get(kernel)
-        if e and e.get("source_hash") == kernel_source_hash():
+        if e and e.get("source_hash") == kernel_source_hash(kernel):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -349,6 +359,79 @@ def time_e2e(torch, cf, w, steps, device):
     return t, h2d, d2h
 
 
+class B2bRunner:
+    """Device buffers of a back-to-back GEMM workload over `nsets` rotating
+    sets, launched through the public C ABI."""
+
+    def __init__(self, torch, cf, w, nsets, seed_offset=0, device="cuda"):
+        self.torch, self.cf, self.w = torch, cf, w
+        d = inputs.workload_inputs(w.name) if seed_offset == 0 else inputs.b2b_inputs(
+            w.M, w.K, w.N1, w.N2, mdist.seed_for(w.seed, seed_offset), x_std=w.x_std, w1_std=w.w1_std,
+            w2_std=w.w2_std, b1_std=w.b1_std)
+        self.host = d
+        bf = torch.bfloat16
+        X = torch.from_numpy(d["X"]).to(device, bf)
+        W1 = torch.from_numpy(d["W1"]).to(device, bf)
+        W2 = torch.from_numpy(d["W2"]).to(device, bf)
+        b1 = torch.from_numpy(d["b1"]).to(device) if d["b1"] is not None else None
+        self.sets = [{"X": X if i == 0 else X.clone(), "W1": W1 if i == 0 else W1.clone(),
+                      "W2": W2 if i == 0 else W2.clone(), "b1": b1,
+                      "O": torch.empty((w.M, w.N2), dtype=bf, device=device)} for i in range(nsets)]
+        self.op = cf.CF_B2B_SOFTMAX if w.op == "softmax" else cf.CF_B2B_GELU_TANH
+        self.ws_bytes = cf.cf_b2b_workspace_size()
+        self.ws = cf.new_workspace(self.ws_bytes, device)
+
+    def launch(self, i, stream=None):
+        w, s = self.w, self.sets[i % len(self.sets)]
+        self.cf.check(self.cf.cf_b2b_gemm(s["X"], s["W1"], s["b1"], s["W2"], s["O"], w.M, w.K, w.N1, w.N2,
+                                          w.alpha, self.op, self.ws, self.ws_bytes, stream), "b2b launch")
+
+
+def b2b_bytes_per_set(w):
+    return w.unavoidable_bytes
+
+
+def b2b_kernel_name(w):
+    return "b2b_kernel<SOFTMAX>" if w.op == "softmax" else "b2b_kernel<GELU>"
+
+
+def torch_b2b_time(torch, runner, reps):
+    """The same chain as a user writes it without fusion: cuBLAS GEMM to a bf16
+    P, F in torch (fp32 math, bf16 S stored), cuBLAS GEMM of S with W2.  Library
+    kernels, not this package's: the context for what keeping S on chip saves."""
+    w = runner.w
+
+    class U:
+        def launch(self, i, stream=None):
+            s = runner.sets[i % len(runner.sets)]
+            P = torch.matmul(s["X"], s["W1"]).float() * w.alpha
+            if s["b1"] is not None:
+                P = P + s["b1"]
+            S = torch.softmax(P, dim=1) if w.op == "softmax" else torch.nn.functional.gelu(P, approximate="tanh")
+            torch.matmul(S.to(torch.bfloat16), s["W2"], out=s["O"])
+
+    t, n, _ = time_steps(torch, U(), reps, 3, lambda: None, graph_len=reps)
+    return t / n
+
+
+def b2b_numbers(torch, cf, w, peaks, device, l2):
+    nsets = max(1, min(32, math.ceil(3 * l2 / b2b_bytes_per_set(w))))
+    r = B2bRunner(torch, cf, w, nsets, device=device)
+    reps = max(nsets, 200)
+    t, n, _ = time_steps(torch, r, reps, 3, lambda: None, graph_len=reps)
+    t1 = t / n
+    troof, bound = roofline_time_s(w, peaks)
+    _, plan = cf.cf_query_b2b_plan(w.M, w.K, w.N1, w.N2, r.op)
+    tu = torch_b2b_time(torch, r, reps)
+    out = {"us": round(t1 * 1e6, 2), "tflops": round(w.flops / t1 / 1e12, 1),
+           "gbs": round(w.unavoidable_bytes / t1 / 1e9, 1), "bound": bound, "roofline_frac": round(troof / t1, 3),
+           "buffer_sets": nsets, "unfused_torch_us": round(tu * 1e6, 2), "fused_speedup_vs_torch": round(tu / t1, 2),
+           "plan": plan.as_dict()}
+    del r
+    torch.cuda.empty_cache()
+    return out
+
+
 def per_workload(torch, cf, peaks, device, names):
     """Each page workload's fused kernel, timed alone (graph of launches,
     rotating buffers where one set is smaller than 3x L2)."""
@@ -358,6 +441,9 @@ def per_workload(torch, cf, peaks, device, names):
         w = inputs.WORKLOADS[name]
         if isinstance(w, inputs.StitchWorkload):
             out[name] = stitch_numbers(torch, cf, w, peaks, device, l2)
+            continue
+        if isinstance(w, inputs.B2bWorkload):
+            out[name] = b2b_numbers(torch, cf, w, peaks, device, l2)
             continue
         nsets = max(1, min(32, math.ceil(3 * l2 / bytes_per_set(w))))
         r = FusedRunner(torch, cf, w, nsets, device=device)
@@ -434,8 +520,17 @@ def cpu_oracle_sample(w, budget_s=10.0, max_rows=None):
         oracle_rows(oracle, w, d, rows)
         t_total += time.perf_counter() - t0
         done_rows += rows_per
-    flops = 2.0 * done_rows * w.N * w.K
-    return flops / t_total, t_total, done_rows
+    return flops_per_row(w) * done_rows / t_total, t_total, done_rows
+
+
+def flops_per_row(w):
+    return w.flops / w.M
+
+
+def workload_config(w):
+    if isinstance(w, inputs.B2bWorkload):
+        return {"workload": w.name, "op": w.op, "M": w.M, "K": w.K, "N1": w.N1, "N2": w.N2}
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K}
 
 
 def blas_threads():
@@ -580,6 +675,51 @@ def run_stitch(args):
     ranks.close()
 
 
+def run_b2b(args):
+    """A back-to-back GEMM workload as the timed workload (TFLOP/s; used to
+    profile the B2B kernel from a plain command line)."""
+    import torch
+    from memory_fusion_gb300 import cf
+
+    ws_, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    ranks = mdist.Ranks("nccl", device)
+    peaks, peak_src = load_peaks()
+    w = inputs.WORKLOADS[args.workload]
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    nsets = max(1, min(32, math.ceil(3 * l2 / b2b_bytes_per_set(w))))
+    r = B2bRunner(torch, cf, w, nsets, seed_offset=rank, device=device)
+    props = torch.cuda.get_device_properties(device)
+    gpu_id = str(getattr(props, "uuid", local))
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id if gpu_id.startswith("GPU-") else str(local))
+    t, n, clocks = time_steps(torch, r, args.steps, args.warmup, ranks.barrier, sampler)
+    t = ranks.max(t)
+    t1 = t / n
+    tf = mdist.job_throughput(w.flops * n, ws_, t) / 1e12
+    kernel = b2b_kernel_name(w)
+    _, plan = cf.cf_query_b2b_plan(w.M, w.K, w.N1, w.N2, r.op)
+    if rank == 0:
+        print(json.dumps({"metric": "back-to-back GEMM TFLOP/s", "value": round(tf, 3), "unit": "TFLOP/s",
+                          "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": round(t1 * 1e3, 6), "higher_is_better": True, "scaling": "weak",
+                          "dtype": "bf16", "data": "synthetic (seeded)",
+                          "config": dict(workload_config(w), plan=plan.as_dict(),
+                                         l2=f"{nsets} rotating input/output sets (>= 3x L2 of {l2 >> 20} MiB)"),
+                          "roofline": {"bound": "tensor", "achieved": round(tf / ws_, 1),
+                                       "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                       "frac": round(tf / ws_ / peaks["bf16_tflops"], 4),
+                                       "traffic": profiled_traffic(w.name, kernel), "kernel": kernel,
+                                       "algorithmic_bytes_per_launch": w.unavoidable_bytes,
+                                       "flops_per_launch": w.flops,
+                                       "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
+                                       else "fallback"},
+                          "gpu_launches": n, "clocks": clocks}), flush=True)
+    ranks.close()
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the fp64 CPU oracle
 # ---------------------------------------------------------------------------
@@ -603,14 +743,15 @@ def run_reference(args):
     for _ in range(args.steps):
         step()
     t = time.perf_counter() - t0
-    flops = 2.0 * rows_per_step * w.N * w.K * args.steps
+    flops = flops_per_row(w) * rows_per_step * args.steps
     v = flops / t / 1e12
     sample = f"{rows_per_step} random whole rows of {w.name} per step (fp64 numpy oracle)"
+    metric = "back-to-back GEMM TFLOP/s" if isinstance(w, inputs.B2bWorkload) else METRIC
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": ws_,
+        "impl": "reference", "metric": metric, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": ws_,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K},
+        "data": "synthetic", "config": workload_config(w),
         "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -638,6 +779,8 @@ def main():
         run_reference(args)
     elif stitched:
         run_stitch(args)
+    elif isinstance(inputs.WORKLOADS[args.workload], inputs.B2bWorkload):
+        run_b2b(args)
     else:
         run_ours(args)
 

@@ -144,6 +144,23 @@ typedef enum {
     CF_TR_EPI_STORED = 11    /* epilogue: output stores issued                 */
 } cf_trace_event;
 
+/* Per-tile trace events of the back-to-back GEMM kernel (same slot layout;
+ * the epilogue's events are stamped by its first thread). */
+typedef enum {
+    CF_TRB_TMA_FIRST = 0,    /* producer issued the tile's first load          */
+    CF_TRB_ML1_FIRST = 1,    /* MMA warp: first MatMul_1 operand stage ready   */
+    CF_TRB_ML1_DONE = 2,     /* MMA warp: MatMul_1 committed                   */
+    CF_TRB_EPI1_START = 3,   /* epilogue: P ready in tensor memory             */
+    CF_TRB_EPI1_LOCAL = 4,   /* epilogue: CTA-local pass of F done             */
+    CF_TRB_EPI1_DONE = 5,    /* epilogue: S written to tensor memory           */
+    CF_TRB_ML2_START = 6,    /* MMA warp: S and the O accumulator ready        */
+    CF_TRB_ML2_DONE = 7,     /* MMA warp: MatMul_2 committed                   */
+    CF_TRB_EPI2_START = 8,   /* epilogue: partial O ready                      */
+    CF_TRB_EPI2_SENT = 9,    /* epilogue: partial columns sent to their owners */
+    CF_TRB_EPI2_RECV = 10,   /* epilogue: every partial of its columns arrived */
+    CF_TRB_EPI2_STORED = 11  /* epilogue: output columns stored                */
+} cf_trb_event;
+
 /* Fill *t with the defaults (all zero). */
 CF_API void cf_tuning_default(cf_tuning *t);
 
@@ -419,7 +436,7 @@ CF_API cf_status cf_b2b_gemm(const void *X, const void *W1, const float *b1, con
                              cf_stream_t stream);
 
 /* As cf_b2b_gemm; tuning fields used: stages, max_clusters, timeout_us,
- * disable_pdl. */
+ * disable_pdl, trace (per-tile events: cf_trb_event). */
 CF_API cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, const void *W2,
                                 void *O, int64_t M, int64_t K, int64_t N1, int64_t N2,
                                 float alpha, cf_b2b_op op, void *workspace,

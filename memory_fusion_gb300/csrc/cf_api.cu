@@ -637,15 +637,15 @@ cf_status cf_gemm_fused_rowsoftmax(const void *X, const void *W, const float *bi
 // -------------------------------------------------------------------------
 size_t cf_b2b_workspace_size(void) { return cf::kErrBytes; }
 
-static int b2b_active_cached(int device, int op, int cluster, int smem) {
-    static std::map<std::tuple<int, int, int, int>, int> cache;
-    auto key = std::make_tuple(device, op, cluster, smem);
+static int b2b_active_cached(int device, int op, int cluster, int n2, int smem) {
+    static std::map<std::tuple<int, int, int, int, int>, int> cache;
+    auto key = std::make_tuple(device, op, cluster, n2, smem);
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    int n = cf::b2b_max_active_clusters(op, cluster, smem);
+    int n = cf::b2b_max_active_clusters(op, cluster, n2, smem);
     std::lock_guard<std::mutex> lk(g_mu);
     cache[key] = n;
     return n;
@@ -674,7 +674,7 @@ static cf_status b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, int op, 
     plan->row_blocks = int32_t((M + 127) / 128);
     plan->stages = stages;
     plan->smem_bytes = smem;
-    const int active = b2b_active_cached(dev.device, op, int(C), smem);
+    const int active = b2b_active_cached(dev.device, op, int(C), int(N2), smem);
     if (active <= 0) return CF_ERR_NOT_RESIDENT;
     int clusters = std::min<int64_t>(plan->row_blocks, active);
     if (tuning && tuning->max_clusters > 0) clusters = std::min(clusters, int(tuning->max_clusters));
@@ -726,6 +726,7 @@ cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, const v
     a.alpha = alpha;
     const uint32_t tus = tuning && tuning->timeout_us ? tuning->timeout_us : kDefaultTimeoutUs;
     a.timeout_ns = 1000ull * tus;
+    a.trace = tuning ? reinterpret_cast<unsigned long long *>(tuning->trace) : nullptr;
     const bool pdl = !(tuning && tuning->disable_pdl);
     cudaError_t e = cf::launch_b2b(int(op), a, plan.clusters, plan.stages, plan.smem_bytes, pdl,
                                    reinterpret_cast<cudaStream_t>(stream));

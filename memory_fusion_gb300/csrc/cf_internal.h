@@ -129,10 +129,11 @@ struct B2bArgs {
     int cluster;          // C = N1 / 256 CTAs per row block
     float alpha;
     unsigned long long timeout_ns;
+    unsigned long long *trace;  // optional %globaltimer stamps, CF_TRACE_SLOTS per CTA
 };
 
 int b2b_smem_bytes(int stages, int cluster, int n2);
-int b2b_max_active_clusters(int op, int cluster, int smem);
+int b2b_max_active_clusters(int op, int cluster, int n2, int smem);
 cudaError_t launch_b2b(int op, const B2bArgs &a, int clusters, int stages, int smem, bool pdl, cudaStream_t stream);
 
 }  // namespace cf

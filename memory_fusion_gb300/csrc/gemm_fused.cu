@@ -45,22 +45,11 @@
 #include "cf_internal.h"
 #include "ptx.cuh"
 #include "rowstats.cuh"
+#include "trace.cuh"
 #include "umma.cuh"
 
 namespace cf {
 namespace {
-
-// optional timeline stamps (tracing): one slot per (CTA, tile, event)
-__device__ __forceinline__ void trace_stamp(unsigned long long *tr, int slot) {
-    if (tr != nullptr) tr[blockIdx.x * CF_TRACE_SLOTS + slot] = ptx::globaltimer();
-}
-__device__ __forceinline__ void trace_tile(unsigned long long *tr, int tile, int ev) {
-    if (tr != nullptr && tile < CF_TRACE_TILES)
-        tr[blockIdx.x * CF_TRACE_SLOTS + 4 + tile * CF_TRACE_EVENTS + ev] = ptx::globaltimer();
-}
-__device__ __forceinline__ void trace_tile_value(unsigned long long *tr, int tile, int ev, unsigned long long v) {
-    if (tr != nullptr && tile < CF_TRACE_TILES) tr[blockIdx.x * CF_TRACE_SLOTS + 4 + tile * CF_TRACE_EVENTS + ev] = v;
-}
 
 constexpr int kThreads = 320;      // 10 warps
 constexpr int kEpiWarps = 8;       // warps 2..9: two groups of 4
