@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
+from oracle import cf_oracle
 from tests import oracle_pins as pins
 
 S = math.sqrt(2 / math.pi)
@@ -262,22 +263,32 @@ def _b2b(X, W1, W2, *, op, alpha=1.0, b1=None, rows=None, mistake):
     X = np.asarray(X, float)
     if rows is not None:
         X = X[rows]
-    z = alpha * (X @ np.asarray(W1, float)) + (0 if b1 is None else np.asarray(b1))
-    S = oracle.softmax_rows(z) if op == "softmax" else oracle.gelu_tanh(z)
+    bias = 0 if (b1 is None or mistake == "b1 dropped") else np.asarray(b1)
+    if mistake == "alpha after bias":
+        z = alpha * (X @ np.asarray(W1, float) + bias)
+    else:
+        z = alpha * (X @ np.asarray(W1, float)) + bias
+    if op == "softmax":
+        S = oracle.softmax_rows(z.T).T if mistake == "softmax over columns" else oracle.softmax_rows(z)
+    else:
+        S = oracle.gelu_tanh(z)
     if mistake == "no bf16 rounding":
         pass
     elif mistake == "fp16 rounding":
         S = S.astype(np.float16).astype(np.float64)
-    else:
+    elif mistake == "truncated to bf16":
         S = S.astype(np.float32).view(np.uint32)
         S = ((S >> 16) << 16).view(np.float32).astype(np.float64)  # truncation instead of rounding
+    else:
+        S = cf_oracle._round_bf16(S)
     if mistake == "W2 transposed" and np.asarray(W2).shape[0] == np.asarray(W2).shape[1]:
         return S @ np.asarray(W2, float).T
     return S @ np.asarray(W2, float)
 
 
 B2B_MUTANTS = {k: (lambda kk: (lambda *a, **kw: _b2b(*a, mistake=kk, **kw)))(k)
-               for k in ("no bf16 rounding", "fp16 rounding", "truncated to bf16")}
+               for k in ("no bf16 rounding", "fp16 rounding", "truncated to bf16", "b1 dropped", "alpha after bias",
+                         "softmax over columns")}
 
 
 @pytest.mark.parametrize("name", sorted(B2B_MUTANTS))
