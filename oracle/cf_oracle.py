@@ -54,6 +54,13 @@ Readings taken where the pages are silent:
     is added after scaling.  Exponent base e.
   * GELU is the tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
   * pow(A, 3) is the real cube with its sign (A*A*A).
+  * Stitched add + LayerNorm: x = A + R (R optional), LayerNorm over each
+    row as above, gamma/beta indexed by column.
+  * Stitched BatchNorm (training-mode statistics): per column j the mean and
+    the biased variance over all rows; y = (A - mean_j) / sqrt(var_j + eps)
+    * gamma_j + beta_j.  The column statistic is a one-to-many dependency
+    over every row (AStitch, "Four stitching schemes": Regional when one
+    block holds all rows of its columns, Global otherwise).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
 forms, invariants, brute force on tiny inputs and library routines.
@@ -76,6 +83,8 @@ __all__ = [
     "gemm_bias_residual_norm",
     "gemm_rowsoftmax_causal",
     "b2b_gemm",
+    "stitch_add_layernorm",
+    "stitch_batchnorm",
     "gemm_rowsoftmax",
     "stitch_rowreduce_broadcast",
     "ROW_CHUNK",
@@ -337,6 +346,44 @@ def _round_bf16(a) -> np.ndarray:
     u = f.view(np.uint32).astype(np.uint64)
     r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
     return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def stitch_add_layernorm(A, R, gamma, beta, eps: float, rows=None) -> np.ndarray:
+    """out = LayerNorm(A + R) * gamma + beta over each row (R may be None).
+
+    AStitch, "Four stitching schemes": an elementwise producer (Local), two
+    reductions over the row (mean, then the variance around it) and their
+    broadcast back, with column parameters shared by every row (a
+    one-to-many dependency: Regional).
+    """
+    A = np.asarray(A)
+    M, N = A.shape
+    out_rows = M if rows is None else len(rows)
+    out = np.empty((out_rows, N), dtype=np.float64)
+    o = 0
+    for idx in _row_chunks(M, rows):
+        x = _f64(A[idx])
+        if R is not None:
+            x = x + _f64(np.asarray(R)[idx])
+        out[o:o + idx.size] = layernorm_rows(x, gamma, beta, eps)
+        o += idx.size
+    return out
+
+
+def stitch_batchnorm(A, gamma, beta, eps: float):
+    """BatchNorm over the rows of A [rows, cols] with batch statistics.
+
+    mean_j = (1/rows) sum_i A_ij;  var_j = (1/rows) sum_i (A_ij - mean_j)^2;
+    out_ij = (A_ij - mean_j) / sqrt(var_j + eps) * gamma_j + beta_j.
+    Returns (out, mean, var).  Every output depends on every row of its
+    column: the reduction runs along the other axis from the row reductions
+    (AStitch, "Four stitching schemes", column reduction -> broadcast).
+    """
+    A = _f64(A)
+    mean = A.mean(axis=0)
+    d = A - mean
+    var = (d * d).mean(axis=0)
+    return d / np.sqrt(var + float(eps)) * _f64(gamma) + _f64(beta), mean, var
 
 
 def stitch_rowreduce_broadcast(A, row_bias, rows=None) -> np.ndarray:

@@ -447,6 +447,79 @@ def check_b2b(fused) -> list:
     return fails
 
 
+def check_stitch_add_layernorm(fn) -> list:
+    """out = LN(A + R) * gamma + beta per row: torch layer_norm in fp64, R
+    optional, a hand-derived row, mean 0 / variance 1 at eps = 0, A and R
+    interchangeable, a per-row constant in R changes nothing, rows= sampling."""
+    import torch
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(31))
+    M, N = 9, 37
+    A = rng.standard_normal((M, N)) * 2
+    R = rng.standard_normal((M, N))
+    g = 1 + 0.3 * rng.standard_normal(N)
+    b = 0.2 * rng.standard_normal(N)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(A + R), (N,), torch.from_numpy(g), torch.from_numpy(b),
+                                         1e-5).numpy()
+    y = np.asarray(fn(A, R, g, b, 1e-5))
+    _fail(fails, y.shape == ref.shape and np.allclose(y, ref, rtol=1e-12, atol=1e-12), "add+LN vs torch layer_norm")
+    y0 = np.asarray(fn(A, None, g, b, 1e-5))
+    yz = np.asarray(fn(A, np.zeros_like(A), g, b, 1e-5))
+    _fail(fails, np.array_equal(y0, yz), "add+LN: R = None equals R = 0")
+    # hand-derived: x = [2, 2, 4, 4] -> mean 3, variance 1 -> [-1, -1, 1, 1] * gamma + beta
+    yh = np.asarray(fn(np.array([[1.0, 2, 3, 4]]), np.array([[1.0, 0, 1, 0]]), np.array([1.0, 2, 3, 4]),
+                       np.array([0.0, 0, 0, 1]), 0.0))[0]
+    _fail(fails, np.allclose(yh, [-1, -2, 3, 5], rtol=0, atol=1e-15), "add+LN hand-derived row")
+    yn = np.asarray(fn(A, R, np.ones(N), np.zeros(N), 0.0))
+    _fail(fails, np.all(np.abs(yn.mean(axis=1)) < 1e-12), "add+LN rows have mean 0 at eps = 0")
+    _fail(fails, all(abs(statistics.pvariance(r) - 1) < 1e-9 for r in yn.tolist()), "add+LN rows have variance 1")
+    _fail(fails, np.allclose(np.asarray(fn(R, A, g, b, 1e-5)), y, rtol=1e-13, atol=1e-13), "add+LN: A + R = R + A")
+    shift = rng.standard_normal((M, 1)) * 5
+    _fail(fails, np.allclose(np.asarray(fn(A, R + shift, g, b, 1e-5)), y, rtol=1e-9, atol=1e-9),
+          "add+LN invariant under a per-row constant in R")
+    rows = [7, 0, 3]
+    _fail(fails, np.allclose(np.asarray(fn(A, R, g, b, 1e-5, rows=rows)), y[rows], rtol=1e-14, atol=1e-14),
+          "add+LN rows= subset")
+    return fails
+
+
+def check_stitch_batchnorm(fn) -> list:
+    """BatchNorm over rows: torch batch_norm (training statistics) in fp64, a
+    hand-derived fixture, per-column mean 0 / variance 1 at eps = 0, a
+    constant column gives beta, column permutation equivariance, the returned
+    mean and biased variance against the statistics module."""
+    import torch
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(32))
+    M, N = 41, 13
+    A = rng.standard_normal((M, N)) * 3 + rng.standard_normal(N) * 4
+    g = 1 + 0.3 * rng.standard_normal(N)
+    b = 0.2 * rng.standard_normal(N)
+    ref = torch.nn.functional.batch_norm(torch.from_numpy(A), None, None, torch.from_numpy(g), torch.from_numpy(b),
+                                         training=True, eps=1e-5).numpy()
+    y, mean, var = fn(A, g, b, 1e-5)
+    y = np.asarray(y)
+    _fail(fails, y.shape == ref.shape and np.allclose(y, ref, rtol=1e-12, atol=1e-12), "BN vs torch batch_norm")
+    cols = A.T.tolist()
+    _fail(fails, all(abs(mean[j] - statistics.fmean(cols[j])) < 1e-12 for j in range(N)), "BN mean")
+    _fail(fails, all(abs(var[j] - statistics.pvariance(cols[j])) < 1e-10 * (1 + var[j]) for j in range(N)),
+          "BN biased variance")
+    gold = _load_golden("batchnorm_worked.txt")
+    yg = np.asarray(fn(np.array([[1.0, 10], [3, 10], [5, 16]]), np.array([2.0, 1]), np.array([0.0, 0.5]), 0.0)[0])
+    _fail(fails, np.allclose(yg, gold, rtol=0, atol=1e-14), "BN hand-derived fixture")
+    yn = np.asarray(fn(A, np.ones(N), np.zeros(N), 0.0)[0])
+    _fail(fails, np.all(np.abs(yn.mean(axis=0)) < 1e-12), "BN columns have mean 0 at eps = 0")
+    _fail(fails, all(abs(statistics.pvariance(c) - 1) < 1e-9 for c in yn.T.tolist()), "BN columns have variance 1")
+    Ac = A.copy()
+    Ac[:, 4] = 2.5
+    yc = np.asarray(fn(Ac, g, b, 1e-5)[0])
+    _fail(fails, np.all(yc[:, 4] == b[4]), "BN constant column gives beta")
+    perm = rng.permutation(N)
+    yp = np.asarray(fn(A[:, perm], g[perm], b[perm], 1e-5)[0])
+    _fail(fails, np.allclose(yp, y[:, perm], rtol=1e-13, atol=1e-13), "BN column permutation")
+    return fails
+
+
 def check_stitch(st) -> list:
     fails = []
     rng = np.random.Generator(np.random.PCG64(16))

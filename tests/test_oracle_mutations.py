@@ -296,6 +296,57 @@ def test_b2b_mutant_caught(name):
     assert pins.check_b2b(B2B_MUTANTS[name]), name
 
 
+def _add_ln(A, R, gamma, beta, eps, rows=None, *, mistake):
+    A = np.asarray(A, float)
+    x = A if R is None else (A - np.asarray(R, float) if mistake == "R subtracted" else A + np.asarray(R, float))
+    if rows is not None:
+        x = x[rows]
+    ax = 0 if mistake == "normalised over columns" else -1
+    mean = x.mean(axis=ax, keepdims=True)
+    d = x - mean
+    var = (d * d).sum(axis=ax, keepdims=True) / (x.shape[ax] - (1 if mistake == "unbiased variance" else 0))
+    g, b = (beta, gamma) if mistake == "gamma and beta swapped" else (gamma, beta)
+    return d / np.sqrt(var + eps) * np.asarray(g, float) + np.asarray(b, float)
+
+
+ADD_LN_MUTANTS = {k: (lambda kk: (lambda *a, **kw: _add_ln(*a, mistake=kk, **kw)))(k)
+                  for k in ("R subtracted", "normalised over columns", "unbiased variance", "gamma and beta swapped")}
+
+
+@pytest.mark.parametrize("name", sorted(ADD_LN_MUTANTS))
+def test_add_layernorm_mutant_caught(name):
+    with np.errstate(divide="ignore", invalid="ignore"):
+        assert pins.check_stitch_add_layernorm(ADD_LN_MUTANTS[name]), name
+
+
+def _bn(A, gamma, beta, eps, *, mistake):
+    A = np.asarray(A, float)
+    ax = 1 if mistake == "normalised over rows" else 0
+    mean = A.mean(axis=ax, keepdims=True)
+    d = A - mean
+    n = A.shape[ax]
+    var = (d * d).sum(axis=ax, keepdims=True) / (n - 1 if mistake == "unbiased variance" else n)
+    if mistake == "eps outside the root":
+        y = d / (np.sqrt(var) + eps)
+    else:
+        y = d / np.sqrt(var + eps)
+    if mistake == "gamma added":
+        y = y + np.asarray(gamma, float) + np.asarray(beta, float)
+    else:
+        y = y * np.asarray(gamma, float) + np.asarray(beta, float)
+    return y, mean.reshape(-1), var.reshape(-1)
+
+
+BN_MUTANTS = {k: (lambda kk: (lambda *a, **kw: _bn(*a, mistake=kk, **kw)))(k)
+              for k in ("normalised over rows", "unbiased variance", "eps outside the root", "gamma added")}
+
+
+@pytest.mark.parametrize("name", sorted(BN_MUTANTS))
+def test_batchnorm_mutant_caught(name):
+    with np.errstate(divide="ignore", invalid="ignore"):
+        assert pins.check_stitch_batchnorm(BN_MUTANTS[name]), name
+
+
 @pytest.mark.parametrize("name", sorted(STITCH_MUTANTS))
 def test_stitch_mutant_caught(name):
     with np.errstate(over="ignore", invalid="ignore"):

@@ -105,3 +105,11 @@ def test_row_chunking_is_transparent(rows, monkeypatch):
     monkeypatch.setattr(cf_oracle, "ROW_CHUNK", 2)
     chunked = cf_oracle.gemm_bias_rownorm(X, W, b, np.ones(12), np.zeros(12), rows=rows)
     np.testing.assert_allclose(full, chunked, rtol=1e-13, atol=1e-14)  # BLAS blocking may differ by 1 ulp
+
+
+def test_stitch_add_layernorm_pinned():
+    assert pins.check_stitch_add_layernorm(oracle.stitch_add_layernorm) == []
+
+
+def test_stitch_batchnorm_pinned():
+    assert pins.check_stitch_batchnorm(oracle.stitch_batchnorm) == []
