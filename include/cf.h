@@ -467,6 +467,78 @@ CF_API cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *r
                                            void *workspace, size_t workspace_bytes,
                                            cf_stream_t stream, const cf_tuning *tuning);
 
+/* out = LayerNorm(A + R) * gamma + beta over each row
+ *
+ * [AStitch] "Four stitching schemes": an elementwise producer (A + R), two
+ * row reductions (the mean, then the variance around it) and their
+ * broadcast, with column parameters shared by every row, in one kernel; the
+ * thread mapping is that of cf_stitch_rowreduce_broadcast (rows of up to 128
+ * columns packed several to a warp, wider rows split over the CTAs of a
+ * cluster with one DSMEM exchange of (mean, M2) per row).
+ *   A, R  (device) fp32 [rows, cols] row-major; R may be NULL (out = LN(A))
+ *   gamma, beta (device) fp32 [cols]
+ *   out   (device) fp32 [rows, cols]; may alias A (each element is read before
+ *         it is written, by the thread that writes it)
+ *   variance biased (divide by cols), eps inside the square root
+ *   workspace >= cf_stitch_workspace_size(rows, cols) bytes
+ * Supported: rows, cols >= 0 (0 is a no-op), cols <= 262144; 4-byte aligned
+ * pointers (16-byte aligned with cols % 4 == 0 takes the 128-bit path).
+ * Tuning fields used: stitch_mapping (1 packed, 2 split), cluster_size,
+ * timeout_us, disable_pdl. */
+CF_API cf_status cf_stitch_add_layernorm(const float *A, const float *R, const float *gamma,
+                                         const float *beta, float *out, int64_t rows, int64_t cols,
+                                         float eps, void *workspace, size_t workspace_bytes,
+                                         cf_stream_t stream);
+
+CF_API cf_status cf_stitch_add_layernorm_ex(const float *A, const float *R, const float *gamma,
+                                            const float *beta, float *out, int64_t rows,
+                                            int64_t cols, float eps, void *workspace,
+                                            size_t workspace_bytes, cf_stream_t stream,
+                                            const cf_tuning *tuning);
+
+/* out = (A - mean_col) / sqrt(var_col + eps) * gamma[col] + beta[col]
+ * with the batch statistics of each column (mean and biased variance over all
+ * rows), as BatchNorm computes them in training.
+ *
+ * [AStitch] "Four stitching schemes": the column statistic is a one-to-many
+ * dependency over every row.  Regional (rows <= 256): one CTA holds all rows
+ * of a 128-column strip in registers and combines its warps' partials in
+ * shared memory -- one HBM pass.  Global (more rows): one resident wave of
+ * CTAs (vertical packing) reduces contiguous row ranges, writes column
+ * partials to the workspace and meets at an in-kernel grid barrier; every
+ * CTA folds all partials in one fixed order, then normalises its rows,
+ * re-reading them from L2 where they still are.  The launch is refused
+ * (CF_ERR_NOT_RESIDENT) if the wave cannot be resident.
+ *   A     (device) fp32 [rows, cols] row-major
+ *   gamma, beta (device) fp32 [cols]
+ *   out   (device) fp32 [rows, cols]; must not alias A
+ *   mean_out, var_out (device) fp32 [cols] or NULL: the batch statistics
+ *   workspace (device) >= cf_stitch_batchnorm_workspace_size(rows, cols)
+ *         bytes, 16-byte aligned, zeroed once by cf_workspace_init; the grid
+ *         barrier's counters reset themselves at the end of each launch (after
+ *         a device-side error, zero the workspace again)
+ * Supported: rows, cols >= 0 (0 is a no-op); 4-byte aligned pointers.
+ * Tuning fields used: stitch_mapping (3 Regional, 4 Global), max_clusters
+ * (cap on the Global grid), timeout_us, disable_pdl, extra_arrivals (TEST
+ * HOOK: > 0 makes the grid barrier wait run out). */
+CF_API size_t cf_stitch_batchnorm_workspace_size(int64_t rows, int64_t cols);
+
+CF_API cf_status cf_stitch_batchnorm(const float *A, const float *gamma, const float *beta,
+                                     float *out, float *mean_out, float *var_out, int64_t rows,
+                                     int64_t cols, float eps, void *workspace,
+                                     size_t workspace_bytes, cf_stream_t stream);
+
+CF_API cf_status cf_stitch_batchnorm_ex(const float *A, const float *gamma, const float *beta,
+                                        float *out, float *mean_out, float *var_out, int64_t rows,
+                                        int64_t cols, float eps, void *workspace,
+                                        size_t workspace_bytes, cf_stream_t stream,
+                                        const cf_tuning *tuning);
+
+/* The mapping (3 Regional, 4 Global) and grid size the BatchNorm call would
+ * use on the current device.  Synchronous, launches nothing. */
+CF_API cf_status cf_query_stitch_batchnorm_plan(int64_t rows, int64_t cols, const cf_tuning *tuning,
+                                                int32_t *mapping, int32_t *grid);
+
 /* ------------------------------------------------------------------------ */
 /* The unfused two-kernel composition (measured baseline)                    */
 /* ------------------------------------------------------------------------ */

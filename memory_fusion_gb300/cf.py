@@ -133,6 +133,15 @@ _SIGS = {
     "cf_b2b_gemm": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F, ctypes.c_int, _P, _SZ, _P]),
     "cf_b2b_gemm_ex": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F, ctypes.c_int, _P, _SZ, _P,
                              ctypes.POINTER(cf_tuning)]),
+    "cf_stitch_add_layernorm": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, _SZ, _P]),
+    "cf_stitch_add_layernorm_ex": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, _SZ, _P,
+                                         ctypes.POINTER(cf_tuning)]),
+    "cf_stitch_batchnorm_workspace_size": (_SZ, [_I64, _I64]),
+    "cf_stitch_batchnorm": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P, _SZ, _P]),
+    "cf_stitch_batchnorm_ex": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P, _SZ, _P,
+                                     ctypes.POINTER(cf_tuning)]),
+    "cf_query_stitch_batchnorm_plan": (_ST, [_I64, _I64, ctypes.POINTER(cf_tuning), ctypes.POINTER(ctypes.c_int32),
+                                             ctypes.POINTER(ctypes.c_int32)]),
     "cf_stitch_rowreduce_broadcast": (_ST, [_P, _P, _P, _I64, _I64, _P, _SZ, _P]),
     "cf_stitch_rowreduce_broadcast_ex": (_ST, [_P, _P, _P, _I64, _I64, _P, _SZ, _P,
                                                ctypes.POINTER(cf_tuning)]),
@@ -445,6 +454,65 @@ def gemm_fused_rowsoftmax(X, W, bias=None, *, scale=1.0, out=None, workspace=Non
     check(cf_gemm_fused_rowsoftmax(X, W, bias, Y, M, N, K, scale, ws, ws.numel(), stream, tuning),
           "cf_gemm_fused_rowsoftmax")
     return Y
+
+
+def cf_stitch_add_layernorm(A, R, gamma, beta, out, rows, cols, eps, workspace, workspace_bytes, stream=None,
+                            tuning=None) -> int:
+    """out = LayerNorm(A + R) * gamma + beta over each row (R may be None)."""
+    L = lib()
+    if tuning is None:
+        return L.cf_stitch_add_layernorm(_ptr(A), _ptr(R), _ptr(gamma), _ptr(beta), _ptr(out), rows, cols, eps,
+                                         _ptr(workspace), workspace_bytes, _stream(stream))
+    return L.cf_stitch_add_layernorm_ex(_ptr(A), _ptr(R), _ptr(gamma), _ptr(beta), _ptr(out), rows, cols, eps,
+                                        _ptr(workspace), workspace_bytes, _stream(stream), _tun(tuning))
+
+
+def cf_stitch_batchnorm_workspace_size(rows, cols) -> int:
+    return lib().cf_stitch_batchnorm_workspace_size(rows, cols)
+
+
+def cf_stitch_batchnorm(A, gamma, beta, out, mean_out, var_out, rows, cols, eps, workspace, workspace_bytes,
+                        stream=None, tuning=None) -> int:
+    """out = (A - mean_col)/sqrt(var_col + eps)*gamma + beta with batch statistics over the rows."""
+    L = lib()
+    if tuning is None:
+        return L.cf_stitch_batchnorm(_ptr(A), _ptr(gamma), _ptr(beta), _ptr(out), _ptr(mean_out), _ptr(var_out),
+                                     rows, cols, eps, _ptr(workspace), workspace_bytes, _stream(stream))
+    return L.cf_stitch_batchnorm_ex(_ptr(A), _ptr(gamma), _ptr(beta), _ptr(out), _ptr(mean_out), _ptr(var_out),
+                                    rows, cols, eps, _ptr(workspace), workspace_bytes, _stream(stream), _tun(tuning))
+
+
+def cf_query_stitch_batchnorm_plan(rows, cols, tuning=None):
+    """(status, mapping 3 Regional / 4 Global, grid) on the current device."""
+    m, g = ctypes.c_int32(0), ctypes.c_int32(0)
+    st = lib().cf_query_stitch_batchnorm_plan(rows, cols, _tun(tuning), ctypes.byref(m), ctypes.byref(g))
+    return st, m.value, g.value
+
+
+def stitch_add_layernorm(A, R, gamma, beta, *, eps=1e-5, out=None, workspace=None, stream=None, tuning=None):
+    """LayerNorm(A + R) * gamma + beta over rows; fp32 CUDA tensors (R may be None)."""
+    import torch
+    rows, cols = A.shape
+    O = out if out is not None else torch.empty_like(A)
+    ws = workspace if workspace is not None else new_workspace(cf_stitch_workspace_size(rows, cols), A.device,
+                                                               stream)
+    check(cf_stitch_add_layernorm(A, R, gamma, beta, O, rows, cols, eps, ws, ws.numel(), stream, tuning),
+          "cf_stitch_add_layernorm")
+    return O
+
+
+def stitch_batchnorm(A, gamma, beta, *, eps=1e-5, out=None, workspace=None, stream=None, tuning=None):
+    """(out, mean, var): BatchNorm of fp32 A [rows, cols] with its batch statistics."""
+    import torch
+    rows, cols = A.shape
+    O = out if out is not None else torch.empty_like(A)
+    mean = torch.empty(cols, dtype=torch.float32, device=A.device)
+    var = torch.empty(cols, dtype=torch.float32, device=A.device)
+    ws = workspace if workspace is not None else new_workspace(cf_stitch_batchnorm_workspace_size(rows, cols),
+                                                               A.device, stream)
+    check(cf_stitch_batchnorm(A, gamma, beta, O, mean, var, rows, cols, eps, ws, ws.numel(), stream, tuning),
+          "cf_stitch_batchnorm")
+    return O, mean, var
 
 
 def b2b_gemm(X, W1, W2, b1=None, *, op="softmax", alpha=1.0, out=None, workspace=None, stream=None,

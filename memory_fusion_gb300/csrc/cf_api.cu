@@ -357,25 +357,13 @@ cf_status cf_get_device_status(void *ws, cf_stream_t stream, int32_t *info) {
 // -------------------------------------------------------------------------
 // stitched subgraph
 // -------------------------------------------------------------------------
-cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *row_bias, float *out, int64_t rows,
-                                           int64_t cols, void *ws, size_t ws_bytes, cf_stream_t stream,
-                                           const cf_tuning *tuning) {
-    if (rows < 0 || cols < 0) return CF_ERR_INVALID_ARG;
-    if (rows == 0 || cols == 0) return CF_OK;
-    if (!A || !row_bias || !out || !ws) return CF_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(row_bias)) & 3u)
-        return CF_ERR_MISALIGNED;
-    if (cols > 262144) return CF_ERR_UNSUPPORTED;
-    if (ws_bytes < cf_stitch_workspace_size(rows, cols)) return CF_ERR_WORKSPACE_TOO_SMALL;
-    cf_tuning tz;
-    cf_tuning_default(&tz);
-    const cf_tuning &t = tuning ? *tuning : tz;
-    cf::DeviceInfo dev;
-    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
-    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
-
-    cf::StitchPlan p;
-    p.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out);
+// Row-task mapping of the stitched row subgraphs ([AStitch] "Adaptive thread
+// mapping"): rows of at most 32 float4 groups are packed several to a warp
+// (lanes per row = groups rounded up to a power of two); wider rows are split
+// over a cluster of C CTAs, C from the row count and the SM count.
+static cf_status plan_row_mapping(int64_t rows, int64_t cols, const cf_tuning &t, const cf::DeviceInfo &dev,
+                                  cf::StitchPlan *pp, int (*packed_bps)(int, bool)) {
+    cf::StitchPlan &p = *pp;
     p.pdl = t.disable_pdl == 0;
     p.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
     const int ng = int((cols + 3) / 4);
@@ -387,7 +375,7 @@ cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *row_bias
         p.lpr = next_pow2(ng);
         const int rows_per_cta_iter = 8 * (32 / p.lpr) * 4;
         const int64_t want = (rows + rows_per_cta_iter - 1) / rows_per_cta_iter;
-        int bps = cf::stitch_packed_blocks_per_sm(p.lpr, p.vec);
+        int bps = packed_bps(p.lpr, p.vec);
         if (bps <= 0) bps = 1;
         p.grid = int(std::min<int64_t>(want, int64_t(dev.sm_count) * bps));
     } else if (mapping == 2) {
@@ -415,15 +403,175 @@ cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *row_bias
     } else {
         return CF_ERR_INVALID_ARG;
     }
+    return CF_OK;
+}
+
+cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *row_bias, float *out, int64_t rows,
+                                           int64_t cols, void *ws, size_t ws_bytes, cf_stream_t stream,
+                                           const cf_tuning *tuning) {
+    if (rows < 0 || cols < 0) return CF_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return CF_OK;
+    if (!A || !row_bias || !out || !ws) return CF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(row_bias)) & 3u)
+        return CF_ERR_MISALIGNED;
+    if (cols > 262144) return CF_ERR_UNSUPPORTED;
+    if (ws_bytes < cf_stitch_workspace_size(rows, cols)) return CF_ERR_WORKSPACE_TOO_SMALL;
+    cf_tuning tz;
+    cf_tuning_default(&tz);
+    const cf_tuning &t = tuning ? *tuning : tz;
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+
+    cf::StitchPlan p;
+    p.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out);
+    cf_status st = plan_row_mapping(rows, cols, t, dev, &p, cf::stitch_packed_blocks_per_sm);
+    if (st != CF_OK) return st;
     cudaError_t e = cf::launch_stitch(p, A, row_bias, out, rows, cols, static_cast<uint32_t *>(ws),
                                       reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return CF_OK;
 }
 
+
 cf_status cf_stitch_rowreduce_broadcast(const float *A, const float *row_bias, float *out, int64_t rows,
                                         int64_t cols, void *ws, size_t ws_bytes, cf_stream_t stream) {
     return cf_stitch_rowreduce_broadcast_ex(A, row_bias, out, rows, cols, ws, ws_bytes, stream, nullptr);
+}
+
+cf_status cf_stitch_add_layernorm_ex(const float *A, const float *R, const float *gamma, const float *beta,
+                                     float *out, int64_t rows, int64_t cols, float eps, void *ws, size_t ws_bytes,
+                                     cf_stream_t stream, const cf_tuning *tuning) {
+    if (rows < 0 || cols < 0) return CF_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return CF_OK;
+    if (!A || !gamma || !beta || !out || !ws) return CF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(R) | reinterpret_cast<uintptr_t>(out) |
+         reinterpret_cast<uintptr_t>(gamma) | reinterpret_cast<uintptr_t>(beta)) & 3u)
+        return CF_ERR_MISALIGNED;
+    if (cols > 262144) return CF_ERR_UNSUPPORTED;
+    if (ws_bytes < cf_stitch_workspace_size(rows, cols)) return CF_ERR_WORKSPACE_TOO_SMALL;
+    cf_tuning tz;
+    cf_tuning_default(&tz);
+    const cf_tuning &t = tuning ? *tuning : tz;
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+    cf::StitchPlan p;
+    p.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out) && (R == nullptr || aligned16(R));
+    cf_status st = plan_row_mapping(rows, cols, t, dev, &p, cf::addln_packed_blocks_per_sm);
+    if (st != CF_OK) return st;
+    cudaError_t e = cf::launch_add_layernorm(p, A, R, gamma, beta, out, rows, cols, eps,
+                                             static_cast<uint32_t *>(ws), reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CF_OK;
+}
+
+cf_status cf_stitch_add_layernorm(const float *A, const float *R, const float *gamma, const float *beta,
+                                  float *out, int64_t rows, int64_t cols, float eps, void *ws, size_t ws_bytes,
+                                  cf_stream_t stream) {
+    return cf_stitch_add_layernorm_ex(A, R, gamma, beta, out, rows, cols, eps, ws, ws_bytes, stream, nullptr);
+}
+
+size_t cf_stitch_batchnorm_workspace_size(int64_t rows, int64_t cols) {
+    (void)rows;
+    (void)cols;
+    // under either mapping (the Global one may be forced for any shape): error
+    // word, arrive/depart counters, one float2 partial per CTA and strip column
+    return cf::kErrBytes + 256 + size_t(cf::kBnMaxGlobalCtas) * 128 * sizeof(float2);
+}
+
+// BatchNorm mapping ([AStitch] "Four stitching schemes", "Adaptive thread
+// mapping"): Regional when one CTA can hold every row of its columns,
+// otherwise Global -- one resident wave of CTAs (vertical packing) meeting at
+// an in-kernel barrier, as many row chunks per column strip as fit.
+static cf_status plan_batchnorm(int64_t rows, int64_t cols, const cf_tuning &t, const cf::DeviceInfo &dev,
+                                cf::BnPlan *pp) {
+    cf::BnPlan &p = *pp;
+    p.pdl = t.disable_pdl == 0;
+    p.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
+    p.extra_arrivals = t.extra_arrivals;
+    const int ng = int((cols + 3) / 4);
+    int mapping = t.stitch_mapping;
+    if (mapping == 0) mapping = rows <= cf::kBnRegionalMaxRows ? 3 : 4;
+    if (mapping == 3) {
+        if (rows > cf::kBnRegionalMaxRows) return CF_ERR_UNSUPPORTED;
+        p.mapping = 3;
+        p.rpt = next_pow2(int((rows + 7) / 8));
+        p.grid = (ng + 31) / 32;
+        return CF_OK;
+    }
+    if (mapping != 4) return CF_ERR_INVALID_ARG;
+    p.mapping = 4;
+    p.lpr = std::min(32, next_pow2(ng));
+    p.strips = (ng + p.lpr - 1) / p.lpr;
+    int bps = cf::bn_global_blocks_per_sm(p.lpr, p.vec);
+    if (bps <= 0) return CF_ERR_NOT_RESIDENT;
+    int cap = std::min(dev.sm_count * bps, cf::kBnMaxGlobalCtas);
+    if (t.max_clusters > 0) cap = std::min(cap, int(t.max_clusters));
+    if (p.strips > cap) return CF_ERR_UNSUPPORTED;
+    int chunks = cap / p.strips;
+    // a chunk of at least 32 rows per CTA (fewer chunks for short columns)
+    chunks = int(std::max<int64_t>(1, std::min<int64_t>(chunks, rows / 32)));
+    p.grid = chunks * p.strips;
+    return CF_OK;
+}
+
+cf_status cf_stitch_batchnorm_ex(const float *A, const float *gamma, const float *beta, float *out,
+                                 float *mean_out, float *var_out, int64_t rows, int64_t cols, float eps, void *ws,
+                                 size_t ws_bytes, cf_stream_t stream, const cf_tuning *tuning) {
+    if (rows < 0 || cols < 0) return CF_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return CF_OK;
+    if (!A || !gamma || !beta || !out || !ws) return CF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(gamma) |
+         reinterpret_cast<uintptr_t>(beta) | reinterpret_cast<uintptr_t>(mean_out) |
+         reinterpret_cast<uintptr_t>(var_out)) & 3u)
+        return CF_ERR_MISALIGNED;
+    if (!aligned16(ws)) return CF_ERR_MISALIGNED;
+    if (cols > (int64_t(1) << 30) || rows > (int64_t(1) << 40)) return CF_ERR_UNSUPPORTED;
+    if (ws_bytes < cf_stitch_batchnorm_workspace_size(rows, cols)) return CF_ERR_WORKSPACE_TOO_SMALL;
+    cf_tuning tz;
+    cf_tuning_default(&tz);
+    const cf_tuning &t = tuning ? *tuning : tz;
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+    cf::BnPlan p;
+    p.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out);
+    cf_status st = plan_batchnorm(rows, cols, t, dev, &p);
+    if (st != CF_OK) return st;
+    if (p.mapping == 4 && ws_bytes < cf::kErrBytes + 256 + size_t(p.grid) * 4 * p.lpr * sizeof(float2))
+        return CF_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    cudaError_t e = cf::launch_batchnorm(p, A, gamma, beta, out, mean_out, var_out, rows, cols, eps,
+                                         reinterpret_cast<uint32_t *>(wsb),
+                                         reinterpret_cast<uint32_t *>(wsb + cf::kErrBytes),
+                                         reinterpret_cast<float2 *>(wsb + cf::kErrBytes + 256),
+                                         reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CF_OK;
+}
+
+cf_status cf_stitch_batchnorm(const float *A, const float *gamma, const float *beta, float *out, float *mean_out,
+                              float *var_out, int64_t rows, int64_t cols, float eps, void *ws, size_t ws_bytes,
+                              cf_stream_t stream) {
+    return cf_stitch_batchnorm_ex(A, gamma, beta, out, mean_out, var_out, rows, cols, eps, ws, ws_bytes, stream,
+                                  nullptr);
+}
+
+cf_status cf_query_stitch_batchnorm_plan(int64_t rows, int64_t cols, const cf_tuning *tuning, int32_t *mapping,
+                                         int32_t *grid) {
+    if (rows <= 0 || cols <= 0 || !mapping || !grid) return CF_ERR_INVALID_ARG;
+    cf_tuning tz;
+    cf_tuning_default(&tz);
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+    cf::BnPlan p;
+    p.vec = cols % 4 == 0;
+    cf_status st = plan_batchnorm(rows, cols, tuning ? *tuning : tz, dev, &p);
+    *mapping = p.mapping;
+    *grid = p.grid;
+    return st;
 }
 
 // -------------------------------------------------------------------------

@@ -49,6 +49,36 @@ cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias
 int stitch_packed_blocks_per_sm(int lpr, bool vec);
 
 // --------------------------------------------------------------------------
+// stitched normalisation subgraphs (stitch_norm.cu)
+// --------------------------------------------------------------------------
+// add + LayerNorm over rows: mapping 1 packed (lpr), 2 split (cluster, per_thread)
+cudaError_t launch_add_layernorm(const StitchPlan &p, const float *A, const float *R, const float *gamma,
+                                 const float *beta, float *out, int64_t rows, int64_t cols, float eps, uint32_t *err,
+                                 cudaStream_t stream);
+int addln_packed_blocks_per_sm(int lpr, bool vec);
+
+// BatchNorm over columns: mapping 3 Regional (one CTA per 128-column strip
+// holding all rows, rpt rows per warp), 4 Global (strips x chunks resident
+// CTAs of 1024 threads, in-kernel grid barrier)
+struct BnPlan {
+    int mapping = 0;
+    int rpt = 0;          // Regional: rows per warp held in registers (1..32, power of two)
+    int lpr = 0;          // Global: 4-column groups per strip (1..32, power of two)
+    int strips = 0;       // Global: column strips
+    int grid = 0;
+    bool vec = false;
+    bool pdl = true;
+    int extra_arrivals = 0;
+    unsigned long long timeout_ns = 200000000ull;
+};
+cudaError_t launch_batchnorm(const BnPlan &p, const float *A, const float *gamma, const float *beta, float *out,
+                             float *mean_out, float *var_out, int64_t rows, int64_t cols, float eps, uint32_t *err,
+                             uint32_t *counters, float2 *partials, cudaStream_t stream);
+int bn_global_blocks_per_sm(int lpr, bool vec);
+constexpr int kBnRegionalMaxRows = 256;   // 8 warps x 32 rows in registers
+constexpr int kBnMaxGlobalCtas = 1024;    // bound of the partial buffer
+
+// --------------------------------------------------------------------------
 // row epilogue kernel of the unfused baseline (rowkernel.cu):
 //   op 0 LN, 1 GELU+LN, 2 softmax over fp32 rows of P -> bf16 Y
 // --------------------------------------------------------------------------

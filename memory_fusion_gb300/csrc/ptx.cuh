@@ -532,6 +532,21 @@ __device__ __forceinline__ void st_async_f4(uint32_t remote_addr, float x, float
                  : "memory");
 }
 
+// global loads under an L2 cache policy (createpolicy): data read twice by
+// a kernel is loaded evict-last the first time so the second read hits L2
+__device__ __forceinline__ float4 ld_f4_hint(const void *p, uint64_t policy) {
+    float4 v;
+    asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+__device__ __forceinline__ float ld_f32_hint(const float *p, uint64_t policy) {
+    float v;
+    asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(policy));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -67,6 +67,30 @@ __device__ __forceinline__ MeanM2 combine_counts(MeanM2 a, float na, MeanM2 b, f
     return r;
 }
 
+// As combine_counts, for partials that may be empty (count 0 on either side).
+__device__ __forceinline__ MeanM2 combine_counts_safe(MeanM2 a, float na, MeanM2 b, float nb) {
+    if (nb == 0.f) return a;
+    if (na == 0.f) return b;
+    return combine_counts(a, na, b, nb);
+}
+
+// level-1 butterfly of (count, mean, M2) partials over groups of `width`
+// lanes spaced `stride` apart (lower lane first: every lane folds the same
+// pairs in the same order, so all lanes end with bitwise-equal results)
+template <int kWidth, int kStride = 1>
+__device__ __forceinline__ void warp_meanm2(MeanM2 &v, float &n) {
+#pragma unroll
+    for (int off = kStride; off < kWidth * kStride; off <<= 1) {
+        MeanM2 o;
+        o.mean = __shfl_xor_sync(0xffffffffu, v.mean, off);
+        o.m2 = __shfl_xor_sync(0xffffffffu, v.m2, off);
+        const float no = __shfl_xor_sync(0xffffffffu, n, off);
+        const bool upper = (threadIdx.x & off) != 0;
+        v = upper ? combine_counts_safe(o, no, v, n) : combine_counts_safe(v, n, o, no);
+        n += no;
+    }
+}
+
 // (mean, M2) of 32 values held by one thread: two passes over registers.
 __device__ __forceinline__ MeanM2 chunk_mean_m2(const float (&x)[32]) {
     float s = 0.f;

@@ -1,0 +1,736 @@
+// stitch_norm.cu -- GEMM-free stitched normalisation subgraphs, each one
+// kernel ([AStitch] "Four stitching schemes", "Adaptive thread mapping"):
+//
+//  * add + LayerNorm over rows:  x = A + R;  out = (x - mean)/sqrt(var + eps)
+//    * gamma[col] + beta[col].  An elementwise producer (Local), two row
+//    reductions (mean, then the variance around it, two passes over values
+//    held in registers) and their broadcast; the column parameters are a
+//    one-to-many dependency, loaded once per thread and reused for every row
+//    it handles.  Thread mapping as for the stitched softmax: rows of up to
+//    128 columns packed several to a warp, wider rows split over the CTAs of a
+//    cluster with one DSMEM exchange of (mean, M2) per row.
+//
+//  * BatchNorm over columns (batch statistics):  out = (A - mean_col) /
+//    sqrt(var_col + eps) * gamma[col] + beta[col].  The statistic of a column
+//    depends on every row.
+//      - Regional (few rows): one CTA holds all rows of a 128-column strip in
+//        registers; warps combine their column partials in shared memory and
+//        normalise from registers.  One HBM pass.
+//      - Global (many rows): vertical packing -- one resident wave of CTAs,
+//        each owning a contiguous row range of a column strip; column
+//        partials go to global memory, an in-kernel grid barrier replaces
+//        the kernel boundary, every CTA folds all partials in one fixed order
+//        (so all hold bitwise-equal statistics) and normalises its rows,
+//        re-reading them from L2 (first read under an evict-last policy).
+//    The choice is the pages' block-locality check: a column's producers and
+//    consumers fit one block (Regional) or they do not (Global).
+//
+// Every wait is bounded by %globaltimer; a timeout records
+// CF_ERR_DEVICE_TIMEOUT in the workspace error word.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "cf_internal.h"
+#include "ptx.cuh"
+#include "rowstats.cuh"
+
+namespace cf {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;          // row slots per thread in flight
+constexpr int kGlobalThreads = 1024;
+
+// float4 group g of a row; zeros past `cols` (scalar path) or past `g1`
+template <bool VEC>
+__device__ __forceinline__ float4 load_group(const float *row, int g, int cols, bool ok) {
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!ok) return t;
+    if constexpr (VEC) {
+        t = __ldcs(reinterpret_cast<const float4 *>(row) + g);
+    } else {
+        const int c = 4 * g;
+        t.x = __ldcs(row + c);
+        if (c + 1 < cols) t.y = __ldcs(row + c + 1);
+        if (c + 2 < cols) t.z = __ldcs(row + c + 2);
+        if (c + 3 < cols) t.w = __ldcs(row + c + 3);
+    }
+    return t;
+}
+
+template <bool VEC>
+__device__ __forceinline__ void store_group(float *row, int g, int cols, float4 v) {
+    if constexpr (VEC) {
+        __stcs(reinterpret_cast<float4 *>(row) + g, v);
+    } else {
+        const int c = 4 * g;
+        __stcs(row + c, v.x);
+        if (c + 1 < cols) __stcs(row + c + 1, v.y);
+        if (c + 2 < cols) __stcs(row + c + 2, v.z);
+        if (c + 3 < cols) __stcs(row + c + 3, v.w);
+    }
+}
+
+__device__ __forceinline__ float4 ldg_group(const float *p, int g, int cols) {
+    float4 t;
+    const int c = 4 * g;
+    t.x = __ldg(p + c);
+    t.y = c + 1 < cols ? __ldg(p + c + 1) : 0.f;
+    t.z = c + 2 < cols ? __ldg(p + c + 2) : 0.f;
+    t.w = c + 3 < cols ? __ldg(p + c + 3) : 0.f;
+    return t;
+}
+
+__device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+
+// valid lanes of a 4-group starting at column c
+__device__ __forceinline__ float nvalid4(int c, int cols) { return float(max(0, min(4, cols - c))); }
+
+// ==========================================================================
+// add + LayerNorm, packed rows (LPR lanes per row, one 4-column group each)
+// ==========================================================================
+template <int LPR, bool VEC>
+__global__ void __launch_bounds__(kThreads) addln_packed_kernel(const float *__restrict__ A,
+                                                                const float *__restrict__ R,
+                                                                const float *__restrict__ gamma,
+                                                                const float *__restrict__ beta,
+                                                                float *__restrict__ out, int64_t rows, int cols,
+                                                                float eps) {
+    constexpr int RPW = 32 / LPR;
+    const int lane = threadIdx.x & 31;
+    const int g = lane & (LPR - 1);
+    const int rsub = lane / LPR;
+    const int c0 = 4 * g;
+    const bool gv = c0 < cols;
+    const float inv_n = 1.0f / float(cols);
+    const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+    constexpr int64_t kRowsPerIter = int64_t(RPW) * kUnroll;
+    ptx::griddep_wait();
+    // column parameters: loaded once, reused for every row this thread handles
+    const float4 ga = gv ? ldg_group(gamma, g, cols) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 be = gv ? ldg_group(beta, g, cols) : make_float4(0.f, 0.f, 0.f, 0.f);
+
+    for (int64_t base = warp * kRowsPerIter; base < rows; base += nwarps * kRowsPerIter) {
+        float4 x[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t r = base + u * RPW + rsub;
+            const bool ok = r < rows && gv;
+            x[u] = load_group<VEC>(A + r * cols, g, cols, ok);
+            if (R != nullptr) x[u] = add4(x[u], load_group<VEC>(R + r * cols, g, cols, ok));
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t r = base + u * RPW + rsub;
+            // two passes over the row held in registers: mean, then M2 about it
+            float s = (x[u].x + x[u].y) + (x[u].z + x[u].w);  // invalid lanes hold 0
+            s = warp_sum<LPR>(s);
+            const float mean = s * inv_n;
+            float4 d = make_float4(x[u].x - mean, x[u].y - mean, x[u].z - mean, x[u].w - mean);
+            if (!gv) d = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!VEC) {
+                if (c0 + 1 >= cols) d.y = 0.f;
+                if (c0 + 2 >= cols) d.z = 0.f;
+                if (c0 + 3 >= cols) d.w = 0.f;
+            }
+            float q = fmaf(d.x, d.x, fmaf(d.y, d.y, fmaf(d.z, d.z, d.w * d.w)));
+            q = warp_sum<LPR>(q);
+            const float rstd = rsqrtf(fmaf(q, inv_n, eps));
+            if (r < rows && gv) {
+                const float4 y = make_float4(fmaf(d.x * rstd, ga.x, be.x), fmaf(d.y * rstd, ga.y, be.y),
+                                             fmaf(d.z * rstd, ga.z, be.z), fmaf(d.w * rstd, ga.w, be.w));
+                store_group<VEC>(out + r * cols, g, cols, y);
+            }
+        }
+    }
+    ptx::griddep_launch_dependents();
+}
+
+// ==========================================================================
+// add + LayerNorm, one row per cluster of C CTAs (task splitting).  CTA
+// `rank` owns 4-column groups [rank*gpc, rank*gpc + gpc); each thread holds
+// up to V groups.  One DSMEM exchange of the CTA's (mean, M2) per row.
+// ==========================================================================
+template <int V, bool VEC>
+__global__ void __launch_bounds__(kThreads) addln_split_kernel(const float *__restrict__ A,
+                                                               const float *__restrict__ R,
+                                                               const float *__restrict__ gamma,
+                                                               const float *__restrict__ beta,
+                                                               float *__restrict__ out, int64_t rows, int cols,
+                                                               float eps, int gpc, uint32_t *err,
+                                                               unsigned long long tmo) {
+    __shared__ MeanM2 red[kThreads / 32];
+    __shared__ float redn[kThreads / 32];
+    __shared__ __align__(16) MeanM2 slot[2][16];  // per-CTA partials, by row parity
+    __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ uint32_t abort_flag;
+
+    const uint32_t C = ptx::cluster_nctarank();
+    const uint32_t rank = ptx::cluster_ctarank();
+    const uint32_t cid = ptx::cluster_id_x();
+    const uint32_t ncl = ptx::nclusters_x();
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int ng = (cols + 3) >> 2;
+    const int g0 = int(rank) * gpc;
+    const int g1 = min(ng, g0 + gpc);
+    volatile uint32_t *abort = &abort_flag;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&xbar[0]), 1);
+        ptx::mbar_init(ptx::smem_u32(&xbar[1]), 1);
+        abort_flag = 0u;
+        ptx::fence_mbarrier_init_cluster();
+    }
+    __syncthreads();
+    ptx::cluster_arrive_relaxed();
+    ptx::griddep_wait();
+
+    int it = 0;
+    for (int64_t row = cid; row < rows; row += ncl, ++it) {
+        const int par = it & 1;
+        const uint32_t xb = ptx::smem_u32(&xbar[par]);
+        const uint32_t xph = uint32_t(it >> 1) & 1u;
+        const float *a = A + row * cols;
+        const float *rr = R != nullptr ? R + row * cols : nullptr;
+        float4 x[V];
+        float nt = 0.f, st = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int g = g0 + threadIdx.x + v * kThreads;
+            const bool ok = g < g1;
+            x[v] = load_group<VEC>(a, g, cols, ok);
+            if (rr != nullptr) x[v] = add4(x[v], load_group<VEC>(rr, g, cols, ok));
+            if (ok) nt += nvalid4(4 * g, cols);
+            st += (x[v].x + x[v].y) + (x[v].z + x[v].w);
+        }
+        if (it == 0) ptx::cluster_wait_acquire();
+        // thread-local (mean, M2), two passes over the registers
+        const float mt = nt > 0.f ? st / nt : 0.f;
+        float qt = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int g = g0 + threadIdx.x + v * kThreads;
+            if (g < g1) {
+                const int c = 4 * g;
+                const float e[4] = {x[v].x - mt, x[v].y - mt, x[v].z - mt, x[v].w - mt};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (c + j < cols) qt = fmaf(e[j], e[j], qt);
+            }
+        }
+        // level 1: warp butterfly; level 2: the CTA's warps through shared memory
+        MeanM2 p{mt, qt};
+        float np = nt;
+        warp_meanm2<32>(p, np);
+        if (lane == 0) {
+            red[warp] = p;
+            redn[warp] = np;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            MeanM2 q = lane < kThreads / 32 ? red[lane] : MeanM2{0.f, 0.f};
+            float nq = lane < kThreads / 32 ? redn[lane] : 0.f;
+            warp_meanm2<kThreads / 32>(q, nq);
+            if (lane == 0 && !*abort) {
+                // level 3: this CTA's (mean, M2) into every CTA's slot
+                const uint32_t my_slot = ptx::smem_u32(&slot[par][rank]);
+                ptx::mbar_arrive_expect_tx(xb, C * 8u);
+                for (uint32_t r = 0; r < C; ++r)
+                    ptx::st_async_f2(ptx::mapa(my_slot, r), q.mean, q.m2, ptx::mapa(xb, r));
+            }
+        }
+        ptx::mbar_wait_bounded<true>(xb, xph, tmo, abort, err, 0x71000000u | uint32_t(par));
+        // fold the C partials in rank order; CTA r's count is known from its slice
+        MeanM2 tot = slot[par][0];
+        float ntot = float(min(cols, 4 * min(ng, gpc)));
+        for (uint32_t r = 1; r < C; ++r) {
+            const int ga = int(r) * gpc, gb = min(ng, ga + gpc);
+            const float nr = gb > ga ? float(min(cols, 4 * gb) - 4 * ga) : 0.f;
+            tot = combine_counts_safe(tot, ntot, slot[par][r], nr);
+            ntot += nr;
+        }
+        const float mean = tot.mean;
+        const float rstd = rsqrtf(fmaf(tot.m2, 1.0f / float(cols), eps));
+        float *o = out + row * cols;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int g = g0 + threadIdx.x + v * kThreads;
+            if (g < g1) {
+                const float4 ga = ldg_group(gamma, g, cols), be = ldg_group(beta, g, cols);
+                const float4 y = make_float4(fmaf((x[v].x - mean) * rstd, ga.x, be.x),
+                                             fmaf((x[v].y - mean) * rstd, ga.y, be.y),
+                                             fmaf((x[v].z - mean) * rstd, ga.z, be.z),
+                                             fmaf((x[v].w - mean) * rstd, ga.w, be.w));
+                store_group<VEC>(o, g, cols, y);
+            }
+        }
+        // slot[par] is written again two rows later: a peer sends for row it+2
+        // only after this CTA sent for row it+1, which its thread 0 does after
+        // the barrier above that every thread passes once done with row it
+    }
+    ptx::griddep_launch_dependents();
+    ptx::cluster_arrive_relaxed();
+    ptx::cluster_wait_acquire();
+}
+
+// ==========================================================================
+// BatchNorm, Regional: one CTA per 128-column strip holds all rows (warp w
+// takes rows w, w+8, ...; RPT of them) in registers.
+// ==========================================================================
+template <int RPT, bool VEC>
+__global__ void __launch_bounds__(kThreads) bn_regional_kernel(const float *__restrict__ A,
+                                                               const float *__restrict__ gamma,
+                                                               const float *__restrict__ beta,
+                                                               float *__restrict__ out, float *__restrict__ mean_out,
+                                                               float *__restrict__ var_out, int rows, int cols,
+                                                               float eps) {
+    __shared__ float2 red[kThreads / 32][128];
+    __shared__ float4 stat[32][3];  // per 4-group: mean, gamma*rstd, beta
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ng = (cols + 3) >> 2;
+    const int g = blockIdx.x * 32 + lane;
+    const bool gv = g < ng;
+    ptx::griddep_wait();
+    float4 x[RPT];
+    float n = 0.f;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+        const int r = warp + 8 * k;
+        const bool ok = gv && r < rows;
+        x[k] = load_group<VEC>(A + int64_t(r) * cols, g, cols, ok);
+        if (r < rows) n += 1.f;
+        s = add4(s, x[k]);
+    }
+    const float in = n > 0.f ? 1.0f / n : 0.f;
+    const float4 m = make_float4(s.x * in, s.y * in, s.z * in, s.w * in);
+    float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+        if (warp + 8 * k < rows) {
+            const float dx = x[k].x - m.x, dy = x[k].y - m.y, dz = x[k].z - m.z, dw = x[k].w - m.w;
+            q.x = fmaf(dx, dx, q.x);
+            q.y = fmaf(dy, dy, q.y);
+            q.z = fmaf(dz, dz, q.z);
+            q.w = fmaf(dw, dw, q.w);
+        }
+    }
+    red[warp][4 * lane + 0] = make_float2(m.x, q.x);
+    red[warp][4 * lane + 1] = make_float2(m.y, q.y);
+    red[warp][4 * lane + 2] = make_float2(m.z, q.z);
+    red[warp][4 * lane + 3] = make_float2(m.w, q.w);
+    __syncthreads();
+    if (threadIdx.x < 128) {
+        // fold the 8 warps' partials of column t in warp order
+        const int t = threadIdx.x;
+        const int col = blockIdx.x * 128 + t;
+        MeanM2 acc{red[0][t].x, red[0][t].y};
+        float na = float((rows + 7) / 8);  // warp w holds rows w, w + 8, ...
+        for (int w = 1; w < kThreads / 32; ++w) {
+            const float nw = float(rows > w ? (rows - w + 7) / 8 : 0);
+            acc = combine_counts_safe(acc, na, MeanM2{red[w][t].x, red[w][t].y}, nw);
+            na += nw;
+        }
+        const float var = acc.m2 / float(rows);
+        const float sc = rsqrtf(var + eps);
+        float *st = reinterpret_cast<float *>(&stat[0][0]);
+        if (col < cols) {
+            st[(t >> 2) * 12 + 0 + (t & 3)] = acc.mean;
+            st[(t >> 2) * 12 + 4 + (t & 3)] = __ldg(gamma + col) * sc;
+            st[(t >> 2) * 12 + 8 + (t & 3)] = __ldg(beta + col);
+            if (mean_out != nullptr) mean_out[col] = acc.mean;
+            if (var_out != nullptr) var_out[col] = var;
+        }
+    }
+    __syncthreads();
+    if (gv) {
+        const float4 mu = stat[lane][0], sc = stat[lane][1], be = stat[lane][2];
+#pragma unroll
+        for (int k = 0; k < RPT; ++k) {
+            const int r = warp + 8 * k;
+            if (r < rows) {
+                const float4 y = make_float4(fmaf(x[k].x - mu.x, sc.x, be.x), fmaf(x[k].y - mu.y, sc.y, be.y),
+                                             fmaf(x[k].z - mu.z, sc.z, be.z), fmaf(x[k].w - mu.w, sc.w, be.w));
+                store_group<VEC>(out + int64_t(r) * cols, g, cols, y);
+            }
+        }
+    }
+    ptx::griddep_launch_dependents();
+}
+
+// ==========================================================================
+// BatchNorm, Global: grid = strips x chunks CTAs, all resident (vertical
+// packing).  CTA b works on strip b % strips (LPR 4-column groups) and the
+// rows of chunk b / strips.
+// ==========================================================================
+template <int LPR, bool VEC>
+__global__ void __launch_bounds__(kGlobalThreads, 1) bn_global_kernel(
+    const float *__restrict__ A, const float *__restrict__ gamma, const float *__restrict__ beta,
+    float *__restrict__ out, float *__restrict__ mean_out, float *__restrict__ var_out, int64_t rows, int cols,
+    float eps, int strips, uint32_t *err, uint32_t *counters, float2 *partials, int extra_arrivals,
+    unsigned long long tmo) {
+    constexpr int RPW = 32 / LPR;          // row slots per warp
+    constexpr int kWarps = kGlobalThreads / 32;
+    constexpr int W = 4 * LPR;             // columns of a strip
+    __shared__ float2 red[kWarps][W];
+    __shared__ float redn[kWarps];
+    __shared__ float4 stat[LPR][3];        // per 4-group: mean, gamma*rstd, beta
+    __shared__ uint32_t abort_flag;
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ng = (cols + 3) >> 2;
+    const int strip = int(blockIdx.x) % strips;
+    const int chunk = int(blockIdx.x) / strips;
+    const int nchunks = int(gridDim.x) / strips;
+    const int sub = lane & (LPR - 1), rsub = lane / LPR;
+    const int g = strip * LPR + sub;
+    const bool gv = g < ng;
+    const int64_t r0 = rows * chunk / nchunks, r1 = rows * (chunk + 1) / nchunks;
+    const int slot = warp * RPW + rsub;
+    constexpr int S = kWarps * RPW;        // row slots of the CTA
+    volatile uint32_t *abort = &abort_flag;
+    if (threadIdx.x == 0) abort_flag = 0u;
+    ptx::griddep_wait();
+    const uint64_t keep = ptx::policy_evict_last();
+
+    // ---- pass 1: running (n, mean, M2) per column over this CTA's rows, in
+    // chunks of kUnroll rows (two passes over each chunk held in registers)
+    float n = 0.f;
+    MeanM2 run[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+    for (int64_t base = r0 + slot; base < r1; base += int64_t(S) * kUnroll) {
+        float4 x[kUnroll];
+        float nc = 0.f;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t r = base + int64_t(u) * S;
+            const bool ok = r < r1;
+            x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ok && gv) {
+                const float *row = A + r * cols;
+                if constexpr (VEC) {
+                    x[u] = ptx::ld_f4_hint(reinterpret_cast<const float4 *>(row) + g, keep);
+                } else {
+                    const int c = 4 * g;
+                    x[u].x = ptx::ld_f32_hint(row + c, keep);
+                    if (c + 1 < cols) x[u].y = ptx::ld_f32_hint(row + c + 1, keep);
+                    if (c + 2 < cols) x[u].z = ptx::ld_f32_hint(row + c + 2, keep);
+                    if (c + 3 < cols) x[u].w = ptx::ld_f32_hint(row + c + 3, keep);
+                }
+            }
+            if (ok) nc += 1.f;
+        }
+        if (nc == 0.f) break;
+        const float ic = 1.0f / nc;
+        float mc[4] = {0.f, 0.f, 0.f, 0.f}, qc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            mc[0] += x[u].x;
+            mc[1] += x[u].y;
+            mc[2] += x[u].z;
+            mc[3] += x[u].w;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mc[j] *= ic;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            if (base + int64_t(u) * S < r1) {
+                const float d[4] = {x[u].x - mc[0], x[u].y - mc[1], x[u].z - mc[2], x[u].w - mc[3]};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) qc[j] = fmaf(d[j], d[j], qc[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) run[j] = combine_counts_safe(run[j], n, MeanM2{mc[j], qc[j]}, nc);
+        n += nc;
+    }
+    // ---- CTA reduce: row slots of a warp (lanes LPR apart), then the warps
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float nj = n;
+        warp_meanm2<RPW, LPR>(run[j], nj);
+        if (j == 3) n = nj;
+    }
+    if (rsub == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) red[warp][4 * sub + j] = make_float2(run[j].mean, run[j].m2);
+        if (sub == 0) redn[warp] = n;
+    }
+    __syncthreads();
+    if (threadIdx.x < W) {
+        const int t = threadIdx.x;
+        MeanM2 acc{red[0][t].x, red[0][t].y};
+        float na = redn[0];
+        for (int w = 1; w < kWarps; ++w) {
+            acc = combine_counts_safe(acc, na, MeanM2{red[w][t].x, red[w][t].y}, redn[w]);
+            na += redn[w];
+        }
+        // this CTA's partial of column strip*W + t (its count follows from r0, r1)
+        partials[size_t(blockIdx.x) * W + t] = make_float2(acc.mean, acc.m2);
+        __threadfence();
+    }
+    __syncthreads();
+    // ---- grid barrier: every CTA of the launch is resident (host-checked)
+    if (threadIdx.x == 0) {
+        const uint32_t want = gridDim.x + uint32_t(extra_arrivals);
+        ptx::red_add_release_gpu(counters, 1u);
+        const uint64_t t0 = ptx::globaltimer();
+        uint32_t spins = 0;
+        while (ptx::ld_acquire_gpu(counters) < want) {
+            if ((++spins & 63u) == 0u) {
+                if (ptx::globaltimer() - t0 > tmo) {
+                    *abort = 1u;
+                    ptx::record_error(err, 7u /*CF_ERR_DEVICE_TIMEOUT*/, 0x72000000u | blockIdx.x);
+                    break;
+                }
+                if (ptx::ld_relaxed_gpu(err) != 0u) {  // another CTA gave up: do not wait out the bound
+                    *abort = 1u;
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (*abort) {
+        ptx::griddep_launch_dependents();
+        return;
+    }
+    // ---- fold every chunk's partial of the strip's columns, one warp per
+    // column, lanes over chunks, in one fixed order (bitwise-equal in all CTAs)
+    for (int t = warp; t < W; t += kWarps) {
+        MeanM2 acc{0.f, 0.f};
+        float na = 0.f;
+        for (int c = lane; c < nchunks; c += 32) {
+            const float2 pc = ptx::ld_relaxed_gpu_f2(partials + size_t(c * strips + strip) * W + t);
+            const float nc = float(rows * (c + 1) / nchunks - rows * c / nchunks);
+            acc = combine_counts_safe(acc, na, MeanM2{pc.x, pc.y}, nc);
+            na += nc;
+        }
+        warp_meanm2<32>(acc, na);
+        if (lane == 0) {
+            const int col = strip * W + t;
+            const float var = na > 0.f ? acc.m2 / na : 0.f;
+            float *st = reinterpret_cast<float *>(&stat[0][0]);
+            if (col < cols) {
+                st[(t >> 2) * 12 + 0 + (t & 3)] = acc.mean;
+                st[(t >> 2) * 12 + 4 + (t & 3)] = __ldg(gamma + col) * rsqrtf(var + eps);
+                st[(t >> 2) * 12 + 8 + (t & 3)] = __ldg(beta + col);
+                if (chunk == 0) {
+                    if (mean_out != nullptr) mean_out[col] = acc.mean;
+                    if (var_out != nullptr) var_out[col] = var;
+                }
+            } else {
+                st[(t >> 2) * 12 + 0 + (t & 3)] = 0.f;
+                st[(t >> 2) * 12 + 4 + (t & 3)] = 0.f;
+                st[(t >> 2) * 12 + 8 + (t & 3)] = 0.f;
+            }
+        }
+    }
+    __syncthreads();
+    // ---- departure: the last CTA to leave the barrier resets the counters
+    if (threadIdx.x == 0) {
+        const uint32_t d = ptx::atom_add_relaxed_gpu(counters + 1, 1u);
+        if (d == gridDim.x - 1u) {
+            ptx::st_relaxed_gpu(counters, 0u);
+            ptx::st_relaxed_gpu(counters + 1, 0u);
+        }
+    }
+    // ---- pass 2: normalise the same rows (an L2 hit for rows kept evict-last)
+    const float4 mu = gv ? stat[sub][0] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 sc = gv ? stat[sub][1] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 be = gv ? stat[sub][2] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (gv) {
+        for (int64_t base = r0 + slot; base < r1; base += int64_t(S) * kUnroll) {
+            float4 x[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t r = base + int64_t(u) * S;
+                x[u] = load_group<VEC>(A + r * cols, g, cols, r < r1);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t r = base + int64_t(u) * S;
+                if (r < r1) {
+                    const float4 y = make_float4(fmaf(x[u].x - mu.x, sc.x, be.x), fmaf(x[u].y - mu.y, sc.y, be.y),
+                                                 fmaf(x[u].z - mu.z, sc.z, be.z), fmaf(x[u].w - mu.w, sc.w, be.w));
+                    store_group<VEC>(out + r * cols, g, cols, y);
+                }
+            }
+        }
+    }
+    ptx::griddep_launch_dependents();
+}
+
+// --------------------------------------------------------------------------
+// kernel tables
+// --------------------------------------------------------------------------
+template <int LPR>
+void *addln_packed_fn(bool vec) {
+    return vec ? reinterpret_cast<void *>(&addln_packed_kernel<LPR, true>)
+               : reinterpret_cast<void *>(&addln_packed_kernel<LPR, false>);
+}
+void *addln_packed_kernel_for(int lpr, bool vec) {
+    switch (lpr) {
+        case 1: return addln_packed_fn<1>(vec);
+        case 2: return addln_packed_fn<2>(vec);
+        case 4: return addln_packed_fn<4>(vec);
+        case 8: return addln_packed_fn<8>(vec);
+        case 16: return addln_packed_fn<16>(vec);
+        case 32: return addln_packed_fn<32>(vec);
+        default: return nullptr;
+    }
+}
+template <int V>
+void *addln_split_fn(bool vec) {
+    return vec ? reinterpret_cast<void *>(&addln_split_kernel<V, true>)
+               : reinterpret_cast<void *>(&addln_split_kernel<V, false>);
+}
+void *addln_split_kernel_for(int v, bool vec) {
+    switch (v) {
+        case 1: return addln_split_fn<1>(vec);
+        case 2: return addln_split_fn<2>(vec);
+        case 4: return addln_split_fn<4>(vec);
+        case 8: return addln_split_fn<8>(vec);
+        case 16: return addln_split_fn<16>(vec);
+        default: return nullptr;
+    }
+}
+template <int RPT>
+void *bn_regional_fn(bool vec) {
+    return vec ? reinterpret_cast<void *>(&bn_regional_kernel<RPT, true>)
+               : reinterpret_cast<void *>(&bn_regional_kernel<RPT, false>);
+}
+void *bn_regional_kernel_for(int rpt, bool vec) {
+    switch (rpt) {
+        case 1: return bn_regional_fn<1>(vec);
+        case 2: return bn_regional_fn<2>(vec);
+        case 4: return bn_regional_fn<4>(vec);
+        case 8: return bn_regional_fn<8>(vec);
+        case 16: return bn_regional_fn<16>(vec);
+        case 32: return bn_regional_fn<32>(vec);
+        default: return nullptr;
+    }
+}
+template <int LPR>
+void *bn_global_fn(bool vec) {
+    return vec ? reinterpret_cast<void *>(&bn_global_kernel<LPR, true>)
+               : reinterpret_cast<void *>(&bn_global_kernel<LPR, false>);
+}
+void *bn_global_kernel_for(int lpr, bool vec) {
+    switch (lpr) {
+        case 1: return bn_global_fn<1>(vec);
+        case 2: return bn_global_fn<2>(vec);
+        case 4: return bn_global_fn<4>(vec);
+        case 8: return bn_global_fn<8>(vec);
+        case 16: return bn_global_fn<16>(vec);
+        case 32: return bn_global_fn<32>(vec);
+        default: return nullptr;
+    }
+}
+
+cudaError_t launch_plain(void *fn, int grid, int threads, bool pdl, cudaStream_t stream, void **args) {
+    if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+int blocks_per_sm_cached(void *fn, int threads, int key) {
+    static int cache[64][64] = {};
+    int dev = 0;
+    if (!fn || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || key < 0 || key >= 64) return 0;
+    int &c = cache[dev][key];
+    if (c == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        c = n;
+    }
+    return c;
+}
+
+int log2i(int v) {
+    int l = 0;
+    while ((1 << l) < v) ++l;
+    return l;
+}
+
+}  // namespace
+
+int addln_packed_blocks_per_sm(int lpr, bool vec) {
+    return blocks_per_sm_cached(addln_packed_kernel_for(lpr, vec), kThreads, log2i(lpr) * 2 + (vec ? 1 : 0));
+}
+
+int bn_global_blocks_per_sm(int lpr, bool vec) {
+    return blocks_per_sm_cached(bn_global_kernel_for(lpr, vec), kGlobalThreads, 32 + log2i(lpr) * 2 + (vec ? 1 : 0));
+}
+
+cudaError_t launch_add_layernorm(const StitchPlan &p, const float *A, const float *R, const float *gamma,
+                                 const float *beta, float *out, int64_t rows, int64_t cols, float eps, uint32_t *err,
+                                 cudaStream_t stream) {
+    int icols = int(cols);
+    if (p.mapping == 1) {
+        void *args[] = {(void *)&A, (void *)&R, (void *)&gamma, (void *)&beta, (void *)&out, (void *)&rows,
+                        (void *)&icols, (void *)&eps};
+        return launch_plain(addln_packed_kernel_for(p.lpr, p.vec), p.grid, kThreads, p.pdl, stream, args);
+    }
+    if (p.mapping != 2) return cudaErrorInvalidValue;
+    void *fn = addln_split_kernel_for(p.per_thread, p.vec);
+    if (!fn) return cudaErrorInvalidValue;
+    if (p.cluster > 8) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    const int ng = int((cols + 3) / 4);
+    int gpc = (ng + p.cluster - 1) / p.cluster;
+    unsigned long long tmo = p.timeout_ns;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.pdl ? 2 : 1;
+    void *args[] = {(void *)&A, (void *)&R, (void *)&gamma, (void *)&beta, (void *)&out, (void *)&rows,
+                    (void *)&icols, (void *)&eps, (void *)&gpc, (void *)&err, (void *)&tmo};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t launch_batchnorm(const BnPlan &p, const float *A, const float *gamma, const float *beta, float *out,
+                             float *mean_out, float *var_out, int64_t rows, int64_t cols, float eps, uint32_t *err,
+                             uint32_t *counters, float2 *partials, cudaStream_t stream) {
+    int icols = int(cols);
+    if (p.mapping == 3) {
+        int irows = int(rows);
+        void *args[] = {(void *)&A, (void *)&gamma, (void *)&beta, (void *)&out, (void *)&mean_out,
+                        (void *)&var_out, (void *)&irows, (void *)&icols, (void *)&eps};
+        return launch_plain(bn_regional_kernel_for(p.rpt, p.vec), p.grid, kThreads, p.pdl, stream, args);
+    }
+    if (p.mapping != 4) return cudaErrorInvalidValue;
+    int strips = p.strips;
+    int extra = p.extra_arrivals;
+    unsigned long long tmo = p.timeout_ns;
+    void *args[] = {(void *)&A, (void *)&gamma, (void *)&beta, (void *)&out, (void *)&mean_out, (void *)&var_out,
+                    (void *)&rows, (void *)&icols, (void *)&eps, (void *)&strips, (void *)&err, (void *)&counters,
+                    (void *)&partials, (void *)&extra, (void *)&tmo};
+    return launch_plain(bn_global_kernel_for(p.lpr, p.vec), p.grid, kGlobalThreads, p.pdl, stream, args);
+}
+
+}  // namespace cf

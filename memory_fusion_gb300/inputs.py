@@ -15,6 +15,9 @@ made in argument order):
 * GEMM + softmax workloads: X, W as above; no bias unless asked.
 * Stitched workload: A[rows, cols] ~ N(0, 2) fp32, then b[rows] ~ U(-1, 1)
   fp32; the generator is re-seeded for every shape.
+* Stitched normalisation workloads: A[rows, cols] ~ N(0, 2) fp32, then (add
+  + LayerNorm only) R[rows, cols] ~ N(0, 1), then gamma[cols] ~ N(1, 0.1),
+  beta[cols] ~ N(0, 0.1) fp32.
 * Back-to-back GEMM workloads: X[M,K], W1[K,N1], W2[N1,N2] (bf16, N(0,
   x_std), N(0, w1_std), N(0, w2_std)), then b1[N1] ~ N(0, b1_std) fp32 (not
   drawn when b1_std is None).
@@ -34,6 +37,8 @@ __all__ = [
     "GemmWorkload",
     "StitchWorkload",
     "B2bWorkload",
+    "StitchNormWorkload",
+    "stitch_norm_inputs",
     "b2b_inputs",
     "WORKLOADS",
     "gemm_inputs",
@@ -112,6 +117,24 @@ class StitchWorkload:
 
 
 @dataclass(frozen=True)
+class StitchNormWorkload:
+    name: str
+    kind: str              # "add_layernorm" | "batchnorm"
+    rows: int
+    cols: int
+    seed: int
+    eps: float = 1e-5
+    description: str = ""
+
+    @property
+    def unavoidable_bytes(self) -> int:
+        """Inputs and outputs once each: A (and R), out, gamma, beta (and the
+        batch mean / variance BatchNorm returns)."""
+        per = 12 if self.kind == "add_layernorm" else 8
+        return per * self.rows * self.cols + (8 if self.kind == "add_layernorm" else 16) * self.cols
+
+
+@dataclass(frozen=True)
 class B2bWorkload:
     name: str
     op: str                # "softmax" | "gelu_tanh"
@@ -184,6 +207,18 @@ WORKLOADS = {
         b1_std=0.1,
         description="B2BGEMM with bias+GELU(tanh) between the GEMMs, MLP-shaped: "
                     "X[16384,1024] W1[1024,2048] W2[2048,128]"),
+    "addln_750000x32": StitchNormWorkload(
+        "addln_750000x32", "add_layernorm", 750000, 32, 10,
+        description="stitched add + LayerNorm over rows, very many tiny rows"),
+    "addln_64x30000": StitchNormWorkload(
+        "addln_64x30000", "add_layernorm", 64, 30000, 11,
+        description="stitched add + LayerNorm over rows, very few huge rows"),
+    "bn_750000x32": StitchNormWorkload(
+        "bn_750000x32", "batchnorm", 750000, 32, 12,
+        description="stitched BatchNorm over 750000 rows (Global scheme: grid barrier, vertical packing)"),
+    "bn_64x30000": StitchNormWorkload(
+        "bn_64x30000", "batchnorm", 64, 30000, 13,
+        description="stitched BatchNorm over 64 rows (Regional scheme: one block per column strip)"),
     "stitch_750000x32": StitchWorkload(
         "stitch_750000x32", 750000, 32, 3,
         description="stitched y=A^3+b[row] -> row softmax, very many tiny rows"),
@@ -237,10 +272,23 @@ def b2b_inputs(M: int, K: int, N1: int, N2: int, seed: int, *, x_std: float = 1.
     return out
 
 
+def stitch_norm_inputs(rows: int, cols: int, seed: int, *, with_R: bool = True) -> dict:
+    """A ~ N(0, 2) [rows, cols], R ~ N(0, 1) (if with_R), gamma ~ N(1, 0.1),
+    beta ~ N(0, 0.1) [cols]; all fp32."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = {"A": _normal(rng, (rows, cols), 2.0)}
+    out["R"] = _normal(rng, (rows, cols), 1.0) if with_R else None
+    out["gamma"] = _normal(rng, (cols,), 0.1, 1.0)
+    out["beta"] = _normal(rng, (cols,), 0.1)
+    return out
+
+
 def workload_inputs(name: str) -> dict:
     w = WORKLOADS[name]
     if isinstance(w, StitchWorkload):
         return stitch_inputs(w.rows, w.cols, w.seed)
+    if isinstance(w, StitchNormWorkload):
+        return stitch_norm_inputs(w.rows, w.cols, w.seed, with_R=w.kind == "add_layernorm")
     if isinstance(w, B2bWorkload):
         return b2b_inputs(w.M, w.K, w.N1, w.N2, w.seed, x_std=w.x_std, w1_std=w.w1_std, w2_std=w.w2_std,
                           b1_std=w.b1_std)
