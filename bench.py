@@ -130,7 +130,8 @@ def roofline_time_s(w, peaks):
     return max(t_flop, t_byte), ("tensor" if t_flop >= t_byte else "hbm")
 
 
-KERNEL_TU = {"gemm_fused_kernel": "gemm_fused.cu", "stitch_": "stitch.cu", "b2b_kernel": "b2b.cu"}
+KERNEL_TU = {"gemm_fused_kernel": "gemm_fused.cu", "stitch_": "stitch.cu", "b2b_kernel": "b2b.cu",
+             "addln_": "stitch_norm.cu", "bn_": "stitch_norm.cu"}
 
 
 def kernel_source_hash(kernel):
@@ -445,6 +446,9 @@ def per_workload(torch, cf, peaks, device, names):
         if isinstance(w, inputs.B2bWorkload):
             out[name] = b2b_numbers(torch, cf, w, peaks, device, l2)
             continue
+        if isinstance(w, inputs.StitchNormWorkload):
+            out[name] = stitch_norm_numbers(torch, cf, w, peaks, device, l2)
+            continue
         nsets = max(1, min(32, math.ceil(3 * l2 / bytes_per_set(w))))
         r = FusedRunner(torch, cf, w, nsets, device=device)
         reps = max(nsets, 20 if w.flops > 1e11 else 400)
@@ -504,6 +508,62 @@ def stitch_numbers(torch, cf, w, peaks, device, l2):
     gbs = w.unavoidable_bytes / t1 / 1e9
     return {"us": round(t1 * 1e6, 2), "gbs": round(gbs, 1), "bound": "hbm",
             "roofline_frac": round(gbs / peaks["hbm_gbs"], 3), "buffer_sets": nsets}
+
+
+class StitchNormRunner:
+    """Device buffers of a stitched normalisation workload over `nsets`
+    rotating sets, launched through the public C ABI."""
+
+    def __init__(self, torch, cf, w, nsets, seed_offset=0, device="cuda"):
+        self.torch, self.cf, self.w = torch, cf, w
+        seed = w.seed if seed_offset == 0 else mdist.seed_for(w.seed, seed_offset)
+        d = inputs.stitch_norm_inputs(w.rows, w.cols, seed, with_R=w.kind == "add_layernorm")
+        self.host = d
+        A = torch.from_numpy(d["A"]).to(device)
+        R = torch.from_numpy(d["R"]).to(device) if d["R"] is not None else None
+        self.g = torch.from_numpy(d["gamma"]).to(device)
+        self.b = torch.from_numpy(d["beta"]).to(device)
+        self.sets = [{"A": A if i == 0 else A.clone(), "R": (R if i == 0 else R.clone()) if R is not None else None,
+                      "out": torch.empty_like(A)} for i in range(nsets)]
+        self.mean = torch.empty(w.cols, device=device)
+        self.var = torch.empty(w.cols, device=device)
+        if w.kind == "add_layernorm":
+            self.ws_bytes = cf.cf_stitch_workspace_size(w.rows, w.cols)
+        else:
+            self.ws_bytes = cf.cf_stitch_batchnorm_workspace_size(w.rows, w.cols)
+        self.ws = cf.new_workspace(self.ws_bytes, device)
+
+    def launch(self, i, stream=None):
+        w, s, cf = self.w, self.sets[i % len(self.sets)], self.cf
+        if w.kind == "add_layernorm":
+            st = cf.cf_stitch_add_layernorm(s["A"], s["R"], self.g, self.b, s["out"], w.rows, w.cols, w.eps, self.ws,
+                                            self.ws_bytes, stream)
+        else:
+            st = cf.cf_stitch_batchnorm(s["A"], self.g, self.b, s["out"], self.mean, self.var, w.rows, w.cols, w.eps,
+                                        self.ws, self.ws_bytes, stream)
+        cf.check(st, "stitched normalisation launch")
+
+
+def stitch_norm_kernel_name(cf, w):
+    if w.kind == "add_layernorm":
+        return "addln_packed_kernel" if (w.cols + 3) // 4 <= 32 else "addln_split_kernel"
+    _, mapping, _ = cf.cf_query_stitch_batchnorm_plan(w.rows, w.cols)
+    return "bn_regional_kernel" if mapping == 3 else "bn_global_kernel"
+
+
+def stitch_norm_numbers(torch, cf, w, peaks, device, l2):
+    nsets = max(1, min(32, math.ceil(3 * l2 / w.unavoidable_bytes)))
+    r = StitchNormRunner(torch, cf, w, nsets, device=device)
+    reps = max(nsets, 200)
+    t, n, _ = time_steps(torch, r, reps, 3, lambda: None, graph_len=reps)
+    t1 = t / n
+    gbs = w.unavoidable_bytes / t1 / 1e9
+    out = {"us": round(t1 * 1e6, 2), "gbs": round(gbs, 1), "bound": "hbm",
+           "roofline_frac": round(gbs / peaks["hbm_gbs"], 3), "buffer_sets": nsets,
+           "kernel": stitch_norm_kernel_name(cf, w)}
+    del r
+    torch.cuda.empty_cache()
+    return out
 
 
 def cpu_oracle_sample(w, budget_s=10.0, max_rows=None):
@@ -635,31 +695,39 @@ def run_stitch(args):
     peaks, peak_src = load_peaks()
     w = inputs.WORKLOADS[args.workload]
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    d = inputs.stitch_inputs(w.rows, w.cols, mdist.seed_for(w.seed, rank))
     nsets = max(1, min(32, math.ceil(3 * l2 / w.unavoidable_bytes)))
-    A = [torch.from_numpy(d["A"]).to(device) for _ in range(nsets)]
-    b = torch.from_numpy(d["row_bias"]).to(device)
-    O = [torch.empty_like(A[0]) for _ in range(nsets)]
-    wsb = cf.cf_stitch_workspace_size(w.rows, w.cols)
-    ws = cf.new_workspace(wsb, device)
+    if isinstance(w, inputs.StitchNormWorkload):
+        runner = StitchNormRunner(torch, cf, w, nsets, seed_offset=rank, device=device)
+        kernel = stitch_norm_kernel_name(cf, w)
+        metric = f"stitched {w.kind} HBM GB/s"
+    else:
+        d = inputs.stitch_inputs(w.rows, w.cols, mdist.seed_for(w.seed, rank))
+        A = [torch.from_numpy(d["A"]).to(device) for _ in range(nsets)]
+        b = torch.from_numpy(d["row_bias"]).to(device)
+        O = [torch.empty_like(A[0]) for _ in range(nsets)]
+        wsb = cf.cf_stitch_workspace_size(w.rows, w.cols)
+        ws = cf.new_workspace(wsb, device)
 
-    class R:
-        def launch(self, i, stream=None):
-            cf.check(cf.cf_stitch_rowreduce_broadcast(A[i % nsets], b, O[i % nsets], w.rows, w.cols, ws, wsb,
-                                                      stream))
+        class R:
+            def launch(self, i, stream=None):
+                cf.check(cf.cf_stitch_rowreduce_broadcast(A[i % nsets], b, O[i % nsets], w.rows, w.cols, ws, wsb,
+                                                          stream))
+
+        runner = R()
+        # the planner's rule: rows of at most 32 float4 groups go packed, wider ones split
+        kernel = "stitch_packed_kernel" if (w.cols + 3) // 4 <= 32 else "stitch_split_kernel"
+        metric = "stitched reduce->broadcast HBM GB/s"
 
     props = torch.cuda.get_device_properties(device)
     gpu_id = str(getattr(props, "uuid", local))
     if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
         gpu_id = "GPU-" + gpu_id
     sampler = ClockSampler(gpu_id if gpu_id.startswith("GPU-") else str(local))
-    t, n, clocks = time_steps(torch, R(), args.steps, args.warmup, ranks.barrier, sampler)
+    t, n, clocks = time_steps(torch, runner, args.steps, args.warmup, ranks.barrier, sampler)
     t = ranks.max(t)
     gbs = mdist.job_throughput(w.unavoidable_bytes * n, ws_, t) / 1e9
-    # the planner's rule: rows of at most 32 float4 groups go packed, wider ones split
-    kernel = "stitch_packed_kernel" if (w.cols + 3) // 4 <= 32 else "stitch_split_kernel"
     if rank == 0:
-        print(json.dumps({"metric": "stitched reduce->broadcast HBM GB/s", "value": round(gbs, 1), "unit": "GB/s",
+        print(json.dumps({"metric": metric, "value": round(gbs, 1), "unit": "GB/s",
                           "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
                           "ms_per_step": round(t / n * 1e3, 6), "higher_is_better": True, "scaling": "weak",
                           "dtype": "f32", "data": "synthetic (seeded, shaped like the page workload)",
@@ -723,11 +791,57 @@ def run_b2b(args):
 # ---------------------------------------------------------------------------
 # reference arm: the fp64 CPU oracle
 # ---------------------------------------------------------------------------
+def run_reference_stitched(args, w):
+    """The oracle on a stitched workload: GB/s over the bytes of the rows it
+    processed (a row sample per step; BatchNorm's column statistics need every
+    row, so a step there is the whole matrix)."""
+    import oracle
+    d = inputs.workload_inputs(w.name)
+    rng = np.random.Generator(np.random.PCG64(1))
+    per_row = w.unavoidable_bytes / w.rows
+    n_rows = min(w.rows, max(1, int(2e6 // w.cols)))
+    if isinstance(w, inputs.StitchNormWorkload) and w.kind == "batchnorm":
+        n_rows = w.rows
+
+        def step():
+            oracle.stitch_batchnorm(d["A"], d["gamma"], d["beta"], w.eps)
+        sample = f"the whole {w.rows}x{w.cols} matrix per step (fp64 numpy oracle)"
+    else:
+        def step():
+            rows = np.sort(rng.choice(w.rows, size=n_rows, replace=False))
+            if isinstance(w, inputs.StitchNormWorkload):
+                oracle.stitch_add_layernorm(d["A"], d["R"], d["gamma"], d["beta"], w.eps, rows=rows)
+            else:
+                oracle.stitch_rowreduce_broadcast(d["A"], d["row_bias"], rows=rows)
+        sample = f"{n_rows} random whole rows of {w.name} per step (fp64 numpy oracle)"
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = time.perf_counter() - t0
+    v = per_row * n_rows * args.steps / t / 1e9
+    metric = (f"stitched {w.kind} HBM GB/s" if isinstance(w, inputs.StitchNormWorkload)
+              else "stitched reduce->broadcast HBM GB/s")
+    print(json.dumps({
+        "impl": "reference", "metric": metric, "value": round(v, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def run_reference(args):
     ws_, rank, _ = dist_env()
     if rank != 0:
         return
     w = inputs.WORKLOADS[args.workload]
+    if isinstance(w, (inputs.StitchWorkload, inputs.StitchNormWorkload)):
+        run_reference_stitched(args, w)
+        return
     import oracle
     d = inputs.workload_inputs(w.name)
     rows_per_step = 128
@@ -771,11 +885,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    stitched = isinstance(inputs.WORKLOADS[args.workload], inputs.StitchWorkload)
+    stitched = isinstance(inputs.WORKLOADS[args.workload], (inputs.StitchWorkload, inputs.StitchNormWorkload))
     if args.impl == "reference":
-        if stitched:
-            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times GEMM workloads"}))
-            return
         run_reference(args)
     elif stitched:
         run_stitch(args)
