@@ -107,6 +107,22 @@ bool make_tmap_f32_store(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_
     return r == CUDA_SUCCESS;
 }
 
+// 2-D fp32 tensor map over a row-major [rows, cols] matrix, box (box_cols x
+// box_rows), no swizzle: loads read zeros outside, stores are clipped
+bool make_tmap_f32(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                   uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // -------------------------------------------------------------------------
 // occupancy cache: max co-resident clusters for (device, kind, cluster, smem)
 // -------------------------------------------------------------------------
@@ -493,6 +509,7 @@ static cf_status plan_batchnorm(int64_t rows, int64_t cols, const cf_tuning &t, 
     const int ng = int((cols + 3) / 4);
     int mapping = t.stitch_mapping;
     if (mapping == 0) mapping = rows <= cf::kBnRegionalMaxRows ? 3 : 4;
+    if (mapping == 5 || mapping == 6) mapping = 4;  // Global without TMA streaming (5) or with tiled copies (6)
     if (mapping == 3) {
         if (rows > cf::kBnRegionalMaxRows) return CF_ERR_UNSUPPORTED;
         p.mapping = 3;
@@ -504,7 +521,9 @@ static cf_status plan_batchnorm(int64_t rows, int64_t cols, const cf_tuning &t, 
     p.mapping = 4;
     p.lpr = std::min(32, next_pow2(ng));
     p.strips = (ng + p.lpr - 1) / p.lpr;
-    int bps = cf::bn_global_blocks_per_sm(p.lpr, p.vec);
+    // 128-bit rows stream through shared memory by TMA (rows addressable as int32)
+    p.tma = p.vec && t.stitch_mapping != 5 && rows < (int64_t(1) << 31);
+    int bps = p.tma ? cf::bn_tma_blocks_per_sm(p.lpr) : cf::bn_global_blocks_per_sm(p.lpr, p.vec);
     if (bps <= 0) return CF_ERR_NOT_RESIDENT;
     int cap = std::min(dev.sm_count * bps, cf::kBnMaxGlobalCtas);
     if (t.max_clusters > 0) cap = std::min(cap, int(t.max_clusters));
@@ -513,6 +532,11 @@ static cf_status plan_batchnorm(int64_t rows, int64_t cols, const cf_tuning &t, 
     // a chunk of at least 32 rows per CTA (fewer chunks for short columns)
     chunks = int(std::max<int64_t>(1, std::min<int64_t>(chunks, rows / 32)));
     p.grid = chunks * p.strips;
+    if (p.tma) {  // chunk boundaries on stage boundaries: no two CTAs store the same rows
+        const int br = cf::bn_tma_box_rows(p.lpr);
+        const int64_t per = (rows + chunks - 1) / chunks;
+        p.rows_per_chunk = ((per + br - 1) / br) * br;
+    }
     return CF_OK;
 }
 
@@ -542,6 +566,34 @@ cf_status cf_stitch_batchnorm_ex(const float *A, const float *gamma, const float
     if (p.mapping == 4 && ws_bytes < cf::kErrBytes + 256 + size_t(p.grid) * 4 * p.lpr * sizeof(float2))
         return CF_ERR_WORKSPACE_TOO_SMALL;
     uint8_t *wsb = static_cast<uint8_t *>(ws);
+    if (p.mapping == 4 && p.tma) {
+        cf::BnTmaArgs a;
+        std::memset(&a, 0, sizeof(a));
+        const uint32_t W = uint32_t(4 * p.lpr), br = uint32_t(cf::bn_tma_box_rows(p.lpr));
+        if (!make_tmap_f32(&a.tmap_a, A, uint64_t(rows), uint64_t(cols), W, br)) return CF_ERR_CUDA;
+        if (!make_tmap_f32(&a.tmap_out, out, uint64_t(rows), uint64_t(cols), W, br)) return CF_ERR_CUDA;
+        a.gamma = gamma;
+        a.beta = beta;
+        a.mean_out = mean_out;
+        a.var_out = var_out;
+        a.err = reinterpret_cast<uint32_t *>(wsb);
+        a.counters = reinterpret_cast<uint32_t *>(wsb + cf::kErrBytes);
+        a.partials = reinterpret_cast<float2 *>(wsb + cf::kErrBytes + 256);
+        a.rows = rows;
+        a.cols = int(cols);
+        a.strips = p.strips;
+        a.rows_per_chunk = int(p.rows_per_chunk);
+        a.extra_arrivals = p.extra_arrivals;
+        a.eps = eps;
+        a.timeout_ns = p.timeout_ns;
+        a.trace = reinterpret_cast<unsigned long long *>(t.trace);
+        a.A = A;
+        a.out = out;
+        a.flat = (cols == int64_t(W) && t.stitch_mapping != 6) ? 1 : 0;  // 6: tiled copies forced (comparison)
+        cudaError_t e = cf::launch_batchnorm_tma(p.lpr, a, p.grid, p.pdl, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e);
+        return CF_OK;
+    }
     cudaError_t e = cf::launch_batchnorm(p, A, gamma, beta, out, mean_out, var_out, rows, cols, eps,
                                          reinterpret_cast<uint32_t *>(wsb),
                                          reinterpret_cast<uint32_t *>(wsb + cf::kErrBytes),

@@ -69,12 +69,36 @@ struct BnPlan {
     bool vec = false;
     bool pdl = true;
     int extra_arrivals = 0;
+    bool tma = false;     // Global: stream the rows through shared memory by TMA
+    int64_t rows_per_chunk = 0;  // Global + TMA: a multiple of the stage height
     unsigned long long timeout_ns = 200000000ull;
 };
 cudaError_t launch_batchnorm(const BnPlan &p, const float *A, const float *gamma, const float *beta, float *out,
                              float *mean_out, float *var_out, int64_t rows, int64_t cols, float eps, uint32_t *err,
                              uint32_t *counters, float2 *partials, cudaStream_t stream);
 int bn_global_blocks_per_sm(int lpr, bool vec);
+
+// Global BatchNorm streamed through shared memory by TMA (cols % 4 == 0,
+// 16-byte aligned A and out): one producer warp, eight compute warps
+struct BnTmaArgs {
+    CUtensorMap tmap_a;    // A [rows, cols] fp32, box (4*lpr) x br, no swizzle
+    CUtensorMap tmap_out;  // out, same box
+    const float *gamma, *beta;
+    float *mean_out, *var_out;
+    uint32_t *err, *counters;
+    float2 *partials;      // [grid][4*lpr]
+    int64_t rows;
+    int cols, strips, rows_per_chunk, extra_arrivals;
+    float eps;
+    unsigned long long timeout_ns;
+    unsigned long long *trace;  // optional: per CTA slots 0..3 = start, pass 1 done, barrier passed, pass 2 done
+    const float *A;        // flat (cols == 4*lpr): stages move as untiled bulk copies
+    float *out;
+    int flat;
+};
+cudaError_t launch_batchnorm_tma(int lpr, const BnTmaArgs &a, int grid, bool pdl, cudaStream_t stream);
+int bn_tma_blocks_per_sm(int lpr);
+int bn_tma_box_rows(int lpr);   // rows of one stage for a strip of 4*lpr columns
 constexpr int kBnRegionalMaxRows = 256;   // 8 warps x 32 rows in registers
 constexpr int kBnMaxGlobalCtas = 1024;    // bound of the partial buffer
 

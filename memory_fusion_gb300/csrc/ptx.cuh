@@ -114,6 +114,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
                  : "memory");
 }
 
+// `count` arrivals at once (one thread standing for several)
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar), "r"(count)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
                  "r"(bytes)
@@ -300,6 +306,22 @@ __device__ __forceinline__ void st_async_f2(uint32_t remote_addr, float x, float
                  : "memory");
 }
 
+// untiled bulk copies (addresses 16-byte aligned, size a multiple of 16)
+__device__ __forceinline__ void bulk_load_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                                   uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store_s2g_hint(void *dst, uint32_t src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
                                                     uint32_t remote_bar) {
     asm volatile(
@@ -331,6 +353,11 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 // at most one of this thread's committed bulk stores is still reading shared memory
 __device__ __forceinline__ void bulk_wait_group_read1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// at most N of this thread's committed bulk stores are still reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 // this thread's committed bulk stores are complete
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

@@ -27,10 +27,13 @@
 //
 // Every wait is bounded by %globaltimer; a timeout records
 // CF_ERR_DEVICE_TIMEOUT in the workspace error word.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
+#include "../../include/cf.h"
 #include "cf_internal.h"
 #include "ptx.cuh"
 #include "rowstats.cuh"
@@ -563,6 +566,290 @@ __global__ void __launch_bounds__(kGlobalThreads, 1) bn_global_kernel(
     ptx::griddep_launch_dependents();
 }
 
+// ==========================================================================
+// BatchNorm, Global, streamed through shared memory by TMA.  A CTA's rows (a
+// contiguous range of one column strip, aligned to the stage height) pass
+// twice through a ring of stages: once for the statistics (loaded
+// evict-last, so the second pass finds them in L2), once to be normalised in
+// place and written back by TMA stores.  The producer issues the second
+// pass's loads while the grid barrier is in progress.  One producer warp,
+// eight compute warps; a compute thread owns one 4-column group of the strip
+// and RPS rows of every stage.
+// ==========================================================================
+constexpr int kTmaStages = 12;
+constexpr int kTmaCompute = 256;
+constexpr int kTmaThreads = kTmaCompute + 32;
+
+template <int LPR>
+struct BnTmaShape {
+    static constexpr int W = 4 * LPR;                                  // strip columns
+    static constexpr int BR = (1024 / LPR) < 256 ? (1024 / LPR) : 256;  // stage rows (box height <= 256)
+    static constexpr int STAGE = W * BR * 4;                           // bytes
+    static constexpr int SLOTS = kTmaCompute / LPR;                    // row slots
+    static constexpr int RPS = BR / SLOTS;                             // rows per thread per stage
+};
+
+// kFlat: the strip is the whole row (cols == 4*LPR), so a stage is one
+// contiguous block of memory and moves by one untiled bulk copy each way
+template <int LPR, bool kFlat>
+__global__ void __launch_bounds__(kTmaThreads, 1) bn_global_tma_kernel(const __grid_constant__ BnTmaArgs a) {
+    using Sh = BnTmaShape<LPR>;
+    constexpr int W = Sh::W, BR = Sh::BR, STAGE = Sh::STAGE, SLOTS = Sh::SLOTS, RPS = Sh::RPS;
+    constexpr int kCW = kTmaCompute / 32;
+    extern __shared__ __align__(128) uint8_t ring_smem[];
+    __shared__ float2 red[kCW][W];
+    __shared__ float redn[kCW];
+    __shared__ float4 stat[LPR][3];  // per 4-group: mean, gamma*rstd, beta
+    __shared__ __align__(8) uint64_t full[kTmaStages];
+    __shared__ __align__(8) uint64_t empty[kTmaStages];
+    __shared__ uint32_t abort_flag;
+
+    const uint32_t ring = ptx::smem_u32(ring_smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int strip = int(blockIdx.x) % a.strips;
+    const int chunk = int(blockIdx.x) / a.strips;
+    const int nchunks = int(gridDim.x) / a.strips;
+    const int64_t r0 = int64_t(chunk) * a.rows_per_chunk;
+    const int64_t r1 = r0 + a.rows_per_chunk < a.rows ? r0 + a.rows_per_chunk : a.rows;
+    const int nst = r1 > r0 ? int((r1 - r0 + BR - 1) / BR) : 0;  // stages per pass
+    volatile uint32_t *abort = &abort_flag;
+    const uint64_t tmo = a.timeout_ns;
+    unsigned long long *const tr = a.trace != nullptr ? a.trace + size_t(blockIdx.x) * CF_TRACE_SLOTS : nullptr;
+    if (threadIdx.x == 0) {
+        if (tr != nullptr) tr[0] = ptx::globaltimer();
+        for (int s = 0; s < kTmaStages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&empty[s]), kCW);
+        }
+        abort_flag = 0u;
+        ptx::fence_mbarrier_init_cluster();
+    }
+    __syncthreads();
+    ptx::griddep_wait();
+
+    if (warp == kCW) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            ptx::prefetch_tensormap(&a.tmap_a);
+            const uint64_t keep = ptx::policy_evict_last(), once = ptx::policy_evict_first();
+            uint32_t s = 0, ph = 0;
+            int issued = 0;
+            for (int i = 0; i < 2 * nst; ++i) {
+                if (!ptx::mbar_wait_bounded(ptx::smem_u32(&empty[s]), ph ^ 1u, tmo, abort, a.err, 0x73000000u | s))
+                    break;
+                const int64_t row = r0 + int64_t(i < nst ? i : i - nst) * BR;
+                if constexpr (kFlat) {
+                    // the rows of this stage that exist (a multiple of 16 bytes: cols % 4 == 0)
+                    const int64_t nrow = r1 - row < BR ? r1 - row : BR;
+                    const uint32_t bytes = uint32_t(nrow) * uint32_t(W) * 4u;
+                    ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[s]), bytes);
+                    ptx::bulk_load_g2s_hint(ring + s * STAGE, a.A + row * W, bytes, ptx::smem_u32(&full[s]),
+                                            i < nst ? keep : once);
+                } else {
+                    ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[s]), uint32_t(STAGE));
+                    ptx::tma_load_2d_hint(ring + s * STAGE, &a.tmap_a, ptx::smem_u32(&full[s]), strip * W, int(row),
+                                          i < nst ? keep : once);
+                }
+                ++issued;
+                if (++s == kTmaStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            // every issued load has landed before the CTA may exit
+            for (int i = issued > kTmaStages ? issued - kTmaStages : 0; i < issued; ++i) {
+                volatile uint32_t local_abort = 0;
+                ptx::mbar_wait_bounded(ptx::smem_u32(&full[i % kTmaStages]), uint32_t(i / kTmaStages) & 1u, tmo,
+                                       &local_abort, nullptr, 0);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- compute
+    const int c = threadIdx.x;
+    const int sub = c % LPR, slot = c / LPR;
+    uint32_t s = 0, ph = 0;
+    // ---- pass 1: running (n, mean, M2) of this thread's 4 columns
+    float n = 0.f;
+    MeanM2 run[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+    for (int i = 0; i < nst; ++i) {
+        if (!ptx::mbar_wait_bounded(ptx::smem_u32(&full[s]), ph, tmo, abort, a.err, 0x74000000u | s)) break;
+        const float4 *st4 = reinterpret_cast<const float4 *>(ring_smem + s * STAGE);
+        const int64_t rb = r0 + int64_t(i) * BR;
+        float4 x[RPS];
+        float nc = 0.f;
+#pragma unroll
+        for (int k = 0; k < RPS; ++k) {
+            const int lr = slot + k * SLOTS;
+            x[k] = st4[lr * LPR + sub];
+            if (rb + lr < r1) nc += 1.f;
+            else x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[s]));
+        if (++s == kTmaStages) {
+            s = 0;
+            ph ^= 1u;
+        }
+        if (nc == 0.f) continue;
+        const float ic = 1.0f / nc;
+        float mc[4] = {0.f, 0.f, 0.f, 0.f}, qc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < RPS; ++k) {
+            mc[0] += x[k].x;
+            mc[1] += x[k].y;
+            mc[2] += x[k].z;
+            mc[3] += x[k].w;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mc[j] *= ic;
+#pragma unroll
+        for (int k = 0; k < RPS; ++k) {
+            if (rb + slot + k * SLOTS < r1) {
+                const float d[4] = {x[k].x - mc[0], x[k].y - mc[1], x[k].z - mc[2], x[k].w - mc[3]};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) qc[j] = fmaf(d[j], d[j], qc[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) run[j] = combine_counts_safe(run[j], n, MeanM2{mc[j], qc[j]}, nc);
+        n += nc;
+    }
+    // ---- CTA reduce: lanes LPR apart hold the same columns, then the warps
+    constexpr int RPW = 32 / LPR;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float nj = n;
+        warp_meanm2<RPW, LPR>(run[j], nj);
+        if (j == 3) n = nj;
+    }
+    if (lane < LPR) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) red[warp][4 * sub + j] = make_float2(run[j].mean, run[j].m2);
+        if (lane == 0) redn[warp] = n;
+    }
+    ptx::named_bar_sync(1, kTmaCompute);
+    if (c < W) {
+        MeanM2 acc{red[0][c].x, red[0][c].y};
+        float na = redn[0];
+        for (int w = 1; w < kCW; ++w) {
+            acc = combine_counts_safe(acc, na, MeanM2{red[w][c].x, red[w][c].y}, redn[w]);
+            na += redn[w];
+        }
+        a.partials[size_t(blockIdx.x) * W + c] = make_float2(acc.mean, acc.m2);
+        __threadfence();
+    }
+    ptx::named_bar_sync(1, kTmaCompute);
+    // ---- grid barrier (every CTA resident: host-checked)
+    if (c == 0) {
+        if (tr != nullptr) tr[1] = ptx::globaltimer();
+        const uint32_t want = gridDim.x + uint32_t(a.extra_arrivals);
+        ptx::red_add_release_gpu(a.counters, 1u);
+        const uint64_t t0 = ptx::globaltimer();
+        uint32_t spins = 0;
+        while (ptx::ld_acquire_gpu(a.counters) < want) {
+            if ((++spins & 63u) == 0u) {
+                if (ptx::globaltimer() - t0 > tmo) {
+                    *abort = 1u;
+                    ptx::record_error(a.err, 7u /*CF_ERR_DEVICE_TIMEOUT*/, 0x72000000u | blockIdx.x);
+                    break;
+                }
+                if (ptx::ld_relaxed_gpu(a.err) != 0u) {
+                    *abort = 1u;
+                    break;
+                }
+            }
+        }
+    }
+    ptx::named_bar_sync(1, kTmaCompute);
+    if (*abort) return;
+    if (c == 0 && tr != nullptr) tr[2] = ptx::globaltimer();
+    // ---- fold every chunk's partial of the strip: one warp per column, lanes
+    // over chunks, one fixed order (bitwise-equal statistics in all CTAs)
+    for (int t = warp; t < W; t += kCW) {
+        MeanM2 acc{0.f, 0.f};
+        float na = 0.f;
+        for (int k = lane; k < nchunks; k += 32) {
+            const float2 pc = ptx::ld_relaxed_gpu_f2(a.partials + size_t(k * a.strips + strip) * W + t);
+            const int64_t q0 = int64_t(k) * a.rows_per_chunk;
+            const int64_t q1 = q0 + a.rows_per_chunk < a.rows ? q0 + a.rows_per_chunk : a.rows;
+            const float nk = q1 > q0 ? float(q1 - q0) : 0.f;
+            acc = combine_counts_safe(acc, na, MeanM2{pc.x, pc.y}, nk);
+            na += nk;
+        }
+        warp_meanm2<32>(acc, na);
+        if (lane == 0) {
+            const int col = strip * W + t;
+            float *st = reinterpret_cast<float *>(&stat[0][0]);
+            const float var = na > 0.f ? acc.m2 / na : 0.f;
+            const bool cv = col < a.cols;
+            st[(t >> 2) * 12 + 0 + (t & 3)] = cv ? acc.mean : 0.f;
+            st[(t >> 2) * 12 + 4 + (t & 3)] = cv ? __ldg(a.gamma + col) * rsqrtf(var + a.eps) : 0.f;
+            st[(t >> 2) * 12 + 8 + (t & 3)] = cv ? __ldg(a.beta + col) : 0.f;
+            if (cv && chunk == 0) {
+                if (a.mean_out != nullptr) a.mean_out[col] = acc.mean;
+                if (a.var_out != nullptr) a.var_out[col] = var;
+            }
+        }
+    }
+    ptx::named_bar_sync(1, kTmaCompute);
+    if (c == 0) {  // departure: the last CTA to leave the barrier resets the counters
+        const uint32_t d = ptx::atom_add_relaxed_gpu(a.counters + 1, 1u);
+        if (d == gridDim.x - 1u) {
+            ptx::st_relaxed_gpu(a.counters, 0u);
+            ptx::st_relaxed_gpu(a.counters + 1, 0u);
+        }
+    }
+    // ---- pass 2: normalise each stage in place, TMA-store it
+    const float4 mu = stat[sub][0], sc = stat[sub][1], be = stat[sub][2];
+    const uint64_t once = ptx::policy_evict_first();
+    // up to kStoresInFlight stores may still be reading their stages; a stage
+    // is handed back to the producer once its store has left shared memory
+    constexpr int kStoresInFlight = 6;
+    uint32_t slot_of[kStoresInFlight + 1];
+    for (int i = 0; i < nst; ++i) {
+        if (!ptx::mbar_wait_bounded(ptx::smem_u32(&full[s]), ph, tmo, abort, a.err, 0x75000000u | s)) break;
+        float4 *st4 = reinterpret_cast<float4 *>(ring_smem + s * STAGE);
+#pragma unroll
+        for (int k = 0; k < RPS; ++k) {
+            const int idx = (slot + k * SLOTS) * LPR + sub;
+            const float4 x = st4[idx];
+            st4[idx] = make_float4(fmaf(x.x - mu.x, sc.x, be.x), fmaf(x.y - mu.y, sc.y, be.y),
+                                   fmaf(x.z - mu.z, sc.z, be.z), fmaf(x.w - mu.w, sc.w, be.w));
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar_sync(1, kTmaCompute);
+        if (c == 0) {
+            // rows past the end and columns past the strip's last are clipped by the store
+            const int64_t row = r0 + int64_t(i) * BR;
+            if constexpr (kFlat) {
+                const int64_t nrow = r1 - row < BR ? r1 - row : BR;
+                ptx::bulk_store_s2g_hint(a.out + row * W, ring + s * STAGE, uint32_t(nrow) * uint32_t(W) * 4u, once);
+            } else {
+                ptx::tma_store_2d_hint(&a.tmap_out, ring + s * STAGE, strip * W, int(row), once);
+            }
+            ptx::bulk_commit_group();
+            slot_of[i % (kStoresInFlight + 1)] = s;
+            ptx::bulk_wait_group_read<kStoresInFlight>();
+            if (i >= kStoresInFlight)
+                ptx::mbar_arrive_cnt(ptx::smem_u32(&empty[slot_of[(i - kStoresInFlight) % (kStoresInFlight + 1)]]),
+                                     kCW);
+        }
+        if (++s == kTmaStages) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    if (c == 0) {
+        ptx::bulk_wait_group0();
+        for (int i = nst > kStoresInFlight ? nst - kStoresInFlight : 0; i < nst; ++i)
+            ptx::mbar_arrive_cnt(ptx::smem_u32(&empty[slot_of[i % (kStoresInFlight + 1)]]), kCW);
+        if (tr != nullptr) tr[3] = ptx::globaltimer();
+    }
+    ptx::griddep_launch_dependents();
+}
+
 // --------------------------------------------------------------------------
 // kernel tables
 // --------------------------------------------------------------------------
@@ -660,6 +947,24 @@ int blocks_per_sm_cached(void *fn, int threads, int key) {
     return c;
 }
 
+template <int LPR>
+void *bn_tma_fn(bool flat) {
+    return flat ? reinterpret_cast<void *>(&bn_global_tma_kernel<LPR, true>)
+                : reinterpret_cast<void *>(&bn_global_tma_kernel<LPR, false>);
+}
+void *bn_tma_kernel_for(int lpr, bool flat) {
+    switch (lpr) {
+        case 1: return bn_tma_fn<1>(flat);
+        case 2: return bn_tma_fn<2>(flat);
+        case 4: return bn_tma_fn<4>(flat);
+        case 8: return bn_tma_fn<8>(flat);
+        case 16: return bn_tma_fn<16>(flat);
+        case 32: return bn_tma_fn<32>(flat);
+        default: return nullptr;
+    }
+}
+int bn_tma_stage_bytes(int lpr) { return 4 * lpr * std::min(256, 1024 / lpr) * 4; }
+
 int log2i(int v) {
     int l = 0;
     while ((1 << l) < v) ++l;
@@ -674,6 +979,50 @@ int addln_packed_blocks_per_sm(int lpr, bool vec) {
 
 int bn_global_blocks_per_sm(int lpr, bool vec) {
     return blocks_per_sm_cached(bn_global_kernel_for(lpr, vec), kGlobalThreads, 32 + log2i(lpr) * 2 + (vec ? 1 : 0));
+}
+
+int bn_tma_box_rows(int lpr) { return std::min(256, 1024 / lpr); }
+
+int bn_tma_blocks_per_sm(int lpr) {
+    static int cache[64][6] = {};
+    void *fn = bn_tma_kernel_for(lpr, false);
+    int dev = 0;
+    if (!fn || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int &c = cache[dev][log2i(lpr)];
+    if (c == 0) {
+        const int smem = kTmaStages * bn_tma_stage_bytes(lpr);
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kTmaThreads, smem) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        c = n;
+    }
+    return c;
+}
+
+cudaError_t launch_batchnorm_tma(int lpr, const BnTmaArgs &a, int grid, bool pdl, cudaStream_t stream) {
+    void *fn = bn_tma_kernel_for(lpr, a.flat != 0);
+    if (!fn) return cudaErrorInvalidValue;
+    const int smem = kTmaStages * bn_tma_stage_bytes(lpr);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    void *args[] = {(void *)&a};
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 cudaError_t launch_add_layernorm(const StitchPlan &p, const float *A, const float *R, const float *gamma,

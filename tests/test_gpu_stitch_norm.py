@@ -124,16 +124,32 @@ def test_batchnorm_global(rows, cols):
     _check_bn(d, _bn(d), f"BN Global {rows}x{cols}")
 
 
+@pytest.mark.parametrize("rows,cols", [(5000, 36), (100000, 520), (40000, 64), (3000, 1000)])
+def test_batchnorm_global_unstreamed(rows, cols):
+    """The Global scheme with plain loads (tuning stitch_mapping 5) instead of
+    the TMA-streamed kernel the planner picks for 128-bit rows."""
+    d = inputs.stitch_norm_inputs(rows, cols, seed=rows + 5 * cols, with_R=False)
+    _check_bn(d, _bn(d, tuning=cf.tuning(stitch_mapping=5)), f"BN Global unstreamed {rows}x{cols}")
+
+
 def test_batchnorm_schemes_agree_and_repeat():
     d = inputs.stitch_norm_inputs(240, 72, seed=9, with_R=False)
     a = _bn(d, tuning=cf.tuning(stitch_mapping=3))
     b = _bn(d, tuning=cf.tuning(stitch_mapping=4))
+    c = _bn(d, tuning=cf.tuning(stitch_mapping=5))
     _check_bn(d, a, "BN Regional forced")
-    _check_bn(d, b, "BN Global forced")
-    assert np.allclose(a[0], b[0], rtol=1e-5, atol=1e-5)
+    _check_bn(d, b, "BN Global forced (TMA-streamed)")
+    _check_bn(d, c, "BN Global forced (plain loads)")
+    assert np.allclose(a[0], b[0], rtol=1e-5, atol=1e-5) and np.allclose(b[0], c[0], rtol=1e-5, atol=1e-5)
     d2 = inputs.stitch_norm_inputs(30000, 32, seed=10, with_R=False)
     r1, r2 = _bn(d2), _bn(d2)
     assert all(np.array_equal(x, y) for x, y in zip(r1, r2)), "Global BatchNorm not bitwise repeatable"
+    u1, u2 = _bn(d2, tuning=cf.tuning(stitch_mapping=5)), _bn(d2, tuning=cf.tuning(stitch_mapping=5))
+    assert all(np.array_equal(x, y) for x, y in zip(u1, u2)), "unstreamed Global BatchNorm not bitwise repeatable"
+    # 32 columns make every stage one contiguous block (untiled bulk copies);
+    # stitch_mapping 6 forces the tiled copies: same arithmetic, same bits
+    t6 = _bn(d2, tuning=cf.tuning(stitch_mapping=6))
+    assert all(np.array_equal(x, y) for x, y in zip(r1, t6)), "flat and tiled streaming differ"
     # a grid capped to a few CTAs still covers every row
     _check_bn(d2, _bn(d2, tuning=cf.tuning(max_clusters=3)), "BN Global 3 CTAs")
 
