@@ -378,7 +378,7 @@ cf_status cf_get_device_status(void *ws, cf_stream_t stream, int32_t *info) {
 // (lanes per row = groups rounded up to a power of two); wider rows are split
 // over a cluster of C CTAs, C from the row count and the SM count.
 static cf_status plan_row_mapping(int64_t rows, int64_t cols, const cf_tuning &t, const cf::DeviceInfo &dev,
-                                  cf::StitchPlan *pp, int (*packed_bps)(int, bool)) {
+                                  cf::StitchPlan *pp, int (*packed_bps)(int, bool), int ctas_per_sm = 1) {
     cf::StitchPlan &p = *pp;
     p.pdl = t.disable_pdl == 0;
     p.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
@@ -398,10 +398,13 @@ static cf_status plan_row_mapping(int64_t rows, int64_t cols, const cf_tuning &t
         int C = t.cluster_size;
         if (C <= 0) {
             const int c_min = (ng + 256 * 16 - 1) / (256 * 16);
-            // about one CTA per SM for few rows (measured on the 64x30000 shape:
-            // 4 CTAs per row beat 8 and 16; the cluster barriers grow with C)
+            // about ctas_per_sm CTAs per SM for few rows (measured on the 64x30000
+            // shape: the softmax is fastest at 4 CTAs per row (one per SM), add +
+            // LayerNorm -- two inputs -- at 8 (two per SM); the cluster barriers
+            // grow with C)
             int c_par = 1;
-            if (rows < dev.sm_count) c_par = next_pow2(int((dev.sm_count + rows - 1) / rows));
+            const int64_t want = int64_t(dev.sm_count) * ctas_per_sm;
+            if (rows < want) c_par = next_pow2(int((want + rows - 1) / rows));
             C = std::max(c_min, c_par);
             C = std::min(C, 16);
             while (C > 1 && C > ng) C >>= 1;
@@ -474,7 +477,7 @@ cf_status cf_stitch_add_layernorm_ex(const float *A, const float *R, const float
     if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
     cf::StitchPlan p;
     p.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out) && (R == nullptr || aligned16(R));
-    cf_status st = plan_row_mapping(rows, cols, t, dev, &p, cf::addln_packed_blocks_per_sm);
+    cf_status st = plan_row_mapping(rows, cols, t, dev, &p, cf::addln_packed_blocks_per_sm, 2);
     if (st != CF_OK) return st;
     cudaError_t e = cf::launch_add_layernorm(p, A, R, gamma, beta, out, rows, cols, eps,
                                              static_cast<uint32_t *>(ws), reinterpret_cast<cudaStream_t>(stream));
