@@ -313,50 +313,72 @@ def time_steps(torch, runner, steps, warmup, barrier, sampler=None, graph_len=50
     return e0.elapsed_time(e1) / 1e3, reps * R + rem, clocks
 
 
-def time_e2e(torch, cf, w, steps, device):
-    """The public call with host buffers: per step, H2D of X and W from pinned
-    memory, the fused call, D2H of Y into pinned memory; CUDA events around."""
+def time_e2e(torch, cf, w, steps, device, depth=3):
+    """The public call with host buffers: every step copies its inputs X and W
+    (and the row vectors, R) from pinned host memory, makes the fused call and
+    copies Y back into pinned host memory.  Steps are pipelined over `depth`
+    buffer sets on three streams (copy-in, compute, copy-out), so the copies
+    of one step overlap the compute of its neighbours; events order each
+    set's reuse.  Returns (seconds per step, H2D bytes, D2H bytes)."""
     d = inputs.workload_inputs(w.name)
     bf = torch.bfloat16
-    hX = torch.from_numpy(d["X"]).to(bf).pin_memory()
-    hW = torch.from_numpy(d["W"]).to(bf).pin_memory()
-    hY = torch.empty((w.M, w.N), dtype=bf).pin_memory()
-    X = torch.empty_like(hX, device=device)
-    W = torch.empty_like(hW, device=device)
-    Y = torch.empty((w.M, w.N), dtype=bf, device=device)
-    extra = {"d_bias": None, "d_gamma": None, "d_beta": None, "d_R": None}
-    for k in row_vectors(w):
-        extra[k] = torch.from_numpy(d[k]).pin_memory()
-        extra["d_" + k] = torch.empty_like(extra[k], device=device)
-    if d.get("R") is not None:
-        extra["R"] = torch.from_numpy(d["R"]).to(bf).pin_memory()
-        extra["d_R"] = torch.empty_like(extra["R"], device=device)
+    names = ["X", "W"] + list(row_vectors(w)) + (["R"] if d.get("R") is not None else [])
+    host = {}
+    for k in names:
+        t = torch.from_numpy(d[k])
+        host[k] = (t.to(bf) if k in ("X", "W", "R") else t).pin_memory()
+    sets = []
+    for _ in range(depth):
+        dev = {k: torch.empty_like(host[k], device=device) for k in names}
+        dev["Y"] = torch.empty((w.M, w.N), dtype=bf, device=device)
+        dev["hY"] = torch.empty((w.M, w.N), dtype=bf).pin_memory()
+        sets.append(dev)
     wsb = cf.cf_gemm_fused_workspace_size(w.M, w.N, w.K)
     ws = cf.new_workspace(wsb, device)
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(depth)]
+    ev_cmp = [torch.cuda.Event() for _ in range(depth)]
+    ev_out = [torch.cuda.Event() for _ in range(depth)]
+    used = [False] * depth
 
-    def step():
-        X.copy_(hX, non_blocking=True)
-        W.copy_(hW, non_blocking=True)
-        for k in row_vectors(w) + (("R",) if extra["d_R"] is not None else ()):
-            extra["d_" + k].copy_(extra[k], non_blocking=True)
-        cf.check(fused_call(cf, w, X, W, extra["d_bias"], extra["d_gamma"], extra["d_beta"], Y, ws, wsb,
-                            R=extra["d_R"]))
-        hY.copy_(Y, non_blocking=True)
+    def step(i):
+        b = i % depth
+        dv = sets[b]
+        if used[b]:
+            s_in.wait_event(ev_cmp[b])    # the previous use of this set's inputs is consumed
+        with torch.cuda.stream(s_in):
+            for k in names:
+                dv[k].copy_(host[k], non_blocking=True)
+            ev_in[b].record(s_in)
+        s_cmp.wait_event(ev_in[b])
+        if used[b]:
+            s_cmp.wait_event(ev_out[b])   # the previous use of this set's Y has been read out
+        cf.check(fused_call(cf, w, dv["X"], dv["W"], dv.get("bias"), dv.get("gamma"), dv.get("beta"), dv["Y"], ws,
+                            wsb, s_cmp.cuda_stream, R=dv.get("R")))
+        ev_cmp[b].record(s_cmp)
+        s_out.wait_event(ev_cmp[b])
+        with torch.cuda.stream(s_out):
+            dv["hY"].copy_(dv["Y"], non_blocking=True)
+            ev_out[b].record(s_out)
+        used[b] = True
 
-    for _ in range(3):
-        step()
+    for i in range(2 * depth):
+        step(i)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
+    e0.record(s_in)
+    s_cmp.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(steps):
+        step(i)
+    s_in.wait_stream(s_out)
+    s_in.wait_stream(s_cmp)
+    e1.record(s_in)
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) / 1e3 / steps
-    h2d = hX.numel() * 2 + hW.numel() * 2 + 4 * w.N * len(row_vectors(w)) + (
-        2 * w.M * w.N if extra["d_R"] is not None else 0)
-    d2h = hY.numel() * 2
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = w.M * w.N * 2
     return t, h2d, d2h
 
 
@@ -548,7 +570,10 @@ def stitch_norm_kernel_name(cf, w):
     if w.kind == "add_layernorm":
         return "addln_packed_kernel" if (w.cols + 3) // 4 <= 32 else "addln_split_kernel"
     _, mapping, _ = cf.cf_query_stitch_batchnorm_plan(w.rows, w.cols)
-    return "bn_regional_kernel" if mapping == 3 else "bn_global_kernel"
+    if mapping == 3:
+        return "bn_regional_kernel"
+    # 128-bit rows stream through shared memory (the planner's rule)
+    return "bn_global_tma_kernel" if w.cols % 4 == 0 else "bn_global_kernel"
 
 
 def stitch_norm_numbers(torch, cf, w, peaks, device, l2):
