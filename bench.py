@@ -591,6 +591,48 @@ def stitch_norm_numbers(torch, cf, w, peaks, device, l2):
     return out
 
 
+def pdl_chain_numbers(torch, cf, device, reps=200):
+    """Three dependent fused calls on one stream -- GEMM+LayerNorm (1024x512x256),
+    GEMM+softmax on its output (1024x256x512), B2B GEMM on that (K 256, N1 512,
+    N2 128) -- replayed from CUDA graphs with programmatic dependent launch
+    off and on: what overlapping each kernel's set-up with its predecessor's
+    tail saves at a kernel boundary that is not fused."""
+    M, K, N1, N2, NB1, NB2 = 1024, 256, 512, 256, 512, 128
+    rng = np.random.Generator(np.random.PCG64(43))
+    bf = torch.bfloat16
+
+    def mat(r, c, sd):
+        return torch.from_numpy(inputs.round_to_bf16(rng.standard_normal((r, c)).astype(np.float32) * sd)).to(
+            device, bf)
+
+    X, W1, W2, W3, W4 = mat(M, K, 1.0), mat(K, N1, K ** -0.5), mat(N1, N2, N1 ** -0.5), mat(N2, NB1, 4.0), \
+        mat(NB1, NB2, NB1 ** -0.5)
+    ones = torch.ones(N1, device=device)
+    zeros = torch.zeros(N1, device=device)
+    Y1 = torch.empty((M, N1), dtype=bf, device=device)
+    Y2 = torch.empty((M, N2), dtype=bf, device=device)
+    O = torch.empty((M, NB2), dtype=bf, device=device)
+    ws = [cf.new_workspace(n, device) for n in (cf.cf_gemm_fused_workspace_size(M, N1, K),
+                                                 cf.cf_gemm_fused_workspace_size(M, N2, N1),
+                                                 cf.cf_b2b_workspace_size())]
+    out = {}
+    for label, tun in (("pdl_off_us", cf.tuning(disable_pdl=1)), ("pdl_on_us", cf.tuning())):
+        class R:
+            def launch(self, i, stream=None, t=tun):
+                cf.check(cf.cf_gemm_fused_rownorm(X, W1, zeros, ones, zeros, Y1, M, N1, K, 1.0, 1e-5, cf.CF_ACT_NONE,
+                                                  ws[0], ws[0].numel(), stream, t))
+                cf.check(cf.cf_gemm_fused_rowsoftmax(Y1, W2, None, Y2, M, N2, N1, N1 ** -0.5, ws[1], ws[1].numel(),
+                                                     stream, t))
+                cf.check(cf.cf_b2b_gemm(Y2, W3, None, W4, O, M, N2, NB1, NB2, 1.0, cf.CF_B2B_GELU_TANH, ws[2],
+                                        ws[2].numel(), stream, t))
+
+        t, n, _ = time_steps(torch, R(), reps, 3, lambda: None, graph_len=reps)
+        out[label] = round(t / n * 1e6, 2)
+    out["saved_us_per_boundary"] = round((out["pdl_off_us"] - out["pdl_on_us"]) / 3, 2)
+    out["chain"] = "GEMM+LN 1024x512x256 -> GEMM+softmax 1024x256x512 -> B2B GELU 1024x256x512x128, per chain"
+    return out
+
+
 def cpu_oracle_sample(w, budget_s=10.0, max_rows=None):
     """The fp64 oracle as it stands, on whole-row samples of the workload,
     repeated until ~budget_s of CPU time; returns (flops/s, seconds, rows)."""
@@ -697,6 +739,7 @@ def run_ours(args):
         if not args.quick:
             names = [k for k in inputs.WORKLOADS]
             line["per_workload"] = per_workload(torch, cf, peaks, device, names)
+            line["pdl_chain"] = pdl_chain_numbers(torch, cf, device)
         if not args.no_cpu:
             v, secs, rows = cpu_oracle_sample(w, budget_s=args.cpu_budget)
             line["cpu_baseline"] = {"value": round(v / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(),
