@@ -45,8 +45,8 @@ Readings taken where the pages are silent:
     and before the reduction (the "add & norm" of a transformer block).
   * B2BGEMM: O = S . W2 with S = F(alpha * X.W1 + b1) held in bf16 -- the
     dtype of the intermediate tensor the unfused chain would materialise
-    (the tensor cores consume bf16 operands); F is GELU(tanh) or the row
-    softmax over N1.
+    (the tensor cores consume bf16 operands); F is GELU(tanh), the row
+    softmax over N1 or the row LayerNorm over N1 (gamma1, beta1 per column).
   * Masked softmax: a causal mask keeps element (i, j) of the scaled scores
     iff j <= i + offset (masked elements are -inf before the softmax); a row
     with no kept element is all zeros.
@@ -314,15 +314,17 @@ def gemm_rowsoftmax_causal(X, W, *, scale: float, offset: int, bias=None, rows=N
     return out
 
 
-def b2b_gemm(X, W1, W2, *, op: str, alpha: float = 1.0, b1=None, rows=None) -> np.ndarray:
-    """O = bf16(F(alpha * X.W1 + b1)) . W2, F = GELU_tanh or the row softmax.
+def b2b_gemm(X, W1, W2, *, op: str, alpha: float = 1.0, b1=None, rows=None, gamma1=None, beta1=None,
+             eps: float = 1e-5) -> np.ndarray:
+    """O = bf16(F(alpha * X.W1 + b1)) . W2, F = GELU_tanh, the row softmax or
+    the row LayerNorm (with gamma1, beta1 over the N1 columns).
 
     ComFuse, B2BGEMM (Eqs. 3-7): MatMul_1, the epilogue F giving S_tile
     (Eq. 3), MatMul_2 over the intermediate dimension N1 (Eqs. 4-5).  The
     intermediate S is rounded to bf16 (round to nearest even), the precision
     of the tensor the unfused chain stores between the two GEMMs.
     """
-    if op not in ("softmax", "gelu_tanh"):
+    if op not in ("softmax", "gelu_tanh", "layernorm"):
         raise ValueError(f"unknown op {op!r}")
     X = np.asarray(X)
     M = X.shape[0]
@@ -333,7 +335,12 @@ def b2b_gemm(X, W1, W2, *, op: str, alpha: float = 1.0, b1=None, rows=None) -> n
     o = 0
     for idx in _row_chunks(M, rows):
         z = float(alpha) * gemm(X[idx], W1) + b
-        S = softmax_rows(z) if op == "softmax" else gelu_tanh(z)
+        if op == "softmax":
+            S = softmax_rows(z)
+        elif op == "gelu_tanh":
+            S = gelu_tanh(z)
+        else:
+            S = layernorm_rows(z, gamma1, beta1, eps)
         S = _round_bf16(S)
         out[o:o + idx.size] = gemm(S, W2)
         o += idx.size

@@ -412,8 +412,8 @@ def check_softmax_causal(fused) -> list:
 
 def check_b2b(fused) -> list:
     """B2BGEMM: torch fp64 compositions with the intermediate cast to bf16 by
-    torch; W2 = identity returns bf16(S); the softmax row sums of bf16(S) . 1
-    equal the rounded S's row sums; linearity in W2."""
+    torch (softmax, GELU, LayerNorm); W2 = identity returns bf16(S); the
+    LayerNorm rows are normalised; linearity in W2."""
     import torch
     F = torch.nn.functional
     fails = []
@@ -435,6 +435,21 @@ def check_b2b(fused) -> list:
         I = np.eye(N1)
         yi = np.asarray(fused(X, W1, I, op=op, alpha=0.5, b1=b1))
         _fail(fails, np.array_equal(yi, S.numpy()), f"b2b {op} identity W2")
+    # F = LayerNorm over N1 with per-column gamma1, beta1
+    g1 = 1 + 0.3 * rng.standard_normal(N1)
+    be1 = 0.2 * rng.standard_normal(N1)
+    z = 0.5 * (t["X"] @ t["W1"]) + t["b"]
+    S = F.layer_norm(z, (N1,), torch.from_numpy(g1), torch.from_numpy(be1), 1e-5)
+    S = S.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    ref = (S @ t["W2"]).numpy()
+    y = np.asarray(fused(X, W1, W2, op="layernorm", alpha=0.5, b1=b1, gamma1=g1, beta1=be1, eps=1e-5))
+    _fail(fails, y.shape == ref.shape and np.allclose(y, ref, rtol=1e-12, atol=1e-13), "b2b layernorm vs torch")
+    yi = np.asarray(fused(X, W1, np.eye(N1), op="layernorm", alpha=0.5, b1=b1, gamma1=g1, beta1=be1, eps=1e-5))
+    _fail(fails, np.array_equal(yi, S.numpy()), "b2b layernorm identity W2")
+    # at eps = 0, gamma = 1, beta = 0 the rounded S rows have mean ~0 and variance ~1
+    y1 = np.asarray(fused(X, W1, np.eye(N1), op="layernorm", gamma1=np.ones(N1), beta1=np.zeros(N1), eps=0.0))
+    _fail(fails, np.all(np.abs(y1.mean(axis=1)) < 1e-2) and
+          all(abs(statistics.pvariance(r) - 1) < 1e-2 for r in y1.tolist()), "b2b layernorm normalised rows")
     # linearity in W2
     W2b = rng.standard_normal((N1, N2))
     y1 = np.asarray(fused(X, W1, W2 + 2.0 * W2b, op="softmax"))

@@ -259,7 +259,7 @@ def test_causal_mutant_caught(name):
         assert pins.check_softmax_causal(CAUSAL_MUTANTS[name]), name
 
 
-def _b2b(X, W1, W2, *, op, alpha=1.0, b1=None, rows=None, mistake):
+def _b2b(X, W1, W2, *, op, alpha=1.0, b1=None, rows=None, gamma1=None, beta1=None, eps=1e-5, mistake):
     X = np.asarray(X, float)
     if rows is not None:
         X = X[rows]
@@ -270,6 +270,11 @@ def _b2b(X, W1, W2, *, op, alpha=1.0, b1=None, rows=None, mistake):
         z = alpha * (X @ np.asarray(W1, float)) + bias
     if op == "softmax":
         S = oracle.softmax_rows(z.T).T if mistake == "softmax over columns" else oracle.softmax_rows(z)
+    elif op == "layernorm":
+        m = z.mean(axis=1, keepdims=True)
+        dz = z - m
+        n = z.shape[1] - (1 if mistake == "layernorm unbiased variance" else 0)
+        S = dz / np.sqrt((dz * dz).sum(axis=1, keepdims=True) / n + eps) * np.asarray(gamma1) + np.asarray(beta1)
     else:
         S = oracle.gelu_tanh(z)
     if mistake == "no bf16 rounding":
@@ -288,7 +293,7 @@ def _b2b(X, W1, W2, *, op, alpha=1.0, b1=None, rows=None, mistake):
 
 B2B_MUTANTS = {k: (lambda kk: (lambda *a, **kw: _b2b(*a, mistake=kk, **kw)))(k)
                for k in ("no bf16 rounding", "fp16 rounding", "truncated to bf16", "b1 dropped", "alpha after bias",
-                         "softmax over columns")}
+                         "softmax over columns", "layernorm unbiased variance")}
 
 
 @pytest.mark.parametrize("name", sorted(B2B_MUTANTS))
