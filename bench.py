@@ -103,7 +103,8 @@ def unfused_call(cf, w, X, W, bias, gamma, beta, Y, ws, wsb, stream=None, R=None
 
 def oracle_rows(oracle, w, d, rows):
     if w.kind == "b2b":
-        return oracle.b2b_gemm(d["X"], d["W1"], d["W2"], op=w.op, alpha=w.alpha, b1=d["b1"], rows=rows)
+        return oracle.b2b_gemm(d["X"], d["W1"], d["W2"], op=w.op, alpha=w.alpha, b1=d["b1"], rows=rows,
+                               gamma1=d.get("gamma1"), beta1=d.get("beta1"), eps=1e-5)
     if w.kind == "softmax":
         return oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows)
     if w.kind == "softmax_causal":
@@ -390,24 +391,32 @@ class B2bRunner:
         self.torch, self.cf, self.w = torch, cf, w
         d = inputs.workload_inputs(w.name) if seed_offset == 0 else inputs.b2b_inputs(
             w.M, w.K, w.N1, w.N2, mdist.seed_for(w.seed, seed_offset), x_std=w.x_std, w1_std=w.w1_std,
-            w2_std=w.w2_std, b1_std=w.b1_std)
+            w2_std=w.w2_std, b1_std=w.b1_std, ln=w.op == "layernorm")
         self.host = d
         bf = torch.bfloat16
         X = torch.from_numpy(d["X"]).to(device, bf)
         W1 = torch.from_numpy(d["W1"]).to(device, bf)
         W2 = torch.from_numpy(d["W2"]).to(device, bf)
         b1 = torch.from_numpy(d["b1"]).to(device) if d["b1"] is not None else None
+        self.g1 = torch.from_numpy(d["gamma1"]).to(device) if d.get("gamma1") is not None else None
+        self.be1 = torch.from_numpy(d["beta1"]).to(device) if d.get("beta1") is not None else None
         self.sets = [{"X": X if i == 0 else X.clone(), "W1": W1 if i == 0 else W1.clone(),
                       "W2": W2 if i == 0 else W2.clone(), "b1": b1,
                       "O": torch.empty((w.M, w.N2), dtype=bf, device=device)} for i in range(nsets)]
-        self.op = cf.CF_B2B_SOFTMAX if w.op == "softmax" else cf.CF_B2B_GELU_TANH
+        self.op = {"softmax": cf.CF_B2B_SOFTMAX, "gelu_tanh": cf.CF_B2B_GELU_TANH,
+                   "layernorm": cf.CF_B2B_LAYERNORM}[w.op]
         self.ws_bytes = cf.cf_b2b_workspace_size()
         self.ws = cf.new_workspace(self.ws_bytes, device)
 
     def launch(self, i, stream=None):
         w, s = self.w, self.sets[i % len(self.sets)]
-        self.cf.check(self.cf.cf_b2b_gemm(s["X"], s["W1"], s["b1"], s["W2"], s["O"], w.M, w.K, w.N1, w.N2,
-                                          w.alpha, self.op, self.ws, self.ws_bytes, stream), "b2b launch")
+        if w.op == "layernorm":
+            st = self.cf.cf_b2b_gemm_layernorm(s["X"], s["W1"], s["b1"], self.g1, self.be1, s["W2"], s["O"], w.M,
+                                               w.K, w.N1, w.N2, w.alpha, 1e-5, self.ws, self.ws_bytes, stream)
+        else:
+            st = self.cf.cf_b2b_gemm(s["X"], s["W1"], s["b1"], s["W2"], s["O"], w.M, w.K, w.N1, w.N2, w.alpha,
+                                     self.op, self.ws, self.ws_bytes, stream)
+        self.cf.check(st, "b2b launch")
 
 
 def b2b_bytes_per_set(w):
@@ -415,7 +424,7 @@ def b2b_bytes_per_set(w):
 
 
 def b2b_kernel_name(w):
-    return "b2b_kernel<SOFTMAX>" if w.op == "softmax" else "b2b_kernel<GELU>"
+    return {"softmax": "b2b_kernel<SOFTMAX>", "gelu_tanh": "b2b_kernel<GELU>", "layernorm": "b2b_kernel<LN>"}[w.op]
 
 
 def torch_b2b_time(torch, runner, reps):
@@ -430,7 +439,12 @@ def torch_b2b_time(torch, runner, reps):
             P = torch.matmul(s["X"], s["W1"]).float() * w.alpha
             if s["b1"] is not None:
                 P = P + s["b1"]
-            S = torch.softmax(P, dim=1) if w.op == "softmax" else torch.nn.functional.gelu(P, approximate="tanh")
+            if w.op == "softmax":
+                S = torch.softmax(P, dim=1)
+            elif w.op == "gelu_tanh":
+                S = torch.nn.functional.gelu(P, approximate="tanh")
+            else:
+                S = torch.nn.functional.layer_norm(P, (w.N1,), runner.g1, runner.be1, 1e-5)
             torch.matmul(S.to(torch.bfloat16), s["W2"], out=s["O"])
 
     t, n, _ = time_steps(torch, U(), reps, 3, lambda: None, graph_len=reps)

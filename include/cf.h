@@ -419,7 +419,8 @@ CF_API cf_status cf_gemm_fused_rowsoftmax_causal_ex(const void *X, const void *W
  * `stream`; device-side timeouts are reported by cf_get_device_status. */
 typedef enum {
     CF_B2B_SOFTMAX = 0,
-    CF_B2B_GELU_TANH = 1
+    CF_B2B_GELU_TANH = 1,
+    CF_B2B_LAYERNORM = 2   /* only through cf_b2b_gemm_layernorm (needs gamma1, beta1) */
 } cf_b2b_op;
 
 CF_API size_t cf_b2b_workspace_size(void);
@@ -442,6 +443,24 @@ CF_API cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, 
                                 float alpha, cf_b2b_op op, void *workspace,
                                 size_t workspace_bytes, cf_stream_t stream,
                                 const cf_tuning *tuning);
+
+/* O = bf16( bf16(LayerNorm(alpha * X.W1 + b1) * gamma1 + beta1) . W2 ): the
+ * back-to-back GEMM with F = LayerNorm over each row's N1 intermediate
+ * values (biased variance, eps inside the square root); the row (mean, M2)
+ * is reduced across the cluster like the softmax statistics.  gamma1, beta1
+ * (device) fp32 [N1], required; everything else as for cf_b2b_gemm. */
+CF_API cf_status cf_b2b_gemm_layernorm(const void *X, const void *W1, const float *b1,
+                                       const float *gamma1, const float *beta1, const void *W2,
+                                       void *O, int64_t M, int64_t K, int64_t N1, int64_t N2,
+                                       float alpha, float eps, void *workspace,
+                                       size_t workspace_bytes, cf_stream_t stream);
+
+CF_API cf_status cf_b2b_gemm_layernorm_ex(const void *X, const void *W1, const float *b1,
+                                          const float *gamma1, const float *beta1, const void *W2,
+                                          void *O, int64_t M, int64_t K, int64_t N1, int64_t N2,
+                                          float alpha, float eps, void *workspace,
+                                          size_t workspace_bytes, cf_stream_t stream,
+                                          const cf_tuning *tuning);
 
 /* ------------------------------------------------------------------------ */
 /* Stitched reduce -> broadcast subgraph (no GEMM)                           */

@@ -133,6 +133,9 @@ _SIGS = {
     "cf_b2b_gemm": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F, ctypes.c_int, _P, _SZ, _P]),
     "cf_b2b_gemm_ex": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F, ctypes.c_int, _P, _SZ, _P,
                              ctypes.POINTER(cf_tuning)]),
+    "cf_b2b_gemm_layernorm": (_ST, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F, _F, _P, _SZ, _P]),
+    "cf_b2b_gemm_layernorm_ex": (_ST, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F, _F, _P, _SZ, _P,
+                                       ctypes.POINTER(cf_tuning)]),
     "cf_stitch_add_layernorm": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, _SZ, _P]),
     "cf_stitch_add_layernorm_ex": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, _SZ, _P,
                                          ctypes.POINTER(cf_tuning)]),
@@ -366,6 +369,7 @@ def cf_unfused_gemm_rowsoftmax(X, W, bias, Y, M, N, K, scale, workspace, workspa
 
 CF_B2B_SOFTMAX = 0
 CF_B2B_GELU_TANH = 1
+CF_B2B_LAYERNORM = 2
 
 
 def cf_b2b_workspace_size() -> int:
@@ -456,6 +460,18 @@ def gemm_fused_rowsoftmax(X, W, bias=None, *, scale=1.0, out=None, workspace=Non
     return Y
 
 
+def cf_b2b_gemm_layernorm(X, W1, b1, gamma1, beta1, W2, O, M, K, N1, N2, alpha, eps, workspace, workspace_bytes,
+                          stream=None, tuning=None) -> int:
+    """O = bf16(LayerNorm(alpha*X.W1 + b1)*gamma1 + beta1) . W2 (LayerNorm over the N1 columns)."""
+    L = lib()
+    if tuning is None:
+        return L.cf_b2b_gemm_layernorm(_ptr(X), _ptr(W1), _ptr(b1), _ptr(gamma1), _ptr(beta1), _ptr(W2), _ptr(O),
+                                       M, K, N1, N2, alpha, eps, _ptr(workspace), workspace_bytes, _stream(stream))
+    return L.cf_b2b_gemm_layernorm_ex(_ptr(X), _ptr(W1), _ptr(b1), _ptr(gamma1), _ptr(beta1), _ptr(W2), _ptr(O),
+                                      M, K, N1, N2, alpha, eps, _ptr(workspace), workspace_bytes, _stream(stream),
+                                      _tun(tuning))
+
+
 def cf_stitch_add_layernorm(A, R, gamma, beta, out, rows, cols, eps, workspace, workspace_bytes, stream=None,
                             tuning=None) -> int:
     """out = LayerNorm(A + R) * gamma + beta over each row (R may be None)."""
@@ -515,11 +531,12 @@ def stitch_batchnorm(A, gamma, beta, *, eps=1e-5, out=None, workspace=None, stre
     return O, mean, var
 
 
-def b2b_gemm(X, W1, W2, b1=None, *, op="softmax", alpha=1.0, out=None, workspace=None, stream=None,
-             tuning=None):
-    """O = bf16(F(alpha*X@W1 + b1)) @ W2, F = "softmax" (rows) or "gelu_tanh"; bf16 CUDA tensors."""
+def b2b_gemm(X, W1, W2, b1=None, *, op="softmax", alpha=1.0, gamma1=None, beta1=None, eps=1e-5, out=None,
+             workspace=None, stream=None, tuning=None):
+    """O = bf16(F(alpha*X@W1 + b1)) @ W2, F = "softmax" (rows), "gelu_tanh" or "layernorm" (rows, with
+    gamma1, beta1); bf16 CUDA tensors."""
     import torch
-    ops = {"softmax": CF_B2B_SOFTMAX, "gelu_tanh": CF_B2B_GELU_TANH}
+    ops = {"softmax": CF_B2B_SOFTMAX, "gelu_tanh": CF_B2B_GELU_TANH, "layernorm": CF_B2B_LAYERNORM}
     if op not in ops:
         raise ValueError(f"unknown op {op!r}")
     M, K = X.shape
@@ -527,8 +544,12 @@ def b2b_gemm(X, W1, W2, b1=None, *, op="softmax", alpha=1.0, out=None, workspace
     N2 = W2.shape[1]
     O = out if out is not None else torch.empty((M, N2), dtype=torch.bfloat16, device=X.device)
     ws = workspace if workspace is not None else new_workspace(cf_b2b_workspace_size(), X.device, stream)
-    check(cf_b2b_gemm(X, W1, b1, W2, O, M, K, N1, N2, alpha, ops[op], ws, ws.numel(), stream, tuning),
-          "cf_b2b_gemm")
+    if op == "layernorm":
+        check(cf_b2b_gemm_layernorm(X, W1, b1, gamma1, beta1, W2, O, M, K, N1, N2, alpha, eps, ws, ws.numel(),
+                                    stream, tuning), "cf_b2b_gemm_layernorm")
+    else:
+        check(cf_b2b_gemm(X, W1, b1, W2, O, M, K, N1, N2, alpha, ops[op], ws, ws.numel(), stream, tuning),
+              "cf_b2b_gemm")
     return O
 
 

@@ -1,15 +1,16 @@
 // b2b.cu -- back-to-back GEMM with the intermediate kept on chip:
 //     O = S . W2,   S = F(alpha * X.W1 + b1) in bf16,   F = row softmax or GELU
-// ([ComFuse] B2BGEMM, Eqs. 3-7, Fig. 5).
+// ([ComFuse] B2BGEMM, Eqs. 3-7, Fig. 5); F = row softmax, GELU(tanh) or row
+// LayerNorm over the N1 columns.
 //
 // Design (sm_103a):
 //  * A cluster of C CTAs takes one 128-row block at a time; CTA rank r owns
 //    the 256 columns [256 r, 256 r + 256) of the intermediate P = X.W1 (the
 //    output space of MatMul_1 is partitioned along N1, Fig. 5).
 //  * ML_1: tcgen05.mma accumulates P_tile (128 x 256, fp32) in tensor memory.
-//  * Epi_1: F over P_tile.  For softmax the row statistics (max, sum exp)
-//    are reduced over the cluster: every thread sends its row's partial to
-//    each CTA with an 8-byte st.async.  S_tile = F(P_tile) is written back to
+//  * Epi_1: F over P_tile.  For softmax (max, sum exp) and LayerNorm
+//    (mean, M2) the row statistics are reduced over the cluster: every thread
+//    sends its row's partial to each CTA with an 8-byte st.async.  S_tile = F(P_tile) is written back to
 //    tensor memory as packed bf16 over the first 128 (consumed) columns of
 //    P, so S never leaves the SM (Eq. 3 keeps it in registers; tcgen05.mma
 //    reads a register-like A operand from tensor memory instead).
@@ -62,7 +63,7 @@ struct Layout {
     uint32_t ring, slot, recv, prm, bars, total;
 };
 
-__host__ __device__ inline Layout layout(int stages, int C, int N2) {
+__host__ __device__ inline Layout layout(int stages, int C, int N2, int op) {
     Layout L;
     L.ring = 0;
     uint32_t off = uint32_t(stages) * kStageBytes;
@@ -71,8 +72,8 @@ __host__ __device__ inline Layout layout(int stages, int C, int N2) {
     L.recv = off;  // float4 [C][N2 / C / 4][128]: the partial output columns this CTA owns
                    // (row fastest, so a warp's 32 rows fill 512 consecutive bytes)
     off += 128u * uint32_t(N2) * 4u;
-    L.prm = off;   // float [256]: b1 of this CTA's columns
-    off += kN1Slice * 4u;
+    L.prm = off;   // float [256] b1 (LayerNorm F: [3][256] b1, gamma1, beta1) of this CTA's columns
+    off += (op == 2 ? 3u : 1u) * kN1Slice * 4u;
     L.bars = off;
     off += 256;
     L.total = off;
@@ -99,7 +100,7 @@ __device__ __forceinline__ Bars bars_at(uint32_t b, int stages) {
     return r;
 }
 
-template <int OP, int kN2>  // OP: 0 softmax, 1 GELU; kN2: 64 or 128
+template <int OP, int kN2>  // OP: 0 softmax, 1 GELU, 2 LayerNorm; kN2: 64 or 128
 __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant__ B2bArgs a, int stages) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = ptx::smem_u32(smem_raw);
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
     const int w = kN2 / C;  // output columns owned by each CTA
     const int nk1 = (a.K + kBK - 1) / kBK;  // a ragged last block reads zeros past K
     constexpr int nk2 = kN1Slice / kBK;     // 4
-    const Layout L = layout(stages, C, kN2);
+    const Layout L = layout(stages, C, kN2, OP);
     const Bars B = bars_at(base + L.bars, stages);
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem_raw + (B.misc - base));
     volatile uint32_t *abort = misc + 1;
@@ -311,7 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
         const float4 *recv = reinterpret_cast<const float4 *>(smem_raw + L.recv);
         const int w4 = w / 4;
         const int n0 = int(rank) * kN1Slice;
-        for (int c = threadIdx.x - 64; c < kN1Slice; c += 256) prm[c] = a.b1 ? __ldg(a.b1 + n0 + c) : 0.f;
+        for (int c = threadIdx.x - 64; c < kN1Slice; c += 256) {
+            prm[c] = a.b1 ? __ldg(a.b1 + n0 + c) : 0.f;
+            if constexpr (OP == 2) {
+                prm[kN1Slice + c] = __ldg(a.gamma1 + n0 + c);
+                prm[2 * kN1Slice + c] = __ldg(a.beta1 + n0 + c);
+            }
+        }
         ptx::named_bar_sync(1, 256);
         for (int t = g, j = 0; t < T; t += 2, ++j) {
             const uint32_t par = uint32_t(j) & 1u;
@@ -378,6 +385,61 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
                         sv[k] = ptx::pack_bf16x2(__uint_as_float(v[2 * k]) * f, __uint_as_float(v[2 * k + 1]) * f);
+                    ptx::tmem_st16(tg + c * 16, sv);
+                }
+            } else if constexpr (OP == 2) {
+                // pass 1: z = alpha * P + b1 back into tensor memory; (mean, M2) of
+                // the row slice, two passes per 32-column fragment, folded by counts
+                MeanM2 acc{0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t v[32];
+                    float z[32];
+                    ptx::tmem_ld32(tg + c * 32, v);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        z[k] = fmaf(a.alpha, __uint_as_float(v[k]), prm[c * 32 + k]);
+                        v[k] = __float_as_uint(z[k]);
+                    }
+                    const MeanM2 cm = chunk_mean_m2(z);
+                    acc = c == 0 ? cm : combine_counts(acc, float(32 * c), cm, 32.f);
+                    ptx::tmem_st32(tg + c * 32, v);
+                }
+                ptx::tmem_st_wait();
+                if (lead) trace_tile(tr, t, CF_TRB_EPI1_LOCAL);
+                // row statistics over the cluster (every CTA holds 256 of the row's
+                // N1 values): each thread sends its (mean, M2) to every CTA, the
+                // gatherers fold them in rank order
+                const uint32_t xb = B.xfull + 8 * g;
+                MeanM2 st = acc;
+                if (C > 1 && !*abort) {
+                    if (lead) ptx::mbar_arrive_expect_tx(xb, uint32_t(C) * 1024u);
+                    const uint32_t mine = base + L.slot + (uint32_t(g) * uint32_t(C) + rank) * 1024u + uint32_t(row) * 8u;
+                    for (int r = 0; r < C; ++r)
+                        ptx::st_async_f2(ptx::mapa(mine, uint32_t(r)), acc.mean, acc.m2, ptx::mapa(xb, uint32_t(r)));
+                    if (!ptx::mbar_wait_bounded<true>(xb, par, tmo, abort, a.err, kInfoEpi | 0x10u | g)) break;
+                    st = MeanM2{slot[row].x, slot[row].y};
+                    for (int r = 1; r < C; ++r) {
+                        const float2 o = slot[r * 128 + row];
+                        st = combine_counts(st, float(kN1Slice * r), MeanM2{o.x, o.y}, float(kN1Slice));
+                    }
+                }
+                const float rstd = rsqrtf(st.m2 / float(kN1Slice * C) + a.eps);
+                // pass 2: S = (z - mean) * rstd * gamma1 + beta1, packed bf16
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t v[32], sv[16];
+                    ptx::tmem_ld32(tg + c * 32, v);
+                    ptx::tmem_ld_wait();
+                    const float *ga = prm + kN1Slice + c * 32, *be = prm + 2 * kN1Slice + c * 32;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float y0 = fmaf((__uint_as_float(v[2 * k]) - st.mean) * rstd, ga[2 * k], be[2 * k]);
+                        const float y1 =
+                            fmaf((__uint_as_float(v[2 * k + 1]) - st.mean) * rstd, ga[2 * k + 1], be[2 * k + 1]);
+                        sv[k] = ptx::pack_bf16x2(y0, y1);
+                    }
                     ptx::tmem_st16(tg + c * 16, sv);
                 }
             } else {
@@ -473,15 +535,19 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
     if (threadIdx.x == 64) trace_stamp(tr, 3);
 }
 
+template <int OP>
+void *b2b_fn_n2(int n2) {
+    return n2 == 64 ? reinterpret_cast<void *>(&b2b_kernel<OP, 64>) : reinterpret_cast<void *>(&b2b_kernel<OP, 128>);
+}
 void *b2b_fn(int op, int n2) {
-    if (op == 0) return n2 == 64 ? reinterpret_cast<void *>(&b2b_kernel<0, 64>)
-                                 : reinterpret_cast<void *>(&b2b_kernel<0, 128>);
-    return n2 == 64 ? reinterpret_cast<void *>(&b2b_kernel<1, 64>) : reinterpret_cast<void *>(&b2b_kernel<1, 128>);
+    if (op == 0) return b2b_fn_n2<0>(n2);
+    if (op == 1) return b2b_fn_n2<1>(n2);
+    return b2b_fn_n2<2>(n2);
 }
 
 }  // namespace
 
-int b2b_smem_bytes(int stages, int cluster, int n2) { return int(layout(stages, cluster, n2).total); }
+int b2b_smem_bytes(int stages, int cluster, int n2, int op) { return int(layout(stages, cluster, n2, op).total); }
 
 int b2b_max_active_clusters(int op, int cluster, int n2, int smem) {
     void *fn = b2b_fn(op, n2);

@@ -857,7 +857,7 @@ static int b2b_active_cached(int device, int op, int cluster, int n2, int smem) 
 static cf_status b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, int op, const cf_tuning *tuning,
                           const cf::DeviceInfo &dev, cf_plan *plan) {
     if (M < 0 || K <= 0 || N1 <= 0 || N2 <= 0) return CF_ERR_INVALID_ARG;
-    if (op != CF_B2B_SOFTMAX && op != CF_B2B_GELU_TANH) return CF_ERR_INVALID_ARG;
+    if (op != CF_B2B_SOFTMAX && op != CF_B2B_GELU_TANH && op != CF_B2B_LAYERNORM) return CF_ERR_INVALID_ARG;
     if (K % 8 != 0 || N1 % 256 != 0 || (N2 != 64 && N2 != 128)) return CF_ERR_UNSUPPORTED;
     const int64_t C = N1 / 256;
     if (C != 1 && C != 2 && C != 4 && C != 8) return CF_ERR_UNSUPPORTED;
@@ -865,8 +865,8 @@ static cf_status b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, int op, 
     const int req = tuning ? tuning->stages : 0;
     if (req < 0 || req > 6) return CF_ERR_UNSUPPORTED;
     int stages = req > 0 ? req : 4;
-    while (stages > 2 && cf::b2b_smem_bytes(stages, int(C), int(N2)) > kMaxSmem) --stages;
-    const int smem = cf::b2b_smem_bytes(stages, int(C), int(N2));
+    while (stages > 2 && cf::b2b_smem_bytes(stages, int(C), int(N2), op) > kMaxSmem) --stages;
+    const int smem = cf::b2b_smem_bytes(stages, int(C), int(N2), op);
     if (smem > kMaxSmem || smem > dev.max_smem_optin) return CF_ERR_UNSUPPORTED;
     std::memset(plan, 0, sizeof(*plan));
     plan->n_slice = 256;
@@ -894,13 +894,16 @@ cf_status cf_query_b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, cf_b2b
     return b2b_plan(M, K, N1, N2, int(op), tuning, dev, plan);
 }
 
-cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, const void *W2, void *O, int64_t M,
-                         int64_t K, int64_t N1, int64_t N2, float alpha, cf_b2b_op op, void *ws, size_t ws_bytes,
-                         cf_stream_t stream, const cf_tuning *tuning) {
+static cf_status b2b_common(const void *X, const void *W1, const float *b1, const float *gamma1,
+                            const float *beta1, const void *W2, void *O, int64_t M, int64_t K, int64_t N1,
+                            int64_t N2, float alpha, float eps, int op, void *ws, size_t ws_bytes,
+                            cf_stream_t stream, const cf_tuning *tuning) {
     if (M < 0 || K <= 0 || N1 <= 0 || N2 <= 0) return CF_ERR_INVALID_ARG;
-    if (op != CF_B2B_SOFTMAX && op != CF_B2B_GELU_TANH) return CF_ERR_INVALID_ARG;
+    if (op != CF_B2B_SOFTMAX && op != CF_B2B_GELU_TANH && op != CF_B2B_LAYERNORM) return CF_ERR_INVALID_ARG;
     if (!X || !W1 || !W2 || !O || !ws) return CF_ERR_INVALID_ARG;
-    if (!aligned16(X) || !aligned16(W1) || !aligned16(W2) || !aligned16(O) || (b1 && !aligned16(b1)))
+    if (op == CF_B2B_LAYERNORM && (!gamma1 || !beta1)) return CF_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W1) || !aligned16(W2) || !aligned16(O) || (b1 && !aligned16(b1)) ||
+        (gamma1 && !aligned16(gamma1)) || (beta1 && !aligned16(beta1)))
         return CF_ERR_MISALIGNED;
     if (O == X || O == W1 || O == W2) return CF_ERR_INVALID_ARG;
     if (K % 8 != 0 || N1 % 256 != 0 || (N2 != 64 && N2 != 128)) return CF_ERR_UNSUPPORTED;
@@ -909,7 +912,7 @@ cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, const v
     if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
     if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
     cf_plan plan;
-    cf_status st = b2b_plan(M, K, N1, N2, int(op), tuning, dev, &plan);
+    cf_status st = b2b_plan(M, K, N1, N2, op, tuning, dev, &plan);
     if (st != CF_OK) return st;
     if (M == 0) return CF_OK;
 
@@ -919,6 +922,9 @@ cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, const v
     if (!make_tmap_w(&a.tmap_w1, W1, uint64_t(K), uint64_t(N1), 4)) return CF_ERR_CUDA;
     if (!make_tmap_w(&a.tmap_w2, W2, uint64_t(N1), uint64_t(N2), uint32_t(N2 / 64))) return CF_ERR_CUDA;
     a.b1 = b1;
+    a.gamma1 = gamma1;
+    a.beta1 = beta1;
+    a.eps = eps;
     a.out = static_cast<uint16_t *>(O);
     a.err = static_cast<uint32_t *>(ws);
     a.M = int(M);
@@ -931,16 +937,39 @@ cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, const v
     a.timeout_ns = 1000ull * tus;
     a.trace = tuning ? reinterpret_cast<unsigned long long *>(tuning->trace) : nullptr;
     const bool pdl = !(tuning && tuning->disable_pdl);
-    cudaError_t e = cf::launch_b2b(int(op), a, plan.clusters, plan.stages, plan.smem_bytes, pdl,
+    cudaError_t e = cf::launch_b2b(op, a, plan.clusters, plan.stages, plan.smem_bytes, pdl,
                                    reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return CF_OK;
+}
+
+cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, const void *W2, void *O, int64_t M,
+                         int64_t K, int64_t N1, int64_t N2, float alpha, cf_b2b_op op, void *ws, size_t ws_bytes,
+                         cf_stream_t stream, const cf_tuning *tuning) {
+    if (op == CF_B2B_LAYERNORM) return CF_ERR_INVALID_ARG;  // needs gamma1, beta1: cf_b2b_gemm_layernorm
+    return b2b_common(X, W1, b1, nullptr, nullptr, W2, O, M, K, N1, N2, alpha, 0.f, int(op), ws, ws_bytes, stream,
+                      tuning);
 }
 
 cf_status cf_b2b_gemm(const void *X, const void *W1, const float *b1, const void *W2, void *O, int64_t M, int64_t K,
                       int64_t N1, int64_t N2, float alpha, cf_b2b_op op, void *ws, size_t ws_bytes,
                       cf_stream_t stream) {
     return cf_b2b_gemm_ex(X, W1, b1, W2, O, M, K, N1, N2, alpha, op, ws, ws_bytes, stream, nullptr);
+}
+
+cf_status cf_b2b_gemm_layernorm_ex(const void *X, const void *W1, const float *b1, const float *gamma1,
+                                   const float *beta1, const void *W2, void *O, int64_t M, int64_t K, int64_t N1,
+                                   int64_t N2, float alpha, float eps, void *ws, size_t ws_bytes, cf_stream_t stream,
+                                   const cf_tuning *tuning) {
+    return b2b_common(X, W1, b1, gamma1, beta1, W2, O, M, K, N1, N2, alpha, eps, CF_B2B_LAYERNORM, ws, ws_bytes,
+                      stream, tuning);
+}
+
+cf_status cf_b2b_gemm_layernorm(const void *X, const void *W1, const float *b1, const float *gamma1,
+                                const float *beta1, const void *W2, void *O, int64_t M, int64_t K, int64_t N1,
+                                int64_t N2, float alpha, float eps, void *ws, size_t ws_bytes, cf_stream_t stream) {
+    return cf_b2b_gemm_layernorm_ex(X, W1, b1, gamma1, beta1, W2, O, M, K, N1, N2, alpha, eps, ws, ws_bytes, stream,
+                                    nullptr);
 }
 
 }  // extern "C"

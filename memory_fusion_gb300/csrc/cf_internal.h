@@ -177,6 +177,9 @@ struct B2bArgs {
     CUtensorMap tmap_w1;  // W1 [K,N1] bf16 as {64, K, N1/64}, box {64, 64, 4}
     CUtensorMap tmap_w2;  // W2 [N1,N2] bf16 as {64, N1, N2/64}, box {64, 64, N2/64}
     const float *b1;      // [N1] or null
+    const float *gamma1;  // LayerNorm F: [N1]
+    const float *beta1;   // LayerNorm F: [N1]
+    float eps;            // LayerNorm F
     uint16_t *out;        // O [M,N2] bf16
     uint32_t *err;        // workspace error word
     int M, K, N1, N2;
@@ -186,7 +189,7 @@ struct B2bArgs {
     unsigned long long *trace;  // optional %globaltimer stamps, CF_TRACE_SLOTS per CTA
 };
 
-int b2b_smem_bytes(int stages, int cluster, int n2);
+int b2b_smem_bytes(int stages, int cluster, int n2, int op);
 int b2b_max_active_clusters(int op, int cluster, int n2, int smem);
 cudaError_t launch_b2b(int op, const B2bArgs &a, int clusters, int stages, int smem, bool pdl, cudaStream_t stream);
 

@@ -20,7 +20,8 @@ made in argument order):
   beta[cols] ~ N(0, 0.1) fp32.
 * Back-to-back GEMM workloads: X[M,K], W1[K,N1], W2[N1,N2] (bf16, N(0,
   x_std), N(0, w1_std), N(0, w2_std)), then b1[N1] ~ N(0, b1_std) fp32 (not
-  drawn when b1_std is None).
+  drawn when b1_std is None), then (LayerNorm epilogue) gamma1 ~ N(1, 0.1),
+  beta1 ~ N(0, 0.1) [N1] fp32.
 
 "N(0, s)" means standard deviation s throughout.
 """
@@ -137,7 +138,7 @@ class StitchNormWorkload:
 @dataclass(frozen=True)
 class B2bWorkload:
     name: str
-    op: str                # "softmax" | "gelu_tanh"
+    op: str                # "softmax" | "gelu_tanh" | "layernorm"
     M: int
     K: int
     N1: int
@@ -157,10 +158,12 @@ class B2bWorkload:
 
     @property
     def unavoidable_bytes(self) -> int:
-        """X, W1, b1, W2 read once and O written once; S never leaves the chip."""
+        """X, W1, b1 (gamma1, beta1), W2 read once and O written once; S never leaves the chip."""
         b = 2 * self.M * self.K + 2 * self.K * self.N1 + 2 * self.N1 * self.N2 + 2 * self.M * self.N2
         if self.b1_std is not None:
             b += 4 * self.N1
+        if self.op == "layernorm":
+            b += 8 * self.N1
         return b
 
 
@@ -207,6 +210,11 @@ WORKLOADS = {
         b1_std=0.1,
         description="B2BGEMM with bias+GELU(tanh) between the GEMMs, MLP-shaped: "
                     "X[16384,1024] W1[1024,2048] W2[2048,128]"),
+    "b2b_ln_16384x1024x2048x128": B2bWorkload(
+        "b2b_ln_16384x1024x2048x128", "layernorm", 16384, 1024, 2048, 128, 14, 1.0, _c(1024), _c(2048),
+        b1_std=0.1,
+        description="B2BGEMM with bias+LayerNorm over N1 between the GEMMs: "
+                    "X[16384,1024] W1[1024,2048] W2[2048,128], gamma1 ~ N(1,0.1), beta1 ~ N(0,0.1)"),
     "addln_750000x32": StitchNormWorkload(
         "addln_750000x32", "add_layernorm", 750000, 32, 10,
         description="stitched add + LayerNorm over rows, very many tiny rows"),
@@ -261,14 +269,17 @@ def stitch_inputs(rows: int, cols: int, seed: int = 3) -> dict:
 
 
 def b2b_inputs(M: int, K: int, N1: int, N2: int, seed: int, *, x_std: float = 1.0, w1_std: float = 1.0,
-               w2_std: float = 1.0, b1_std: float | None = None) -> dict:
-    """X, W1, W2 (bf16-valued float32) and b1 (float32, or None)."""
+               w2_std: float = 1.0, b1_std: float | None = None, ln: bool = False) -> dict:
+    """X, W1, W2 (bf16-valued float32), b1 (float32, or None) and, for the
+    LayerNorm epilogue, gamma1 ~ N(1, 0.1) and beta1 ~ N(0, 0.1) (float32)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     out = {}
     out["X"] = round_to_bf16(_normal(rng, (M, K), x_std))
     out["W1"] = round_to_bf16(_normal(rng, (K, N1), w1_std))
     out["W2"] = round_to_bf16(_normal(rng, (N1, N2), w2_std))
     out["b1"] = None if b1_std is None else _normal(rng, (N1,), b1_std)
+    out["gamma1"] = _normal(rng, (N1,), 0.1, 1.0) if ln else None
+    out["beta1"] = _normal(rng, (N1,), 0.1) if ln else None
     return out
 
 
@@ -291,7 +302,7 @@ def workload_inputs(name: str) -> dict:
         return stitch_norm_inputs(w.rows, w.cols, w.seed, with_R=w.kind == "add_layernorm")
     if isinstance(w, B2bWorkload):
         return b2b_inputs(w.M, w.K, w.N1, w.N2, w.seed, x_std=w.x_std, w1_std=w.w1_std, w2_std=w.w2_std,
-                          b1_std=w.b1_std)
+                          b1_std=w.b1_std, ln=w.op == "layernorm")
     if w.kind in ("rownorm", "rmsnorm"):
         return gemm_inputs(w.M, w.N, w.K, w.seed, x_std=w.x_std, w_std=w.w_std,
                            bias_std=w.bias_std, gamma_std=w.gamma_std,

@@ -1,5 +1,6 @@
 """GPU parity of the back-to-back GEMM O = bf16(F(alpha X.W1 + b1)) . W2
-(through the C ABI) against the fp64 oracle: both epilogues, every cluster
+(through the C ABI) against the fp64 oracle: the softmax, GELU and
+LayerNorm epilogues, every cluster
 width N1/256 in {1, 2, 4, 8}, both output widths, ragged rows and a ragged
 last K block, several row blocks per cluster (the ring, tensor memory and the
 reduce-scatter buffer reused across tiles), ring depths, a selector W2 that
@@ -13,8 +14,9 @@ kernel's S carries its own fp32 error e_j.  So per output element
     |O - O_ref| <= sum_j (2^-7 |s_j| + e_j) |W2_jk| + N1 2^-24 sum_j |s_j W2_jk|
                    + half a bf16 ulp of the output,
 
-with e_j <= 2^-16 |s_j| (exp2/FMA chain) and, for GELU, e_j also carries the
-tanh.approx absolute error 2^-10.98 times 0.5 |z_j|.  The bound assumes every
+with e_j <= 2^-16 |s_j| (exp2/FMA chain); for GELU, e_j also carries the
+tanh.approx absolute error 2^-10.98 times 0.5 |z_j|; for LayerNorm, the fp32
+row statistics add up to 2^-14 (|s_j| + 1) (the normalised values are O(1)).  The bound assumes every
 S element flips, so the mean error is checked as well: at most half a bf16
 ulp of the output on average plus 2^-12 of the flip term (a flip fraction
 far above what rounding noise produces fails it).
@@ -28,7 +30,7 @@ from tests.gpu_util import bf16_half_ulp, dev_bf16, dev_f32, host, sample_rows, 
 
 pytestmark = pytest.mark.gpu
 
-OPS = {"softmax": cf.CF_B2B_SOFTMAX, "gelu_tanh": cf.CF_B2B_GELU_TANH}
+OPS = {"softmax": cf.CF_B2B_SOFTMAX, "gelu_tanh": cf.CF_B2B_GELU_TANH, "layernorm": cf.CF_B2B_LAYERNORM}
 
 
 def _run(d, op, alpha, tuning=None, expect=cf.CF_OK):
@@ -40,7 +42,11 @@ def _run(d, op, alpha, tuning=None, expect=cf.CF_OK):
     b1 = dev_f32(d.get("b1"))
     O = torch.full((max(M, 1), N2), float("nan"), dtype=torch.bfloat16, device="cuda")
     ws = cf.new_workspace(cf.cf_b2b_workspace_size())
-    st = cf.cf_b2b_gemm(X, W1, b1, W2, O, M, K, N1, N2, alpha, OPS[op], ws, ws.numel(), None, tuning)
+    if op == "layernorm":
+        st = cf.cf_b2b_gemm_layernorm(X, W1, b1, dev_f32(d["gamma1"]), dev_f32(d["beta1"]), W2, O, M, K, N1, N2,
+                                      alpha, 1e-5, ws, ws.numel(), None, tuning)
+    else:
+        st = cf.cf_b2b_gemm(X, W1, b1, W2, O, M, K, N1, N2, alpha, OPS[op], ws, ws.numel(), None, tuning)
     assert st == expect, cf.status_string(st)
     torch.cuda.synchronize()
     dst, info = cf.cf_get_device_status(ws)
@@ -48,11 +54,19 @@ def _run(d, op, alpha, tuning=None, expect=cf.CF_OK):
     return host(O)[:M]
 
 
+def _s(d, op, z):
+    if op == "softmax":
+        return oracle.softmax_rows(z)
+    if op == "gelu_tanh":
+        return oracle.gelu_tanh(z)
+    return oracle.layernorm_rows(z, d["gamma1"], d["beta1"], 1e-5)
+
+
 def _terms(d, op, alpha, rows=None):
     """Per element of the output: sum_j |s_j||W2_jk| and sum_j |z_j||W2_jk|."""
     X = d["X"] if rows is None else d["X"][rows]
     z = alpha * oracle.gemm(X, d["W1"]) + (0.0 if d.get("b1") is None else np.asarray(d["b1"], np.float64))
-    s = oracle.softmax_rows(z) if op == "softmax" else oracle.gelu_tanh(z)
+    s = _s(d, op, z)
     aw = np.abs(np.asarray(d["W2"], np.float64))
     return np.abs(s) @ aw, np.abs(z) @ aw
 
@@ -64,6 +78,8 @@ def check_b2b(o, ref, d, op, alpha, what, rows=None):
     flip = (2.0 ** -7 + 2.0 ** -16 + N1 * 2.0 ** -24) * A
     if op == "gelu_tanh":
         flip = flip + 0.5 * 2.0 ** -10.98 * Z
+    if op == "layernorm":  # fp32 statistics: an error near 2^-14 of the row spread in each S element
+        flip = flip + 2.0 ** -14 * (A + np.abs(np.asarray(d["W2"], np.float64)).sum(axis=0))
     bound = flip + bf16_half_ulp(np.abs(ref) + flip)
     err = np.abs(o - ref)
     worst = np.argmax(err - bound)
@@ -75,21 +91,27 @@ def check_b2b(o, ref, d, op, alpha, what, rows=None):
 
 def _inputs(M, K, N1, N2, seed, op, b1=True):
     return inputs.b2b_inputs(M, K, N1, N2, seed, x_std=1.0, w1_std=K ** -0.5,
-                             w2_std=1.0 if op == "softmax" else N1 ** -0.5, b1_std=0.2 if b1 else None)
+                             w2_std=1.0 if op == "softmax" else N1 ** -0.5, b1_std=0.2 if b1 else None,
+                             ln=op == "layernorm")
 
 
-@pytest.mark.parametrize("op", ["softmax", "gelu_tanh"])
+def _ref(d, op, alpha, rows=None):
+    return oracle.b2b_gemm(d["X"], d["W1"], d["W2"], op=op, alpha=alpha, b1=d["b1"], rows=rows,
+                           gamma1=d.get("gamma1"), beta1=d.get("beta1"), eps=1e-5)
+
+
+@pytest.mark.parametrize("op", ["softmax", "gelu_tanh", "layernorm"])
 @pytest.mark.parametrize("M,K,N1,N2", [(128, 64, 256, 64), (200, 128, 512, 128), (333, 128, 1024, 64),
                                        (257, 192, 2048, 128), (130, 136, 1024, 128)])
 def test_b2b_shapes(op, M, K, N1, N2):
     d = _inputs(M, K, N1, N2, seed=M + K + N1 + N2, op=op)
     alpha = K ** -0.5 if op == "softmax" else 1.0
     o = _run(d, op, alpha)
-    ref = oracle.b2b_gemm(d["X"], d["W1"], d["W2"], op=op, alpha=alpha, b1=d["b1"])
+    ref = _ref(d, op, alpha)
     check_b2b(o, ref, d, op, alpha, f"b2b {op} {M}x{K}x{N1}x{N2}")
 
 
-@pytest.mark.parametrize("op", ["softmax", "gelu_tanh"])
+@pytest.mark.parametrize("op", ["softmax", "gelu_tanh", "layernorm"])
 @pytest.mark.parametrize("kw", [dict(max_clusters=1), dict(max_clusters=3, stages=2), dict(stages=3),
                                 dict(max_clusters=2, disable_pdl=1)])
 def test_b2b_persistent_tiles(op, kw):
@@ -98,11 +120,11 @@ def test_b2b_persistent_tiles(op, kw):
     d = _inputs(M, K, N1, N2, seed=17, op=op, b1=False)
     alpha = 0.25 if op == "softmax" else 1.0
     o = _run(d, op, alpha, tuning=cf.tuning(**kw))
-    ref = oracle.b2b_gemm(d["X"], d["W1"], d["W2"], op=op, alpha=alpha)
+    ref = _ref(d, op, alpha)
     check_b2b(o, ref, d, op, alpha, f"b2b {op} {kw}")
 
 
-@pytest.mark.parametrize("op", ["softmax", "gelu_tanh"])
+@pytest.mark.parametrize("op", ["softmax", "gelu_tanh", "layernorm"])
 @pytest.mark.parametrize("N1,N2", [(256, 64), (2048, 128)])
 def test_b2b_selector_reads_back_s(op, N1, N2):
     """W2 with a single 1 per column: O[:, k] = bf16(S[:, c_k]) exactly up to
@@ -117,9 +139,11 @@ def test_b2b_selector_reads_back_s(op, N1, N2):
     alpha = K ** -0.5
     o = _run(d, op, alpha)
     z = alpha * oracle.gemm(d["X"], d["W1"]) + np.asarray(d["b1"], np.float64)
-    s = oracle.softmax_rows(z) if op == "softmax" else oracle.gelu_tanh(z)
+    s = _s(d, op, z)
     sel = s[:, cols]
     e = 2.0 ** -16 * np.abs(sel) + (0.5 * 2.0 ** -10.98 * np.abs(z[:, cols]) if op == "gelu_tanh" else 0.0)
+    if op == "layernorm":
+        e = e + 2.0 ** -14 * (np.abs(sel) + 1.0)
     bound = 2 * bf16_half_ulp(np.abs(sel) + e) + e
     err = np.abs(o - sel)
     worst = np.argmax(err - bound)
@@ -140,7 +164,12 @@ def test_b2b_empty_and_unsupported():
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 96, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 12, 512, 128, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 4096, 128, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 128, 1.0, 3, ws, n) == cf.CF_ERR_INVALID_ARG
+    # the LayerNorm epilogue needs gamma1 and beta1: only through its own entry point
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 128, 1.0, 2, ws, n) == cf.CF_ERR_INVALID_ARG
+    g = torch.ones(512, device="cuda")
+    assert cf.cf_b2b_gemm_layernorm(X, W1, None, None, g, W2, O, 128, 128, 512, 128, 1.0, 1e-5, ws,
+                                    n) == cf.CF_ERR_INVALID_ARG
     assert cf.cf_b2b_gemm(X, W1, None, W2, X, 128, 128, 512, 128, 1.0, 0, ws, n) == cf.CF_ERR_INVALID_ARG
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 128, 1.0, 0, ws, 16) == cf.CF_ERR_WORKSPACE_TOO_SMALL
     torch.cuda.synchronize()
@@ -157,12 +186,13 @@ def test_b2b_plan():
     assert st == cf.CF_OK and p.cluster_size == 8 and p.clusters == 1
 
 
-@pytest.mark.parametrize("name", ["b2b_attn_32768x128x1024x128", "b2b_gelu_16384x1024x2048x128"])
+@pytest.mark.parametrize("name", ["b2b_attn_32768x128x1024x128", "b2b_gelu_16384x1024x2048x128",
+                                  "b2b_ln_16384x1024x2048x128"])
 def test_b2b_full_workload(name):
     w = inputs.WORKLOADS[name]
     d = inputs.workload_inputs(name)
     o = _run(d, w.op, w.alpha)
     rows = sample_rows(w.M, 384, seed=11)
-    ref = oracle.b2b_gemm(d["X"], d["W1"], d["W2"], op=w.op, alpha=w.alpha, b1=d["b1"], rows=rows)
+    ref = _ref(d, w.op, w.alpha, rows=rows)
     sub = dict(d, X=d["X"][rows])
     check_b2b(o[rows], ref, sub, w.op, w.alpha, name)
