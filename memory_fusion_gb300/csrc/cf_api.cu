@@ -908,13 +908,14 @@ static cf_status b2b_common(const void *X, const void *W1, const float *b1, cons
     if (O == X || O == W1 || O == W2) return CF_ERR_INVALID_ARG;
     if (K % 8 != 0 || N1 % 256 != 0 || (N2 != 64 && N2 != 128)) return CF_ERR_UNSUPPORTED;
     if (ws_bytes < cf_b2b_workspace_size()) return CF_ERR_WORKSPACE_TOO_SMALL;
+    if (N1 / 256 > 8) return CF_ERR_UNSUPPORTED;
+    if (M == 0) return CF_OK;
     cf::DeviceInfo dev;
     if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
     if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
     cf_plan plan;
     cf_status st = b2b_plan(M, K, N1, N2, op, tuning, dev, &plan);
     if (st != CF_OK) return st;
-    if (M == 0) return CF_OK;
 
     cf::B2bArgs a;
     std::memset(&a, 0, sizeof(a));

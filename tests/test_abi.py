@@ -198,3 +198,44 @@ def test_argument_errors_need_no_gpu():
     assert cf.cf_stitch_rowreduce_broadcast(16, 16, 16, 4, 300000, 16, 4096, 0) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_stitch_rowreduce_broadcast(18, 16, 16, 4, 32, 16, 4096, 0) == cf.CF_ERR_MISALIGNED
     assert L is not None
+
+
+def test_newer_entry_points_check_arguments_without_a_gpu():
+    big = 1 << 20
+    # back-to-back GEMM
+    assert cf.cf_b2b_workspace_size() == 256
+    assert cf.cf_b2b_gemm(None, 16, None, 16, 16, 128, 128, 512, 128, 1.0, 0, 16, big, 0) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 128, 512, 128, 1.0, 7, 16, big, 0) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_b2b_gemm(24, 32, None, 48, 64, 128, 128, 512, 128, 1.0, 0, 16, big, 0) == cf.CF_ERR_MISALIGNED
+    assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 128, 384, 128, 1.0, 0, 16, big, 0) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 128, 4096, 128, 1.0, 0, 16, big, 0) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 12, 512, 128, 1.0, 0, 16, big, 0) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 128, 512, 96, 1.0, 0, 16, big, 0) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 128, 512, 128, 1.0, 0, 80, 8, 0) == cf.CF_ERR_WORKSPACE_TOO_SMALL
+    # the output may not alias an input
+    assert cf.cf_b2b_gemm(16, 32, None, 48, 16, 128, 128, 512, 128, 1.0, 0, 64, big, 0) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 0, 128, 512, 128, 1.0, 0, 80, big, 0) == cf.CF_OK
+    # the LayerNorm epilogue needs gamma1 and beta1, and only has its own entry
+    assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 128, 512, 128, 1.0, 2, 80, big, 0) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_b2b_gemm_layernorm(16, 32, None, None, 16, 48, 64, 128, 128, 512, 128, 1.0, 1e-5, 80,
+                                    big, 0) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_b2b_gemm_layernorm(16, 32, None, 16, 16, 48, 64, 0, 128, 512, 128, 1.0, 1e-5, 80,
+                                    big, 0) == cf.CF_OK
+    # stitched add + LayerNorm
+    assert cf.cf_stitch_add_layernorm(16, None, 16, 16, 16, 0, 32, 1e-5, 16, 4096, 0) == cf.CF_OK
+    assert cf.cf_stitch_add_layernorm(16, None, None, 16, 16, 4, 32, 1e-5, 16, 4096, 0) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_stitch_add_layernorm(18, None, 16, 16, 16, 4, 32, 1e-5, 16, 4096, 0) == cf.CF_ERR_MISALIGNED
+    assert cf.cf_stitch_add_layernorm(16, 16, 16, 16, 16, 4, 300000, 1e-5, 16, 4096, 0) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_stitch_add_layernorm(16, 16, 16, 16, 16, 4, 32, 1e-5, 16, 8, 0) == cf.CF_ERR_WORKSPACE_TOO_SMALL
+    # stitched BatchNorm: the workspace covers either scheme
+    assert cf.cf_stitch_batchnorm_workspace_size(64, 30000) == cf.cf_stitch_batchnorm_workspace_size(750000, 32)
+    assert cf.cf_stitch_batchnorm_workspace_size(1, 1) >= 256 + 256 + 1024 * 128 * 8
+    assert cf.cf_stitch_batchnorm(16, 16, 16, 16, None, None, 0, 32, 1e-5, 16, 0, 0) == cf.CF_OK
+    assert cf.cf_stitch_batchnorm(16, 16, 16, 16, None, None, -2, 32, 1e-5, 16, big, 0) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_stitch_batchnorm(16, None, 16, 16, None, None, 8, 32, 1e-5, 16, big, 0) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_stitch_batchnorm(16, 16, 16, 16, 2, None, 8, 32, 1e-5, 16, big, 0) == cf.CF_ERR_MISALIGNED
+    assert cf.cf_stitch_batchnorm(16, 16, 16, 16, None, None, 8, 32, 1e-5, 16, 1024, 0) == \
+        cf.CF_ERR_WORKSPACE_TOO_SMALL
+    # plan queries need the device
+    assert cf.cf_query_stitch_batchnorm_plan(8, 32)[0] == cf.CF_ERR_NO_DEVICE
+    assert cf.cf_query_b2b_plan(128, 128, 512, 128, 0)[0] == cf.CF_ERR_NO_DEVICE
