@@ -460,6 +460,36 @@ def gemm_fused_rowsoftmax(X, W, bias=None, *, scale=1.0, out=None, workspace=Non
     return Y
 
 
+def gemm_fused_residual_norm(X, W, bias, R, gamma, beta=None, *, alpha=1.0, eps=1e-5, act="none", norm="layer",
+                             out=None, workspace=None, stream=None, tuning=None):
+    """Y = Norm(act(alpha*X@W + bias) + R)*gamma (+ beta), Norm = "layer" or "rms"; X, W, R bf16 CUDA tensors."""
+    import torch
+    M, K = X.shape
+    N = W.shape[1]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    ws = workspace if workspace is not None else new_workspace(cf_gemm_fused_workspace_size(M, N, K),
+                                                               X.device, stream)
+    a = {"none": CF_ACT_NONE, "gelu_tanh": CF_ACT_GELU_TANH}[act]
+    n = {"layer": CF_NORM_LAYER, "rms": CF_NORM_RMS}[norm]
+    check(cf_gemm_fused_residual_norm(X, W, bias, R, gamma, beta, Y, M, N, K, alpha, eps, a, n, ws, ws.numel(),
+                                      stream, tuning), "cf_gemm_fused_residual_norm")
+    return Y
+
+
+def gemm_fused_rowsoftmax_causal(X, W, bias=None, *, scale=1.0, offset=0, out=None, workspace=None, stream=None,
+                                 tuning=None):
+    """Y = softmax over each row of scale*X@W + bias keeping column j of row i iff j <= i + offset."""
+    import torch
+    M, K = X.shape
+    N = W.shape[1]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    ws = workspace if workspace is not None else new_workspace(cf_gemm_fused_workspace_size(M, N, K),
+                                                               X.device, stream)
+    check(cf_gemm_fused_rowsoftmax_causal(X, W, bias, Y, M, N, K, scale, offset, ws, ws.numel(), stream, tuning),
+          "cf_gemm_fused_rowsoftmax_causal")
+    return Y
+
+
 def cf_b2b_gemm_layernorm(X, W1, b1, gamma1, beta1, W2, O, M, K, N1, N2, alpha, eps, workspace, workspace_bytes,
                           stream=None, tuning=None) -> int:
     """O = bf16(LayerNorm(alpha*X.W1 + b1)*gamma1 + beta1) . W2 (LayerNorm over the N1 columns)."""
