@@ -240,7 +240,9 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
     // measured on GB300 with the device trace (128x256 tiles per CTA):
     //   mainloop  ~ 0.35 us per 64-deep k-block for a CTA pair, 0.50 us single
     //               (per 256 columns of W staged)
-    //   epilogue  ~ 4.5 us; + 1.5 + 0.2 G us when the row spans G > 1 clusters
+    //   epilogue  ~ 1.4 us + 3.1 us per 256 columns a thread's row slice holds
+    //               (4.5 us for a 256-column slice); + 1.5 + 0.2 G us when
+    //               the row spans G > 1 clusters
     //               (the global barrier waits for the slowest of G clusters);
     //               + 0.5 us for a CTA pair when K < 512
     //               + 0.05 C_N us for the cluster exchange (peer all-to-all), or
@@ -265,7 +267,9 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
         const double t_main = nk * (cm == 2 ? 0.35 : 0.50) * (ns / 256.0);
         const int pm = t.peer_max == 0 ? 8 : t.peer_max;
         const double t_x = (pm < 0 || cn > pm) ? 1.0 : 0.05 * cn;
-        const double t_epi = 4.5 + t_x + (g > 1 ? 1.5 + 0.2 * g : 0.0) + (cm == 2 && nk < 8 ? 0.5 : 0.0);
+        const double cols = wide ? 256.0 : double(ns);  // a wide tile splits its columns over both groups
+        const double t_epi = 1.4 + 3.1 * (cols / 256.0) + t_x + (g > 1 ? 1.5 + 0.2 * g : 0.0) +
+                             (cm == 2 && nk < 8 ? 0.5 : 0.0);
         *ncl_out = n;
         if (wide) return double(per) * (t_main + t_epi);
         return double((per + 1) / 2) * std::max(2.0 * t_main, t_epi) + t_main + (g > 1 ? per * 0.05 * g : 0.0);
@@ -273,9 +277,16 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
     int ns = 0, C = 0, CMs = 0, ncl = 0;
     {
         double best = 0.0;
-        const int cand[2] = {t.n_slice != 0 ? int(t.n_slice) : ns_narrow,
-                             (t.n_slice == 0 && N % 512 == 0) ? 512 : 0};
-        for (int ci = 0; ci < 2; ++ci) {
+        // narrower tiles than the widest that divides N only when the widest
+        // cannot give every SM a tile: more CTAs per row then shorten the
+        // latency chain (a one-row-block LayerNorm: 10.3 us at 256 columns,
+        // 6.8 us at 64 columns over a cluster of 8)
+        const bool few = int64_t(rb) * (N / ns_narrow) < int64_t(sm_count);
+        const int cand[4] = {t.n_slice != 0 ? int(t.n_slice) : ns_narrow,
+                             (t.n_slice == 0 && N % 512 == 0) ? 512 : 0,
+                             (t.n_slice == 0 && few && ns_narrow > 128) ? 128 : 0,
+                             (t.n_slice == 0 && few && ns_narrow > 64) ? 64 : 0};
+        for (int ci = 0; ci < 4; ++ci) {
             const int nsc = cand[ci];
             if (nsc == 0) continue;
             const int cpr = int(N / nsc);
@@ -644,6 +655,9 @@ static cf_status device_plan(int kind, int64_t M, int64_t N, int64_t K, const cf
     int ns = t.n_slice ? t.n_slice : ((N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64);
     if ((ns != 64 && ns != 128 && ns != 256 && ns != 512) || N % ns != 0) return CF_ERR_UNSUPPORTED;
     if (ns == 512) ns = 256;
+    // too few tiles to give every SM one: the planner also weighs narrower
+    // tiles, whose cluster sizes divide N / 64
+    if (t.n_slice == 0 && ((M + cf::kBlockM - 1) / cf::kBlockM) * (N / ns) < dev.sm_count) ns = 64;
     const int64_t cpr = N / ns;
     for (int c = 0; c <= 16; ++c) active[c] = 0;
     // residency is per SM (one CTA per SM at any of these shared-memory

@@ -76,12 +76,13 @@ def test_plan_forced_single_cluster_rows():
 def test_plan_chooses_fastest_predicted():
     """The automatic choice minimises the planner's time model: ceil(T/ncl) tiles per
     CTA in rounds of two (two accumulators, two epilogue groups), each round
-    max(2 mainloops, epilogue), plus the global barrier's skew."""
+    max(2 mainloops, epilogue), plus the global barrier's skew; the epilogue
+    grows with the columns of a thread's row slice."""
     cases = {
         (4096, 2048, 128): (4, 1, 1, 32),     # wide tiles: one per CTA, each row in one cluster of 4
         (16384, 4096, 4096): (1, 2, 16, 76),  # CTA pairs (cta_group::2), rows over 16 clusters
         (8192, 16384, 2048): (2, 2, 32, 36),  # CTA pairs, rows over 32 clusters
-        (128, 512, 256): (2, 1, 1, 1),        # one row block: no pair
+        (128, 512, 256): (8, 1, 1, 1),        # one row block: 64-column tiles over a cluster of 8, no pair
     }
     for (M, N, K), (C, CM, G, ncl) in cases.items():
         st, p = cf.cf_plan_gemm_fused(M, N, K, 152, GB300)
@@ -134,8 +135,11 @@ def test_plan_wide_rows_use_global_path():
     # cluster 8 forced: G = 8 and all 15 resident clusters are used
     st, p = cf.cf_plan_gemm_fused(8192, 16384, 2048, 152, GB300, cf.tuning(cluster_size=8))
     assert (p.cluster_size, p.groups, p.clusters) == (8, 8, 15)
-    # never more clusters than tickets
+    # never more clusters than tickets (one row block: 128-column tiles give
+    # every SM work, so G = 64 clusters of 2, one ticket each)
     st, p = cf.cf_plan_gemm_fused(128, 16384, 2048, 152, GB300, cf.tuning(cluster_size=2))
+    assert (p.n_slice, p.groups, p.clusters) == (128, 64, 64)
+    st, p = cf.cf_plan_gemm_fused(128, 16384, 2048, 152, GB300, cf.tuning(cluster_size=2, n_slice=256))
     assert (p.groups, p.clusters) == (32, 32)
 
 
@@ -155,9 +159,13 @@ def test_plan_shapes():
     assert (p.n_slice, p.ctas_per_row) == (64, 3)
     st, p = cf.cf_plan_gemm_fused(1, 384, 64, 152, _active({3: 40}))
     assert (p.n_slice, p.cluster_size, p.row_blocks, p.clusters) == (128, 3, 1, 1)
-    # tiny: one row block, one cluster of 2
+    # tiny: one row block, too few 256-column tiles to fill the GPU: 64-column
+    # tiles over one cluster of 8 (measured 6.8 us against 10.3 us at 256)
     st, p = cf.cf_plan_gemm_fused(128, 512, 256, 152, GB300)
-    assert (p.cluster_size, p.clusters, p.row_blocks) == (2, 1, 1)
+    assert (p.n_slice, p.cluster_size, p.clusters, p.row_blocks) == (64, 8, 1, 1)
+    # many row blocks: the widest tile stays (the headline softmax shape)
+    st, p = cf.cf_plan_gemm_fused(4096, 2048, 128, 152, GB300)
+    assert (p.n_slice, p.cluster_size, p.clusters) == (512, 4, 32)
 
 
 def test_workspace_sizes():
