@@ -9,9 +9,9 @@ input generator, which holds none of the method's arithmetic.
 What is computed, and where it is defined
 -----------------------------------------
 The pages describe *exact* fusion: the fused kernel must reach the result of
-the unfused operator chain ("semantics fully preserved", ComFuse, Fusion Spec
-IR, Eq. (10); ownership legality, sass2mlir "Kernel fusion", section
-"Epilogue fusion - the core technique").  So the oracle is the unfused chain
+the unfused operator chain (the fusion keeps the semantics of the unfused
+operators: ComFuse, Fusion Spec IR, Eq. (10); ownership legality: sass2mlir
+"Kernel fusion", section "Epilogue fusion - the core technique").  So the oracle is the unfused chain
 written out in float64 on the same (bf16 / fp32) input values:
 
 * MatMul      P = X . W                       (ComFuse, Eq. (6) notation)
@@ -144,8 +144,8 @@ def layernorm_rows(g, gamma, beta, eps: float) -> np.ndarray:
 
     mean = (1/N) sum g;  var = (1/N) sum (g - mean)^2  (biased);
     y = (g - mean) / sqrt(var + eps) * gamma + beta.
-    This is the "reduce over inputs but normalise using original values"
-    pattern the ComFuse Fusion Spec IR nests at a Reduction node: the first
+    This is the pattern the ComFuse Fusion Spec IR nests at a Reduction
+    node -- reduce over the inputs, then normalise the original values: the first
     reduction (mean) feeds the second (variance), whose statistic is then
     broadcast back over the row together with the bypassed values.
     """
