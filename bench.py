@@ -132,7 +132,7 @@ def roofline_time_s(w, peaks):
 
 
 KERNEL_TU = {"gemm_fused_kernel": "gemm_fused.cu", "stitch_": "stitch.cu", "b2b_kernel": "b2b.cu",
-             "addln_": "stitch_norm.cu", "bn_": "stitch_norm.cu"}
+             "b2b_stream_kernel": "b2b_stream.cu", "addln_": "stitch_norm.cu", "bn_": "stitch_norm.cu"}
 
 
 def kernel_source_hash(kernel):
@@ -423,8 +423,11 @@ def b2b_bytes_per_set(w):
     return w.unavoidable_bytes
 
 
-def b2b_kernel_name(w):
-    return {"softmax": "b2b_kernel<SOFTMAX>", "gelu_tanh": "b2b_kernel<GELU>", "layernorm": "b2b_kernel<LN>"}[w.op]
+def b2b_kernel_name(w, plan):
+    """The kernel the plan launches: the stream kernel (n_slice 128: one CTA per
+    row block) or the cluster kernel (n_slice 256)."""
+    op = {"softmax": "SOFTMAX", "gelu_tanh": "GELU", "layernorm": "LN"}[w.op]
+    return f"b2b_stream_kernel<{op}>" if plan.n_slice == 128 else f"b2b_kernel<{op}>"
 
 
 def torch_b2b_time(torch, runner, reps):
@@ -849,8 +852,8 @@ def run_b2b(args):
     t = ranks.max(t)
     t1 = t / n
     tf = mdist.job_throughput(w.flops * n, ws_, t) / 1e12
-    kernel = b2b_kernel_name(w)
     _, plan = cf.cf_query_b2b_plan(w.M, w.K, w.N1, w.N2, r.op)
+    kernel = b2b_kernel_name(w, plan)
     if rank == 0:
         print(json.dumps({"metric": "back-to-back GEMM TFLOP/s", "value": round(tf, 3), "unit": "TFLOP/s",
                           "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,

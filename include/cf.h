@@ -90,7 +90,8 @@ CF_API int cf_last_cuda_error(void);
 /* Tuning knobs.  Every field's zero value means "choose automatically".    */
 /* ------------------------------------------------------------------------ */
 typedef struct cf_tuning {
-    int32_t n_slice;        /* GEMM: columns of one CTA tile (64, 128, 256)        */
+    int32_t n_slice;        /* GEMM: columns of one CTA tile (64, 128, 256, 512);
+                               B2B: selects the kernel, 128 stream, 256 cluster   */
     int32_t cluster_size;   /* GEMM: CTAs per cluster along the row (1..16)
                                stitched: CTAs per row for the split mapping      */
     int32_t peer_max;       /* inter-CTA aggregation: peer all-to-all when the
@@ -397,15 +398,26 @@ CF_API cf_status cf_gemm_fused_rowsoftmax_causal_ex(const void *X, const void *W
 /* ------------------------------------------------------------------------ */
 /* O = bf16( S . W2 ),  S = bf16( F(alpha * X.W1 + b1) )
  *
- * [ComFuse] B2BGEMM, Eqs. 3-7 and Fig. 5: MatMul_1 is partitioned along the
- * intermediate dimension N1 over the C = N1/256 CTAs of a thread-block
- * cluster (256 columns each); the epilogue F turns each CTA's P tile into its
- * S tile in tensor memory (S never reaches global memory); MatMul_2 reads S
- * from there with the CTA's 256-row slice of W2 staged through the same
- * operand ring as X and W1; the C partial output tiles are summed across the
- * cluster (in rank order, deterministic) and written once.
- *   op   CF_B2B_SOFTMAX: F = row softmax over all N1 columns (the row max and
- *        sum are reduced across the cluster); CF_B2B_GELU_TANH: F = GELU(tanh)
+ * [ComFuse] B2BGEMM, Eqs. 3-7 and Fig. 5, in two kernels; S never reaches
+ * global memory in either.
+ *  - Cluster kernel (tuning n_slice = 256; the only one for LayerNorm):
+ *    MatMul_1 is partitioned along the intermediate dimension N1 over the
+ *    C = N1/256 CTAs of a thread-block cluster (256 columns each); the
+ *    epilogue F turns each CTA's P tile into its S tile in tensor memory;
+ *    MatMul_2 reads S from there with the CTA's 256-row slice of W2 staged
+ *    through the same operand ring as X and W1; the C partial output tiles
+ *    are summed across the cluster (in rank order, deterministic) and
+ *    written once.  N1 in {256, 512, 1024, 2048}.
+ *  - Stream kernel (n_slice = 128; the default for softmax and GELU): one
+ *    CTA per 128-row block; N1 in 256-column chunks through tensor memory,
+ *    MatMul_1 of the next chunk running while the epilogue works on the
+ *    current one; one O accumulator per row block.  Softmax is evaluated
+ *    online (running row max, raised with O rescaled only when a chunk passes
+ *    it by 2^8): the bf16 values fed to MatMul_2 are the exponentials against
+ *    that running max, and the division by the row sum is applied to the
+ *    fp32 O.  Any N1 that is a multiple of 256.
+ *   op   CF_B2B_SOFTMAX: F = row softmax over all N1 columns;
+ *        CF_B2B_GELU_TANH: F = GELU(tanh)
  *   X  (device) bf16 [M, K] row-major      W1 (device) bf16 [K, N1] row-major
  *   b1 (device) fp32 [N1] or NULL           W2 (device) bf16 [N1, N2] row-major
  *   O  (device) bf16 [M, N2] row-major, written; must not alias an input
@@ -414,7 +426,8 @@ CF_API cf_status cf_gemm_fused_rowsoftmax_causal_ex(const void *X, const void *W
  * S is rounded to bf16 before MatMul_2 (the operand precision of the tensor
  * core), as the unfused chain rounds the tensor it stores between the GEMMs.
  * Supported: M >= 0 (0 is a no-op); K > 0 with K % 8 == 0 (a ragged last
- * 64-deep block is zero-filled); N1 in {256, 512, 1024, 2048}; N2 in {64, 128}.
+ * 64-deep block is zero-filled); N1 % 256 == 0 (cluster kernel: N1 <= 2048);
+ * N2 in {64, 128}.
  * All pointers 16-byte aligned (CF_ERR_MISALIGNED).  Asynchronous on
  * `stream`; device-side timeouts are reported by cf_get_device_status. */
 typedef enum {
@@ -425,9 +438,11 @@ typedef enum {
 
 CF_API size_t cf_b2b_workspace_size(void);
 
-/* The launch the B2B calls would make on the current device (cluster_size =
- * C, clusters, stages, smem_bytes, row_blocks; n_slice = 256).  Tuning fields
- * used: stages, max_clusters (others ignored).  Synchronous, launches nothing. */
+/* The launch the B2B calls would make on the current device: n_slice 256
+ * (cluster kernel: cluster_size = C, clusters) or 128 (stream kernel:
+ * cluster_size = 1, clusters = CTAs); stages, smem_bytes, row_blocks.  Tuning
+ * fields used: n_slice, stages, max_clusters (others ignored).  Synchronous,
+ * launches nothing. */
 CF_API cf_status cf_query_b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, cf_b2b_op op,
                                    const cf_tuning *tuning, cf_plan *plan);
 
@@ -436,7 +451,8 @@ CF_API cf_status cf_b2b_gemm(const void *X, const void *W1, const float *b1, con
                              cf_b2b_op op, void *workspace, size_t workspace_bytes,
                              cf_stream_t stream);
 
-/* As cf_b2b_gemm; tuning fields used: stages, max_clusters, timeout_us,
+/* As cf_b2b_gemm; tuning fields used: n_slice (the kernel), stages,
+ * max_clusters (cluster kernel: clusters; stream kernel: CTAs), timeout_us,
  * disable_pdl, trace (per-tile events: cf_trb_event). */
 CF_API cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, const void *W2,
                                 void *O, int64_t M, int64_t K, int64_t N1, int64_t N2,
@@ -476,7 +492,11 @@ CF_API cf_status cf_b2b_gemm_layernorm_ex(const void *X, const void *W1, const f
  *   workspace (device) >= cf_stitch_workspace_size(rows, cols) bytes
  * Supported: rows >= 0, cols >= 0 (either 0 is a no-op), cols <= 262144.
  * 16-byte aligned A/out with cols % 4 == 0 take the 128-bit path; anything
- * else takes the scalar path of the same kernels. */
+ * else takes the scalar path of the same kernels.
+ * Tuning fields used (_ex): stitch_mapping (1 packed, 2 split), cluster_size
+ * (CTAs per split row), max_clusters (split: cap on clusters, each then walks
+ * several rows with the next row's loads in flight), peer_max, timeout_us,
+ * disable_pdl. */
 CF_API cf_status cf_stitch_rowreduce_broadcast(const float *A, const float *row_bias, float *out,
                                         int64_t rows, int64_t cols, void *workspace,
                                         size_t workspace_bytes, cf_stream_t stream);

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcf.so")
 
-SOURCES = ["cf_api.cu", "gemm_fused.cu", "stitch.cu", "stitch_norm.cu", "rowkernel.cu", "b2b.cu"]
+SOURCES = ["cf_api.cu", "gemm_fused.cu", "stitch.cu", "stitch_norm.cu", "rowkernel.cu", "b2b.cu", "b2b_stream.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]

@@ -76,12 +76,12 @@ bool make_tmap_bf16(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t col
 // W [K, N] bf16 row-major as a 3-D tensor {64 columns, K rows, N/64 column
 // blocks} with strides N*2 and 128 bytes; a box of `blocks` 64x64 blocks lands
 // as consecutive 8 KB, 128B-swizzled blocks (the MN-major B operand layout)
-bool make_tmap_w(CUtensorMap *m, const void *ptr, uint64_t K, uint64_t N, uint32_t blocks) {
+bool make_tmap_w(CUtensorMap *m, const void *ptr, uint64_t K, uint64_t N, uint32_t blocks, uint32_t rows = 64) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {64, K, N / 64};
     cuuint64_t strides[2] = {N * 2, 128};
-    cuuint32_t box[3] = {64, 64, blocks};
+    cuuint32_t box[3] = {64, rows, blocks};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -428,7 +428,8 @@ static cf_status plan_row_mapping(int64_t rows, int64_t cols, const cf_tuning &t
         p.per_thread = v;
         const int peer_max = t.peer_max == 0 ? 8 : t.peer_max;
         p.leader = (peer_max < 0 || C > peer_max) ? 1 : 0;
-        const int64_t clusters = std::min<int64_t>(rows, 8192);
+        int64_t clusters = std::min<int64_t>(rows, 8192);
+        if (t.max_clusters > 0) clusters = std::min<int64_t>(clusters, t.max_clusters);
         p.grid = int(clusters * C);
     } else {
         return CF_ERR_INVALID_ARG;
@@ -868,27 +869,57 @@ static int b2b_active_cached(int device, int op, int cluster, int n2, int smem) 
     return n;
 }
 
+// B2B kernel choice: the cluster kernel (C = N1/256 CTAs per row block, the
+// intermediate's columns partitioned over the cluster, partial outputs
+// reduce-scattered) or the stream kernel (one CTA per row block, N1 streamed
+// in 256-column chunks; softmax and GELU only).  tuning->n_slice selects:
+// 0 auto, 128 stream, 256 cluster (the plan reports the same values).
 static cf_status b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, int op, const cf_tuning *tuning,
                           const cf::DeviceInfo &dev, cf_plan *plan) {
     if (M < 0 || K <= 0 || N1 <= 0 || N2 <= 0) return CF_ERR_INVALID_ARG;
     if (op != CF_B2B_SOFTMAX && op != CF_B2B_GELU_TANH && op != CF_B2B_LAYERNORM) return CF_ERR_INVALID_ARG;
     if (K % 8 != 0 || N1 % 256 != 0 || (N2 != 64 && N2 != 128)) return CF_ERR_UNSUPPORTED;
+    if (M > (int64_t(1) << 31) - 128 || K > (int64_t(1) << 30) || N1 > (int64_t(1) << 30)) return CF_ERR_UNSUPPORTED;
     const int64_t C = N1 / 256;
-    if (C != 1 && C != 2 && C != 4 && C != 8) return CF_ERR_UNSUPPORTED;
-    if (M > (int64_t(1) << 31) - 128 || K > (int64_t(1) << 30)) return CF_ERR_UNSUPPORTED;
+    const bool cluster_ok = C == 1 || C == 2 || C == 4 || C == 8;
+    const bool stream_ok = op != CF_B2B_LAYERNORM;
+    const int reqn = tuning ? tuning->n_slice : 0;
+    bool stream;
+    if (reqn == 0) stream = stream_ok;  // one CTA per row block: no cluster exchange at all
+    else if (reqn == 128 && stream_ok) stream = true;
+    else if (reqn == 256) stream = false;
+    else return CF_ERR_UNSUPPORTED;
+    if (!stream && !cluster_ok) return CF_ERR_UNSUPPORTED;
     const int req = tuning ? tuning->stages : 0;
     if (req < 0 || req > 6) return CF_ERR_UNSUPPORTED;
+    std::memset(plan, 0, sizeof(*plan));
+    plan->groups = 1;
+    plan->cluster_m = 1;
+    plan->row_blocks = int32_t((M + 127) / 128);
+    if (stream) {
+        // the ring depth is fixed per mode (tuning->stages does not apply); at
+        // least half the SM's shared memory, so that one CTA (with all 512
+        // tensor-memory columns) runs per SM
+        const int stages = cf::b2b_stream_stages(op, int(K));
+        const int smem = std::max(cf::b2b_stream_smem_bytes(op, int(K)), kMaxSmem / 2 + 1024);
+        if (smem > kMaxSmem || smem > dev.max_smem_optin) return CF_ERR_UNSUPPORTED;
+        plan->n_slice = 128;  // the stream kernel's selector value (its chunks are 256 columns)
+        plan->ctas_per_row = 1;
+        plan->cluster_size = 1;
+        plan->stages = stages;
+        plan->smem_bytes = smem;
+        int ctas = int(std::min<int64_t>(plan->row_blocks, dev.sm_count));
+        if (tuning && tuning->max_clusters > 0) ctas = std::min(ctas, int(tuning->max_clusters));
+        plan->clusters = ctas;
+        return CF_OK;
+    }
     int stages = req > 0 ? req : 4;
     while (stages > 2 && cf::b2b_smem_bytes(stages, int(C), int(N2), op) > kMaxSmem) --stages;
     const int smem = cf::b2b_smem_bytes(stages, int(C), int(N2), op);
     if (smem > kMaxSmem || smem > dev.max_smem_optin) return CF_ERR_UNSUPPORTED;
-    std::memset(plan, 0, sizeof(*plan));
     plan->n_slice = 256;
     plan->ctas_per_row = int32_t(C);
     plan->cluster_size = int32_t(C);
-    plan->groups = 1;
-    plan->cluster_m = 1;
-    plan->row_blocks = int32_t((M + 127) / 128);
     plan->stages = stages;
     plan->smem_bytes = smem;
     const int active = b2b_active_cached(dev.device, op, int(C), int(N2), smem);
@@ -922,7 +953,7 @@ static cf_status b2b_common(const void *X, const void *W1, const float *b1, cons
     if (O == X || O == W1 || O == W2) return CF_ERR_INVALID_ARG;
     if (K % 8 != 0 || N1 % 256 != 0 || (N2 != 64 && N2 != 128)) return CF_ERR_UNSUPPORTED;
     if (ws_bytes < cf_b2b_workspace_size()) return CF_ERR_WORKSPACE_TOO_SMALL;
-    if (N1 / 256 > 8) return CF_ERR_UNSUPPORTED;
+    if (op == CF_B2B_LAYERNORM && N1 / 256 > 8) return CF_ERR_UNSUPPORTED;  // a cluster of at most 8
     if (M == 0) return CF_OK;
     cf::DeviceInfo dev;
     if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
@@ -933,9 +964,14 @@ static cf_status b2b_common(const void *X, const void *W1, const float *b1, cons
 
     cf::B2bArgs a;
     std::memset(&a, 0, sizeof(a));
+    const bool stream_kernel = plan.cluster_size == 1 && plan.n_slice == 128;
     if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, 128)) return CF_ERR_CUDA;
-    if (!make_tmap_w(&a.tmap_w1, W1, uint64_t(K), uint64_t(N1), 4)) return CF_ERR_CUDA;
-    if (!make_tmap_w(&a.tmap_w2, W2, uint64_t(N1), uint64_t(N2), uint32_t(N2 / 64))) return CF_ERR_CUDA;
+    if (!make_tmap_w(&a.tmap_w1, W1, uint64_t(K), uint64_t(N1), 4)) return CF_ERR_CUDA;  // 256 columns
+    if (!make_tmap_w(&a.tmap_w2, W2, uint64_t(N1), uint64_t(N2), uint32_t(N2 / 64), stream_kernel ? 128 : 64))
+        return CF_ERR_CUDA;
+    if (stream_kernel &&
+        !make_tmap_bf16(&a.tmap_o, O, uint64_t(M), uint64_t(N2), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return CF_ERR_CUDA;
     a.b1 = b1;
     a.gamma1 = gamma1;
     a.beta1 = beta1;
@@ -952,8 +988,10 @@ static cf_status b2b_common(const void *X, const void *W1, const float *b1, cons
     a.timeout_ns = 1000ull * tus;
     a.trace = tuning ? reinterpret_cast<unsigned long long *>(tuning->trace) : nullptr;
     const bool pdl = !(tuning && tuning->disable_pdl);
-    cudaError_t e = cf::launch_b2b(op, a, plan.clusters, plan.stages, plan.smem_bytes, pdl,
-                                   reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = stream_kernel ? cf::launch_b2b_stream(op, a, plan.clusters, plan.smem_bytes, pdl,
+                                                          reinterpret_cast<cudaStream_t>(stream))
+                                  : cf::launch_b2b(op, a, plan.clusters, plan.stages, plan.smem_bytes, pdl,
+                                                   reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return CF_OK;
 }

@@ -176,6 +176,7 @@ struct B2bArgs {
     CUtensorMap tmap_x;   // X [M,K] bf16, box 64(K) x 128(M), 128B swizzle
     CUtensorMap tmap_w1;  // W1 [K,N1] bf16 as {64, K, N1/64}, box {64, 64, 4}
     CUtensorMap tmap_w2;  // W2 [N1,N2] bf16 as {64, N1, N2/64}, box {64, 64, N2/64}
+    CUtensorMap tmap_o;   // stream kernel: O [M,N2] bf16, box 32 x 32, 64B swizzle (TMA stores)
     const float *b1;      // [N1] or null
     const float *gamma1;  // LayerNorm F: [N1]
     const float *beta1;   // LayerNorm F: [N1]
@@ -192,5 +193,10 @@ struct B2bArgs {
 int b2b_smem_bytes(int stages, int cluster, int n2, int op);
 int b2b_max_active_clusters(int op, int cluster, int n2, int smem);
 cudaError_t launch_b2b(int op, const B2bArgs &a, int clusters, int stages, int smem, bool pdl, cudaStream_t stream);
+// one CTA per 128-row block, N1 streamed in 256-column chunks (softmax, GELU);
+// tmap_w1 box {64, 64, 4}, tmap_w2 box {64, 128, N2/64}
+int b2b_stream_stages(int op, int K);  // ring depth, fixed per epilogue and mode (X resident or streamed)
+int b2b_stream_smem_bytes(int op, int K);
+cudaError_t launch_b2b_stream(int op, const B2bArgs &a, int ctas, int smem, bool pdl, cudaStream_t stream);
 
 }  // namespace cf

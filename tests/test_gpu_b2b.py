@@ -1,11 +1,14 @@
 """GPU parity of the back-to-back GEMM O = bf16(F(alpha X.W1 + b1)) . W2
-(through the C ABI) against the fp64 oracle: the softmax, GELU and
-LayerNorm epilogues, every cluster
-width N1/256 in {1, 2, 4, 8}, both output widths, ragged rows and a ragged
-last K block, several row blocks per cluster (the ring, tensor memory and the
-reduce-scatter buffer reused across tiles), ring depths, a selector W2 that
-reads S back column by column, unsupported shapes, and both page-sized
-workloads on sampled rows.
+(through the C ABI) against the fp64 oracle, on both kernels -- the cluster
+kernel (N1 partitioned over C = N1/256 CTAs, tuning n_slice = 256) and the
+stream kernel (one CTA per row block, N1 in 128-column chunks, n_slice = 128;
+softmax and GELU): the softmax, GELU and LayerNorm epilogues, every cluster
+width N1/256 in {1, 2, 4, 8} and wider N1 on the stream kernel, both output
+widths, ragged rows and a ragged last K block, X resident and streamed, the
+online softmax's rescaling, several row blocks per CTA or cluster (the ring,
+tensor memory and exchange buffers reused across tiles), ring depths, a
+selector W2 that reads S back column by column, unsupported shapes, and the
+page-sized workloads on sampled rows.
 
 Tolerance.  The kernel rounds its fp32 S to bf16 and the oracle rounds its
 fp64 S to bf16; the two roundings can land one bf16 ulp apart, and the
@@ -20,6 +23,14 @@ row statistics add up to 2^-14 (|s_j| + 1) (the normalised values are O(1)).  Th
 S element flips, so the mean error is checked as well: at most half a bf16
 ulp of the output on average plus 2^-12 of the flip term (a flip fraction
 far above what rounding noise produces fails it).
+
+The stream kernel's softmax rounds the unnormalised exponentials to bf16 and
+divides by the row sum on the fp32 output; the oracle rounds the normalised
+values.  Each is a bf16 rounding of S up to a positive per-row factor, so an
+element still differs by at most 2^-8 |s_j| (inside the flip term), but the
+two roundings are now independent: their difference adds noise of RMS at
+most 2^-9 sqrt(2/3) sqrt(sum_j s_j^2 W2_jk^2) to each output, which the mean
+check allows for on that kernel.
 """
 import numpy as np
 import pytest
@@ -31,6 +42,19 @@ from tests.gpu_util import bf16_half_ulp, dev_bf16, dev_f32, host, sample_rows, 
 pytestmark = pytest.mark.gpu
 
 OPS = {"softmax": cf.CF_B2B_SOFTMAX, "gelu_tanh": cf.CF_B2B_GELU_TANH, "layernorm": cf.CF_B2B_LAYERNORM}
+
+
+def _tuning(mode, N1, **kw):
+    """cf_tuning selecting the kernel: the cluster kernel (C = N1/256 CTAs of
+    256 columns) or the stream kernel (one CTA per row block, 128-column chunks)."""
+    return cf.tuning(n_slice=128 if mode == "stream" else 256, **kw)
+
+
+def _modes(op):
+    return ["cluster"] if op == "layernorm" else ["cluster", "stream"]
+
+
+CASES = [(op, mode) for op in OPS for mode in _modes(op)]
 
 
 def _run(d, op, alpha, tuning=None, expect=cf.CF_OK):
@@ -63,18 +87,19 @@ def _s(d, op, z):
 
 
 def _terms(d, op, alpha, rows=None):
-    """Per element of the output: sum_j |s_j||W2_jk| and sum_j |z_j||W2_jk|."""
+    """Per element of the output: sum_j |s_j||W2_jk|, sum_j |z_j||W2_jk| and
+    sqrt(sum_j s_j^2 W2_jk^2)."""
     X = d["X"] if rows is None else d["X"][rows]
     z = alpha * oracle.gemm(X, d["W1"]) + (0.0 if d.get("b1") is None else np.asarray(d["b1"], np.float64))
     s = _s(d, op, z)
     aw = np.abs(np.asarray(d["W2"], np.float64))
-    return np.abs(s) @ aw, np.abs(z) @ aw
+    return np.abs(s) @ aw, np.abs(z) @ aw, np.sqrt((s * s) @ (aw * aw))
 
 
-def check_b2b(o, ref, d, op, alpha, what, rows=None):
+def check_b2b(o, ref, d, op, alpha, what, rows=None, mode="cluster"):
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
     N1 = d["W1"].shape[1]
-    A, Z = _terms(d, op, alpha, rows)
+    A, Z, Q = _terms(d, op, alpha, rows)
     flip = (2.0 ** -7 + 2.0 ** -16 + N1 * 2.0 ** -24) * A
     if op == "gelu_tanh":
         flip = flip + 0.5 * 2.0 ** -10.98 * Z
@@ -86,6 +111,8 @@ def check_b2b(o, ref, d, op, alpha, what, rows=None):
     assert err.flat[worst] <= bound.flat[worst], (
         f"{what}: error {err.flat[worst]:.3e} > bound {bound.flat[worst]:.3e} at |ref|={abs(ref.flat[worst]):.3e}")
     mean_bound = bf16_half_ulp(np.abs(ref)).mean() + 2.0 ** -12 * flip.mean()
+    if mode == "stream" and op == "softmax":  # independent roundings of S (see the module docstring)
+        mean_bound += 2.0 ** -9 * np.sqrt(2.0 / 3.0) * Q.mean()
     assert err.mean() <= mean_bound, f"{what}: mean error {err.mean():.3e} > {mean_bound:.3e}"
 
 
@@ -100,33 +127,75 @@ def _ref(d, op, alpha, rows=None):
                            gamma1=d.get("gamma1"), beta1=d.get("beta1"), eps=1e-5)
 
 
-@pytest.mark.parametrize("op", ["softmax", "gelu_tanh", "layernorm"])
+@pytest.mark.parametrize("op,mode", CASES)
 @pytest.mark.parametrize("M,K,N1,N2", [(128, 64, 256, 64), (200, 128, 512, 128), (333, 128, 1024, 64),
-                                       (257, 192, 2048, 128), (130, 136, 1024, 128)])
-def test_b2b_shapes(op, M, K, N1, N2):
+                                       (257, 192, 2048, 128), (130, 136, 1024, 128), (150, 320, 512, 64)])
+def test_b2b_shapes(op, mode, M, K, N1, N2):
     d = _inputs(M, K, N1, N2, seed=M + K + N1 + N2, op=op)
     alpha = K ** -0.5 if op == "softmax" else 1.0
-    o = _run(d, op, alpha)
+    o = _run(d, op, alpha, tuning=_tuning(mode, N1))
     ref = _ref(d, op, alpha)
-    check_b2b(o, ref, d, op, alpha, f"b2b {op} {M}x{K}x{N1}x{N2}")
+    check_b2b(o, ref, d, op, alpha, f"b2b {op} {mode} {M}x{K}x{N1}x{N2}", mode=mode)
 
 
-@pytest.mark.parametrize("op", ["softmax", "gelu_tanh", "layernorm"])
+@pytest.mark.parametrize("op,mode", CASES)
 @pytest.mark.parametrize("kw", [dict(max_clusters=1), dict(max_clusters=3, stages=2), dict(stages=3),
                                 dict(max_clusters=2, disable_pdl=1)])
-def test_b2b_persistent_tiles(op, kw):
-    """Few clusters for many row blocks: each cluster walks several tiles."""
+def test_b2b_persistent_tiles(op, mode, kw):
+    """Few clusters (CTAs) for many row blocks: each walks several tiles."""
     M, K, N1, N2 = 1000, 256, 1024, 128
     d = _inputs(M, K, N1, N2, seed=17, op=op, b1=False)
     alpha = 0.25 if op == "softmax" else 1.0
-    o = _run(d, op, alpha, tuning=cf.tuning(**kw))
+    o = _run(d, op, alpha, tuning=_tuning(mode, N1, **kw))
     ref = _ref(d, op, alpha)
-    check_b2b(o, ref, d, op, alpha, f"b2b {op} {kw}")
+    check_b2b(o, ref, d, op, alpha, f"b2b {op} {mode} {kw}", mode=mode)
 
 
-@pytest.mark.parametrize("op", ["softmax", "gelu_tanh", "layernorm"])
+@pytest.mark.parametrize("op", ["softmax", "gelu_tanh"])
+@pytest.mark.parametrize("M,K,N1,N2,kw", [(300, 128, 4096, 128, {}), (129, 512, 768, 64, {}),
+                                          (640, 1024, 512, 128, dict(max_clusters=2)),
+                                          (256, 72, 256, 64, dict(stages=3))])
+def test_b2b_stream_only_shapes(op, M, K, N1, N2, kw):
+    """Stream kernel beyond the cluster kernel's reach (N1 > 8 * 256, N1 not
+    a power-of-two multiple of 256) and with X streamed next to W1 (K > 256)."""
+    d = _inputs(M, K, N1, N2, seed=M + 3 * K + N1, op=op)
+    alpha = K ** -0.5 if op == "softmax" else 1.0
+    o = _run(d, op, alpha, tuning=_tuning("stream", N1, **kw))
+    ref = _ref(d, op, alpha)
+    check_b2b(o, ref, d, op, alpha, f"b2b stream {op} {M}x{K}x{N1}x{N2} {kw}", mode="stream")
+
+
+@pytest.mark.parametrize("ramp", [0.0, 0.05, -0.05, 1.0])
+def test_b2b_stream_softmax_rescaling(ramp):
+    """Row maxima that rise (or fall) from chunk to chunk: b1 ramps with the
+    column, so later chunks pass the running reference by more than 2^8 and
+    the online softmax rescales O and the row sum (ramp 1.0: a rise of about
+    128 per chunk in log2 units, every chunk)."""
+    M, K, N1, N2 = 256, 128, 2048, 128
+    d = _inputs(M, K, N1, N2, seed=31, op="softmax")
+    d["b1"] = (d["b1"] + ramp * np.arange(N1)).astype(np.float32)
+    alpha = K ** -0.5
+    o = _run(d, "softmax", alpha, tuning=_tuning("stream", N1))
+    ref = _ref(d, "softmax", alpha)
+    check_b2b(o, ref, d, "softmax", alpha, f"b2b stream rescale {ramp}", mode="stream")
+
+
+def test_b2b_kernels_agree_on_gelu():
+    """GELU rounds the same value in both kernels: outputs within fp32
+    accumulation-order noise of each other (the sums over N1 run in a
+    different order)."""
+    M, K, N1, N2 = 384, 128, 1024, 128
+    d = _inputs(M, K, N1, N2, seed=37, op="gelu_tanh")
+    a = _run(d, "gelu_tanh", 1.0, tuning=_tuning("cluster", N1))
+    b = _run(d, "gelu_tanh", 1.0, tuning=_tuning("stream", N1))
+    A, _, _ = _terms(d, "gelu_tanh", 1.0)
+    bound = 2 * bf16_half_ulp(np.abs(a) + N1 * 2.0 ** -23 * A) + N1 * 2.0 ** -23 * A
+    assert np.all(np.abs(a - b) <= bound)
+
+
+@pytest.mark.parametrize("op,mode", CASES)
 @pytest.mark.parametrize("N1,N2", [(256, 64), (2048, 128)])
-def test_b2b_selector_reads_back_s(op, N1, N2):
+def test_b2b_selector_reads_back_s(op, mode, N1, N2):
     """W2 with a single 1 per column: O[:, k] = bf16(S[:, c_k]) exactly up to
     the one-ulp rounding difference of S, for columns c_k spread over every
     CTA of the cluster and every position of the packed bf16 pairs."""
@@ -137,7 +206,7 @@ def test_b2b_selector_reads_back_s(op, N1, N2):
     W2[cols, np.arange(N2)] = 1.0
     d["W2"] = W2
     alpha = K ** -0.5
-    o = _run(d, op, alpha)
+    o = _run(d, op, alpha, tuning=_tuning(mode, N1))
     z = alpha * oracle.gemm(d["X"], d["W1"]) + np.asarray(d["b1"], np.float64)
     s = _s(d, op, z)
     sel = s[:, cols]
@@ -145,6 +214,10 @@ def test_b2b_selector_reads_back_s(op, N1, N2):
     if op == "layernorm":
         e = e + 2.0 ** -14 * (np.abs(sel) + 1.0)
     bound = 2 * bf16_half_ulp(np.abs(sel) + e) + e
+    if mode == "stream" and op == "softmax":
+        # the unnormalised exponential is rounded (relative error <= 2^-8), then
+        # the output: one bf16 rounding more than the cluster kernel's
+        bound = bf16_half_ulp(np.abs(sel) + e) + 2.0 ** -8 * (np.abs(sel) + e) + e
     err = np.abs(o - sel)
     worst = np.argmax(err - bound)
     assert err.flat[worst] <= bound.flat[worst], (
@@ -163,11 +236,20 @@ def test_b2b_empty_and_unsupported():
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 384, 128, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 96, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 12, 512, 128, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
-    assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 4096, 128, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
+    # N1 = 4096: 16 CTAs per row block is beyond the cluster kernel (the stream
+    # kernel, which has no such limit, serves softmax and GELU only); a tile
+    # width other than 128 (stream) or 256 (cluster)
+    g = torch.ones(512, device="cuda")
+    assert cf.cf_b2b_gemm_layernorm(X, W1, None, g, g, W2, O, 128, 128, 4096, 128, 1.0, 1e-5, ws,
+                                    n) == cf.CF_ERR_UNSUPPORTED
+    for ns in (64, 192, 512):
+        assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 128, 1.0, 0, ws, n, None,
+                              cf.tuning(n_slice=ns)) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm_layernorm(X, W1, None, g, g, W2, O, 128, 128, 512, 128, 1.0, 1e-5, ws, n, None,
+                                    cf.tuning(n_slice=128)) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 128, 1.0, 3, ws, n) == cf.CF_ERR_INVALID_ARG
     # the LayerNorm epilogue needs gamma1 and beta1: only through its own entry point
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 128, 1.0, 2, ws, n) == cf.CF_ERR_INVALID_ARG
-    g = torch.ones(512, device="cuda")
     assert cf.cf_b2b_gemm_layernorm(X, W1, None, None, g, W2, O, 128, 128, 512, 128, 1.0, 1e-5, ws,
                                     n) == cf.CF_ERR_INVALID_ARG
     assert cf.cf_b2b_gemm(X, W1, None, W2, X, 128, 128, 512, 128, 1.0, 0, ws, n) == cf.CF_ERR_INVALID_ARG
@@ -177,22 +259,33 @@ def test_b2b_empty_and_unsupported():
 
 
 def test_b2b_plan():
-    torch_cuda()
+    torch = torch_cuda()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # softmax and GELU default to the stream kernel: one CTA per SM, 128-column chunks
     st, p = cf.cf_query_b2b_plan(32768, 128, 1024, 128, cf.CF_B2B_SOFTMAX)
     assert st == cf.CF_OK
-    assert p.cluster_size == 4 and p.row_blocks == 256 and 1 <= p.clusters <= 256 // 1
-    assert p.clusters * p.cluster_size <= 152 and p.smem_bytes <= 232448 and p.stages >= 2
+    assert p.cluster_size == 1 and p.n_slice == 128 and p.row_blocks == 256 and p.clusters == min(256, sms)
+    assert 232448 // 2 < p.smem_bytes <= 232448 and p.stages >= 3
+    st, p = cf.cf_query_b2b_plan(32768, 128, 1024, 128, cf.CF_B2B_SOFTMAX, cf.tuning(n_slice=256))
+    assert st == cf.CF_OK
+    assert p.cluster_size == 4 and p.n_slice == 256 and p.row_blocks == 256 and 1 <= p.clusters <= 256
+    assert p.clusters * p.cluster_size <= sms and p.smem_bytes <= 232448 and p.stages >= 2
     st, p = cf.cf_query_b2b_plan(100, 64, 2048, 64, cf.CF_B2B_GELU_TANH, cf.tuning(max_clusters=1))
-    assert st == cf.CF_OK and p.cluster_size == 8 and p.clusters == 1
+    assert st == cf.CF_OK and p.cluster_size == 1 and p.clusters == 1
+    st, p = cf.cf_query_b2b_plan(100, 64, 2048, 64, cf.CF_B2B_LAYERNORM)
+    assert st == cf.CF_OK and p.cluster_size == 8
 
 
-@pytest.mark.parametrize("name", ["b2b_attn_32768x128x1024x128", "b2b_gelu_16384x1024x2048x128",
-                                  "b2b_ln_16384x1024x2048x128"])
-def test_b2b_full_workload(name):
+@pytest.mark.parametrize("name,mode", [("b2b_attn_32768x128x1024x128", "stream"),
+                                       ("b2b_attn_32768x128x1024x128", "cluster"),
+                                       ("b2b_gelu_16384x1024x2048x128", "stream"),
+                                       ("b2b_gelu_16384x1024x2048x128", "cluster"),
+                                       ("b2b_ln_16384x1024x2048x128", "cluster")])
+def test_b2b_full_workload(name, mode):
     w = inputs.WORKLOADS[name]
     d = inputs.workload_inputs(name)
-    o = _run(d, w.op, w.alpha)
+    o = _run(d, w.op, w.alpha, tuning=_tuning(mode, w.N1))
     rows = sample_rows(w.M, 384, seed=11)
     ref = _ref(d, w.op, w.alpha, rows=rows)
     sub = dict(d, X=d["X"][rows])
-    check_b2b(o[rows], ref, sub, w.op, w.alpha, name)
+    check_b2b(o[rows], ref, sub, w.op, w.alpha, f"{name} {mode}", mode=mode)

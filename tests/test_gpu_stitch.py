@@ -44,6 +44,20 @@ def test_split_mapping(rows, cols, C, leader):
                   f"split {rows}x{cols} C={C} leader={leader}")
 
 
+@pytest.mark.parametrize("rows,cols,C,clusters,leader", [
+    (9, 30000, 8, 2, 0), (17, 4100, 4, 3, 1), (40, 1000, 2, 7, 0), (5, 30000, 16, 1, 0), (33, 130, 1, 4, 0),
+])
+def test_split_several_rows_per_cluster(rows, cols, C, clusters, leader):
+    # a cluster walks rows cid, cid + clusters, ... with the next row's loads in
+    # flight while the current one is reduced, exchanged and stored; ragged row
+    # counts leave some clusters one row short
+    d = inputs.stitch_inputs(rows, cols, 6)
+    t = cf.tuning(stitch_mapping=2, cluster_size=C, max_clusters=clusters, peer_max=-1 if leader else 16)
+    O = _run(dev_f32(d["A"]), dev_f32(d["row_bias"]), t)
+    check_softmax(host(O), oracle.stitch_rowreduce_broadcast(d["A"], d["row_bias"]),
+                  f"split {rows}x{cols} C={C} clusters={clusters}")
+
+
 def test_packed_and_split_agree():
     d = inputs.stitch_inputs(300, 128, 5)
     A, b = dev_f32(d["A"]), dev_f32(d["row_bias"])
