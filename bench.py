@@ -136,11 +136,13 @@ KERNEL_TU = {"gemm_fused_kernel": "gemm_fused.cu", "stitch_": "stitch.cu", "b2b_
 
 
 def kernel_source_hash(kernel):
-    """Hash of the translation unit that holds `kernel` and of every shared
-    header (a kernel's DRAM traffic can only change when one of them does)."""
+    """Hash of the device code behind `kernel`: the translation unit that holds
+    it and every shared device header (.cuh).  A kernel's DRAM traffic can only
+    change when one of them does (cf_internal.h, host-side declarations and the
+    launch-argument structs, is not part of it)."""
     csrc = os.path.join(ROOT, "memory_fusion_gb300", "csrc")
     tu = next((f for k, f in KERNEL_TU.items() if kernel.startswith(k)), None)
-    files = sorted(f for f in os.listdir(csrc) if f.endswith((".cuh", ".h")) or f == tu)
+    files = sorted(f for f in os.listdir(csrc) if f.endswith(".cuh") or f == tu)
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
