@@ -26,6 +26,7 @@ from __future__ import annotations
 import argparse
 import datetime
 import hashlib
+import re
 import json
 import math
 import os
@@ -135,18 +136,26 @@ KERNEL_TU = {"gemm_fused_kernel": "gemm_fused.cu", "stitch_": "stitch.cu", "b2b_
              "b2b_stream_kernel": "b2b_stream.cu", "addln_": "stitch_norm.cu", "bn_": "stitch_norm.cu"}
 
 
+def _code_only(text):
+    """Source text without comments and with whitespace runs collapsed (a
+    comment edit does not change the code)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel):
     """Hash of the device code behind `kernel`: the translation unit that holds
-    it and every shared device header (.cuh).  A kernel's DRAM traffic can only
-    change when one of them does (cf_internal.h, host-side declarations and the
-    launch-argument structs, is not part of it)."""
+    it and every shared device header (.cuh), comments and layout ignored.  A
+    kernel's DRAM traffic can only change when one of them does (cf_internal.h,
+    host-side declarations and the launch-argument structs, is not part of it)."""
     csrc = os.path.join(ROOT, "memory_fusion_gb300", "csrc")
     tu = next((f for k, f in KERNEL_TU.items() if kernel.startswith(k)), None)
     files = sorted(f for f in os.listdir(csrc) if f.endswith(".cuh") or f == tu)
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -14,22 +14,25 @@
 //    MMAs from shared-memory operands take about as long each).  X stays in
 //    shared memory for the row block when K <= 128 (double-buffered across row
 //    blocks); otherwise each k-block of X streams through the ring with W1's.
-//  * Epi_1(J): the two epilogue groups (4 warps each, one row per thread) take
-//    128 columns of the chunk each.  Once S is in registers it may be
-//    overwritten, so ML_1(J+1) starts while Epi_1(J) computes
+//  * Epi_1(J): four epilogue groups (4 warps each, one per TMEM lane quadrant;
+//    thread = row) take 64 columns of the chunk each, so a thread holds 64
+//    values (576 threads: 96 registers each).  Once S is in registers it may
+//    be overwritten, so ML_1(J+1) starts while Epi_1(J) computes
 //    z = alpha * S + b1 and F, and writes the bf16 values to P as soon as
 //    ML_2(J-1) has read the previous ones.
 //    Softmax is evaluated online (running max m and sum l per row, base-2
-//    exponentials): the groups exchange their halves' maxima through shared
-//    memory; m is raised -- and O and l rescaled -- only when the chunk's max
-//    exceeds it by more than 8 (a factor 256), so most chunks leave O alone.
+//    exponentials): the groups exchange their parts' row maxima through
+//    shared memory; m is raised -- and O and l rescaled -- only when the
+//    chunk's max exceeds it by more than 8 (a factor 256), so most chunks
+//    leave O alone.
 //    The values rounded to bf16 are these unnormalised exponentials (at most
 //    256); the division by the row sum happens once, on the fp32 output.
 //  * ML_2(J): O += P . W2[chunk J, :] (K = 256), A read from tensor memory.
 //  * Issue order: ML_1(0), then ML_1(J+1), ML_2(J) for each J: the tensor
 //    core runs ML_1(J+1) and ML_2(J-1) under Epi_1(J).
 //  * End of a row block: O / l (GELU: O), group g writing output columns
-//    [g N2/2, (g+1) N2/2).  No cluster, no exchange with other CTAs.
+//    [32 g, 32 g + 32) through a 2 KB staging buffer per warp and 32 x 32 TMA
+//    stores.  No cluster, no exchange with other CTAs.
 //  * Every wait is bounded by %globaltimer; a timeout records
 //    CF_ERR_DEVICE_TIMEOUT in the workspace error word and the roles drain.
 #include <cuda.h>
@@ -63,9 +66,10 @@ constexpr uint32_t kInfoProducer = 0x91000000u;
 constexpr uint32_t kInfoMma = 0x92000000u;
 constexpr uint32_t kInfoEpi = 0x93000000u;
 
-// Shared-memory layout, fixed per mode (compile-time offsets keep the
-// epilogue's registers for its data): resident X (K <= 128) with a 3-stage
-// ring of 32 KB, or X streamed with W1 through a 4-stage ring of 48 KB.
+// Shared-memory layout, fixed per epilogue and mode (compile-time offsets keep
+// the epilogue's registers for its data): resident X (K <= 128) with a
+// 3-stage ring of 32 KB, or X streamed with W1 through a ring of 48 KB stages
+// (4 for GELU, 3 for softmax, whose row statistics take the room of one).
 struct Layout {
     uint32_t xres, xbytes, ring, stage, stages, stg, bias, xm, stat, bars, total;
 };
