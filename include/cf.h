@@ -145,8 +145,13 @@ typedef enum {
     CF_TR_EPI_STORED = 11    /* epilogue: output stores issued                 */
 } cf_trace_event;
 
-/* Per-tile trace events of the back-to-back GEMM kernel (same slot layout;
- * the epilogue's events are stamped by its first thread). */
+/* Per-tile trace events of the back-to-back GEMM kernels (same slot layout;
+ * the epilogue's events are stamped by its first thread).  In the stream
+ * kernel a "tile" is a 256-column chunk (index = the CTA's chunk count);
+ * EPI1_START / EPI2_START mark the chunk's start in the first / second
+ * epilogue group, EPI1_LOCAL the softmax exponentials done, EPI1_DONE the
+ * chunk's bf16 values written, EPI2_STORED (on a row block's last chunk) the
+ * row block's output stored; SENT / RECV are not used. */
 typedef enum {
     CF_TRB_TMA_FIRST = 0,    /* producer issued the tile's first load          */
     CF_TRB_ML1_FIRST = 1,    /* MMA warp: first MatMul_1 operand stage ready   */

@@ -51,6 +51,12 @@ CF_TRACE_EVENTS = 12
 CF_TRACE_SLOTS = 4 + CF_TRACE_TILES * CF_TRACE_EVENTS
 TRACE_EVENT_NAMES = ["tma_first", "tma_last", "mma_acc_free", "mma_first", "mma_done", "mma_wait_ns",
                      "epi_start", "epi_stats", "epi_cta", "epi_cluster", "epi_global", "epi_stored"]
+# cf_trace_event (fused GEMM) and cf_trb_event (back-to-back GEMM) slots
+(CF_TR_TMA_FIRST, CF_TR_TMA_LAST, CF_TR_MMA_ACC_FREE, CF_TR_MMA_FIRST, CF_TR_MMA_DONE, CF_TR_MMA_WAIT_NS,
+ CF_TR_EPI_START, CF_TR_EPI_STATS, CF_TR_EPI_CTA, CF_TR_EPI_CLUSTER, CF_TR_EPI_GLOBAL, CF_TR_EPI_STORED) = range(12)
+(CF_TRB_TMA_FIRST, CF_TRB_ML1_FIRST, CF_TRB_ML1_DONE, CF_TRB_EPI1_START, CF_TRB_EPI1_LOCAL, CF_TRB_EPI1_DONE,
+ CF_TRB_ML2_START, CF_TRB_ML2_DONE, CF_TRB_EPI2_START, CF_TRB_EPI2_SENT, CF_TRB_EPI2_RECV,
+ CF_TRB_EPI2_STORED) = range(12)
 
 
 class cf_plan(ctypes.Structure):
