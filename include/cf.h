@@ -103,9 +103,10 @@ typedef struct cf_tuning {
     int32_t stitch_mapping; /* 0 auto, 1 packed rows, 2 split rows over a cluster  */
     uint32_t timeout_us;    /* bound of every device spin (0 = 200000 us)          */
     int32_t extra_arrivals; /* TEST HOOK: added to the arrival count the global
-                               barrier waits for; > 0 makes that wait run out
-                               (CF_ERR_DEVICE_TIMEOUT) without faulting.  0 in
-                               normal use.                                        */
+                               barrier waits for (B2B stream kernel: the
+                               per-chunk P-ready barrier); > 0 makes that wait
+                               run out (CF_ERR_DEVICE_TIMEOUT) without
+                               faulting.  0 in normal use.                        */
     int32_t cluster_m;      /* GEMM: row blocks per cluster (1 or 2); 2 pairs the
                                two row blocks' CTAs into one tcgen05 MMA stream
                                (cta_group::2, M = 256; each CTA stages half of

@@ -208,7 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
         }
         ptx::mbar_init(B.s_full, 1);
         ptx::mbar_init(B.s_free, 4 * kGroups);
-        ptx::mbar_init(B.p_full, 4 * kGroups);
+        // (test hook: extra arrivals that never come make the MMA warp's wait
+        // for P run out -- CF_ERR_DEVICE_TIMEOUT, every role drains)
+        ptx::mbar_init(B.p_full, 4 * kGroups + uint32_t(a.extra_arrivals));
         ptx::mbar_init(B.o_full, 1);
         ptx::mbar_init(B.mfree, 4 * kGroups);
         ptx::mbar_init(B.mma_done, 1);

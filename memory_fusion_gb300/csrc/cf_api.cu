@@ -987,6 +987,7 @@ static cf_status b2b_common(const void *X, const void *W1, const float *b1, cons
     const uint32_t tus = tuning && tuning->timeout_us ? tuning->timeout_us : kDefaultTimeoutUs;
     a.timeout_ns = 1000ull * tus;
     a.trace = tuning ? reinterpret_cast<unsigned long long *>(tuning->trace) : nullptr;
+    a.extra_arrivals = tuning && tuning->extra_arrivals > 0 ? tuning->extra_arrivals : 0;
     const bool pdl = !(tuning && tuning->disable_pdl);
     cudaError_t e = stream_kernel ? cf::launch_b2b_stream(op, a, plan.clusters, plan.smem_bytes, pdl,
                                                           reinterpret_cast<cudaStream_t>(stream))

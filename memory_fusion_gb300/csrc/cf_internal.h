@@ -188,6 +188,7 @@ struct B2bArgs {
     float alpha;
     unsigned long long timeout_ns;
     unsigned long long *trace;  // optional %globaltimer stamps, CF_TRACE_SLOTS per CTA
+    int extra_arrivals;   // test hook (stream kernel): added to the per-chunk P-ready count
 };
 
 int b2b_smem_bytes(int stages, int cluster, int n2, int op);
