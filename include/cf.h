@@ -406,7 +406,7 @@ CF_API cf_status cf_gemm_fused_rowsoftmax_causal_ex(const void *X, const void *W
  *
  * [ComFuse] B2BGEMM, Eqs. 3-7 and Fig. 5, in two kernels; S never reaches
  * global memory in either.
- *  - Cluster kernel (tuning n_slice = 256; the only one for LayerNorm):
+ *  - Cluster kernel (tuning n_slice = 256):
  *    MatMul_1 is partitioned along the intermediate dimension N1 over the
  *    C = N1/256 CTAs of a thread-block cluster (256 columns each); the
  *    epilogue F turns each CTA's P tile into its S tile in tensor memory;
@@ -414,14 +414,16 @@ CF_API cf_status cf_gemm_fused_rowsoftmax_causal_ex(const void *X, const void *W
  *    through the same operand ring as X and W1; the C partial output tiles
  *    are summed across the cluster (in rank order, deterministic) and
  *    written once.  N1 in {256, 512, 1024, 2048}.
- *  - Stream kernel (n_slice = 128; the default for softmax and GELU): one
+ *  - Stream kernel (n_slice = 128; the default): one
  *    CTA per 128-row block; N1 in 256-column chunks through tensor memory,
  *    MatMul_1 of the next chunk running while the epilogue works on the
  *    current one; one O accumulator per row block.  Softmax is evaluated
  *    online (running row max, raised with O rescaled only when a chunk passes
  *    it by 2^8): the bf16 values fed to MatMul_2 are the exponentials against
  *    that running max, and the division by the row sum is applied to the
- *    fp32 O.  Any N1 that is a multiple of 256.
+ *    fp32 O.  LayerNorm takes two passes over the chunks (MatMul_1 runs
+ *    twice): the row (mean, M2) first, then the normalised values for
+ *    MatMul_2.  Any N1 that is a multiple of 256.
  *   op   CF_B2B_SOFTMAX: F = row softmax over all N1 columns;
  *        CF_B2B_GELU_TANH: F = GELU(tanh)
  *   X  (device) bf16 [M, K] row-major      W1 (device) bf16 [K, N1] row-major
@@ -469,7 +471,8 @@ CF_API cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, 
 /* O = bf16( bf16(LayerNorm(alpha * X.W1 + b1) * gamma1 + beta1) . W2 ): the
  * back-to-back GEMM with F = LayerNorm over each row's N1 intermediate
  * values (biased variance, eps inside the square root); the row (mean, M2)
- * is reduced across the cluster like the softmax statistics.  gamma1, beta1
+ * is reduced across the cluster like the softmax statistics (stream kernel:
+ * over the chunks of a first pass).  gamma1, beta1
  * (device) fp32 [N1], required; everything else as for cf_b2b_gemm. */
 CF_API cf_status cf_b2b_gemm_layernorm(const void *X, const void *W1, const float *b1,
                                        const float *gamma1, const float *beta1, const void *W2,

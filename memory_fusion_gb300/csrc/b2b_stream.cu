@@ -86,10 +86,15 @@ __host__ __device__ constexpr Layout layout() {
     // (GELU has no row statistics: a fourth stage fits when X streams)
     L.stages = (!kRes && OP == 1) ? 4u : 3u;
     L.stg = L.ring + L.stages * L.stage;  // bf16 output staging: 2 KB (32 x 32, 64B swizzle) per epilogue warp
-    L.bias = L.stg + 4u * kGroups * 2048u;  // float [groups][2 chunk parities][kCols]: b1 of the group's columns
-    L.xm = L.bias + kGroups * 2u * kCols * 4u;  // softmax: float [2 chunk parities][groups][128] row maxima
-    L.stat = L.xm + (OP == 0 ? 2u * kGroups * 128u * 4u : 0u);  // softmax: float [2 rb parities][groups][128] sums
-    L.bars = L.stat + (OP == 0 ? 2u * kGroups * 128u * 4u : 0u);
+    // float [groups][2 chunk parities][kCols]: b1 of the group's columns (LayerNorm:
+    // [groups][2][3][kCols], b1, gamma1, beta1)
+    L.bias = L.stg + 4u * kGroups * 2048u;
+    L.xm = L.bias + kGroups * 2u * kCols * 4u * (OP == 2 ? 3u : 1u);
+    // softmax: float [2 chunk parities][groups][128] row maxima
+    L.stat = L.xm + (OP == 0 ? 2u * kGroups * 128u * 4u : 0u);
+    // softmax: float [2 rb parities][groups][128] row sums; LayerNorm: float2
+    // [2 rb parities][groups][128] (mean, M2) of each group's columns
+    L.bars = L.stat + (OP == 0 ? 2u * kGroups * 128u * 4u : OP == 2 ? 2u * kGroups * 128u * 8u : 0u);
     L.total = L.bars + 256u;
     return L;
 }
@@ -185,6 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
     constexpr Layout L = layout<OP, kRes>();
     constexpr int stages = int(L.stages);
     const int nc = a.N1 / kChunk;           // chunks per row block
+    // LayerNorm takes two passes over a row block's chunks: the statistics,
+    // then the normalised values for ML_2 (ML_1 runs twice); "virtual chunks"
+    // count both, output chunks the second
+    constexpr int kPasses = OP == 2 ? 2 : 1;
+    const int nv = kPasses * nc;
     const Bars B = bars_at(base + L.bars, stages);
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem_raw + (B.misc - base));
     volatile uint32_t *abort = misc + 1;
@@ -193,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
     const int RB = (a.M + 127) / 128;
     // row blocks of this CTA: blockIdx.x, + gridDim.x, ...; chunks J = i * nc + j
     const int nrb = int(blockIdx.x) < RB ? (RB - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x) : 0;
-    const int NJ = nrb * nc;
+    const int NJ = nrb * nv;  // virtual chunks of this CTA
     unsigned long long *const tr = a.trace;
     const unsigned long long t_start = ptx::globaltimer();
 
@@ -256,16 +266,16 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                     ph ^= 1u;
                 }
             };
-            int i1 = 0, j1 = 0;  // (row block, chunk) of the next ML_1
+            int i1 = 0, v1 = 0;  // (row block, virtual chunk) of the next ML_1
             auto load_ml1 = [&](int J) {
-                const int i = i1, j = j1;
-                if (++j1 == nc) {
-                    j1 = 0;
+                const int i = i1, v = v1, j = v1 < nc ? v1 : v1 - nc;
+                if (++v1 == nv) {
+                    v1 = 0;
                     ++i1;
                 }
                 const int m0 = (int(blockIdx.x) + i * int(gridDim.x)) * 128;
                 trace_tile(tr, J, CF_TRB_TMA_FIRST);
-                if (resident && j == 0) {
+                if (resident && v == 0) {
                     // X of row block i into buffer i & 1, once row block i - 2 is done with it
                     const int b = i & 1;
                     if (i >= 2) {
@@ -307,9 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                 }
             };
             if (NJ > 0) load_ml1(0);
+            int vo = 0;  // virtual chunk J within its row block
             for (int J = 0; J < NJ && ok; ++J) {
                 if (J + 1 < NJ) load_ml1(J + 1);
-                load_ml2(J);
+                if (vo >= nv - nc) load_ml2(J);  // an output chunk
+                if (++vo == nv) vo = 0;
             }
             // every stage filled has been released before the CTA may exit
             const uint32_t first = it > uint32_t(stages) ? it - uint32_t(stages) : 0u;
@@ -354,11 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
             // (row block, chunk) of the next ML_1 and the next ML_2, advanced in
             // place: this thread's instructions between MMA groups are few (it
             // shares its SMSP's issue slots with four epilogue warps)
-            int i1 = 0, j1 = 0, i2 = 0, j2 = 0;
+            int i1 = 0, v1 = 0, i2 = 0, j2 = 0, o2 = 0;  // o2: output chunks issued
             auto ml1 = [&](int J) {
-                const int i = i1, j = j1;
-                if (++j1 == nc) {
-                    j1 = 0;
+                const int i = i1, v = v1;
+                if (++v1 == nv) {
+                    v1 = 0;
                     ++i1;
                 }
                 // S is free once both groups read the previous chunk
@@ -366,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                     ok = ptx::mbar_wait_bounded(B.s_free, uint32_t(J - 1) & 1u, tmo, abort, a.err, kInfoMma | 0x100u);
                     if (!ok) return;
                 }
-                if (resident && j == 0) {
+                if (resident && v == 0) {
                     ok = ptx::mbar_wait_bounded(B.xfull0 + 8 * (i & 1), uint32_t(i >> 1) & 1u, tmo, abort, a.err,
                                                 kInfoMma | 0x500u);
                     if (!ok) return;
@@ -386,17 +398,17 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                         ptx::mma_bf16(tmem, ad + uint64_t(2 * k), bd + uint64_t(128 * k), id1, (kb | k) != 0 ? 1u : 0u);
                     release();
                 }
-                if (resident && j == nc - 1) ptx::mma_commit(B.xfree0 + 8 * (i & 1));  // X buffer reusable
+                if (resident && v == nv - 1) ptx::mma_commit(B.xfree0 + 8 * (i & 1));  // X buffer reusable
                 ptx::mma_commit(B.s_full);
                 trace_tile(tr, J, CF_TRB_ML1_DONE);
             };
             auto ml2 = [&](int J) {
-                const int i = i2, j = j2;
+                const int i = i2, j = j2, O = o2++;  // (row block, output chunk), output chunks before
                 if (++j2 == nc) {
                     j2 = 0;
                     ++i2;
                 }
-                ok = ptx::mbar_wait_bounded(B.p_full, uint32_t(J) & 1u, tmo, abort, a.err, kInfoMma | 0x200u);
+                ok = ptx::mbar_wait_bounded(B.p_full, uint32_t(O) & 1u, tmo, abort, a.err, kInfoMma | 0x200u);
                 if (!ok) return;
                 // the row block's first ML_2 overwrites O: the previous row block's
                 // output has read it
@@ -423,9 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                 trace_tile(tr, J, CF_TRB_ML2_DONE);
             };
             if (NJ > 0) ml1(0);
+            int vo = 0;  // virtual chunk J within its row block
             for (int J = 0; J < NJ && ok; ++J) {
                 if (J + 1 < NJ) ml1(J + 1);
-                if (ok) ml2(J);
+                if (ok && vo >= nv - nc) ml2(J);  // an output chunk
+                if (++vo == nv) vo = 0;
             }
             ptx::mma_commit(B.mma_done);
             volatile uint32_t local_abort = 0;
@@ -448,30 +462,53 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
         const uint32_t tP = tmem + lane_off + kColP + uint32_t(kCols / 2 * g); // and its packed P columns
         const uint32_t tO = tmem + lane_off + kColO + uint32_t(32 * g);       // its O columns (rescale)
         const bool owns_o = 32 * g < kN2;                                     // (N2 = 64: groups 0, 1)
-        float *const bias = reinterpret_cast<float *>(smem_raw + L.bias) + g * 2 * kCols;
+        constexpr int kPrm = OP == 2 ? 3 : 1;  // staged column parameters: b1 (LayerNorm: and gamma1, beta1)
+        float *const prm = reinterpret_cast<float *>(smem_raw + L.bias) + g * 2 * kPrm * kCols;
         float *const xm = reinterpret_cast<float *>(smem_raw + L.xm);
         float *const stat = reinterpret_cast<float *>(smem_raw + L.stat);
         const float bscale = OP == 0 ? kLog2e : 1.f;
         const float ascale = a.alpha * bscale;  // softmax works in base 2: t = z log2 e
-        // b1 of the group's next chunk, loaded one chunk ahead (threads gt < 64)
-        float nb = (a.b1 && gt < kCols) ? __ldg(a.b1 + kCols * g + gt) : 0.f;
-        int J = 0;
+        // the parameters of the group's next chunk, loaded one chunk ahead (threads gt < 64)
+        const bool pl = gt < kCols;
+        auto ldp = [&](const float *v, int jc) -> float { return (v && pl) ? __ldg(v + jc * kChunk + kCols * g + gt) : 0.f; };
+        float nb = ldp(a.b1, 0), ng = 0.f, ne = 0.f;
+        if constexpr (OP == 2) {
+            ng = ldp(a.gamma1, 0);
+            ne = ldp(a.beta1, 0);
+        }
+        int J = 0;  // virtual chunks processed
+        int O = 0;  // output chunks processed
         for (int i = 0; i < nrb; ++i) {
-            float m = neg_inf(), l = 0.f;
-            for (int j = 0; j < nc; ++j, ++J) {
-                // the chunk's b1, double-buffered by chunk parity (the previous
+            float m = neg_inf(), l = 0.f;     // softmax: running max and sum of this group's columns
+            MeanM2 ls{0.f, 0.f};               // LayerNorm: (mean, M2) of this group's columns so far
+            float mu = 0.f, rstd = 0.f;        // LayerNorm: the row's statistics, after the first pass
+            for (int v = 0; v < nv; ++v, ++J) {
+                const int j = v < nc ? v : v - nc;     // W1 chunk
+                const bool out = v >= nv - nc;         // this chunk feeds ML_2
+                // the chunk's parameters, double-buffered by chunk parity (the previous
                 // chunk's barrier ordered every read of this buffer before this write)
-                float *const bb = bias + (J & 1) * kCols;
-                if (gt < kCols) bb[gt] = nb * bscale;
-                const int jn = j + 1 < nc ? j + 1 : 0;
-                nb = (a.b1 && gt < kCols) ? __ldg(a.b1 + jn * kChunk + kCols * g + gt) : 0.f;
+                float *const bb = prm + (J & 1) * kPrm * kCols;
+                if (pl) {
+                    bb[gt] = nb * bscale;
+                    if constexpr (OP == 2) {
+                        bb[kCols + gt] = ng;
+                        bb[2 * kCols + gt] = ne;
+                    }
+                }
+                const int vn = v + 1 < nv ? v + 1 : 0;
+                const int jn = vn < nc ? vn : vn - nc;
+                nb = ldp(a.b1, jn);
+                if constexpr (OP == 2) {
+                    ng = ldp(a.gamma1, jn);
+                    ne = ldp(a.beta1, jn);
+                }
                 ptx::named_bar_sync(1u + uint32_t(g), 128);
                 ptx::mbar_wait_bounded(B.s_full, uint32_t(J) & 1u, tmo, abort, a.err, kInfoEpi | uint32_t(g));
                 ptx::tc_fence_after();
                 if (lead && g < 2) trace_tile(tr, J, g == 0 ? CF_TRB_EPI1_START : CF_TRB_EPI2_START);
-                uint32_t v[kFrag][32];  // the chunk's z; then (first halves) its packed bf16 pairs
+                uint32_t x[kFrag][32];  // the chunk's z; then (first halves) its packed bf16 pairs
 #pragma unroll
-                for (int c = 0; c < kFrag; ++c) ptx::tmem_ld32(tS + c * 32, v[c]);
+                for (int c = 0; c < kFrag; ++c) ptx::tmem_ld32(tS + c * 32, x[c]);
                 ptx::tmem_ld_wait();
                 // S is in registers: ML_1 of the next chunk may overwrite it
                 ptx::tc_fence_before();
@@ -489,8 +526,8 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                     for (int c = 0; c < kFrag; ++c)
 #pragma unroll
                         for (int k = 0; k < 32; ++k) {
-                            const float t = fmaf(ascale, __uint_as_float(v[c][k]), bb[c * 32 + k]);
-                            v[c][k] = __float_as_uint(t);
+                            const float t = fmaf(ascale, __uint_as_float(x[c][k]), bb[c * 32 + k]);
+                            x[c][k] = __float_as_uint(t);
                             cmv[k & 3] = fmaxf(cmv[k & 3], t);
                         }
                     // the row's max over the whole chunk: every group's part, through
@@ -512,34 +549,89 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
 #pragma unroll
                     for (int r = 0; r < 4; ++r) sv[r] = 0.f;
                     // the chunk's bf16 pairs are packed in place: pair k of fragment c
-                    // goes to v[c][k] once v[c][2k] and v[c][2k+1] were read
+                    // goes to x[c][k] once x[c][2k] and x[c][2k+1] were read
 #pragma unroll
                     for (int c = 0; c < kFrag; ++c)
 #pragma unroll
                         for (int k = 0; k < 16; ++k) {
-                            const float e0 = ptx::ex2_approx(__uint_as_float(v[c][2 * k]) - mn);
-                            const float e1 = ptx::ex2_approx(__uint_as_float(v[c][2 * k + 1]) - mn);
+                            const float e0 = ptx::ex2_approx(__uint_as_float(x[c][2 * k]) - mn);
+                            const float e1 = ptx::ex2_approx(__uint_as_float(x[c][2 * k + 1]) - mn);
                             sv[k & 3] += e0 + e1;
-                            v[c][k] = ptx::pack_bf16x2(e0, e1);
+                            x[c][k] = ptx::pack_bf16x2(e0, e1);
                         }
                     l = fmaf(l, f, (sv[0] + sv[1]) + (sv[2] + sv[3]));
                     m = mn;
                     if (lead && g == 0) trace_tile(tr, J, CF_TRB_EPI1_LOCAL);
+                } else if constexpr (OP == 2) {
+#pragma unroll
+                    for (int c = 0; c < kFrag; ++c)
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            x[c][k] = __float_as_uint(fmaf(ascale, __uint_as_float(x[c][k]), bb[c * 32 + k]));
+                    if (!out) {
+                        // first pass: (mean, M2) of the chunk's 64 values (two passes over the
+                        // registers), folded into the group's running pair by counts
+                        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int c = 0; c < kFrag; ++c)
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) s4[k & 3] += __uint_as_float(x[c][k]);
+                        const float cmean = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * (1.f / float(kCols));
+                        float q4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int c = 0; c < kFrag; ++c)
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                const float d = __uint_as_float(x[c][k]) - cmean;
+                                q4[k & 3] = fmaf(d, d, q4[k & 3]);
+                            }
+                        const MeanM2 cs{cmean, (q4[0] + q4[1]) + (q4[2] + q4[3])};
+                        ls = j == 0 ? cs : combine_counts(ls, float(kCols * j), cs, float(kCols));
+                        if (v == nc - 1) {
+                            // the row's statistics over all N1 columns: every group's part
+                            // (equal counts), through shared memory
+                            float2 *const st2 = reinterpret_cast<float2 *>(stat) + (i & 1) * (128 * kGroups);
+                            st2[g * 128 + row] = make_float2(ls.mean, ls.m2);
+                            ptx::named_bar_sync(kGroups + 1, 128 * kGroups);
+                            const float ng_cols = float(kCols * nc);
+                            MeanM2 rs{st2[row].x, st2[row].y};
+#pragma unroll
+                            for (int h = 1; h < kGroups; ++h)
+                                rs = combine_counts(rs, ng_cols * float(h), MeanM2{st2[h * 128 + row].x, st2[h * 128 + row].y},
+                                                    ng_cols);
+                            mu = rs.mean;
+                            rstd = rsqrtf(rs.m2 / float(a.N1) + a.eps);
+                        }
+                    } else {
+                        // second pass: (z - mean) * rstd * gamma1 + beta1, packed in place
+#pragma unroll
+                        for (int c = 0; c < kFrag; ++c)
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                const int n0 = c * 32 + 2 * k;
+                                const float y0 =
+                                    fmaf((__uint_as_float(x[c][2 * k]) - mu) * rstd, bb[kCols + n0], bb[2 * kCols + n0]);
+                                const float y1 = fmaf((__uint_as_float(x[c][2 * k + 1]) - mu) * rstd,
+                                                      bb[kCols + n0 + 1], bb[2 * kCols + n0 + 1]);
+                                x[c][k] = ptx::pack_bf16x2(y0, y1);
+                            }
+                    }
                 } else {
 #pragma unroll
                     for (int c = 0; c < kFrag; ++c)
 #pragma unroll
                         for (int k = 0; k < 16; ++k) {
-                            const float x0 = gelu_tanh_dev(fmaf(ascale, __uint_as_float(v[c][2 * k]), bb[c * 32 + 2 * k]));
+                            const float x0 = gelu_tanh_dev(fmaf(ascale, __uint_as_float(x[c][2 * k]), bb[c * 32 + 2 * k]));
                             const float x1 =
-                                gelu_tanh_dev(fmaf(ascale, __uint_as_float(v[c][2 * k + 1]), bb[c * 32 + 2 * k + 1]));
-                            v[c][k] = ptx::pack_bf16x2(x0, x1);
+                                gelu_tanh_dev(fmaf(ascale, __uint_as_float(x[c][2 * k + 1]), bb[c * 32 + 2 * k + 1]));
+                            x[c][k] = ptx::pack_bf16x2(x0, x1);
                         }
                 }
-                // P and O: ML_2 of the previous chunk is complete (it read P; O holds
-                // every earlier chunk)
-                if (J > 0)
-                    ptx::mbar_wait_bounded(B.o_full, uint32_t(J - 1) & 1u, tmo, abort, a.err, kInfoEpi | 0x10u);
+                if (!out) continue;  // (LayerNorm's first pass feeds no ML_2)
+                // P and O: ML_2 of the previous output chunk is complete (it read P; O
+                // holds every earlier chunk)
+                if (O > 0)
+                    ptx::mbar_wait_bounded(B.o_full, uint32_t(O - 1) & 1u, tmo, abort, a.err, kInfoEpi | 0x10u);
                 ptx::tc_fence_after();
                 if constexpr (OP == 0) {
                     // O carries the previous chunks against the old reference: rescale
@@ -559,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                 for (int c = 0; c < kFrag; ++c) {
                     uint32_t pk[16];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) pk[k] = v[c][k];
+                    for (int k = 0; k < 16; ++k) pk[k] = x[c][k];
                     ptx::tmem_st16(tP + c * 16, pk);
                 }
                 ptx::tmem_st_wait();
@@ -567,10 +659,11 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(B.p_full);
                 if (lead && g == 0) trace_tile(tr, J, CF_TRB_EPI1_DONE);
+                ++O;
             }
             // ---------------- the row block's output, once its last ML_2 completed;
             // ML_1 of the next row block's first chunk runs meanwhile
-            ptx::mbar_wait_bounded(B.o_full, uint32_t(J - 1) & 1u, tmo, abort, a.err, kInfoEpi | 0x20u);
+            ptx::mbar_wait_bounded(B.o_full, uint32_t(O - 1) & 1u, tmo, abort, a.err, kInfoEpi | 0x20u);
             ptx::tc_fence_after();
             stream_output<OP, kN2>(&a.tmap_o, a.out == nullptr, a.M, (int(blockIdx.x) + i * int(gridDim.x)) * 128,
                                    tmem + lane_off + kColO, base + L.stg + uint32_t(warp - 2) * 2048u,
@@ -602,6 +695,7 @@ void *stream_fn_n2(int n2) {
 }
 void *stream_fn(int op, int n2, bool res) {
     if (op == 0) return res ? stream_fn_n2<0, true>(n2) : stream_fn_n2<0, false>(n2);
+    if (op == 2) return res ? stream_fn_n2<2, true>(n2) : stream_fn_n2<2, false>(n2);
     return res ? stream_fn_n2<1, true>(n2) : stream_fn_n2<1, false>(n2);
 }
 
@@ -612,12 +706,16 @@ Layout layout_for(int K) {
     return K <= kMaxResidentK ? layout<OP, true>() : layout<OP, false>();
 }
 
-int b2b_stream_stages(int op, int K) { return int((op == 0 ? layout_for<0>(K) : layout_for<1>(K)).stages); }
+static Layout layout_op(int op, int K) {
+    return op == 0 ? layout_for<0>(K) : op == 2 ? layout_for<2>(K) : layout_for<1>(K);
+}
 
-int b2b_stream_smem_bytes(int op, int K) { return int((op == 0 ? layout_for<0>(K) : layout_for<1>(K)).total); }
+int b2b_stream_stages(int op, int K) { return int(layout_op(op, K).stages); }
+
+int b2b_stream_smem_bytes(int op, int K) { return int(layout_op(op, K).total); }
 
 cudaError_t launch_b2b_stream(int op, const B2bArgs &a, int ctas, int smem, bool pdl, cudaStream_t stream) {
-    if (op != 0 && op != 1) return cudaErrorInvalidValue;
+    if (op < 0 || op > 2) return cudaErrorInvalidValue;
     void *fn = stream_fn(op, a.N2, a.K <= kMaxResidentK);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

@@ -872,7 +872,7 @@ static int b2b_active_cached(int device, int op, int cluster, int n2, int smem) 
 // B2B kernel choice: the cluster kernel (C = N1/256 CTAs per row block, the
 // intermediate's columns partitioned over the cluster, partial outputs
 // reduce-scattered) or the stream kernel (one CTA per row block, N1 streamed
-// in 256-column chunks; softmax and GELU only).  tuning->n_slice selects:
+// in 256-column chunks; LayerNorm in two passes).  tuning->n_slice selects:
 // 0 auto, 128 stream, 256 cluster (the plan reports the same values).
 static cf_status b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, int op, const cf_tuning *tuning,
                           const cf::DeviceInfo &dev, cf_plan *plan) {
@@ -882,11 +882,11 @@ static cf_status b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, int op, 
     if (M > (int64_t(1) << 31) - 128 || K > (int64_t(1) << 30) || N1 > (int64_t(1) << 30)) return CF_ERR_UNSUPPORTED;
     const int64_t C = N1 / 256;
     const bool cluster_ok = C == 1 || C == 2 || C == 4 || C == 8;
-    const bool stream_ok = op != CF_B2B_LAYERNORM;
     const int reqn = tuning ? tuning->n_slice : 0;
     bool stream;
-    if (reqn == 0) stream = stream_ok;  // one CTA per row block: no cluster exchange at all
-    else if (reqn == 128 && stream_ok) stream = true;
+    // one CTA per row block: no cluster exchange at all
+    if (reqn == 0) stream = true;
+    else if (reqn == 128) stream = true;
     else if (reqn == 256) stream = false;
     else return CF_ERR_UNSUPPORTED;
     if (!stream && !cluster_ok) return CF_ERR_UNSUPPORTED;
@@ -953,7 +953,6 @@ static cf_status b2b_common(const void *X, const void *W1, const float *b1, cons
     if (O == X || O == W1 || O == W2) return CF_ERR_INVALID_ARG;
     if (K % 8 != 0 || N1 % 256 != 0 || (N2 != 64 && N2 != 128)) return CF_ERR_UNSUPPORTED;
     if (ws_bytes < cf_b2b_workspace_size()) return CF_ERR_WORKSPACE_TOO_SMALL;
-    if (op == CF_B2B_LAYERNORM && N1 / 256 > 8) return CF_ERR_UNSUPPORTED;  // a cluster of at most 8
     if (M == 0) return CF_OK;
     cf::DeviceInfo dev;
     if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;

@@ -216,8 +216,10 @@ def test_newer_entry_points_check_arguments_without_a_gpu():
     assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 128, 512, 128, 1.0, 7, 16, big, 0) == cf.CF_ERR_INVALID_ARG
     assert cf.cf_b2b_gemm(24, 32, None, 48, 64, 128, 128, 512, 128, 1.0, 0, 16, big, 0) == cf.CF_ERR_MISALIGNED
     assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 128, 384, 128, 1.0, 0, 16, big, 0) == cf.CF_ERR_UNSUPPORTED
-    # 16 CTAs per row block: beyond the cluster kernel, the only one with the LayerNorm epilogue
-    assert cf.cf_b2b_gemm_layernorm(16, 32, None, 16, 16, 48, 64, 128, 128, 4096, 128, 1.0, 1e-5, 80, big,
+    # the LayerNorm epilogue: N1 in 256-column chunks, N2 in {64, 128}
+    assert cf.cf_b2b_gemm_layernorm(16, 32, None, 16, 16, 48, 64, 128, 128, 640, 128, 1.0, 1e-5, 80, big,
+                                    0) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm_layernorm(16, 32, None, 16, 16, 48, 64, 128, 128, 4096, 96, 1.0, 1e-5, 80, big,
                                     0) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 12, 512, 128, 1.0, 0, 16, big, 0) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 128, 512, 96, 1.0, 0, 16, big, 0) == cf.CF_ERR_UNSUPPORTED

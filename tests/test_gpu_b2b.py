@@ -51,7 +51,7 @@ def _tuning(mode, N1, **kw):
 
 
 def _modes(op):
-    return ["cluster"] if op == "layernorm" else ["cluster", "stream"]
+    return ["cluster", "stream"]
 
 
 CASES = [(op, mode) for op in OPS for mode in _modes(op)]
@@ -151,7 +151,7 @@ def test_b2b_persistent_tiles(op, mode, kw):
     check_b2b(o, ref, d, op, alpha, f"b2b {op} {mode} {kw}", mode=mode)
 
 
-@pytest.mark.parametrize("op", ["softmax", "gelu_tanh"])
+@pytest.mark.parametrize("op", ["softmax", "gelu_tanh", "layernorm"])
 @pytest.mark.parametrize("M,K,N1,N2,kw", [(300, 128, 4096, 128, {}), (129, 512, 768, 64, {}),
                                           (640, 1024, 512, 128, dict(max_clusters=2)),
                                           (256, 72, 256, 64, dict(stages=3))])
@@ -261,17 +261,15 @@ def test_b2b_empty_and_unsupported():
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 384, 128, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 96, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 12, 512, 128, 1.0, 0, ws, n) == cf.CF_ERR_UNSUPPORTED
-    # N1 = 4096: 16 CTAs per row block is beyond the cluster kernel (the stream
-    # kernel, which has no such limit, serves softmax and GELU only); a tile
-    # width other than 128 (stream) or 256 (cluster)
+    # N1 = 4096: 16 CTAs per row block is beyond the cluster kernel (the
+    # stream kernel has no such limit); a tile width other than 128 (stream)
+    # or 256 (cluster)
     g = torch.ones(512, device="cuda")
-    assert cf.cf_b2b_gemm_layernorm(X, W1, None, g, g, W2, O, 128, 128, 4096, 128, 1.0, 1e-5, ws,
-                                    n) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_b2b_gemm_layernorm(X, W1, None, g, g, W2, O, 128, 128, 4096, 128, 1.0, 1e-5, ws, n, None,
+                                    cf.tuning(n_slice=256)) == cf.CF_ERR_UNSUPPORTED
     for ns in (64, 192, 512):
         assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 128, 1.0, 0, ws, n, None,
                               cf.tuning(n_slice=ns)) == cf.CF_ERR_UNSUPPORTED
-    assert cf.cf_b2b_gemm_layernorm(X, W1, None, g, g, W2, O, 128, 128, 512, 128, 1.0, 1e-5, ws, n, None,
-                                    cf.tuning(n_slice=128)) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 128, 1.0, 3, ws, n) == cf.CF_ERR_INVALID_ARG
     # the LayerNorm epilogue needs gamma1 and beta1: only through its own entry point
     assert cf.cf_b2b_gemm(X, W1, None, W2, O, 128, 128, 512, 128, 1.0, 2, ws, n) == cf.CF_ERR_INVALID_ARG
@@ -286,7 +284,7 @@ def test_b2b_empty_and_unsupported():
 def test_b2b_plan():
     torch = torch_cuda()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # softmax and GELU default to the stream kernel: one CTA per SM, 128-column chunks
+    # the stream kernel is the default: one CTA per SM, 256-column chunks
     st, p = cf.cf_query_b2b_plan(32768, 128, 1024, 128, cf.CF_B2B_SOFTMAX)
     assert st == cf.CF_OK
     assert p.cluster_size == 1 and p.n_slice == 128 and p.row_blocks == 256 and p.clusters == min(256, sms)
@@ -297,15 +295,20 @@ def test_b2b_plan():
     assert p.clusters * p.cluster_size <= sms and p.smem_bytes <= 232448 and p.stages >= 2
     st, p = cf.cf_query_b2b_plan(100, 64, 2048, 64, cf.CF_B2B_GELU_TANH, cf.tuning(max_clusters=1))
     assert st == cf.CF_OK and p.cluster_size == 1 and p.clusters == 1
-    st, p = cf.cf_query_b2b_plan(100, 64, 2048, 64, cf.CF_B2B_LAYERNORM)
+    st, p = cf.cf_query_b2b_plan(100, 64, 2048, 64, cf.CF_B2B_LAYERNORM, cf.tuning(n_slice=256))
     assert st == cf.CF_OK and p.cluster_size == 8
+    # LayerNorm defaults to the stream kernel too, at any N1
+    for N1 in (2048, 4096):
+        st, p = cf.cf_query_b2b_plan(100, 64, N1, 64, cf.CF_B2B_LAYERNORM)
+        assert st == cf.CF_OK and p.cluster_size == 1 and p.n_slice == 128
 
 
 @pytest.mark.parametrize("name,mode", [("b2b_attn_32768x128x1024x128", "stream"),
                                        ("b2b_attn_32768x128x1024x128", "cluster"),
                                        ("b2b_gelu_16384x1024x2048x128", "stream"),
                                        ("b2b_gelu_16384x1024x2048x128", "cluster"),
-                                       ("b2b_ln_16384x1024x2048x128", "cluster")])
+                                       ("b2b_ln_16384x1024x2048x128", "cluster"),
+                                       ("b2b_ln_16384x1024x2048x128", "stream")])
 def test_b2b_full_workload(name, mode):
     w = inputs.WORKLOADS[name]
     d = inputs.workload_inputs(name)
