@@ -87,11 +87,12 @@ __host__ __device__ constexpr Layout layout() {
     L.stages = (!kRes && OP == 1) ? 4u : 3u;
     L.stg = L.ring + L.stages * L.stage;  // bf16 output staging: 2 KB (32 x 32, 64B swizzle) per epilogue warp
     // float [groups][2 chunk parities][kCols]: b1 of the group's columns (LayerNorm:
-    // [groups][2][3][kCols], b1, gamma1, beta1)
+    // [groups][2][2][kCols], b1 and gamma1)
     L.bias = L.stg + 4u * kGroups * 2048u;
-    L.xm = L.bias + kGroups * 2u * kCols * 4u * (OP == 2 ? 3u : 1u);
-    // softmax: float [2 chunk parities][groups][128] row maxima
-    L.stat = L.xm + (OP == 0 ? 2u * kGroups * 128u * 4u : 0u);
+    L.xm = L.bias + kGroups * 2u * kCols * 4u * (OP == 2 ? 2u : 1u);
+    // softmax: float [2 chunk parities][groups][128] row maxima; LayerNorm:
+    // float [2 rb parities][groups][128] means of the row block's first chunk
+    L.stat = L.xm + (OP != 1 ? 2u * kGroups * 128u * 4u : 0u);
     // softmax: float [2 rb parities][groups][128] row sums; LayerNorm: float2
     // [2 rb parities][groups][128] (mean, M2) of each group's columns
     L.bars = L.stat + (OP == 0 ? 2u * kGroups * 128u * 4u : OP == 2 ? 2u * kGroups * 128u * 8u : 0u);
@@ -120,7 +121,8 @@ __device__ __forceinline__ Bars bars_at(uint32_t b, int stages) {
 
 template <int OP, int kN2>
 __device__ __forceinline__ void stream_output(const CUtensorMap *tmap_o, bool no_out, int M, int m0, uint32_t tO_group,
-                                           uint32_t stg, float *st, float lk, int g, int q, int lane, uint32_t mfree,
+                                           uint32_t stg, float *st, float lk, MeanM2 ls, float mu0, const float *fold,
+                                           float n1, float eps, int g, int q, int lane, uint32_t mfree,
                                            volatile uint32_t *abort, unsigned long long *stamp) {
     constexpr int kOut = 32;  // output columns of a group: groups 0 .. N2/32 - 1 write, the rest only sync
     const int row = q * 32 + lane;
@@ -133,6 +135,21 @@ __device__ __forceinline__ void stream_output(const CUtensorMap *tmap_o, bool no
 #pragma unroll
         for (int h = 0; h < kGroups; ++h) lsum += st[h * 128 + row];
         inv = 1.f / lsum;
+    }
+    // LayerNorm: O = rstd (sum_n (z_n - mu0) gamma1_n W2_nk) - rstd (mu - mu0) c1_k + c0_k,
+    // c1 = gamma1^T W2 and c0 = beta1^T W2 (fold)
+    float sh = 0.f;
+    if constexpr (OP == 2) {
+        float2 *const st2 = reinterpret_cast<float2 *>(st);
+        st2[g * 128 + row] = make_float2(ls.mean, ls.m2);
+        ptx::named_bar_sync(kGroups + 1, 128 * kGroups);
+        const float ng = n1 * (1.f / float(kGroups));  // columns of a group
+        MeanM2 rs{st2[row].x, st2[row].y};
+#pragma unroll
+        for (int h = 1; h < kGroups; ++h)
+            rs = combine_counts(rs, ng * float(h), MeanM2{st2[h * 128 + row].x, st2[h * 128 + row].y}, ng);
+        inv = rsqrtf(rs.m2 / n1 + eps);
+        sh = (rs.mean - mu0) * inv;
     }
     if (g * kOut >= kN2) {
         ptx::tc_fence_before();
@@ -155,9 +172,20 @@ __device__ __forceinline__ void stream_output(const CUtensorMap *tmap_o, bool no
         }
         if (live) {
             uint32_t w[16];
+            if constexpr (OP == 2) {
+                const int k0 = g * kOut + c * 32;
 #pragma unroll
-            for (int h = 0; h < 16; ++h)
-                w[h] = ptx::pack_bf16x2(__uint_as_float(o[2 * h]) * inv, __uint_as_float(o[2 * h + 1]) * inv);
+                for (int h = 0; h < 16; ++h) {
+                    const float2 c1 = __ldg(reinterpret_cast<const float2 *>(fold + k0) + h);
+                    const float2 c0 = __ldg(reinterpret_cast<const float2 *>(fold + kN2 + k0) + h);
+                    w[h] = ptx::pack_bf16x2(fmaf(__uint_as_float(o[2 * h]), inv, fmaf(-sh, c1.x, c0.x)),
+                                            fmaf(__uint_as_float(o[2 * h + 1]), inv, fmaf(-sh, c1.y, c0.y)));
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < 16; ++h)
+                    w[h] = ptx::pack_bf16x2(__uint_as_float(o[2 * h]) * inv, __uint_as_float(o[2 * h + 1]) * inv);
+            }
             if (lane == 0) ptx::bulk_wait_group_read0();  // the previous store read the buffer
             __syncwarp();
 #pragma unroll
@@ -190,11 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
     constexpr Layout L = layout<OP, kRes>();
     constexpr int stages = int(L.stages);
     const int nc = a.N1 / kChunk;           // chunks per row block
-    // LayerNorm takes two passes over a row block's chunks: the statistics,
-    // then the normalised values for ML_2 (ML_1 runs twice); "virtual chunks"
-    // count both, output chunks the second
-    constexpr int kPasses = OP == 2 ? 2 : 1;
-    const int nv = kPasses * nc;
     const Bars B = bars_at(base + L.bars, stages);
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem_raw + (B.misc - base));
     volatile uint32_t *abort = misc + 1;
@@ -203,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
     const int RB = (a.M + 127) / 128;
     // row blocks of this CTA: blockIdx.x, + gridDim.x, ...; chunks J = i * nc + j
     const int nrb = int(blockIdx.x) < RB ? (RB - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x) : 0;
-    const int NJ = nrb * nv;  // virtual chunks of this CTA
+    const int NJ = nrb * nc;
     unsigned long long *const tr = a.trace;
     const unsigned long long t_start = ptx::globaltimer();
 
@@ -266,16 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                     ph ^= 1u;
                 }
             };
-            int i1 = 0, v1 = 0;  // (row block, virtual chunk) of the next ML_1
+            int i1 = 0, j1 = 0;  // (row block, chunk) of the next ML_1
             auto load_ml1 = [&](int J) {
-                const int i = i1, v = v1, j = v1 < nc ? v1 : v1 - nc;
-                if (++v1 == nv) {
-                    v1 = 0;
+                const int i = i1, j = j1;
+                if (++j1 == nc) {
+                    j1 = 0;
                     ++i1;
                 }
                 const int m0 = (int(blockIdx.x) + i * int(gridDim.x)) * 128;
                 trace_tile(tr, J, CF_TRB_TMA_FIRST);
-                if (resident && v == 0) {
+                if (resident && j == 0) {
                     // X of row block i into buffer i & 1, once row block i - 2 is done with it
                     const int b = i & 1;
                     if (i >= 2) {
@@ -317,11 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                 }
             };
             if (NJ > 0) load_ml1(0);
-            int vo = 0;  // virtual chunk J within its row block
             for (int J = 0; J < NJ && ok; ++J) {
                 if (J + 1 < NJ) load_ml1(J + 1);
-                if (vo >= nv - nc) load_ml2(J);  // an output chunk
-                if (++vo == nv) vo = 0;
+                load_ml2(J);
             }
             // every stage filled has been released before the CTA may exit
             const uint32_t first = it > uint32_t(stages) ? it - uint32_t(stages) : 0u;
@@ -366,11 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
             // (row block, chunk) of the next ML_1 and the next ML_2, advanced in
             // place: this thread's instructions between MMA groups are few (it
             // shares its SMSP's issue slots with four epilogue warps)
-            int i1 = 0, v1 = 0, i2 = 0, j2 = 0, o2 = 0;  // o2: output chunks issued
+            int i1 = 0, j1 = 0, i2 = 0, j2 = 0;
             auto ml1 = [&](int J) {
-                const int i = i1, v = v1;
-                if (++v1 == nv) {
-                    v1 = 0;
+                const int i = i1, j = j1;
+                if (++j1 == nc) {
+                    j1 = 0;
                     ++i1;
                 }
                 // S is free once both groups read the previous chunk
@@ -378,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                     ok = ptx::mbar_wait_bounded(B.s_free, uint32_t(J - 1) & 1u, tmo, abort, a.err, kInfoMma | 0x100u);
                     if (!ok) return;
                 }
-                if (resident && v == 0) {
+                if (resident && j == 0) {
                     ok = ptx::mbar_wait_bounded(B.xfull0 + 8 * (i & 1), uint32_t(i >> 1) & 1u, tmo, abort, a.err,
                                                 kInfoMma | 0x500u);
                     if (!ok) return;
@@ -398,17 +419,17 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                         ptx::mma_bf16(tmem, ad + uint64_t(2 * k), bd + uint64_t(128 * k), id1, (kb | k) != 0 ? 1u : 0u);
                     release();
                 }
-                if (resident && v == nv - 1) ptx::mma_commit(B.xfree0 + 8 * (i & 1));  // X buffer reusable
+                if (resident && j == nc - 1) ptx::mma_commit(B.xfree0 + 8 * (i & 1));  // X buffer reusable
                 ptx::mma_commit(B.s_full);
                 trace_tile(tr, J, CF_TRB_ML1_DONE);
             };
             auto ml2 = [&](int J) {
-                const int i = i2, j = j2, O = o2++;  // (row block, output chunk), output chunks before
+                const int i = i2, j = j2;
                 if (++j2 == nc) {
                     j2 = 0;
                     ++i2;
                 }
-                ok = ptx::mbar_wait_bounded(B.p_full, uint32_t(O) & 1u, tmo, abort, a.err, kInfoMma | 0x200u);
+                ok = ptx::mbar_wait_bounded(B.p_full, uint32_t(J) & 1u, tmo, abort, a.err, kInfoMma | 0x200u);
                 if (!ok) return;
                 // the row block's first ML_2 overwrites O: the previous row block's
                 // output has read it
@@ -435,11 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                 trace_tile(tr, J, CF_TRB_ML2_DONE);
             };
             if (NJ > 0) ml1(0);
-            int vo = 0;  // virtual chunk J within its row block
             for (int J = 0; J < NJ && ok; ++J) {
                 if (J + 1 < NJ) ml1(J + 1);
-                if (ok && vo >= nv - nc) ml2(J);  // an output chunk
-                if (++vo == nv) vo = 0;
+                if (ok) ml2(J);
             }
             ptx::mma_commit(B.mma_done);
             volatile uint32_t local_abort = 0;
@@ -462,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
         const uint32_t tP = tmem + lane_off + kColP + uint32_t(kCols / 2 * g); // and its packed P columns
         const uint32_t tO = tmem + lane_off + kColO + uint32_t(32 * g);       // its O columns (rescale)
         const bool owns_o = 32 * g < kN2;                                     // (N2 = 64: groups 0, 1)
-        constexpr int kPrm = OP == 2 ? 3 : 1;  // staged column parameters: b1 (LayerNorm: and gamma1, beta1)
+        constexpr int kPrm = OP == 2 ? 2 : 1;  // staged column parameters: b1 (LayerNorm: and gamma1)
         float *const prm = reinterpret_cast<float *>(smem_raw + L.bias) + g * 2 * kPrm * kCols;
         float *const xm = reinterpret_cast<float *>(smem_raw + L.xm);
         float *const stat = reinterpret_cast<float *>(smem_raw + L.stat);
@@ -471,37 +490,24 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
         // the parameters of the group's next chunk, loaded one chunk ahead (threads gt < 64)
         const bool pl = gt < kCols;
         auto ldp = [&](const float *v, int jc) -> float { return (v && pl) ? __ldg(v + jc * kChunk + kCols * g + gt) : 0.f; };
-        float nb = ldp(a.b1, 0), ng = 0.f, ne = 0.f;
-        if constexpr (OP == 2) {
-            ng = ldp(a.gamma1, 0);
-            ne = ldp(a.beta1, 0);
-        }
-        int J = 0;  // virtual chunks processed
-        int O = 0;  // output chunks processed
+        float nb = ldp(a.b1, 0), ng = 0.f;
+        if constexpr (OP == 2) ng = ldp(a.gamma1, 0);
+        int J = 0;
         for (int i = 0; i < nrb; ++i) {
-            float m = neg_inf(), l = 0.f;     // softmax: running max and sum of this group's columns
-            MeanM2 ls{0.f, 0.f};               // LayerNorm: (mean, M2) of this group's columns so far
-            float mu = 0.f, rstd = 0.f;        // LayerNorm: the row's statistics, after the first pass
-            for (int v = 0; v < nv; ++v, ++J) {
-                const int j = v < nc ? v : v - nc;     // W1 chunk
-                const bool out = v >= nv - nc;         // this chunk feeds ML_2
+            float m = neg_inf(), l = 0.f;  // softmax: running max and sum of this group's columns
+            MeanM2 ls{0.f, 0.f};            // LayerNorm: (mean, M2) of this group's columns so far
+            float mu0 = 0.f;                // LayerNorm: the row's shift (its first chunk's mean)
+            for (int j = 0; j < nc; ++j, ++J) {
                 // the chunk's parameters, double-buffered by chunk parity (the previous
                 // chunk's barrier ordered every read of this buffer before this write)
                 float *const bb = prm + (J & 1) * kPrm * kCols;
                 if (pl) {
                     bb[gt] = nb * bscale;
-                    if constexpr (OP == 2) {
-                        bb[kCols + gt] = ng;
-                        bb[2 * kCols + gt] = ne;
-                    }
+                    if constexpr (OP == 2) bb[kCols + gt] = ng;
                 }
-                const int vn = v + 1 < nv ? v + 1 : 0;
-                const int jn = vn < nc ? vn : vn - nc;
+                const int jn = j + 1 < nc ? j + 1 : 0;
                 nb = ldp(a.b1, jn);
-                if constexpr (OP == 2) {
-                    ng = ldp(a.gamma1, jn);
-                    ne = ldp(a.beta1, jn);
-                }
+                if constexpr (OP == 2) ng = ldp(a.gamma1, jn);
                 ptx::named_bar_sync(1u + uint32_t(g), 128);
                 ptx::mbar_wait_bounded(B.s_full, uint32_t(J) & 1u, tmo, abort, a.err, kInfoEpi | uint32_t(g));
                 ptx::tc_fence_after();
@@ -568,54 +574,47 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
 #pragma unroll
                         for (int k = 0; k < 32; ++k)
                             x[c][k] = __float_as_uint(fmaf(ascale, __uint_as_float(x[c][k]), bb[c * 32 + k]));
-                    if (!out) {
-                        // first pass: (mean, M2) of the chunk's 64 values (two passes over the
-                        // registers), folded into the group's running pair by counts
-                        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                    // (mean, M2) of the chunk's 64 values (two passes over the registers),
+                    // folded into the group's running pair by counts
+                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int c = 0; c < kFrag; ++c)
+                    for (int c = 0; c < kFrag; ++c)
 #pragma unroll
-                            for (int k = 0; k < 32; ++k) s4[k & 3] += __uint_as_float(x[c][k]);
-                        const float cmean = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * (1.f / float(kCols));
-                        float q4[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int k = 0; k < 32; ++k) s4[k & 3] += __uint_as_float(x[c][k]);
+                    const float cmean = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * (1.f / float(kCols));
+                    float q4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int c = 0; c < kFrag; ++c)
+                    for (int c = 0; c < kFrag; ++c)
 #pragma unroll
-                            for (int k = 0; k < 32; ++k) {
-                                const float d = __uint_as_float(x[c][k]) - cmean;
-                                q4[k & 3] = fmaf(d, d, q4[k & 3]);
-                            }
-                        const MeanM2 cs{cmean, (q4[0] + q4[1]) + (q4[2] + q4[3])};
-                        ls = j == 0 ? cs : combine_counts(ls, float(kCols * j), cs, float(kCols));
-                        if (v == nc - 1) {
-                            // the row's statistics over all N1 columns: every group's part
-                            // (equal counts), through shared memory
-                            float2 *const st2 = reinterpret_cast<float2 *>(stat) + (i & 1) * (128 * kGroups);
-                            st2[g * 128 + row] = make_float2(ls.mean, ls.m2);
-                            ptx::named_bar_sync(kGroups + 1, 128 * kGroups);
-                            const float ng_cols = float(kCols * nc);
-                            MeanM2 rs{st2[row].x, st2[row].y};
-#pragma unroll
-                            for (int h = 1; h < kGroups; ++h)
-                                rs = combine_counts(rs, ng_cols * float(h), MeanM2{st2[h * 128 + row].x, st2[h * 128 + row].y},
-                                                    ng_cols);
-                            mu = rs.mean;
-                            rstd = rsqrtf(rs.m2 / float(a.N1) + a.eps);
+                        for (int k = 0; k < 32; ++k) {
+                            const float d = __uint_as_float(x[c][k]) - cmean;
+                            q4[k & 3] = fmaf(d, d, q4[k & 3]);
                         }
+                    const MeanM2 cs{cmean, (q4[0] + q4[1]) + (q4[2] + q4[3])};
+                    if (j == 0) {
+                        // the row's shift: the mean of its first chunk, from every
+                        // group's part (every group sums them in the same order)
+                        float *const xmi = xm + (i & 1) * (128 * kGroups);
+                        xmi[g * 128 + row] = cmean;
+                        ptx::named_bar_sync(kGroups + 1, 128 * kGroups);
+                        float t = xmi[row];
+#pragma unroll
+                        for (int h = 1; h < kGroups; ++h) t += xmi[h * 128 + row];
+                        mu0 = t * (1.f / float(kGroups));
+                        ls = cs;
                     } else {
-                        // second pass: (z - mean) * rstd * gamma1 + beta1, packed in place
-#pragma unroll
-                        for (int c = 0; c < kFrag; ++c)
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) {
-                                const int n0 = c * 32 + 2 * k;
-                                const float y0 =
-                                    fmaf((__uint_as_float(x[c][2 * k]) - mu) * rstd, bb[kCols + n0], bb[2 * kCols + n0]);
-                                const float y1 = fmaf((__uint_as_float(x[c][2 * k + 1]) - mu) * rstd,
-                                                      bb[kCols + n0 + 1], bb[2 * kCols + n0 + 1]);
-                                x[c][k] = ptx::pack_bf16x2(y0, y1);
-                            }
+                        ls = combine_counts(ls, float(kCols * j), cs, float(kCols));
                     }
+                    // the shifted, scaled values (z - mu0) gamma1; the statistics and
+                    // beta1 are applied to the fp32 output
+#pragma unroll
+                    for (int c = 0; c < kFrag; ++c)
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const int n0 = c * 32 + 2 * k;
+                            x[c][k] = ptx::pack_bf16x2((__uint_as_float(x[c][2 * k]) - mu0) * bb[kCols + n0],
+                                                       (__uint_as_float(x[c][2 * k + 1]) - mu0) * bb[kCols + n0 + 1]);
+                        }
                 } else {
 #pragma unroll
                     for (int c = 0; c < kFrag; ++c)
@@ -627,11 +626,10 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                             x[c][k] = ptx::pack_bf16x2(x0, x1);
                         }
                 }
-                if (!out) continue;  // (LayerNorm's first pass feeds no ML_2)
-                // P and O: ML_2 of the previous output chunk is complete (it read P; O
-                // holds every earlier chunk)
-                if (O > 0)
-                    ptx::mbar_wait_bounded(B.o_full, uint32_t(O - 1) & 1u, tmo, abort, a.err, kInfoEpi | 0x10u);
+                // P and O: ML_2 of the previous chunk is complete (it read P; O holds
+                // every earlier chunk)
+                if (J > 0)
+                    ptx::mbar_wait_bounded(B.o_full, uint32_t(J - 1) & 1u, tmo, abort, a.err, kInfoEpi | 0x10u);
                 ptx::tc_fence_after();
                 if constexpr (OP == 0) {
                     // O carries the previous chunks against the old reference: rescale
@@ -659,15 +657,15 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(B.p_full);
                 if (lead && g == 0) trace_tile(tr, J, CF_TRB_EPI1_DONE);
-                ++O;
             }
             // ---------------- the row block's output, once its last ML_2 completed;
             // ML_1 of the next row block's first chunk runs meanwhile
-            ptx::mbar_wait_bounded(B.o_full, uint32_t(O - 1) & 1u, tmo, abort, a.err, kInfoEpi | 0x20u);
+            ptx::mbar_wait_bounded(B.o_full, uint32_t(J - 1) & 1u, tmo, abort, a.err, kInfoEpi | 0x20u);
             ptx::tc_fence_after();
             stream_output<OP, kN2>(&a.tmap_o, a.out == nullptr, a.M, (int(blockIdx.x) + i * int(gridDim.x)) * 128,
                                    tmem + lane_off + kColO, base + L.stg + uint32_t(warp - 2) * 2048u,
-                                   stat + (i & 1) * (128 * kGroups), l, g, q, lane, B.mfree, abort,
+                                   stat + (i & 1) * (128 * kGroups) * (OP == 2 ? 2 : 1), l, ls, mu0, a.fold,
+                                   float(a.N1), a.eps, g, q, lane, B.mfree, abort,
                                    (lead && g == 0 && tr != nullptr && J - 1 < CF_TRACE_TILES)
                                        ? tr + blockIdx.x * CF_TRACE_SLOTS + 4 + (J - 1) * CF_TRACE_EVENTS +
                                              CF_TRB_EPI2_STORED
@@ -686,6 +684,61 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
     ptx::tc_fence_after();
     if (warp == 1) ptx::tmem_dealloc(tmem, 512);
     if (threadIdx.x == 64) trace_stamp(tr, 3);
+}
+
+// c[0][k] = sum_n gamma1[n] W2[n, k], c[1][k] = sum_n beta1[n] W2[n, k].  Block
+// (x, y): columns [64 x, 64 x + 64) (a bf16 pair per lane), rows of split y
+// (eight warps, interleaved); the block's sums go to partials[y], and the
+// last block of column group x to finish adds the partials in split order
+// (a fixed order: the result does not depend on which block finished last).
+__global__ void __launch_bounds__(256) b2b_ln_fold_kernel(const uint32_t *__restrict__ w2, const float *__restrict__ gamma,
+                                                          const float *__restrict__ beta, float *c, float *part,
+                                                          unsigned int *counter, int N1, int N2) {
+    ptx::griddep_wait();  // W2, gamma1, beta1 may come from the previous kernel; it has read c
+    ptx::griddep_launch_dependents();
+    __shared__ float red[8][2][64];
+    __shared__ unsigned int is_last;
+    const int x = blockIdx.x, y = blockIdx.y, S = gridDim.y;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int per = (N1 + S - 1) / S;
+    const int n0 = y * per, n1 = min(N1, n0 + per);
+    const size_t pitch = size_t(N2 / 2);  // bf16 pairs per row of W2
+    const uint32_t *col = w2 + 32 * x + lane;
+    float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll 4
+    for (int n = n0 + w; n < n1; n += 8) {
+        const uint32_t p = __ldg(col + size_t(n) * pitch);
+        const float w0 = __uint_as_float(p << 16), w1 = __uint_as_float(p & 0xffff0000u);
+        const float gn = __ldg(gamma + n), bn = __ldg(beta + n);
+        g0 = fmaf(gn, w0, g0);
+        g1 = fmaf(gn, w1, g1);
+        b0 = fmaf(bn, w0, b0);
+        b1 = fmaf(bn, w1, b1);
+    }
+    red[w][0][2 * lane] = g0;
+    red[w][0][2 * lane + 1] = g1;
+    red[w][1][2 * lane] = b0;
+    red[w][1][2 * lane + 1] = b1;
+    __syncthreads();
+    const int kind = threadIdx.x >> 6, k = threadIdx.x & 63;  // threads < 128
+    if (threadIdx.x < 128) {
+        float t = 0.f;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) t += red[h][kind][k];
+        part[(size_t(y) * 2 + size_t(kind)) * 128 + size_t(64 * x + k)] = t;
+        __threadfence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(counter + x, 1u) == unsigned(S - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    if (threadIdx.x < 128) {
+        float t = 0.f;
+        for (int h = 0; h < S; ++h) t += __ldcg(part + (size_t(h) * 2 + size_t(kind)) * 128 + size_t(64 * x + k));
+        c[kind * N2 + 64 * x + k] = t;
+    }
+    if (threadIdx.x == 0) counter[x] = 0u;  // for the next call (every block of this one has counted)
 }
 
 template <int OP, bool kRes>
@@ -713,6 +766,23 @@ static Layout layout_op(int op, int K) {
 int b2b_stream_stages(int op, int K) { return int(layout_op(op, K).stages); }
 
 int b2b_stream_smem_bytes(int op, int K) { return int(layout_op(op, K).total); }
+
+cudaError_t launch_b2b_ln_fold(const void *W2, const float *gamma1, const float *beta1, int N1, int N2,
+                               unsigned char *ws, bool pdl, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(N2 / 64), unsigned(N1 / 64 < kB2bFoldSplits ? (N1 / 64 > 0 ? N1 / 64 : 1)
+                                                                              : kB2bFoldSplits));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, b2b_ln_fold_kernel, static_cast<const uint32_t *>(W2), gamma1, beta1,
+                              reinterpret_cast<float *>(ws + kB2bFoldOff), reinterpret_cast<float *>(ws + kB2bFoldPartialsOff),
+                              reinterpret_cast<unsigned int *>(ws + kB2bFoldCountersOff), N1, N2);
+}
 
 cudaError_t launch_b2b_stream(int op, const B2bArgs &a, int ctas, int smem, bool pdl, cudaStream_t stream) {
     if (op < 0 || op > 2) return cudaErrorInvalidValue;

@@ -853,7 +853,7 @@ cf_status cf_gemm_fused_rowsoftmax(const void *X, const void *W, const float *bi
 // -------------------------------------------------------------------------
 // back-to-back GEMM
 // -------------------------------------------------------------------------
-size_t cf_b2b_workspace_size(void) { return cf::kErrBytes; }
+size_t cf_b2b_workspace_size(void) { return cf::kB2bWorkspaceBytes; }
 
 static int b2b_active_cached(int device, int op, int cluster, int n2, int smem) {
     static std::map<std::tuple<int, int, int, int, int>, int> cache;
@@ -988,6 +988,14 @@ static cf_status b2b_common(const void *X, const void *W1, const float *b1, cons
     a.trace = tuning ? reinterpret_cast<unsigned long long *>(tuning->trace) : nullptr;
     a.extra_arrivals = tuning && tuning->extra_arrivals > 0 ? tuning->extra_arrivals : 0;
     const bool pdl = !(tuning && tuning->disable_pdl);
+    if (stream_kernel && op == CF_B2B_LAYERNORM) {
+        // the LayerNorm output terms gamma1^T W2 and beta1^T W2, read by the
+        // stream kernel once its row statistics are known
+        a.fold = reinterpret_cast<const float *>(static_cast<unsigned char *>(ws) + cf::kB2bFoldOff);
+        cudaError_t ef = cf::launch_b2b_ln_fold(W2, gamma1, beta1, int(N1), int(N2), static_cast<unsigned char *>(ws),
+                                                pdl, reinterpret_cast<cudaStream_t>(stream));
+        if (ef != cudaSuccess) return cuda_fail(ef);
+    }
     cudaError_t e = stream_kernel ? cf::launch_b2b_stream(op, a, plan.clusters, plan.smem_bytes, pdl,
                                                           reinterpret_cast<cudaStream_t>(stream))
                                   : cf::launch_b2b(op, a, plan.clusters, plan.stages, plan.smem_bytes, pdl,

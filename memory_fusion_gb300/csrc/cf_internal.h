@@ -189,6 +189,7 @@ struct B2bArgs {
     unsigned long long timeout_ns;
     unsigned long long *trace;  // optional %globaltimer stamps, CF_TRACE_SLOTS per CTA
     int extra_arrivals;   // test hook (stream kernel): added to the per-chunk P-ready count
+    const float *fold;    // stream kernel, LayerNorm F: c1 = gamma1^T W2, c0 = beta1^T W2 (fp32 [2][N2])
 };
 
 int b2b_smem_bytes(int stages, int cluster, int n2, int op);
@@ -199,5 +200,15 @@ cudaError_t launch_b2b(int op, const B2bArgs &a, int clusters, int stages, int s
 int b2b_stream_stages(int op, int K);  // ring depth, fixed per epilogue and mode (X resident or streamed)
 int b2b_stream_smem_bytes(int op, int K);
 cudaError_t launch_b2b_stream(int op, const B2bArgs &a, int ctas, int smem, bool pdl, cudaStream_t stream);
+// The stream kernel's LayerNorm output terms c1 = gamma1^T W2 and c0 = beta1^T W2
+// (fp32, fixed summation order), computed by a small kernel launched before it.
+// Workspace: the error word, c [2][128] fp32, two counters, the partial sums.
+constexpr int kB2bFoldSplits = 32;
+constexpr size_t kB2bFoldOff = kErrBytes;
+constexpr size_t kB2bFoldCountersOff = kB2bFoldOff + 2 * 128 * sizeof(float);
+constexpr size_t kB2bFoldPartialsOff = kB2bFoldCountersOff + 256;
+constexpr size_t kB2bWorkspaceBytes = kB2bFoldPartialsOff + size_t(kB2bFoldSplits) * 2 * 128 * sizeof(float);
+cudaError_t launch_b2b_ln_fold(const void *W2, const float *gamma1, const float *beta1, int N1, int N2,
+                               unsigned char *ws, bool pdl, cudaStream_t stream);
 
 }  // namespace cf

@@ -211,7 +211,9 @@ def test_argument_errors_need_no_gpu():
 def test_newer_entry_points_check_arguments_without_a_gpu():
     big = 1 << 20
     # back-to-back GEMM
-    assert cf.cf_b2b_workspace_size() == 256
+    # the error word, then (LayerNorm on the stream kernel) gamma1^T W2 and
+    # beta1^T W2, two counters and 32 x 2 x 128 partial sums
+    assert cf.cf_b2b_workspace_size() == 256 + 1024 + 256 + 32 * 2 * 128 * 4
     assert cf.cf_b2b_gemm(None, 16, None, 16, 16, 128, 128, 512, 128, 1.0, 0, 16, big, 0) == cf.CF_ERR_INVALID_ARG
     assert cf.cf_b2b_gemm(16, 32, None, 48, 64, 128, 128, 512, 128, 1.0, 7, 16, big, 0) == cf.CF_ERR_INVALID_ARG
     assert cf.cf_b2b_gemm(24, 32, None, 48, 64, 128, 128, 512, 128, 1.0, 0, 16, big, 0) == cf.CF_ERR_MISALIGNED

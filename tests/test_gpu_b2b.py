@@ -1,8 +1,8 @@
 """GPU parity of the back-to-back GEMM O = bf16(F(alpha X.W1 + b1)) . W2
 (through the C ABI) against the fp64 oracle, on both kernels -- the cluster
 kernel (N1 partitioned over C = N1/256 CTAs, tuning n_slice = 256) and the
-stream kernel (one CTA per row block, N1 in 128-column chunks, n_slice = 128;
-softmax and GELU): the softmax, GELU and LayerNorm epilogues, every cluster
+stream kernel (one CTA per row block, N1 in 256-column chunks, n_slice = 128):
+the softmax, GELU and LayerNorm epilogues, every cluster
 width N1/256 in {1, 2, 4, 8} and wider N1 on the stream kernel, both output
 widths, ragged rows and a ragged last K block, X resident and streamed, the
 online softmax's rescaling, several row blocks per CTA or cluster (the ring,
@@ -31,6 +31,14 @@ element still differs by at most 2^-8 |s_j| (inside the flip term), but the
 two roundings are now independent: their difference adds noise of RMS at
 most 2^-9 sqrt(2/3) sqrt(sum_j s_j^2 W2_jk^2) to each output, which the mean
 check allows for on that kernel.
+
+The stream kernel's LayerNorm feeds MatMul_2 the bf16 values
+t_j / rstd = (z_j - mu0) gamma1_j, mu0 the mean of the row's first 256
+columns, and applies rstd, the mean correction -(mu - mu0) rstd gamma1^T W2
+and beta1^T W2 to the fp32 output.  Its rounding is relative to
+|t_j| = |(z_j - mu0) gamma1_j rstd| instead of |s_j|, and independent of the
+oracle's: the flip term gains 2^-8 sum_j |t_j||W2_jk| and the mean check the
+noise 2^-9 sqrt(2/3) sqrt(sum_j t_j^2 W2_jk^2).
 """
 import numpy as np
 import pytest
@@ -86,32 +94,44 @@ def _s(d, op, z):
     return oracle.layernorm_rows(z, d["gamma1"], d["beta1"], 1e-5)
 
 
-def _terms(d, op, alpha, rows=None):
-    """Per element of the output: sum_j |s_j||W2_jk|, sum_j |z_j||W2_jk| and
-    sqrt(sum_j s_j^2 W2_jk^2)."""
+def _shifted(d, z):
+    """The stream kernel's LayerNorm operand of MatMul_2 in units of S:
+    t_j = (z_j - mu0) gamma1_j rstd, mu0 the mean of the row's first 256 columns."""
+    mu0 = z[:, :256].mean(axis=1, keepdims=True)
+    rstd = 1.0 / np.sqrt(z.var(axis=1, keepdims=True) + 1e-5)
+    return (z - mu0) * np.asarray(d["gamma1"], np.float64) * rstd
+
+
+def _terms(d, op, alpha, rows=None, mode="cluster"):
+    """Per element of the output: sum_j |s_j||W2_jk|, sum_j |z_j||W2_jk|,
+    sqrt(sum_j r_j^2 W2_jk^2) and sum_j |r_j||W2_jk|, r the values the kernel
+    rounds to bf16 (s, or t for the stream kernel's LayerNorm)."""
     X = d["X"] if rows is None else d["X"][rows]
     z = alpha * oracle.gemm(X, d["W1"]) + (0.0 if d.get("b1") is None else np.asarray(d["b1"], np.float64))
     s = _s(d, op, z)
+    r = _shifted(d, z) if (op == "layernorm" and mode == "stream") else s
     aw = np.abs(np.asarray(d["W2"], np.float64))
-    return np.abs(s) @ aw, np.abs(z) @ aw, np.sqrt((s * s) @ (aw * aw))
+    return np.abs(s) @ aw, np.abs(z) @ aw, np.sqrt((r * r) @ (aw * aw)), np.abs(r) @ aw
 
 
 def check_b2b(o, ref, d, op, alpha, what, rows=None, mode="cluster"):
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
     N1 = d["W1"].shape[1]
-    A, Z, Q = _terms(d, op, alpha, rows)
+    A, Z, Q, R = _terms(d, op, alpha, rows, mode)
     flip = (2.0 ** -7 + 2.0 ** -16 + N1 * 2.0 ** -24) * A
     if op == "gelu_tanh":
         flip = flip + 0.5 * 2.0 ** -10.98 * Z
     if op == "layernorm":  # fp32 statistics: an error near 2^-14 of the row spread in each S element
         flip = flip + 2.0 ** -14 * (A + np.abs(np.asarray(d["W2"], np.float64)).sum(axis=0))
+        if mode == "stream":
+            flip = flip + 2.0 ** -8 * R
     bound = flip + bf16_half_ulp(np.abs(ref) + flip)
     err = np.abs(o - ref)
     worst = np.argmax(err - bound)
     assert err.flat[worst] <= bound.flat[worst], (
         f"{what}: error {err.flat[worst]:.3e} > bound {bound.flat[worst]:.3e} at |ref|={abs(ref.flat[worst]):.3e}")
     mean_bound = bf16_half_ulp(np.abs(ref)).mean() + 2.0 ** -12 * flip.mean()
-    if mode == "stream" and op == "softmax":  # independent roundings of S (see the module docstring)
+    if mode == "stream" and op in ("softmax", "layernorm"):  # independent roundings (module docstring)
         mean_bound += 2.0 ** -9 * np.sqrt(2.0 / 3.0) * Q.mean()
     assert err.mean() <= mean_bound, f"{what}: mean error {err.mean():.3e} > {mean_bound:.3e}"
 
@@ -180,6 +200,20 @@ def test_b2b_stream_softmax_rescaling(ramp):
     check_b2b(o, ref, d, "softmax", alpha, f"b2b stream rescale {ramp}", mode="stream")
 
 
+@pytest.mark.parametrize("offset,ramp", [(40.0, 0.0), (0.0, 6.0), (-25.0, -3.0)])
+def test_b2b_stream_layernorm_shifted_rows(offset, ramp):
+    """Rows whose mean is far from 0 (b1 offset) and whose first chunk's mean
+    is far from the row's (b1 ramps over N1): the stream kernel's shift mu0
+    and its correction -(mu - mu0) rstd gamma1^T W2 are exercised, and the
+    normalised result must not lose the precision of the row's spread."""
+    M, K, N1, N2 = 384, 128, 1024, 128
+    d = _inputs(M, K, N1, N2, seed=71, op="layernorm")
+    d["b1"] = (np.asarray(d["b1"], np.float64) + offset + ramp * np.linspace(-1.0, 1.0, N1)).astype(np.float32)
+    o = _run(d, "layernorm", 1.0, tuning=_tuning("stream", N1))
+    ref = _ref(d, "layernorm", 1.0)
+    check_b2b(o, ref, d, "layernorm", 1.0, f"stream LayerNorm offset {offset} ramp {ramp}", mode="stream")
+
+
 def test_b2b_kernels_agree_on_gelu():
     """GELU rounds the same value in both kernels: outputs within fp32
     accumulation-order noise of each other (the sums over N1 run in a
@@ -188,7 +222,7 @@ def test_b2b_kernels_agree_on_gelu():
     d = _inputs(M, K, N1, N2, seed=37, op="gelu_tanh")
     a = _run(d, "gelu_tanh", 1.0, tuning=_tuning("cluster", N1))
     b = _run(d, "gelu_tanh", 1.0, tuning=_tuning("stream", N1))
-    A, _, _ = _terms(d, "gelu_tanh", 1.0)
+    A, _, _, _ = _terms(d, "gelu_tanh", 1.0)
     bound = 2 * bf16_half_ulp(np.abs(a) + N1 * 2.0 ** -23 * A) + N1 * 2.0 ** -23 * A
     assert np.all(np.abs(a - b) <= bound)
 
@@ -218,6 +252,10 @@ def test_b2b_selector_reads_back_s(op, mode, N1, N2):
         # the unnormalised exponential is rounded (relative error <= 2^-8), then
         # the output: one bf16 rounding more than the cluster kernel's
         bound = bf16_half_ulp(np.abs(sel) + e) + 2.0 ** -8 * (np.abs(sel) + e) + e
+    if mode == "stream" and op == "layernorm":
+        # (z - mu0) gamma1 is rounded (relative error <= 2^-9 of |t|), then the output
+        t = np.abs(_shifted(d, z)[:, cols])
+        bound = bf16_half_ulp(np.abs(sel) + 2.0 ** -8 * t + e) + 2.0 ** -8 * t + e
     err = np.abs(o - sel)
     worst = np.argmax(err - bound)
     assert err.flat[worst] <= bound.flat[worst], (
