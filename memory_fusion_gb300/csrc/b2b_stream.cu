@@ -68,8 +68,16 @@ constexpr uint32_t kInfoEpi = 0x93000000u;
 
 // Shared-memory layout, fixed per epilogue and mode (compile-time offsets keep
 // the epilogue's registers for its data): resident X (K <= 128) with a
-// 3-stage ring of 32 KB, or X streamed with W1 through a ring of 48 KB stages
-// (4 for GELU, 3 for softmax, whose row statistics take the room of one).
+// 3-stage ring of 32 KB, or X streamed with W1 through a ring of 4 stages of
+// 48 KB.  The output leaves through TMA stores from a staging buffer, except
+// where X streams and the epilogue keeps row statistics (softmax, LayerNorm):
+// there the fourth stage takes that room and each thread writes its row's
+// 64-byte segments directly.
+template <int OP, bool kRes>
+__host__ __device__ constexpr bool direct_out() {
+    return !kRes && OP != 1;
+}
+
 struct Layout {
     uint32_t xres, xbytes, ring, stage, stages, stg, bias, xm, stat, bars, total;
 };
@@ -84,11 +92,11 @@ __host__ __device__ constexpr Layout layout() {
     // of a W2 chunk (128 rows x N2 <= 32 KB)
     L.stage = kRes ? uint32_t(kW1Block) : uint32_t(kXBlock + kW1Block);
     // (GELU has no row statistics: a fourth stage fits when X streams)
-    L.stages = (!kRes && OP == 1) ? 4u : 3u;
+    L.stages = kRes ? 3u : 4u;
     L.stg = L.ring + L.stages * L.stage;  // bf16 output staging: 2 KB (32 x 32, 64B swizzle) per epilogue warp
     // float [groups][2 chunk parities][kCols]: b1 of the group's columns (LayerNorm:
     // [groups][2][2][kCols], b1 and gamma1)
-    L.bias = L.stg + 4u * kGroups * 2048u;
+    L.bias = L.stg + (direct_out<OP, kRes>() ? 0u : 4u * kGroups * 2048u);
     L.xm = L.bias + kGroups * 2u * kCols * 4u * (OP == 2 ? 2u : 1u);
     // softmax: float [2 chunk parities][groups][128] row maxima; LayerNorm:
     // float [2 rb parities][groups][128] means of the row block's first chunk
@@ -119,8 +127,8 @@ __device__ __forceinline__ Bars bars_at(uint32_t b, int stages) {
     return r;
 }
 
-template <int OP, int kN2>
-__device__ __forceinline__ void stream_output(const CUtensorMap *tmap_o, bool no_out, int M, int m0, uint32_t tO_group,
+template <int OP, int kN2, bool kDirect>
+__device__ __forceinline__ void stream_output(const CUtensorMap *tmap_o, uint16_t *out, int M, int m0, uint32_t tO_group,
                                            uint32_t stg, float *st, float lk, MeanM2 ls, float mu0, const float *fold,
                                            float n1, float eps, int g, int q, int lane, uint32_t mfree,
                                            volatile uint32_t *abort, unsigned long long *stamp) {
@@ -157,7 +165,7 @@ __device__ __forceinline__ void stream_output(const CUtensorMap *tmap_o, bool no
         if (lane == 0) ptx::mbar_arrive(mfree);
         return;
     }
-    const bool live = m0 + q * 32 < M && !*abort && !no_out;  // warp-uniform
+    const bool live = m0 + q * 32 < M && !*abort && out != nullptr;  // warp-uniform
     const uint32_t sw = (uint32_t(lane) >> 1) & 3u;
     const uint64_t pol_o = ptx::policy_evict_first();  // the output is written once
 #pragma unroll
@@ -185,6 +193,16 @@ __device__ __forceinline__ void stream_output(const CUtensorMap *tmap_o, bool no
 #pragma unroll
                 for (int h = 0; h < 16; ++h)
                     w[h] = ptx::pack_bf16x2(__uint_as_float(o[2 * h]) * inv, __uint_as_float(o[2 * h + 1]) * inv);
+            }
+            if constexpr (kDirect) {
+                // the row's 32 columns: 64 contiguous bytes
+                if (m0 + row < M) {
+                    uint4 *const dst =
+                        reinterpret_cast<uint4 *>(out + size_t(m0 + row) * size_t(kN2) + size_t(g * kOut + c * 32));
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) dst[k4] = make_uint4(w[4 * k4], w[4 * k4 + 1], w[4 * k4 + 2], w[4 * k4 + 3]);
+                }
+                continue;
             }
             if (lane == 0) ptx::bulk_wait_group_read0();  // the previous store read the buffer
             __syncwarp();
@@ -662,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
             // ML_1 of the next row block's first chunk runs meanwhile
             ptx::mbar_wait_bounded(B.o_full, uint32_t(J - 1) & 1u, tmo, abort, a.err, kInfoEpi | 0x20u);
             ptx::tc_fence_after();
-            stream_output<OP, kN2>(&a.tmap_o, a.out == nullptr, a.M, (int(blockIdx.x) + i * int(gridDim.x)) * 128,
+            stream_output<OP, kN2, direct_out<OP, kRes>()>(&a.tmap_o, a.out, a.M, (int(blockIdx.x) + i * int(gridDim.x)) * 128,
                                    tmem + lane_off + kColO, base + L.stg + uint32_t(warp - 2) * 2048u,
                                    stat + (i & 1) * (128 * kGroups) * (OP == 2 ? 2 : 1), l, ls, mu0, a.fold,
                                    float(a.N1), a.eps, g, q, lane, B.mfree, abort,
@@ -697,6 +715,7 @@ __global__ void __launch_bounds__(256) b2b_ln_fold_kernel(const uint32_t *__rest
     ptx::griddep_wait();  // W2, gamma1, beta1 may come from the previous kernel; it has read c
     ptx::griddep_launch_dependents();
     __shared__ float red[8][2][64];
+    float(*const red2)[128] = reinterpret_cast<float(*)[128]>(&red[0][0][0]);  // the last block's [2][128]
     __shared__ unsigned int is_last;
     const int x = blockIdx.x, y = blockIdx.y, S = gridDim.y;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -705,7 +724,7 @@ __global__ void __launch_bounds__(256) b2b_ln_fold_kernel(const uint32_t *__rest
     const size_t pitch = size_t(N2 / 2);  // bf16 pairs per row of W2
     const uint32_t *col = w2 + 32 * x + lane;
     float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int n = n0 + w; n < n1; n += 8) {
         const uint32_t p = __ldg(col + size_t(n) * pitch);
         const float w0 = __uint_as_float(p << 16), w1 = __uint_as_float(p & 0xffff0000u);
@@ -733,11 +752,18 @@ __global__ void __launch_bounds__(256) b2b_ln_fold_kernel(const uint32_t *__rest
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    if (threadIdx.x < 128) {
-        float t = 0.f;
-        for (int h = 0; h < S; ++h) t += __ldcg(part + (size_t(h) * 2 + size_t(kind)) * 128 + size_t(64 * x + k));
-        c[kind * N2 + 64 * x + k] = t;
+    // two halves of the splits (S is even), every load issued before the adds
+    {
+        const int half = threadIdx.x >> 7, v = threadIdx.x & 127, hs = S / 2;
+        const float *src = part + (size_t(half * hs) * 2 + size_t(v >> 6)) * 128 + size_t(64 * x + (v & 63));
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < kB2bFoldSplits / 2; ++h)
+            if (h < hs) acc[h & 3] += __ldcg(src + size_t(h) * 256);
+        red2[half][v] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
+    __syncthreads();
+    if (threadIdx.x < 128) c[kind * N2 + 64 * x + k] = red2[0][threadIdx.x] + red2[1][threadIdx.x];
     if (threadIdx.x == 0) counter[x] = 0u;  // for the next call (every block of this one has counted)
 }
 
