@@ -148,6 +148,7 @@ __device__ __forceinline__ void stream_output(const CUtensorMap *tmap_o, uint16_
     // c1 = gamma1^T W2 and c0 = beta1^T W2 (fold)
     float sh = 0.f;
     if constexpr (OP == 2) {
+        ptx::griddep_wait();  // the fold kernel has completed (no-op after the first row block)
         float2 *const st2 = reinterpret_cast<float2 *>(st);
         st2[g * 128 + row] = make_float2(ls.mean, ls.m2);
         ptx::named_bar_sync(kGroups + 1, 128 * kGroups);
@@ -282,7 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
     ptx::griddep_launch_dependents();
-    ptx::griddep_wait();
+    // LayerNorm: the fold kernel launched just before this one let it start
+    // only once the grids before the fold had completed, so the inputs are
+    // ready; the fold's own output is waited for before the first output stage
+    if constexpr (OP != 2) ptx::griddep_wait();
     if (threadIdx.x == 0 && tr != nullptr) {
         tr[blockIdx.x * CF_TRACE_SLOTS + 0] = t_start;
         trace_stamp(tr, 1);
@@ -712,7 +716,10 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
 __global__ void __launch_bounds__(256) b2b_ln_fold_kernel(const uint32_t *__restrict__ w2, const float *__restrict__ gamma,
                                                           const float *__restrict__ beta, float *c, float *part,
                                                           unsigned int *counter, int N1, int N2) {
-    ptx::griddep_wait();  // W2, gamma1, beta1 may come from the previous kernel; it has read c
+    // W2, gamma1, beta1 may come from the previous kernel, which may still read
+    // c; the stream kernel that follows may start (and read its own inputs)
+    // only once every block here has seen the previous grids complete
+    ptx::griddep_wait();
     ptx::griddep_launch_dependents();
     __shared__ float red[8][2][64];
     float(*const red2)[128] = reinterpret_cast<float(*)[128]>(&red[0][0][0]);  // the last block's [2][128]
