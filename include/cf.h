@@ -430,7 +430,10 @@ CF_API cf_status cf_gemm_fused_rowsoftmax_causal_ex(const void *X, const void *W
  *   b1 (device) fp32 [N1] or NULL           W2 (device) bf16 [N1, N2] row-major
  *   O  (device) bf16 [M, N2] row-major, written; must not alias an input
  *   workspace (device) >= cf_b2b_workspace_size() bytes, zeroed once by
- *        cf_workspace_init; holds the device error word
+ *        cf_workspace_init; holds the device error word (and, for
+ *        LayerNorm on the stream kernel, gamma1^T W2, beta1^T W2 and their
+ *        partial sums, written by a small kernel launched first on `stream`:
+ *        calls sharing a workspace must be ordered on one stream)
  * S is rounded to bf16 before MatMul_2 (the operand precision of the tensor
  * core), as the unfused chain rounds the tensor it stores between the GEMMs.
  * Supported: M >= 0 (0 is a no-op); K > 0 with K % 8 == 0 (a ragged last
