@@ -5,6 +5,10 @@ stream in which every call consumes its predecessor's output --
     Y1 = LayerNorm(X . W1 + b) (bf16)        fused GEMM + LayerNorm
     Y2 = softmax(Y1 . W2 / sqrt(N1)) (bf16)  fused GEMM + softmax
     O  = bf16(GELU(Y2 . W3)) . W4            back-to-back GEMM
+    O2 = bf16(LayerNorm(O . W5)) . W6        back-to-back GEMM, LayerNorm F
+                                             (stream kernel: a fold kernel,
+                                             then the GEMMs, which read O
+                                             before waiting on the fold)
 
 -- run with PDL off, with PDL on, and replayed from a captured CUDA graph
 (PDL edges inside the graph).  Every kernel waits on griddepcontrol before
@@ -30,14 +34,21 @@ def _setup():
     W2 = inputs.round_to_bf16(rng.standard_normal((N1, N2)).astype(np.float32) * N1 ** -0.5)
     W3 = inputs.round_to_bf16(rng.standard_normal((N2, NB1)).astype(np.float32) * 4.0)
     W4 = inputs.round_to_bf16(rng.standard_normal((NB1, NB2)).astype(np.float32) * NB1 ** -0.5)
+    W5 = inputs.round_to_bf16(rng.standard_normal((NB2, NB1)).astype(np.float32) * NB2 ** -0.5)
+    W6 = inputs.round_to_bf16(rng.standard_normal((NB1, NB2)).astype(np.float32) * NB1 ** -0.5)
+    g5 = (1.0 + 0.1 * rng.standard_normal(NB1)).astype(np.float32)
+    be5 = (0.1 * rng.standard_normal(NB1)).astype(np.float32)
     t = dict(X=dev_bf16(d["X"]), W1=dev_bf16(d["W"]), b=dev_f32(d["bias"]), g=dev_f32(d["gamma"]),
-             be=dev_f32(d["beta"]), W2=dev_bf16(W2), W3=dev_bf16(W3), W4=dev_bf16(W4))
+             be=dev_f32(d["beta"]), W2=dev_bf16(W2), W3=dev_bf16(W3), W4=dev_bf16(W4), W5=dev_bf16(W5),
+             W6=dev_bf16(W6), g5=dev_f32(g5), be5=dev_f32(be5))
     t["Y1"] = torch.empty((M, N1), dtype=torch.bfloat16, device="cuda")
     t["Y2"] = torch.empty((M, N2), dtype=torch.bfloat16, device="cuda")
     t["O"] = torch.empty((M, NB2), dtype=torch.bfloat16, device="cuda")
+    t["O2"] = torch.empty((M, NB2), dtype=torch.bfloat16, device="cuda")
     t["ws1"] = cf.new_workspace(cf.cf_gemm_fused_workspace_size(M, N1, K))
     t["ws2"] = cf.new_workspace(cf.cf_gemm_fused_workspace_size(M, N2, N1))
     t["ws3"] = cf.new_workspace(cf.cf_b2b_workspace_size())
+    t["ws4"] = cf.new_workspace(cf.cf_b2b_workspace_size())
     return torch, d, t
 
 
@@ -48,18 +59,20 @@ def _chain(t, tuning, stream=None):
                                          t["ws2"].numel(), stream, tuning), "stage 2")
     cf.check(cf.cf_b2b_gemm(t["Y2"], t["W3"], None, t["W4"], t["O"], M, N2, NB1, NB2, 1.0, cf.CF_B2B_GELU_TANH,
                             t["ws3"], t["ws3"].numel(), stream, tuning), "stage 3")
+    cf.check(cf.cf_b2b_gemm_layernorm(t["O"], t["W5"], None, t["g5"], t["be5"], t["W6"], t["O2"], M, NB2, NB1, NB2,
+                                      1.0, 1e-5, t["ws4"], t["ws4"].numel(), stream, tuning), "stage 4")
 
 
 def _outputs(torch, t):
     torch.cuda.synchronize()
-    for k in ("ws1", "ws2", "ws3"):
+    for k in ("ws1", "ws2", "ws3", "ws4"):
         st, info = cf.cf_get_device_status(t[k])
         assert st == cf.CF_OK, (k, cf.status_string(st), hex(info))
-    return [t[k].clone() for k in ("Y1", "Y2", "O")]
+    return [t[k].clone() for k in ("Y1", "Y2", "O", "O2")]
 
 
 def _clear(t):
-    for k in ("Y1", "Y2", "O"):
+    for k in ("Y1", "Y2", "O", "O2"):
         t[k].fill_(float("nan"))
 
 
@@ -74,7 +87,7 @@ def test_chain_same_bits_with_pdl_and_graph():
         _clear(t)
         _chain(t, None)
         got = _outputs(torch, t)
-        for a, b, name in zip(ref, got, ("Y1", "Y2", "O")):
+        for a, b, name in zip(ref, got, ("Y1", "Y2", "O", "O2")):
             assert torch.equal(a, b), f"PDL run {rep}: {name} differs"
     # the whole chain captured as one graph (PDL edges between its kernels)
     s = torch.cuda.Stream()
@@ -88,5 +101,5 @@ def test_chain_same_bits_with_pdl_and_graph():
         _clear(t)
         g.replay()
         got = _outputs(torch, t)
-        for a, b, name in zip(ref, got, ("Y1", "Y2", "O")):
+        for a, b, name in zip(ref, got, ("Y1", "Y2", "O", "O2")):
             assert torch.equal(a, b), f"graph replay {rep}: {name} differs"
