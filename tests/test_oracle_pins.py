@@ -113,3 +113,24 @@ def test_stitch_add_layernorm_pinned():
 
 def test_stitch_batchnorm_pinned():
     assert pins.check_stitch_batchnorm(oracle.stitch_batchnorm) == []
+
+
+def test_b2b_layernorm_fold_identity():
+    """The stream kernel's one-pass LayerNorm rests on LayerNorm being affine
+    in a row once its mean and rstd are fixed: for any shift mu0,
+    LN(z) . W2 = rstd ((z - mu0) gamma) . W2 - rstd (mu - mu0) gamma^T W2 + beta^T W2.
+    Checked in fp64 against the oracle's LayerNorm (before any bf16
+    rounding) with mu0 the mean of each row's first 256 columns, on rows whose
+    mean is far from 0 and whose first chunk is far from the row's mean."""
+    rng = np.random.Generator(np.random.PCG64(31))
+    M, N1, N2 = 8, 1024, 64
+    z = rng.standard_normal((M, N1)) + 30.0 + 5.0 * np.linspace(-1.0, 1.0, N1)
+    gamma = 1.0 + 0.1 * rng.standard_normal(N1)
+    beta = 0.1 * rng.standard_normal(N1)
+    W2 = rng.standard_normal((N1, N2))
+    direct = oracle.layernorm_rows(z, gamma, beta, 1e-5) @ W2
+    mu = z.mean(axis=1, keepdims=True)
+    rstd = 1.0 / np.sqrt(((z - mu) ** 2).mean(axis=1, keepdims=True) + 1e-5)
+    mu0 = z[:, :256].mean(axis=1, keepdims=True)
+    folded = rstd * (((z - mu0) * gamma) @ W2) - rstd * (mu - mu0) * (gamma @ W2) + beta @ W2
+    np.testing.assert_allclose(folded, direct, rtol=1e-10, atol=1e-9 * np.abs(direct).max())
