@@ -1,5 +1,6 @@
 // b2b_stream.cu -- back-to-back GEMM with one CTA per 128-row block:
-//     O = S . W2,   S = F(alpha * X.W1 + b1) in bf16,   F = row softmax or GELU
+//     O = S . W2,   S = F(alpha * X.W1 + b1) in bf16,
+//     F = row softmax, GELU or row LayerNorm (gamma1, beta1)
 // ([ComFuse] B2BGEMM, Eqs. 3-7, Fig. 5), with the N1 columns of the
 // intermediate streamed through tensor memory in 256-column chunks instead of
 // being partitioned over a cluster.
@@ -27,12 +28,20 @@
 //    leave O alone.
 //    The values rounded to bf16 are these unnormalised exponentials (at most
 //    256); the division by the row sum happens once, on the fp32 output.
+//    LayerNorm in one pass: the row's shift mu0 is the mean of its first
+//    chunk (the groups exchange their parts); each chunk feeds ML_2 with
+//    (z - mu0) gamma1 and folds its (mean, M2) into the group's running pair;
+//    the output is rstd O - rstd (mu - mu0) gamma1^T W2 + beta1^T W2, the two
+//    rows from b2b_ln_fold_kernel (launched first; waited for only before the
+//    first output stage).
 //  * ML_2(J): O += P . W2[chunk J, :] (K = 256), A read from tensor memory.
 //  * Issue order: ML_1(0), then ML_1(J+1), ML_2(J) for each J: the tensor
 //    core runs ML_1(J+1) and ML_2(J-1) under Epi_1(J).
-//  * End of a row block: O / l (GELU: O), group g writing output columns
-//    [32 g, 32 g + 32) through a 2 KB staging buffer per warp and 32 x 32 TMA
-//    stores.  No cluster, no exchange with other CTAs.
+//  * End of a row block: O / l (GELU: O; LayerNorm: as above), group g
+//    writing output columns [32 g, 32 g + 32) through a 2 KB staging buffer
+//    per warp and 32 x 32 TMA stores (where X streams and F keeps row
+//    statistics, directly from registers: that room is a fourth ring stage).
+//    No cluster, no exchange with other CTAs.
 //  * Every wait is bounded by %globaltimer; a timeout records
 //    CF_ERR_DEVICE_TIMEOUT in the workspace error word and the roles drain.
 #include <cuda.h>
@@ -222,7 +231,7 @@ __device__ __forceinline__ void stream_output(const CUtensorMap *tmap_o, uint16_
     if (stamp != nullptr && lane == 0) *stamp = ptx::globaltimer();
 }
 
-// OP: 0 softmax, 1 GELU; kN2: 64 or 128; kRes: X resident (K <= 128)
+// OP: 0 softmax, 1 GELU, 2 LayerNorm; kN2: 64 or 128; kRes: X resident (K <= 128)
 template <int OP, int kN2, bool kRes>
 __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_constant__ B2bArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];

@@ -195,7 +195,7 @@ struct B2bArgs {
 int b2b_smem_bytes(int stages, int cluster, int n2, int op);
 int b2b_max_active_clusters(int op, int cluster, int n2, int smem);
 cudaError_t launch_b2b(int op, const B2bArgs &a, int clusters, int stages, int smem, bool pdl, cudaStream_t stream);
-// one CTA per 128-row block, N1 streamed in 256-column chunks (softmax, GELU);
+// one CTA per 128-row block, N1 streamed in 256-column chunks (softmax, GELU, LayerNorm);
 // tmap_w1 box {64, 64, 4}, tmap_w2 box {64, 128, N2/64}
 int b2b_stream_stages(int op, int K);  // ring depth, fixed per epilogue and mode (X resident or streamed)
 int b2b_stream_smem_bytes(int op, int K);
