@@ -262,13 +262,14 @@ def test_b2b_selector_reads_back_s(op, mode, N1, N2):
         f"selector {op}: error {err.flat[worst]:.3e} > {bound.flat[worst]:.3e} (col {cols[worst % N2]})")
 
 
-def test_b2b_stream_timeout_is_reported():
+@pytest.mark.parametrize("op", ["softmax", "layernorm"])
+def test_b2b_stream_timeout_is_reported(op):
     """One more arrival at the P-ready barrier than can happen: the MMA warp's
     bounded wait runs out (or the producer's, blocked behind it, first), the
-    kernel records CF_ERR_DEVICE_TIMEOUT with the role and every role drains;
-    the context stays usable."""
+    kernel records CF_ERR_DEVICE_TIMEOUT with the role and every role drains
+    (LayerNorm: with its fold kernel before it); the context stays usable."""
     M, K, N1, N2 = 512, 128, 512, 128
-    d = _inputs(M, K, N1, N2, seed=43, op="softmax")
+    d = _inputs(M, K, N1, N2, seed=43, op=op)
     alpha = K ** -0.5
     torch = torch_cuda()
     X, W1, W2 = dev_bf16(d["X"]), dev_bf16(d["W1"]), dev_bf16(d["W2"])
@@ -276,15 +277,19 @@ def test_b2b_stream_timeout_is_reported():
     O = torch.zeros((M, N2), dtype=torch.bfloat16, device="cuda")
     ws = cf.new_workspace(cf.cf_b2b_workspace_size())
     t = _tuning("stream", N1, extra_arrivals=1, timeout_us=2000)
-    assert cf.cf_b2b_gemm(X, W1, b1, W2, O, M, K, N1, N2, alpha, cf.CF_B2B_SOFTMAX, ws, ws.numel(), None,
-                          t) == cf.CF_OK
+    if op == "layernorm":
+        st = cf.cf_b2b_gemm_layernorm(X, W1, b1, dev_f32(d["gamma1"]), dev_f32(d["beta1"]), W2, O, M, K, N1, N2,
+                                      alpha, 1e-5, ws, ws.numel(), None, t)
+    else:
+        st = cf.cf_b2b_gemm(X, W1, b1, W2, O, M, K, N1, N2, alpha, cf.CF_B2B_SOFTMAX, ws, ws.numel(), None, t)
+    assert st == cf.CF_OK
     dst, info = cf.cf_get_device_status(ws)
     assert dst == cf.CF_ERR_DEVICE_TIMEOUT
     info &= 0xFFFFFFFF  # (the binding returns the word signed)
     assert (info >> 24) in (0x91, 0x92, 0x93), hex(info)  # a wait of the stream kernel's roles
     assert cf.cf_get_device_status(ws)[0] == cf.CF_OK  # cleared by the read
-    o = _run(d, "softmax", alpha, tuning=_tuning("stream", N1))
-    check_b2b(o, _ref(d, "softmax", alpha), d, "softmax", alpha, "after a timeout", mode="stream")
+    o = _run(d, op, alpha, tuning=_tuning("stream", N1))
+    check_b2b(o, _ref(d, op, alpha), d, op, alpha, "after a timeout", mode="stream")
 
 
 def test_b2b_empty_and_unsupported():
