@@ -80,3 +80,31 @@ def test_trace_b2b(n_slice):
     assert (t0[:, cf.CF_TRB_ML1_DONE] >= t0[:, cf.CF_TRB_ML1_FIRST]).all()
     assert (t0[:, cf.CF_TRB_EPI1_START] >= t0[:, cf.CF_TRB_ML1_FIRST]).all()
     assert (t0[:, cf.CF_TRB_ML2_DONE] >= t0[:, cf.CF_TRB_ML2_START]).all()
+
+
+def test_trace_b2b_layernorm_stream():
+    """The stream kernel's LayerNorm path (its fold kernel launched first):
+    stamps in causal order and the traced result within the parity bound."""
+    torch = torch_cuda()
+    M, K, N1, N2 = 1024, 128, 1024, 128
+    d = inputs.b2b_inputs(M, K, N1, N2, 63, x_std=1.0, w1_std=K ** -0.5, w2_std=N1 ** -0.5, b1_std=0.2, ln=True)
+    st, plan = cf.cf_query_b2b_plan(M, K, N1, N2, cf.CF_B2B_LAYERNORM, cf.tuning(n_slice=128))
+    assert st == cf.CF_OK and plan.cluster_size == 1
+    ctas = plan.clusters
+    tr = _trace_buffer(torch, ctas)
+    X, W1, W2 = dev_bf16(d["X"]), dev_bf16(d["W1"]), dev_bf16(d["W2"])
+    O = torch.empty((M, N2), dtype=torch.bfloat16, device="cuda")
+    ws = cf.new_workspace(cf.cf_b2b_workspace_size())
+    cf.check(cf.cf_b2b_gemm_layernorm(X, W1, dev_f32(d["b1"]), dev_f32(d["gamma1"]), dev_f32(d["beta1"]), W2, O, M,
+                                      K, N1, N2, 1.0, 1e-5, ws, ws.numel(), None, cf.tuning(n_slice=128, trace=tr)))
+    torch.cuda.synchronize()
+    assert cf.cf_get_device_status(ws)[0] == cf.CF_OK
+    ref = oracle.b2b_gemm(d["X"], d["W1"], d["W2"], op="layernorm", b1=d["b1"], gamma1=d["gamma1"],
+                          beta1=d["beta1"], eps=1e-5)
+    o = host(O)
+    assert np.abs(o - ref).max() <= 4 * 2.0 ** -8 * (np.abs(ref).max() + 1e-3)
+    E = _check_cta_stamps(tr, ctas)
+    t0 = E[:, 0]
+    assert (t0[:, cf.CF_TRB_ML1_DONE] >= t0[:, cf.CF_TRB_ML1_FIRST]).all()
+    assert (t0[:, cf.CF_TRB_EPI1_START] >= t0[:, cf.CF_TRB_ML1_FIRST]).all()
+    assert (t0[:, cf.CF_TRB_ML2_DONE] >= t0[:, cf.CF_TRB_ML2_START]).all()
