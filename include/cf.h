@@ -421,9 +421,11 @@ CF_API cf_status cf_gemm_fused_rowsoftmax_causal_ex(const void *X, const void *W
  *    online (running row max, raised with O rescaled only when a chunk passes
  *    it by 2^8): the bf16 values fed to MatMul_2 are the exponentials against
  *    that running max, and the division by the row sum is applied to the
- *    fp32 O.  LayerNorm takes two passes over the chunks (MatMul_1 runs
- *    twice): the row (mean, M2) first, then the normalised values for
- *    MatMul_2.  Any N1 that is a multiple of 256.
+ *    fp32 O.  LayerNorm in one pass: MatMul_2 takes bf16((z - mu0) gamma1),
+ *    mu0 the mean of the row's first 256 columns, while the row (mean, M2)
+ *    accumulates; the output is rstd O - rstd (mean - mu0) gamma1^T W2 +
+ *    beta1^T W2, the two fp32 rows computed by a small kernel launched just
+ *    before on `stream`.  Any N1 that is a multiple of 256.
  *   op   CF_B2B_SOFTMAX: F = row softmax over all N1 columns;
  *        CF_B2B_GELU_TANH: F = GELU(tanh)
  *   X  (device) bf16 [M, K] row-major      W1 (device) bf16 [K, N1] row-major
@@ -475,7 +477,7 @@ CF_API cf_status cf_b2b_gemm_ex(const void *X, const void *W1, const float *b1, 
  * back-to-back GEMM with F = LayerNorm over each row's N1 intermediate
  * values (biased variance, eps inside the square root); the row (mean, M2)
  * is reduced across the cluster like the softmax statistics (stream kernel:
- * over the chunks of a first pass).  gamma1, beta1
+ * over the chunks, applied to the fp32 output as above).  gamma1, beta1
  * (device) fp32 [N1], required; everything else as for cf_b2b_gemm. */
 CF_API cf_status cf_b2b_gemm_layernorm(const void *X, const void *W1, const float *b1,
                                        const float *gamma1, const float *beta1, const void *W2,

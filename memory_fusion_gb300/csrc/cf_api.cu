@@ -872,7 +872,7 @@ static int b2b_active_cached(int device, int op, int cluster, int n2, int smem) 
 // B2B kernel choice: the cluster kernel (C = N1/256 CTAs per row block, the
 // intermediate's columns partitioned over the cluster, partial outputs
 // reduce-scattered) or the stream kernel (one CTA per row block, N1 streamed
-// in 256-column chunks; LayerNorm in two passes).  tuning->n_slice selects:
+// in 256-column chunks; LayerNorm in one pass).  tuning->n_slice selects:
 // 0 auto, 128 stream, 256 cluster (the plan reports the same values).
 static cf_status b2b_plan(int64_t M, int64_t K, int64_t N1, int64_t N2, int op, const cf_tuning *tuning,
                           const cf::DeviceInfo &dev, cf_plan *plan) {
