@@ -111,8 +111,6 @@ typedef struct cf_tuning {
                                two row blocks' CTAs into one tcgen05 MMA stream
                                (cta_group::2, M = 256; each CTA stages half of
                                the W tile).  0 = auto                           */
-    int32_t multicast_x;    /* GEMM, C_M = 1: multicast each X tile along the row
-                               group instead of loading it in every CTA        */
     int32_t disable_pdl;    /* 1 = launch without programmatic dependent
                                launch (by default the kernel's set-up overlaps
                                the previous kernel's tail on the same stream and

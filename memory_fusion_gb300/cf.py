@@ -40,7 +40,6 @@ class cf_tuning(ctypes.Structure):
         ("timeout_us", ctypes.c_uint32),
         ("extra_arrivals", ctypes.c_int32),
         ("cluster_m", ctypes.c_int32),
-        ("multicast_x", ctypes.c_int32),
         ("disable_pdl", ctypes.c_int32),
         ("trace", ctypes.c_void_p),
     ]

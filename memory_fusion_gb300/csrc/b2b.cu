@@ -23,9 +23,9 @@
 //    reduce-scatter: CTA r owns output columns [r N2/C, (r+1) N2/C); every
 //    CTA sends each owner its partial columns with 16-byte st.async, and the
 //    owner adds them in rank order (deterministic), rounds to bf16, stores.
-//  * Every CTA loads the whole X tile itself: multicasting it across the
-//    cluster couples the CTAs' operand rings (a slot is refilled only when
-//    all C MMAs released it), which measured slower than the L2 reads saved.
+//  * Every CTA loads the whole X tile itself from L2: sharing one copy
+//    across the cluster would couple the CTAs' operand rings (a slot is
+//    refilled only when all C MMAs released it).
 //  * Two epilogue groups (4 warps each, one row per thread) own 256 tensor-
 //    memory columns each and take alternate tiles, staggered by one stage
 //    (Eq. 7): while one group runs Epi_1 / Epi_2, the MMA warp runs the other

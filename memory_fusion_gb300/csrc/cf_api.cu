@@ -719,11 +719,7 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
 
     cf::GemmArgs a;
     std::memset(&a, 0, sizeof(a));
-    {
-        const bool mcx = t.multicast_x && plan.cluster_m == 1 && plan.cluster_size > 1;
-        if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, mcx ? 128 / plan.cluster_size : 128))
-            return CF_ERR_CUDA;
-    }
+    if (!make_tmap_bf16(&a.tmap_x, X, uint64_t(M), uint64_t(K), 64, 128)) return CF_ERR_CUDA;
     if (!make_tmap_w(&a.tmap_w, W, uint64_t(K), uint64_t(N), w_blocks(plan.n_slice, plan.cluster_m)))
         return CF_ERR_CUDA;
     if (!make_tmap_bf16(&a.tmap_y, Y, uint64_t(M), uint64_t(N), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return CF_ERR_CUDA;
@@ -757,7 +753,6 @@ static cf_status gemm_fused_common(int kind, const void *X, const void *W, const
     a.mask_offset = mask_offset;
     a.timeout_ns = 1000ull * (t.timeout_us ? t.timeout_us : kDefaultTimeoutUs);
     a.trace = reinterpret_cast<unsigned long long *>(t.trace);
-    a.multicast_x = (t.multicast_x && plan.cluster_m == 1 && plan.cluster_size > 1) ? 1 : 0;
     a.stg_bufs = plan.staging_buffers;
     cudaError_t e = cf::launch_gemm_fused(kind, a, plan.clusters, plan.stages, plan.smem_bytes, t.disable_pdl == 0,
                                           reinterpret_cast<cudaStream_t>(stream));

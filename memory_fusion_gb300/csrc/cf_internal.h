@@ -140,7 +140,6 @@ struct GemmArgs {
     int cluster;          // C_N: CTAs of one row group (along N)
     int cluster_m;        // C_M: row blocks per cluster; 2 = CTA pairs sharing one
                           // cta_group::2 MMA stream (M = 256, W split between the pair)
-    int multicast_x;      // single-CTA MMA: multicast each X tile along the row group
     int stg_bufs;         // output staging buffers per epilogue warp (1 or 2)
     int groups;           // G
     int leader;           // leader-follower aggregation in the row group

@@ -282,18 +282,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     const uint32_t rank = crank / uint32_t(CM);
     const uint32_t pair_leader = crank & ~1u;         // even CTA of the pair (issues the MMAs)
     const bool is_leader = !kPair || (crank & 1u) == 0u;
-    // optional X multicast along the row group (single-CTA MMA only)
-    const bool mcx = !kPair && a.multicast_x && C > 1;
-    uint16_t a_mask = uint16_t(1u << crank);
-    if (mcx) a_mask = uint16_t((1u << C) - 1u);
-    const int a_rows = mcx ? kBlockM / C : kBlockM;  // rows of the X tile this CTA loads
     const uint32_t tmem_cols = wide ? 512u : (ns * 2 <= 32) ? 32u : uint32_t(ns * 2);
     const unsigned long long t_start = ptx::globaltimer();  // traced after the dependency wait
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             ptx::mbar_init(B.full0 + 8 * s, 1);
-            ptx::mbar_init(B.empty0 + 8 * s, uint32_t(__popc(a_mask)));
+            ptx::mbar_init(B.empty0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(B.tmem_full0 + 8 * b, 1);
@@ -371,10 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         // my_boxes 64-column blocks in one 3-D copy
                         ptx::tma_load_3d_pair_hint(sb, &a.tmap_w, fbl, 0, kb * kBK, n0 / 64 + m_sub * my_boxes, pol_w);
                     } else {
-                        ptx::mbar_arrive_expect_tx(fb, tx);  // the whole stage, whoever loads it
-                        const uint32_t adst = sa + uint32_t(mcx ? rank : 0u) * uint32_t(a_rows) * 128u;
-                        if (mcx) ptx::tma_load_2d_mc(adst, &a.tmap_x, fb, kb * kBK, m0 + int(rank) * a_rows, a_mask);
-                        else ptx::tma_load_2d(adst, &a.tmap_x, fb, kb * kBK, m0);
+                        ptx::mbar_arrive_expect_tx(fb, tx);
+                        ptx::tma_load_2d(sa, &a.tmap_x, fb, kb * kBK, m0);
                         ptx::tma_load_3d_hint(sb, &a.tmap_w, fb, 0, kb * kBK, n0 / 64, pol_w);  // nbox blocks
                     }
                     if (kb == 0) trace_tile(a.trace, ptile, CF_TR_TMA_FIRST);
@@ -405,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             // a wide tile is two N = 256 MMAs per K step into adjacent TMEM columns
             const uint32_t idesc = idesc_bf16(kPair ? 2 * kBlockM : kBlockM, wide ? 256 : ns);
             const uint16_t pair_mask = uint16_t(3u << pair_leader);
-            const bool commit_mc = !kPair && a_mask != uint16_t(1u << crank);
             // Operand descriptors of ring stage 0.  A stage's own are these plus its
             // byte offset >> 4 in the address field (the ring ends below 256 KB, so
             // the 14-bit field never carries); within a stage, A advances 16 K
@@ -451,10 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                             if (wide) ptx::mma_bf16(d + 256u, ad, bd + uint64_t(32768 >> 4), idesc, accum);
                         }
                     }
-                    // the stage is free once these MMAs completed: tell every CTA whose
-                    // producer filled it
+                    // the stage is free once these MMAs completed (pair: in both CTAs)
                     if constexpr (kPair) ptx::mma_commit_pair_mc(B.empty0 + 8 * s, pair_mask);
-                    else if (commit_mc) ptx::mma_commit_mc(B.empty0 + 8 * s, a_mask);
                     else ptx::mma_commit(B.empty0 + 8 * s);
                     if (++s == uint32_t(stages)) {
                         s = 0;

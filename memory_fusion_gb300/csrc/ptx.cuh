@@ -282,18 +282,6 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap,
         : "memory");
 }
 
-// 2-D tiled TMA load multicast to every CTA of `mask` in the cluster: the box
-// lands at the same shared-memory offset in each, and complete_tx is signalled
-// on the mbarrier at the same offset in each
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-        : "memory");
-}
-
 // bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
 // shared::cluster address; completion is signalled (complete_tx) on the
 // mbarrier at shared::cluster address `remote_bar` in the destination CTA.
@@ -471,16 +459,6 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-// arrive (once) on the mbarrier at this offset in every CTA of `mask` when all
-// prior tcgen05 async ops of this thread have completed
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(mask)
-        : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }

@@ -103,7 +103,7 @@ def test_rownorm_global_path(C, N, leader):
 
 @pytest.mark.parametrize("C,CM,N,M,leader", [(1, 2, 1024, 390, 0), (2, 2, 1024, 390, 0), (4, 2, 2048, 300, 1),
                                                (8, 2, 2048, 260, 0), (2, 2, 4096, 384, 0), (1, 2, 256, 129, 0)])
-def test_rownorm_multicast_clusters(C, CM, N, M, leader):
+def test_rownorm_pair_clusters(C, CM, N, M, leader):
     """Clusters of two row blocks x C_N column slices run CTA pairs as one cta_group::2
     MMA stream (M = 256, each CTA stages half of W); an odd row-block count leaves a
     phantom block."""
@@ -139,26 +139,12 @@ def test_wide_tile_modes(C, leader, epi, M, K, max_clusters):
         check_ln(_rownorm(d, act=epi, tuning=t), _ref_ln(d, act=epi), f"wide {epi} C={C} leader={leader}")
 
 
-def test_wide_tile_x_multicast():
-    d = _ln_inputs(300, 2048, 128, seed=78)
-    t = cf.tuning(n_slice=512, cluster_size=4, multicast_x=1)
-    check_ln(_rownorm(d, act="gelu_tanh", tuning=t), _ref_ln(d, act="gelu_tanh"), "wide multicast_x")
-
-
-def test_rownorm_x_multicast_row_group():
-    """Single-CTA MMAs with each X tile multicast along the row group."""
-    d = _ln_inputs(300, 1024, 256, seed=77)
-    for C in (2, 4):
-        t = cf.tuning(cluster_size=C, cluster_m=1, multicast_x=1)
-        check_ln(_rownorm(d, tuning=t), _ref_ln(d), f"multicast_x C={C}")
-
-
-def test_softmax_multicast_cluster():
+def test_softmax_pair_clusters():
     d = inputs.gemm_inputs(300, 2048, 1024, seed=8, x_std=1.0, w_std=1024 ** -0.5,
                            bias_std=None, gamma_std=None, beta_std=None)
     ref = oracle.gemm_rowsoftmax(d["X"], d["W"], scale=0.05)
     for t in (cf.tuning(cluster_size=4, cluster_m=2), cf.tuning(cluster_size=8, cluster_m=2)):
-        check_softmax(_softmax(d, 0.05, tuning=t), ref, "softmax multicast", bf16_out=True)
+        check_softmax(_softmax(d, 0.05, tuning=t), ref, "softmax CTA pairs", bf16_out=True)
 
 
 def test_rownorm_alpha_and_no_bias():

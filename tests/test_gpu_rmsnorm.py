@@ -59,11 +59,11 @@ def test_rmsnorm_small(M, N, K, act, beta):
 
 @pytest.mark.parametrize("kw", [
     dict(n_slice=64), dict(n_slice=512), dict(cluster_size=16, peer_max=-1), dict(cluster_size=8, peer_max=16),
-    dict(n_slice=256, cluster_size=2), dict(cluster_size=2, cluster_m=2), dict(cluster_size=4, multicast_x=1),
+    dict(n_slice=256, cluster_size=2), dict(cluster_size=2, cluster_m=2), dict(cluster_size=4),
 ])
 def test_rmsnorm_schedules(kw):
     """Cluster sizes, leader/peer, global partials (n_slice 256 in clusters of 2 over
-    4096 columns: 8 groups), CTA pairs, wide tiles, X multicast."""
+    4096 columns: 8 groups), CTA pairs, wide tiles."""
     N = 4096
     d = _inputs(390, N, 128, seed=71, beta=False)
     t = cf.tuning(**kw)
