@@ -291,14 +291,28 @@ CF_API cf_status cf_gemm_fused_rownorm_ex(const void *X, const void *W, const fl
  *     counters (cudaMemsetAsync on `stream`) before its kernel.  Calls whose
  *     work can overlap on the GPU (different streams, or several host
  *     threads) race on the array and must be serialised by the caller.
- *   - Device-side errors are not reported by this call (the error word is
- *     cleared by the next call); bounded waits still end the kernel.
+ *   - Device-side errors (a bounded wait that ran out: the output is then
+ *     garbage) are recorded in the array's error word; read them with
+ *     cf_gemm_fused_rownorm_noalloc_status() before the next call, which
+ *     clears the word.
+ *   - The array's address is cached per device for the life of the process;
+ *     after cudaDeviceReset (or anything else that destroys and re-creates
+ *     the device's primary context) the cached address is stale, so do not
+ *     use this call in a process that resets a device it has used before.
  * Arguments, layouts, supported shapes and error codes are otherwise those
  * of cf_gemm_fused_rownorm with default tuning. */
 CF_API cf_status cf_gemm_fused_rownorm_noalloc(const void *X, const void *W, const float *bias,
                                                const float *gamma, const float *beta, void *Y,
                                                int64_t M, int64_t N, int64_t K, float alpha,
                                                float eps, cf_activation act, cf_stream_t stream);
+
+/* The device-side status of cf_gemm_fused_rownorm_noalloc calls on the
+ * current device: waits for `stream`, then reads and clears the error word
+ * of the library's fixed scratch array (no allocation).  Returns CF_OK or the
+ * first device-side error recorded since the last read (or since the last
+ * no-allocation call, which clears the word before its kernel); *info (may be
+ * NULL) as for cf_get_device_status.  No counterpart in the pages. */
+CF_API cf_status cf_gemm_fused_rownorm_noalloc_status(cf_stream_t stream, int32_t *info);
 
 /* ------------------------------------------------------------------------ */
 /* Fused GEMM + bias (+ GELU) + RMSNorm                                      */

@@ -110,6 +110,7 @@ _SIGS = {
                                        _P, _SZ, _P, ctypes.POINTER(cf_tuning)]),
     "cf_gemm_fused_rownorm_noalloc": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
                                             _P]),
+    "cf_gemm_fused_rownorm_noalloc_status": (_ST, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "cf_gemm_fused_rmsnorm": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
                                     _P, _SZ, _P]),
     "cf_gemm_fused_rmsnorm_ex": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
@@ -314,6 +315,14 @@ def cf_gemm_fused_rownorm_noalloc(X, W, bias, gamma, beta, Y, M, N, K, alpha, ep
     allocate device memory; its scratch is a fixed 4 MiB array inside libcf."""
     return lib().cf_gemm_fused_rownorm_noalloc(_ptr(X), _ptr(W), _ptr(bias), _ptr(gamma), _ptr(beta), _ptr(Y),
                                                M, N, K, alpha, eps, act, _stream(stream))
+
+
+def cf_gemm_fused_rownorm_noalloc_status(stream=None):
+    """(status, info) of the no-allocation calls on the current device: waits
+    for the stream, reads and clears the fixed scratch array's error word."""
+    info = ctypes.c_int32(0)
+    st = lib().cf_gemm_fused_rownorm_noalloc_status(_stream(stream), ctypes.byref(info))
+    return st, info.value
 
 
 def cf_gemm_fused_rowsoftmax(X, W, bias, Y, M, N, K, scale, workspace, workspace_bytes,

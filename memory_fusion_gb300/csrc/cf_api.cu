@@ -1137,6 +1137,16 @@ extern "C" cf_status cf_gemm_fused_rownorm_noalloc(const void *X, const void *W,
     return CF_OK;
 }
 
+extern "C" cf_status cf_gemm_fused_rownorm_noalloc_status(cf_stream_t stream, int32_t *info) {
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e);
+    void *scratch = nullptr;
+    cf_status st = noalloc_scratch(device, &scratch);
+    if (st != CF_OK) return st;
+    return cf_get_device_status(scratch, stream, info);
+}
+
 // =========================================================================
 // The unfused two-kernel composition (a measured baseline, not a fallback):
 // GEMM -> fp32 P in global memory -> row kernel.  Same results within the

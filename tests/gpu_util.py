@@ -87,3 +87,32 @@ def sample_rows(M, n, seed=0):
     rows = set(rng.choice(M, size=min(n, M), replace=False).tolist())
     rows.update([0, M - 1])
     return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_ln_all_rows(Y, ref_rows, what="", strict=False, chunk=2048):
+    """check_ln over every row of the device output Y [M, N], in row chunks
+    (the oracle is row-independent, so each chunk's reference is exact):
+    the max-abs bound per element, the mean-abs bound over all M*N elements.
+    ``ref_rows(rows)`` returns the oracle's rows ``rows``."""
+    M = Y.shape[0]
+    tot, n = 0.0, 0
+    worst = 0.0
+    for r0 in range(0, M, chunk):
+        rows = np.arange(r0, min(M, r0 + chunk), dtype=np.int64)
+        y = host(Y[r0:r0 + len(rows)])
+        ref = ref_rows(rows)
+        err = np.abs(y - ref)
+        assert np.all(np.isfinite(y)), f"{what}: non-finite output in rows {r0}.."
+        if strict:
+            assert np.abs(ref).max() < 8.0, f"{what}: |ref| reaches {np.abs(ref).max():.3f}"
+        bound = np.maximum(LN_MAX_ABS, bf16_half_ulp(ref) + (LN_MAX_ABS - 2.0 ** -6))
+        w = np.argmax(err - bound)
+        assert err.flat[w] <= bound.flat[w], (
+            f"{what}: error {err.flat[w]:.3e} at row {r0 + w // y.shape[1]} (|ref|={abs(ref.flat[w]):.3f})"
+            f" > {bound.flat[w]:.3e}")
+        worst = max(worst, float(err.max()))
+        tot += float(err.sum())
+        n += err.size
+    assert n == Y.shape[0] * Y.shape[1]
+    assert tot / n <= LN_MEAN_ABS, f"{what}: mean-abs {tot / n:.3e} > {LN_MEAN_ABS}"
+    return worst, tot / n

@@ -2,14 +2,14 @@
 ABI) against the fp64 oracle: LayerNorm, GELU+LayerNorm and softmax
 epilogues; ragged row tails; tile widths 64/128/256; cluster sizes 1..16;
 peer and leader-follower aggregation; the global partial-buffer path; the
-full workloads on sampled rows; determinism, invariants and the device
+full workloads on every row; determinism, invariants and the device
 timeout path (a bounded wait that runs out, reported without a fault)."""
 import numpy as np
 import pytest
 
 import oracle
 from memory_fusion_gb300 import cf, inputs
-from tests.gpu_util import check_ln, check_softmax, dev_bf16, dev_f32, host, sample_rows, torch_cuda
+from tests.gpu_util import check_ln, check_ln_all_rows, check_softmax, dev_bf16, dev_f32, host, torch_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -187,8 +187,8 @@ def test_softmax_small(M, N, K):
 @pytest.mark.parametrize("scale,n_slice", [(128 ** -0.5, 0), (1.0, 0), (4.0, 256)])
 def test_softmax_within_one_bf16_ulp(scale, n_slice):
     """Every output within one bf16 ulp of the exact value: the exponentials
-    (three of four on MUFU ex2, one on the FMA pipe) and the row sums are
-    fp32-accurate, so only the final rounding to bf16 remains.  Scale 4 gives
+    (MUFU ex2) and the row sums are fp32-accurate, so only the final rounding
+    to bf16 remains.  Scale 4 gives
     peaked rows whose largest entries carry the relative error."""
     M, N, K = 300, 2048, 128
     d = inputs.gemm_inputs(M, N, K, seed=61, x_std=1.0, w_std=K ** -0.5,
@@ -211,25 +211,31 @@ def test_softmax_with_bias_and_modes():
 
 
 # ---------------------------------------------------------------------------
-# the full workloads, sampled rows (every row is independent)
+# the full workloads, every row against the oracle
 # ---------------------------------------------------------------------------
 def test_softmax_full_workload():
     w = inputs.WORKLOADS["softmax_4096x2048x128"]
     d = inputs.workload_inputs(w.name)
     y = _softmax(d, w.scale)
-    rows = sample_rows(w.M, 512)
-    check_softmax(y[rows], oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale, rows=rows), w.name, bf16_out=True,
-                  strict=True)
-    assert np.abs(y.sum(1) - 1).max() <= 1e-2  # every row
+    check_softmax(y, oracle.gemm_rowsoftmax(d["X"], d["W"], scale=w.scale), w.name, bf16_out=True, strict=True)
 
 
 @pytest.mark.parametrize("name", ["gelu_ln_16384x4096x4096", "wide_ln_8192x16384x2048"])
 def test_rownorm_full_workload(name):
+    """All M rows (16384 x 4096 and 8192 x 16384), compared chunk by chunk."""
+    torch = torch_cuda()
     w = inputs.WORKLOADS[name]
     d = inputs.workload_inputs(name)
-    y = _rownorm(d, act=w.act, eps=w.eps)
-    rows = sample_rows(w.M, 512)
-    check_ln(y[rows], _ref_ln(d, act=w.act, eps=w.eps, rows=rows), name, strict=True)
+    Y = torch.full((w.M, w.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = cf.new_workspace(cf.cf_gemm_fused_workspace_size(w.M, w.N, w.K))
+    st = cf.cf_gemm_fused_rownorm(dev_bf16(d["X"]), dev_bf16(d["W"]), dev_f32(d["bias"]), dev_f32(d["gamma"]),
+                                  dev_f32(d["beta"]), Y, w.M, w.N, w.K, w.alpha, w.eps,
+                                  {"none": cf.CF_ACT_NONE, "gelu_tanh": cf.CF_ACT_GELU_TANH}[w.act],
+                                  ws, ws.numel(), None, None)
+    assert st == cf.CF_OK, cf.status_string(st)
+    torch.cuda.synchronize()
+    assert cf.cf_get_device_status(ws)[0] == cf.CF_OK
+    check_ln_all_rows(Y, lambda rows: _ref_ln(d, act=w.act, eps=w.eps, rows=rows), name, strict=True)
 
 
 # ---------------------------------------------------------------------------
