@@ -935,6 +935,8 @@ def run_reference_stitched(args, w):
             rows = np.sort(rng.choice(w.rows, size=n_rows, replace=False))
             if isinstance(w, inputs.StitchNormWorkload):
                 oracle.stitch_add_layernorm(d["A"], d["R"], d["gamma"], d["beta"], w.eps, rows=rows)
+            elif isinstance(w, inputs.StitchPowWorkload):
+                oracle.stitch_powadd_softmax(d["A"], d["w"], w.p, rows=rows)
             else:
                 oracle.stitch_rowreduce_broadcast(d["A"], d["row_bias"], rows=rows)
         sample = f"{n_rows} random whole rows of {w.name} per step (fp64 numpy oracle)"
@@ -946,6 +948,7 @@ def run_reference_stitched(args, w):
     t = time.perf_counter() - t0
     v = per_row * n_rows * args.steps / t / 1e9
     metric = (f"stitched {w.kind} HBM GB/s" if isinstance(w, inputs.StitchNormWorkload)
+              else "stitched power->broadcast->softmax HBM GB/s" if isinstance(w, inputs.StitchPowWorkload)
               else "stitched reduce->broadcast HBM GB/s")
     print(json.dumps({
         "impl": "reference", "metric": metric, "value": round(v, 4), "unit": "GB/s", "n_gpus": 1,
@@ -963,7 +966,7 @@ def run_reference(args):
     if rank != 0:
         return
     w = inputs.WORKLOADS[args.workload]
-    if isinstance(w, (inputs.StitchWorkload, inputs.StitchNormWorkload)):
+    if isinstance(w, (inputs.StitchWorkload, inputs.StitchNormWorkload, inputs.StitchPowWorkload)):
         run_reference_stitched(args, w)
         return
     import oracle

@@ -39,7 +39,9 @@ __all__ = [
     "StitchWorkload",
     "B2bWorkload",
     "StitchNormWorkload",
+    "StitchPowWorkload",
     "stitch_norm_inputs",
+    "powadd_inputs",
     "b2b_inputs",
     "WORKLOADS",
     "gemm_inputs",
@@ -136,6 +138,22 @@ class StitchNormWorkload:
 
 
 @dataclass(frozen=True)
+class StitchPowWorkload:
+    """out = softmax_row(A + w[col]^p): an expensive element-wise power of a
+    column vector broadcast to every row, then the row reduction."""
+    name: str
+    rows: int
+    cols: int
+    seed: int
+    p: float = 2.5
+    description: str = ""
+
+    @property
+    def unavoidable_bytes(self) -> int:
+        return 4 * self.rows * self.cols * 2 + 4 * self.cols
+
+
+@dataclass(frozen=True)
 class B2bWorkload:
     name: str
     op: str                # "softmax" | "gelu_tanh" | "layernorm"
@@ -227,6 +245,12 @@ WORKLOADS = {
     "bn_64x30000": StitchNormWorkload(
         "bn_64x30000", "batchnorm", 64, 30000, 13,
         description="stitched BatchNorm over 64 rows (Regional scheme: one block per column strip)"),
+    "powsm_750000x32": StitchPowWorkload(
+        "powsm_750000x32", 750000, 32, 16,
+        description="stitched y=A+w[col]^2.5 -> row softmax, very many tiny rows (power computed once per column)"),
+    "powsm_64x30000": StitchPowWorkload(
+        "powsm_64x30000", 64, 30000, 17,
+        description="stitched y=A+w[col]^2.5 -> row softmax, very few huge rows (power computed once per column)"),
     "stitch_750000x32": StitchWorkload(
         "stitch_750000x32", 750000, 32, 3,
         description="stitched y=A^3+b[row] -> row softmax, very many tiny rows"),
@@ -283,6 +307,14 @@ def b2b_inputs(M: int, K: int, N1: int, N2: int, seed: int, *, x_std: float = 1.
     return out
 
 
+def powadd_inputs(rows: int, cols: int, seed: int) -> dict:
+    """A[rows, cols] ~ N(0, 1) fp32 and w[cols] ~ U(0.5, 2) fp32 (positive bases)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    A = _normal(rng, (rows, cols), 1.0)
+    w = (rng.random(size=cols) * 1.5 + 0.5).astype(np.float32)
+    return {"A": A, "w": w}
+
+
 def stitch_norm_inputs(rows: int, cols: int, seed: int, *, with_R: bool = True) -> dict:
     """A ~ N(0, 2) [rows, cols], R ~ N(0, 1) (if with_R), gamma ~ N(1, 0.1),
     beta ~ N(0, 0.1) [cols]; all fp32."""
@@ -300,6 +332,8 @@ def workload_inputs(name: str) -> dict:
         return stitch_inputs(w.rows, w.cols, w.seed)
     if isinstance(w, StitchNormWorkload):
         return stitch_norm_inputs(w.rows, w.cols, w.seed, with_R=w.kind == "add_layernorm")
+    if isinstance(w, StitchPowWorkload):
+        return powadd_inputs(w.rows, w.cols, w.seed)
     if isinstance(w, B2bWorkload):
         return b2b_inputs(w.M, w.K, w.N1, w.N2, w.seed, x_std=w.x_std, w1_std=w.w1_std, w2_std=w.w2_std,
                           b1_std=w.b1_std, ln=w.op == "layernorm")

@@ -56,6 +56,10 @@ Readings taken where the pages are silent:
   * pow(A, 3) is the real cube with its sign (A*A*A).
   * Stitched add + LayerNorm: x = A + R (R optional), LayerNorm over each
     row as above, gamma/beta indexed by column.
+  * Stitched power -> broadcast -> add -> softmax: y = A + w[col]^p with w > 0
+    (the real power function w^p = exp(p ln w)), then the row softmax; the
+    power of each column is a one-to-many value (AStitch's power -> broadcast
+    -> add example, "What people did before").
   * Stitched BatchNorm (training-mode statistics): per column j the mean and
     the biased variance over all rows; y = (A - mean_j) / sqrt(var_j + eps)
     * gamma_j + beta_j.  The column statistic is a one-to-many dependency
@@ -87,6 +91,7 @@ __all__ = [
     "stitch_batchnorm",
     "gemm_rowsoftmax",
     "stitch_rowreduce_broadcast",
+    "stitch_powadd_softmax",
     "ROW_CHUNK",
 ]
 
@@ -408,6 +413,30 @@ def stitch_rowreduce_broadcast(A, row_bias, rows=None) -> np.ndarray:
     for idx in _row_chunks(M, rows):
         a = _f64(A[idx])
         y = a * a * a + _f64(b[idx])[:, None]
+        out[o:o + idx.size] = softmax_rows(y)
+        o += idx.size
+    return out
+
+
+def stitch_powadd_softmax(A, w, p: float, rows=None) -> np.ndarray:
+    """Stitched subgraph with both one-to-many dependencies (AStitch, "What
+    people did before": an expensive element-wise power feeding a broadcast
+    and an add; "Four stitching schemes": the reduction feeding consumers):
+
+    y = A + w[col] ** p   (w > 0: the real power w^p = exp(p ln w));
+    m = rowmax(y); s = rowsum(exp(y - m)); out = exp(y - m) / s.
+    """
+    A = np.asarray(A)
+    w = _f64(w)
+    if np.any(w <= 0):
+        raise ValueError("stitch_powadd_softmax: w must be positive")
+    pw = w ** float(p)
+    M, N = A.shape
+    out_rows = M if rows is None else len(rows)
+    out = np.empty((out_rows, N), dtype=np.float64)
+    o = 0
+    for idx in _row_chunks(M, rows):
+        y = _f64(A[idx]) + pw[None, :]
         out[o:o + idx.size] = softmax_rows(y)
         o += idx.size
     return out

@@ -566,3 +566,51 @@ def check_stitch(st) -> list:
         ref[i] = [v / s for v in e]
     _fail(fails, np.allclose(np.asarray(st(A, b)), ref, rtol=1e-13, atol=1e-16), "stitch brute force")
     return fails
+
+
+def check_stitch_powadd(fn) -> list:
+    """out = softmax_row(A + w[col]^p): closed forms, invariants, brute force."""
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(18))
+    A = rng.standard_normal((4, 9))
+    w = rng.random(9) * 1.5 + 0.5
+    # p = 0: every power is 1, a shift of every row: the plain row softmax
+    e = np.exp(A - A.max(axis=1, keepdims=True))
+    ref = e / e.sum(axis=1, keepdims=True)
+    _fail(fails, np.allclose(np.asarray(fn(A, w, 0.0)), ref, rtol=1e-13, atol=1e-300), "powadd p=0 is softmax(A)")
+    # w = 1: 1^p = 1 for any p
+    ones = np.ones(9)
+    _fail(fails, np.allclose(np.asarray(fn(A, ones, 2.7)), ref, rtol=1e-13, atol=1e-300), "powadd w=1")
+    # two-element row [a0, a1] with [w0, w1], p = 2: sigmoid of the difference
+    a0, a1, w0, w1 = 0.3, -0.2, 1.5, 0.5
+    y = np.asarray(fn(np.array([[a0, a1]]), np.array([w0, w1]), 2.0))[0]
+    d = (a1 + w1 * w1) - (a0 + w0 * w0)
+    p1 = 1 / (1 + math.exp(-d))
+    _fail(fails, abs(y[1] - p1) < 1e-15 and abs(y[0] - (1 - p1)) < 1e-15, "powadd two-element closed form")
+    # the power broadcasts along the rows (one value per column): A = 0 gives
+    # the softmax of w^p in every row
+    z = np.asarray(fn(np.zeros((3, 9)), w, 1.5))
+    pw = [float(x) ** 1.5 for x in w]
+    m = max(pw)
+    ez = [math.exp(v - m) for v in pw]
+    sz = math.fsum(ez)
+    _fail(fails, all(np.allclose(z[i], [v / sz for v in ez], rtol=1e-13) for i in range(3)),
+          "powadd column broadcast")
+    # brute force with Python floats (math.pow, math.fsum), non-integer p
+    B = rng.standard_normal((3, 6))
+    v = rng.random(6) + 0.25
+    p = 2.5
+    bf = np.zeros_like(B)
+    for i in range(3):
+        yv = [float(B[i, j]) + math.pow(float(v[j]), p) for j in range(6)]
+        mm = max(yv)
+        ev = [math.exp(t - mm) for t in yv]
+        ss = math.fsum(ev)
+        bf[i] = [t / ss for t in ev]
+    _fail(fails, np.allclose(np.asarray(fn(B, v, p)), bf, rtol=1e-13, atol=1e-16), "powadd brute force")
+    out = np.asarray(fn(B, v, p))
+    _fail(fails, np.all(np.abs(out.sum(axis=1) - 1) < 1e-12), "powadd row sums")
+    # rows= selects rows of the full result
+    rws = np.array([2, 0])
+    _fail(fails, np.array_equal(np.asarray(fn(B, v, p, rows=rws)), out[rws]), "powadd rows= sampling")
+    return fails

@@ -356,3 +356,38 @@ def test_batchnorm_mutant_caught(name):
 def test_stitch_mutant_caught(name):
     with np.errstate(over="ignore", invalid="ignore"):
         assert pins.check_stitch(STITCH_MUTANTS[name]), name
+
+
+def _powadd(A, w, p, rows=None, *, mistake):
+    A = np.asarray(A, float)
+    w = np.asarray(w, float)
+    if rows is not None:
+        A = A[np.asarray(rows)]
+    if mistake == "power per row":          # broadcast along the wrong axis
+        k = min(A.shape)
+        y = A.copy()
+        y[:k, :] += (w[:k] ** p)[:, None]
+    elif mistake == "power multiplies":     # A * w^p instead of A + w^p
+        y = A * (w ** p)[None, :]
+    elif mistake == "base times exponent":  # w * p instead of w^p
+        y = A + (w * p)[None, :]
+    elif mistake == "exponent reciprocal":  # w^(1/p)
+        y = A + (w ** (1.0 / p if p else 0.0))[None, :]
+    elif mistake == "softmax over columns":
+        y = A + (w ** p)[None, :]
+        e = np.exp(y - y.max(axis=0, keepdims=True))
+        return e / e.sum(axis=0, keepdims=True)
+    else:
+        raise ValueError(mistake)
+    return oracle.softmax_rows(y)
+
+
+POWADD_MUTANTS = {k: (lambda kk: (lambda A, w, p, rows=None: _powadd(A, w, p, rows, mistake=kk)))(k)
+                  for k in ("power per row", "power multiplies", "base times exponent", "exponent reciprocal",
+                            "softmax over columns")}
+
+
+@pytest.mark.parametrize("name", sorted(POWADD_MUTANTS))
+def test_powadd_mutant_caught(name):
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        assert pins.check_stitch_powadd(POWADD_MUTANTS[name]), name

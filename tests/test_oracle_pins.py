@@ -134,3 +134,12 @@ def test_b2b_layernorm_fold_identity():
     mu0 = z[:, :256].mean(axis=1, keepdims=True)
     folded = rstd * (((z - mu0) * gamma) @ W2) - rstd * (mu - mu0) * (gamma @ W2) + beta @ W2
     np.testing.assert_allclose(folded, direct, rtol=1e-10, atol=1e-9 * np.abs(direct).max())
+
+
+def test_stitch_powadd_pinned():
+    assert pins.check_stitch_powadd(oracle.stitch_powadd_softmax) == []
+
+
+def test_stitch_powadd_rejects_nonpositive_base():
+    with pytest.raises(ValueError):
+        oracle.stitch_powadd_softmax(np.zeros((1, 2)), np.array([1.0, 0.0]), 2.0)
