@@ -501,6 +501,9 @@ def per_workload(torch, cf, peaks, device, names):
         if isinstance(w, inputs.StitchNormWorkload):
             out[name] = stitch_norm_numbers(torch, cf, w, peaks, device, l2)
             continue
+        if isinstance(w, inputs.StitchPowWorkload):
+            out[name] = stitch_pow_numbers(torch, cf, w, peaks, device, l2)
+            continue
         nsets = max(1, min(32, math.ceil(3 * l2 / bytes_per_set(w))))
         r = FusedRunner(torch, cf, w, nsets, device=device)
         reps = max(nsets, 20 if w.flops > 1e11 else 400)
@@ -552,6 +555,29 @@ def unfused_time(torch, cf, runner, reps):
     t, n, _ = time_steps(torch, U(), reps, 3, lambda: None, graph_len=reps)
     del ws
     return t / n
+
+
+def stitch_pow_numbers(torch, cf, w, peaks, device, l2):
+    """The stitched power -> broadcast -> add -> softmax subgraph, timed alone."""
+    d = inputs.workload_inputs(w.name)
+    nsets = max(1, min(32, math.ceil(3 * l2 / w.unavoidable_bytes)))
+    A = [torch.from_numpy(d["A"]).to(device) for _ in range(nsets)]
+    wv = torch.from_numpy(d["w"]).to(device)
+    O = [torch.empty_like(A[0]) for _ in range(nsets)]
+    wsb = cf.cf_stitch_workspace_size(w.rows, w.cols)
+    ws = cf.new_workspace(wsb, device)
+
+    class R:
+        def launch(self, i, stream=None):
+            cf.check(cf.cf_stitch_powadd_softmax(A[i % nsets], wv, w.p, O[i % nsets], w.rows, w.cols, ws, wsb,
+                                                 stream))
+
+    reps = max(nsets, 200)
+    t, n, _ = time_steps(torch, R(), reps, 3, lambda: None, graph_len=reps)
+    t1 = t / n
+    gbs = w.unavoidable_bytes / t1 / 1e9
+    return {"us": round(t1 * 1e6, 2), "gbs": round(gbs, 1), "bound": "hbm",
+            "roofline_frac": round(gbs / peaks["hbm_gbs"], 3), "buffer_sets": nsets}
 
 
 def stitch_numbers(torch, cf, w, peaks, device, l2):
@@ -820,6 +846,22 @@ def run_stitch(args):
         runner = StitchNormRunner(torch, cf, w, nsets, seed_offset=rank, device=device)
         kernel = stitch_norm_kernel_name(cf, w)
         metric = f"stitched {w.kind} HBM GB/s"
+    elif isinstance(w, inputs.StitchPowWorkload):
+        d = inputs.powadd_inputs(w.rows, w.cols, mdist.seed_for(w.seed, rank))
+        A = [torch.from_numpy(d["A"]).to(device) for _ in range(nsets)]
+        wv = torch.from_numpy(d["w"]).to(device)
+        O = [torch.empty_like(A[0]) for _ in range(nsets)]
+        wsb = cf.cf_stitch_workspace_size(w.rows, w.cols)
+        ws = cf.new_workspace(wsb, device)
+
+        class RP:
+            def launch(self, i, stream=None):
+                cf.check(cf.cf_stitch_powadd_softmax(A[i % nsets], wv, w.p, O[i % nsets], w.rows, w.cols, ws, wsb,
+                                                     stream))
+
+        runner = RP()
+        kernel = "stitch_packed_kernel" if (w.cols + 3) // 4 <= 32 else "stitch_split_kernel"
+        metric = "stitched power->broadcast->softmax HBM GB/s"
     else:
         d = inputs.stitch_inputs(w.rows, w.cols, mdist.seed_for(w.seed, rank))
         A = [torch.from_numpy(d["A"]).to(device) for _ in range(nsets)]
@@ -1012,7 +1054,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    stitched = isinstance(inputs.WORKLOADS[args.workload], (inputs.StitchWorkload, inputs.StitchNormWorkload))
+    stitched = isinstance(inputs.WORKLOADS[args.workload],
+                          (inputs.StitchWorkload, inputs.StitchNormWorkload, inputs.StitchPowWorkload))
     if args.impl == "reference":
         run_reference(args)
     elif stitched:

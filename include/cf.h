@@ -532,6 +532,35 @@ CF_API cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *r
                                            void *workspace, size_t workspace_bytes,
                                            cf_stream_t stream, const cf_tuning *tuning);
 
+/* ------------------------------------------------------------------------ */
+/* Stitched power -> broadcast -> add -> row softmax                          */
+/* ------------------------------------------------------------------------ */
+/* out[i, j] = softmax_j(A[i, j] + w[j]^p): an expensive element-wise power of a
+ * column vector, broadcast to every row, added, then the row softmax.
+ *
+ * [AStitch] "What people did before" names power -> broadcast -> add as the
+ * pattern register-only fusion recomputes once per consumer element;
+ * "Four stitching schemes" gives it the Regional scheme: every CTA computes the
+ * powers of the columns it touches once, into shared memory, and every row it
+ * handles reads them there.  The row softmax and its thread mapping (packed
+ * rows up to 128 columns, cluster-split wider rows) are those of
+ * cf_stitch_rowreduce_broadcast.
+ *   A   (device) fp32 [rows, cols] row-major     w (device) fp32 [cols], > 0
+ *   p   exponent (host scalar); w^p is the real power 2^(p log2 w): a w <= 0
+ *       gives NaN or 0 in its column, as the power function has no real value
+ *       or zero there
+ *   out (device) fp32 [rows, cols]; must not alias A or w
+ * Pointers 4-byte aligned (16-byte aligned A/out with cols % 4 == 0 take the
+ * 128-bit path); cols <= 262144 (else CF_ERR_UNSUPPORTED); workspace and
+ * device-side errors as for cf_stitch_rowreduce_broadcast. */
+CF_API cf_status cf_stitch_powadd_softmax(const float *A, const float *w, float p, float *out, int64_t rows,
+                                          int64_t cols, void *workspace, size_t workspace_bytes,
+                                          cf_stream_t stream);
+
+CF_API cf_status cf_stitch_powadd_softmax_ex(const float *A, const float *w, float p, float *out, int64_t rows,
+                                             int64_t cols, void *workspace, size_t workspace_bytes,
+                                             cf_stream_t stream, const cf_tuning *tuning);
+
 /* out = LayerNorm(A + R) * gamma + beta over each row
  *
  * [AStitch] "Four stitching schemes": an elementwise producer (A + R), two

@@ -154,6 +154,8 @@ _SIGS = {
     "cf_stitch_rowreduce_broadcast": (_ST, [_P, _P, _P, _I64, _I64, _P, _SZ, _P]),
     "cf_stitch_rowreduce_broadcast_ex": (_ST, [_P, _P, _P, _I64, _I64, _P, _SZ, _P,
                                                ctypes.POINTER(cf_tuning)]),
+    "cf_stitch_powadd_softmax": (_ST, [_P, _P, _F, _P, _I64, _I64, _P, _SZ, _P]),
+    "cf_stitch_powadd_softmax_ex": (_ST, [_P, _P, _F, _P, _I64, _I64, _P, _SZ, _P, ctypes.POINTER(cf_tuning)]),
 }
 
 _lib = None
@@ -344,6 +346,15 @@ def cf_stitch_rowreduce_broadcast(A, row_bias, out, rows, cols, workspace, works
     return L.cf_stitch_rowreduce_broadcast_ex(_ptr(A), _ptr(row_bias), _ptr(out), rows, cols,
                                               _ptr(workspace), workspace_bytes, _stream(stream),
                                               _tun(tuning))
+
+
+def cf_stitch_powadd_softmax(A, w, p, out, rows, cols, workspace, workspace_bytes, stream=None, tuning=None) -> int:
+    L = lib()
+    if tuning is None:
+        return L.cf_stitch_powadd_softmax(_ptr(A), _ptr(w), p, _ptr(out), rows, cols, _ptr(workspace),
+                                          workspace_bytes, _stream(stream))
+    return L.cf_stitch_powadd_softmax_ex(_ptr(A), _ptr(w), p, _ptr(out), rows, cols, _ptr(workspace),
+                                         workspace_bytes, _stream(stream), _tun(tuning))
 
 
 def cf_unfused_workspace_size(M, N, K) -> int:
@@ -606,4 +617,16 @@ def stitch_rowreduce_broadcast(A, row_bias, *, out=None, workspace=None, stream=
                                                                A.device, stream)
     check(cf_stitch_rowreduce_broadcast(A, row_bias, O, rows, cols, ws, ws.numel(), stream, tuning),
           "cf_stitch_rowreduce_broadcast")
+    return O
+
+
+def stitch_powadd_softmax(A, w, p, *, out=None, workspace=None, stream=None, tuning=None):
+    """out = softmax_row(A + w[None, :] ** p) (w > 0); fp32 CUDA tensors."""
+    import torch
+    rows, cols = A.shape
+    O = out if out is not None else torch.empty_like(A)
+    ws = workspace if workspace is not None else new_workspace(cf_stitch_workspace_size(rows, cols),
+                                                               A.device, stream)
+    check(cf_stitch_powadd_softmax(A, w, float(p), O, rows, cols, ws, ws.numel(), stream, tuning),
+          "cf_stitch_powadd_softmax")
     return O

@@ -465,6 +465,38 @@ cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *row_bias
 }
 
 
+cf_status cf_stitch_powadd_softmax_ex(const float *A, const float *w, float p, float *out, int64_t rows,
+                                      int64_t cols, void *ws, size_t ws_bytes, cf_stream_t stream,
+                                      const cf_tuning *tuning) {
+    if (rows < 0 || cols < 0) return CF_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return CF_OK;
+    if (!A || !w || !out || !ws) return CF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(w)) & 3u)
+        return CF_ERR_MISALIGNED;
+    if (cols > 262144) return CF_ERR_UNSUPPORTED;
+    if (ws_bytes < cf_stitch_workspace_size(rows, cols)) return CF_ERR_WORKSPACE_TOO_SMALL;
+    cf_tuning tz;
+    cf_tuning_default(&tz);
+    const cf_tuning &t = tuning ? *tuning : tz;
+    cf::DeviceInfo dev;
+    if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
+
+    cf::StitchPlan pl;
+    pl.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out);
+    cf_status st = plan_row_mapping(rows, cols, t, dev, &pl, cf::stitch_packed_blocks_per_sm);
+    if (st != CF_OK) return st;
+    cudaError_t e = cf::launch_stitch(pl, A, nullptr, out, rows, cols, static_cast<uint32_t *>(ws),
+                                      reinterpret_cast<cudaStream_t>(stream), w, p);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CF_OK;
+}
+
+cf_status cf_stitch_powadd_softmax(const float *A, const float *w, float p, float *out, int64_t rows, int64_t cols,
+                                   void *ws, size_t ws_bytes, cf_stream_t stream) {
+    return cf_stitch_powadd_softmax_ex(A, w, p, out, rows, cols, ws, ws_bytes, stream, nullptr);
+}
+
 cf_status cf_stitch_rowreduce_broadcast(const float *A, const float *row_bias, float *out, int64_t rows,
                                         int64_t cols, void *ws, size_t ws_bytes, cf_stream_t stream) {
     return cf_stitch_rowreduce_broadcast_ex(A, row_bias, out, rows, cols, ws, ws_bytes, stream, nullptr);

@@ -43,8 +43,11 @@ struct StitchPlan {
     unsigned long long timeout_ns = 200000000ull;  // bound of every wait (split mapping)
 };
 
+// y = A^3 + bias[row] (w == null), or y = A + w[col]^pexp (w != null, w > 0),
+// then the row softmax
 cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias, float *out, int64_t rows,
-                          int64_t cols, uint32_t *err, cudaStream_t stream);
+                          int64_t cols, uint32_t *err, cudaStream_t stream, const float *w = nullptr,
+                          float pexp = 0.f);
 
 int stitch_packed_blocks_per_sm(int lpr, bool vec);
 

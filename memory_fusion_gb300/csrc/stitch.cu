@@ -7,7 +7,19 @@
 // Every element is read from HBM once with a 128-bit streaming load (the
 // value is single-use: [sass2mlir] "Load widening and cache policy"), kept in
 // registers through the whole subgraph (the exp is computed once and reused
-// for the output), and written once.  The reduction is the three-level
+// for the output), and written once.
+//
+// Two producer nodes feed the row softmax:
+//   kCube:   y = a^3 + b[row]      (the pages' 750000x32 / 64x30000 subgraph)
+//   kPowCol: y = a + w[col]^p      (an expensive element-wise power feeding a
+//            broadcast: [AStitch] "Four stitching schemes", Regional -- every
+//            CTA computes the powers of the columns it touches exactly once,
+//            into shared memory, before its row loop, and every row it handles
+//            reads them there: one power per column and CTA instead of one per
+//            element, as register-only fusion would recompute it.  Where a CTA
+//            handles a single row the producer and its consumers are one to
+//            one (kPowColLocal: the power is computed with the element's load,
+//            the Local scheme), as the pages' locality check would decide.)  The reduction is the three-level
 // scheme of [ComFuse] (three-level reduction, Fig. 4): warp butterfly, then
 // shared memory across warps, then -- when a row is split over the CTAs of a
 // thread-block cluster -- distributed shared memory, peer all-to-all for few
@@ -28,15 +40,44 @@ constexpr int kUnroll = 4;  // row slots per thread in flight (memory-level para
 
 __device__ __forceinline__ float cube_plus(float a, float b) { return a * a * a + b; }
 
+// kPowCol: the column powers in a shared-memory table, once per CTA (Regional:
+// the CTA's rows share them); kPowColLocal: computed with each element's load
+// (Local: a CTA of one row uses each power once, so a table would only add a
+// phase -- the split mapping with one row per cluster)
+enum StitchProd : int { kCube = 0, kPowCol = 1, kPowColLocal = 2 };
+
+// w^p for w > 0 as 2^(p log2 w) on the MUFU (lg2.approx, ex2.approx: relative
+// error about 2^-21 for |p log2 w| < 4, far inside the softmax tolerance)
+__device__ __forceinline__ float pow_pos(float w, float p) { return ptx::ex2_approx(p * ptx::lg2_approx(w)); }
+
+// the Regional producer: powers of columns [c_begin, c_end) into pw[0 ..),
+// each computed by exactly one thread of the CTA, visible to all after the
+// barrier.  A thread's loads of w are issued in batches of kB before any power
+// is computed, so a CTA's 7500 columns cost two memory latencies, not thirty.
+template <int kB>
+__device__ __forceinline__ void powers_to_smem(float *pw, const float *w, float p, int c_begin, int c_end) {
+    const int nt = int(blockDim.x);
+    for (int c0 = c_begin + int(threadIdx.x); c0 < c_end; c0 += kB * nt) {
+        float wv[kB];
+#pragma unroll
+        for (int k = 0; k < kB; ++k) wv[k] = (c0 + k * nt < c_end) ? __ldg(w + c0 + k * nt) : 1.f;
+#pragma unroll
+        for (int k = 0; k < kB; ++k)
+            if (c0 + k * nt < c_end) pw[c0 + k * nt - c_begin] = pow_pos(wv[k], p);
+    }
+    __syncthreads();
+}
+
 // --------------------------------------------------------------------------
 // Packed mapping: LPR lanes per row (horizontal packing), each lane one
 // 4-column group, 32/LPR rows per warp and kUnroll row slots per thread.
 // --------------------------------------------------------------------------
-template <int LPR, bool VEC>
+template <int LPR, bool VEC, int PROD>
 __global__ void __launch_bounds__(kThreads) stitch_packed_kernel(const float *__restrict__ A,
                                                                  const float *__restrict__ bias,
                                                                  float *__restrict__ out, int64_t rows,
-                                                                 int cols) {
+                                                                 int cols, const float *__restrict__ w, float pexp) {
+    __shared__ __align__(16) float pw[PROD == kPowCol ? 4 * 32 : 1];  // the columns' powers (cols <= 128)
     constexpr int RPW = 32 / LPR;
     const int lane = threadIdx.x & 31;
     const int sub = lane & (LPR - 1);
@@ -48,6 +89,14 @@ __global__ void __launch_bounds__(kThreads) stitch_packed_kernel(const float *__
     // programmatic dependent launch: nothing in global memory before the
     // previous grid on the stream has completed
     ptx::griddep_wait();
+    // kPowCol: this lane's four column powers, computed once per CTA in shared
+    // memory and read once into registers for every row of the loop
+    float pc[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (PROD == kPowCol) {
+        powers_to_smem<1>(pw, w, pexp, 0, cols);  // cols <= 128: one power per thread
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pc[j] = (c0 + j < cols) ? pw[c0 + j] : 0.f;
+    }
 
     for (int64_t base = warp * kRowsPerIter; base < rows; base += nwarps * kRowsPerIter) {
         float v[kUnroll][4];
@@ -67,7 +116,8 @@ __global__ void __launch_bounds__(kThreads) stitch_packed_kernel(const float *__
 #pragma unroll
                 for (int j = 0; j < 4; ++j) v[u][j] = (rv && c0 + j < cols) ? __ldcs(A + r * cols + c0 + j) : 0.f;
             }
-            bb[u] = rv ? __ldg(bias + r) : 0.f;
+            if constexpr (PROD == kCube) bb[u] = rv ? __ldg(bias + r) : 0.f;
+            else bb[u] = 0.f;
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -75,7 +125,8 @@ __global__ void __launch_bounds__(kThreads) stitch_packed_kernel(const float *__
             float m = neg_inf();
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                v[u][j] = cube_plus(v[u][j], bb[u]);
+                if constexpr (PROD == kCube) v[u][j] = cube_plus(v[u][j], bb[u]);
+                else v[u][j] += pc[j];
                 if (c0 + j < cols) m = fmaxf(m, v[u][j]);
             }
             m = warp_max<LPR>(m);
@@ -110,12 +161,14 @@ __global__ void __launch_bounds__(kThreads) stitch_packed_kernel(const float *__
 // owns 4-column groups [rank*gpc, rank*gpc + gpc); each thread holds up to V
 // groups in registers.
 // --------------------------------------------------------------------------
-template <int V, bool VEC>
+template <int V, bool VEC, int PROD>
 __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__restrict__ A,
                                                                 const float *__restrict__ bias,
                                                                 float *__restrict__ out, int64_t rows, int cols,
                                                                 int gpc, int leader, uint32_t *err,
-                                                                unsigned long long tmo) {
+                                                                unsigned long long tmo, const float *__restrict__ w,
+                                                                float pexp) {
+    extern __shared__ __align__(16) float pws[];  // kPowCol: powers of this CTA's 4 gpc columns
     __shared__ MaxSum red[kThreads / 32];
     __shared__ __align__(16) MaxSum slot[2][16];  // level-3 partials, by row parity
     __shared__ __align__(16) MaxSum res[2];       // leader's result, by row parity
@@ -147,7 +200,6 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
     // programmatic dependent launch: nothing in global memory before the
     // previous grid on the stream has completed
     ptx::griddep_wait();
-
     int it = 0;
     for (int64_t row = cid; row < rows; row += ncl, ++it) {
         const int par = it & 1;
@@ -155,9 +207,10 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
         const uint32_t xph = uint32_t(it >> 1) & 1u;
         const float *a = A + row * cols;
         float *o = out + row * cols;
-        const float bb = __ldg(bias + row);
+        const float bb = PROD == kCube ? __ldg(bias + row) : 0.f;
 
         float e[V][4];
+        float wl[PROD == kPowColLocal ? V : 1][4];  // kPowColLocal: the columns' bases, loaded with A
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int g = g0 + threadIdx.x + v * kThreads;
@@ -168,11 +221,25 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
                 e[v][1] = t.y;
                 e[v][2] = t.z;
                 e[v][3] = t.w;
+                if constexpr (PROD == kPowColLocal) {
+                    float4 b4 = make_float4(1.f, 1.f, 1.f, 1.f);
+                    if (g < g1) b4 = __ldg(reinterpret_cast<const float4 *>(w) + g);
+                    wl[v][0] = b4.x;
+                    wl[v][1] = b4.y;
+                    wl[v][2] = b4.z;
+                    wl[v][3] = b4.w;
+                }
             } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) e[v][j] = (g < g1 && 4 * g + j < cols) ? __ldcs(a + 4 * g + j) : 0.f;
+                for (int j = 0; j < 4; ++j) {
+                    e[v][j] = (g < g1 && 4 * g + j < cols) ? __ldcs(a + 4 * g + j) : 0.f;
+                    if constexpr (PROD == kPowColLocal) wl[v][j] = (g < g1 && 4 * g + j < cols) ? __ldg(w + 4 * g + j) : 1.f;
+                }
             }
         }
+        // kPowCol: the powers of this CTA's columns, once, into shared memory (the
+        // cluster's rows all reuse them), computed while the first row's loads fly
+        if (PROD == kPowCol && it == 0) powers_to_smem<16>(pws, w, pexp, 4 * g0, min(cols, 4 * g1));
         if (it == 0) ptx::cluster_wait_acquire();
         // thread-local aggregation: max, then sum of exp (exp kept for the output)
         float mt = neg_inf();
@@ -181,7 +248,9 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
             const int g = g0 + threadIdx.x + v * kThreads;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                e[v][j] = cube_plus(e[v][j], bb);
+                if constexpr (PROD == kCube) e[v][j] = cube_plus(e[v][j], bb);
+                else if constexpr (PROD == kPowColLocal) e[v][j] += pow_pos(wl[v][j], pexp);
+                else if (g < g1 && 4 * g + j < cols) e[v][j] += pws[4 * (g - g0) + j];
                 if (g < g1 && 4 * g + j < cols) mt = fmaxf(mt, e[v][j]);
             }
         }
@@ -261,34 +330,37 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
 }
 
 template <int LPR, bool VEC>
-void *packed_fn() {
-    return reinterpret_cast<void *>(&stitch_packed_kernel<LPR, VEC>);
+void *packed_fn(int prod) {
+    return prod == kPowCol ? reinterpret_cast<void *>(&stitch_packed_kernel<LPR, VEC, kPowCol>)
+                           : reinterpret_cast<void *>(&stitch_packed_kernel<LPR, VEC, kCube>);
 }
 
-void *packed_kernel(int lpr, bool vec) {
+void *packed_kernel(int lpr, bool vec, int prod = kCube) {
     switch (lpr) {
-        case 1: return vec ? packed_fn<1, true>() : packed_fn<1, false>();
-        case 2: return vec ? packed_fn<2, true>() : packed_fn<2, false>();
-        case 4: return vec ? packed_fn<4, true>() : packed_fn<4, false>();
-        case 8: return vec ? packed_fn<8, true>() : packed_fn<8, false>();
-        case 16: return vec ? packed_fn<16, true>() : packed_fn<16, false>();
-        case 32: return vec ? packed_fn<32, true>() : packed_fn<32, false>();
+        case 1: return vec ? packed_fn<1, true>(prod) : packed_fn<1, false>(prod);
+        case 2: return vec ? packed_fn<2, true>(prod) : packed_fn<2, false>(prod);
+        case 4: return vec ? packed_fn<4, true>(prod) : packed_fn<4, false>(prod);
+        case 8: return vec ? packed_fn<8, true>(prod) : packed_fn<8, false>(prod);
+        case 16: return vec ? packed_fn<16, true>(prod) : packed_fn<16, false>(prod);
+        case 32: return vec ? packed_fn<32, true>(prod) : packed_fn<32, false>(prod);
         default: return nullptr;
     }
 }
 
 template <int V, bool VEC>
-void *split_fn() {
-    return reinterpret_cast<void *>(&stitch_split_kernel<V, VEC>);
+void *split_fn(int prod) {
+    if (prod == kPowCol) return reinterpret_cast<void *>(&stitch_split_kernel<V, VEC, kPowCol>);
+    if (prod == kPowColLocal) return reinterpret_cast<void *>(&stitch_split_kernel<V, VEC, kPowColLocal>);
+    return reinterpret_cast<void *>(&stitch_split_kernel<V, VEC, kCube>);
 }
 
-void *split_kernel(int v, bool vec) {
+void *split_kernel(int v, bool vec, int prod) {
     switch (v) {
-        case 1: return vec ? split_fn<1, true>() : split_fn<1, false>();
-        case 2: return vec ? split_fn<2, true>() : split_fn<2, false>();
-        case 4: return vec ? split_fn<4, true>() : split_fn<4, false>();
-        case 8: return vec ? split_fn<8, true>() : split_fn<8, false>();
-        case 16: return vec ? split_fn<16, true>() : split_fn<16, false>();
+        case 1: return vec ? split_fn<1, true>(prod) : split_fn<1, false>(prod);
+        case 2: return vec ? split_fn<2, true>(prod) : split_fn<2, false>(prod);
+        case 4: return vec ? split_fn<4, true>(prod) : split_fn<4, false>(prod);
+        case 8: return vec ? split_fn<8, true>(prod) : split_fn<8, false>(prod);
+        case 16: return vec ? split_fn<16, true>(prod) : split_fn<16, false>(prod);
         default: return nullptr;
     }
 }
@@ -317,12 +389,14 @@ int stitch_packed_blocks_per_sm(int lpr, bool vec) {
 }
 
 cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias, float *out, int64_t rows,
-                          int64_t cols, uint32_t *err, cudaStream_t stream) {
+                          int64_t cols, uint32_t *err, cudaStream_t stream, const float *w, float pexp) {
+    const int prod = w != nullptr ? kPowCol : kCube;
     if (p.mapping == 1) {
-        void *fn = packed_kernel(p.lpr, p.vec);
+        void *fn = packed_kernel(p.lpr, p.vec, prod);
         if (!fn) return cudaErrorInvalidValue;
         int icols = int(cols);
-        void *args[] = {(void *)&A, (void *)&bias, (void *)&out, (void *)&rows, (void *)&icols};
+        void *args[] = {(void *)&A, (void *)&bias, (void *)&out, (void *)&rows, (void *)&icols, (void *)&w,
+                        (void *)&pexp};
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(p.grid);
         cfg.blockDim = dim3(kThreads);
@@ -336,30 +410,43 @@ cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias
         return cudaLaunchKernelExC(&cfg, fn, args);
     }
     if (p.mapping == 2) {
-        void *fn = split_kernel(p.per_thread, p.vec);
+        // one row per cluster: each power is used once per CTA (Local scheme);
+        // several: the CTA's rows share a shared-memory table (Regional)
+        const int sprod = (prod == kPowCol && int64_t(p.grid / p.cluster) >= rows) ? int(kPowColLocal) : prod;
+        void *fn = split_kernel(p.per_thread, p.vec, sprod);
         if (!fn) return cudaErrorInvalidValue;
-        if (p.cluster > 8) {
-            static bool done[64][5][2] = {};
+        const int ng = int((cols + 3) / 4);
+        int gpc = (ng + p.cluster - 1) / p.cluster;
+        // kPowCol: the CTA's column powers in dynamic shared memory
+        const int smem = sprod == kPowCol ? gpc * 16 : 0;
+        {
+            // attributes once per (device, variant): non-portable clusters, and the
+            // largest power table seen
+            static bool done[64][5][2][3] = {};
+            static int set_smem[64][5][2] = {};
             int dev = 0;
             cudaError_t e = cudaGetDevice(&dev);
             if (e != cudaSuccess) return e;
             int vi = 0;
             while ((1 << vi) < p.per_thread) ++vi;
             if (dev < 0 || dev >= 64 || vi > 4) return cudaErrorInvalidValue;
-            if (!done[dev][vi][p.vec ? 1 : 0]) {
+            if (p.cluster > 8 && !done[dev][vi][p.vec ? 1 : 0][sprod]) {
                 e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
                 if (e != cudaSuccess) return e;
-                done[dev][vi][p.vec ? 1 : 0] = true;
+                done[dev][vi][p.vec ? 1 : 0][sprod] = true;
+            }
+            if (smem > 48 * 1024 && smem > set_smem[dev][vi][p.vec ? 1 : 0]) {
+                e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                if (e != cudaSuccess) return e;
+                set_smem[dev][vi][p.vec ? 1 : 0] = smem;
             }
         }
-        const int ng = int((cols + 3) / 4);
-        int gpc = (ng + p.cluster - 1) / p.cluster;
         int icols = int(cols);
         int leader = p.leader;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(p.grid);
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = 0;
+        cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -372,7 +459,7 @@ cudaError_t launch_stitch(const StitchPlan &p, const float *A, const float *bias
         cfg.numAttrs = p.pdl ? 2 : 1;
         unsigned long long tmo = p.timeout_ns;
         void *args[] = {(void *)&A, (void *)&bias, (void *)&out, (void *)&rows, (void *)&icols, (void *)&gpc,
-                        (void *)&leader, (void *)&err, (void *)&tmo};
+                        (void *)&leader, (void *)&err, (void *)&tmo, (void *)&w, (void *)&pexp};
         return cudaLaunchKernelExC(&cfg, fn, args);
     }
     return cudaErrorInvalidValue;
