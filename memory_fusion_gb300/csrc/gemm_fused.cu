@@ -128,46 +128,54 @@ __device__ __forceinline__ Bars bars_at(uint32_t base, int stages) {
     return b;
 }
 
-// Softmax stage-1 nodes on one 32-column fragment: z = alpha*acc + bias;
-// online (max, sum exp) update; the fragment is replaced by exp(z - m) where m
+// Softmax stage-1 nodes on one 32-column fragment, in base-2 units:
+// t = acc * (alpha log2 e) + bias log2 e (p holds bias log2 e); online
+// (max, sum 2^(t - max)) update; the fragment is replaced by 2^(t - m) where m
 // is the running max after this fragment.  kMask: only the first `nvalid`
 // columns take part (the rest are -inf, exp 0); a thread with no kept column
 // so far keeps (m, s) = (-inf, 0).
 template <bool kMask>
-__device__ __forceinline__ void softmax_fragment(uint32_t (&v)[32], const float *p, float alpha, float &m,
+__device__ __forceinline__ void softmax_fragment(uint32_t (&v)[32], const float *p, float aL, float &m,
                                                  float &ssum, int nvalid = 32) {
-    float z[32];
-    float cm = neg_inf();
+    float t[32];
 #pragma unroll
     for (int j4 = 0; j4 < 8; ++j4) {
         const float4 b = *reinterpret_cast<const float4 *>(p + 4 * j4);
-        z[4 * j4 + 0] = fmaf(alpha, __uint_as_float(v[4 * j4 + 0]), b.x);
-        z[4 * j4 + 1] = fmaf(alpha, __uint_as_float(v[4 * j4 + 1]), b.y);
-        z[4 * j4 + 2] = fmaf(alpha, __uint_as_float(v[4 * j4 + 2]), b.z);
-        z[4 * j4 + 3] = fmaf(alpha, __uint_as_float(v[4 * j4 + 3]), b.w);
+        ptx::fma2(t[4 * j4 + 0], t[4 * j4 + 1], __uint_as_float(v[4 * j4 + 0]), __uint_as_float(v[4 * j4 + 1]), aL,
+                  aL, b.x, b.y);
+        ptx::fma2(t[4 * j4 + 2], t[4 * j4 + 3], __uint_as_float(v[4 * j4 + 2]), __uint_as_float(v[4 * j4 + 3]), aL,
+                  aL, b.z, b.w);
     }
     if constexpr (kMask) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            if (j >= nvalid) z[j] = neg_inf();
+            if (j >= nvalid) t[j] = neg_inf();
     }
+    // fragment max: a tree of three-input maxima (17 instructions for 32 values)
+    float c[11];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) cm = fmaxf(cm, z[j]);
+    for (int i = 0; i < 10; ++i) c[i] = ptx::max3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+    c[10] = fmaxf(t[30], t[31]);
+    const float cm = ptx::max3(ptx::max3(c[0], c[1], c[2]), ptx::max3(c[3], c[4], c[5]),
+                               ptx::max3(c[6], c[7], fmaxf(c[8], fmaxf(c[9], c[10]))));
     const float mn = fmaxf(m, cm);
     if (kMask && mn == neg_inf()) {  // nothing kept yet in this row slice
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0u;
         return;
     }
-    float s = ssum * ptx::ex2_approx((m - mn) * kLog2e);  // m = -inf on the first fragment: s stays 0
-    const float off = mn * kLog2e;
+    // exponentials and their sum two at a time (packed fp32 pairs, two partial sums)
+    float sa = ssum * ptx::ex2_approx(m - mn), sb = 0.f;  // m = -inf on the first fragment: stays 0
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float ex = ptx::ex2_approx(fmaf(z[j], kLog2e, -off));  // masked: exp(-inf) = 0
-        s += ex;
-        v[j] = __float_as_uint(ex);
+    for (int j = 0; j < 32; j += 2) {
+        float d0, d1;
+        ptx::add2(d0, d1, t[j], t[j + 1], -mn, -mn);
+        const float e0 = ptx::ex2_approx(d0), e1 = ptx::ex2_approx(d1);  // masked: 2^-inf = 0
+        ptx::add2(sa, sb, sa, sb, e0, e1);
+        v[j] = __float_as_uint(e0);
+        v[j + 1] = __float_as_uint(e1);
     }
-    ssum = s;
+    ssum = sa + sb;
     m = mn;
 }
 
@@ -284,6 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     const bool is_leader = !kPair || (crank & 1u) == 0u;
     const uint32_t tmem_cols = wide ? 512u : (ns * 2 <= 32) ? 32u : uint32_t(ns * 2);
     const unsigned long long t_start = ptx::globaltimer();  // traced after the dependency wait
+    // this thread arrived on the cluster barrier that ends the kernel (early: once no
+    // peer can touch this CTA's shared memory any more)
+    bool arrived = false;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -392,6 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             }
         }
         __syncwarp();
+        if constexpr (!kPair) {  // a single CTA's producer touches no peer's shared memory
+            ptx::cluster_arrive_relaxed();
+            arrived = true;
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && is_leader) {
@@ -465,6 +480,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             ptx::mbar_wait_bounded(B.mma_done, 0, tmo, &local_abort, nullptr, 0);
         }
         __syncwarp();
+        if constexpr (!kPair) {  // commits of a single CTA signal only its own barriers
+            ptx::cluster_arrive_relaxed();
+            arrived = true;
+        }
     } else {
         // ------------------------------------------------------------ epilogue
         // Two groups of 4 warps take alternate tiles (PingPong over the two TMEM
@@ -510,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
             // tile finished reading them before the group barrier that ended it.
             if constexpr (EPI != EPI_STORE_F32) {
                 for (int c = gt; c < ecols; c += kGroupThreads) {
-                    pb[c] = a.bias ? __ldg(a.bias + ncta + c) : 0.f;
+                    pb[c] = a.bias ? __ldg(a.bias + ncta + c) * (kSm ? kLog2e : 1.f) : 0.f;
                     if constexpr (!kSm) {
                         pg[c] = __ldg(a.gamma + ncta + c);
                         pe[c] = a.beta ? __ldg(a.beta + ncta + c) : 0.f;
@@ -597,16 +616,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         const int nv1 = kMask ? int(keep - 32 * (c + 1) < 0 ? 0 : keep - 32 * (c + 1) > 32 ? 32
                                                                                                   : keep - 32 * (c + 1))
                                               : 32;
-                        softmax_fragment<kMask>(v0, pb + c * 32, a.alpha, m, ssum, nv0);
+                        softmax_fragment<kMask>(v0, pb + c * 32, a.alpha * kLog2e, m, ssum, nv0);
                         mrun[c] = m;
                         ptx::tmem_st32(tacc + c * 32, v0);
-                        softmax_fragment<kMask>(v1, pb + (c + 1) * 32, a.alpha, m, ssum, nv1);
+                        softmax_fragment<kMask>(v1, pb + (c + 1) * 32, a.alpha * kLog2e, m, ssum, nv1);
                         mrun[c + 1] = m;
                         ptx::tmem_st32(tacc + (c + 1) * 32, v1);
                     }
                 }
                 ptx::tmem_st_wait();
-                part = make_float2(m, ssum);
+                part = make_float2(m * kLn2, ssum);  // natural units for the exchange
             } else {
                 MeanM2 acc{0.f, 0.f};
                 // residual R [M, N] bf16: this thread's row slice of the fragment pair,
@@ -695,6 +714,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                 stat = part;  // aborting: the values no longer matter
             }
             if (gt0) trace_tile(a.trace, tile, CF_TR_EPI_CLUSTER);
+            // After the group's last exchange no peer writes into this CTA's shared
+            // memory again (every partial and result aimed at it has landed), and
+            // every write of this thread into a peer has landed before that peer's
+            // own wait passed: arrive on the final cluster barrier now, so the CTA
+            // need not wait for its peers' stores at the end.  (Not after an abort,
+            // where a wait may have given up with a partial still in flight.)
+            if constexpr (!kPair) {
+                if (!arrived && t + tstep * int(ncl) >= T && __all_sync(0xffffffffu, *abort == 0u)) {
+                    ptx::cluster_arrive_relaxed();
+                    arrived = true;
+                }
+            }
 
             // ---------------- level 4: rows wider than a cluster (global partials).
             // Layout [row block][g][128 rows] float2: one cluster group's 128 partials
@@ -797,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                         if constexpr (kSm) {
                             // a fully masked row (sum 0) is all zeros
                             const float f =
-                                (kMask && !(stat.y > 0.f)) ? 0.f : ptx::ex2_approx((mrun[cc] - stat.x) * kLog2e) / stat.y;
+                                (kMask && !(stat.y > 0.f)) ? 0.f : ptx::ex2_approx(mrun[cc] - stat.x * kLog2e) / stat.y;
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
                                 w[j] = ptx::pack_bf16x2(__uint_as_float(v[2 * j]) * f, __uint_as_float(v[2 * j + 1]) * f);
@@ -873,7 +904,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
     __syncthreads();
     ptx::tc_fence_after();
     // no CTA leaves while a peer may still access its shared memory
-    ptx::cluster_sync();
+    if (!arrived) ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
     if (warp == 1) {
         if constexpr (kPair) ptx::tmem_dealloc_pair(tmem_base, tmem_cols);
         else ptx::tmem_dealloc(tmem_base, tmem_cols);

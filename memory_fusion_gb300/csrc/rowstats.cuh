@@ -24,6 +24,7 @@
 namespace cf {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
 
 // The GELU node (tanh form): 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))),
 // tanh by the tanh.approx.f32 instruction.
