@@ -410,9 +410,9 @@ static cf_status plan_row_mapping(int64_t rows, int64_t cols, const cf_tuning &t
         if (C <= 0) {
             const int c_min = (ng + 256 * 16 - 1) / (256 * 16);
             // about ctas_per_sm CTAs per SM for few rows (measured on the 64x30000
-            // shape: the softmax is fastest at 4 CTAs per row (one per SM), add +
-            // LayerNorm -- two inputs -- at 8 (two per SM); the cluster barriers
-            // grow with C)
+            // shape: the softmax and add + LayerNorm are fastest at 8 CTAs per row,
+            // two or more per SM, so an SM's loads are spread over several CTAs'
+            // exchanges; 16 lost to the cluster barriers)
             int c_par = 1;
             const int64_t want = int64_t(dev.sm_count) * ctas_per_sm;
             if (rows < want) c_par = next_pow2(int((want + rows - 1) / rows));
@@ -456,7 +456,7 @@ cf_status cf_stitch_rowreduce_broadcast_ex(const float *A, const float *row_bias
 
     cf::StitchPlan p;
     p.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out);
-    cf_status st = plan_row_mapping(rows, cols, t, dev, &p, cf::stitch_packed_blocks_per_sm);
+    cf_status st = plan_row_mapping(rows, cols, t, dev, &p, cf::stitch_packed_blocks_per_sm, 2);
     if (st != CF_OK) return st;
     cudaError_t e = cf::launch_stitch(p, A, row_bias, out, rows, cols, static_cast<uint32_t *>(ws),
                                       reinterpret_cast<cudaStream_t>(stream));
@@ -484,7 +484,7 @@ cf_status cf_stitch_powadd_softmax_ex(const float *A, const float *w, float p, f
 
     cf::StitchPlan pl;
     pl.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out);
-    cf_status st = plan_row_mapping(rows, cols, t, dev, &pl, cf::stitch_packed_blocks_per_sm);
+    cf_status st = plan_row_mapping(rows, cols, t, dev, &pl, cf::stitch_packed_blocks_per_sm, 2);
     if (st != CF_OK) return st;
     cudaError_t e = cf::launch_stitch(pl, A, nullptr, out, rows, cols, static_cast<uint32_t *>(ws),
                                       reinterpret_cast<cudaStream_t>(stream), w, p);

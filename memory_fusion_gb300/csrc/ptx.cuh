@@ -236,6 +236,11 @@ __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// bring the line holding p into this SM's L1 (no register result)
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // 2-D tiled TMA load: box at (x = inner coordinate, y = outer coordinate)
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y) {
     asm volatile(
@@ -516,6 +521,18 @@ __device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1, f
         "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
         "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
         : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// maximum of v over the 32 lanes of the warp in one instruction (sm_100+)
+__device__ __forceinline__ float warp_redux_max(float v) {
+    float d;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(d) : "f"(v));
+    return d;
 }
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;

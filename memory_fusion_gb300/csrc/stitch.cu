@@ -98,6 +98,9 @@ __global__ void __launch_bounds__(kThreads) stitch_packed_kernel(const float *__
         for (int j = 0; j < 4; ++j) pc[j] = (c0 + j < cols) ? pw[c0 + j] : 0.f;
     }
 
+    bool colok[4];  // this lane's four columns exist
+#pragma unroll
+    for (int j = 0; j < 4; ++j) colok[j] = c0 + j < cols;
     for (int64_t base = warp * kRowsPerIter; base < rows; base += nwarps * kRowsPerIter) {
         float v[kUnroll][4];
         float bb[kUnroll];
@@ -122,32 +125,47 @@ __global__ void __launch_bounds__(kThreads) stitch_packed_kernel(const float *__
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int64_t r = base + u * RPW + rsub;
-            float m = neg_inf();
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if constexpr (PROD == kCube) v[u][j] = cube_plus(v[u][j], bb[u]);
-                else v[u][j] += pc[j];
-                if (c0 + j < cols) m = fmaxf(m, v[u][j]);
+            // producer node on packed pairs; a column past the row end becomes
+            // -inf (the max ignores it, its exponential is 0)
+            if constexpr (PROD == kCube) {
+                float s0, s1, s2, s3;
+                ptx::mul2(s0, s1, v[u][0], v[u][1], v[u][0], v[u][1]);
+                ptx::mul2(s2, s3, v[u][2], v[u][3], v[u][2], v[u][3]);
+                ptx::fma2(v[u][0], v[u][1], s0, s1, v[u][0], v[u][1], bb[u], bb[u]);
+                ptx::fma2(v[u][2], v[u][3], s2, s3, v[u][2], v[u][3], bb[u], bb[u]);
+            } else {
+                ptx::add2(v[u][0], v[u][1], v[u][0], v[u][1], pc[0], pc[1]);
+                ptx::add2(v[u][2], v[u][3], v[u][2], v[u][3], pc[2], pc[3]);
             }
-            m = warp_max<LPR>(m);
-            float s = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float e = (c0 + j < cols) ? ptx::ex2_approx((v[u][j] - m) * kLog2e) : 0.f;
-                v[u][j] = e;
-                s += e;
+            for (int j = 0; j < 4; ++j) v[u][j] = colok[j] ? v[u][j] : neg_inf();
+            // every row has its column 0 in lane group position 0: m is finite
+            const float m = warp_max<LPR>(fmaxf(ptx::max3(v[u][0], v[u][1], v[u][2]), v[u][3]));
+            const float mL = m * kLog2e;
+            float sa, sb;
+            {
+                float d0, d1, d2, d3;
+                ptx::fma2(d0, d1, v[u][0], v[u][1], kLog2e, kLog2e, -mL, -mL);
+                ptx::fma2(d2, d3, v[u][2], v[u][3], kLog2e, kLog2e, -mL, -mL);
+                v[u][0] = ptx::ex2_approx(d0);
+                v[u][1] = ptx::ex2_approx(d1);
+                v[u][2] = ptx::ex2_approx(d2);
+                v[u][3] = ptx::ex2_approx(d3);
+                ptx::add2(sa, sb, v[u][0], v[u][1], v[u][2], v[u][3]);
             }
-            s = warp_sum<LPR>(s);
-            const float inv = 1.0f / s;
+            const float inv = __frcp_rn(warp_sum<LPR>(sa + sb));
             if (r < rows) {
                 if constexpr (VEC) {
-                    if (c0 < cols)
-                        __stcs(reinterpret_cast<float4 *>(out + r * cols + c0),
-                               make_float4(v[u][0] * inv, v[u][1] * inv, v[u][2] * inv, v[u][3] * inv));
+                    if (c0 < cols) {
+                        float4 y;
+                        ptx::mul2(y.x, y.y, v[u][0], v[u][1], inv, inv);
+                        ptx::mul2(y.z, y.w, v[u][2], v[u][3], inv, inv);
+                        __stcs(reinterpret_cast<float4 *>(out + r * cols + c0), y);
+                    }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        if (c0 + j < cols) __stcs(out + r * cols + c0 + j, v[u][j] * inv);
+                        if (colok[j]) __stcs(out + r * cols + c0 + j, v[u][j] * inv);
                 }
             }
         }
@@ -241,62 +259,87 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
         // cluster's rows all reuse them), computed while the first row's loads fly
         if (PROD == kPowCol && it == 0) powers_to_smem<16>(pws, w, pexp, 4 * g0, min(cols, 4 * g1));
         if (it == 0) ptx::cluster_wait_acquire();
-        // thread-local aggregation: max, then sum of exp (exp kept for the output)
+        // producer node; a column outside the row slice becomes -inf, so the max
+        // ignores it and its exponential is 0 without further tests
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int g = g0 + threadIdx.x + v * kThreads;
+            if constexpr (PROD == kCube) {  // a^3 + b on packed pairs
+                float s0, s1, s2, s3;
+                ptx::mul2(s0, s1, e[v][0], e[v][1], e[v][0], e[v][1]);
+                ptx::mul2(s2, s3, e[v][2], e[v][3], e[v][2], e[v][3]);
+                ptx::fma2(e[v][0], e[v][1], s0, s1, e[v][0], e[v][1], bb, bb);
+                ptx::fma2(e[v][2], e[v][3], s2, s3, e[v][2], e[v][3], bb, bb);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool ok = VEC ? g < g1 : (g < g1 && 4 * g + j < cols);
+                if constexpr (PROD == kPowColLocal) e[v][j] += pow_pos(wl[v][j], pexp);
+                else if constexpr (PROD == kPowCol) e[v][j] += ok ? pws[4 * (g - g0) + j] : 0.f;
+                e[v][j] = ok ? e[v][j] : neg_inf();
+            }
+        }
+        // thread-local aggregation: max (three-input), then the sum of the
+        // exponentials on packed pairs (kept for the output)
         float mt = neg_inf();
 #pragma unroll
-        for (int v = 0; v < V; ++v) {
-            const int g = g0 + threadIdx.x + v * kThreads;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if constexpr (PROD == kCube) e[v][j] = cube_plus(e[v][j], bb);
-                else if constexpr (PROD == kPowColLocal) e[v][j] += pow_pos(wl[v][j], pexp);
-                else if (g < g1 && 4 * g + j < cols) e[v][j] += pws[4 * (g - g0) + j];
-                if (g < g1 && 4 * g + j < cols) mt = fmaxf(mt, e[v][j]);
-            }
-        }
-        float st = 0.f;
+        for (int v = 0; v < V; ++v) mt = ptx::max3(ptx::max3(mt, e[v][0], e[v][1]), e[v][2], e[v][3]);
+        const float mL = mt == neg_inf() ? 0.f : mt * kLog2e;  // no column: every exponent is -inf
+        float sa = 0.f, sb = 0.f;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
-            const int g = g0 + threadIdx.x + v * kThreads;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const bool ok = g < g1 && 4 * g + j < cols;
-                const float x = ok ? ptx::ex2_approx((e[v][j] - mt) * kLog2e) : 0.f;
-                e[v][j] = x;
-                st += x;
+            for (int j = 0; j < 4; j += 2) {
+                float d0, d1;
+                ptx::fma2(d0, d1, e[v][j], e[v][j + 1], kLog2e, kLog2e, -mL, -mL);
+                e[v][j] = ptx::ex2_approx(d0);  // 2^-inf = 0
+                e[v][j + 1] = ptx::ex2_approx(d1);
+                ptx::add2(sa, sb, sa, sb, e[v][j], e[v][j + 1]);
             }
         }
-        // level 1: warp butterfly
-        MaxSum p = warp_maxsum<32>(MaxSum{mt, st});
-        // level 2: across the CTA's warps through shared memory
-        if (lane == 0) red[warp] = p;
+        const float st = sa + sb;
+        // level 1 (warp): the max in one redux, each lane's sum rescaled to it,
+        // then a butterfly of plain sums (no exponential on the shuffle chain)
+        const float mw = ptx::warp_redux_max(mt);
+        const float sw = warp_sum<32>(mt == neg_inf() ? 0.f : st * ptx::ex2_approx((mt - mw) * kLog2e));
+        // level 2: across the CTA's warps through shared memory, the same way (a
+        // full-warp sum, so every lane that sends below holds the CTA's total)
+        if (lane == 0) red[warp] = MaxSum{mw, sw};
         __syncthreads();
         if (warp == 0) {
-            MaxSum q = (lane < kThreads / 32) ? red[lane] : MaxSum{neg_inf(), 0.f};
-            q = warp_maxsum<kThreads / 32>(q);
-            if (lane == 0 && !*abort) {
+            const MaxSum q = (lane < kThreads / 32) ? red[lane] : MaxSum{neg_inf(), 0.f};
+            const float mc = ptx::warp_redux_max(q.m);
+            const float sc = warp_sum<32>(q.m == neg_inf() ? 0.f : q.s * ptx::ex2_approx((q.m - mc) * kLog2e));
+            if (!*abort) {
                 // level 3: an 8-byte st.async of this CTA's (max, sum) into the
-                // gathering CTAs' shared memory, completing on their barrier
+                // gathering CTAs' shared memory, completing on their barrier; lane r
+                // sends to CTA r, so the remote stores are in flight together
                 const uint32_t my_slot = ptx::smem_u32(&slot[par][rank]);
                 if (!leader) {
-                    ptx::mbar_arrive_expect_tx(xb, C * 8u);
-                    for (uint32_t r = 0; r < C; ++r)
-                        ptx::st_async_f2(ptx::mapa(my_slot, r), q.m, q.s, ptx::mapa(xb, r));
-                } else {
+                    if (lane == 0) ptx::mbar_arrive_expect_tx(xb, C * 8u);
+                    if (uint32_t(lane) < C)
+                        ptx::st_async_f2(ptx::mapa(my_slot, uint32_t(lane)), mc, sc, ptx::mapa(xb, uint32_t(lane)));
+                } else if (lane == 0) {
                     ptx::mbar_arrive_expect_tx(xb, rank == 0 ? C * 8u : 8u);
-                    ptx::st_async_f2(ptx::mapa(my_slot, 0), q.m, q.s, ptx::mapa(xb, 0));
+                    ptx::st_async_f2(ptx::mapa(my_slot, 0), mc, sc, ptx::mapa(xb, 0));
                 }
             }
         }
+        // the row's statistics from the C partials, max first and then the
+        // rescaled sums, in rank order (every CTA folds them identically)
         MaxSum tot;
         if (!leader || rank == 0) {
             ptx::mbar_wait_bounded<true>(xb, xph, tmo, abort, err, 0x70000000u | uint32_t(par));
-            tot = slot[par][0];
-            for (uint32_t r = 1; r < C; ++r) tot = combine_maxsum(tot, slot[par][r]);
-            if (leader && threadIdx.x == 0 && !*abort) {
-                // the leader sends the row statistics back to each follower
+            float m = slot[par][0].m;
+            for (uint32_t r = 1; r < C; ++r) m = fmaxf(m, slot[par][r].m);
+            float sum = 0.f;
+            for (uint32_t r = 0; r < C; ++r)
+                sum += slot[par][r].m == neg_inf() ? 0.f : slot[par][r].s * ptx::ex2_approx((slot[par][r].m - m) * kLog2e);
+            tot = MaxSum{m, sum};
+            if (leader && warp == 0 && !*abort && lane >= 1 && uint32_t(lane) < C) {
+                // the leader sends the row statistics back to the followers (lane r to CTA r)
                 const uint32_t res_addr = ptx::smem_u32(&res[par]);
-                for (uint32_t r = 1; r < C; ++r) ptx::st_async_f2(ptx::mapa(res_addr, r), tot.m, tot.s, ptx::mapa(xb, r));
+                ptx::st_async_f2(ptx::mapa(res_addr, uint32_t(lane)), tot.m, tot.s, ptx::mapa(xb, uint32_t(lane)));
             }
         } else {
             ptx::mbar_wait_bounded<true>(xb, xph, tmo, abort, err, 0x70000010u | uint32_t(par));
@@ -308,9 +351,12 @@ __global__ void __launch_bounds__(kThreads) stitch_split_kernel(const float *__r
         for (int v = 0; v < V; ++v) {
             const int g = g0 + threadIdx.x + v * kThreads;
             if constexpr (VEC) {
-                if (g < g1)
-                    __stcs(reinterpret_cast<float4 *>(o) + g,
-                           make_float4(e[v][0] * f, e[v][1] * f, e[v][2] * f, e[v][3] * f));
+                if (g < g1) {
+                    float4 y;
+                    ptx::mul2(y.x, y.y, e[v][0], e[v][1], f, f);
+                    ptx::mul2(y.z, y.w, e[v][2], e[v][3], f, f);
+                    __stcs(reinterpret_cast<float4 *>(o) + g, y);
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)

@@ -164,8 +164,8 @@ __global__ void __launch_bounds__(kThreads) addln_split_kernel(const float *__re
                                                                float *__restrict__ out, int64_t rows, int cols,
                                                                float eps, int gpc, uint32_t *err,
                                                                unsigned long long tmo) {
-    __shared__ MeanM2 red[kThreads / 32];
-    __shared__ float redn[kThreads / 32];
+    __shared__ float reds[kThreads / 32];         // the warps' sums
+    __shared__ float redq[kThreads / 32];         // the warps' squared deviations
     __shared__ __align__(16) MeanM2 slot[2][16];  // per-CTA partials, by row parity
     __shared__ __align__(8) uint64_t xbar[2];
     __shared__ uint32_t abort_flag;
@@ -179,6 +179,12 @@ __global__ void __launch_bounds__(kThreads) addln_split_kernel(const float *__re
     const int ng = (cols + 3) >> 2;
     const int g0 = int(rank) * gpc;
     const int g1 = min(ng, g0 + gpc);
+    // columns of CTA r's slice (the same for every row)
+    auto slice_count = [&](int r) {
+        const int ga = r * gpc, gb = min(ng, ga + gpc);
+        return gb > ga ? float(min(cols, 4 * gb) - 4 * ga) : 0.f;
+    };
+    const float ncta = slice_count(int(rank));
     volatile uint32_t *abort = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -199,64 +205,83 @@ __global__ void __launch_bounds__(kThreads) addln_split_kernel(const float *__re
         const float *a = A + row * cols;
         const float *rr = R != nullptr ? R + row * cols : nullptr;
         float4 x[V];
-        float nt = 0.f, st = 0.f;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int g = g0 + threadIdx.x + v * kThreads;
             const bool ok = g < g1;
             x[v] = load_group<VEC>(a, g, cols, ok);
             if (rr != nullptr) x[v] = add4(x[v], load_group<VEC>(rr, g, cols, ok));
-            if (ok) nt += nvalid4(4 * g, cols);
-            st += (x[v].x + x[v].y) + (x[v].z + x[v].w);
         }
-        if (it == 0) ptx::cluster_wait_acquire();
-        // thread-local (mean, M2), two passes over the registers
-        const float mt = nt > 0.f ? st / nt : 0.f;
-        float qt = 0.f;
+        if (it == 0) {
+            // gamma and beta of this CTA's columns (the same for every row) into L1
+            // under the first row's loads, so the output pass after the exchange
+            // does not wait on L2 for them
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const int g = g0 + threadIdx.x + v * kThreads;
+                if (g < g1) {
+                    ptx::prefetch_l1(gamma + 4 * g);
+                    ptx::prefetch_l1(beta + 4 * g);
+                }
+            }
+            ptx::cluster_wait_acquire();
+        }
+        // the CTA's mean (levels 1 and 2 on plain sums: missing columns hold 0)
+        float st = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) st += (x[v].x + x[v].y) + (x[v].z + x[v].w);
+        st = warp_sum<32>(st);
+        if (lane == 0) reds[warp] = st;
+        __syncthreads();
+        float scta = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) scta += reds[w];
+        const float mc = ncta > 0.f ? scta / ncta : 0.f;
+        // the squared deviations from it, over this thread's existing columns
+        float qa = 0.f, qb = 0.f;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int g = g0 + threadIdx.x + v * kThreads;
             if (g < g1) {
-                const int c = 4 * g;
-                const float e[4] = {x[v].x - mt, x[v].y - mt, x[v].z - mt, x[v].w - mt};
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (c + j < cols) qt = fmaf(e[j], e[j], qt);
+                float d0, d1, d2, d3;
+                ptx::add2(d0, d1, x[v].x, x[v].y, -mc, -mc);
+                ptx::add2(d2, d3, x[v].z, x[v].w, -mc, -mc);
+                if constexpr (!VEC) {  // a row's last group may be partial
+                    const int c = 4 * g;
+                    d1 = c + 1 < cols ? d1 : 0.f;
+                    d2 = c + 2 < cols ? d2 : 0.f;
+                    d3 = c + 3 < cols ? d3 : 0.f;
+                }
+                ptx::fma2(qa, qb, d0, d1, d0, d1, qa, qb);
+                ptx::fma2(qa, qb, d2, d3, d2, d3, qa, qb);
             }
         }
-        // level 1: warp butterfly; level 2: the CTA's warps through shared memory
-        MeanM2 p{mt, qt};
-        float np = nt;
-        warp_meanm2<32>(p, np);
-        if (lane == 0) {
-            red[warp] = p;
-            redn[warp] = np;
-        }
+        const float qt = warp_sum<32>(qa + qb);
+        if (lane == 0) redq[warp] = qt;
         __syncthreads();
         if (warp == 0) {
-            MeanM2 q = lane < kThreads / 32 ? red[lane] : MeanM2{0.f, 0.f};
-            float nq = lane < kThreads / 32 ? redn[lane] : 0.f;
-            warp_meanm2<kThreads / 32>(q, nq);
-            if (lane == 0 && !*abort) {
-                // level 3: this CTA's (mean, M2) into every CTA's slot
+            const float qc = warp_sum<32>(lane < kThreads / 32 ? redq[lane] : 0.f);
+            if (!*abort) {
+                // level 3: this CTA's (mean, M2) into every CTA's slot, lane r to CTA r
                 const uint32_t my_slot = ptx::smem_u32(&slot[par][rank]);
-                ptx::mbar_arrive_expect_tx(xb, C * 8u);
-                for (uint32_t r = 0; r < C; ++r)
-                    ptx::st_async_f2(ptx::mapa(my_slot, r), q.mean, q.m2, ptx::mapa(xb, r));
+                if (lane == 0) ptx::mbar_arrive_expect_tx(xb, C * 8u);
+                if (uint32_t(lane) < C)
+                    ptx::st_async_f2(ptx::mapa(my_slot, uint32_t(lane)), mc, qc, ptx::mapa(xb, uint32_t(lane)));
             }
         }
         ptx::mbar_wait_bounded<true>(xb, xph, tmo, abort, err, 0x71000000u | uint32_t(par));
-        // fold the C partials in rank order; CTA r's count is known from its slice
-        MeanM2 tot = slot[par][0];
-        float ntot = float(min(cols, 4 * min(ng, gpc)));
-        for (uint32_t r = 1; r < C; ++r) {
-            const int ga = int(r) * gpc, gb = min(ng, ga + gpc);
-            const float nr = gb > ga ? float(min(cols, 4 * gb) - 4 * ga) : 0.f;
-            tot = combine_counts_safe(tot, ntot, slot[par][r], nr);
-            ntot += nr;
+        // the row's statistics from the C partials (counts known from the
+        // slices), in rank order: mean = sum(n_r mean_r) / N, then
+        // M2 = sum(M2_r + n_r (mean_r - mean)^2)
+        float sm = 0.f;
+        for (uint32_t r = 0; r < C; ++r) sm = fmaf(slice_count(int(r)), slot[par][r].mean, sm);
+        const float mean = sm / float(cols);
+        float m2 = 0.f;
+        for (uint32_t r = 0; r < C; ++r) {
+            const float d = slot[par][r].mean - mean;
+            m2 += fmaf(slice_count(int(r)) * d, d, slot[par][r].m2);
         }
-        const float mean = tot.mean;
-        const float rstd = rsqrtf(fmaf(tot.m2, 1.0f / float(cols), eps));
+        const float rstd = rsqrtf(fmaf(m2, 1.0f / float(cols), eps));
         float *o = out + row * cols;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
@@ -271,8 +296,8 @@ __global__ void __launch_bounds__(kThreads) addln_split_kernel(const float *__re
             }
         }
         // slot[par] is written again two rows later: a peer sends for row it+2
-        // only after this CTA sent for row it+1, which its thread 0 does after
-        // the barrier above that every thread passes once done with row it
+        // only after this CTA sent for row it+1, which its warp 0 does after
+        // the barriers above that every thread passes once done with row it
     }
     ptx::griddep_launch_dependents();
     ptx::cluster_arrive_relaxed();
