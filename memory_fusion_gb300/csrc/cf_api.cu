@@ -261,6 +261,16 @@ cf_status cf_plan_gemm_fused(int64_t M, int64_t N, int64_t K, int32_t sm_count,
         int n = max_active_clusters[c];
         if (t.max_clusters > 0) n = std::min(n, int(t.max_clusters));
         if (g > 1 && n < g) return -1.0;
+        // With fewer resident clusters than two row groups, every row group's G
+        // tickets straddle two rounds of the static ticket order (its first
+        // clusters wait at the global barrier for a whole mainloop) and every
+        // cluster's column group changes from ticket to ticket, so each row
+        // block streams all of W again through L2.  Exactly G clusters keep one
+        // column group each: the rounds align with the row groups and each W
+        // column block is read once per launch (wide LN 8192x16384x2048: DRAM
+        // reads 282 -> 110 MB a launch, 413 -> 406 us under the power cap,
+        // 391 -> 398 us in a short burst).
+        if (g > 1 && n < 2 * g) n = g;
         const int64_t T = int64_t((rb + cm - 1) / cm) * g;
         if (T < n) n = int(T);
         const int64_t per = (T + n - 1) / n;

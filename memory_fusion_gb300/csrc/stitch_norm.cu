@@ -43,7 +43,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;          // row slots per thread in flight
-constexpr int kGlobalThreads = 1024;
+constexpr int kGlobalThreads = 512;  // Global BatchNorm: ~100 registers a thread, no spills
+constexpr int kGlobalUnroll = 8;     // its row slots per thread in flight (4 KB per warp)
 
 // float4 group g of a row; zeros past `cols` (scalar path) or past `g1`
 template <bool VEC>
@@ -425,14 +426,14 @@ __global__ void __launch_bounds__(kGlobalThreads, 1) bn_global_kernel(
     const uint64_t keep = ptx::policy_evict_last();
 
     // ---- pass 1: running (n, mean, M2) per column over this CTA's rows, in
-    // chunks of kUnroll rows (two passes over each chunk held in registers)
+    // chunks of kGlobalUnroll rows (two passes over each chunk held in registers)
     float n = 0.f;
     MeanM2 run[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-    for (int64_t base = r0 + slot; base < r1; base += int64_t(S) * kUnroll) {
-        float4 x[kUnroll];
+    for (int64_t base = r0 + slot; base < r1; base += int64_t(S) * kGlobalUnroll) {
+        float4 x[kGlobalUnroll];
         float nc = 0.f;
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kGlobalUnroll; ++u) {
             const int64_t r = base + int64_t(u) * S;
             const bool ok = r < r1;
             x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(kGlobalThreads, 1) bn_global_kernel(
         const float ic = 1.0f / nc;
         float mc[4] = {0.f, 0.f, 0.f, 0.f}, qc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kGlobalUnroll; ++u) {
             mc[0] += x[u].x;
             mc[1] += x[u].y;
             mc[2] += x[u].z;
@@ -463,7 +464,7 @@ __global__ void __launch_bounds__(kGlobalThreads, 1) bn_global_kernel(
 #pragma unroll
         for (int j = 0; j < 4; ++j) mc[j] *= ic;
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kGlobalUnroll; ++u) {
             if (base + int64_t(u) * S < r1) {
                 const float d[4] = {x[u].x - mc[0], x[u].y - mc[1], x[u].z - mc[2], x[u].w - mc[3]};
 #pragma unroll
@@ -570,15 +571,15 @@ __global__ void __launch_bounds__(kGlobalThreads, 1) bn_global_kernel(
     const float4 sc = gv ? stat[sub][1] : make_float4(0.f, 0.f, 0.f, 0.f);
     const float4 be = gv ? stat[sub][2] : make_float4(0.f, 0.f, 0.f, 0.f);
     if (gv) {
-        for (int64_t base = r0 + slot; base < r1; base += int64_t(S) * kUnroll) {
-            float4 x[kUnroll];
+        for (int64_t base = r0 + slot; base < r1; base += int64_t(S) * kGlobalUnroll) {
+            float4 x[kGlobalUnroll];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < kGlobalUnroll; ++u) {
                 const int64_t r = base + int64_t(u) * S;
                 x[u] = load_group<VEC>(A + r * cols, g, cols, r < r1);
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < kGlobalUnroll; ++u) {
                 const int64_t r = base + int64_t(u) * S;
                 if (r < r1) {
                     const float4 y = make_float4(fmaf(x[u].x - mu.x, sc.x, be.x), fmaf(x[u].y - mu.y, sc.y, be.y),
