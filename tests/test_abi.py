@@ -81,7 +81,7 @@ def test_plan_chooses_fastest_predicted():
     cases = {
         (4096, 2048, 128): (4, 1, 1, 32),     # wide tiles: one per CTA, each row in one cluster of 4
         (16384, 4096, 4096): (1, 2, 16, 76),  # CTA pairs (cta_group::2), rows over 16 clusters
-        (8192, 16384, 2048): (2, 2, 32, 36),  # CTA pairs, rows over 32 clusters
+        (8192, 16384, 2048): (2, 2, 32, 32),  # CTA pairs, rows over 32 clusters: 32 of the 36 that fit
         (128, 512, 256): (8, 1, 1, 1),        # one row block: 64-column tiles over a cluster of 8, no pair
     }
     for (M, N, K), (C, CM, G, ncl) in cases.items():
@@ -131,16 +131,30 @@ def test_plan_wide_rows_use_global_path():
     # N = 16384 -> 64 slices; a cluster of 16 needs G = 4 resident clusters per row block
     st, p = cf.cf_plan_gemm_fused(8192, 16384, 2048, 152, GB300, cf.tuning(cluster_size=16))
     assert st == cf.CF_OK
-    assert (p.cluster_size, p.groups, p.clusters) == (16, 4, 7)
-    # cluster 8 forced: G = 8 and all 15 resident clusters are used
+    assert (p.cluster_size, p.groups, p.clusters) == (16, 4, 4)
+    # cluster 8 forced: G = 8 of the 15 resident clusters
     st, p = cf.cf_plan_gemm_fused(8192, 16384, 2048, 152, GB300, cf.tuning(cluster_size=8))
-    assert (p.cluster_size, p.groups, p.clusters) == (8, 8, 15)
+    assert (p.cluster_size, p.groups, p.clusters) == (8, 8, 8)
     # never more clusters than tickets (one row block: 128-column tiles give
     # every SM work, so G = 64 clusters of 2, one ticket each)
     st, p = cf.cf_plan_gemm_fused(128, 16384, 2048, 152, GB300, cf.tuning(cluster_size=2))
     assert (p.n_slice, p.groups, p.clusters) == (128, 64, 64)
     st, p = cf.cf_plan_gemm_fused(128, 16384, 2048, 152, GB300, cf.tuning(cluster_size=2, n_slice=256))
     assert (p.groups, p.clusters) == (32, 32)
+
+
+def test_plan_row_groups_keep_one_column_group():
+    """A row spanning G > 1 clusters: with fewer than 2G resident clusters the
+    grid holds exactly G (each cluster then keeps one column group and the
+    static ticket rounds line up with the row groups); with 2G or more, all
+    that fit (up to the tickets)."""
+    for nres, want in ((32, 32), (36, 32), (63, 32), (64, 64), (76, 76)):
+        st, p = cf.cf_plan_gemm_fused(8192, 16384, 2048, 152, _active({4: nres}),
+                                      cf.tuning(cluster_size=2, cluster_m=2))
+        assert st == cf.CF_OK and p.groups == 32 and p.clusters == want, (nres, p.as_dict())
+    # 16 groups of CTA pairs over 4096 columns: 76 pairs fit, more than 2G, all used
+    st, p = cf.cf_plan_gemm_fused(16384, 4096, 4096, 152, GB300, cf.tuning(cluster_size=1, cluster_m=2))
+    assert (p.groups, p.clusters) == (16, 76)
 
 
 def test_plan_residency_refused():
