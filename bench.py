@@ -161,19 +161,32 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload, kernel):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+def _traffic_entry(workload, kernel):
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         e = d.get(workload, {}).get(kernel)
         if e and e.get("source_hash") == kernel_source_hash(kernel):
-            return float(e["dram_bytes_per_launch"])
+            return e
     except Exception:
         pass
     return None
+
+
+def profiled_traffic(workload, kernel):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    e = _traffic_entry(workload, kernel)
+    return float(e["dram_bytes_per_launch"]) if e else None
+
+
+def profiled_traffic_kind(workload, kernel):
+    """How that figure was taken: one cold launch, or steady state (no cache
+    flush between launches, so a launch also writes back the previous one's
+    output that the L2 still held)."""
+    e = _traffic_entry(workload, kernel)
+    return e.get("kind") if e else None
 
 
 class ClockSampler:
@@ -782,6 +795,7 @@ def run_ours(args):
                 "frac_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
     traffic = profiled_traffic(w.name, kernel)
     roof["traffic"] = traffic
+    roof["traffic_kind"] = profiled_traffic_kind(w.name, kernel)
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
     roof["kernel"] = kernel
     roof["algorithmic_bytes_per_launch"] = w.unavoidable_bytes
@@ -897,7 +911,8 @@ def run_stitch(args):
                                      "l2": f"{nsets} rotating input/output sets (>= 3x L2 of {l2 >> 20} MiB)"},
                           "roofline": {"bound": "hbm", "achieved": round(gbs / ws_, 1), "peak": peaks["hbm_gbs"],
                                        "unit": "GB/s", "frac": round(gbs / ws_ / peaks["hbm_gbs"], 4),
-                                       "traffic": profiled_traffic(w.name, kernel), "kernel": kernel,
+                                       "traffic": profiled_traffic(w.name, kernel),
+                                       "traffic_kind": profiled_traffic_kind(w.name, kernel), "kernel": kernel,
                                        "algorithmic_bytes_per_launch": w.unavoidable_bytes,
                                        "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
                                        else "fallback"},
@@ -944,7 +959,8 @@ def run_b2b(args):
                           "roofline": {"bound": "tensor", "achieved": round(tf / ws_, 1),
                                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                        "frac": round(tf / ws_ / peaks["bf16_tflops"], 4),
-                                       "traffic": profiled_traffic(w.name, kernel), "kernel": kernel,
+                                       "traffic": profiled_traffic(w.name, kernel),
+                                       "traffic_kind": profiled_traffic_kind(w.name, kernel), "kernel": kernel,
                                        "algorithmic_bytes_per_launch": w.unavoidable_bytes,
                                        "flops_per_launch": w.flops,
                                        "launches_per_step": per_step,
