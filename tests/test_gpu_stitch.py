@@ -35,6 +35,8 @@ def test_packed_mapping(rows, cols):
 @pytest.mark.parametrize("rows,cols,C,leader", [
     (3, 130, 1, 0), (4, 1000, 2, 0), (4, 1000, 4, 1), (2, 4097, 8, 0), (5, 30000, 8, 0),
     (5, 30000, 8, 1), (3, 30000, 16, 0), (3, 30000, 16, 1), (2, 65536, 16, 0), (6, 2050, 3, 0),
+    # CTAs whose column slice is empty (their partial is (-inf, 0)), one ragged group
+    (2, 70, 16, 0), (2, 70, 16, 1), (3, 66, 16, 0),
 ])
 def test_split_mapping(rows, cols, C, leader):
     d = inputs.stitch_inputs(rows, cols, 3)
