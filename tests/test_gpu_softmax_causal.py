@@ -66,6 +66,21 @@ def test_causal_schedules(kw):
     _check(y, ref, M, N, 1000, f"causal {kw}")
 
 
+@pytest.mark.parametrize("offset", [-300, -129, 0, 200, 1500])
+def test_causal_row_groups_past_the_mask(offset):
+    """Rows over G = 4 cluster groups (1024 columns each, through the global
+    barrier): groups lying entirely past a row block's last kept column are all
+    zeros, and row blocks whose rows keep nothing are zeros throughout."""
+    M, N, K = 650, 4096, 128
+    d = _inputs(M, N, K, seed=93 + offset % 89)
+    t = cf.tuning(n_slice=256, cluster_size=4)
+    st, plan, _ = cf.cf_query_gemm_fused_plan(M, N, K, 2, t)
+    assert st == cf.CF_OK and plan.groups == 4
+    y = _run(d, K ** -0.5, offset, bias=d["bias"], tuning=t)
+    ref = oracle.gemm_rowsoftmax_causal(d["X"], d["W"], scale=K ** -0.5, offset=offset, bias=d["bias"])
+    _check(y, ref, M, N, offset, f"causal G=4 offset {offset}")
+
+
 def test_causal_keeping_everything_is_the_unmasked_kernel():
     """With every column kept the masked kernel does the unmasked one's arithmetic."""
     d = _inputs(300, 2048, 128, seed=92)
