@@ -182,29 +182,52 @@ __device__ __forceinline__ void softmax_fragment(uint32_t (&v)[32], const float 
 // LayerNorm stage-1 nodes on one fragment: x = alpha*acc + bias (-> GELU);
 // the fragment is replaced by the stage-1 value; returns its (mean, M2).
 // (With a residual: `r` holds the fragment's 32 bf16 residual values of this
-// thread's row, added after the activation.)
+// thread's row, added after the activation.)  Packed fp32 pairs throughout;
+// the sums run in four independent chains.
 template <bool kGelu>
 __device__ __forceinline__ MeanM2 ln_fragment(uint32_t (&v)[32], const float *p, float alpha, const uint4 *r) {
     float x[32];
 #pragma unroll
     for (int j4 = 0; j4 < 8; ++j4) {
         const float4 b = *reinterpret_cast<const float4 *>(p + 4 * j4);
-        x[4 * j4 + 0] = fmaf(alpha, __uint_as_float(v[4 * j4 + 0]), b.x);
-        x[4 * j4 + 1] = fmaf(alpha, __uint_as_float(v[4 * j4 + 1]), b.y);
-        x[4 * j4 + 2] = fmaf(alpha, __uint_as_float(v[4 * j4 + 2]), b.z);
-        x[4 * j4 + 3] = fmaf(alpha, __uint_as_float(v[4 * j4 + 3]), b.w);
+        ptx::fma2(x[4 * j4 + 0], x[4 * j4 + 1], __uint_as_float(v[4 * j4 + 0]), __uint_as_float(v[4 * j4 + 1]), alpha,
+                  alpha, b.x, b.y);
+        ptx::fma2(x[4 * j4 + 2], x[4 * j4 + 3], __uint_as_float(v[4 * j4 + 2]), __uint_as_float(v[4 * j4 + 3]), alpha,
+                  alpha, b.z, b.w);
     }
+    if constexpr (kGelu) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        if constexpr (kGelu) x[j] = gelu_tanh_dev(x[j]);
-        if (r != nullptr) {
+        for (int j = 0; j < 32; j += 2) gelu_tanh_pair(x[j], x[j + 1]);
+    }
+    if (r != nullptr) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
             const uint4 q = r[j >> 3];
             const uint32_t w = ((j >> 1) & 3) == 0 ? q.x : ((j >> 1) & 3) == 1 ? q.y : ((j >> 1) & 3) == 2 ? q.z : q.w;
-            x[j] += __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));  // bf16 -> fp32
+            ptx::add2(x[j], x[j + 1], x[j], x[j + 1], __uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
         }
-        v[j] = __float_as_uint(x[j]);
     }
-    return chunk_mean_m2(x);
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        v[j] = __float_as_uint(x[j]);
+        v[j + 1] = __float_as_uint(x[j + 1]);
+        v[j + 2] = __float_as_uint(x[j + 2]);
+        v[j + 3] = __float_as_uint(x[j + 3]);
+        ptx::add2(s0, s1, s0, s1, x[j], x[j + 1]);
+        ptx::add2(s2, s3, s2, s3, x[j + 2], x[j + 3]);
+    }
+    const float mean = ((s0 + s1) + (s2 + s3)) * (1.0f / 32.0f);
+    float q0 = 0.f, q1 = 0.f, q2 = 0.f, q3 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        float d0, d1, d2, d3;
+        ptx::add2(d0, d1, x[j], x[j + 1], -mean, -mean);
+        ptx::add2(d2, d3, x[j + 2], x[j + 3], -mean, -mean);
+        ptx::fma2(q0, q1, d0, d1, d0, d1, q0, q1);
+        ptx::fma2(q2, q3, d2, d3, d2, d3, q2, q3);
+    }
+    return MeanM2{mean, (q0 + q1) + (q2 + q3)};
 }
 
 // Fold n (<= kN) partials p[0..n) of equal column count `cnt` in a fixed
@@ -839,12 +862,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fused_kernel(const __grid_co
                             for (int j4 = 0; j4 < 8; ++j4) {
                                 const float4 gm = *reinterpret_cast<const float4 *>(gp + 4 * j4);
                                 const float4 bt = *reinterpret_cast<const float4 *>(bp + 4 * j4);
-                                const float y0 = fmaf((__uint_as_float(v[4 * j4 + 0]) - mean) * rstd, gm.x, bt.x);
-                                const float y1 = fmaf((__uint_as_float(v[4 * j4 + 1]) - mean) * rstd, gm.y, bt.y);
-                                const float y2 = fmaf((__uint_as_float(v[4 * j4 + 2]) - mean) * rstd, gm.z, bt.z);
-                                const float y3 = fmaf((__uint_as_float(v[4 * j4 + 3]) - mean) * rstd, gm.w, bt.w);
-                                w[2 * j4] = ptx::pack_bf16x2(y0, y1);
-                                w[2 * j4 + 1] = ptx::pack_bf16x2(y2, y3);
+                                float d0, d1, d2, d3;  // (g - mean) rstd, then * gamma + beta, on pairs
+                                ptx::add2(d0, d1, __uint_as_float(v[4 * j4 + 0]), __uint_as_float(v[4 * j4 + 1]), -mean, -mean);
+                                ptx::add2(d2, d3, __uint_as_float(v[4 * j4 + 2]), __uint_as_float(v[4 * j4 + 3]), -mean, -mean);
+                                ptx::mul2(d0, d1, d0, d1, rstd, rstd);
+                                ptx::mul2(d2, d3, d2, d3, rstd, rstd);
+                                ptx::fma2(d0, d1, d0, d1, gm.x, gm.y, bt.x, bt.y);
+                                ptx::fma2(d2, d3, d2, d3, gm.z, gm.w, bt.z, bt.w);
+                                w[2 * j4] = ptx::pack_bf16x2(d0, d1);
+                                w[2 * j4 + 1] = ptx::pack_bf16x2(d2, d3);
                             }
                         }
                         if (rows_live) {

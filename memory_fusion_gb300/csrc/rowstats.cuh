@@ -35,6 +35,20 @@ __device__ __forceinline__ float gelu_tanh_dev(float x) {
     return 0.5f * x * (1.0f + ptx::tanh_approx(u));
 }
 
+// GELU(tanh) on a packed pair: 0.5 x (1 + tanh(x (c0 + c0 c1 x^2))), the two
+// tanh on the MUFU
+__device__ __forceinline__ void gelu_tanh_pair(float &x0, float &x1) {
+    constexpr float c0 = 0.7978845608028654f;                 // sqrt(2 / pi)
+    constexpr float c01 = 0.7978845608028654f * 0.044715f;    // sqrt(2 / pi) * 0.044715
+    float q0, q1, u0, u1, h0, h1;
+    ptx::mul2(q0, q1, x0, x1, x0, x1);                 // x^2
+    ptx::fma2(q0, q1, q0, q1, c01, c01, c0, c0);       // c0 + c0 c1 x^2
+    ptx::mul2(u0, u1, q0, q1, x0, x1);                 // the tanh argument
+    ptx::mul2(h0, h1, x0, x1, 0.5f, 0.5f);             // x / 2
+    const float t0 = ptx::tanh_approx(u0), t1 = ptx::tanh_approx(u1);
+    ptx::fma2(x0, x1, h0, h1, t0, t1, h0, h1);         // x/2 + x/2 tanh
+}
+
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
 // --------------------------------------------------------------------------
