@@ -562,10 +562,13 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
 #pragma unroll
                     for (int c = 0; c < kFrag; ++c)
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            const float t = fmaf(ascale, __uint_as_float(x[c][k]), bb[c * 32 + k]);
-                            x[c][k] = __float_as_uint(t);
-                            cmv[k & 3] = fmaxf(cmv[k & 3], t);
+                        for (int k = 0; k < 32; k += 2) {  // on packed pairs, three-input max
+                            float t0, t1;
+                            ptx::fma2(t0, t1, __uint_as_float(x[c][k]), __uint_as_float(x[c][k + 1]), ascale, ascale,
+                                      bb[c * 32 + k], bb[c * 32 + k + 1]);
+                            x[c][k] = __float_as_uint(t0);
+                            x[c][k + 1] = __float_as_uint(t1);
+                            cmv[(k >> 1) & 3] = ptx::max3(cmv[(k >> 1) & 3], t0, t1);
                         }
                     // the row's max over the whole chunk: every group's part, through
                     // shared memory
@@ -591,35 +594,42 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
                     for (int c = 0; c < kFrag; ++c)
 #pragma unroll
                         for (int k = 0; k < 16; ++k) {
-                            const float e0 = ptx::ex2_approx(__uint_as_float(x[c][2 * k]) - mn);
-                            const float e1 = ptx::ex2_approx(__uint_as_float(x[c][2 * k + 1]) - mn);
-                            sv[k & 3] += e0 + e1;
+                            float d0, d1;
+                            ptx::add2(d0, d1, __uint_as_float(x[c][2 * k]), __uint_as_float(x[c][2 * k + 1]), -mn, -mn);
+                            const float e0 = ptx::ex2_approx(d0);
+                            const float e1 = ptx::ex2_approx(d1);
+                            ptx::add2(sv[(k & 1) * 2], sv[(k & 1) * 2 + 1], sv[(k & 1) * 2], sv[(k & 1) * 2 + 1], e0, e1);
                             x[c][k] = ptx::pack_bf16x2(e0, e1);
                         }
                     l = fmaf(l, f, (sv[0] + sv[1]) + (sv[2] + sv[3]));
                     m = mn;
                     if (lead && g == 0) trace_tile(tr, J, CF_TRB_EPI1_LOCAL);
                 } else if constexpr (OP == 2) {
-#pragma unroll
-                    for (int c = 0; c < kFrag; ++c)
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            x[c][k] = __float_as_uint(fmaf(ascale, __uint_as_float(x[c][k]), bb[c * 32 + k]));
-                    // (mean, M2) of the chunk's 64 values (two passes over the registers),
-                    // folded into the group's running pair by counts
+                    // z on packed pairs; (mean, M2) of the chunk's 64 values (two passes
+                    // over the registers, four chains), folded into the group's running
+                    // pair by counts
                     float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int c = 0; c < kFrag; ++c)
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) s4[k & 3] += __uint_as_float(x[c][k]);
+                        for (int k = 0; k < 32; k += 2) {
+                            float z0, z1;
+                            ptx::fma2(z0, z1, __uint_as_float(x[c][k]), __uint_as_float(x[c][k + 1]), ascale, ascale,
+                                      bb[c * 32 + k], bb[c * 32 + k + 1]);
+                            x[c][k] = __float_as_uint(z0);
+                            x[c][k + 1] = __float_as_uint(z1);
+                            ptx::add2(s4[(k >> 1) & 2], s4[((k >> 1) & 2) + 1], s4[(k >> 1) & 2], s4[((k >> 1) & 2) + 1], z0, z1);
+                        }
                     const float cmean = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * (1.f / float(kCols));
                     float q4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int c = 0; c < kFrag; ++c)
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            const float d = __uint_as_float(x[c][k]) - cmean;
-                            q4[k & 3] = fmaf(d, d, q4[k & 3]);
+                        for (int k = 0; k < 32; k += 2) {
+                            float d0, d1;
+                            ptx::add2(d0, d1, __uint_as_float(x[c][k]), __uint_as_float(x[c][k + 1]), -cmean, -cmean);
+                            ptx::fma2(q4[(k >> 1) & 2], q4[((k >> 1) & 2) + 1], d0, d1, d0, d1, q4[(k >> 1) & 2],
+                                      q4[((k >> 1) & 2) + 1]);
                         }
                     const MeanM2 cs{cmean, (q4[0] + q4[1]) + (q4[2] + q4[3])};
                     if (j == 0) {
@@ -641,19 +651,22 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_stream_kernel(const __grid_co
 #pragma unroll
                     for (int c = 0; c < kFrag; ++c)
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
+                        for (int k = 0; k < 16; ++k) {  // on packed pairs
                             const int n0 = c * 32 + 2 * k;
-                            x[c][k] = ptx::pack_bf16x2((__uint_as_float(x[c][2 * k]) - mu0) * bb[kCols + n0],
-                                                       (__uint_as_float(x[c][2 * k + 1]) - mu0) * bb[kCols + n0 + 1]);
+                            float d0, d1;
+                            ptx::add2(d0, d1, __uint_as_float(x[c][2 * k]), __uint_as_float(x[c][2 * k + 1]), -mu0, -mu0);
+                            ptx::mul2(d0, d1, d0, d1, bb[kCols + n0], bb[kCols + n0 + 1]);
+                            x[c][k] = ptx::pack_bf16x2(d0, d1);
                         }
                 } else {
 #pragma unroll
                     for (int c = 0; c < kFrag; ++c)
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const float x0 = gelu_tanh_dev(fmaf(ascale, __uint_as_float(x[c][2 * k]), bb[c * 32 + 2 * k]));
-                            const float x1 =
-                                gelu_tanh_dev(fmaf(ascale, __uint_as_float(x[c][2 * k + 1]), bb[c * 32 + 2 * k + 1]));
+                        for (int k = 0; k < 16; ++k) {  // on packed pairs
+                            float x0, x1;
+                            ptx::fma2(x0, x1, __uint_as_float(x[c][2 * k]), __uint_as_float(x[c][2 * k + 1]), ascale,
+                                      ascale, bb[c * 32 + 2 * k], bb[c * 32 + 2 * k + 1]);
+                            gelu_tanh_pair(x0, x1);
                             x[c][k] = ptx::pack_bf16x2(x0, x1);
                         }
                 }
