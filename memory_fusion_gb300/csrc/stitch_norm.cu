@@ -323,6 +323,12 @@ __global__ void __launch_bounds__(kThreads) bn_regional_kernel(const float *__re
     const int g = blockIdx.x * 32 + lane;
     const bool gv = g < ng;
     ptx::griddep_wait();
+    // gamma and beta of the column this thread folds below, loaded with the rows
+    // (an L2 round trip after the fold otherwise)
+    const int tcol = blockIdx.x * 128 + int(threadIdx.x);
+    const bool tc = threadIdx.x < 128 && tcol < cols;
+    const float gcol = tc ? __ldg(gamma + tcol) : 0.f;
+    const float bcol = tc ? __ldg(beta + tcol) : 0.f;
     float4 x[RPT];
     float n = 0.f;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -353,23 +359,29 @@ __global__ void __launch_bounds__(kThreads) bn_regional_kernel(const float *__re
     red[warp][4 * lane + 3] = make_float2(m.w, q.w);
     __syncthreads();
     if (threadIdx.x < 128) {
-        // fold the 8 warps' partials of column t in warp order
+        // fold the 8 warps' partials of column t in warp order (warp w holds rows
+        // w, w + 8, ...): mean = sum(n_w mean_w) / rows, then
+        // M2 = sum(M2_w + n_w (mean_w - mean)^2)
         const int t = threadIdx.x;
-        const int col = blockIdx.x * 128 + t;
-        MeanM2 acc{red[0][t].x, red[0][t].y};
-        float na = float((rows + 7) / 8);  // warp w holds rows w, w + 8, ...
-        for (int w = 1; w < kThreads / 32; ++w) {
-            const float nw = float(rows > w ? (rows - w + 7) / 8 : 0);
-            acc = combine_counts_safe(acc, na, MeanM2{red[w][t].x, red[w][t].y}, nw);
-            na += nw;
+        const int col = tcol;
+        float sm = 0.f;
+#pragma unroll 1
+        for (int w = 0; w < kThreads / 32; ++w) sm = fmaf(float(rows > w ? (rows - w + 7) / 8 : 0), red[w][t].x, sm);
+        const float mean = sm / float(rows);
+        float m2 = 0.f;
+#pragma unroll 1
+        for (int w = 0; w < kThreads / 32; ++w) {
+            const float d = red[w][t].x - mean;
+            m2 += fmaf(float(rows > w ? (rows - w + 7) / 8 : 0) * d, d, red[w][t].y);
         }
+        const MeanM2 acc{mean, m2};
         const float var = acc.m2 / float(rows);
         const float sc = rsqrtf(var + eps);
         float *st = reinterpret_cast<float *>(&stat[0][0]);
         if (col < cols) {
             st[(t >> 2) * 12 + 0 + (t & 3)] = acc.mean;
-            st[(t >> 2) * 12 + 4 + (t & 3)] = __ldg(gamma + col) * sc;
-            st[(t >> 2) * 12 + 8 + (t & 3)] = __ldg(beta + col);
+            st[(t >> 2) * 12 + 4 + (t & 3)] = gcol * sc;
+            st[(t >> 2) * 12 + 8 + (t & 3)] = bcol;
             if (mean_out != nullptr) mean_out[col] = acc.mean;
             if (var_out != nullptr) var_out[col] = var;
         }
