@@ -99,7 +99,10 @@ typedef struct cf_tuning {
                                leader-follower ([ComFuse] dual-mode strategy).
                                0 = 8; negative = always leader-follower          */
     int32_t max_clusters;   /* cap on resident clusters of the persistent grid     */
-    int32_t stages;         /* GEMM: depth of the shared-memory operand ring       */
+    int32_t stages;         /* GEMM: depth of the shared-memory operand ring;
+                               Global BatchNorm: stage buffers of the streaming
+                               ring (the CTA's other buffers hold its first
+                               stages from the first pass to the second)        */
     int32_t stitch_mapping; /* 0 auto, 1 packed rows, 2 split rows over a cluster  */
     uint32_t timeout_us;    /* bound of every device spin (0 = 200000 us)          */
     int32_t extra_arrivals; /* TEST HOOK: added to the arrival count the global

@@ -530,7 +530,8 @@ cf_status cf_stitch_add_layernorm_ex(const float *A, const float *R, const float
     if (!cf::current_device_info(&dev)) return CF_ERR_NO_DEVICE;
     if (dev.cc_major != 10 || dev.cc_minor != 3) return CF_ERR_NO_DEVICE;
     cf::StitchPlan p;
-    p.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out) && (R == nullptr || aligned16(R));
+    p.vec = (cols % 4 == 0) && aligned16(A) && aligned16(out) && (R == nullptr || aligned16(R)) &&
+            aligned16(gamma) && aligned16(beta);
     cf_status st = plan_row_mapping(rows, cols, t, dev, &p, cf::addln_packed_blocks_per_sm, 2);
     if (st != CF_OK) return st;
     cudaError_t e = cf::launch_add_layernorm(p, A, R, gamma, beta, out, rows, cols, eps,
@@ -628,7 +629,6 @@ cf_status cf_stitch_batchnorm_ex(const float *A, const float *gamma, const float
         std::memset(&a, 0, sizeof(a));
         const uint32_t W = uint32_t(4 * p.lpr), br = uint32_t(cf::bn_tma_box_rows(p.lpr));
         if (!make_tmap_f32(&a.tmap_a, A, uint64_t(rows), uint64_t(cols), W, br)) return CF_ERR_CUDA;
-        if (!make_tmap_f32(&a.tmap_out, out, uint64_t(rows), uint64_t(cols), W, br)) return CF_ERR_CUDA;
         a.gamma = gamma;
         a.beta = beta;
         a.mean_out = mean_out;
@@ -647,6 +647,7 @@ cf_status cf_stitch_batchnorm_ex(const float *A, const float *gamma, const float
         a.A = A;
         a.out = out;
         a.flat = (cols == int64_t(W) && t.stitch_mapping != 6) ? 1 : 0;  // 6: tiled copies forced (comparison)
+        cf::bn_tma_buffers(p.lpr, t.stages, &a.ring, &a.res);
         cudaError_t e = cf::launch_batchnorm_tma(p.lpr, a, p.grid, p.pdl, reinterpret_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e);
         return CF_OK;

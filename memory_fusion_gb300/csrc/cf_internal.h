@@ -85,7 +85,6 @@ int bn_global_blocks_per_sm(int lpr, bool vec);
 // 16-byte aligned A and out): one producer warp, eight compute warps
 struct BnTmaArgs {
     CUtensorMap tmap_a;    // A [rows, cols] fp32, box (4*lpr) x br, no swizzle
-    CUtensorMap tmap_out;  // out, same box
     const float *gamma, *beta;
     float *mean_out, *var_out;
     uint32_t *err, *counters;
@@ -95,13 +94,17 @@ struct BnTmaArgs {
     float eps;
     unsigned long long timeout_ns;
     unsigned long long *trace;  // optional: per CTA slots 0..3 = start, pass 1 done, barrier passed, pass 2 done
-    const float *A;        // flat (cols == 4*lpr): stages move as untiled bulk copies
-    float *out;
+    const float *A;        // flat (cols == 4*lpr): stages load as untiled bulk copies
+    float *out;            // [rows, cols], written from registers
     int flat;
+    int ring, res;  // stage buffers streaming, and holding the first stages resident
 };
 cudaError_t launch_batchnorm_tma(int lpr, const BnTmaArgs &a, int grid, bool pdl, cudaStream_t stream);
 int bn_tma_blocks_per_sm(int lpr);
 int bn_tma_box_rows(int lpr);   // rows of one stage for a strip of 4*lpr columns
+// split the CTA's stage buffers into a streaming ring (`stages` of them, 0 =
+// default) and resident stages
+void bn_tma_buffers(int lpr, int stages, int *ring, int *res);
 constexpr int kBnRegionalMaxRows = 256;   // 8 warps x 32 rows in registers
 constexpr int kBnMaxGlobalCtas = 1024;    // bound of the partial buffer
 

@@ -154,6 +154,20 @@ def test_batchnorm_schemes_agree_and_repeat():
     _check_bn(d2, _bn(d2, tuning=cf.tuning(max_clusters=3)), "BN Global 3 CTAs")
 
 
+@pytest.mark.parametrize("rows,cols", [(200000, 32), (60000, 4), (40000, 520)])
+def test_batchnorm_global_ring_and_resident_split(rows, cols):
+    """The TMA-streamed Global kernel splits its stage buffers into a
+    streaming ring (tuning `stages`) and stages held resident from the first
+    pass to the second: every split, from a 2-stage ring with the most
+    resident to no resident stage at all, gives the same bits."""
+    d = inputs.stitch_norm_inputs(rows, cols, seed=rows + 11 * cols, with_R=False)
+    ref = _bn(d)
+    _check_bn(d, ref, f"BN Global {rows}x{cols} default split")
+    for stages in (2, 3, 13, 26, 100):
+        got = _bn(d, tuning=cf.tuning(stages=stages))
+        assert all(np.array_equal(x, y) for x, y in zip(ref, got)), f"{rows}x{cols}: stages={stages} differs"
+
+
 def test_batchnorm_grid_barrier_timeout_is_reported():
     """One arrival more than can happen: every CTA's bounded wait runs out,
     the error word says so, and the context stays usable."""
