@@ -88,6 +88,15 @@ __device__ __forceinline__ float4 ldg_group(const float *p, int g, int cols) {
     return t;
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only, no L1 allocation);
+// complete for this thread after cp_async_wait_all
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 
 // valid lanes of a 4-group starting at column c
@@ -229,15 +238,15 @@ __global__ void __launch_bounds__(kThreads) addln_split_kernel(const float *__re
                 const int g = g0 + threadIdx.x + v * kThreads;
                 if (g < g1) {
                     if constexpr (kGB) {
-                        ptx::cp_async_16(ptx::smem_u32(&gbs[v * kThreads + threadIdx.x]), gamma + 4 * g);
-                        ptx::cp_async_16(ptx::smem_u32(&gbs[(V + v) * kThreads + threadIdx.x]), beta + 4 * g);
+                        cp_async_16(ptx::smem_u32(&gbs[v * kThreads + threadIdx.x]), gamma + 4 * g);
+                        cp_async_16(ptx::smem_u32(&gbs[(V + v) * kThreads + threadIdx.x]), beta + 4 * g);
                     } else {
                         ptx::prefetch_l1(gamma + 4 * g);
                         ptx::prefetch_l1(beta + 4 * g);
                     }
                 }
             }
-            if constexpr (kGB) ptx::cp_async_commit();
+            if constexpr (kGB) cp_async_commit();
             ptx::cluster_wait_acquire();
         }
         // the CTA's mean (levels 1 and 2 on plain sums: missing columns hold 0)
@@ -298,7 +307,7 @@ __global__ void __launch_bounds__(kThreads) addln_split_kernel(const float *__re
         const float rstd = rsqrtf(fmaf(m2, 1.0f / float(cols), eps));
         float *o = out + row * cols;
         if constexpr (kGB) {
-            if (it == 0) ptx::cp_async_wait_all();  // this thread's own copies
+            if (it == 0) cp_async_wait_all();  // this thread's own copies
         }
 #pragma unroll
         for (int v = 0; v < V; ++v) {
