@@ -148,12 +148,12 @@ def _code_only(text):
 
 def kernel_source_hash(kernel):
     """Hash of the device code behind `kernel`: the translation unit that holds
-    it and every shared device header (.cuh), comments and layout ignored.  A
-    kernel's DRAM traffic can only change when one of them does (cf_internal.h,
-    host-side declarations and the launch-argument structs, is not part of it)."""
+    it, every shared device header (.cuh) and the internal header of shared
+    constants and launch-argument structs (cf_internal.h), comments and layout
+    ignored.  A kernel's DRAM traffic can only change when one of them does."""
     csrc = os.path.join(ROOT, "memory_fusion_gb300", "csrc")
     tu = next((f for k, f in KERNEL_TU.items() if kernel.startswith(k)), None)
-    files = sorted(f for f in os.listdir(csrc) if f.endswith(".cuh") or f == tu)
+    files = sorted(f for f in os.listdir(csrc) if f.endswith(".cuh") or f == tu or f == "cf_internal.h")
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:

@@ -410,7 +410,7 @@ static cf_status plan_row_mapping(int64_t rows, int64_t cols, const cf_tuning &t
     p.mapping = mapping;
     if (mapping == 1) {
         p.lpr = next_pow2(ng);
-        const int rows_per_cta_iter = 8 * (32 / p.lpr) * 4;
+        const int rows_per_cta_iter = 8 * (32 / p.lpr) * cf::kPackedUnroll;
         const int64_t want = (rows + rows_per_cta_iter - 1) / rows_per_cta_iter;
         int bps = packed_bps(p.lpr, p.vec);
         if (bps <= 0) bps = 1;

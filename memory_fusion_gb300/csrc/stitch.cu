@@ -36,7 +36,7 @@ namespace cf {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;  // row slots per thread in flight (memory-level parallelism)
+constexpr int kUnroll = kPackedUnroll;  // row slots per thread per iteration
 
 __device__ __forceinline__ float cube_plus(float a, float b) { return a * a * a + b; }
 

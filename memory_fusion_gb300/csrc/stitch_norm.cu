@@ -42,7 +42,7 @@ namespace cf {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;          // row slots per thread in flight
+constexpr int kUnroll = kPackedUnroll;  // row slots per thread per iteration (packed rows)
 constexpr int kGlobalThreads = 512;  // Global BatchNorm: ~100 registers a thread, no spills
 constexpr int kGlobalUnroll = 8;     // its row slots per thread in flight (4 KB per warp)
 
