@@ -31,15 +31,23 @@ def check_close(y, ref, what):
     assert err.mean() <= 1e-5, f"{what}: mean-abs {err.mean():.3e}"
 
 
-def _addln(d, eps=1e-5, tuning=None, in_place=False, use_R=True):
+def _shifted(x):
+    """x on the device at an address 4 bytes past a 16-byte boundary."""
+    torch = torch_cuda()
+    buf = torch.empty(x.size + 1, dtype=torch.float32, device="cuda")
+    buf[1:].copy_(torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)))
+    return buf[1:]
+
+
+def _addln(d, eps=1e-5, tuning=None, in_place=False, use_R=True, params_16b=True):
     torch = torch_cuda()
     rows, cols = d["A"].shape
     A = dev_f32(d["A"])
     R = dev_f32(d["R"]) if use_R else None
     out = A if in_place else torch.full_like(A, float("nan"))
     ws = cf.new_workspace(cf.cf_stitch_workspace_size(rows, cols))
-    st = cf.cf_stitch_add_layernorm(A, R, dev_f32(d["gamma"]), dev_f32(d["beta"]), out, rows, cols, eps, ws,
-                                    ws.numel(), None, tuning)
+    g, b = (dev_f32(d["gamma"]), dev_f32(d["beta"])) if params_16b else (_shifted(d["gamma"]), _shifted(d["beta"]))
+    st = cf.cf_stitch_add_layernorm(A, R, g, b, out, rows, cols, eps, ws, ws.numel(), None, tuning)
     assert st == cf.CF_OK, cf.status_string(st)
     torch.cuda.synchronize()
     dst, info = cf.cf_get_device_status(ws)
@@ -54,6 +62,16 @@ def test_add_layernorm_shapes(rows, cols):
     y = _addln(d)
     ref = oracle.stitch_add_layernorm(d["A"], d["R"], d["gamma"], d["beta"], 1e-5)
     check_close(y, ref, f"add+LN {rows}x{cols}")
+
+
+@pytest.mark.parametrize("rows,cols", [(1000, 32), (64, 30000), (40, 8192)])
+def test_add_layernorm_params_not_16_byte_aligned(rows, cols):
+    """gamma and beta 4 bytes past a 16-byte boundary: the kernels read them
+    with scalar loads (the 128-bit path, and the split kernel's shared-memory
+    staging of gamma and beta, need 16-byte aligned vectors)."""
+    d = inputs.stitch_norm_inputs(rows, cols, seed=rows + 3 * cols)
+    ref = oracle.stitch_add_layernorm(d["A"], d["R"], d["gamma"], d["beta"], 1e-5)
+    check_close(_addln(d, params_16b=False), ref, f"add+LN {rows}x{cols}, shifted gamma/beta")
 
 
 @pytest.mark.parametrize("kw", [dict(stitch_mapping=2, cluster_size=2), dict(stitch_mapping=2, cluster_size=8),
