@@ -616,8 +616,10 @@ CF_API cf_status cf_stitch_add_layernorm_ex(const float *A, const float *R, cons
  *         a device-side error, zero the workspace again)
  * Supported: rows, cols >= 0 (0 is a no-op); 4-byte aligned pointers.
  * Tuning fields used: stitch_mapping (3 Regional, 4 Global), max_clusters
- * (cap on the Global grid), timeout_us, disable_pdl, extra_arrivals (TEST
- * HOOK: > 0 makes the grid barrier wait run out). */
+ * (cap on the Global grid), stages (Global with 16-byte aligned rows: the
+ * stage buffers of each CTA's streaming ring, the others holding its first
+ * stages between the passes; 0 = 128 KB of ring), timeout_us, disable_pdl,
+ * extra_arrivals (TEST HOOK: > 0 makes the grid barrier wait run out). */
 CF_API size_t cf_stitch_batchnorm_workspace_size(int64_t rows, int64_t cols);
 
 CF_API cf_status cf_stitch_batchnorm(const float *A, const float *gamma, const float *beta,
