@@ -973,36 +973,62 @@ def run_b2b(args):
 # ---------------------------------------------------------------------------
 # reference arm: the fp64 CPU oracle
 # ---------------------------------------------------------------------------
+def _ref_sample_size(step_of, n_max, calls, budget_s):
+    """Rows per step for the reference arm: the largest sample (at most n_max
+    rows, at least one) whose `calls` oracle calls fit in budget_s, found by
+    timing the oracle on this host at growing sample sizes."""
+    target = budget_s / max(1, calls)
+    step_of(1)  # first touch of the inputs and the BLAS threads
+    n, best = 1, 1
+    while True:
+        t0 = time.perf_counter()
+        step_of(n)
+        t = time.perf_counter() - t0
+        if t > target:
+            return best
+        best = n
+        if n >= n_max:
+            return n
+        # grow at least twofold, faster while far below the target
+        n = min(n_max, max(2 * n, int(n * 0.5 * target / max(t, 1e-6))))
+
+
 def run_reference_stitched(args, w):
     """The oracle on a stitched workload: GB/s over the bytes of the rows it
-    processed (a row sample per step; BatchNorm's column statistics need every
-    row, so a step there is the whole matrix)."""
+    processed.  Each step is a random sample of whole rows, sized so that the
+    warm-up and the K timed steps take about --ref-budget seconds (BatchNorm:
+    the column statistics of the sampled rows, i.e. BatchNorm of a smaller
+    batch drawn from the matrix)."""
     import oracle
     d = inputs.workload_inputs(w.name)
     rng = np.random.Generator(np.random.PCG64(1))
     per_row = w.unavoidable_bytes / w.rows
-    n_rows = min(w.rows, max(1, int(2e6 // w.cols)))
-    if isinstance(w, inputs.StitchNormWorkload) and w.kind == "batchnorm":
-        n_rows = w.rows
+    bn = isinstance(w, inputs.StitchNormWorkload) and w.kind == "batchnorm"
 
-        def step():
-            oracle.stitch_batchnorm(d["A"], d["gamma"], d["beta"], w.eps)
-        sample = f"the whole {w.rows}x{w.cols} matrix per step (fp64 numpy oracle)"
-    else:
-        def step():
-            rows = np.sort(rng.choice(w.rows, size=n_rows, replace=False))
-            if isinstance(w, inputs.StitchNormWorkload):
-                oracle.stitch_add_layernorm(d["A"], d["R"], d["gamma"], d["beta"], w.eps, rows=rows)
-            elif isinstance(w, inputs.StitchPowWorkload):
-                oracle.stitch_powadd_softmax(d["A"], d["w"], w.p, rows=rows)
-            else:
-                oracle.stitch_rowreduce_broadcast(d["A"], d["row_bias"], rows=rows)
-        sample = f"{n_rows} random whole rows of {w.name} per step (fp64 numpy oracle)"
+    def step_of(n):
+        # a contiguous block of rows at a random offset (drawing n distinct row
+        # indices out of 750000 would cost more than the oracle's own step)
+        r0 = int(rng.integers(0, w.rows - n + 1))
+        rows = np.arange(r0, r0 + n)
+        if bn:
+            oracle.stitch_batchnorm(d["A"][r0:r0 + n], d["gamma"], d["beta"], w.eps)
+        elif isinstance(w, inputs.StitchNormWorkload):
+            oracle.stitch_add_layernorm(d["A"], d["R"], d["gamma"], d["beta"], w.eps, rows=rows)
+        elif isinstance(w, inputs.StitchPowWorkload):
+            oracle.stitch_powadd_softmax(d["A"], d["w"], w.p, rows=rows)
+        else:
+            oracle.stitch_rowreduce_broadcast(d["A"], d["row_bias"], rows=rows)
+
+    n_max = w.rows if bn else min(w.rows, max(1, int(2e6 // w.cols)))
+    n_rows = _ref_sample_size(step_of, n_max, args.steps + args.warmup, args.ref_budget)
+    sample = (f"{n_rows} whole rows of {w.name} per step, a block at a random offset "
+              f"({'BatchNorm over the sampled rows; ' if bn else ''}"
+              f"fp64 numpy oracle; sized for about {args.ref_budget:.0f} s over warm-up and timed steps)")
     for _ in range(args.warmup):
-        step()
+        step_of(n_rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        step_of(n_rows)
     t = time.perf_counter() - t0
     v = per_row * n_rows * args.steps / t / 1e9
     metric = (f"stitched {w.kind} HBM GB/s" if isinstance(w, inputs.StitchNormWorkload)
@@ -1028,23 +1054,26 @@ def run_reference(args):
         run_reference_stitched(args, w)
         return
     import oracle
-    d = inputs.workload_inputs(w.name)
-    rows_per_step = 128
+    # bf16 / fp32 inputs widened to float64 once, before any timing: the same
+    # values the oracle would widen them to on every call
+    d = {k: (v.astype(np.float64) if isinstance(v, np.ndarray) else v)
+         for k, v in inputs.workload_inputs(w.name).items()}
     rng = np.random.Generator(np.random.PCG64(1))
 
-    def step():
-        rows = np.sort(rng.choice(w.M, size=rows_per_step, replace=False))
-        oracle_rows(oracle, w, d, rows)
+    def step_of(n):
+        oracle_rows(oracle, w, d, np.sort(rng.choice(w.M, size=n, replace=False)))
 
+    rows_per_step = _ref_sample_size(step_of, 128, args.steps + args.warmup, args.ref_budget)
     for _ in range(args.warmup):
-        step()
+        step_of(rows_per_step)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        step_of(rows_per_step)
     t = time.perf_counter() - t0
     flops = flops_per_row(w) * rows_per_step * args.steps
     v = flops / t / 1e12
-    sample = f"{rows_per_step} random whole rows of {w.name} per step (fp64 numpy oracle)"
+    sample = (f"{rows_per_step} random whole rows of {w.name} per step (fp64 numpy oracle; sized for about "
+              f"{args.ref_budget:.0f} s over warm-up and timed steps)")
     metric = "back-to-back GEMM TFLOP/s" if isinstance(w, inputs.B2bWorkload) else METRIC
     print(json.dumps({
         "impl": "reference", "metric": metric, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": ws_,
@@ -1060,14 +1089,22 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100000)
-    ap.add_argument("--warmup", type=int, default=200)
+    # defaults: ours, 100000 launches (about half a minute on the headline
+    # workload); the reference arm (the fp64 CPU oracle), 20 steps
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip the per-workload table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=90.0,
+                    help="reference arm: seconds of oracle time over warm-up and timed steps")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 20 if args.impl == "reference" else 100000
+    if args.warmup is None:
+        args.warmup = 5 if args.impl == "reference" else 200
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     stitched = isinstance(inputs.WORKLOADS[args.workload],

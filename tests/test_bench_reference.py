@@ -1,0 +1,41 @@
+"""The benchmark's reference arm (the fp64 CPU oracle, `bench.py --impl
+reference`) on the CPU: it prints the contract's JSON line, and its per-step
+sample is sized from a time budget, so that a large step count still ends in
+bounded time."""
+import json
+import os
+import subprocess
+import sys
+import time
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args, timeout=240):
+    t0 = time.time()
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", *args],
+                       capture_output=True, text=True, timeout=timeout, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    return line, time.time() - t0
+
+
+@pytest.mark.parametrize("workload", ["stitch_64x30000", "bn_750000x32"])
+def test_reference_line_and_bounded_time(workload):
+    line, secs = _run("--workload", workload, "--steps", "400", "--warmup", "3", "--ref-budget", "3")
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["steps"] == 400 and line["warmup"] == 3
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    # 3 s of oracle time plus input generation and sizing; far below what
+    # 403 whole-matrix steps would take
+    assert secs < 120, secs
+
+
+def test_reference_gemm_headline_defaults():
+    line, secs = _run("--ref-budget", "4")
+    assert line["unit"] == "TFLOP/s" and line["steps"] == 20 and line["warmup"] == 5
+    assert line["config"]["M"] == 16384 and line["value"] > 0
