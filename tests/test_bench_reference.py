@@ -39,3 +39,17 @@ def test_reference_gemm_headline_defaults():
     line, secs = _run("--ref-budget", "4")
     assert line["unit"] == "TFLOP/s" and line["steps"] == 20 and line["warmup"] == 5
     assert line["config"]["M"] == 16384 and line["value"] > 0
+
+
+def test_reference_under_two_ranks_prints_once():
+    """Launched as two ranks (torchrun, CPU only): rank 0 alone runs the
+    oracle and prints the line; the other rank exits 0 without work."""
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", "29531",
+                        os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--workload", "stitch_64x30000", "--steps", "3", "--warmup", "3", "--ref-budget", "1"],
+                       capture_output=True, text=True, timeout=240, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    assert json.loads(lines[0])["impl"] == "reference"
