@@ -64,6 +64,18 @@ def test_add_layernorm_shapes(rows, cols):
     check_close(y, ref, f"add+LN {rows}x{cols}")
 
 
+@pytest.mark.parametrize("rows,cols,C,clusters,aligned", [(21, 8192, 4, 3, True), (21, 8192, 4, 3, False),
+                                                        (10, 30000, 8, 2, True), (7, 4097, 2, 1, True)])
+def test_add_layernorm_split_rows_per_cluster(rows, cols, C, clusters, aligned):
+    """Fewer clusters than rows: each cluster walks several rows, reusing its
+    exchange slots by row parity and (16-byte aligned rows) the gamma/beta it
+    staged in shared memory for the first row."""
+    d = inputs.stitch_norm_inputs(rows, cols, seed=rows * 7 + cols + C)
+    ref = oracle.stitch_add_layernorm(d["A"], d["R"], d["gamma"], d["beta"], 1e-5)
+    t = cf.tuning(stitch_mapping=2, cluster_size=C, max_clusters=clusters)
+    check_close(_addln(d, tuning=t, params_16b=aligned), ref, f"add+LN split {rows}x{cols} C={C} x{clusters}")
+
+
 @pytest.mark.parametrize("rows,cols", [(1000, 32), (64, 30000), (40, 8192)])
 def test_add_layernorm_params_not_16_byte_aligned(rows, cols):
     """gamma and beta 4 bytes past a 16-byte boundary: the kernels read them
