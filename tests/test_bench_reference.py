@@ -53,3 +53,21 @@ def test_reference_under_two_ranks_prints_once():
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1, r.stdout[-2000:]
     assert json.loads(lines[0])["impl"] == "reference"
+
+
+def test_ref_sample_size_fits_the_budget():
+    """The sample-size search against a step whose cost is a + b n seconds
+    (simulated by sleeping): the chosen n keeps calls x cost(n) within the
+    budget, grows to n_max when the budget allows, and stays >= 1."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    def make(a, b):
+        def step_of(n):
+            time.sleep(a + b * n)
+        return step_of
+
+    n = bench._ref_sample_size(make(0.0005, 0.0001), 10000, 40, 0.4)  # 10 ms a call: n <= 95
+    assert 1 <= n <= 95 and 40 * (0.0005 + 0.0001 * n) <= 0.4 * 1.05
+    assert bench._ref_sample_size(make(0.0, 1e-7), 64, 5, 10.0) == 64        # budget allows all
+    assert bench._ref_sample_size(make(0.05, 0.0), 1000, 100, 0.1) == 1      # even one row is over
